@@ -1,0 +1,235 @@
+/*
+ * pkv.h -- C ABI of the paged KV cache hot path (GB300 / sm_103a).
+ *
+ * A pool of fixed-size KV blocks, per-sequence block tables with fork and
+ * copy-on-write, and four device operations on the block pool: writing new
+ * tokens' keys/values at their slots, ragged-batch GQA decode attention read
+ * through the block tables, whole-block copies for copy-on-write, and swapping
+ * blocks between the HBM pool and a page-locked host tier.
+ *
+ * Sources (page title, section):
+ *   [KVM] "KV Cache Management" (cs249r book, vol. 3 ch. 5):
+ *         "The PagedAttention virtual memory model" (Definition 0.1, Table 3,
+ *         M_block), "Zero-copy deliberation via copy-on-write branching",
+ *         "Chunked prefill mechanics" (online-softmax merge),
+ *         "Asynchronous paged swapping".
+ *   [PA]  "PagedAttention" (programmer.ie Inference book, ch. 14): "Paging",
+ *         "The real cache", "Sharing and copy-on-write", "Inference Lab increment".
+ *
+ * Conventions
+ *   - Every call returns an int status (enum pkv_status).  On failure the call
+ *     changes no host state (all or nothing, [PA] "Inference Lab increment") and
+ *     pkv_last_error_message() gives a thread-local description.
+ *   - No C++ exception crosses the ABI.
+ *   - Device operations are asynchronous on the given stream (a cudaStream_t;
+ *     NULL = the legacy default stream).  They never allocate device memory.
+ *   - Ownership: the caller owns every device buffer (pools, q, out, workspace,
+ *     slot mappings, tables) and the page-locked host tier.  The library owns
+ *     only the host control-plane state behind the opaque pkv_pool handle.
+ *   - Device-side argument checks (block ids, slots, lengths) never trap: a
+ *     kernel that meets a bad value records it in a per-device error word, skips
+ *     or clamps the access, and finishes; pkv_check_device_error() reports it.
+ *
+ * Data layouts (row-major, element type = geometry.dtype)
+ *   k_pool, v_pool : [num_blocks][L][H_kv][block_size][d_head]
+ *                    A (block, layer, head) slab is block_size*d_head contiguous
+ *                    elements; a block over all layers is contiguous, so one
+ *                    physical block of K plus V is M_block = 2*L*H_kv*B*d*b bytes
+ *                    ([KVM] M_block).  Slot s = block * block_size + offset.
+ *   host tier      : frames of M_block bytes: [frame][2 (K, V)][L][H_kv][B][d].
+ *   q, out         : [n_seq][H_q][d_head]
+ *   block_tables   : int32 [n_seq][W]; entry l is the physical block of logical
+ *                    block l = floor(t / block_size) ([KVM] Definition 0.1).
+ *   Query head h reads KV head floor(h / G), G = H_q / H_kv.
+ */
+#ifndef PKV_H
+#define PKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define PKV_VERSION 1
+
+typedef struct CUstream_st* pkv_stream_t; /* identical to cudaStream_t */
+typedef struct pkv_pool pkv_pool;         /* opaque host control-plane state */
+
+enum pkv_status {
+  PKV_OK = 0,
+  PKV_ERR_INVALID_ARG = 1,   /* bad argument, unknown or swapped-out sequence */
+  PKV_ERR_OUT_OF_BLOCKS = 2, /* the free list cannot satisfy the request */
+  PKV_ERR_DOUBLE_FREE = 3,   /* a sequence (or block) released twice */
+  PKV_ERR_BAD_BLOCK_ID = 4,  /* a block id, slot or host frame out of range */
+  PKV_ERR_CUDA = 5,          /* a CUDA runtime call failed (message has the name) */
+  PKV_ERR_DEVICE_CHECK = 6,  /* a kernel recorded a bad index (pkv_check_device_error) */
+  PKV_ERR_TIMEOUT = 7,       /* a bounded device wait gave up */
+  PKV_ERR_UNSUPPORTED = 8    /* geometry or dtype this build does not handle */
+};
+
+enum pkv_dtype { PKV_F32 = 0, PKV_F16 = 1, PKV_BF16 = 2 };
+
+/* Pool geometry ([KVM] Eq. 1: m_token = 2 * L * H_kv * d_head * b). */
+typedef struct pkv_geometry {
+  int32_t L;          /* layers held per block */
+  int32_t H_q;        /* query heads (multiple of H_kv) */
+  int32_t H_kv;       /* key/value heads */
+  int32_t d_head;     /* head dimension (even, <= 256) */
+  int32_t block_size; /* B, tokens per block */
+  int32_t dtype;      /* enum pkv_dtype */
+  int64_t num_blocks; /* N, physical blocks in the pool (< 2^31) */
+} pkv_geometry;
+
+/* ---------------------------------------------------------------- library */
+
+int pkv_version(void);
+/* Thread-local text of the last failure on this thread ("" if none). */
+const char* pkv_last_error_message(void);
+const char* pkv_status_name(int status);
+
+/* ---------------------------------------------------------------- control plane (host only)
+ *
+ * The free list is a FIFO of block ids ([KVM] "free-list ring buffer", Table 3
+ * "free-list stack / FIFO"): allocation pops the front, release pushes the back.
+ * Sequence ids are assigned 0, 1, 2, ... and never reused.
+ */
+
+/* Create a pool.  initial_free_order: a permutation of [0, num_blocks) giving the
+ * FIFO's initial order, or NULL for 0, 1, 2, ...  Errors: INVALID_ARG (geometry,
+ * not a permutation), UNSUPPORTED (dtype). */
+int pkv_pool_create(const pkv_geometry* geometry, const int32_t* initial_free_order, pkv_pool** out);
+int pkv_pool_destroy(pkv_pool* pool);
+int pkv_pool_geometry(const pkv_pool* pool, pkv_geometry* out);
+
+/* New empty sequence. */
+int pkv_seq_create(pkv_pool* pool, int32_t* seq_id);
+
+/* Fork ([KVM] "Zero-copy deliberation via copy-on-write branching"): the child
+ * gets a copy of the parent's table, every shared block gains one owner, and the
+ * child's length is the parent's.  No data moves.  Errors: INVALID_ARG. */
+int pkv_seq_fork(pkv_pool* pool, int32_t parent, int32_t* child);
+
+/* Release ([KVM] release_sequence_blocks): walk the table in order, drop one
+ * owner per block, push blocks that reach zero owners to the FIFO back.
+ * Errors: DOUBLE_FREE (already released), INVALID_ARG (never created). */
+int pkv_seq_free(pkv_pool* pool, int32_t seq);
+
+int pkv_seq_len(const pkv_pool* pool, int32_t seq, int64_t* len);
+
+/* Plan an append of n_new[i] tokens to sequence seq_ids[i], i < n (distinct ids,
+ * resident).  Sequences are processed in ascending id; for each token t:
+ * l = t / B, o = t mod B; o == 0 allocates a block for T[l]; otherwise if T[l]
+ * has more than one owner it is copied first (copy-on-write: a fresh block is
+ * allocated, the pair (old, new) is emitted, the old block loses one owner and
+ * T[l] = new); the token's slot is T[l] * B + o ([KVM] PagedAttention model and
+ * CoW branching; [PA] "Sharing and copy-on-write").
+ *   slot_mapping : host int32 [sum n_new], sequence i's tokens start at
+ *                  sum_{j<i} n_new[j] (the caller's order).
+ *   cow_pairs    : host int32 [capacity n][2] (src, dst), at most one per sequence;
+ *                  *n_cow receives the count.  The caller copies them with
+ *                  pkv_copy_blocks BEFORE writing the new tokens.
+ * All or nothing: OUT_OF_BLOCKS leaves every table, count and the FIFO unchanged
+ * ([PA] "a failed multi-block reservation leaks no blocks"). */
+int pkv_plan_append(pkv_pool* pool, const int32_t* seq_ids, const int32_t* n_new, int32_t n,
+                    int32_t* slot_mapping, int32_t* cow_pairs, int32_t* n_cow);
+
+/* Host copy of the tables of n resident sequences: tables is int32 [n][W], row i
+ * holds seq_ids[i]'s blocks then zeros; seq_lens is int32 [n].
+ * Errors: INVALID_ARG (unknown / swapped-out id, W too small). */
+int pkv_export_tables(const pkv_pool* pool, const int32_t* seq_ids, int32_t n, int32_t* tables, int32_t W,
+                      int32_t* seq_lens);
+
+/* Reference count of every block: int32 [num_blocks]. */
+int pkv_refcounts(const pkv_pool* pool, int32_t* out);
+
+/* FIFO contents, front to back, into out (capacity num_blocks); *n = count. */
+int pkv_free_list(const pkv_pool* pool, int32_t* out, int64_t* n);
+
+/* ---------------------------------------------------------------- data plane (device, async)
+ *
+ * k_pool / v_pool are device pointers to the caller's pools (layout above,
+ * 16-byte aligned).  Every kernel checks its indices against the geometry.
+ */
+
+/* Write new keys/values at their slots ([PA] "The real cache"; [KVM] Table 3):
+ * K_pool[slot / B][layer][h][slot mod B][:] = k_new[i][h][:], same for V.
+ *   layer >= 0 : k_new, v_new are device [n_tok][H_kv][d_head] for that layer.
+ *   layer == -1: they are device [L][n_tok][H_kv][d_head], all layers written.
+ *   slot_mapping: device int32 [n_tok]; a slot outside [0, N*B) is skipped and
+ *   recorded in the device error word. */
+int pkv_append_kv(const pkv_pool* pool, int32_t layer, const void* k_new, const void* v_new,
+                  const int32_t* slot_mapping, int32_t n_tok, void* k_pool, void* v_pool, pkv_stream_t stream);
+
+/* Bytes of device workspace pkv_decode_attention needs for n_seq sequences on
+ * the current device. */
+int pkv_decode_workspace_size(const pkv_pool* pool, int32_t n_seq, size_t* bytes);
+
+/* Decode attention over the block tables ([KVM] PagedAttention model: the kernel
+ * takes the block table and walks logical blocks 0 .. floor((S-1)/B); [PA] "It is
+ * the same function"):
+ *   out[s][h][:] = sum_{t < len_s} softmax_t(scale * q[s][h] . K_s[t]) V_s[t],
+ *   K_s[t] = k_pool[T_s[floor(t/B)]][layer][floor(h/G)][t mod B].
+ * The context is split into 16-token tiles shared evenly across all warps of a
+ * persistent grid; partial (m, l, O) statistics of a sequence split across warps
+ * are merged with the online-softmax rule of [KVM] "Chunked prefill mechanics".
+ *   q, out      : device [n_seq][H_q][d_head], dtype = geometry dtype.
+ *   block_tables: device int32 [n_seq][W];  seq_lens: device int32 [n_seq]
+ *                 (0 <= len <= W*B; len 0 gives a zero output).
+ *   workspace   : device, >= pkv_decode_workspace_size bytes, 256-byte aligned;
+ *                 no state survives between calls.
+ * Calls on one workspace must not overlap on the GPU.
+ * bf16/f16 with d_head 64 or 128, G <= 8 and B a multiple of 16 run on the
+ * tensor-core path (TMA-staged tiles, mma.sync); other geometries on CUDA cores. */
+int pkv_decode_attention(const pkv_pool* pool, int32_t layer, const void* q, const void* k_pool,
+                         const void* v_pool, const int32_t* block_tables, int32_t W, const int32_t* seq_lens,
+                         int32_t n_seq, float scale, void* out, void* workspace, size_t ws_bytes,
+                         pkv_stream_t stream);
+
+/* Copy-on-write data step ([KVM] "copies the B tokens from the shared block into
+ * p_new"): for each (src, dst) in pairs (HOST int32 [n][2]), copy every slot of
+ * every layer of block src into block dst, for K and V.  Pairs are passed to the
+ * kernel by value.  Errors: BAD_BLOCK_ID. */
+int pkv_copy_blocks(const pkv_pool* pool, const int32_t* pairs, int32_t n, void* k_pool, void* v_pool,
+                    pkv_stream_t stream);
+
+/* Swap a resident sequence out to the host tier ([KVM] "Asynchronous paged
+ * swapping", swap_out_trajectory): block j of its table (j < n, n = its block
+ * count) is copied to host frame host_slots[j] (HOST int64 [n], each in
+ * [0, host_frames)); then, on the host, each GPU block loses one owner and blocks
+ * reaching zero go to the FIFO back; the sequence keeps its length and is marked
+ * swapped out.  Freed blocks may be reallocated at once: later writes to them
+ * must be ordered after this call's stream work (same stream, or an event).
+ *   host: page-locked (cudaHostAlloc / cudaHostRegister) or device-accessible
+ *         host memory of host_frames * M_block bytes.
+ *   block_ids_out: optional HOST int32 [n], the blocks copied (table order).
+ * The copy runs as an SM kernel, or on the copy engines after
+ * pkv_pool_set_swap_engine(pool, 1). */
+int pkv_swap_out(pkv_pool* pool, int32_t seq, const void* k_pool, const void* v_pool, void* host,
+                 int64_t host_frames, const int64_t* host_slots, int32_t n, int32_t* block_ids_out,
+                 pkv_stream_t stream);
+
+/* Swap a swapped-out sequence back in: allocate n fresh blocks from the FIFO
+ * front (all or nothing), copy the host frames recorded at swap-out into them in
+ * table order, and point the table at them.  new_block_ids: optional HOST int32 [n]. */
+int pkv_swap_in(pkv_pool* pool, int32_t seq, const void* host, int64_t host_frames, int32_t n, void* k_pool,
+                void* v_pool, int32_t* new_block_ids, pkv_stream_t stream);
+
+/* Host frames recorded for a swapped-out sequence: HOST int64 [capacity], *n = count. */
+int pkv_seq_host_slots(const pkv_pool* pool, int32_t seq, int64_t* out, int32_t capacity, int32_t* n);
+
+/* 0 = swap with SM kernels (default), 1 = with cudaMemcpyAsync on the copy engines. */
+int pkv_pool_set_swap_engine(pkv_pool* pool, int32_t engine);
+
+/* Synchronize the stream, then read and clear the current device's error word.
+ * Returns DEVICE_CHECK if a kernel recorded a bad index since the last check;
+ * *code (kernel-specific, nonzero) and *detail (the offending value) describe it.
+ * Either output pointer may be NULL. */
+int pkv_check_device_error(pkv_stream_t stream, int32_t* code, int64_t* detail);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H */

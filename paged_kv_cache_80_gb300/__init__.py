@@ -1,0 +1,342 @@
+"""Python binding of libpkv (the paged KV cache hot path for GB300).
+
+Argument marshalling only: every function below calls the C entry point of the
+same name in ``libpkv.so`` (declared in ``include/pkv.h``).  Device buffers are
+torch CUDA tensors (their data pointers are passed), host control-plane arrays
+are numpy arrays, and streams default to torch's current stream.  There is no
+fallback: if the library is not built, or a buffer is on the wrong device, the
+call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence, Union
+
+import numpy as np
+
+__all__ = [
+    "PkvError", "Geometry", "Pool", "library_path", "F32", "F16", "BF16",
+    "pkv_version", "pkv_pool_create", "pkv_pool_destroy", "pkv_pool_geometry", "pkv_seq_create", "pkv_seq_fork",
+    "pkv_seq_free", "pkv_seq_len", "pkv_plan_append", "pkv_export_tables", "pkv_refcounts", "pkv_free_list",
+    "pkv_append_kv", "pkv_decode_workspace_size", "pkv_decode_attention", "pkv_copy_blocks", "pkv_swap_out",
+    "pkv_swap_in", "pkv_seq_host_slots", "pkv_pool_set_swap_engine", "pkv_check_device_error",
+]
+
+F32, F16, BF16 = 0, 1, 2
+DTYPES = {"f32": F32, "f16": F16, "bf16": BF16}
+_HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+def library_path() -> str:
+    return os.path.join(_HERE, "libpkv.so")
+
+
+class PkvError(RuntimeError):
+    def __init__(self, status: int, name: str, message: str, where: str):
+        super().__init__(f"{where}: {name}: {message}")
+        self.status = status
+        self.name = name
+
+
+class Geometry(ctypes.Structure):
+    _fields_ = [("L", ctypes.c_int32), ("H_q", ctypes.c_int32), ("H_kv", ctypes.c_int32),
+                ("d_head", ctypes.c_int32), ("block_size", ctypes.c_int32), ("dtype", ctypes.c_int32),
+                ("num_blocks", ctypes.c_int64)]
+
+
+_lib = None
+
+
+def _L():
+    global _lib
+    if _lib is None:
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is not built: run `python -c 'import __graft_entry__ as g; g.build()'`")
+        L = ctypes.CDLL(path)
+        vp, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+        P32, P64 = ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int64)
+        sig = {
+            "pkv_version": ([], ctypes.c_int),
+            "pkv_last_error_message": ([], ctypes.c_char_p),
+            "pkv_status_name": ([ctypes.c_int], ctypes.c_char_p),
+            "pkv_pool_create": ([ctypes.POINTER(Geometry), P32, ctypes.POINTER(vp)], ctypes.c_int),
+            "pkv_pool_destroy": ([vp], ctypes.c_int),
+            "pkv_pool_geometry": ([vp, ctypes.POINTER(Geometry)], ctypes.c_int),
+            "pkv_seq_create": ([vp, P32], ctypes.c_int),
+            "pkv_seq_fork": ([vp, i32, P32], ctypes.c_int),
+            "pkv_seq_free": ([vp, i32], ctypes.c_int),
+            "pkv_seq_len": ([vp, i32, P64], ctypes.c_int),
+            "pkv_plan_append": ([vp, P32, P32, i32, P32, P32, P32], ctypes.c_int),
+            "pkv_export_tables": ([vp, P32, i32, P32, i32, P32], ctypes.c_int),
+            "pkv_refcounts": ([vp, P32], ctypes.c_int),
+            "pkv_free_list": ([vp, P32, P64], ctypes.c_int),
+            "pkv_append_kv": ([vp, i32, vp, vp, vp, i32, vp, vp, vp], ctypes.c_int),
+            "pkv_decode_workspace_size": ([vp, i32, ctypes.POINTER(ctypes.c_size_t)], ctypes.c_int),
+            "pkv_decode_attention": ([vp, i32, vp, vp, vp, vp, i32, vp, i32, ctypes.c_float, vp, vp, ctypes.c_size_t,
+                                      vp], ctypes.c_int),
+            "pkv_copy_blocks": ([vp, P32, i32, vp, vp, vp], ctypes.c_int),
+            "pkv_swap_out": ([vp, i32, vp, vp, vp, i64, P64, i32, P32, vp], ctypes.c_int),
+            "pkv_swap_in": ([vp, i32, vp, i64, i32, vp, vp, P32, vp], ctypes.c_int),
+            "pkv_seq_host_slots": ([vp, i32, P64, i32, P32], ctypes.c_int),
+            "pkv_pool_set_swap_engine": ([vp, i32], ctypes.c_int),
+            "pkv_check_device_error": ([vp, P32, P64], ctypes.c_int),
+        }
+        for name, (args, res) in sig.items():
+            f = getattr(L, name)
+            f.argtypes = args
+            f.restype = res
+        _lib = L
+    return _lib
+
+
+def _check(rc: int, where: str):
+    if rc != 0:
+        L = _L()
+        raise PkvError(rc, L.pkv_status_name(rc).decode(), L.pkv_last_error_message().decode(), where)
+
+
+def _i32(a) -> np.ndarray:
+    return np.ascontiguousarray(a, dtype=np.int32)
+
+
+def _i64(a) -> np.ndarray:
+    return np.ascontiguousarray(a, dtype=np.int64)
+
+
+def _p32(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+
+
+def _p64(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_int64))
+
+
+def _dev(t, what: str) -> int:
+    """Device pointer of a CUDA tensor (raises for anything else)."""
+    if not hasattr(t, "is_cuda") or not t.is_cuda:
+        raise TypeError(f"{what} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{what} must be contiguous")
+    return t.data_ptr()
+
+
+def _host_ptr(t, what: str) -> int:
+    """Address of a host buffer: a CPU torch tensor (pinned for kernel access) or numpy array."""
+    if isinstance(t, np.ndarray):
+        if not t.flags.c_contiguous:
+            raise ValueError(f"{what} must be contiguous")
+        return t.ctypes.data
+    if hasattr(t, "is_cuda") and not t.is_cuda:
+        if not t.is_contiguous():
+            raise ValueError(f"{what} must be contiguous")
+        return t.data_ptr()
+    raise TypeError(f"{what} must be a host buffer")
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+class Pool:
+    """Owner of a pkv_pool handle (destroyed with the object)."""
+
+    def __init__(self, handle: ctypes.c_void_p, geometry: Geometry):
+        self.handle = handle
+        self.geometry = geometry
+
+    @property
+    def _as_parameter_(self):
+        return self.handle
+
+    def __del__(self):
+        h = getattr(self, "handle", None)
+        if h and _lib is not None:
+            _lib.pkv_pool_destroy(h)
+            self.handle = None
+
+
+PoolLike = Union[Pool, ctypes.c_void_p]
+
+
+def _h(pool: PoolLike):
+    return pool.handle if isinstance(pool, Pool) else pool
+
+
+# ------------------------------------------------------------------ library
+
+
+def pkv_version() -> int:
+    return _L().pkv_version()
+
+
+# ------------------------------------------------------------------ control plane
+
+
+def pkv_pool_create(L: int, H_q: int, H_kv: int, d_head: int, block_size: int, dtype: Union[str, int],
+                    num_blocks: int, initial_free_order: Optional[np.ndarray] = None) -> Pool:
+    g = Geometry(L, H_q, H_kv, d_head, block_size, DTYPES.get(dtype, dtype), num_blocks)
+    fo = None
+    if initial_free_order is not None:
+        fo_arr = _i32(initial_free_order)
+        if fo_arr.size != num_blocks:
+            raise ValueError("initial_free_order must have num_blocks entries")
+        fo = _p32(fo_arr)
+    h = ctypes.c_void_p()
+    _check(_L().pkv_pool_create(ctypes.byref(g), fo, ctypes.byref(h)), "pkv_pool_create")
+    return Pool(h, g)
+
+
+def pkv_pool_destroy(pool: Pool) -> None:
+    _check(_L().pkv_pool_destroy(_h(pool)), "pkv_pool_destroy")
+    if isinstance(pool, Pool):
+        pool.handle = None
+
+
+def pkv_pool_geometry(pool: PoolLike) -> Geometry:
+    g = Geometry()
+    _check(_L().pkv_pool_geometry(_h(pool), ctypes.byref(g)), "pkv_pool_geometry")
+    return g
+
+
+def pkv_seq_create(pool: PoolLike) -> int:
+    out = ctypes.c_int32()
+    _check(_L().pkv_seq_create(_h(pool), ctypes.byref(out)), "pkv_seq_create")
+    return out.value
+
+
+def pkv_seq_fork(pool: PoolLike, parent: int) -> int:
+    out = ctypes.c_int32()
+    _check(_L().pkv_seq_fork(_h(pool), parent, ctypes.byref(out)), "pkv_seq_fork")
+    return out.value
+
+
+def pkv_seq_free(pool: PoolLike, seq: int) -> None:
+    _check(_L().pkv_seq_free(_h(pool), seq), "pkv_seq_free")
+
+
+def pkv_seq_len(pool: PoolLike, seq: int) -> int:
+    out = ctypes.c_int64()
+    _check(_L().pkv_seq_len(_h(pool), seq, ctypes.byref(out)), "pkv_seq_len")
+    return out.value
+
+
+def pkv_plan_append(pool: PoolLike, seq_ids: Sequence[int], n_new: Sequence[int]):
+    """Returns (slot_mapping int32[sum n_new], cow_pairs int32[n_cow, 2])."""
+    ids, nn = _i32(seq_ids), _i32(n_new)
+    if ids.shape != nn.shape:
+        raise ValueError("seq_ids and n_new differ in length")
+    total = int(nn.sum()) if nn.size else 0
+    slots = np.zeros(max(total, 1), np.int32)
+    pairs = np.zeros((max(ids.size, 1), 2), np.int32)
+    ncow = ctypes.c_int32()
+    _check(_L().pkv_plan_append(_h(pool), _p32(ids), _p32(nn), ids.size, _p32(slots), _p32(pairs),
+                                ctypes.byref(ncow)), "pkv_plan_append")
+    return slots[:total], pairs[: ncow.value]
+
+
+def pkv_export_tables(pool: PoolLike, seq_ids: Sequence[int], W: int, tables: Optional[np.ndarray] = None,
+                      seq_lens: Optional[np.ndarray] = None):
+    """Returns (tables int32[n, W], seq_lens int32[n]); fills the given arrays if passed."""
+    ids = _i32(seq_ids)
+    if tables is None:
+        tables = np.zeros((ids.size, max(W, 1)), np.int32)
+    if seq_lens is None:
+        seq_lens = np.zeros(max(ids.size, 1), np.int32)
+    _check(_L().pkv_export_tables(_h(pool), _p32(ids), ids.size, _p32(tables), W, _p32(seq_lens)),
+           "pkv_export_tables")
+    return tables[: ids.size, :W], seq_lens[: ids.size]
+
+
+def pkv_refcounts(pool: PoolLike) -> np.ndarray:
+    g = pkv_pool_geometry(pool)
+    out = np.zeros(g.num_blocks, np.int32)
+    _check(_L().pkv_refcounts(_h(pool), _p32(out)), "pkv_refcounts")
+    return out
+
+
+def pkv_free_list(pool: PoolLike) -> np.ndarray:
+    g = pkv_pool_geometry(pool)
+    out = np.zeros(g.num_blocks, np.int32)
+    n = ctypes.c_int64()
+    _check(_L().pkv_free_list(_h(pool), _p32(out), ctypes.byref(n)), "pkv_free_list")
+    return out[: n.value]
+
+
+def pkv_pool_set_swap_engine(pool: PoolLike, engine: int) -> None:
+    _check(_L().pkv_pool_set_swap_engine(_h(pool), engine), "pkv_pool_set_swap_engine")
+
+
+def pkv_seq_host_slots(pool: PoolLike, seq: int) -> np.ndarray:
+    n = ctypes.c_int32()
+    _check(_L().pkv_seq_host_slots(_h(pool), seq, None, 0, ctypes.byref(n)), "pkv_seq_host_slots")
+    out = np.zeros(max(n.value, 1), np.int64)
+    _check(_L().pkv_seq_host_slots(_h(pool), seq, _p64(out), n.value, ctypes.byref(n)), "pkv_seq_host_slots")
+    return out[: n.value]
+
+
+# ------------------------------------------------------------------ data plane
+
+
+def pkv_append_kv(pool: PoolLike, layer: int, k_new, v_new, slot_mapping, k_pool, v_pool, stream=None) -> None:
+    n_tok = int(slot_mapping.numel())
+    _check(_L().pkv_append_kv(_h(pool), layer, _dev(k_new, "k_new"), _dev(v_new, "v_new"),
+                              _dev(slot_mapping, "slot_mapping"), n_tok, _dev(k_pool, "k_pool"),
+                              _dev(v_pool, "v_pool"), _stream(stream)), "pkv_append_kv")
+
+
+def pkv_decode_workspace_size(pool: PoolLike, n_seq: int) -> int:
+    out = ctypes.c_size_t()
+    _check(_L().pkv_decode_workspace_size(_h(pool), n_seq, ctypes.byref(out)), "pkv_decode_workspace_size")
+    return out.value
+
+
+def pkv_decode_attention(pool: PoolLike, layer: int, q, k_pool, v_pool, block_tables, seq_lens, scale: float, out,
+                         workspace, stream=None) -> None:
+    n_seq = int(seq_lens.numel())
+    W = int(block_tables.shape[1]) if block_tables.dim() == 2 else 0
+    _check(_L().pkv_decode_attention(_h(pool), layer, _dev(q, "q"), _dev(k_pool, "k_pool"), _dev(v_pool, "v_pool"),
+                                     _dev(block_tables, "block_tables"), W, _dev(seq_lens, "seq_lens"), n_seq,
+                                     float(scale), _dev(out, "out"), _dev(workspace, "workspace"),
+                                     workspace.numel() * workspace.element_size(), _stream(stream)),
+           "pkv_decode_attention")
+
+
+def pkv_copy_blocks(pool: PoolLike, pairs, k_pool, v_pool, stream=None) -> None:
+    pr = _i32(pairs).reshape(-1, 2)
+    _check(_L().pkv_copy_blocks(_h(pool), _p32(pr), pr.shape[0], _dev(k_pool, "k_pool"), _dev(v_pool, "v_pool"),
+                                _stream(stream)), "pkv_copy_blocks")
+
+
+def pkv_swap_out(pool: PoolLike, seq: int, k_pool, v_pool, host, host_frames: int, host_slots,
+                 stream=None) -> np.ndarray:
+    hs = _i64(host_slots)
+    ids = np.zeros(max(hs.size, 1), np.int32)
+    _check(_L().pkv_swap_out(_h(pool), seq, _dev(k_pool, "k_pool"), _dev(v_pool, "v_pool"), _host_ptr(host, "host"),
+                             host_frames, _p64(hs), hs.size, _p32(ids), _stream(stream)), "pkv_swap_out")
+    return ids[: hs.size]
+
+
+def pkv_swap_in(pool: PoolLike, seq: int, host, host_frames: int, n: int, k_pool, v_pool,
+                stream=None) -> np.ndarray:
+    ids = np.zeros(max(n, 1), np.int32)
+    _check(_L().pkv_swap_in(_h(pool), seq, _host_ptr(host, "host"), host_frames, n, _dev(k_pool, "k_pool"),
+                            _dev(v_pool, "v_pool"), _p32(ids), _stream(stream)), "pkv_swap_in")
+    return ids[:n]
+
+
+def pkv_check_device_error(stream=None):
+    """Synchronise the stream and read/clear the device error word.  Returns
+    (code, detail); raises PkvError(DEVICE_CHECK) if a kernel recorded one."""
+    code = ctypes.c_int32()
+    detail = ctypes.c_int64()
+    rc = _L().pkv_check_device_error(_stream(stream), ctypes.byref(code), ctypes.byref(detail))
+    _check(rc, "pkv_check_device_error")
+    return code.value, detail.value

@@ -1,0 +1,542 @@
+// Host control plane and C ABI entry points.
+//
+// The control plane follows "KV Cache Management" (cs249r vol. 3 ch. 5), "The
+// PagedAttention virtual memory model" (block table T: l -> p with l = floor(t/B),
+// o = t mod B; allocation from a free-list ring buffer when o == 0) and "Zero-copy
+// deliberation via copy-on-write branching" (fork = table duplication plus a
+// reference-count increment; a write into a block with more than one owner first
+// copies it into a fresh block; release walks the table and returns blocks that
+// reach zero owners to the free list), and "PagedAttention" (programmer.ie ch. 14),
+// "Inference Lab increment" (out-of-blocks and double-free errors; a failed
+// reservation leaks nothing).
+//
+// All-or-nothing reservation is done with a dry run that counts the blocks an
+// append needs (new blocks plus copy-on-write copies, with the owner counts the
+// earlier sequences of the same call leave behind) before anything is changed.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstring>
+#include <string>
+#include <unordered_map>
+#include <vector>
+
+#include "pkv_internal.h"
+
+namespace pkv {
+
+static thread_local std::string g_msg;
+
+int fail(int status, const std::string& msg) {
+  g_msg = msg;
+  return status;
+}
+
+void clear_error() { g_msg.clear(); }
+
+// ------------------------------------------------------------------ free ring
+
+void FreeRing::reset(const std::vector<int32_t>& order) {
+  ring_ = order;
+  cap_ = static_cast<int64_t>(order.size());
+  head_ = 0;
+  count_ = cap_;
+}
+
+int32_t FreeRing::pop_front() {
+  int32_t p = ring_[head_];
+  head_ = (head_ + 1) % cap_;
+  --count_;
+  return p;
+}
+
+void FreeRing::push_back(int32_t p) {
+  ring_[(head_ + count_) % cap_] = p;
+  ++count_;
+}
+
+}  // namespace pkv
+
+using pkv::fail;
+using pkv::Pool;
+using pkv::SeqState;
+
+namespace {
+
+Pool* as_pool(pkv_pool* p) { return reinterpret_cast<Pool*>(p); }
+const Pool* as_pool(const pkv_pool* p) { return reinterpret_cast<const Pool*>(p); }
+
+int check_geometry(const pkv_geometry* g) {
+  if (!g) return fail(PKV_ERR_INVALID_ARG, "geometry is NULL");
+  if (g->L <= 0 || g->H_kv <= 0 || g->H_q <= 0 || g->d_head <= 0 || g->block_size <= 0 || g->num_blocks <= 0)
+    return fail(PKV_ERR_INVALID_ARG, "geometry fields must be positive");
+  if (g->H_q % g->H_kv) return fail(PKV_ERR_INVALID_ARG, "H_q must be a multiple of H_kv");
+  if (g->d_head % 2 || g->d_head > 256) return fail(PKV_ERR_INVALID_ARG, "d_head must be even and <= 256");
+  if (g->dtype != PKV_F32 && g->dtype != PKV_F16 && g->dtype != PKV_BF16)
+    return fail(PKV_ERR_UNSUPPORTED, "dtype must be PKV_F32, PKV_F16 or PKV_BF16");
+  if (g->num_blocks >= (int64_t(1) << 31)) return fail(PKV_ERR_INVALID_ARG, "num_blocks must be < 2^31");
+  if (g->num_blocks * g->block_size >= (int64_t(1) << 31))
+    return fail(PKV_ERR_INVALID_ARG, "num_blocks * block_size must be < 2^31 (int32 slots)");
+  return PKV_OK;
+}
+
+SeqState* find_seq(Pool& P, int32_t id) {
+  auto it = P.seqs.find(id);
+  return it == P.seqs.end() ? nullptr : &it->second;
+}
+
+const SeqState* find_seq(const Pool& P, int32_t id) {
+  auto it = P.seqs.find(id);
+  return it == P.seqs.end() ? nullptr : &it->second;
+}
+
+// Releasing a released sequence is a double free; any other use of it, or of an
+// id never created, is an invalid argument.
+int unknown_seq(const Pool& P, int32_t id, bool releasing = false) {
+  if (releasing && id >= 0 && id < static_cast<int32_t>(P.released.size()) && P.released[id])
+    return fail(PKV_ERR_DOUBLE_FREE, "sequence " + std::to_string(id) + " was already released");
+  return fail(PKV_ERR_INVALID_ARG, "unknown or released sequence " + std::to_string(id));
+}
+
+// Drop one owner of block p; at zero it goes to the back of the FIFO.
+void drop_owner(Pool& P, int32_t p) {
+  if (--P.ref[p] == 0) P.free.push_back(p);
+}
+
+// Device-accessible address of a host-tier buffer, or nullptr.
+void* device_view_of_host(void* host) {
+  cudaPointerAttributes attr{};
+  if (cudaPointerGetAttributes(&attr, host) == cudaSuccess) {
+    if (attr.type == cudaMemoryTypeHost && attr.devicePointer) return attr.devicePointer;
+    if (attr.type == cudaMemoryTypeManaged) return host;
+  }
+  cudaGetLastError();
+  int dev = 0, pageable = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess &&
+      cudaDeviceGetAttribute(&pageable, cudaDevAttrPageableMemoryAccess, dev) == cudaSuccess && pageable)
+    return host;
+  cudaGetLastError();
+  return nullptr;
+}
+
+// Copy n images of `bytes` with the copy engines.
+int copy_engine(const void* src_base, void* dst_base, const pkv::CopyItem* items, int64_t n, int64_t bytes,
+                cudaStream_t s) {
+  for (int64_t i = 0; i < n; ++i) {
+    cudaError_t e = cudaMemcpyAsync(static_cast<char*>(dst_base) + items[i].dst_off,
+                                    static_cast<const char*>(src_base) + items[i].src_off, bytes, cudaMemcpyDefault, s);
+    if (e != cudaSuccess) return fail(PKV_ERR_CUDA, std::string("cudaMemcpyAsync: ") + cudaGetErrorString(e));
+  }
+  return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int pkv_version(void) { return PKV_VERSION; }
+
+const char* pkv_last_error_message(void) { return pkv::g_msg.c_str(); }
+
+const char* pkv_status_name(int s) {
+  switch (s) {
+    case PKV_OK: return "PKV_OK";
+    case PKV_ERR_INVALID_ARG: return "PKV_ERR_INVALID_ARG";
+    case PKV_ERR_OUT_OF_BLOCKS: return "PKV_ERR_OUT_OF_BLOCKS";
+    case PKV_ERR_DOUBLE_FREE: return "PKV_ERR_DOUBLE_FREE";
+    case PKV_ERR_BAD_BLOCK_ID: return "PKV_ERR_BAD_BLOCK_ID";
+    case PKV_ERR_CUDA: return "PKV_ERR_CUDA";
+    case PKV_ERR_DEVICE_CHECK: return "PKV_ERR_DEVICE_CHECK";
+    case PKV_ERR_TIMEOUT: return "PKV_ERR_TIMEOUT";
+    case PKV_ERR_UNSUPPORTED: return "PKV_ERR_UNSUPPORTED";
+    default: return "PKV_ERR_UNKNOWN";
+  }
+}
+
+int pkv_pool_create(const pkv_geometry* geometry, const int32_t* initial_free_order, pkv_pool** out) {
+  pkv::clear_error();
+  if (!out) return fail(PKV_ERR_INVALID_ARG, "out is NULL");
+  if (int rc = check_geometry(geometry)) return rc;
+  const int64_t N = geometry->num_blocks;
+  std::vector<int32_t> order(N);
+  if (initial_free_order) {
+    std::vector<uint8_t> seen(N, 0);
+    for (int64_t i = 0; i < N; ++i) {
+      int32_t p = initial_free_order[i];
+      if (p < 0 || p >= N || seen[p]) return fail(PKV_ERR_INVALID_ARG, "initial_free_order is not a permutation");
+      seen[p] = 1;
+      order[i] = p;
+    }
+  } else {
+    for (int64_t i = 0; i < N; ++i) order[i] = static_cast<int32_t>(i);
+  }
+  Pool* P = new Pool();
+  P->geo = *geometry;
+  P->slab_elems = static_cast<int64_t>(geometry->block_size) * geometry->d_head;
+  P->block_elems = static_cast<int64_t>(geometry->L) * geometry->H_kv * P->slab_elems;
+  P->block_bytes = P->block_elems * pkv::elem_size(geometry->dtype);
+  P->free.reset(order);
+  P->ref.assign(N, 0);
+  *out = reinterpret_cast<pkv_pool*>(P);
+  return PKV_OK;
+}
+
+int pkv_pool_destroy(pkv_pool* pool) {
+  pkv::clear_error();
+  if (!pool) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
+  Pool* P = as_pool(pool);
+  pkv::destroy_tensor_maps(*P);
+  delete P;
+  return PKV_OK;
+}
+
+int pkv_pool_geometry(const pkv_pool* pool, pkv_geometry* out) {
+  pkv::clear_error();
+  if (!pool || !out) return fail(PKV_ERR_INVALID_ARG, "NULL argument");
+  *out = as_pool(pool)->geo;
+  return PKV_OK;
+}
+
+int pkv_seq_create(pkv_pool* pool, int32_t* seq_id) {
+  pkv::clear_error();
+  if (!pool || !seq_id) return fail(PKV_ERR_INVALID_ARG, "NULL argument");
+  Pool& P = *as_pool(pool);
+  if (P.next_id == INT32_MAX) return fail(PKV_ERR_INVALID_ARG, "sequence ids exhausted");
+  const int32_t id = P.next_id++;
+  P.seqs.emplace(id, SeqState());
+  P.released.push_back(0);
+  *seq_id = id;
+  return PKV_OK;
+}
+
+int pkv_seq_fork(pkv_pool* pool, int32_t parent, int32_t* child) {
+  pkv::clear_error();
+  if (!pool || !child) return fail(PKV_ERR_INVALID_ARG, "NULL argument");
+  Pool& P = *as_pool(pool);
+  const SeqState* par = find_seq(P, parent);
+  if (!par) return unknown_seq(P, parent);
+  if (par->swapped) return fail(PKV_ERR_INVALID_ARG, "cannot fork a swapped-out sequence");
+  if (P.next_id == INT32_MAX) return fail(PKV_ERR_INVALID_ARG, "sequence ids exhausted");
+  SeqState c;
+  c.table = par->table;  // table duplication
+  c.len = par->len;      // S_child = S_prefix
+  for (int32_t p : c.table) ++P.ref[p];  // one more owner per shared block
+  const int32_t id = P.next_id++;
+  P.seqs.emplace(id, std::move(c));
+  P.released.push_back(0);
+  *child = id;
+  return PKV_OK;
+}
+
+int pkv_seq_free(pkv_pool* pool, int32_t seq) {
+  pkv::clear_error();
+  if (!pool) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
+  Pool& P = *as_pool(pool);
+  SeqState* s = find_seq(P, seq);
+  if (!s) return unknown_seq(P, seq, true);
+  for (int32_t p : s->table)
+    if (P.ref[p] <= 0) return fail(PKV_ERR_DOUBLE_FREE, "block " + std::to_string(p) + " has no owner");
+  for (int32_t p : s->table) drop_owner(P, p);
+  P.seqs.erase(seq);
+  P.released[seq] = 1;
+  return PKV_OK;
+}
+
+int pkv_seq_len(const pkv_pool* pool, int32_t seq, int64_t* len) {
+  pkv::clear_error();
+  if (!pool || !len) return fail(PKV_ERR_INVALID_ARG, "NULL argument");
+  const Pool& P = *as_pool(pool);
+  const SeqState* s = find_seq(P, seq);
+  if (!s) return unknown_seq(P, seq);
+  *len = s->len;
+  return PKV_OK;
+}
+
+int pkv_plan_append(pkv_pool* pool, const int32_t* seq_ids, const int32_t* n_new, int32_t n, int32_t* slot_mapping,
+                    int32_t* cow_pairs, int32_t* n_cow) {
+  pkv::clear_error();
+  if (!pool || n < 0 || (n > 0 && (!seq_ids || !n_new || !slot_mapping || !cow_pairs)) || !n_cow)
+    return fail(PKV_ERR_INVALID_ARG, "bad arguments to pkv_plan_append");
+  Pool& P = *as_pool(pool);
+  const int64_t B = P.geo.block_size;
+
+  // validate, and order the requests by ascending sequence id
+  std::vector<int32_t> order(n);
+  std::vector<int64_t> first_tok(n + 1, 0);
+  for (int32_t i = 0; i < n; ++i) {
+    const SeqState* s = find_seq(P, seq_ids[i]);
+    if (!s) return unknown_seq(P, seq_ids[i]);
+    if (s->swapped) return fail(PKV_ERR_INVALID_ARG, "sequence " + std::to_string(seq_ids[i]) + " is swapped out");
+    if (n_new[i] < 0) return fail(PKV_ERR_INVALID_ARG, "n_new must be >= 0");
+    if (s->len + n_new[i] > (int64_t(1) << 31) - 1) return fail(PKV_ERR_INVALID_ARG, "sequence too long");
+    order[i] = i;
+    first_tok[i + 1] = first_tok[i] + n_new[i];
+  }
+  std::sort(order.begin(), order.end(), [&](int32_t a, int32_t b) { return seq_ids[a] < seq_ids[b]; });
+  for (int32_t k = 1; k < n; ++k)
+    if (seq_ids[order[k]] == seq_ids[order[k - 1]]) return fail(PKV_ERR_INVALID_ARG, "duplicate sequence id");
+
+  // dry run: blocks needed, with owner counts as earlier copies leave them
+  std::unordered_map<int32_t, int32_t> dropped;  // block -> owners given up by earlier CoWs in this call
+  int64_t needed = 0;
+  for (int32_t i : order) {
+    if (n_new[i] == 0) continue;
+    const SeqState& s = *find_seq(P, seq_ids[i]);
+    const int64_t len = s.len;
+    if (len % B != 0) {
+      const int32_t tail = s.table[len / B];
+      auto it = dropped.find(tail);
+      const int32_t owners = P.ref[tail] - (it == dropped.end() ? 0 : it->second);
+      if (owners > 1) {
+        ++needed;
+        ++dropped[tail];
+      }
+    }
+    needed += (len + n_new[i] + B - 1) / B - (len + B - 1) / B;  // positions with o == 0
+  }
+  if (needed > P.free.size())
+    return fail(PKV_ERR_OUT_OF_BLOCKS, "append needs " + std::to_string(needed) + " blocks, " +
+                                           std::to_string(P.free.size()) + " free");
+
+  // commit
+  int32_t cows = 0;
+  for (int32_t i : order) {
+    SeqState& s = *find_seq(P, seq_ids[i]);
+    int32_t* out = slot_mapping + first_tok[i];
+    for (int32_t k = 0; k < n_new[i]; ++k) {
+      const int64_t t = s.len;
+      const int64_t l = t / B, o = t % B;
+      if (o == 0) {
+        s.table.push_back(P.free.pop_front());
+        P.ref[s.table.back()] = 1;
+      } else if (P.ref[s.table[l]] > 1) {
+        const int32_t old = s.table[l];
+        const int32_t fresh = P.free.pop_front();
+        P.ref[fresh] = 1;
+        cow_pairs[2 * cows] = old;
+        cow_pairs[2 * cows + 1] = fresh;
+        ++cows;
+        drop_owner(P, old);
+        s.table[l] = fresh;
+      }
+      out[k] = static_cast<int32_t>(s.table[l] * B + o);
+      ++s.len;
+    }
+  }
+  *n_cow = cows;
+  return PKV_OK;
+}
+
+int pkv_export_tables(const pkv_pool* pool, const int32_t* seq_ids, int32_t n, int32_t* tables, int32_t W,
+                      int32_t* seq_lens) {
+  pkv::clear_error();
+  if (!pool || n < 0 || W < 0 || (n > 0 && (!seq_ids || (W > 0 && !tables) || !seq_lens)))
+    return fail(PKV_ERR_INVALID_ARG, "bad arguments to pkv_export_tables");
+  const Pool& P = *as_pool(pool);
+  for (int32_t i = 0; i < n; ++i) {
+    const SeqState* s = find_seq(P, seq_ids[i]);
+    if (!s) return unknown_seq(P, seq_ids[i]);
+    if (s->swapped) return fail(PKV_ERR_INVALID_ARG, "sequence " + std::to_string(seq_ids[i]) + " is swapped out");
+    if (static_cast<int64_t>(s->table.size()) > W)
+      return fail(PKV_ERR_INVALID_ARG, "W = " + std::to_string(W) + " is smaller than a table of " +
+                                           std::to_string(s->table.size()) + " blocks");
+  }
+  for (int32_t i = 0; i < n; ++i) {
+    const SeqState& s = *find_seq(P, seq_ids[i]);
+    int32_t* row = tables + static_cast<int64_t>(i) * W;
+    std::copy(s.table.begin(), s.table.end(), row);
+    std::fill(row + s.table.size(), row + W, 0);
+    seq_lens[i] = static_cast<int32_t>(s.len);
+  }
+  return PKV_OK;
+}
+
+int pkv_refcounts(const pkv_pool* pool, int32_t* out) {
+  pkv::clear_error();
+  if (!pool || !out) return fail(PKV_ERR_INVALID_ARG, "NULL argument");
+  const Pool& P = *as_pool(pool);
+  std::copy(P.ref.begin(), P.ref.end(), out);
+  return PKV_OK;
+}
+
+int pkv_free_list(const pkv_pool* pool, int32_t* out, int64_t* n) {
+  pkv::clear_error();
+  if (!pool || !out || !n) return fail(PKV_ERR_INVALID_ARG, "NULL argument");
+  const Pool& P = *as_pool(pool);
+  for (int64_t i = 0; i < P.free.size(); ++i) out[i] = P.free.front_at(i);
+  *n = P.free.size();
+  return PKV_OK;
+}
+
+int pkv_pool_set_swap_engine(pkv_pool* pool, int32_t engine) {
+  pkv::clear_error();
+  if (!pool || (engine != 0 && engine != 1)) return fail(PKV_ERR_INVALID_ARG, "engine must be 0 or 1");
+  as_pool(pool)->swap_engine = engine;
+  return PKV_OK;
+}
+
+// ------------------------------------------------------------------ data plane
+
+int pkv_append_kv(const pkv_pool* pool, int32_t layer, const void* k_new, const void* v_new,
+                  const int32_t* slot_mapping, int32_t n_tok, void* k_pool, void* v_pool, pkv_stream_t stream) {
+  pkv::clear_error();
+  if (!pool || n_tok < 0) return fail(PKV_ERR_INVALID_ARG, "bad arguments to pkv_append_kv");
+  const Pool& P = *as_pool(pool);
+  if (layer < -1 || layer >= P.geo.L) return fail(PKV_ERR_INVALID_ARG, "layer out of range");
+  if (n_tok > 0 && (!k_new || !v_new || !slot_mapping || !k_pool || !v_pool))
+    return fail(PKV_ERR_INVALID_ARG, "NULL buffer");
+  return pkv::launch_append(P, layer, k_new, v_new, slot_mapping, n_tok, k_pool, v_pool, stream);
+}
+
+int pkv_decode_workspace_size(const pkv_pool* pool, int32_t n_seq, size_t* bytes) {
+  pkv::clear_error();
+  if (!pool || !bytes || n_seq < 0) return fail(PKV_ERR_INVALID_ARG, "bad arguments");
+  return pkv::decode_workspace_bytes(*as_pool(pool), n_seq, bytes);
+}
+
+int pkv_decode_attention(const pkv_pool* pool, int32_t layer, const void* q, const void* k_pool, const void* v_pool,
+                         const int32_t* block_tables, int32_t W, const int32_t* seq_lens, int32_t n_seq, float scale,
+                         void* out, void* workspace, size_t ws_bytes, pkv_stream_t stream) {
+  pkv::clear_error();
+  if (!pool || n_seq < 0 || W < 0) return fail(PKV_ERR_INVALID_ARG, "bad arguments to pkv_decode_attention");
+  const Pool& P = *as_pool(pool);
+  if (layer < 0 || layer >= P.geo.L) return fail(PKV_ERR_INVALID_ARG, "layer out of range");
+  if (n_seq == 0) return PKV_OK;
+  if (!q || !k_pool || !v_pool || !block_tables || !seq_lens || !out || !workspace)
+    return fail(PKV_ERR_INVALID_ARG, "NULL buffer");
+  return pkv::launch_decode(const_cast<Pool&>(P), layer, q, k_pool, v_pool, block_tables, W, seq_lens, n_seq, scale,
+                            out, workspace, ws_bytes, stream);
+}
+
+int pkv_copy_blocks(const pkv_pool* pool, const int32_t* pairs, int32_t n, void* k_pool, void* v_pool,
+                    pkv_stream_t stream) {
+  pkv::clear_error();
+  if (!pool || n < 0 || (n > 0 && (!pairs || !k_pool || !v_pool)))
+    return fail(PKV_ERR_INVALID_ARG, "bad arguments to pkv_copy_blocks");
+  const Pool& P = *as_pool(pool);
+  std::vector<uint8_t> is_dst(P.geo.num_blocks, 0), is_src(P.geo.num_blocks, 0);
+  for (int32_t i = 0; i < n; ++i) {
+    const int32_t s = pairs[2 * i], d = pairs[2 * i + 1];
+    if (s < 0 || s >= P.geo.num_blocks || d < 0 || d >= P.geo.num_blocks)
+      return fail(PKV_ERR_BAD_BLOCK_ID, "copy pair (" + std::to_string(s) + ", " + std::to_string(d) + ") out of range");
+    if (is_dst[d]) return fail(PKV_ERR_INVALID_ARG, "a destination block appears twice");
+    is_dst[d] = 1;
+    is_src[s] = 1;
+  }
+  for (int32_t i = 0; i < n; ++i)
+    if (is_src[pairs[2 * i + 1]] && pairs[2 * i] != pairs[2 * i + 1])
+      return fail(PKV_ERR_INVALID_ARG, "a destination block is also a source");
+  std::vector<pkv::CopyItem> items(n);
+  for (int32_t i = 0; i < n; ++i)
+    items[i] = {pairs[2 * i] * P.block_bytes, pairs[2 * i + 1] * P.block_bytes};
+  if (int rc = pkv::launch_copy_images(k_pool, k_pool, items.data(), n, P.block_bytes, stream)) return rc;
+  return pkv::launch_copy_images(v_pool, v_pool, items.data(), n, P.block_bytes, stream);
+}
+
+int pkv_swap_out(pkv_pool* pool, int32_t seq, const void* k_pool, const void* v_pool, void* host, int64_t host_frames,
+                 const int64_t* host_slots, int32_t n, int32_t* block_ids_out, pkv_stream_t stream) {
+  pkv::clear_error();
+  if (!pool || n < 0 || host_frames < 0 || (n > 0 && (!k_pool || !v_pool || !host || !host_slots)))
+    return fail(PKV_ERR_INVALID_ARG, "bad arguments to pkv_swap_out");
+  Pool& P = *as_pool(pool);
+  SeqState* s = find_seq(P, seq);
+  if (!s) return unknown_seq(P, seq);
+  if (s->swapped) return fail(PKV_ERR_INVALID_ARG, "sequence is already swapped out");
+  if (static_cast<int64_t>(s->table.size()) != n)
+    return fail(PKV_ERR_INVALID_ARG, "n must equal the sequence's block count (" + std::to_string(s->table.size()) + ")");
+  std::unordered_map<int64_t, int> seen;
+  for (int32_t j = 0; j < n; ++j) {
+    if (host_slots[j] < 0 || host_slots[j] >= host_frames)
+      return fail(PKV_ERR_BAD_BLOCK_ID, "host frame " + std::to_string(host_slots[j]) + " out of range");
+    if (seen[host_slots[j]]++) return fail(PKV_ERR_INVALID_ARG, "a host frame appears twice");
+  }
+  for (int32_t p : s->table)
+    if (P.ref[p] <= 0) return fail(PKV_ERR_DOUBLE_FREE, "block " + std::to_string(p) + " has no owner");
+  if (n > 0) {
+    void* dhost = host;
+    if (P.swap_engine == 0 && !(dhost = device_view_of_host(host)))
+      return fail(PKV_ERR_INVALID_ARG, "host tier is not device-accessible (use page-locked memory)");
+    std::vector<pkv::CopyItem> kit(n), vit(n);
+    for (int32_t j = 0; j < n; ++j) {
+      const int64_t frame = host_slots[j] * 2 * P.block_bytes;
+      kit[j] = {s->table[j] * P.block_bytes, frame};
+      vit[j] = {s->table[j] * P.block_bytes, frame + P.block_bytes};
+    }
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    int rc = P.swap_engine == 0 ? pkv::launch_copy_images(k_pool, dhost, kit.data(), n, P.block_bytes, st)
+                                : copy_engine(k_pool, dhost, kit.data(), n, P.block_bytes, st);
+    if (rc == PKV_OK)
+      rc = P.swap_engine == 0 ? pkv::launch_copy_images(v_pool, dhost, vit.data(), n, P.block_bytes, st)
+                              : copy_engine(v_pool, dhost, vit.data(), n, P.block_bytes, st);
+    if (rc != PKV_OK) return rc;
+  }
+  // remap: the frames now hold the blocks; the GPU blocks lose this owner
+  if (block_ids_out) std::copy(s->table.begin(), s->table.end(), block_ids_out);
+  s->host_frames.assign(host_slots, host_slots + n);
+  for (int32_t p : s->table) drop_owner(P, p);
+  s->table.clear();
+  s->swapped = true;
+  return PKV_OK;
+}
+
+int pkv_swap_in(pkv_pool* pool, int32_t seq, const void* host, int64_t host_frames, int32_t n, void* k_pool,
+                void* v_pool, int32_t* new_block_ids, pkv_stream_t stream) {
+  pkv::clear_error();
+  if (!pool || n < 0 || (n > 0 && (!k_pool || !v_pool || !host)))
+    return fail(PKV_ERR_INVALID_ARG, "bad arguments to pkv_swap_in");
+  Pool& P = *as_pool(pool);
+  SeqState* s = find_seq(P, seq);
+  if (!s) return unknown_seq(P, seq);
+  if (!s->swapped) return fail(PKV_ERR_INVALID_ARG, "sequence is not swapped out");
+  if (static_cast<int64_t>(s->host_frames.size()) != n)
+    return fail(PKV_ERR_INVALID_ARG, "n must equal the sequence's swapped block count (" +
+                                         std::to_string(s->host_frames.size()) + ")");
+  for (int64_t f : s->host_frames)
+    if (f >= host_frames) return fail(PKV_ERR_BAD_BLOCK_ID, "recorded host frame beyond host_frames");
+  if (P.free.size() < n)
+    return fail(PKV_ERR_OUT_OF_BLOCKS, "swap-in needs " + std::to_string(n) + " blocks, " +
+                                           std::to_string(P.free.size()) + " free");
+  if (n > 0) {
+    void* dhost = const_cast<void*>(host);
+    if (P.swap_engine == 0 && !(dhost = device_view_of_host(dhost)))
+      return fail(PKV_ERR_INVALID_ARG, "host tier is not device-accessible (use page-locked memory)");
+    std::vector<pkv::CopyItem> kit(n), vit(n);
+    for (int32_t j = 0; j < n; ++j) {
+      const int64_t frame = s->host_frames[j] * 2 * P.block_bytes;
+      const int64_t blk = P.free.front_at(j) * P.block_bytes;  // the blocks that will be popped
+      kit[j] = {frame, blk};
+      vit[j] = {frame + P.block_bytes, blk};
+    }
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    int rc = P.swap_engine == 0 ? pkv::launch_copy_images(dhost, k_pool, kit.data(), n, P.block_bytes, st)
+                                : copy_engine(dhost, k_pool, kit.data(), n, P.block_bytes, st);
+    if (rc == PKV_OK)
+      rc = P.swap_engine == 0 ? pkv::launch_copy_images(dhost, v_pool, vit.data(), n, P.block_bytes, st)
+                              : copy_engine(dhost, v_pool, vit.data(), n, P.block_bytes, st);
+    if (rc != PKV_OK) return rc;
+  }
+  for (int32_t j = 0; j < n; ++j) {
+    const int32_t p = P.free.pop_front();
+    P.ref[p] = 1;
+    s->table.push_back(p);
+    if (new_block_ids) new_block_ids[j] = p;
+  }
+  s->host_frames.clear();
+  s->swapped = false;
+  return PKV_OK;
+}
+
+int pkv_seq_host_slots(const pkv_pool* pool, int32_t seq, int64_t* out, int32_t capacity, int32_t* n) {
+  pkv::clear_error();
+  if (!pool || !n || capacity < 0) return fail(PKV_ERR_INVALID_ARG, "bad arguments");
+  const Pool& P = *as_pool(pool);
+  const SeqState* s = find_seq(P, seq);
+  if (!s) return unknown_seq(P, seq);
+  if (!s->swapped) return fail(PKV_ERR_INVALID_ARG, "sequence is not swapped out");
+  *n = static_cast<int32_t>(s->host_frames.size());
+  if (out)
+    for (int32_t j = 0; j < *n && j < capacity; ++j) out[j] = s->host_frames[j];
+  return PKV_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,900 @@
+// Paged decode attention for one layer of a ragged batch.
+//
+// What it computes ("KV Cache Management", cs249r vol. 3 ch. 5, "The PagedAttention
+// virtual memory model"; "PagedAttention", programmer.ie ch. 14, "It is the same
+// function"): for sequence s and query head h (KV head g = floor(h / G)),
+//   out[s][h] = sum_{t < len_s} softmax_t(scale * q[s][h] . K_s[t]) V_s[t],
+//   K_s[t] = k_pool[T_s[floor(t / B)]][layer][g][t mod B].
+// The kernel takes the block table and walks the sequence's logical blocks,
+// fetching each physical block where it lies.
+//
+// Tensor-core path (bf16/f16, d_head 64 or 128, G <= 8, B a multiple of 16):
+//   * Work unit = a 16-token tile of one (sequence, KV head) pair: the K and V
+//     slabs of 16 x d_head elements, contiguous in the pool.  All tiles of the
+//     batch are laid end to end (sequence-major, then KV head) and cut into equal
+//     contiguous ranges, one per warp of a persistent grid sized to the SM count
+//     (stream-K style), so every warp reads the same number of bytes whatever the
+//     length mix.
+//   * Each warp runs its own S-stage pipeline: lane 0 issues TMA tensor loads of
+//     the K and V tiles (128-byte swizzled boxes) and, at the first tile of a pair,
+//     a bulk copy of the G query rows, completing on a per-stage mbarrier.
+//   * One KV read serves all G query heads of the group: S^T = K q^T is one
+//     m16n8k16 mma per 16 columns of d_head (M = 16 tokens, N = 8 heads), and
+//     O^T += V^T P^T is one mma per 16 rows of d_head, with P^T moved from the
+//     accumulator layout into the operand layout by movmatrix.
+//   * Online softmax across tiles: running max m and normaliser l per head, the
+//     accumulator rescaled by exp(m_prev - m_new) ("Chunked prefill mechanics":
+//     m_new = max(m_prev, m_blk), l_new = l_prev e^{m_prev-m_new} + l_blk e^{m_blk-m_new},
+//     O_new likewise), in base 2 with log2(e) folded into the scale.
+//   * A pair fully inside one warp's range is normalised and written directly; a
+//     pair split across warps leaves (m, l, O) partials that a merge kernel
+//     combines with the same rule.
+// CUDA-core path (fp32, or other geometries): one CTA per (sequence, KV head),
+// warps stride over tokens with an online softmax per head, then merge in smem.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "pkv_device.cuh"
+#include "pkv_internal.h"
+
+namespace pkv {
+
+namespace {
+
+constexpr int TILE = 16;   // tokens per tile (the mma M dimension)
+constexpr int GPAD = 8;    // query heads per mma N dimension
+constexpr int kHdrBytes = 256;
+constexpr uint64_t kWaitNs = 2000000000ull;  // a tile load that takes 2 s is a fault: give up
+
+struct DecodeArgs {
+  const void* q;
+  void* out;
+  const int32_t* tables;
+  const int32_t* seq_lens;
+  int32_t* tile_prefix;  // [n_seq + 1]: tiles of sequences before s (per KV head)
+  int32_t* lens_c;       // [n_seq]: lengths clamped to [0, W*B]
+  int32_t* hdr;          // [0] = total tiles over all pairs
+  float* partials;
+  int* err;
+  int64_t num_blocks;
+  int32_t n_seq, W, H_q, H_kv, G, L, layer, B;
+  float scale_log2;  // scale * log2(e)
+  int32_t total_warps;
+};
+
+// --------------------------------------------------------------------------- plan
+
+// One CTA: clamp lengths, tiles per sequence, exclusive prefix, total tile count.
+__global__ void __launch_bounds__(1024) plan_kernel(const DecodeArgs a) {
+  __shared__ int32_t warp_sums[32];
+  const int tid = threadIdx.x;
+  const int per = (a.n_seq + blockDim.x - 1) / blockDim.x;
+  const int s0 = min(a.n_seq, tid * per), s1 = min(a.n_seq, s0 + per);
+  const int64_t maxlen = static_cast<int64_t>(a.W) * a.B;
+  int32_t local = 0;
+  for (int s = s0; s < s1; ++s) {
+    int32_t len = a.seq_lens[s];
+    if (len < 0 || len > maxlen) {
+      record_error(a.err, DERR_DECODE_LEN, s);
+      len = len < 0 ? 0 : static_cast<int32_t>(maxlen);
+    }
+    a.lens_c[s] = len;
+    local += (len + TILE - 1) / TILE;
+  }
+  // block-wide exclusive scan of `local`
+  const int lane = tid & 31, warp = tid >> 5;
+  int32_t incl = local;
+  for (int o = 1; o < 32; o <<= 1) {
+    int32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) warp_sums[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int32_t w = lane < (blockDim.x >> 5) ? warp_sums[lane] : 0;
+    for (int o = 1; o < 32; o <<= 1) {
+      int32_t v = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += v;
+    }
+    warp_sums[lane] = w;  // inclusive over warps
+  }
+  __syncthreads();
+  int32_t run = (warp > 0 ? warp_sums[warp - 1] : 0) + incl - local;
+  for (int s = s0; s < s1; ++s) {
+    a.tile_prefix[s] = run;
+    run += (a.lens_c[s] + TILE - 1) / TILE;
+  }
+  if (tid == blockDim.x - 1) {
+    a.tile_prefix[a.n_seq] = run;
+    a.hdr[0] = run * a.H_kv;
+  }
+}
+
+// --------------------------------------------------------------------------- tensor-core path
+
+template <int D>
+struct TcCfg {
+  static constexpr int KV_TILE_BYTES = TILE * D * 2;      // one 16 x D tile of K (or V)
+  static constexpr int Q_BYTES = GPAD * D * 2;             // up to 8 query rows
+  static constexpr int STAGE_BYTES = 2 * KV_TILE_BYTES + Q_BYTES;
+  static constexpr int NBOX = D / 64;                      // 128-byte TMA boxes per tile row
+  static constexpr int NKC = D / 16;                       // 16-wide chunks of d_head
+  static constexpr int PSTRIDE = NKC * 32 * 4 + 2 * GPAD;  // floats per partial slot
+  static_assert(STAGE_BYTES % 1024 == 0, "stages must keep 1024-byte alignment for the swizzle");
+};
+
+template <int D, int S, int NW>
+struct TcSmem {
+  static constexpr int WARP_BYTES = S * TcCfg<D>::STAGE_BYTES + 64 * 16 + S * 8 + 8;
+  static constexpr int WARP_STRIDE = (WARP_BYTES + 1023) / 1024 * 1024;
+  static constexpr int TOTAL = NW * WARP_STRIDE + 1024;  // + alignment slack
+};
+
+template <typename T>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  if constexpr (std::is_same<T, __nv_bfloat16>::value) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+  } else {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+  }
+}
+
+template <typename T>
+__device__ __forceinline__ T from_float(float x);
+template <>
+__device__ __forceinline__ __nv_bfloat16 from_float<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
+template <>
+__device__ __forceinline__ __half from_float<__half>(float x) { return __float2half_rn(x); }
+
+// Descriptor of one tile, built by the warp a batch at a time:
+//   x = TMA row coordinate of the slab, y = pair id (s * H_kv + g),
+//   z = valid tokens | first-of-pair << 8 | last-of-pair << 9 | new-pair-in-range << 10.
+constexpr int F_FIRST = 1 << 8, F_LAST = 1 << 9, F_NEWPAIR = 1 << 10;
+
+template <typename T, int D, int S, int NW>
+__global__ void __launch_bounds__(NW * 32) decode_tc_kernel(const __grid_constant__ CUtensorMap tmk,
+                                                            const __grid_constant__ CUtensorMap tmv,
+                                                            const DecodeArgs a) {
+  using C = TcCfg<D>;
+  using SM = TcSmem<D, S, NW>;
+  constexpr bool BF16 = std::is_same<T, __nv_bfloat16>::value;
+  extern __shared__ uint8_t smem_raw[];
+
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int gw = blockIdx.x * NW + warp;
+  const int total = a.hdr[0];
+  const int R = (total + a.total_warps - 1) / a.total_warps;
+  const int my_start = gw * R;
+  const int my_end = min(total, my_start + R);
+  if (my_start >= my_end) return;  // the whole warp leaves; no block-level barriers are used
+  const int n_my = my_end - my_start;
+
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* region = base + warp * SM::WARP_STRIDE;
+  int4* desc = reinterpret_cast<int4*>(region + S * C::STAGE_BYTES);
+  const uint32_t bar0 = smem_u32(region + S * C::STAGE_BYTES + 64 * 16);
+  const uint32_t stage0 = smem_u32(region);
+
+  if (lane == 0) {
+    for (int st = 0; st < S; ++st) mbar_init(bar0 + 8 * st, 1);
+    fence_barrier_init();
+  }
+  __syncwarp();
+
+  // ---- tile walk state: (sequence, KV head, tile within pair, tiles of the pair)
+  const int32_t* Q = a.tile_prefix;
+  int cs, ch, cj, cn;
+  {
+    // sequence containing tile my_start: largest s with H_kv * Q[s] <= my_start
+    int lo = 0, hi = a.n_seq - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (a.H_kv * Q[mid] <= my_start) lo = mid; else hi = mid - 1;
+    }
+    cs = lo;  // non-empty: H_kv * Q[lo] <= my_start < H_kv * Q[lo + 1]
+    cn = Q[cs + 1] - Q[cs];
+    const int within = my_start - a.H_kv * Q[cs];
+    ch = within / cn;
+    cj = within - ch * cn;
+  }
+
+  // Fill descriptors for range tiles [t0, t0 + 32) into ring slots (t & 63).
+  auto fill = [&](int t0) {
+    int ss = cs, hh = ch, jj = cj + lane, nn = cn;
+    while (jj >= nn && ss < a.n_seq) {
+      jj -= nn;
+      if (++hh == a.H_kv) {
+        hh = 0;
+        ++ss;
+        nn = ss < a.n_seq ? Q[ss + 1] - Q[ss] : 0;
+      }
+    }
+    const int t = t0 + lane;
+    if (t < n_my) {
+      const int tok0 = jj * TILE;
+      const int lb = tok0 / a.B;
+      const int sub = tok0 - lb * a.B;
+      int blk = a.tables[static_cast<int64_t>(ss) * a.W + lb];
+      if (blk < 0 || blk >= a.num_blocks) {
+        record_error(a.err, DERR_DECODE_BLOCK, blk);
+        blk = 0;
+      }
+      const int valid = min(TILE, a.lens_c[ss] - tok0);
+      int flags = valid;
+      if (jj == 0) flags |= F_FIRST;
+      if (jj == nn - 1) flags |= F_LAST;
+      if (jj == 0 || t == 0) flags |= F_NEWPAIR;
+      const int row = ((blk * a.L + a.layer) * a.H_kv + hh) * a.B + sub;
+      desc[t & 63] = make_int4(row, ss * a.H_kv + hh, flags, 0);
+    }
+    // carry = position of tile t0 + 32 (one past lane 31's tile)
+    int ns = __shfl_sync(0xffffffffu, ss, 31), nh = __shfl_sync(0xffffffffu, hh, 31);
+    int nj = __shfl_sync(0xffffffffu, jj, 31) + 1, nnn = __shfl_sync(0xffffffffu, nn, 31);
+    while (nj >= nnn && ns < a.n_seq) {
+      nj -= nnn;
+      if (++nh == a.H_kv) {
+        nh = 0;
+        ++ns;
+        nnn = ns < a.n_seq ? Q[ns + 1] - Q[ns] : 0;
+      }
+    }
+    cs = ns; ch = nh; cj = nj; cn = nnn;
+    __syncwarp();
+  };
+
+  auto issue = [&](int t) {  // lane 0 only
+    const int4 d = desc[t & 63];
+    const int st = t % S;
+    const uint32_t bar = bar0 + 8 * st;
+    const uint32_t sk = stage0 + st * C::STAGE_BYTES;
+    const uint32_t sv = sk + C::KV_TILE_BYTES;
+    const bool newpair = d.z & F_NEWPAIR;
+    fence_proxy_async();
+    mbar_arrive_expect_tx(bar, 2 * C::KV_TILE_BYTES + (newpair ? a.G * D * 2 : 0));
+#pragma unroll
+    for (int b = 0; b < C::NBOX; ++b) {
+      tma_load_2d(sk + b * (TILE * 128), &tmk, b * 64, d.x, bar);
+      tma_load_2d(sv + b * (TILE * 128), &tmv, b * 64, d.x, bar);
+    }
+    if (newpair) {
+      const int s = d.y / a.H_kv, g = d.y - (d.y / a.H_kv) * a.H_kv;
+      const T* qsrc = static_cast<const T*>(a.q) + (static_cast<int64_t>(s) * a.H_q + g * a.G) * D;
+      bulk_load(sk + 2 * C::KV_TILE_BYTES, qsrc, a.G * D * 2, bar);
+    }
+  };
+
+  fill(0);
+  if (n_my > 32) fill(32);
+  if (lane == 0)
+    for (int t = 0; t < S && t < n_my; ++t) issue(t);
+
+  // per-lane ldmatrix geometry (128-byte swizzle: chunk c of row r sits at c ^ (r & 7))
+  const int r8 = lane & 7, mi = lane >> 3;
+  const int k_row = r8 + 8 * (mi & 1), k_add = mi >> 1;  // QK: A = K tile (t x d)
+  const int v_row = r8 + 8 * (mi >> 1), v_add = mi & 1;  // PV: A = V^T via .trans
+  const int h0 = 2 * (lane & 3);                         // heads of this lane's columns
+  const int trow = lane >> 2;                            // token row of c0/c1 (c2/c3: +8)
+
+  float o[C::NKC][4];
+  uint32_t qf[C::NKC][2];
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+  int cur_pair = -1;
+  bool cur_started = false, cur_first_in_range = false;
+
+  for (int i = 0; i < n_my; ++i) {
+    if (i >= 32 && (i & 31) == 0 && i + 32 < n_my) fill(i + 32);
+    const int4 d = desc[i & 63];
+    const int st = i % S;
+    const uint32_t sk = stage0 + st * C::STAGE_BYTES;
+    const uint32_t sv = sk + C::KV_TILE_BYTES;
+    if (!mbar_wait_bounded(bar0 + 8 * st, (i / S) & 1, kWaitNs)) {
+      if (lane == 0) record_error(a.err, DERR_DECODE_TIMEOUT, i);
+      // drain the other stages' loads (bounded) before leaving
+      for (int k = 1; k < S && i + k < n_my; ++k)
+        mbar_wait_bounded(bar0 + 8 * ((i + k) % S), ((i + k) / S) & 1, kWaitNs);
+      return;
+    }
+
+    if (d.z & F_NEWPAIR) {
+      cur_pair = d.y;
+      cur_started = d.z & F_FIRST;
+      cur_first_in_range = (i == 0);
+      m0 = m1 = -INFINITY;
+      l0 = l1 = 0.f;
+#pragma unroll
+      for (int c = 0; c < C::NKC; ++c) o[c][0] = o[c][1] = o[c][2] = o[c][3] = 0.f;
+      const uint8_t* qs = region + st * C::STAGE_BYTES + 2 * C::KV_TILE_BYTES;
+      const bool live = trow < a.G;
+#pragma unroll
+      for (int c = 0; c < C::NKC; ++c) {
+        const uint32_t* p = reinterpret_cast<const uint32_t*>(qs + trow * D * 2 + (16 * c + h0) * 2);
+        qf[c][0] = live ? p[0] : 0u;
+        qf[c][1] = live ? p[4] : 0u;
+      }
+    }
+
+    // ---- S^T = K q^T  (16 tokens x 8 heads), two accumulation chains
+    float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int c = 0; c < C::NKC; ++c) {
+      const int chunk = 2 * (c & 3) + k_add;
+      const uint32_t addr = sk + (c >> 2) * (TILE * 128) + k_row * 128 + ((chunk ^ r8) << 4);
+      uint32_t a0, a1, a2, a3;
+      ldmatrix_x4(addr, a0, a1, a2, a3);
+      if (c & 1) mma_16816<BF16>(sb, a0, a1, a2, a3, qf[c][0], qf[c][1]);
+      else mma_16816<BF16>(sa, a0, a1, a2, a3, qf[c][0], qf[c][1]);
+    }
+    float s0 = (sa[0] + sb[0]) * a.scale_log2, s1 = (sa[1] + sb[1]) * a.scale_log2;
+    float s2 = (sa[2] + sb[2]) * a.scale_log2, s3 = (sa[3] + sb[3]) * a.scale_log2;
+    const int valid = d.z & 0xff;
+    if (valid < TILE) {
+      if (trow >= valid) s0 = s1 = -INFINITY;
+      if (trow + 8 >= valid) s2 = s3 = -INFINITY;
+      // zero the V rows past the end so that 0 * (stale value) cannot make NaN
+      uint8_t* vrows = region + st * C::STAGE_BYTES + C::KV_TILE_BYTES;
+      for (int k = lane; k < (TILE - valid) * 8 * C::NBOX; k += 32) {
+        const int b = k / ((TILE - valid) * 8);
+        const int rem = k - b * (TILE - valid) * 8;
+        const int r = valid + rem / 8, c16 = rem & 7;
+        *reinterpret_cast<int4*>(vrows + b * (TILE * 128) + r * 128 + c16 * 16) = make_int4(0, 0, 0, 0);
+      }
+      __syncwarp();
+    }
+
+    // ---- online softmax over this tile (per head: columns h0, h0 + 1)
+    float x0 = fmaxf(s0, s2), x1 = fmaxf(s1, s3);
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      x0 = fmaxf(x0, __shfl_xor_sync(0xffffffffu, x0, off));
+      x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, off));
+    }
+    const float n0 = fmaxf(m0, x0), n1 = fmaxf(m1, x1);
+    const float c0 = exp2f(m0 - n0), c1 = exp2f(m1 - n1);
+    m0 = n0;
+    m1 = n1;
+    const float p0 = exp2f(s0 - n0), p2 = exp2f(s2 - n0);
+    const float p1 = exp2f(s1 - n1), p3 = exp2f(s3 - n1);
+    l0 = l0 * c0 + (p0 + p2);
+    l1 = l1 * c1 + (p1 + p3);
+#pragma unroll
+    for (int c = 0; c < C::NKC; ++c) {
+      o[c][0] *= c0;
+      o[c][1] *= c1;
+      o[c][2] *= c0;
+      o[c][3] *= c1;
+    }
+    // P^T (16 tokens x 8 heads) from the accumulator layout into the B-operand layout
+    const uint32_t pb0 = movmatrix_trans(pack2<T>(p0, p1));
+    const uint32_t pb1 = movmatrix_trans(pack2<T>(p2, p3));
+
+    // ---- O^T += V^T P^T  (d_head x 8 heads)
+#pragma unroll
+    for (int c = 0; c < C::NKC; ++c) {
+      const int chunk = 2 * (c & 3) + v_add;
+      const uint32_t addr = sv + (c >> 2) * (TILE * 128) + v_row * 128 + ((chunk ^ r8) << 4);
+      uint32_t a0, a1, a2, a3;
+      ldmatrix_x4_trans(addr, a0, a1, a2, a3);
+      mma_16816<BF16>(o[c], a0, a1, a2, a3, pb0, pb1);
+    }
+
+    __syncwarp();  // every lane is done with this stage
+    if (lane == 0 && i + S < n_my) issue(i + S);
+
+    // ---- end of this pair within the range: write the result or a partial
+    if ((d.z & F_LAST) || i == n_my - 1) {
+      float L0 = l0, L1 = l1;
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        L0 += __shfl_xor_sync(0xffffffffu, L0, off);
+        L1 += __shfl_xor_sync(0xffffffffu, L1, off);
+      }
+      const int s = cur_pair / a.H_kv, g = cur_pair - (cur_pair / a.H_kv) * a.H_kv;
+      if (cur_started && (d.z & F_LAST)) {
+        const float i0 = 1.f / L0, i1 = 1.f / L1;
+        T* out = static_cast<T*>(a.out) + (static_cast<int64_t>(s) * a.H_q + g * a.G) * D;
+#pragma unroll
+        for (int c = 0; c < C::NKC; ++c) {
+          const int dd = 16 * c + trow;
+          if (h0 < a.G) {
+            out[h0 * D + dd] = from_float<T>(o[c][0] * i0);
+            out[h0 * D + dd + 8] = from_float<T>(o[c][2] * i0);
+          }
+          if (h0 + 1 < a.G) {
+            out[(h0 + 1) * D + dd] = from_float<T>(o[c][1] * i1);
+            out[(h0 + 1) * D + dd + 8] = from_float<T>(o[c][3] * i1);
+          }
+        }
+      } else {
+        const int slot = cur_first_in_range ? 0 : 1;
+        float* ps = a.partials + static_cast<int64_t>(gw * 2 + slot) * C::PSTRIDE;
+#pragma unroll
+        for (int c = 0; c < C::NKC; ++c)
+          reinterpret_cast<float4*>(ps)[c * 32 + lane] = make_float4(o[c][0], o[c][1], o[c][2], o[c][3]);
+        if (lane < 4) {
+          ps[C::NKC * 128 + h0] = m0;
+          ps[C::NKC * 128 + h0 + 1] = m1;
+          ps[C::NKC * 128 + GPAD + h0] = L0;
+          ps[C::NKC * 128 + GPAD + h0 + 1] = L1;
+        }
+      }
+    }
+  }
+}
+
+// Merge the partials of pairs split across warps; zero the outputs of empty sequences.
+template <typename T, int D>
+__global__ void __launch_bounds__(D * 2) merge_tc_kernel(const DecodeArgs a) {
+  using C = TcCfg<D>;
+  const int pair = blockIdx.x;
+  const int s = pair / a.H_kv, g = pair - (pair / a.H_kv) * a.H_kv;
+  const int nt = a.tile_prefix[s + 1] - a.tile_prefix[s];
+  T* out = static_cast<T*>(a.out) + (static_cast<int64_t>(s) * a.H_q + g * a.G) * D;
+  if (nt == 0) {
+    for (int k = threadIdx.x; k < a.G * D; k += blockDim.x) out[k] = from_float<T>(0.f);
+    return;
+  }
+  const int total = a.hdr[0];
+  const int R = (total + a.total_warps - 1) / a.total_warps;
+  const int ps = a.H_kv * a.tile_prefix[s] + g * nt, pe = ps + nt;
+  const int wa = ps / R, wb = (pe - 1) / R;
+  if (wa == wb) return;  // written whole by one warp
+  const int f = threadIdx.x;   // float4 index: chunk c = f / 32, lane = f % 32
+  const int lane = f & 31, c = f >> 5;
+  const int h0 = 2 * (lane & 3);
+  float M0 = -INFINITY, M1 = -INFINITY;
+  for (int w = wa; w <= wb; ++w) {
+    const int slot = (w == wa && ps != wa * R) ? 1 : 0;
+    const float* p = a.partials + static_cast<int64_t>(w * 2 + slot) * C::PSTRIDE + C::NKC * 128;
+    M0 = fmaxf(M0, p[h0]);
+    M1 = fmaxf(M1, p[h0 + 1]);
+  }
+  float L0 = 0.f, L1 = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int w = wa; w <= wb; ++w) {
+    const int slot = (w == wa && ps != wa * R) ? 1 : 0;
+    const float* p = a.partials + static_cast<int64_t>(w * 2 + slot) * C::PSTRIDE;
+    const float e0 = exp2f(p[C::NKC * 128 + h0] - M0), e1 = exp2f(p[C::NKC * 128 + h0 + 1] - M1);
+    L0 += p[C::NKC * 128 + GPAD + h0] * e0;
+    L1 += p[C::NKC * 128 + GPAD + h0 + 1] * e1;
+    const float4 v = reinterpret_cast<const float4*>(p)[f];
+    acc.x += v.x * e0;
+    acc.y += v.y * e1;
+    acc.z += v.z * e0;
+    acc.w += v.w * e1;
+  }
+  const int dd = 16 * c + (lane >> 2);
+  if (h0 < a.G) {
+    out[h0 * D + dd] = from_float<T>(acc.x / L0);
+    out[h0 * D + dd + 8] = from_float<T>(acc.z / L0);
+  }
+  if (h0 + 1 < a.G) {
+    out[(h0 + 1) * D + dd] = from_float<T>(acc.y / L1);
+    out[(h0 + 1) * D + dd + 8] = from_float<T>(acc.w / L1);
+  }
+}
+
+// --------------------------------------------------------------------------- CUDA-core path
+
+template <typename T>
+__device__ __forceinline__ float to_f(T x);
+template <>
+__device__ __forceinline__ float to_f<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ float to_f<__half>(__half x) { return __half2float(x); }
+template <>
+__device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+template <typename T>
+__device__ __forceinline__ T f_to(float x);
+template <>
+__device__ __forceinline__ float f_to<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ __half f_to<__half>(float x) { return __float2half_rn(x); }
+template <>
+__device__ __forceinline__ __nv_bfloat16 f_to<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
+
+constexpr int SIMT_WARPS = 4;
+
+// One CTA per (sequence, KV head).  Lane j holds elements j, j+32, ... of the head
+// vector; warp w takes tokens w, w+4, ...; each token's score is a warp reduction.
+template <typename T, int NPL>
+__global__ void __launch_bounds__(SIMT_WARPS * 32) decode_simt_kernel(const DecodeArgs a, const T* __restrict__ kp,
+                                                                        const T* __restrict__ vp, int d) {
+  const int pair = blockIdx.x;
+  const int s = pair / a.H_kv, g = pair - (pair / a.H_kv) * a.H_kv;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int G = a.G;
+  int len = a.seq_lens[s];
+  const int64_t maxlen = static_cast<int64_t>(a.W) * a.B;
+  if (len < 0 || len > maxlen) {
+    if (threadIdx.x == 0 && g == 0) record_error(a.err, DERR_DECODE_LEN, s);
+    len = len < 0 ? 0 : static_cast<int>(maxlen);
+  }
+  const T* q = static_cast<const T*>(a.q) + (static_cast<int64_t>(s) * a.H_q + g * G) * d;
+  float qv[GPAD][NPL], o[GPAD][NPL], m[GPAD], l[GPAD];
+#pragma unroll
+  for (int h = 0; h < GPAD; ++h) {
+    m[h] = -INFINITY;
+    l[h] = 0.f;
+#pragma unroll
+    for (int j = 0; j < NPL; ++j) {
+      const int e = lane + 32 * j;
+      qv[h][j] = (h < G && e < d) ? to_f(q[h * d + e]) : 0.f;
+      o[h][j] = 0.f;
+    }
+  }
+  for (int t = warp; t < len; t += SIMT_WARPS) {
+    int blk = a.tables[static_cast<int64_t>(s) * a.W + t / a.B];
+    if (blk < 0 || blk >= a.num_blocks) {
+      if (lane == 0) record_error(a.err, DERR_DECODE_BLOCK, blk);
+      continue;
+    }
+    const int64_t base = (((static_cast<int64_t>(blk) * a.L + a.layer) * a.H_kv + g) * a.B + t % a.B) * d;
+    float k[NPL], v[NPL];
+#pragma unroll
+    for (int j = 0; j < NPL; ++j) {
+      const int e = lane + 32 * j;
+      k[j] = e < d ? to_f(kp[base + e]) : 0.f;
+      v[j] = e < d ? to_f(vp[base + e]) : 0.f;
+    }
+#pragma unroll
+    for (int h = 0; h < GPAD; ++h) {
+      if (h >= G) break;
+      float dot = 0.f;
+#pragma unroll
+      for (int j = 0; j < NPL; ++j) dot = fmaf(qv[h][j], k[j], dot);
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
+      const float sc = dot * a.scale_log2;
+      const float mn = fmaxf(m[h], sc);
+      const float corr = exp2f(m[h] - mn), p = exp2f(sc - mn);
+      l[h] = l[h] * corr + p;
+#pragma unroll
+      for (int j = 0; j < NPL; ++j) o[h][j] = fmaf(p, v[j], o[h][j] * corr);
+      m[h] = mn;
+    }
+  }
+  // merge the warps: smem [warp][head] (m, l) and [warp][head][d]
+  extern __shared__ float sm[];
+  float* sml = sm;                                 // SIMT_WARPS * GPAD * 2
+  float* so = sm + SIMT_WARPS * GPAD * 2;          // SIMT_WARPS * GPAD * d
+  for (int h = 0; h < G; ++h) {
+    if (lane == 0) {
+      sml[(warp * GPAD + h) * 2] = m[h];
+      sml[(warp * GPAD + h) * 2 + 1] = l[h];
+    }
+#pragma unroll
+    for (int j = 0; j < NPL; ++j) {
+      const int e = lane + 32 * j;
+      if (e < d) so[(warp * GPAD + h) * d + e] = o[h][j];
+    }
+  }
+  __syncthreads();
+  T* out = static_cast<T*>(a.out) + (static_cast<int64_t>(s) * a.H_q + g * G) * d;
+  for (int k = threadIdx.x; k < G * d; k += blockDim.x) {
+    const int h = k / d, e = k - h * d;
+    float M = -INFINITY;
+    for (int w = 0; w < SIMT_WARPS; ++w) M = fmaxf(M, sml[(w * GPAD + h) * 2]);
+    float L = 0.f, acc = 0.f;
+    if (M != -INFINITY) {
+      for (int w = 0; w < SIMT_WARPS; ++w) {
+        const float mw = sml[(w * GPAD + h) * 2];
+        if (mw == -INFINITY) continue;
+        const float e2 = exp2f(mw - M);
+        L += sml[(w * GPAD + h) * 2 + 1] * e2;
+        acc += so[(w * GPAD + h) * d + e] * e2;
+      }
+    }
+    out[h * d + e] = f_to<T>(L > 0.f ? acc / L : 0.f);
+  }
+}
+
+// --------------------------------------------------------------------------- host side
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    cudaGetLastError();
+  }
+  return fn;
+}
+
+struct TcVariant {
+  int stages, warps;
+};
+
+// Pipeline depth and warps per CTA; PKV_TC_VARIANT selects another for tuning.
+TcVariant tc_variant() {
+  static const TcVariant table[] = {{2, 4}, {3, 4}, {4, 4}, {2, 8}, {3, 2}};
+  int idx = 0;
+  if (const char* e = std::getenv("PKV_TC_VARIANT")) idx = std::max(0, std::min(4, std::atoi(e)));
+  return table[idx];
+}
+
+bool tc_eligible(const Pool& P) {
+  const auto& g = P.geo;
+  const int G = g.H_q / g.H_kv;
+  const int64_t rows = g.num_blocks * g.L * g.H_kv * g.block_size;
+  return (g.dtype == PKV_BF16 || g.dtype == PKV_F16) && (g.d_head == 64 || g.d_head == 128) && G <= GPAD &&
+         g.block_size % TILE == 0 && rows < (int64_t(1) << 31) && encode_fn() != nullptr;
+}
+
+int device_sm_count(int* n) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(n, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return fail(PKV_ERR_CUDA, std::string("device query: ") + cudaGetErrorString(e));
+  return PKV_OK;
+}
+
+template <typename T, int D, int S, int NW>
+const void* tc_kernel_ptr() {
+  return reinterpret_cast<const void*>(&decode_tc_kernel<T, D, S, NW>);
+}
+
+using KernelPtr = const void*;
+
+template <typename T, int D>
+KernelPtr pick_tc(const TcVariant& v, int* smem) {
+#define PKV_TC_CASE(S_, NW_)                           \
+  if (v.stages == S_ && v.warps == NW_) {              \
+    *smem = TcSmem<D, S_, NW_>::TOTAL;                 \
+    return tc_kernel_ptr<T, D, S_, NW_>();             \
+  }
+  PKV_TC_CASE(2, 4)
+  PKV_TC_CASE(3, 4)
+  PKV_TC_CASE(4, 4)
+  PKV_TC_CASE(2, 8)
+  PKV_TC_CASE(3, 2)
+#undef PKV_TC_CASE
+  *smem = TcSmem<D, 2, 4>::TOTAL;
+  return tc_kernel_ptr<T, D, 2, 4>();
+}
+
+KernelPtr tc_kernel_for(const Pool& P, int* smem) {
+  const TcVariant v = tc_variant();
+  const bool bf = P.geo.dtype == PKV_BF16;
+  if (P.geo.d_head == 128) return bf ? pick_tc<__nv_bfloat16, 128>(v, smem) : pick_tc<__half, 128>(v, smem);
+  return bf ? pick_tc<__nv_bfloat16, 64>(v, smem) : pick_tc<__half, 64>(v, smem);
+}
+
+// Persistent grid for the tensor-core kernel: resident CTAs per SM x SM count.
+int tc_grid(const Pool& P, int* grid, int* warps, int* smem) {
+  KernelPtr k = tc_kernel_for(P, smem);
+  int dev = 0;
+  cudaGetDevice(&dev);
+  struct Known {
+    int dev;
+    KernelPtr k;
+    int grid;
+  };
+  static std::mutex mu;
+  static std::vector<Known> known;
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    for (const auto& kn : known)
+      if (kn.dev == dev && kn.k == k) {
+        *grid = kn.grid;
+        *warps = tc_variant().warps;
+        return PKV_OK;
+      }
+  }
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, *smem);
+  if (e != cudaSuccess) return fail(PKV_ERR_CUDA, std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e));
+  int per_sm = 0;
+  const int nw = tc_variant().warps;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, nw * 32, *smem);
+  if (e != cudaSuccess || per_sm < 1)
+    return fail(PKV_ERR_CUDA, std::string("occupancy query: ") + cudaGetErrorString(e));
+  int sms = 0;
+  if (int rc = device_sm_count(&sms)) return rc;
+  *grid = per_sm * sms;
+  *warps = nw;
+  std::lock_guard<std::mutex> lk(mu);
+  known.push_back({dev, k, *grid});
+  return PKV_OK;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct WsLayout {
+  size_t prefix, lens, partials, total;
+};
+
+WsLayout ws_layout(int n_seq, int64_t total_warps, int D) {
+  WsLayout w;
+  w.prefix = kHdrBytes;
+  w.lens = w.prefix + align256(sizeof(int32_t) * (n_seq + 1));
+  w.partials = w.lens + align256(sizeof(int32_t) * n_seq);
+  const int pstride = (D / 16) * 32 * 4 + 2 * GPAD;
+  w.total = w.partials + align256(sizeof(float) * total_warps * 2 * pstride);
+  return w;
+}
+
+}  // namespace
+
+struct TensorMaps {
+  struct Entry {
+    int device;
+    const void* k;
+    const void* v;
+    CUtensorMap tk, tv;
+  };
+  std::vector<Entry> entries;  // most recent last, at most 8
+};
+
+void destroy_tensor_maps(Pool& P) {
+  delete P.tmaps;
+  P.tmaps = nullptr;
+}
+
+static int get_tensor_maps(Pool& P, const void* k, const void* v, CUtensorMap* tk, CUtensorMap* tv) {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  std::lock_guard<std::mutex> lk(P.tmap_mu);
+  if (!P.tmaps) P.tmaps = new TensorMaps();
+  auto& es = P.tmaps->entries;
+  for (auto& e : es)
+    if (e.device == dev && e.k == k && e.v == v) {
+      *tk = e.tk;
+      *tv = e.tv;
+      return PKV_OK;
+    }
+  const auto& g = P.geo;
+  if ((reinterpret_cast<uintptr_t>(k) & 15) || (reinterpret_cast<uintptr_t>(v) & 15))
+    return fail(PKV_ERR_INVALID_ARG, "k_pool and v_pool must be 16-byte aligned");
+  TensorMaps::Entry ent;
+  ent.device = dev;
+  ent.k = k;
+  ent.v = v;
+  const CUtensorMapDataType dt = g.dtype == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(g.d_head),
+                        static_cast<cuuint64_t>(g.num_blocks) * g.L * g.H_kv * g.block_size};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(g.d_head) * 2};
+  cuuint32_t box[2] = {64, TILE};
+  cuuint32_t estr[2] = {1, 1};
+  auto fn = encode_fn();
+  for (int which = 0; which < 2; ++which) {
+    CUresult r = fn(which ? &ent.tv : &ent.tk, dt, 2, const_cast<void*>(which ? v : k), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled failed: " + std::to_string(r));
+  }
+  if (es.size() >= 8) es.erase(es.begin());
+  es.push_back(ent);
+  *tk = ent.tk;
+  *tv = ent.tv;
+  return PKV_OK;
+}
+
+int decode_workspace_bytes(const Pool& P, int32_t n_seq, size_t* bytes) {
+  int64_t warps_total = 0;
+  if (tc_eligible(P)) {
+    int grid = 0, nw = 0, smem = 0;
+    if (int rc = tc_grid(P, &grid, &nw, &smem)) return rc;
+    warps_total = static_cast<int64_t>(grid) * nw;
+  }
+  *bytes = ws_layout(n_seq, warps_total, P.geo.d_head).total;
+  return PKV_OK;
+}
+
+int launch_decode(Pool& P, int32_t layer, const void* q, const void* k_pool, const void* v_pool,
+                  const int32_t* tables, int32_t W, const int32_t* seq_lens, int32_t n_seq, float scale, void* out,
+                  void* ws, size_t ws_bytes, void* stream) {
+  const auto& g = P.geo;
+  const int G = g.H_q / g.H_kv;
+  if (G > GPAD) return fail(PKV_ERR_UNSUPPORTED, "more than 8 query heads per KV head");
+  if (reinterpret_cast<uintptr_t>(ws) & 255) return fail(PKV_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  if (static_cast<int64_t>(n_seq) * g.H_kv * ((static_cast<int64_t>(W) * g.block_size + TILE - 1) / TILE) >=
+      (int64_t(1) << 31))
+    return fail(PKV_ERR_INVALID_ARG, "batch too large (tile count must stay below 2^31)");
+  void* err = nullptr;
+  if (int rc = device_error_word(&err)) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+  DecodeArgs a{};
+  a.q = q;
+  a.out = out;
+  a.tables = tables;
+  a.seq_lens = seq_lens;
+  a.err = static_cast<int*>(err);
+  a.num_blocks = g.num_blocks;
+  a.n_seq = n_seq;
+  a.W = W;
+  a.H_q = g.H_q;
+  a.H_kv = g.H_kv;
+  a.G = G;
+  a.L = g.L;
+  a.layer = layer;
+  a.B = g.block_size;
+  a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+
+  if (tc_eligible(P)) {
+    int grid = 0, nw = 0, smem = 0;
+    if (int rc = tc_grid(P, &grid, &nw, &smem)) return rc;
+    const WsLayout L = ws_layout(n_seq, static_cast<int64_t>(grid) * nw, g.d_head);
+    if (ws_bytes < L.total) return fail(PKV_ERR_INVALID_ARG, "workspace too small: need " + std::to_string(L.total));
+    if ((reinterpret_cast<uintptr_t>(q) & 15)) return fail(PKV_ERR_INVALID_ARG, "q must be 16-byte aligned");
+    CUtensorMap tk, tv;
+    if (int rc = get_tensor_maps(P, k_pool, v_pool, &tk, &tv)) return rc;
+    char* w = static_cast<char*>(ws);
+    a.hdr = reinterpret_cast<int32_t*>(w);
+    a.tile_prefix = reinterpret_cast<int32_t*>(w + L.prefix);
+    a.lens_c = reinterpret_cast<int32_t*>(w + L.lens);
+    a.partials = reinterpret_cast<float*>(w + L.partials);
+    a.total_warps = grid * nw;
+    plan_kernel<<<1, 1024, 0, st>>>(a);
+    KernelPtr k = tc_kernel_for(P, &smem);
+    void* args[] = {&tk, &tv, &a};
+    cudaError_t e = cudaLaunchKernel(k, dim3(grid), dim3(nw * 32), args, static_cast<size_t>(smem), st);
+    if (e != cudaSuccess) return fail(PKV_ERR_CUDA, std::string("decode launch: ") + cudaGetErrorString(e));
+    const bool bf = g.dtype == PKV_BF16;
+    const int pairs = n_seq * g.H_kv;
+    if (g.d_head == 128) {
+      if (bf) merge_tc_kernel<__nv_bfloat16, 128><<<pairs, 256, 0, st>>>(a);
+      else merge_tc_kernel<__half, 128><<<pairs, 256, 0, st>>>(a);
+    } else {
+      if (bf) merge_tc_kernel<__nv_bfloat16, 64><<<pairs, 128, 0, st>>>(a);
+      else merge_tc_kernel<__half, 64><<<pairs, 128, 0, st>>>(a);
+    }
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(PKV_ERR_CUDA, std::string("decode launch: ") + cudaGetErrorString(e));
+    return PKV_OK;
+  }
+
+  // CUDA-core path
+  const int d = g.d_head;
+  const int npl = (d + 31) / 32;
+  const size_t smem = sizeof(float) * (SIMT_WARPS * GPAD * 2 + SIMT_WARPS * GPAD * d);
+  const int pairs = n_seq * g.H_kv;
+  cudaError_t e = cudaSuccess;
+#define PKV_SIMT(TYPE, NPL)                                                                          \
+  {                                                                                                  \
+    auto kern = decode_simt_kernel<TYPE, NPL>;                                                       \
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)); \
+    kern<<<pairs, SIMT_WARPS * 32, smem, st>>>(a, static_cast<const TYPE*>(k_pool),                  \
+                                               static_cast<const TYPE*>(v_pool), d);                 \
+  }
+#define PKV_SIMT_T(TYPE)                         \
+  switch (npl) {                                 \
+    case 1: PKV_SIMT(TYPE, 1) break;             \
+    case 2: PKV_SIMT(TYPE, 2) break;             \
+    case 3: case 4: PKV_SIMT(TYPE, 4) break;     \
+    default: PKV_SIMT(TYPE, 8) break;            \
+  }
+  if (g.dtype == PKV_F32) {
+    PKV_SIMT_T(float)
+  } else if (g.dtype == PKV_F16) {
+    PKV_SIMT_T(__half)
+  } else {
+    PKV_SIMT_T(__nv_bfloat16)
+  }
+#undef PKV_SIMT_T
+#undef PKV_SIMT
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(PKV_ERR_CUDA, std::string("decode launch: ") + cudaGetErrorString(e));
+  return PKV_OK;
+}
+
+}  // namespace pkv

@@ -1,0 +1,98 @@
+// Internal declarations shared by the library's translation units.
+#pragma once
+
+#include <cstdint>
+#include <mutex>
+#include <string>
+#include <unordered_map>
+#include <vector>
+
+#include "../../include/pkv.h"
+
+namespace pkv {
+
+// ------------------------------------------------------------------ errors
+
+// Set the thread-local message and return the status (for `return fail(...)`).
+int fail(int status, const std::string& msg);
+void clear_error();
+
+// ------------------------------------------------------------------ control plane
+
+// FIFO of free block ids kept in a fixed ring of capacity num_blocks
+// ("free-list ring buffer", KV Cache Management, PagedAttention model).
+class FreeRing {
+ public:
+  void reset(const std::vector<int32_t>& order);
+  int64_t size() const { return count_; }
+  int32_t front_at(int64_t i) const { return ring_[(head_ + i) % cap_]; }
+  int32_t pop_front();
+  void push_back(int32_t p);
+
+ private:
+  std::vector<int32_t> ring_;
+  int64_t cap_ = 0, head_ = 0, count_ = 0;
+};
+
+struct SeqState {
+  std::vector<int32_t> table;       // logical block -> physical block
+  int64_t len = 0;                  // tokens written
+  bool swapped = false;             // blocks live in host frames
+  std::vector<int64_t> host_frames; // frames holding the blocks while swapped
+};
+
+struct TensorMaps;  // cached TMA descriptors (defined in pkv_decode.cu)
+
+struct Pool {
+  pkv_geometry geo{};
+  int64_t slab_elems = 0;   // B * d: one (block, layer, head) slab
+  int64_t block_elems = 0;  // L * H_kv * B * d: one block of K (or V), all layers
+  int64_t block_bytes = 0;  // block_elems * element size
+  FreeRing free;
+  std::vector<int32_t> ref;
+  std::unordered_map<int32_t, SeqState> seqs;
+  std::vector<uint8_t> released;  // by seq id: 1 once freed
+  int32_t next_id = 0;
+  int32_t swap_engine = 0;  // 0 SM kernel, 1 copy engine
+
+  std::mutex tmap_mu;
+  TensorMaps* tmaps = nullptr;
+};
+
+inline int64_t elem_size(int32_t dtype) { return dtype == PKV_F32 ? 4 : 2; }
+
+// ------------------------------------------------------------------ device side
+
+// Address of the current device's error word: int32 code, int32 pad, int64 detail.
+int device_error_word(void** out);
+
+// Kernel launchers (return PKV_OK or a failure with the message set).
+struct CopyItem {
+  int64_t src_off;  // byte offsets
+  int64_t dst_off;
+};
+
+int launch_append(const Pool& P, int32_t layer, const void* k_new, const void* v_new, const int32_t* slots,
+                  int32_t n_tok, void* k_pool, void* v_pool, void* stream);
+
+// Copy `n` contiguous images of `bytes` bytes each, image i from src_base +
+// items[i].src_off to dst_base + items[i].dst_off (device-accessible pointers).
+int launch_copy_images(const void* src_base, void* dst_base, const CopyItem* items, int64_t n, int64_t bytes,
+                       void* stream);
+
+int decode_workspace_bytes(const Pool& P, int32_t n_seq, size_t* bytes);
+int launch_decode(Pool& P, int32_t layer, const void* q, const void* k_pool, const void* v_pool,
+                  const int32_t* tables, int32_t W, const int32_t* seq_lens, int32_t n_seq, float scale, void* out,
+                  void* ws, size_t ws_bytes, void* stream);
+void destroy_tensor_maps(Pool& P);
+
+// Device error codes recorded by kernels (the `code` of pkv_check_device_error).
+enum DeviceErr : int32_t {
+  DERR_NONE = 0,
+  DERR_APPEND_SLOT = 1,     // slot out of range in append
+  DERR_DECODE_LEN = 2,      // seq_len < 0 or > W * B
+  DERR_DECODE_BLOCK = 3,    // block id out of range in a table
+  DERR_DECODE_TIMEOUT = 4,  // a bounded mbarrier wait gave up
+};
+
+}  // namespace pkv
