@@ -1,0 +1,770 @@
+#!/usr/bin/env python3
+"""Benchmark of the paged KV cache hot path on one GB300 (or N replicas).
+
+One step = one pass of the hot path over the batch: plan the step's appends on
+the host control plane (slots, copy-on-write pairs, block tables), copy the
+control-plane output to the device, copy shared blocks (CoW), write the new
+tokens' K/V at their slots, run paged decode attention over len + 1 tokens, and
+release finished sequences.  Workloads (synthetic, seeded):
+
+  agent32k (default): 48 sequences x 32,768 tokens, 70B GQA layer (64 query /
+      8 KV heads, d_head 128, bf16, 16-token blocks), block ids a seeded random
+      permutation of the pool; 6.4 GB of K/V read per step.
+  chat:     256 sequences, lognormal prompt (mean 217) + generated (mean 154)
+      lengths clipped to 1,024, 32,768-block pool in a shuffled order; a step is
+      one decode step of the 64-step schedule (finished sequences are released).
+  forked:   a 16,376-token prefix forked into 64 branches with U[0, 2048] suffixes
+      (first append of each branch copies the shared tail block).
+  swap:     80-layer 70B geometry (5 MiB blocks); a step evicts 512 chunks of 16
+      blocks to a pinned host tier and restores all of them into new blocks.
+  tiny:     GPT-2-small geometry, fp32, 8 sequences.
+
+Prints one JSON line.  `--impl reference` times the CPU oracle instead (on a
+bounded sample of the same workload, on the host cores).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "paged decode attention KV GB/s & tokens/s (% of 8 TB/s HBM); swap GB/s vs host link"
+NOMINAL_HBM_GBS = 8000.0
+
+
+# ------------------------------------------------------------------ environment
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples taken while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.file, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.file.flush()
+        rows = []
+        with open(self.file.name) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.file.name)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+# ------------------------------------------------------------------ our arm: workloads
+
+
+class Staging:
+    """Ring of pinned host / device buffers for the control plane's per-step output
+    (slot mapping, block tables, lengths), copied to the device in one transfer."""
+
+    def __init__(self, torch, dev, n_ints: int, depth: int = 4):
+        self.torch = torch
+        self.host = [torch.empty(n_ints, dtype=torch.int32, pin_memory=True) for _ in range(depth)]
+        self.dev = [torch.empty(n_ints, dtype=torch.int32, device=dev) for _ in range(depth)]
+        self.events = [None] * depth
+        self.i = 0
+
+    def next(self):
+        k = self.i % len(self.host)
+        self.i += 1
+        if self.events[k] is not None:
+            self.events[k].synchronize()
+        return k, self.host[k].numpy(), self.host[k], self.dev[k]
+
+    def upload(self, k, n_ints: int):
+        self.dev[k][:n_ints].copy_(self.host[k][:n_ints], non_blocking=True)
+        ev = self.torch.cuda.Event()
+        ev.record()
+        self.events[k] = ev
+        return n_ints * 4
+
+
+class DecodeRunner:
+    """Decode steps over a paged batch: plan -> CoW copy -> append -> attend -> release."""
+
+    name = "decode"
+
+    def __init__(self, torch, pkv, dev, total_steps: int):
+        self.torch, self.pkv, self.dev = torch, pkv, dev
+        self.total_steps = total_steps
+        self.decode_ms = []  # per timed step (CUDA events around the attention call)
+        self.kv_bytes = []
+        self.alg_bytes = []
+        self.tokens = []
+        self.h2d_meta = 0
+        self.e2e_in_bytes = 0
+        self.e2e_out_bytes = 0
+
+    # subclasses set: g, pool, ids (live batch in order), kp, vp, Wd, scale,
+    # q/kn/vn device tensors [steps][n_max][...], and implement running(t)
+
+    def _alloc_common(self, n_max: int):
+        torch, g = self.torch, self.g
+        td = {"bf16": torch.bfloat16, "f16": torch.float16, "f32": torch.float32}[g.dtype]
+        self.td = td
+        self.out = torch.empty((n_max, g.H_q, g.d_head), dtype=td, device=self.dev)
+        self.ws = torch.empty(self.pkv.pkv_decode_workspace_size(self.pool, n_max), dtype=torch.uint8,
+                              device=self.dev)
+        self.staging = Staging(torch, self.dev, n_max * (self.Wd + 2))
+        self.ones = np.ones(n_max, np.int32)
+
+    def step(self, t: int, timed: bool = False, host_inputs=None):
+        torch, pkv, g = self.torch, self.pkv, self.g
+        ids = self.running(t)
+        n = len(ids)
+        if n == 0:
+            return
+        self.last_ids = ids
+        slots, cows = pkv.pkv_plan_append(self.pool, ids, self.ones[:n])
+        k, hnp, _, dmeta = self.staging.next()
+        hnp[:n] = slots
+        tables = hnp[n:n + n * self.Wd].reshape(n, self.Wd)
+        lens = hnp[n + n * self.Wd:n + n * self.Wd + n]
+        pkv.pkv_export_tables(self.pool, ids, self.Wd, tables=tables, seq_lens=lens)
+        nbytes = self.staging.upload(k, n * (self.Wd + 2))
+        if len(cows):
+            pkv.pkv_copy_blocks(self.pool, cows, self.kp, self.vp)
+        if host_inputs is not None:
+            q, kn, vn = self.q_e2e[:n], self.kn_e2e[:n], self.vn_e2e[:n]
+            q.copy_(host_inputs[0][t][:n], non_blocking=True)
+            kn.copy_(host_inputs[1][t][:n], non_blocking=True)
+            vn.copy_(host_inputs[2][t][:n], non_blocking=True)
+        else:
+            q, kn, vn = self.q[t][:n], self.kn[t][:n], self.vn[t][:n]
+        d_slots = dmeta[:n]
+        d_tables = dmeta[n:n + n * self.Wd].view(n, self.Wd)
+        d_lens = dmeta[n + n * self.Wd:n + n * self.Wd + n]
+        pkv.pkv_append_kv(self.pool, 0, kn, vn, d_slots, self.kp, self.vp)
+        if timed:
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record()
+        pkv.pkv_decode_attention(self.pool, 0, q, self.kp, self.vp, d_tables, d_lens, self.scale, self.out[:n],
+                                 self.ws)
+        if timed:
+            e1.record()
+            self.decode_ms.append((e0, e1))
+            tok = int(lens.astype(np.int64).sum())
+            kvb = tok * g.H_kv * g.d_head * g.elem_bytes * 2
+            self.kv_bytes.append(kvb)
+            qo = 2 * n * g.H_q * g.d_head * g.elem_bytes
+            self.alg_bytes.append(kvb + qo + n * self.Wd * 4 + n * 4)
+            self.tokens.append(n)
+            self.h2d_meta += nbytes
+        if host_inputs is not None:
+            self.out_host[:n].copy_(self.out[:n], non_blocking=True)
+            torch.cuda.current_stream().synchronize()  # the step's result is read on the host
+            self.e2e_in_bytes += nbytes + (q.numel() + kn.numel() + vn.numel()) * g.elem_bytes
+            self.e2e_out_bytes += n * g.H_q * g.d_head * g.elem_bytes
+        self.after_step(t, ids)
+
+    def after_step(self, t, ids):
+        pass
+
+    def prepare_e2e(self):
+        torch, g = self.torch, self.g
+        n = self.n_max
+        sh_q = (self.total_steps, n, g.H_q, g.d_head)
+        sh_k = (self.total_steps, n, g.H_kv, g.d_head)
+        # host copies of the step inputs, in pinned memory
+        host = []
+        for src in (self.q, self.kn, self.vn):
+            h = torch.empty(src.shape, dtype=src.dtype, pin_memory=True)
+            h.copy_(src)
+            host.append(h)
+        self.q_e2e = torch.empty(sh_q[1:], dtype=self.td, device=self.dev)
+        self.kn_e2e = torch.empty(sh_k[1:], dtype=self.td, device=self.dev)
+        self.vn_e2e = torch.empty(sh_k[1:], dtype=self.td, device=self.dev)
+        self.out_host = torch.empty(self.out.shape, dtype=self.td, pin_memory=True)
+        return host
+
+    def inputs_for_steps(self, tag):
+        torch, g = self.torch, self.g
+        n = self.n_max
+        self.q = W.device_normal(self.seed, f"{tag}_q", (self.total_steps, n, g.H_q, g.d_head), g.dtype, self.dev)
+        self.kn = W.device_normal(self.seed, f"{tag}_k", (self.total_steps, n, g.H_kv, g.d_head), g.dtype, self.dev)
+        self.vn = W.device_normal(self.seed, f"{tag}_v", (self.total_steps, n, g.H_kv, g.d_head), g.dtype, self.dev)
+
+
+class AgentRunner(DecodeRunner):
+    name = "agent32k"
+
+    def __init__(self, torch, pkv, dev, total_steps, n_seq=48, context=32768):
+        super().__init__(torch, pkv, dev, total_steps)
+        wl = W.agent(n_seq, context, spare_steps=total_steps + 16)
+        self.wl, self.g, self.seed = wl, wl.geometry, wl.seed
+        g = self.g
+        self.n_max = n_seq
+        self.scale = wl.scale
+        self.pool = pkv.pkv_pool_create(g.L, g.H_q, g.H_kv, g.d_head, g.block_size, g.dtype, g.num_blocks,
+                                        wl.free_order)
+        self.ids = [pkv.pkv_seq_create(self.pool) for _ in range(n_seq)]
+        pkv.pkv_plan_append(self.pool, self.ids, [context] * n_seq)
+        # the pool's contents are the prompt keys/values: N(0,1) drawn on the device
+        self.kp = W.device_normal(self.seed, "k_pool", g.pool_shape(), g.dtype, dev)
+        self.vp = W.device_normal(self.seed, "v_pool", g.pool_shape(), g.dtype, dev)
+        self.Wd = -(-(context + total_steps + 1) // g.block_size)
+        self.inputs_for_steps("agent")
+        self._alloc_common(n_seq)
+        self.config = {"workload": f"agent{context // 1024}k: {n_seq} sequences x {context} tokens, 64 query / "
+                                   f"8 KV heads, d_head 128, bf16, 16-token blocks, permuted block ids",
+                       "n_seq": n_seq, "context": context, "H_q": g.H_q, "H_kv": g.H_kv, "d_head": g.d_head,
+                       "block_size": g.block_size, "pool_blocks": g.num_blocks,
+                       "l2": f"inputs larger than L2 ({n_seq * context * 4096 / 1e9:.2f} GB of K/V per step)",
+                       "parallelism": "replicas (no collectives)"}
+
+    def running(self, t):
+        return self.ids
+
+
+class ChatRunner(DecodeRunner):
+    name = "chat"
+
+    def __init__(self, torch, pkv, dev, total_steps, n_seq=256):
+        super().__init__(torch, pkv, dev, total_steps)
+        wl = W.chat(n_seq=n_seq)
+        self.wl, self.g, self.seed = wl, wl.geometry, wl.seed
+        g = self.g
+        self.n_max = n_seq
+        self.scale = wl.scale
+        self.sched_steps = wl.extra["steps"]
+        self.gen = wl.extra["generated"]
+        self.prompt = wl.lengths
+        self.kp = W.device_normal(self.seed, "k_pool", g.pool_shape(), g.dtype, dev)
+        self.vp = W.device_normal(self.seed, "v_pool", g.pool_shape(), g.dtype, dev)
+        self.Wd = -(-1024 // g.block_size) + 1
+        # one control-plane state per pass of the 64-step schedule, made up front
+        n_pass = -(-total_steps // self.sched_steps) + 1
+        self.states = [self._fresh_state() for _ in range(n_pass)]
+        self.pool = self.states[0][0]
+        self.inputs_for_steps("chat")
+        self._alloc_common(n_seq)
+        self.config = {"workload": "chat: 256 sequences, lognormal prompt (mean 217) + generated (mean 154) "
+                                   "lengths <= 1024, 64 query / 8 KV heads, d_head 128, bf16, 16-token blocks, "
+                                   "32,768-block pool in shuffled order, 64-step schedule",
+                       "n_seq": n_seq, "H_q": g.H_q, "H_kv": g.H_kv, "d_head": g.d_head,
+                       "block_size": g.block_size, "pool_blocks": g.num_blocks,
+                       "l2": "inputs larger than L2 (0.2-0.3 GB of K/V per step)",
+                       "parallelism": "replicas (no collectives)"}
+
+    def _fresh_state(self):
+        g, pkv = self.g, self.pkv
+        pool = pkv.pkv_pool_create(g.L, g.H_q, g.H_kv, g.d_head, g.block_size, g.dtype, g.num_blocks,
+                                   self.wl.free_order)
+        ids = [pkv.pkv_seq_create(pool) for _ in range(self.n_max if hasattr(self, "n_max") else 256)]
+        pkv.pkv_plan_append(pool, ids, self.prompt)
+        return (pool, ids)
+
+    def running(self, t):
+        k = t % self.sched_steps
+        self.pool, ids = self.states[t // self.sched_steps]
+        return [s for s in ids if self.gen[s] > k]
+
+    def after_step(self, t, ids):
+        k = t % self.sched_steps
+        for s in ids:
+            if self.gen[s] == k + 1:  # generated budget reached: release
+                self.pkv.pkv_seq_free(self.pool, s)
+
+
+class ForkedRunner(DecodeRunner):
+    name = "forked"
+
+    def __init__(self, torch, pkv, dev, total_steps, n_branch=64):
+        super().__init__(torch, pkv, dev, total_steps)
+        wl = W.forked(n_branch=n_branch)
+        self.wl, self.g, self.seed = wl, wl.geometry, wl.seed
+        g = self.g
+        self.n_max = n_branch
+        self.scale = wl.scale
+        self.pool = pkv.pkv_pool_create(g.L, g.H_q, g.H_kv, g.d_head, g.block_size, g.dtype, g.num_blocks,
+                                        wl.free_order)
+        self.kp = W.device_normal(self.seed, "k_pool", g.pool_shape(), g.dtype, dev)
+        self.vp = W.device_normal(self.seed, "v_pool", g.pool_shape(), g.dtype, dev)
+        parent = pkv.pkv_seq_create(self.pool)
+        pkv.pkv_plan_append(self.pool, [parent], [int(wl.lengths[0])])
+        self.ids = [pkv.pkv_seq_fork(self.pool, parent) for _ in range(n_branch)]
+        suffix = [int(x) for x in wl.extra["suffix"]]
+        slots, cows = pkv.pkv_plan_append(self.pool, self.ids, suffix)
+        pkv.pkv_copy_blocks(self.pool, cows, self.kp, self.vp)
+        if len(slots):
+            kn = W.device_normal(self.seed, "suffix_k", (len(slots), g.H_kv, g.d_head), g.dtype, dev)
+            vn = W.device_normal(self.seed, "suffix_v", (len(slots), g.H_kv, g.d_head), g.dtype, dev)
+            pkv.pkv_append_kv(self.pool, 0, kn, vn, torch.from_numpy(slots).to(dev), self.kp, self.vp)
+        self.unique_tokens = int(wl.lengths[0]) + sum(suffix)
+        self.Wd = -(-(int(wl.lengths[0]) + 2048 + total_steps + 1) // g.block_size)
+        self.inputs_for_steps("forked")
+        self._alloc_common(n_branch)
+        self.config = {"workload": "forked: 16,376-token prefix forked into 64 branches (refcount 65) with "
+                                   "U[0,2048] suffixes, 64 query / 8 KV heads, d_head 128, bf16, 16-token blocks",
+                       "n_seq": n_branch, "prefix": int(wl.lengths[0]), "H_q": g.H_q, "H_kv": g.H_kv,
+                       "d_head": g.d_head, "block_size": g.block_size,
+                       "l2": "logical K/V per step 4.5 GB > L2; the 67 MB shared prefix is re-read by every branch",
+                       "parallelism": "replicas (no collectives)"}
+
+    def running(self, t):
+        return self.ids
+
+
+class TinyRunner(DecodeRunner):
+    name = "tiny"
+
+    def __init__(self, torch, pkv, dev, total_steps):
+        super().__init__(torch, pkv, dev, total_steps)
+        wl = W.tiny()
+        self.wl, self.g, self.seed = wl, wl.geometry, wl.seed
+        g = self.g
+        self.n_max = len(wl.lengths)
+        self.scale = wl.scale
+        self.pool = pkv.pkv_pool_create(g.L, g.H_q, g.H_kv, g.d_head, g.block_size, g.dtype, g.num_blocks,
+                                        wl.free_order)
+        self.ids = [pkv.pkv_seq_create(self.pool) for _ in range(self.n_max)]
+        pkv.pkv_plan_append(self.pool, self.ids, wl.lengths)
+        self.kp = W.device_normal(self.seed, "k_pool", g.pool_shape(), g.dtype, dev)
+        self.vp = W.device_normal(self.seed, "v_pool", g.pool_shape(), g.dtype, dev)
+        self.Wd = -(-(512 + total_steps + 1) // g.block_size)
+        self.inputs_for_steps("tiny")
+        self._alloc_common(self.n_max)
+        self.config = {"workload": "tiny: GPT-2-small geometry (12 heads, d_head 64, fp32), 8 sequences of "
+                                   "U[1,512] tokens, 512-block permuted pool",
+                       "n_seq": self.n_max, "l2": "inputs smaller than L2 (launch-bound case)",
+                       "parallelism": "replicas (no collectives)"}
+
+    def running(self, t):
+        return self.ids
+
+
+RUNNERS = {"agent32k": AgentRunner, "chat": ChatRunner, "forked": ForkedRunner, "tiny": TinyRunner}
+
+
+def run_decode(args, torch, pkv, dev, world, rank):
+    total = args.warmup + args.steps + 2 + args.steps  # timed region, then e2e warm-up + e2e steps
+    r = RUNNERS[args.workload](torch, pkv, dev, total)
+    g = r.g
+    launches0 = None
+    for t in range(args.warmup):
+        r.step(t)
+    torch.cuda.synchronize()
+    pkv.pkv_check_device_error()
+    barrier(world)
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    e_start = torch.cuda.Event(enable_timing=True)
+    e_end = torch.cuda.Event(enable_timing=True)
+    launches0 = pkv.pkv_launch_count()
+    e_start.record()
+    for t in range(args.warmup, args.warmup + args.steps):
+        r.step(t, timed=True)
+    e_end.record()
+    torch.cuda.synchronize()
+    launches = pkv.pkv_launch_count() - launches0
+    barrier(world)
+    clk = clocks.stop()
+    ms = e_start.elapsed_time(e_end)
+    ms_max = reduce_max(torch, world, ms)
+    pkv.pkv_check_device_error()
+    dec_ms = [a.elapsed_time(b) for a, b in r.decode_ms]
+    kv_total = sum(r.kv_bytes)
+    alg_avg = sum(r.alg_bytes) / len(r.alg_bytes)
+    dec_avg = sum(dec_ms) / len(dec_ms)
+
+    # end to end: inputs from pinned host memory each step, result read back each step
+    host = r.prepare_e2e()
+    t0 = args.warmup + args.steps
+    for t in range(t0, t0 + 2):
+        r.step(t, host_inputs=host)
+    r.e2e_in_bytes = r.e2e_out_bytes = 0
+    kv_before = len(r.kv_bytes)
+    barrier(world)
+    torch.cuda.synchronize()
+    h0 = time.perf_counter()
+    for t in range(t0 + 2, t0 + 2 + args.steps):
+        r.step(t, timed=True, host_inputs=host)
+    torch.cuda.synchronize()
+    e2e_s = reduce_max(torch, world, (time.perf_counter() - h0) * 1e3) / 1e3
+    e2e_kv = sum(r.kv_bytes[kv_before:])
+
+    peak, peak_kind = load_peaks()
+    value = world * kv_total / (ms_max / 1e3) / 1e9
+    achieved = alg_avg / (dec_avg / 1e3) / 1e9
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_max / args.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": g.dtype, "data": "synthetic", "config": r.config,
+        "tokens_per_s": round(world * sum(r.tokens[:args.steps]) / (ms_max / 1e3), 1),
+        "hbm_frac_of_8tbs": round(value / world / NOMINAL_HBM_GBS, 4),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": args.traffic,
+                     "kernel": "pkv_decode_attention (plan + stream-K attention + merge)",
+                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+                     else "fallback 6.8 TB/s",
+                     "alg_bytes_per_launch": int(alg_avg), "avg_launch_ms": round(dec_avg, 4)},
+        "e2e": {"value": round(world * e2e_kv / e2e_s / 1e9, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": int(r.e2e_in_bytes / args.steps),
+                "d2h_bytes_per_step": int(r.e2e_out_bytes / args.steps)},
+        "gpu_launches": int(launches),
+        "clocks": clk,
+    }
+    return line, r
+
+
+def run_swap(args, torch, pkv, dev, world, rank):
+    wl = W.swap()
+    g = wl.geometry
+    nchunk = len(wl.lengths)
+    cb = wl.extra["chunk_blocks"]
+    pool = pkv.pkv_pool_create(g.L, g.H_q, g.H_kv, g.d_head, g.block_size, g.dtype, g.num_blocks, wl.free_order)
+    if args.swap_engine:
+        pkv.pkv_pool_set_swap_engine(pool, 1)
+    ids = [pkv.pkv_seq_create(pool) for _ in range(nchunk)]
+    pkv.pkv_plan_append(pool, ids, wl.lengths)
+    kp = W.device_normal(wl.seed, "k_pool", g.pool_shape(), g.dtype, dev)
+    vp = W.device_normal(wl.seed, "v_pool", g.pool_shape(), g.dtype, dev)
+    frame = 2 * g.L * g.H_kv * g.block_size * g.d_head * g.elem_bytes
+    n_frames = nchunk * cb
+    host = torch.empty(n_frames * frame, dtype=torch.uint8, pin_memory=True)
+    order = [int(x) for x in wl.extra["evict_order"]]
+    frames_of = {s: np.arange(i * cb, (i + 1) * cb, dtype=np.int64) for i, s in enumerate(ids)}
+
+    # host-link roofline: one 1 GiB pinned copy each way on the copy engines
+    probe_d = torch.empty(1 << 30, dtype=torch.uint8, device=dev)
+    probe_h = torch.empty(1 << 30, dtype=torch.uint8, pin_memory=True)
+    link = {}
+    for name, (dst, src) in (("d2h", (probe_h, probe_d)), ("h2d", (probe_d, probe_h))):
+        for _ in range(2):
+            dst.copy_(src, non_blocking=True)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(3):
+            dst.copy_(src, non_blocking=True)
+        b.record()
+        torch.cuda.synchronize()
+        link[name] = 3 * (1 << 30) / (a.elapsed_time(b) / 1e3) / 1e9
+    del probe_d, probe_h
+
+    out_ms, in_ms = [], []
+
+    def one_step(timed):
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        e[0].record()
+        for s in order:
+            pkv.pkv_swap_out(pool, ids[s], kp, vp, host, n_frames, frames_of[ids[s]])
+        e[1].record()
+        for s in order[::-1]:
+            pkv.pkv_swap_in(pool, ids[s], host, n_frames, cb, kp, vp)
+        e[2].record()
+        if timed:
+            out_ms.append((e[0], e[1]))
+            in_ms.append((e[1], e[2]))
+
+    for _ in range(args.warmup):
+        one_step(False)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    l0 = pkv.pkv_launch_count()
+    es, ee = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    es.record()
+    for _ in range(args.steps):
+        one_step(True)
+    ee.record()
+    torch.cuda.synchronize()
+    launches = pkv.pkv_launch_count() - l0
+    clk = clocks.stop()
+    ms = reduce_max(torch, world, es.elapsed_time(ee))
+    pkv.pkv_check_device_error()
+    bytes_dir = nchunk * cb * frame
+    t_out = statistics.mean(a.elapsed_time(b) for a, b in out_ms) / 1e3
+    t_in = statistics.mean(a.elapsed_time(b) for a, b in in_ms) / 1e3
+    out_gbs, in_gbs = bytes_dir / t_out / 1e9, bytes_dir / t_in / 1e9
+    value = world * 2 * bytes_dir * args.steps / (ms / 1e3) / 1e9
+    peak = min(link["d2h"], link["h2d"])
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": g.dtype, "data": "synthetic",
+        "config": {"workload": "swap: 80-layer 70B GQA geometry (327,680 B/token), 512 chunks x 16 blocks "
+                               "(42.9 GB) evicted to pinned host memory and restored into new blocks",
+                   "engine": "copy engines" if args.swap_engine else "SM kernel",
+                   "l2": "inputs larger than L2 (43 GB per direction)", "parallelism": "replicas (no collectives)"},
+        "swap_out_gbs": round(out_gbs, 1), "swap_in_gbs": round(in_gbs, 1),
+        "host_link_gbs": {k: round(v, 1) for k, v in link.items()},
+        "roofline": {"bound": "host-link", "achieved": round(min(out_gbs, in_gbs), 1), "peak": round(peak, 1),
+                     "unit": "GB/s", "frac": round(min(out_gbs / link["d2h"], in_gbs / link["h2d"]), 4),
+                     "traffic": None, "kernel": "pkv_swap_out / pkv_swap_in",
+                     "peak_source": "measured in this run: 1 GiB pinned cudaMemcpyAsync per direction"},
+        "e2e": {"value": round(value, 2), "unit": "GB/s", "h2d_bytes_per_step": bytes_dir,
+                "d2h_bytes_per_step": bytes_dir},
+        "gpu_launches": int(launches), "clocks": clk,
+    }
+    return line, None
+
+
+# ------------------------------------------------------------------ CPU baseline (the oracle)
+
+
+def oracle_sample_decode(runner, n_sample: int, reps: int = 1):
+    """Time the oracle's attention on n_sample sequences of the runner's batch, on
+    host copies of exactly their blocks.  Returns (GB/s, seconds, description)."""
+    import torch
+    import oracle
+
+    g = runner.g
+    pool = runner.pool
+    ids = []
+    for s in runner.last_ids:  # sequences still resident after the last step
+        try:
+            runner.pkv.pkv_seq_len(pool, s)
+            ids.append(s)
+        except runner.pkv.PkvError:
+            pass
+    ids = ids[:n_sample]
+    Wd = runner.Wd
+    tables, lens = runner.pkv.pkv_export_tables(pool, ids, Wd)
+    used = sorted({int(b) for i in range(len(ids)) for b in tables[i, : -(-int(lens[i]) // g.block_size)]})
+    remap = {b: j for j, b in enumerate(used)}
+    idx = torch.tensor(used, dtype=torch.long, device=runner.kp.device)
+    store = {"bf16": np.uint16, "f16": np.float16, "f32": np.float32}[g.dtype]
+
+    def host_copy(t):
+        x = t.index_select(0, idx).cpu().contiguous()
+        if g.dtype == "bf16":
+            return x.view(torch.int16).numpy().view(np.uint16)
+        return x.numpy()
+
+    hk, hv = host_copy(runner.kp), host_copy(runner.vp)
+    gc = W.Geometry(g.L, g.H_q, g.H_kv, g.d_head, g.block_size, g.dtype, len(used))
+    ct = np.zeros_like(tables)
+    for i in range(len(ids)):
+        nb = -(-int(lens[i]) // g.block_size)
+        ct[i, :nb] = [remap[int(b)] for b in tables[i, :nb]]
+    q = W.normal(runner.seed, "oracle_q", (len(ids), g.H_q, g.d_head), g.dtype).astype(store)
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        oracle.decode_attention(gc, 0, q, hk, hv, ct, lens, runner.scale)
+    dt = (time.perf_counter() - t0) / reps
+    kvb = int(lens.astype(np.int64).sum()) * g.H_kv * g.d_head * g.elem_bytes * 2
+    return kvb / dt / 1e9, dt, f"oracle attention over {len(ids)} of the batch's sequences " \
+                               f"({int(lens.sum())} tokens), {oracle.hardware_threads()} threads"
+
+
+# ------------------------------------------------------------------ reference arm (the oracle alone)
+
+
+def reference_arm(args, world, rank):
+    import oracle
+
+    if rank != 0:
+        return None
+    cores = oracle.hardware_threads()
+    if args.workload == "swap":
+        wl = W.swap(n_chunks=16)
+        g = wl.geometry
+        nb = 64
+        gs = W.Geometry(g.L, g.H_q, g.H_kv, g.d_head, g.block_size, g.dtype, nb)
+        kp = W.normal(wl.seed, "k_pool", gs.pool_shape(), "bf16")
+        vp = W.normal(wl.seed, "v_pool", gs.pool_shape(), "bf16")
+        frame = 2 * g.L * g.H_kv * g.block_size * g.d_head * 2
+        host = np.zeros(nb * frame, np.uint8)
+        ids = np.arange(nb, dtype=np.int32)
+        slots = np.arange(nb, dtype=np.int64)[::-1].copy()
+        times = []
+        for step in range(args.warmup + args.steps):
+            t0 = time.perf_counter()
+            oracle.swap_out_data(gs, ids, slots, kp, vp, host)
+            oracle.swap_in_data(gs, ids, slots, host, kp, vp)
+            if step >= args.warmup:
+                times.append(time.perf_counter() - t0)
+        bytes_step = 2 * nb * frame
+        value = bytes_step / statistics.mean(times) / 1e9
+        desc = f"oracle memcpy swap-out + swap-in of {nb} 5 MiB blocks per step"
+        config = {"workload": "swap: 80-layer 70B GQA geometry, 5 MiB blocks (sampled)"}
+        dtype = "bf16"
+    else:
+        spec = {"agent32k": (lambda: W.agent(48, 32768, 256), 2),
+                "chat": (lambda: W.chat(), 64),
+                "forked": (lambda: W.forked(), 4),
+                "tiny": (lambda: W.tiny(), 8)}[args.workload]
+        wl, n_s = spec[0](), spec[1]
+        g = wl.geometry
+        lens = np.array([int(x) for x in wl.lengths[:n_s]], np.int32) if args.workload != "forked" else \
+            np.array([int(wl.lengths[0]) + int(s) for s in wl.extra["suffix"][:n_s]], np.int32)
+        if args.workload == "chat":
+            lens = np.array([int(wl.lengths[i]) + 1 for i in range(n_s)], np.int32)
+        nblk = [-(-int(x) // g.block_size) for x in lens]
+        gs = W.Geometry(g.L, g.H_q, g.H_kv, g.d_head, g.block_size, g.dtype, sum(nblk))
+        kp = W.normal(wl.seed, "ref_k", gs.pool_shape(), g.dtype)
+        vp = W.normal(wl.seed, "ref_v", gs.pool_shape(), g.dtype)
+        perm = W.permutation(wl.seed, "ref_perm", sum(nblk))
+        Wd = max(nblk)
+        tables = np.zeros((n_s, Wd), np.int32)
+        o = 0
+        for i, nb in enumerate(nblk):
+            tables[i, :nb] = perm[o:o + nb]
+            o += nb
+        q = W.normal(wl.seed, "ref_q", (n_s, g.H_q, g.d_head), g.dtype)
+        times = []
+        for step in range(args.warmup + args.steps):
+            t0 = time.perf_counter()
+            oracle.decode_attention(gs, 0, q, kp, vp, tables, lens, wl.scale)
+            if step >= args.warmup:
+                times.append(time.perf_counter() - t0)
+        bytes_step = int(lens.astype(np.int64).sum()) * g.H_kv * g.d_head * g.elem_bytes * 2
+        value = bytes_step / statistics.mean(times) / 1e9
+        desc = f"oracle attention over {n_s} sequences ({int(lens.sum())} tokens) of the {args.workload} workload"
+        config = {"workload": args.workload, "sampled_sequences": n_s}
+        dtype = g.dtype
+    t_step = statistics.mean(times)
+    return {
+        "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(t_step * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": dtype, "data": "synthetic", "config": config,
+        "impl": "reference",
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": desc},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+# ------------------------------------------------------------------ plumbing
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def reduce_max(torch, world, x: float) -> float:
+    if world <= 1:
+        return x
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=["agent32k", "chat", "forked", "swap", "tiny"], default="agent32k")
+    ap.add_argument("--swap-engine", type=int, default=0, help="swap workload: 0 SM kernel, 1 copy engines")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="ncu dram bytes per decode launch, if captured for this kernel version")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world, rank, local = dist_setup()
+
+    if args.impl == "reference":
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.init_process_group("gloo")
+        line = reference_arm(args, world, rank)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+
+    import torch
+
+    import paged_kv_cache_80_gb300 as pkv
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+    if args.workload == "swap":
+        line, runner = run_swap(args, torch, pkv, dev, world, rank)
+    else:
+        line, runner = run_decode(args, torch, pkv, dev, world, rank)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        if runner is not None:
+            n_sample = {"agent32k": 16, "chat": 256, "forked": 16, "tiny": 8}[args.workload]
+            v, dt, desc = oracle_sample_decode(runner, n_sample)
+            line["cpu_baseline"] = {"value": round(v, 4), "unit": "GB/s", "cores": __import__("oracle").hardware_threads(),
+                                    "kind": "oracle", "sample": desc + f", {dt:.2f} s"}
+        else:
+            ref = reference_arm(argparse.Namespace(workload="swap", steps=2, warmup=1), 1, 0)
+            line["cpu_baseline"] = dict(ref["cpu_baseline"])
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

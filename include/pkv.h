@@ -222,6 +222,9 @@ int pkv_seq_host_slots(const pkv_pool* pool, int32_t seq, int64_t* out, int32_t 
 /* 0 = swap with SM kernels (default), 1 = with cudaMemcpyAsync on the copy engines. */
 int pkv_pool_set_swap_engine(pkv_pool* pool, int32_t engine);
 
+/* Number of kernels this library has launched in this process (all devices). */
+uint64_t pkv_launch_count(void);
+
 /* Synchronize the stream, then read and clear the current device's error word.
  * Returns DEVICE_CHECK if a kernel recorded a bad index since the last check;
  * *code (kernel-specific, nonzero) and *detail (the offending value) describe it.

@@ -20,7 +20,7 @@ __all__ = [
     "pkv_version", "pkv_pool_create", "pkv_pool_destroy", "pkv_pool_geometry", "pkv_seq_create", "pkv_seq_fork",
     "pkv_seq_free", "pkv_seq_len", "pkv_plan_append", "pkv_export_tables", "pkv_refcounts", "pkv_free_list",
     "pkv_append_kv", "pkv_decode_workspace_size", "pkv_decode_attention", "pkv_copy_blocks", "pkv_swap_out",
-    "pkv_swap_in", "pkv_seq_host_slots", "pkv_pool_set_swap_engine", "pkv_check_device_error",
+    "pkv_swap_in", "pkv_seq_host_slots", "pkv_pool_set_swap_engine", "pkv_check_device_error", "pkv_launch_count",
 ]
 
 F32, F16, BF16 = 0, 1, 2
@@ -82,6 +82,7 @@ def _L():
             "pkv_seq_host_slots": ([vp, i32, P64, i32, P32], ctypes.c_int),
             "pkv_pool_set_swap_engine": ([vp, i32], ctypes.c_int),
             "pkv_check_device_error": ([vp, P32, P64], ctypes.c_int),
+            "pkv_launch_count": ([], ctypes.c_uint64),
         }
         for name, (args, res) in sig.items():
             f = getattr(L, name)
@@ -330,6 +331,10 @@ def pkv_swap_in(pool: PoolLike, seq: int, host, host_frames: int, n: int, k_pool
     _check(_L().pkv_swap_in(_h(pool), seq, _host_ptr(host, "host"), host_frames, n, _dev(k_pool, "k_pool"),
                             _dev(v_pool, "v_pool"), _p32(ids), _stream(stream)), "pkv_swap_in")
     return ids[:n]
+
+
+def pkv_launch_count() -> int:
+    return int(_L().pkv_launch_count())
 
 
 def pkv_check_device_error(stream=None):

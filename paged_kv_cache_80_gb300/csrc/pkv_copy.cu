@@ -12,12 +12,19 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstring>
 
 #include "pkv_device.cuh"
 #include "pkv_internal.h"
 
 namespace pkv {
+
+// ------------------------------------------------------------------ launch counter
+
+static std::atomic<uint64_t> g_launches{0};
+
+void count_launch(int n) { g_launches.fetch_add(static_cast<uint64_t>(n), std::memory_order_relaxed); }
 
 // ------------------------------------------------------------------ error word
 
@@ -150,6 +157,7 @@ int launch_append(const Pool& P, int32_t layer, const void* k_new, const void* v
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return fail(PKV_ERR_CUDA, std::string("append launch: ") + cudaGetErrorString(e));
+  count_launch();
   return PKV_OK;
 }
 
@@ -214,6 +222,7 @@ int launch_copy_images(const void* src_base, void* dst_base, const CopyItem* ite
     copy_images_kernel<<<grid, kCopyThreads, 0, s>>>(b);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return fail(PKV_ERR_CUDA, std::string("copy launch: ") + cudaGetErrorString(e));
+    count_launch();
   }
   return PKV_OK;
 }
@@ -221,6 +230,8 @@ int launch_copy_images(const void* src_base, void* dst_base, const CopyItem* ite
 }  // namespace pkv
 
 // ------------------------------------------------------------------ C ABI: device error check
+
+extern "C" uint64_t pkv_launch_count(void) { return pkv::g_launches.load(std::memory_order_relaxed); }
 
 extern "C" int pkv_check_device_error(pkv_stream_t stream, int32_t* code, int64_t* detail) {
   pkv::clear_error();

@@ -860,6 +860,7 @@ int launch_decode(Pool& P, int32_t layer, const void* q, const void* k_pool, con
     }
     e = cudaGetLastError();
     if (e != cudaSuccess) return fail(PKV_ERR_CUDA, std::string("decode launch: ") + cudaGetErrorString(e));
+    count_launch(3);
     return PKV_OK;
   }
 
@@ -894,6 +895,7 @@ int launch_decode(Pool& P, int32_t layer, const void* q, const void* k_pool, con
 #undef PKV_SIMT
   e = cudaGetLastError();
   if (e != cudaSuccess) return fail(PKV_ERR_CUDA, std::string("decode launch: ") + cudaGetErrorString(e));
+  count_launch();
   return PKV_OK;
 }
 

@@ -63,6 +63,9 @@ inline int64_t elem_size(int32_t dtype) { return dtype == PKV_F32 ? 4 : 2; }
 
 // ------------------------------------------------------------------ device side
 
+// Count one kernel launch (reported by pkv_launch_count).
+void count_launch(int n = 1);
+
 // Address of the current device's error word: int32 code, int32 pad, int64 detail.
 int device_error_word(void** out);
 
