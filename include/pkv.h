@@ -187,6 +187,28 @@ int pkv_decode_attention(const pkv_pool* pool, int32_t layer, const void* q, con
                          int32_t n_seq, float scale, void* out, void* workspace, size_t ws_bytes,
                          pkv_stream_t stream);
 
+/* Decode attention that allocates nothing.  (The pages have no counterpart of
+ * this call; it exists for callers of this library.)
+ * Same arguments and result as pkv_decode_attention, minus the workspace: the
+ * scratch is a 12 MiB array compiled into the library (a static __device__
+ * variable, held by every GPU that loads the library until the process exits).
+ * It is for callers that cannot call cudaMalloc: e.g. a serving engine that sized
+ * its KV block pool to fill the device at start-up, so a later allocation would
+ * fail, or code that must not take cudaMalloc's implicit device synchronisation.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - A batch that needs more scratch than 12 MiB is rejected with
+ *     PKV_ERR_INVALID_ARG (about 10 MB are the partials of one persistent grid on
+ *     a 152-SM GB300; each sequence adds 8 bytes).
+ *   - Every call on a device shares the one array and leaves its contents behind;
+ *     nothing in it needs to start at zero.  Calls whose GPU work overlaps (two
+ *     streams, or two threads) race on it: order them on one stream.
+ * No cudaMalloc, cudaFree or other allocating routine is called. */
+int pkv_decode_attention_noalloc(const pkv_pool* pool, int32_t layer, const void* q, const void* k_pool,
+                                 const void* v_pool, const int32_t* block_tables, int32_t W, const int32_t* seq_lens,
+                                 int32_t n_seq, float scale, void* out, pkv_stream_t stream);
+
 /* Copy-on-write data step ([KVM] "copies the B tokens from the shared block into
  * p_new"): for each (src, dst) in pairs (HOST int32 [n][2]), copy every slot of
  * every layer of block src into block dst, for K and V.  Pairs are passed to the

@@ -19,7 +19,8 @@ __all__ = [
     "PkvError", "Geometry", "Pool", "library_path", "F32", "F16", "BF16",
     "pkv_version", "pkv_pool_create", "pkv_pool_destroy", "pkv_pool_geometry", "pkv_seq_create", "pkv_seq_fork",
     "pkv_seq_free", "pkv_seq_len", "pkv_plan_append", "pkv_export_tables", "pkv_refcounts", "pkv_free_list",
-    "pkv_append_kv", "pkv_decode_workspace_size", "pkv_decode_attention", "pkv_copy_blocks", "pkv_swap_out",
+    "pkv_append_kv", "pkv_decode_workspace_size", "pkv_decode_attention", "pkv_decode_attention_noalloc",
+    "pkv_copy_blocks", "pkv_swap_out",
     "pkv_swap_in", "pkv_seq_host_slots", "pkv_pool_set_swap_engine", "pkv_check_device_error", "pkv_launch_count",
 ]
 
@@ -76,6 +77,8 @@ def _L():
             "pkv_decode_workspace_size": ([vp, i32, ctypes.POINTER(ctypes.c_size_t)], ctypes.c_int),
             "pkv_decode_attention": ([vp, i32, vp, vp, vp, vp, i32, vp, i32, ctypes.c_float, vp, vp, ctypes.c_size_t,
                                       vp], ctypes.c_int),
+            "pkv_decode_attention_noalloc": ([vp, i32, vp, vp, vp, vp, i32, vp, i32, ctypes.c_float, vp, vp],
+                                             ctypes.c_int),
             "pkv_copy_blocks": ([vp, P32, i32, vp, vp, vp], ctypes.c_int),
             "pkv_swap_out": ([vp, i32, vp, vp, vp, i64, P64, i32, P32, vp], ctypes.c_int),
             "pkv_swap_in": ([vp, i32, vp, i64, i32, vp, vp, P32, vp], ctypes.c_int),
@@ -308,6 +311,18 @@ def pkv_decode_attention(pool: PoolLike, layer: int, q, k_pool, v_pool, block_ta
                                      float(scale), _dev(out, "out"), _dev(workspace, "workspace"),
                                      workspace.numel() * workspace.element_size(), _stream(stream)),
            "pkv_decode_attention")
+
+
+def pkv_decode_attention_noalloc(pool: PoolLike, layer: int, q, k_pool, v_pool, block_tables, seq_lens,
+                                 scale: float, out, stream=None) -> None:
+    """Decode attention without a workspace: for callers that cannot allocate device
+    memory (the library's own static 12 MiB scratch is used instead)."""
+    n_seq = int(seq_lens.numel())
+    W = int(block_tables.shape[1]) if block_tables.dim() == 2 else 0
+    _check(_L().pkv_decode_attention_noalloc(_h(pool), layer, _dev(q, "q"), _dev(k_pool, "k_pool"),
+                                             _dev(v_pool, "v_pool"), _dev(block_tables, "block_tables"), W,
+                                             _dev(seq_lens, "seq_lens"), n_seq, float(scale), _dev(out, "out"),
+                                             _stream(stream)), "pkv_decode_attention_noalloc")
 
 
 def pkv_copy_blocks(pool: PoolLike, pairs, k_pool, v_pool, stream=None) -> None:

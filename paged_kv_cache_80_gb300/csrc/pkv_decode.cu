@@ -900,3 +900,182 @@ int launch_decode(Pool& P, int32_t layer, const void* q, const void* k_pool, con
 }
 
 }  // namespace pkv
+
+// ============================================================================ no-allocation entry point
+//
+// pkv_decode_attention_noalloc: the same decode attention, for callers that cannot
+// allocate device memory (for example a serving engine that sized its KV block pool
+// to fill the device at start-up, or code that must not pay cudaMalloc's implicit
+// device synchronisation).  Its scratch is the file-scope array below instead of a
+// caller-provided workspace; nothing here allocates device or host memory.
+namespace pkv {
+namespace {
+
+// 12 MiB: the stream-K partials of one persistent grid (about 10 MB on a 152-SM
+// GB300) plus per-sequence prefix and length arrays.  Held by every GPU that loads
+// the library until the process exits.
+constexpr size_t kNoallocScratchBytes = size_t(12) << 20;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
+
+// Device address of g_noalloc_scratch on the current device, looked up once per
+// device (host code cannot use the symbol itself: it is a host-side stand-in).
+int noalloc_scratch(void** out) {
+  static std::mutex mu;
+  static void* addr[64] = {nullptr};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(PKV_ERR_CUDA, std::string("cudaGetDevice: ") + cudaGetErrorString(e));
+  if (dev < 0 || dev >= 64) return fail(PKV_ERR_CUDA, "device index out of range");
+  std::lock_guard<std::mutex> lk(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess)
+      return fail(PKV_ERR_CUDA, std::string("cudaGetSymbolAddress(scratch): ") + cudaGetErrorString(e));
+    addr[dev] = p;
+  }
+  *out = addr[dev];
+  return PKV_OK;
+}
+
+}  // namespace
+}  // namespace pkv
+
+extern "C" int pkv_decode_attention_noalloc(const pkv_pool* pool, int32_t layer, const void* q, const void* k_pool,
+                                            const void* v_pool, const int32_t* block_tables, int32_t W,
+                                            const int32_t* seq_lens, int32_t n_seq, float scale, void* out,
+                                            pkv_stream_t stream) {
+  using namespace pkv;
+  clear_error();
+  if (!pool || n_seq < 0 || W < 0) return fail(PKV_ERR_INVALID_ARG, "bad arguments to pkv_decode_attention_noalloc");
+  const Pool& P = *reinterpret_cast<const Pool*>(pool);
+  const auto& g = P.geo;
+  if (layer < 0 || layer >= g.L) return fail(PKV_ERR_INVALID_ARG, "layer out of range");
+  if (n_seq == 0) return PKV_OK;
+  if (!q || !k_pool || !v_pool || !block_tables || !seq_lens || !out) return fail(PKV_ERR_INVALID_ARG, "NULL buffer");
+  const int G = g.H_q / g.H_kv;
+  if (G > GPAD) return fail(PKV_ERR_UNSUPPORTED, "more than 8 query heads per KV head");
+  if (static_cast<int64_t>(n_seq) * g.H_kv * ((static_cast<int64_t>(W) * g.block_size + TILE - 1) / TILE) >=
+      (int64_t(1) << 31))
+    return fail(PKV_ERR_INVALID_ARG, "batch too large (tile count must stay below 2^31)");
+  void* err = nullptr;
+  if (int rc = device_error_word(&err)) return rc;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+
+  DecodeArgs a{};
+  a.q = q;
+  a.out = out;
+  a.tables = block_tables;
+  a.seq_lens = seq_lens;
+  a.err = static_cast<int*>(err);
+  a.num_blocks = g.num_blocks;
+  a.n_seq = n_seq;
+  a.W = W;
+  a.H_q = g.H_q;
+  a.H_kv = g.H_kv;
+  a.G = G;
+  a.L = g.L;
+  a.layer = layer;
+  a.B = g.block_size;
+  a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+
+  if (!tc_eligible(P)) {
+    // the CUDA-core kernel needs no scratch at all
+    const int d = g.d_head;
+    const size_t smem = sizeof(float) * (SIMT_WARPS * GPAD * 2 + SIMT_WARPS * GPAD * d);
+    const int pairs = n_seq * g.H_kv;
+    const int npl = (d + 31) / 32;
+#define PKV_NA_SIMT(TYPE, NPL)                                                                       \
+  {                                                                                                  \
+    auto kern = decode_simt_kernel<TYPE, NPL>;                                                       \
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)); \
+    kern<<<pairs, SIMT_WARPS * 32, smem, st>>>(a, static_cast<const TYPE*>(k_pool),                  \
+                                               static_cast<const TYPE*>(v_pool), d);                 \
+  }
+#define PKV_NA_SIMT_T(TYPE)                      \
+  switch (npl) {                                 \
+    case 1: PKV_NA_SIMT(TYPE, 1) break;          \
+    case 2: PKV_NA_SIMT(TYPE, 2) break;          \
+    case 3: case 4: PKV_NA_SIMT(TYPE, 4) break;  \
+    default: PKV_NA_SIMT(TYPE, 8) break;         \
+  }
+    if (g.dtype == PKV_F32) {
+      PKV_NA_SIMT_T(float)
+    } else if (g.dtype == PKV_F16) {
+      PKV_NA_SIMT_T(__half)
+    } else {
+      PKV_NA_SIMT_T(__nv_bfloat16)
+    }
+#undef PKV_NA_SIMT_T
+#undef PKV_NA_SIMT
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(PKV_ERR_CUDA, std::string("decode launch: ") + cudaGetErrorString(e));
+    count_launch();
+    return PKV_OK;
+  }
+
+  // persistent grid, computed here without any cache
+  int smem = 0;
+  KernelPtr k = tc_kernel_for(P, &smem);
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return fail(PKV_ERR_CUDA, std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e));
+  int per_sm = 0, sms = 0, dev = 0;
+  const int nw = tc_variant().warps;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, nw * 32, smem);
+  if (e == cudaSuccess) e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess || per_sm < 1) return fail(PKV_ERR_CUDA, std::string("grid query: ") + cudaGetErrorString(e));
+  const int grid = per_sm * sms;
+  const WsLayout L = ws_layout(n_seq, static_cast<int64_t>(grid) * nw, g.d_head);
+  if (L.total > kNoallocScratchBytes)
+    return fail(PKV_ERR_INVALID_ARG, "pkv_decode_attention_noalloc: this batch needs " + std::to_string(L.total) +
+                                         " bytes of scratch, more than the static " +
+                                         std::to_string(kNoallocScratchBytes) +
+                                         "; use pkv_decode_attention with a caller workspace");
+  if (reinterpret_cast<uintptr_t>(q) & 15) return fail(PKV_ERR_INVALID_ARG, "q must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(k_pool) & 15) || (reinterpret_cast<uintptr_t>(v_pool) & 15))
+    return fail(PKV_ERR_INVALID_ARG, "k_pool and v_pool must be 16-byte aligned");
+  void* ws = nullptr;
+  if (int rc = noalloc_scratch(&ws)) return rc;
+
+  // tensor maps encoded on the stack (no cache)
+  CUtensorMap maps[2];
+  const CUtensorMapDataType dt = g.dtype == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(g.d_head),
+                        static_cast<cuuint64_t>(g.num_blocks) * g.L * g.H_kv * g.block_size};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(g.d_head) * 2};
+  cuuint32_t box[2] = {64, TILE};
+  cuuint32_t estr[2] = {1, 1};
+  for (int which = 0; which < 2; ++which) {
+    CUresult r = encode_fn()(&maps[which], dt, 2, const_cast<void*>(which ? v_pool : k_pool), dims, strides, box, estr,
+                             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled failed: " + std::to_string(r));
+  }
+  // every field the kernels read is written by the plan kernel (header, prefix,
+  // clamped lengths) or by the attention kernel (partials) earlier in this call,
+  // so nothing in the scratch has to start at zero
+  char* w = static_cast<char*>(ws);
+  a.hdr = reinterpret_cast<int32_t*>(w);
+  a.tile_prefix = reinterpret_cast<int32_t*>(w + L.prefix);
+  a.lens_c = reinterpret_cast<int32_t*>(w + L.lens);
+  a.partials = reinterpret_cast<float*>(w + L.partials);
+  a.total_warps = grid * nw;
+  plan_kernel<<<1, 1024, 0, st>>>(a);
+  void* args[] = {&maps[0], &maps[1], &a};
+  e = cudaLaunchKernel(k, dim3(grid), dim3(nw * 32), args, static_cast<size_t>(smem), st);
+  if (e != cudaSuccess) return fail(PKV_ERR_CUDA, std::string("decode launch: ") + cudaGetErrorString(e));
+  const bool bf = g.dtype == PKV_BF16;
+  const int pairs = n_seq * g.H_kv;
+  if (g.d_head == 128) {
+    if (bf) merge_tc_kernel<__nv_bfloat16, 128><<<pairs, 256, 0, st>>>(a);
+    else merge_tc_kernel<__half, 128><<<pairs, 256, 0, st>>>(a);
+  } else {
+    if (bf) merge_tc_kernel<__nv_bfloat16, 64><<<pairs, 128, 0, st>>>(a);
+    else merge_tc_kernel<__half, 64><<<pairs, 128, 0, st>>>(a);
+  }
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(PKV_ERR_CUDA, std::string("decode launch: ") + cudaGetErrorString(e));
+  count_launch(3);
+  return PKV_OK;
+}
