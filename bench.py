@@ -106,6 +106,70 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
+class NvmlSampler:
+    """Read-only NVML queries (SM clock, max SM clock, clock-event reasons) every
+    10 ms from a thread while the timed region runs."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+               0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, torch, dev):
+        import ctypes
+        import threading
+
+        self.ctypes, self.threading = ctypes, threading
+        self.nv = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.nv.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit failed")
+        self.h = ctypes.c_void_p()
+        ok = False
+        try:
+            uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+            ok = self.nv.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(self.h)) == 0
+        except Exception:
+            ok = False
+        if not ok and self.nv.nvmlDeviceGetHandleByIndex_v2(0, ctypes.byref(self.h)) != 0:
+            raise RuntimeError("no NVML handle")
+        self.reason_fn = getattr(self.nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.nv.nvmlDeviceGetCurrentClocksThrottleReasons
+        self.samples = []
+        self.stop_flag = False
+
+    def _sample(self):
+        c = self.ctypes
+        mhz, mx, rs = c.c_uint(), c.c_uint(), c.c_ulonglong()
+        self.nv.nvmlDeviceGetClockInfo(self.h, 1, c.byref(mhz))  # NVML_CLOCK_SM
+        self.nv.nvmlDeviceGetMaxClockInfo(self.h, 1, c.byref(mx))
+        self.reason_fn(self.h, c.byref(rs))
+        self.samples.append((mhz.value, mx.value, rs.value))
+
+    def _loop(self):
+        while not self.stop_flag:
+            self._sample()
+            time.sleep(0.01)
+
+    def start(self):
+        self.thread = self.threading.Thread(target=self._loop, daemon=True)
+        self.thread.start()
+
+    def stop(self):
+        self.stop_flag = True
+        self.thread.join()
+        if not self.samples:
+            self._sample()
+        sm = [s[0] for s in self.samples]
+        reasons = sorted({name for s in self.samples for bit, name in self.REASONS.items() if s[2] & bit})
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(s[1] for s in self.samples),
+                "reasons": reasons, "samples": len(self.samples), "source": "NVML every 10 ms"}
+
+
+def clock_sampler(torch, dev):
+    try:
+        return NvmlSampler(torch, dev)
+    except Exception:
+        return ClockSampler(torch.cuda.current_device())
+
+
 def dist_setup():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -402,7 +466,10 @@ RUNNERS = {"agent32k": AgentRunner, "chat": ChatRunner, "forked": ForkedRunner, 
 
 def run_decode(args, torch, pkv, dev, world, rank):
     total = args.warmup + args.steps + 2 + args.steps  # timed region, then e2e warm-up + e2e steps
-    r = RUNNERS[args.workload](torch, pkv, dev, total)
+    if args.workload == "agent32k" and (args.context or args.n_seq):
+        r = AgentRunner(torch, pkv, dev, total, n_seq=args.n_seq or 48, context=args.context or 32768)
+    else:
+        r = RUNNERS[args.workload](torch, pkv, dev, total)
     g = r.g
     launches0 = None
     for t in range(args.warmup):
@@ -410,7 +477,7 @@ def run_decode(args, torch, pkv, dev, world, rank):
     torch.cuda.synchronize()
     pkv.pkv_check_device_error()
     barrier(world)
-    clocks = ClockSampler(torch.cuda.current_device())
+    clocks = clock_sampler(torch, dev)
     clocks.start()
     e_start = torch.cuda.Event(enable_timing=True)
     e_end = torch.cuda.Event(enable_timing=True)
@@ -524,7 +591,7 @@ def run_swap(args, torch, pkv, dev, world, rank):
         one_step(False)
     torch.cuda.synchronize()
     barrier(world)
-    clocks = ClockSampler(torch.cuda.current_device())
+    clocks = clock_sampler(torch, dev)
     clocks.start()
     l0 = pkv.pkv_launch_count()
     es, ee = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -712,12 +779,14 @@ def reduce_max(torch, world, x: float) -> float:
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=["agent32k", "chat", "forked", "swap", "tiny"], default="agent32k")
     ap.add_argument("--swap-engine", type=int, default=0, help="swap workload: 0 SM kernel, 1 copy engines")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--context", type=int, default=0, help="agent workload: tokens per sequence (default 32768)")
+    ap.add_argument("--n-seq", type=int, default=0, help="agent workload: sequences (default 48)")
     ap.add_argument("--traffic", type=float, default=None,
                     help="ncu dram bytes per decode launch, if captured for this kernel version")
     args = ap.parse_args()
