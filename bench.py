@@ -779,8 +779,8 @@ def reduce_max(torch, world, x: float) -> float:
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=100)
-    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=None, help="timed steps (default 100; swap 4)")
+    ap.add_argument("--warmup", type=int, default=None, help="warm-up steps (default 10; swap 3)")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=["agent32k", "chat", "forked", "swap", "tiny"], default="agent32k")
     ap.add_argument("--swap-engine", type=int, default=0, help="swap workload: 0 SM kernel, 1 copy engines")
@@ -790,6 +790,10 @@ def main():
     ap.add_argument("--traffic", type=float, default=None,
                     help="ncu dram bytes per decode launch, if captured for this kernel version")
     args = ap.parse_args()
+    if args.steps is None:
+        args.steps = 4 if args.workload == "swap" else 100
+    if args.warmup is None:
+        args.warmup = 3 if args.workload == "swap" else 10
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     world, rank, local = dist_setup()

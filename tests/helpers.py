@@ -93,15 +93,19 @@ class PagedBatch:
         self.orc.seq_free(seq)
         self.ids.remove(seq)
 
-    def append(self, seq_ids, n_new, tag, layer=0, write_host=True):
+    def append(self, seq_ids, n_new, tag, layer=0, write_host=True, plan_only=False):
         """Plan on both sides (slots and CoW pairs must match), copy CoW blocks,
-        then write fresh N(0,1) keys/values for the new tokens."""
+        then write fresh N(0,1) keys/values for the new tokens (unless plan_only:
+        the pool's existing contents then stand for the tokens)."""
         import torch
 
         g = self.g
         slots, cows = pkv.pkv_plan_append(self.lib, seq_ids, n_new)
         oslots, ocows = self.orc.append(seq_ids, n_new)
         assert np.array_equal(slots, oslots) and np.array_equal(cows, ocows)
+        if plan_only:
+            assert len(cows) == 0
+            return slots, cows
         if len(cows):
             pkv.pkv_copy_blocks(self.lib, cows, self.kp, self.vp)
             if write_host and self.hk is not None:
