@@ -767,11 +767,13 @@ def barrier(world):
 
 
 def reduce_max(torch, world, x: float) -> float:
+    """Max over ranks (timing only; the data path has no collective)."""
     if world <= 1:
         return x
     import torch.distributed as dist
 
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
 
