@@ -188,21 +188,21 @@ class Staging:
         self.torch = torch
         self.host = [torch.empty(n_ints, dtype=torch.int32, pin_memory=True) for _ in range(depth)]
         self.dev = [torch.empty(n_ints, dtype=torch.int32, device=dev) for _ in range(depth)]
-        self.events = [None] * depth
+        self.host_np = [h.numpy() for h in self.host]
+        self.events = [torch.cuda.Event() for _ in range(depth)]
+        for e in self.events:
+            e.record()
         self.i = 0
 
     def next(self):
         k = self.i % len(self.host)
         self.i += 1
-        if self.events[k] is not None:
-            self.events[k].synchronize()
-        return k, self.host[k].numpy(), self.host[k], self.dev[k]
+        self.events[k].synchronize()
+        return k, self.host_np[k], self.host[k], self.dev[k]
 
-    def upload(self, k, n_ints: int):
-        self.dev[k][:n_ints].copy_(self.host[k][:n_ints], non_blocking=True)
-        ev = self.torch.cuda.Event()
-        ev.record()
-        self.events[k] = ev
+    def mark(self, k, n_ints: int):
+        """Record that slot k's host buffer is in use by work enqueued so far."""
+        self.events[k].record()
         return n_ints * 4
 
 
@@ -233,45 +233,71 @@ class DecodeRunner:
         self.ws = torch.empty(self.pkv.pkv_decode_workspace_size(self.pool, n_max), dtype=torch.uint8,
                               device=self.dev)
         self.staging = Staging(torch, self.dev, n_max * (self.Wd + 2))
-        self.ones = np.ones(n_max, np.int32)
+        self.stream = torch.cuda.current_stream().cuda_stream
+        self._fast_pool = self.pool
+        self._prepare_fast()
 
-    def step(self, t: int, timed: bool = False, host_inputs=None):
+    def _prepare_fast(self):
+        """Addresses and events for the timed loop, made once: the loop then calls
+        pkv_decode_step through a raw ctypes prototype with plain integers."""
+        import ctypes
+
+        torch = self.torch
+        vp_, i32 = ctypes.c_void_p, ctypes.c_int32
+        f = self.pkv._L()["pkv_decode_step"]  # a separate function object (argtypes below)
+        f.argtypes = [vp_, i32, vp_, i32, i32, vp_, vp_, vp_, vp_, vp_, ctypes.c_float, vp_, vp_, vp_, vp_,
+                      ctypes.c_size_t, vp_, vp_, vp_]
+        f.restype = ctypes.c_int
+        self.raw_step = f
+        es = lambda x: x.element_size() * x[0].numel()
+        self.q_base, self.q_stride = self.q.data_ptr(), es(self.q)
+        self.k_base, self.k_stride = self.kn.data_ptr(), es(self.kn)
+        self.v_base, self.v_stride = self.vn.data_ptr(), es(self.vn)
+        self.ptrs = (self.kp.data_ptr(), self.vp.data_ptr(), self.out.data_ptr(), self.ws.data_ptr(),
+                     self.ws.numel())
+        self.handle = self.pool.handle.value if hasattr(self.pool.handle, "value") else self.pool.handle
+
+    def make_events(self, n):
+        """n pairs of timing events, created up front (torch creates a CUDA event at its first record)."""
+        torch = self.torch
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        for a, b in evs:
+            a.record()
+            b.record()
+        return evs
+
+    def step(self, t: int, timed: bool = False, host_inputs=None, events=None):
+        """Plan, CoW copy, append and attend through one pkv_decode_step call."""
         torch, pkv, g = self.torch, self.pkv, self.g
         ids = self.running(t)
         n = len(ids)
         if n == 0:
             return
         self.last_ids = ids
-        slots, cows = pkv.pkv_plan_append(self.pool, ids, self.ones[:n])
-        k, hnp, _, dmeta = self.staging.next()
-        hnp[:n] = slots
-        tables = hnp[n:n + n * self.Wd].reshape(n, self.Wd)
-        lens = hnp[n + n * self.Wd:n + n * self.Wd + n]
-        pkv.pkv_export_tables(self.pool, ids, self.Wd, tables=tables, seq_lens=lens)
-        nbytes = self.staging.upload(k, n * (self.Wd + 2))
-        if len(cows):
-            pkv.pkv_copy_blocks(self.pool, cows, self.kp, self.vp)
+        k, hnp, hbuf, dmeta = self.staging.next()
         if host_inputs is not None:
+            # end to end: the public binding, inputs copied from pinned host memory
             q, kn, vn = self.q_e2e[:n], self.kn_e2e[:n], self.vn_e2e[:n]
             q.copy_(host_inputs[0][t][:n], non_blocking=True)
             kn.copy_(host_inputs[1][t][:n], non_blocking=True)
             vn.copy_(host_inputs[2][t][:n], non_blocking=True)
+            pkv.pkv_decode_step(self.pool, 0, ids, self.Wd, q, kn, vn, self.kp, self.vp, self.scale, self.out[:n],
+                                hbuf, dmeta, self.ws, attn_events=events)
         else:
-            q, kn, vn = self.q[t][:n], self.kn[t][:n], self.vn[t][:n]
-        d_slots = dmeta[:n]
-        d_tables = dmeta[n:n + n * self.Wd].view(n, self.Wd)
-        d_lens = dmeta[n + n * self.Wd:n + n * self.Wd + n]
-        pkv.pkv_append_kv(self.pool, 0, kn, vn, d_slots, self.kp, self.vp)
+            kp, vp, outp, wsp, wsb = self.ptrs
+            h = self.handle if self.pool is self._fast_pool else self._refresh_handle()
+            rc = self.raw_step(h, 0, ids.ctypes.data, n, self.Wd, self.q_base + t * self.q_stride,
+                               self.k_base + t * self.k_stride, self.v_base + t * self.v_stride, kp, vp,
+                               self.scale, outp, hbuf.data_ptr(), dmeta.data_ptr(), wsp, wsb,
+                               events[0].cuda_event if events else None, events[1].cuda_event if events else None,
+                               self.stream)
+            if rc:
+                pkv._check(rc, "pkv_decode_step")
+        nbytes = self.staging.mark(k, n * (self.Wd + 2))
         if timed:
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            e0.record()
-        pkv.pkv_decode_attention(self.pool, 0, q, self.kp, self.vp, d_tables, d_lens, self.scale, self.out[:n],
-                                 self.ws)
-        if timed:
-            e1.record()
-            self.decode_ms.append((e0, e1))
-            tok = int(lens.astype(np.int64).sum())
+            self.decode_ms.append(events)
+            lens = hnp[n + n * self.Wd:n + n * self.Wd + n]
+            tok = int(lens.sum(dtype=np.int64))
             kvb = tok * g.H_kv * g.d_head * g.elem_bytes * 2
             self.kv_bytes.append(kvb)
             qo = 2 * n * g.H_q * g.d_head * g.elem_bytes
@@ -284,6 +310,11 @@ class DecodeRunner:
             self.e2e_in_bytes += nbytes + (q.numel() + kn.numel() + vn.numel()) * g.elem_bytes
             self.e2e_out_bytes += n * g.H_q * g.d_head * g.elem_bytes
         self.after_step(t, ids)
+
+    def _refresh_handle(self):
+        self._fast_pool = self.pool
+        self.handle = self.pool.handle.value if hasattr(self.pool.handle, "value") else self.pool.handle
+        return self.handle
 
     def after_step(self, t, ids):
         pass
@@ -326,6 +357,7 @@ class AgentRunner(DecodeRunner):
         self.pool = pkv.pkv_pool_create(g.L, g.H_q, g.H_kv, g.d_head, g.block_size, g.dtype, g.num_blocks,
                                         wl.free_order)
         self.ids = [pkv.pkv_seq_create(self.pool) for _ in range(n_seq)]
+        self.ids_np = np.array(self.ids, np.int32)
         pkv.pkv_plan_append(self.pool, self.ids, [context] * n_seq)
         # the pool's contents are the prompt keys/values: N(0,1) drawn on the device
         self.kp = W.device_normal(self.seed, "k_pool", g.pool_shape(), g.dtype, dev)
@@ -341,7 +373,7 @@ class AgentRunner(DecodeRunner):
                        "parallelism": "replicas (no collectives)"}
 
     def running(self, t):
-        return self.ids
+        return self.ids_np
 
 
 class ChatRunner(DecodeRunner):
@@ -356,6 +388,8 @@ class ChatRunner(DecodeRunner):
         self.scale = wl.scale
         self.sched_steps = wl.extra["steps"]
         self.gen = wl.extra["generated"]
+        self.gen_np = np.asarray(self.gen)
+        self.all_ids = np.arange(n_seq, dtype=np.int32)
         self.prompt = wl.lengths
         self.kp = W.device_normal(self.seed, "k_pool", g.pool_shape(), g.dtype, dev)
         self.vp = W.device_normal(self.seed, "v_pool", g.pool_shape(), g.dtype, dev)
@@ -385,13 +419,12 @@ class ChatRunner(DecodeRunner):
     def running(self, t):
         k = t % self.sched_steps
         self.pool, ids = self.states[t // self.sched_steps]
-        return [s for s in ids if self.gen[s] > k]
+        return self.all_ids[self.gen_np > k]
 
     def after_step(self, t, ids):
         k = t % self.sched_steps
-        for s in ids:
-            if self.gen[s] == k + 1:  # generated budget reached: release
-                self.pkv.pkv_seq_free(self.pool, s)
+        for s in ids[self.gen_np[ids] == k + 1]:  # generated budget reached: release
+            self.pkv.pkv_seq_free(self.pool, int(s))
 
 
 class ForkedRunner(DecodeRunner):
@@ -419,6 +452,7 @@ class ForkedRunner(DecodeRunner):
             vn = W.device_normal(self.seed, "suffix_v", (len(slots), g.H_kv, g.d_head), g.dtype, dev)
             pkv.pkv_append_kv(self.pool, 0, kn, vn, torch.from_numpy(slots).to(dev), self.kp, self.vp)
         self.unique_tokens = int(wl.lengths[0]) + sum(suffix)
+        self.ids_np = np.array(self.ids, np.int32)
         self.Wd = -(-(int(wl.lengths[0]) + 2048 + total_steps + 1) // g.block_size)
         self.inputs_for_steps("forked")
         self._alloc_common(n_branch)
@@ -430,7 +464,7 @@ class ForkedRunner(DecodeRunner):
                        "parallelism": "replicas (no collectives)"}
 
     def running(self, t):
-        return self.ids
+        return self.ids_np
 
 
 class TinyRunner(DecodeRunner):
@@ -446,6 +480,7 @@ class TinyRunner(DecodeRunner):
         self.pool = pkv.pkv_pool_create(g.L, g.H_q, g.H_kv, g.d_head, g.block_size, g.dtype, g.num_blocks,
                                         wl.free_order)
         self.ids = [pkv.pkv_seq_create(self.pool) for _ in range(self.n_max)]
+        self.ids_np = np.array(self.ids, np.int32)
         pkv.pkv_plan_append(self.pool, self.ids, wl.lengths)
         self.kp = W.device_normal(self.seed, "k_pool", g.pool_shape(), g.dtype, dev)
         self.vp = W.device_normal(self.seed, "v_pool", g.pool_shape(), g.dtype, dev)
@@ -458,7 +493,7 @@ class TinyRunner(DecodeRunner):
                        "parallelism": "replicas (no collectives)"}
 
     def running(self, t):
-        return self.ids
+        return self.ids_np
 
 
 RUNNERS = {"agent32k": AgentRunner, "chat": ChatRunner, "forked": ForkedRunner, "tiny": TinyRunner}
@@ -481,10 +516,11 @@ def run_decode(args, torch, pkv, dev, world, rank):
     clocks.start()
     e_start = torch.cuda.Event(enable_timing=True)
     e_end = torch.cuda.Event(enable_timing=True)
+    evs = r.make_events(args.steps)
     launches0 = pkv.pkv_launch_count()
     e_start.record()
-    for t in range(args.warmup, args.warmup + args.steps):
-        r.step(t, timed=True)
+    for i, t in enumerate(range(args.warmup, args.warmup + args.steps)):
+        r.step(t, timed=True, events=evs[i])
     e_end.record()
     torch.cuda.synchronize()
     launches = pkv.pkv_launch_count() - launches0
@@ -507,9 +543,11 @@ def run_decode(args, torch, pkv, dev, world, rank):
     kv_before = len(r.kv_bytes)
     barrier(world)
     torch.cuda.synchronize()
+    evs2 = r.make_events(args.steps)
+    torch.cuda.synchronize()
     h0 = time.perf_counter()
-    for t in range(t0 + 2, t0 + 2 + args.steps):
-        r.step(t, timed=True, host_inputs=host)
+    for i, t in enumerate(range(t0 + 2, t0 + 2 + args.steps)):
+        r.step(t, timed=True, host_inputs=host, events=evs2[i])
     torch.cuda.synchronize()
     e2e_s = reduce_max(torch, world, (time.perf_counter() - h0) * 1e3) / 1e3
     e2e_kv = sum(r.kv_bytes[kv_before:])
@@ -643,7 +681,7 @@ def oracle_sample_decode(runner, n_sample: int, reps: int = 1):
     g = runner.g
     pool = runner.pool
     ids = []
-    for s in runner.last_ids:  # sequences still resident after the last step
+    for s in (int(x) for x in runner.last_ids):  # sequences still resident after the last step
         try:
             runner.pkv.pkv_seq_len(pool, s)
             ids.append(s)

@@ -21,6 +21,7 @@
  *     changes no host state (all or nothing, [PA] "Inference Lab increment") and
  *     pkv_last_error_message() gives a thread-local description.
  *   - No C++ exception crosses the ABI.
+ *   - A pool's control plane is not thread-safe: serialise calls on one pool.
  *   - Device operations are asynchronous on the given stream (a cudaStream_t;
  *     NULL = the legacy default stream).  They never allocate device memory.
  *   - Ownership: the caller owns every device buffer (pools, q, out, workspace,
@@ -186,6 +187,30 @@ int pkv_decode_attention(const pkv_pool* pool, int32_t layer, const void* q, con
                          const void* v_pool, const int32_t* block_tables, int32_t W, const int32_t* seq_lens,
                          int32_t n_seq, float scale, void* out, void* workspace, size_t ws_bytes,
                          pkv_stream_t stream);
+
+/* One decode step for n resident sequences, in one call: plan one new token per
+ * sequence (pkv_plan_append), copy shared tail blocks (pkv_copy_blocks), write
+ * the new keys/values (pkv_append_kv) and attend over len + 1 tokens
+ * (pkv_decode_attention) -- [PA] "The real cache": write each new key and value
+ * at its block and offset, then attend.
+ *   seq_ids : HOST int32 [n], distinct resident sequences; row i of q, k_new,
+ *             v_new and out belongs to seq_ids[i].
+ *   q, out  : device [n][H_q][d_head];  k_new, v_new: device [n][H_kv][d_head].
+ *   W       : table width; every sequence needs ceil((len + 1) / B) <= W.
+ *   meta_host: page-locked host int32 [n * (W + 2)]: the step writes its slot
+ *             mapping, tables and lengths there and copies them to meta_dev
+ *             (device int32, same size) on the stream; do not reuse meta_host
+ *             until that copy has run (e.g. a ring of buffers and events).
+ *   workspace: as for pkv_decode_attention (pkv_decode_workspace_size(pool, n)).
+ *   attn_begin, attn_end: optional cudaEvent_t (NULL = none) recorded on the
+ *             stream just before and after the attention kernels.
+ * Arguments are validated before anything changes; after the plan is applied,
+ * only a CUDA launch failure (PKV_ERR_CUDA) can still fail the call. */
+typedef struct CUevent_st* pkv_event_t; /* identical to cudaEvent_t */
+int pkv_decode_step(pkv_pool* pool, int32_t layer, const int32_t* seq_ids, int32_t n, int32_t W, const void* q,
+                    const void* k_new, const void* v_new, void* k_pool, void* v_pool, float scale, void* out,
+                    int32_t* meta_host, int32_t* meta_dev, void* workspace, size_t ws_bytes, pkv_event_t attn_begin,
+                    pkv_event_t attn_end, pkv_stream_t stream);
 
 /* Decode attention that allocates nothing.  (The pages have no counterpart of
  * this call; it exists for callers of this library.)

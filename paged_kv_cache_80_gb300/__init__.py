@@ -20,6 +20,7 @@ __all__ = [
     "pkv_version", "pkv_pool_create", "pkv_pool_destroy", "pkv_pool_geometry", "pkv_seq_create", "pkv_seq_fork",
     "pkv_seq_free", "pkv_seq_len", "pkv_plan_append", "pkv_export_tables", "pkv_refcounts", "pkv_free_list",
     "pkv_append_kv", "pkv_decode_workspace_size", "pkv_decode_attention", "pkv_decode_attention_noalloc",
+    "pkv_decode_step",
     "pkv_copy_blocks", "pkv_swap_out",
     "pkv_swap_in", "pkv_seq_host_slots", "pkv_pool_set_swap_engine", "pkv_check_device_error", "pkv_launch_count",
 ]
@@ -80,6 +81,8 @@ def _L():
             "pkv_decode_attention_noalloc": ([vp, i32, vp, vp, vp, vp, i32, vp, i32, ctypes.c_float, vp, vp],
                                              ctypes.c_int),
             "pkv_copy_blocks": ([vp, P32, i32, vp, vp, vp], ctypes.c_int),
+            "pkv_decode_step": ([vp, i32, P32, i32, i32, vp, vp, vp, vp, vp, ctypes.c_float, vp, vp, vp, vp,
+                                 ctypes.c_size_t, vp, vp, vp], ctypes.c_int),
             "pkv_swap_out": ([vp, i32, vp, vp, vp, i64, P64, i32, P32, vp], ctypes.c_int),
             "pkv_swap_in": ([vp, i32, vp, i64, i32, vp, vp, P32, vp], ctypes.c_int),
             "pkv_seq_host_slots": ([vp, i32, P64, i32, P32], ctypes.c_int),
@@ -323,6 +326,27 @@ def pkv_decode_attention_noalloc(pool: PoolLike, layer: int, q, k_pool, v_pool, 
                                              _dev(v_pool, "v_pool"), _dev(block_tables, "block_tables"), W,
                                              _dev(seq_lens, "seq_lens"), n_seq, float(scale), _dev(out, "out"),
                                              _stream(stream)), "pkv_decode_attention_noalloc")
+
+
+def pkv_decode_step(pool: PoolLike, layer: int, seq_ids, W: int, q, k_new, v_new, k_pool, v_pool, scale: float,
+                    out, meta_host, meta_dev, workspace, attn_events=None, stream=None) -> None:
+    """One decode step (plan, CoW copy, append, attend) for the sequences seq_ids.
+    meta_host: pinned CPU int32 tensor, meta_dev: CUDA int32 tensor, each >= n*(W+2)."""
+    ids = _i32(seq_ids)
+    n = ids.size
+    if meta_host.numel() < n * (W + 2) or meta_dev.numel() < n * (W + 2):
+        raise ValueError("metadata buffers smaller than n * (W + 2)")
+    ev0 = ev1 = None
+    if attn_events is not None:
+        for ev in attn_events:
+            if not ev.cuda_event:  # torch creates its CUDA event at the first record
+                ev.record()
+        ev0, ev1 = attn_events[0].cuda_event, attn_events[1].cuda_event
+    _check(_L().pkv_decode_step(_h(pool), layer, _p32(ids), n, W, _dev(q, "q"), _dev(k_new, "k_new"),
+                                _dev(v_new, "v_new"), _dev(k_pool, "k_pool"), _dev(v_pool, "v_pool"), float(scale),
+                                _dev(out, "out"), _host_ptr(meta_host, "meta_host"), _dev(meta_dev, "meta_dev"),
+                                _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(), ev0, ev1,
+                                _stream(stream)), "pkv_decode_step")
 
 
 def pkv_copy_blocks(pool: PoolLike, pairs, k_pool, v_pool, stream=None) -> None:

@@ -81,19 +81,19 @@ int check_geometry(const pkv_geometry* g) {
 }
 
 SeqState* find_seq(Pool& P, int32_t id) {
-  auto it = P.seqs.find(id);
-  return it == P.seqs.end() ? nullptr : &it->second;
+  if (id < 0 || id >= P.next_id || P.seqs[id].state != 0) return nullptr;
+  return &P.seqs[id];
 }
 
 const SeqState* find_seq(const Pool& P, int32_t id) {
-  auto it = P.seqs.find(id);
-  return it == P.seqs.end() ? nullptr : &it->second;
+  if (id < 0 || id >= P.next_id || P.seqs[id].state != 0) return nullptr;
+  return &P.seqs[id];
 }
 
 // Releasing a released sequence is a double free; any other use of it, or of an
 // id never created, is an invalid argument.
 int unknown_seq(const Pool& P, int32_t id, bool releasing = false) {
-  if (releasing && id >= 0 && id < static_cast<int32_t>(P.released.size()) && P.released[id])
+  if (releasing && id >= 0 && id < P.next_id && P.seqs[id].state == 1)
     return fail(PKV_ERR_DOUBLE_FREE, "sequence " + std::to_string(id) + " was already released");
   return fail(PKV_ERR_INVALID_ARG, "unknown or released sequence " + std::to_string(id));
 }
@@ -177,6 +177,7 @@ int pkv_pool_create(const pkv_geometry* geometry, const int32_t* initial_free_or
   P->block_bytes = P->block_elems * pkv::elem_size(geometry->dtype);
   P->free.reset(order);
   P->ref.assign(N, 0);
+  P->dropped.assign(N, 0);
   *out = reinterpret_cast<pkv_pool*>(P);
   return PKV_OK;
 }
@@ -202,10 +203,8 @@ int pkv_seq_create(pkv_pool* pool, int32_t* seq_id) {
   if (!pool || !seq_id) return fail(PKV_ERR_INVALID_ARG, "NULL argument");
   Pool& P = *as_pool(pool);
   if (P.next_id == INT32_MAX) return fail(PKV_ERR_INVALID_ARG, "sequence ids exhausted");
-  const int32_t id = P.next_id++;
-  P.seqs.emplace(id, SeqState());
-  P.released.push_back(0);
-  *seq_id = id;
+  P.seqs.emplace_back();
+  *seq_id = P.next_id++;
   return PKV_OK;
 }
 
@@ -221,10 +220,8 @@ int pkv_seq_fork(pkv_pool* pool, int32_t parent, int32_t* child) {
   c.table = par->table;  // table duplication
   c.len = par->len;      // S_child = S_prefix
   for (int32_t p : c.table) ++P.ref[p];  // one more owner per shared block
-  const int32_t id = P.next_id++;
-  P.seqs.emplace(id, std::move(c));
-  P.released.push_back(0);
-  *child = id;
+  P.seqs.push_back(std::move(c));  // may move the parent's state: `par` is not used after this
+  *child = P.next_id++;
   return PKV_OK;
 }
 
@@ -237,8 +234,8 @@ int pkv_seq_free(pkv_pool* pool, int32_t seq) {
   for (int32_t p : s->table)
     if (P.ref[p] <= 0) return fail(PKV_ERR_DOUBLE_FREE, "block " + std::to_string(p) + " has no owner");
   for (int32_t p : s->table) drop_owner(P, p);
-  P.seqs.erase(seq);
-  P.released[seq] = 1;
+  *s = SeqState();
+  s->state = 1;
   return PKV_OK;
 }
 
@@ -261,8 +258,10 @@ int pkv_plan_append(pkv_pool* pool, const int32_t* seq_ids, const int32_t* n_new
   const int64_t B = P.geo.block_size;
 
   // validate, and order the requests by ascending sequence id
-  std::vector<int32_t> order(n);
-  std::vector<int64_t> first_tok(n + 1, 0);
+  std::vector<int32_t>& order = P.order;
+  order.resize(n);
+  bool ascending = true;
+  int64_t total_tok = 0;
   for (int32_t i = 0; i < n; ++i) {
     const SeqState* s = find_seq(P, seq_ids[i]);
     if (!s) return unknown_seq(P, seq_ids[i]);
@@ -270,38 +269,45 @@ int pkv_plan_append(pkv_pool* pool, const int32_t* seq_ids, const int32_t* n_new
     if (n_new[i] < 0) return fail(PKV_ERR_INVALID_ARG, "n_new must be >= 0");
     if (s->len + n_new[i] > (int64_t(1) << 31) - 1) return fail(PKV_ERR_INVALID_ARG, "sequence too long");
     order[i] = i;
-    first_tok[i + 1] = first_tok[i] + n_new[i];
+    if (i > 0 && seq_ids[i] <= seq_ids[i - 1]) ascending = false;
+    total_tok += n_new[i];
   }
-  std::sort(order.begin(), order.end(), [&](int32_t a, int32_t b) { return seq_ids[a] < seq_ids[b]; });
-  for (int32_t k = 1; k < n; ++k)
-    if (seq_ids[order[k]] == seq_ids[order[k - 1]]) return fail(PKV_ERR_INVALID_ARG, "duplicate sequence id");
+  if (total_tok > INT32_MAX) return fail(PKV_ERR_INVALID_ARG, "too many tokens in one append");
+  if (!ascending) {
+    std::sort(order.begin(), order.end(), [&](int32_t a, int32_t b) { return seq_ids[a] < seq_ids[b]; });
+    for (int32_t k = 1; k < n; ++k)
+      if (seq_ids[order[k]] == seq_ids[order[k - 1]]) return fail(PKV_ERR_INVALID_ARG, "duplicate sequence id");
+  }
 
-  // dry run: blocks needed, with owner counts as earlier copies leave them
-  std::unordered_map<int32_t, int32_t> dropped;  // block -> owners given up by earlier CoWs in this call
+  // dry run: blocks needed, with owner counts as earlier copies in this call leave them
   int64_t needed = 0;
   for (int32_t i : order) {
     if (n_new[i] == 0) continue;
-    const SeqState& s = *find_seq(P, seq_ids[i]);
+    const SeqState& s = P.seqs[seq_ids[i]];
     const int64_t len = s.len;
     if (len % B != 0) {
       const int32_t tail = s.table[len / B];
-      auto it = dropped.find(tail);
-      const int32_t owners = P.ref[tail] - (it == dropped.end() ? 0 : it->second);
-      if (owners > 1) {
+      if (P.ref[tail] - P.dropped[tail] > 1) {
         ++needed;
-        ++dropped[tail];
+        ++P.dropped[tail];
       }
     }
     needed += (len + n_new[i] + B - 1) / B - (len + B - 1) / B;  // positions with o == 0
   }
+  for (int32_t i : order)  // reset the scratch counts
+    if (n_new[i] != 0 && P.seqs[seq_ids[i]].len % B != 0) P.dropped[P.seqs[seq_ids[i]].table[P.seqs[seq_ids[i]].len / B]] = 0;
   if (needed > P.free.size())
     return fail(PKV_ERR_OUT_OF_BLOCKS, "append needs " + std::to_string(needed) + " blocks, " +
                                            std::to_string(P.free.size()) + " free");
 
-  // commit
+  // commit; sequence i's tokens start at the caller's offset sum_{j<i} n_new[j]
+  std::vector<int64_t>& first_tok = P.first_tok;
+  first_tok.resize(n + 1);
+  first_tok[0] = 0;
+  for (int32_t i = 0; i < n; ++i) first_tok[i + 1] = first_tok[i] + n_new[i];
   int32_t cows = 0;
   for (int32_t i : order) {
-    SeqState& s = *find_seq(P, seq_ids[i]);
+    SeqState& s = P.seqs[seq_ids[i]];
     int32_t* out = slot_mapping + first_tok[i];
     for (int32_t k = 0; k < n_new[i]; ++k) {
       const int64_t t = s.len;
@@ -536,6 +542,56 @@ int pkv_seq_host_slots(const pkv_pool* pool, int32_t seq, int64_t* out, int32_t 
   *n = static_cast<int32_t>(s->host_frames.size());
   if (out)
     for (int32_t j = 0; j < *n && j < capacity; ++j) out[j] = s->host_frames[j];
+  return PKV_OK;
+}
+
+int pkv_decode_step(pkv_pool* pool, int32_t layer, const int32_t* seq_ids, int32_t n, int32_t W, const void* q,
+                    const void* k_new, const void* v_new, void* k_pool, void* v_pool, float scale, void* out,
+                    int32_t* meta_host, int32_t* meta_dev, void* workspace, size_t ws_bytes, pkv_event_t attn_begin,
+                    pkv_event_t attn_end, pkv_stream_t stream) {
+  pkv::clear_error();
+  if (!pool || n < 0 || W <= 0) return fail(PKV_ERR_INVALID_ARG, "bad arguments to pkv_decode_step");
+  if (n == 0) return PKV_OK;
+  if (!seq_ids || !q || !k_new || !v_new || !k_pool || !v_pool || !out || !meta_host || !meta_dev || !workspace)
+    return fail(PKV_ERR_INVALID_ARG, "NULL buffer");
+  Pool& P = *as_pool(pool);
+  const Pool& CP = P;
+  if (layer < 0 || layer >= P.geo.L) return fail(PKV_ERR_INVALID_ARG, "layer out of range");
+  const int64_t B = P.geo.block_size;
+  for (int32_t i = 0; i < n; ++i) {
+    const SeqState* s = find_seq(CP, seq_ids[i]);
+    if (!s) return unknown_seq(CP, seq_ids[i]);
+    if (s->swapped) return fail(PKV_ERR_INVALID_ARG, "sequence " + std::to_string(seq_ids[i]) + " is swapped out");
+    if ((s->len + 1 + B - 1) / B > W)
+      return fail(PKV_ERR_INVALID_ARG, "W = " + std::to_string(W) + " cannot hold sequence " +
+                                           std::to_string(seq_ids[i]) + " after the step");
+  }
+  size_t need = 0;
+  if (int rc = pkv::decode_workspace_bytes(P, n, &need)) return rc;
+  if (ws_bytes < need) return fail(PKV_ERR_INVALID_ARG, "workspace too small: need " + std::to_string(need));
+
+  static thread_local std::vector<int32_t> ones, cows;
+  if (static_cast<int32_t>(ones.size()) < n) ones.assign(n, 1);
+  if (static_cast<int32_t>(cows.size()) < 2 * n) cows.resize(2 * n);
+  int32_t n_cow = 0;
+  int32_t* slots = meta_host;
+  int32_t* tables = meta_host + n;
+  int32_t* lens = meta_host + n + static_cast<int64_t>(n) * W;
+  if (int rc = pkv_plan_append(pool, seq_ids, ones.data(), n, slots, cows.data(), &n_cow)) return rc;
+  if (int rc = pkv_export_tables(pool, seq_ids, n, tables, W, lens)) return rc;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const size_t meta_bytes = sizeof(int32_t) * static_cast<size_t>(n) * (W + 2);
+  cudaError_t e = cudaMemcpyAsync(meta_dev, meta_host, meta_bytes, cudaMemcpyHostToDevice, st);
+  if (e != cudaSuccess) return fail(PKV_ERR_CUDA, std::string("cudaMemcpyAsync (step metadata): ") + cudaGetErrorString(e));
+  if (n_cow > 0)
+    if (int rc = pkv_copy_blocks(pool, cows.data(), n_cow, k_pool, v_pool, stream)) return rc;
+  if (int rc = pkv_append_kv(pool, layer, k_new, v_new, meta_dev, n, k_pool, v_pool, stream)) return rc;
+  if (attn_begin) cudaEventRecord(reinterpret_cast<cudaEvent_t>(attn_begin), st);
+  if (int rc = pkv_decode_attention(pool, layer, q, k_pool, v_pool, meta_dev + n, W,
+                                    meta_dev + n + static_cast<int64_t>(n) * W, n, scale, out, workspace, ws_bytes,
+                                    stream))
+    return rc;
+  if (attn_end) cudaEventRecord(reinterpret_cast<cudaEvent_t>(attn_end), st);
   return PKV_OK;
 }
 

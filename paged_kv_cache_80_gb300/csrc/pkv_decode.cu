@@ -65,18 +65,25 @@ struct DecodeArgs {
   int32_t* tile_prefix;  // [n_seq + 1]: tiles of sequences before s (per KV head)
   int32_t* lens_c;       // [n_seq]: lengths clamped to [0, W*B]
   int32_t* hdr;          // [0] = total tiles over all pairs
+  int32_t* counters;     // [n_seq * H_kv]: partials written so far for a split pair
+  int4* wstart;          // [total_warps]: (sequence, KV head, tile, tiles of pair) at each warp's first tile
   float* partials;
   int* err;
   int64_t num_blocks;
   int32_t n_seq, W, H_q, H_kv, G, L, layer, B;
+  int32_t D, elem;   // head dimension, bytes per element
   float scale_log2;  // scale * log2(e)
   int32_t total_warps;
 };
 
 // --------------------------------------------------------------------------- plan
 
+__device__ __forceinline__ int run_total_from(const DecodeArgs& a) { return *const_cast<volatile int32_t*>(a.hdr); }
+
 // One CTA: clamp lengths, tiles per sequence, exclusive prefix, total tile count.
 __global__ void __launch_bounds__(1024) plan_kernel(const DecodeArgs a) {
+  // let the attention kernel launch now; it waits for this grid before reading its outputs
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   __shared__ int32_t warp_sums[32];
   const int tid = threadIdx.x;
   const int per = (a.n_seq + blockDim.x - 1) / blockDim.x;
@@ -119,6 +126,34 @@ __global__ void __launch_bounds__(1024) plan_kernel(const DecodeArgs a) {
     a.tile_prefix[a.n_seq] = run;
     a.hdr[0] = run * a.H_kv;
   }
+  // counters of split pairs start at zero
+  for (int p = tid; p < a.n_seq * a.H_kv; p += blockDim.x) a.counters[p] = 0;
+  // an empty sequence attends to nothing: zero output (16-byte stores; H_q*D*b is a multiple of 16)
+  const int row16 = a.H_q * a.D * a.elem / 16;
+  for (int s = s0; s < s1; ++s)
+    if (a.lens_c[s] == 0)
+      for (int k = 0; k < row16; ++k)
+        reinterpret_cast<int4*>(static_cast<char*>(a.out) + static_cast<int64_t>(s) * row16 * 16)[k] =
+            make_int4(0, 0, 0, 0);
+  __syncthreads();  // the prefix array is complete (global writes of this block are visible)
+  // each warp's first tile: sequence s (largest with H_kv*Q[s] <= start), KV head, tile, tiles of pair
+  const int total = run_total_from(a);
+  const int R = (total + a.total_warps - 1) / a.total_warps;
+  for (int w = tid; w < a.total_warps; w += blockDim.x) {
+    const int start = w * R;
+    if (start >= total) {
+      a.wstart[w] = make_int4(-1, 0, 0, 0);
+      continue;
+    }
+    int lo = 0, hi = a.n_seq - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (a.H_kv * a.tile_prefix[mid] <= start) lo = mid; else hi = mid - 1;
+    }
+    const int nt = a.tile_prefix[lo + 1] - a.tile_prefix[lo];
+    const int within = start - a.H_kv * a.tile_prefix[lo];
+    a.wstart[w] = make_int4(lo, within / nt, within - (within / nt) * nt, nt);
+  }
 }
 
 // --------------------------------------------------------------------------- tensor-core path
@@ -159,6 +194,58 @@ __device__ __forceinline__ __nv_bfloat16 from_float<__nv_bfloat16>(float x) { re
 template <>
 __device__ __forceinline__ __half from_float<__half>(float x) { return __float2half_rn(x); }
 
+// Merge the partials of one split pair (contributing warps wa..wb) and write its
+// G output rows.  Run by one whole warp; lane l owns float4 l of every d-chunk.
+// Partials are read through L2 (ld.global.cg): other SMs wrote them.
+template <typename T, int D>
+__device__ __forceinline__ void merge_pair(const DecodeArgs& a, int s, int g, int pbeg, int wa, int wb, int R,
+                                           int lane) {
+  using C = TcCfg<D>;
+  const int h0 = 2 * (lane & 3);
+  float M0 = -INFINITY, M1 = -INFINITY;
+  for (int w = wa; w <= wb; ++w) {
+    const int slot = (w == wa && pbeg != wa * R) ? 1 : 0;
+    const float* p = a.partials + static_cast<int64_t>(w * 2 + slot) * C::PSTRIDE + C::NKC * 128;
+    M0 = fmaxf(M0, __ldcg(p + h0));
+    M1 = fmaxf(M1, __ldcg(p + h0 + 1));
+  }
+  float L0 = 0.f, L1 = 0.f;
+  float4 acc[C::NKC];
+#pragma unroll
+  for (int c = 0; c < C::NKC; ++c) acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int w = wa; w <= wb; ++w) {
+    const int slot = (w == wa && pbeg != wa * R) ? 1 : 0;
+    const float* p = a.partials + static_cast<int64_t>(w * 2 + slot) * C::PSTRIDE;
+    const float e0 = exp2f(__ldcg(p + C::NKC * 128 + h0) - M0);
+    const float e1 = exp2f(__ldcg(p + C::NKC * 128 + h0 + 1) - M1);
+    L0 += __ldcg(p + C::NKC * 128 + GPAD + h0) * e0;
+    L1 += __ldcg(p + C::NKC * 128 + GPAD + h0 + 1) * e1;
+#pragma unroll
+    for (int c = 0; c < C::NKC; ++c) {
+      const float4 v = __ldcg(reinterpret_cast<const float4*>(p) + c * 32 + lane);
+      acc[c].x += v.x * e0;
+      acc[c].y += v.y * e1;
+      acc[c].z += v.z * e0;
+      acc[c].w += v.w * e1;
+    }
+  }
+  const float i0 = 1.f / L0, i1 = 1.f / L1;
+  T* out = static_cast<T*>(a.out) + (static_cast<int64_t>(s) * a.H_q + g * a.G) * D;
+  const int trow = lane >> 2;
+#pragma unroll
+  for (int c = 0; c < C::NKC; ++c) {
+    const int dd = 16 * c + trow;
+    if (h0 < a.G) {
+      out[h0 * D + dd] = from_float<T>(acc[c].x * i0);
+      out[h0 * D + dd + 8] = from_float<T>(acc[c].z * i0);
+    }
+    if (h0 + 1 < a.G) {
+      out[(h0 + 1) * D + dd] = from_float<T>(acc[c].y * i1);
+      out[(h0 + 1) * D + dd + 8] = from_float<T>(acc[c].w * i1);
+    }
+  }
+}
+
 // Descriptor of one tile, built by the warp a batch at a time:
 //   x = TMA row coordinate of the slab, y = pair id (s * H_kv + g),
 //   z = valid tokens | first-of-pair << 8 | last-of-pair << 9 | new-pair-in-range << 10.
@@ -175,12 +262,6 @@ __global__ void __launch_bounds__(NW * 32) decode_tc_kernel(const __grid_constan
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int gw = blockIdx.x * NW + warp;
-  const int total = a.hdr[0];
-  const int R = (total + a.total_warps - 1) / a.total_warps;
-  const int my_start = gw * R;
-  const int my_end = min(total, my_start + R);
-  if (my_start >= my_end) return;  // the whole warp leaves; no block-level barriers are used
-  const int n_my = my_end - my_start;
 
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* region = base + warp * SM::WARP_STRIDE;
@@ -194,22 +275,19 @@ __global__ void __launch_bounds__(NW * 32) decode_tc_kernel(const __grid_constan
   }
   __syncwarp();
 
-  // ---- tile walk state: (sequence, KV head, tile within pair, tiles of the pair)
+  // everything above overlaps the plan kernel; its outputs are read from here on
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int total = a.hdr[0];
+  const int R = (total + a.total_warps - 1) / a.total_warps;
+  const int my_start = gw * R;
+  const int my_end = min(total, my_start + R);
+  if (my_start >= my_end) return;  // the whole warp leaves; no block-level barriers are used
+  const int n_my = my_end - my_start;
+
+  // ---- tile walk state: (sequence, KV head, tile within pair, tiles of the pair), from the plan
   const int32_t* Q = a.tile_prefix;
-  int cs, ch, cj, cn;
-  {
-    // sequence containing tile my_start: largest s with H_kv * Q[s] <= my_start
-    int lo = 0, hi = a.n_seq - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (a.H_kv * Q[mid] <= my_start) lo = mid; else hi = mid - 1;
-    }
-    cs = lo;  // non-empty: H_kv * Q[lo] <= my_start < H_kv * Q[lo + 1]
-    cn = Q[cs + 1] - Q[cs];
-    const int within = my_start - a.H_kv * Q[cs];
-    ch = within / cn;
-    cj = within - ch * cn;
-  }
+  const int4 w0 = a.wstart[gw];
+  int cs = w0.x, ch = w0.y, cj = w0.z, cn = w0.w;
 
   // Fill descriptors for range tiles [t0, t0 + 32) into ring slots (t & 63).
   auto fill = [&](int t0) {
@@ -429,60 +507,22 @@ __global__ void __launch_bounds__(NW * 32) decode_tc_kernel(const __grid_constan
           ps[C::NKC * 128 + GPAD + h0] = L0;
           ps[C::NKC * 128 + GPAD + h0 + 1] = L1;
         }
+        // the warp that writes a split pair's last partial merges it ("Chunked prefill
+        // mechanics" rule): publish, count, and let the last arrival read everyone's
+        __threadfence();
+        __syncwarp();
+        int arrived = 0;
+        if (lane == 0) arrived = atomicAdd(&a.counters[cur_pair], 1);
+        arrived = __shfl_sync(0xffffffffu, arrived, 0);
+        const int nt = Q[s + 1] - Q[s];
+        const int pbeg = a.H_kv * Q[s] + g * nt;
+        const int wa = pbeg / R, wb = (pbeg + nt - 1) / R;
+        if (arrived == wb - wa) {
+          __threadfence();
+          merge_pair<T, D>(a, s, g, pbeg, wa, wb, R, lane);
+        }
       }
     }
-  }
-}
-
-// Merge the partials of pairs split across warps; zero the outputs of empty sequences.
-template <typename T, int D>
-__global__ void __launch_bounds__(D * 2) merge_tc_kernel(const DecodeArgs a) {
-  using C = TcCfg<D>;
-  const int pair = blockIdx.x;
-  const int s = pair / a.H_kv, g = pair - (pair / a.H_kv) * a.H_kv;
-  const int nt = a.tile_prefix[s + 1] - a.tile_prefix[s];
-  T* out = static_cast<T*>(a.out) + (static_cast<int64_t>(s) * a.H_q + g * a.G) * D;
-  if (nt == 0) {
-    for (int k = threadIdx.x; k < a.G * D; k += blockDim.x) out[k] = from_float<T>(0.f);
-    return;
-  }
-  const int total = a.hdr[0];
-  const int R = (total + a.total_warps - 1) / a.total_warps;
-  const int ps = a.H_kv * a.tile_prefix[s] + g * nt, pe = ps + nt;
-  const int wa = ps / R, wb = (pe - 1) / R;
-  if (wa == wb) return;  // written whole by one warp
-  const int f = threadIdx.x;   // float4 index: chunk c = f / 32, lane = f % 32
-  const int lane = f & 31, c = f >> 5;
-  const int h0 = 2 * (lane & 3);
-  float M0 = -INFINITY, M1 = -INFINITY;
-  for (int w = wa; w <= wb; ++w) {
-    const int slot = (w == wa && ps != wa * R) ? 1 : 0;
-    const float* p = a.partials + static_cast<int64_t>(w * 2 + slot) * C::PSTRIDE + C::NKC * 128;
-    M0 = fmaxf(M0, p[h0]);
-    M1 = fmaxf(M1, p[h0 + 1]);
-  }
-  float L0 = 0.f, L1 = 0.f;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int w = wa; w <= wb; ++w) {
-    const int slot = (w == wa && ps != wa * R) ? 1 : 0;
-    const float* p = a.partials + static_cast<int64_t>(w * 2 + slot) * C::PSTRIDE;
-    const float e0 = exp2f(p[C::NKC * 128 + h0] - M0), e1 = exp2f(p[C::NKC * 128 + h0 + 1] - M1);
-    L0 += p[C::NKC * 128 + GPAD + h0] * e0;
-    L1 += p[C::NKC * 128 + GPAD + h0 + 1] * e1;
-    const float4 v = reinterpret_cast<const float4*>(p)[f];
-    acc.x += v.x * e0;
-    acc.y += v.y * e1;
-    acc.z += v.z * e0;
-    acc.w += v.w * e1;
-  }
-  const int dd = 16 * c + (lane >> 2);
-  if (h0 < a.G) {
-    out[h0 * D + dd] = from_float<T>(acc.x / L0);
-    out[h0 * D + dd + 8] = from_float<T>(acc.z / L0);
-  }
-  if (h0 + 1 < a.G) {
-    out[(h0 + 1) * D + dd] = from_float<T>(acc.y / L1);
-    out[(h0 + 1) * D + dd + 8] = from_float<T>(acc.w / L1);
   }
 }
 
@@ -719,17 +759,44 @@ int tc_grid(const Pool& P, int* grid, int* warps, int* smem) {
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct WsLayout {
-  size_t prefix, lens, partials, total;
+  size_t prefix, lens, counters, wstart, partials, total;
 };
 
-WsLayout ws_layout(int n_seq, int64_t total_warps, int D) {
+WsLayout ws_layout(int n_seq, int H_kv, int64_t total_warps, int D) {
   WsLayout w;
   w.prefix = kHdrBytes;
   w.lens = w.prefix + align256(sizeof(int32_t) * (n_seq + 1));
-  w.partials = w.lens + align256(sizeof(int32_t) * n_seq);
+  w.counters = w.lens + align256(sizeof(int32_t) * n_seq);
+  w.wstart = w.counters + align256(sizeof(int32_t) * static_cast<size_t>(n_seq) * H_kv);
+  w.partials = w.wstart + align256(sizeof(int4) * total_warps);
   const int pstride = (D / 16) * 32 * 4 + 2 * GPAD;
   w.total = w.partials + align256(sizeof(float) * total_warps * 2 * pstride);
   return w;
+}
+
+// plan_kernel, then the attention kernel as a programmatic dependent launch: its
+// CTAs become resident and initialise their barriers while the plan kernel runs,
+// and wait (griddepcontrol.wait) before reading the plan's outputs.
+int launch_tc_sequence(DecodeArgs& a, CUtensorMap* maps, KernelPtr k, int grid, int nw, int smem,
+                       cudaStream_t st) {
+  plan_kernel<<<1, 1024, 0, st>>>(a);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(PKV_ERR_CUDA, std::string("plan launch: ") + cudaGetErrorString(e));
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(nw * 32);
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  void* args[] = {&maps[0], &maps[1], &a};
+  e = cudaLaunchKernelExC(&cfg, k, args);
+  if (e != cudaSuccess) return fail(PKV_ERR_CUDA, std::string("decode launch: ") + cudaGetErrorString(e));
+  count_launch(2);
+  return PKV_OK;
 }
 
 }  // namespace
@@ -795,7 +862,7 @@ int decode_workspace_bytes(const Pool& P, int32_t n_seq, size_t* bytes) {
     if (int rc = tc_grid(P, &grid, &nw, &smem)) return rc;
     warps_total = static_cast<int64_t>(grid) * nw;
   }
-  *bytes = ws_layout(n_seq, warps_total, P.geo.d_head).total;
+  *bytes = ws_layout(n_seq, P.geo.H_kv, warps_total, P.geo.d_head).total;
   return PKV_OK;
 }
 
@@ -828,12 +895,14 @@ int launch_decode(Pool& P, int32_t layer, const void* q, const void* k_pool, con
   a.L = g.L;
   a.layer = layer;
   a.B = g.block_size;
+  a.D = g.d_head;
+  a.elem = static_cast<int32_t>(elem_size(g.dtype));
   a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
 
   if (tc_eligible(P)) {
     int grid = 0, nw = 0, smem = 0;
     if (int rc = tc_grid(P, &grid, &nw, &smem)) return rc;
-    const WsLayout L = ws_layout(n_seq, static_cast<int64_t>(grid) * nw, g.d_head);
+    const WsLayout L = ws_layout(n_seq, g.H_kv, static_cast<int64_t>(grid) * nw, g.d_head);
     if (ws_bytes < L.total) return fail(PKV_ERR_INVALID_ARG, "workspace too small: need " + std::to_string(L.total));
     if ((reinterpret_cast<uintptr_t>(q) & 15)) return fail(PKV_ERR_INVALID_ARG, "q must be 16-byte aligned");
     CUtensorMap tk, tv;
@@ -842,26 +911,12 @@ int launch_decode(Pool& P, int32_t layer, const void* q, const void* k_pool, con
     a.hdr = reinterpret_cast<int32_t*>(w);
     a.tile_prefix = reinterpret_cast<int32_t*>(w + L.prefix);
     a.lens_c = reinterpret_cast<int32_t*>(w + L.lens);
+    a.counters = reinterpret_cast<int32_t*>(w + L.counters);
+    a.wstart = reinterpret_cast<int4*>(w + L.wstart);
     a.partials = reinterpret_cast<float*>(w + L.partials);
     a.total_warps = grid * nw;
-    plan_kernel<<<1, 1024, 0, st>>>(a);
-    KernelPtr k = tc_kernel_for(P, &smem);
-    void* args[] = {&tk, &tv, &a};
-    cudaError_t e = cudaLaunchKernel(k, dim3(grid), dim3(nw * 32), args, static_cast<size_t>(smem), st);
-    if (e != cudaSuccess) return fail(PKV_ERR_CUDA, std::string("decode launch: ") + cudaGetErrorString(e));
-    const bool bf = g.dtype == PKV_BF16;
-    const int pairs = n_seq * g.H_kv;
-    if (g.d_head == 128) {
-      if (bf) merge_tc_kernel<__nv_bfloat16, 128><<<pairs, 256, 0, st>>>(a);
-      else merge_tc_kernel<__half, 128><<<pairs, 256, 0, st>>>(a);
-    } else {
-      if (bf) merge_tc_kernel<__nv_bfloat16, 64><<<pairs, 128, 0, st>>>(a);
-      else merge_tc_kernel<__half, 64><<<pairs, 128, 0, st>>>(a);
-    }
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return fail(PKV_ERR_CUDA, std::string("decode launch: ") + cudaGetErrorString(e));
-    count_launch(3);
-    return PKV_OK;
+    CUtensorMap maps[2] = {tk, tv};
+    return launch_tc_sequence(a, maps, tc_kernel_for(P, &smem), grid, nw, smem, st);
   }
 
   // CUDA-core path
@@ -977,6 +1032,8 @@ extern "C" int pkv_decode_attention_noalloc(const pkv_pool* pool, int32_t layer,
   a.L = g.L;
   a.layer = layer;
   a.B = g.block_size;
+  a.D = g.d_head;
+  a.elem = static_cast<int32_t>(elem_size(g.dtype));
   a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
 
   if (!tc_eligible(P)) {
@@ -1026,7 +1083,7 @@ extern "C" int pkv_decode_attention_noalloc(const pkv_pool* pool, int32_t layer,
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess || per_sm < 1) return fail(PKV_ERR_CUDA, std::string("grid query: ") + cudaGetErrorString(e));
   const int grid = per_sm * sms;
-  const WsLayout L = ws_layout(n_seq, static_cast<int64_t>(grid) * nw, g.d_head);
+  const WsLayout L = ws_layout(n_seq, g.H_kv, static_cast<int64_t>(grid) * nw, g.d_head);
   if (L.total > kNoallocScratchBytes)
     return fail(PKV_ERR_INVALID_ARG, "pkv_decode_attention_noalloc: this batch needs " + std::to_string(L.total) +
                                          " bytes of scratch, more than the static " +
@@ -1052,30 +1109,16 @@ extern "C" int pkv_decode_attention_noalloc(const pkv_pool* pool, int32_t layer,
                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled failed: " + std::to_string(r));
   }
-  // every field the kernels read is written by the plan kernel (header, prefix,
-  // clamped lengths) or by the attention kernel (partials) earlier in this call,
-  // so nothing in the scratch has to start at zero
+  // every field the kernels read is written earlier in the same call: the plan
+  // kernel writes the header, prefix, clamped lengths, warp starts and zeroes the
+  // split-pair counters; the attention kernel writes a partial before counting it
   char* w = static_cast<char*>(ws);
   a.hdr = reinterpret_cast<int32_t*>(w);
   a.tile_prefix = reinterpret_cast<int32_t*>(w + L.prefix);
   a.lens_c = reinterpret_cast<int32_t*>(w + L.lens);
+  a.counters = reinterpret_cast<int32_t*>(w + L.counters);
+  a.wstart = reinterpret_cast<int4*>(w + L.wstart);
   a.partials = reinterpret_cast<float*>(w + L.partials);
   a.total_warps = grid * nw;
-  plan_kernel<<<1, 1024, 0, st>>>(a);
-  void* args[] = {&maps[0], &maps[1], &a};
-  e = cudaLaunchKernel(k, dim3(grid), dim3(nw * 32), args, static_cast<size_t>(smem), st);
-  if (e != cudaSuccess) return fail(PKV_ERR_CUDA, std::string("decode launch: ") + cudaGetErrorString(e));
-  const bool bf = g.dtype == PKV_BF16;
-  const int pairs = n_seq * g.H_kv;
-  if (g.d_head == 128) {
-    if (bf) merge_tc_kernel<__nv_bfloat16, 128><<<pairs, 256, 0, st>>>(a);
-    else merge_tc_kernel<__half, 128><<<pairs, 256, 0, st>>>(a);
-  } else {
-    if (bf) merge_tc_kernel<__nv_bfloat16, 64><<<pairs, 128, 0, st>>>(a);
-    else merge_tc_kernel<__half, 64><<<pairs, 128, 0, st>>>(a);
-  }
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return fail(PKV_ERR_CUDA, std::string("decode launch: ") + cudaGetErrorString(e));
-  count_launch(3);
-  return PKV_OK;
+  return launch_tc_sequence(a, maps, k, grid, nw, smem, st);
 }

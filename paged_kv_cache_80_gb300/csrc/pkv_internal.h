@@ -37,6 +37,7 @@ class FreeRing {
 struct SeqState {
   std::vector<int32_t> table;       // logical block -> physical block
   int64_t len = 0;                  // tokens written
+  uint8_t state = 0;                // 0 live, 1 released
   bool swapped = false;             // blocks live in host frames
   std::vector<int64_t> host_frames; // frames holding the blocks while swapped
 };
@@ -50,8 +51,12 @@ struct Pool {
   int64_t block_bytes = 0;  // block_elems * element size
   FreeRing free;
   std::vector<int32_t> ref;
-  std::unordered_map<int32_t, SeqState> seqs;
-  std::vector<uint8_t> released;  // by seq id: 1 once freed
+  // Sequence ids are 0, 1, 2, ... and never reused, so states are indexed by id;
+  // a released sequence keeps an empty state marked released.
+  std::vector<SeqState> seqs;
+  std::vector<int32_t> dropped;  // per block: owners given up by earlier CoWs of one append (dry run)
+  std::vector<int32_t> order;    // scratch: request order of one append
+  std::vector<int64_t> first_tok;  // scratch: caller offsets of one append
   int32_t next_id = 0;
   int32_t swap_engine = 0;  // 0 SM kernel, 1 copy engine
 

@@ -1,0 +1,74 @@
+"""pkv_decode_step (plan + CoW copy + append + attend in one call) against the oracle."""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+import paged_kv_cache_80_gb300 as pkv
+import workloads as W
+from helpers import PagedBatch, check_attention, out_f64, to_dev, to_raw, torch_dtype
+
+pytestmark = pytest.mark.gpu
+
+
+def test_decode_step_matches_oracle_with_forks():
+    import torch
+
+    g = W.Geometry(L=2, H_q=32, H_kv=4, d_head=128, block_size=16, dtype="bf16", num_blocks=512)
+    b = PagedBatch(g, W.permutation(41, "fo", g.num_blocks), seed=41)
+    ids = b.new_seqs(6)
+    b.append(ids, [1, 16, 40, 300, 0, 77], "prompt", layer=-1)
+    kids = [b.fork(ids[2]), b.fork(ids[3])]  # the first step copies their shared tail blocks
+    run = np.array(ids[:4] + kids + [ids[5]], np.int32)
+    n, Wd = len(run), 24
+    meta_host = torch.zeros(n * (Wd + 2), dtype=torch.int32).pin_memory()
+    meta_dev = torch.zeros(n * (Wd + 2), dtype=torch.int32, device="cuda")
+    ws = torch.empty(pkv.pkv_decode_workspace_size(b.lib, n), dtype=torch.uint8, device="cuda")
+    scale = 1.0 / math.sqrt(g.d_head)
+    for step in range(3):
+        for layer in (0, 1):
+            q = W.normal(41, f"q{step}{layer}", (n, g.H_q, g.d_head), "bf16")
+            kn = W.normal(41, f"k{step}{layer}", (n, g.H_kv, g.d_head), "bf16")
+            vn = W.normal(41, f"v{step}{layer}", (n, g.H_kv, g.d_head), "bf16")
+            out = torch.full((n, g.H_q, g.d_head), float("nan"), dtype=torch.bfloat16, device="cuda")
+            if layer == 0:
+                pkv.pkv_decode_step(b.lib, 0, run, Wd, to_dev(q, "bf16"), to_dev(kn, "bf16"), to_dev(vn, "bf16"),
+                                    b.kp, b.vp, scale, out, meta_host, meta_dev, ws)
+                oslots, ocows = b.orc.append(run.tolist(), [1] * n)
+                if len(ocows):
+                    oracle.copy_blocks(g, ocows, b.hk, b.hv)
+                assert np.array_equal(meta_host[:n].numpy(), oslots)
+            else:
+                # a second layer of the same step: the slots are already planned
+                pkv.pkv_append_kv(b.lib, 1, to_dev(kn, "bf16"), to_dev(vn, "bf16"), meta_dev[:n], b.kp, b.vp)
+                tables = meta_dev[n:n + n * Wd].view(n, Wd)
+                lens = meta_dev[n + n * Wd:n + n * Wd + n]
+                pkv.pkv_decode_attention(b.lib, 1, to_dev(q, "bf16"), b.kp, b.vp, tables, lens, scale, out, ws)
+            oracle.write_slots(g, layer, kn, vn, oslots, b.hk, b.hv)
+            pkv.pkv_check_device_error()
+            tables, lens = b.tables(run.tolist(), Wd)
+            ref = b.decode_ref(q, tables, lens, scale, layer=layer)
+            check_attention(out_f64(out, "bf16"), ref, "bf16")
+        b.check_state()
+    b.check_pools_bitexact()
+
+
+def test_decode_step_rejects_a_narrow_table_without_change():
+    import torch
+
+    g = W.Geometry(L=1, H_q=8, H_kv=2, d_head=64, block_size=16, dtype="bf16", num_blocks=64)
+    b = PagedBatch(g, None, seed=42)
+    ids = b.new_seqs(2)
+    b.append(ids, [32, 3], "p")
+    before = (pkv.pkv_refcounts(b.lib).copy(), pkv.pkv_free_list(b.lib).copy())
+    meta_host = torch.zeros(2 * 4, dtype=torch.int32).pin_memory()
+    meta_dev = torch.zeros(2 * 4, dtype=torch.int32, device="cuda")
+    ws = torch.empty(pkv.pkv_decode_workspace_size(b.lib, 2), dtype=torch.uint8, device="cuda")
+    x = torch.zeros((2, 8, 64), dtype=torch.bfloat16, device="cuda")
+    kv = torch.zeros((2, 2, 64), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(pkv.PkvError) as e:  # W = 2 cannot hold 33 tokens
+        pkv.pkv_decode_step(b.lib, 0, ids, 2, x, kv, kv, b.kp, b.vp, 0.1, x, meta_host, meta_dev, ws)
+    assert e.value.name == "PKV_ERR_INVALID_ARG"
+    assert np.array_equal(before[0], pkv.pkv_refcounts(b.lib)) and np.array_equal(before[1], pkv.pkv_free_list(b.lib))
+    assert pkv.pkv_seq_len(b.lib, ids[0]) == 32
