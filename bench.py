@@ -42,6 +42,22 @@ sys.path.insert(0, ROOT)
 import workloads as W  # noqa: E402
 
 METRIC = "paged decode attention KV GB/s & tokens/s (% of 8 TB/s HBM); swap GB/s vs host link"
+
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per algorithmic byte
+# of the decode call, from an ncu capture of the kernels built from the sources
+# with this digest (summary in profiles/).  Reported only while the sources match.
+TRAFFIC_RECORD = {"sources_sha256": "047a427e88ba5f0a3f31ba90c0a134a7f22cc1da8de6e532bad7ff0dc6ec40af",
+                  "ratio": 1.0114}  # 817.14 MB DRAM / 807.91 MB algorithmic, agent 48 x 4,096 capture
+
+
+def decode_sources_digest() -> str:
+    import hashlib
+
+    h = hashlib.sha256()
+    for f in ("pkv_decode.cu", "pkv_device.cuh"):
+        with open(os.path.join(ROOT, "paged_kv_cache_80_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
 NOMINAL_HBM_GBS = 8000.0
 
 
@@ -554,6 +570,9 @@ def run_decode(args, torch, pkv, dev, world, rank):
 
     peak, peak_kind = load_peaks()
     value = world * kv_total / (ms_max / 1e3) / 1e9
+    traffic = args.traffic
+    if traffic is None and TRAFFIC_RECORD["ratio"] and TRAFFIC_RECORD["sources_sha256"] == decode_sources_digest():
+        traffic = round(TRAFFIC_RECORD["ratio"] * alg_avg)
     achieved = alg_avg / (dec_avg / 1e3) / 1e9
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -562,7 +581,7 @@ def run_decode(args, torch, pkv, dev, world, rank):
         "tokens_per_s": round(world * sum(r.tokens[:args.steps]) / (ms_max / 1e3), 1),
         "hbm_frac_of_8tbs": round(value / world / NOMINAL_HBM_GBS, 4),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": args.traffic,
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
                      "kernel": "pkv_decode_attention (plan + stream-K attention + merge)",
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
                      else "fallback 6.8 TB/s",

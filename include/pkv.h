@@ -269,6 +269,14 @@ int pkv_seq_host_slots(const pkv_pool* pool, int32_t seq, int64_t* out, int32_t 
 /* 0 = swap with SM kernels (default), 1 = with cudaMemcpyAsync on the copy engines. */
 int pkv_pool_set_swap_engine(pkv_pool* pool, int32_t engine);
 
+/* Failure-path self-test: launch one warp that waits on an mbarrier nothing will
+ * complete, bounded by timeout_ns (<= 10 s) of the GPU's global timer -- the same
+ * bounded wait the decode kernel uses for its tile loads.  When the bound runs out
+ * the kernel records code 5 (detail = nanoseconds waited) in the device error word
+ * and returns; pkv_check_device_error then reports PKV_ERR_DEVICE_CHECK and the
+ * context stays usable.  No fault, trap or hang is involved. */
+int pkv_selftest_bounded_wait(int64_t timeout_ns, pkv_stream_t stream);
+
 /* Number of kernels this library has launched in this process (all devices). */
 uint64_t pkv_launch_count(void);
 

@@ -23,6 +23,7 @@ __all__ = [
     "pkv_decode_step",
     "pkv_copy_blocks", "pkv_swap_out",
     "pkv_swap_in", "pkv_seq_host_slots", "pkv_pool_set_swap_engine", "pkv_check_device_error", "pkv_launch_count",
+    "pkv_selftest_bounded_wait",
 ]
 
 F32, F16, BF16 = 0, 1, 2
@@ -89,6 +90,7 @@ def _L():
             "pkv_pool_set_swap_engine": ([vp, i32], ctypes.c_int),
             "pkv_check_device_error": ([vp, P32, P64], ctypes.c_int),
             "pkv_launch_count": ([], ctypes.c_uint64),
+            "pkv_selftest_bounded_wait": ([i64, vp], ctypes.c_int),
         }
         for name, (args, res) in sig.items():
             f = getattr(L, name)
@@ -370,6 +372,10 @@ def pkv_swap_in(pool: PoolLike, seq: int, host, host_frames: int, n: int, k_pool
     _check(_L().pkv_swap_in(_h(pool), seq, _host_ptr(host, "host"), host_frames, n, _dev(k_pool, "k_pool"),
                             _dev(v_pool, "v_pool"), _p32(ids), _stream(stream)), "pkv_swap_in")
     return ids[:n]
+
+
+def pkv_selftest_bounded_wait(timeout_ns: int, stream=None) -> None:
+    _check(_L().pkv_selftest_bounded_wait(int(timeout_ns), _stream(stream)), "pkv_selftest_bounded_wait")
 
 
 def pkv_launch_count() -> int:

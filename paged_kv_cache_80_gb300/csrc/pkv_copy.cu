@@ -231,6 +231,39 @@ int launch_copy_images(const void* src_base, void* dst_base, const CopyItem* ite
 
 // ------------------------------------------------------------------ C ABI: device error check
 
+// ------------------------------------------------------------------ failure-path self-test
+
+namespace pkv {
+// One warp waits on an mbarrier that nothing will complete, with the same bounded
+// wait the decode kernel uses; when the bound runs out it records a timeout and
+// returns, leaving the context usable.
+__global__ void selftest_wait_kernel(int* err, uint64_t timeout_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  const uint32_t b = smem_u32(&bar);
+  if (threadIdx.x == 0) {
+    mbar_init(b, 1);
+    fence_barrier_init();
+  }
+  __syncwarp();
+  const uint64_t t0 = global_ns();
+  const bool done = mbar_wait_bounded(b, 0, timeout_ns);
+  if (!done && threadIdx.x == 0) record_error(err, DERR_SELFTEST_TIMEOUT, static_cast<long long>(global_ns() - t0));
+}
+}  // namespace pkv
+
+extern "C" int pkv_selftest_bounded_wait(int64_t timeout_ns, pkv_stream_t stream) {
+  pkv::clear_error();
+  if (timeout_ns <= 0 || timeout_ns > 10000000000ll) return pkv::fail(PKV_ERR_INVALID_ARG, "timeout must be in (0, 10 s]");
+  void* w = nullptr;
+  if (int rc = pkv::device_error_word(&w)) return rc;
+  pkv::selftest_wait_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(static_cast<int*>(w),
+                                                                                   static_cast<uint64_t>(timeout_ns));
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return pkv::fail(PKV_ERR_CUDA, std::string("self-test launch: ") + cudaGetErrorString(e));
+  pkv::count_launch();
+  return PKV_OK;
+}
+
 extern "C" uint64_t pkv_launch_count(void) { return pkv::g_launches.load(std::memory_order_relaxed); }
 
 extern "C" int pkv_check_device_error(pkv_stream_t stream, int32_t* code, int64_t* detail) {

@@ -546,13 +546,18 @@ __device__ __forceinline__ __half f_to<__half>(float x) { return __float2half_rn
 template <>
 __device__ __forceinline__ __nv_bfloat16 f_to<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
 
-constexpr int SIMT_WARPS = 4;
+constexpr int SIMT_WARPS = 8;
 
 // One CTA per (sequence, KV head).  Lane j holds elements j, j+32, ... of the head
-// vector; warp w takes tokens w, w+4, ...; each token's score is a warp reduction.
+// vector.  Warp w takes chunks of TOK consecutive tokens (w*TOK, w*TOK + 8*TOK, ...):
+// it loads all TOK keys and values first (independent loads in flight), then
+// scores them for every query head of the group (warp reductions) and folds them
+// into the running (m, l, O) of each head with one rescale per chunk.  The warps
+// are merged in shared memory at the end.
 template <typename T, int NPL>
 __global__ void __launch_bounds__(SIMT_WARPS * 32) decode_simt_kernel(const DecodeArgs a, const T* __restrict__ kp,
                                                                         const T* __restrict__ vp, int d) {
+  constexpr int TOK = NPL >= 8 ? 2 : (NPL >= 4 ? 4 : 8);
   const int pair = blockIdx.x;
   const int s = pair / a.H_kv, g = pair - (pair / a.H_kv) * a.H_kv;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -572,54 +577,83 @@ __global__ void __launch_bounds__(SIMT_WARPS * 32) decode_simt_kernel(const Deco
 #pragma unroll
     for (int j = 0; j < NPL; ++j) {
       const int e = lane + 32 * j;
-      qv[h][j] = (h < G && e < d) ? to_f(q[h * d + e]) : 0.f;
+      qv[h][j] = (h < G && e < d) ? to_f(q[h * d + e]) * a.scale_log2 : 0.f;
       o[h][j] = 0.f;
     }
   }
-  for (int t = warp; t < len; t += SIMT_WARPS) {
-    int blk = a.tables[static_cast<int64_t>(s) * a.W + t / a.B];
-    if (blk < 0 || blk >= a.num_blocks) {
-      if (lane == 0) record_error(a.err, DERR_DECODE_BLOCK, blk);
-      continue;
-    }
-    const int64_t base = (((static_cast<int64_t>(blk) * a.L + a.layer) * a.H_kv + g) * a.B + t % a.B) * d;
-    float k[NPL], v[NPL];
+  for (int t0 = warp * TOK; t0 < len; t0 += SIMT_WARPS * TOK) {
+    float k[TOK][NPL], v[TOK][NPL];
+    bool ok[TOK];
 #pragma unroll
-    for (int j = 0; j < NPL; ++j) {
-      const int e = lane + 32 * j;
-      k[j] = e < d ? to_f(kp[base + e]) : 0.f;
-      v[j] = e < d ? to_f(vp[base + e]) : 0.f;
+    for (int u = 0; u < TOK; ++u) {
+      const int t = t0 + u;
+      ok[u] = t < len;
+      int64_t base = 0;
+      if (ok[u]) {
+        int blk = a.tables[static_cast<int64_t>(s) * a.W + t / a.B];
+        if (blk < 0 || blk >= a.num_blocks) {
+          if (lane == 0) record_error(a.err, DERR_DECODE_BLOCK, blk);
+          ok[u] = false;
+        } else {
+          base = (((static_cast<int64_t>(blk) * a.L + a.layer) * a.H_kv + g) * a.B + t % a.B) * d;
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < NPL; ++j) {
+        const int e = lane + 32 * j;
+        k[u][j] = (ok[u] && e < d) ? to_f(kp[base + e]) : 0.f;
+        v[u][j] = (ok[u] && e < d) ? to_f(vp[base + e]) : 0.f;
+      }
     }
 #pragma unroll
     for (int h = 0; h < GPAD; ++h) {
       if (h >= G) break;
-      float dot = 0.f;
+      float sc[TOK];
 #pragma unroll
-      for (int j = 0; j < NPL; ++j) dot = fmaf(qv[h][j], k[j], dot);
+      for (int u = 0; u < TOK; ++u) {
+        float dot = 0.f;
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
-      const float sc = dot * a.scale_log2;
-      const float mn = fmaxf(m[h], sc);
-      const float corr = exp2f(m[h] - mn), p = exp2f(sc - mn);
-      l[h] = l[h] * corr + p;
+        for (int j = 0; j < NPL; ++j) dot = fmaf(qv[h][j], k[u][j], dot);
+        sc[u] = dot;
+      }
 #pragma unroll
-      for (int j = 0; j < NPL; ++j) o[h][j] = fmaf(p, v[j], o[h][j] * corr);
-      m[h] = mn;
+      for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+        for (int u = 0; u < TOK; ++u) sc[u] += __shfl_xor_sync(0xffffffffu, sc[u], off);
+      float mx = m[h];
+#pragma unroll
+      for (int u = 0; u < TOK; ++u)
+        if (ok[u]) mx = fmaxf(mx, sc[u]);
+      const float corr = exp2f(m[h] - mx);
+      float psum = 0.f;
+#pragma unroll
+      for (int j = 0; j < NPL; ++j) o[h][j] *= corr;
+#pragma unroll
+      for (int u = 0; u < TOK; ++u) {
+        const float p = ok[u] ? exp2f(sc[u] - mx) : 0.f;
+        psum += p;
+#pragma unroll
+        for (int j = 0; j < NPL; ++j) o[h][j] = fmaf(p, v[u][j], o[h][j]);
+      }
+      l[h] = l[h] * corr + psum;
+      m[h] = mx;
     }
   }
   // merge the warps: smem [warp][head] (m, l) and [warp][head][d]
   extern __shared__ float sm[];
-  float* sml = sm;                                 // SIMT_WARPS * GPAD * 2
-  float* so = sm + SIMT_WARPS * GPAD * 2;          // SIMT_WARPS * GPAD * d
-  for (int h = 0; h < G; ++h) {
+  float* sml = sm;                          // SIMT_WARPS * G * 2
+  float* so = sm + SIMT_WARPS * G * 2;      // SIMT_WARPS * G * d
+#pragma unroll
+  for (int h = 0; h < GPAD; ++h) {
+    if (h >= G) break;
     if (lane == 0) {
-      sml[(warp * GPAD + h) * 2] = m[h];
-      sml[(warp * GPAD + h) * 2 + 1] = l[h];
+      sml[(warp * G + h) * 2] = m[h];
+      sml[(warp * G + h) * 2 + 1] = l[h];
     }
 #pragma unroll
     for (int j = 0; j < NPL; ++j) {
       const int e = lane + 32 * j;
-      if (e < d) so[(warp * GPAD + h) * d + e] = o[h][j];
+      if (e < d) so[(warp * G + h) * d + e] = o[h][j];
     }
   }
   __syncthreads();
@@ -627,15 +661,15 @@ __global__ void __launch_bounds__(SIMT_WARPS * 32) decode_simt_kernel(const Deco
   for (int k = threadIdx.x; k < G * d; k += blockDim.x) {
     const int h = k / d, e = k - h * d;
     float M = -INFINITY;
-    for (int w = 0; w < SIMT_WARPS; ++w) M = fmaxf(M, sml[(w * GPAD + h) * 2]);
+    for (int w = 0; w < SIMT_WARPS; ++w) M = fmaxf(M, sml[(w * G + h) * 2]);
     float L = 0.f, acc = 0.f;
     if (M != -INFINITY) {
       for (int w = 0; w < SIMT_WARPS; ++w) {
-        const float mw = sml[(w * GPAD + h) * 2];
+        const float mw = sml[(w * G + h) * 2];
         if (mw == -INFINITY) continue;
         const float e2 = exp2f(mw - M);
-        L += sml[(w * GPAD + h) * 2 + 1] * e2;
-        acc += so[(w * GPAD + h) * d + e] * e2;
+        L += sml[(w * G + h) * 2 + 1] * e2;
+        acc += so[(w * G + h) * d + e] * e2;
       }
     }
     out[h * d + e] = f_to<T>(L > 0.f ? acc / L : 0.f);
@@ -922,7 +956,7 @@ int launch_decode(Pool& P, int32_t layer, const void* q, const void* k_pool, con
   // CUDA-core path
   const int d = g.d_head;
   const int npl = (d + 31) / 32;
-  const size_t smem = sizeof(float) * (SIMT_WARPS * GPAD * 2 + SIMT_WARPS * GPAD * d);
+  const size_t smem = sizeof(float) * (SIMT_WARPS * G * 2 + SIMT_WARPS * G * static_cast<size_t>(d));
   const int pairs = n_seq * g.H_kv;
   cudaError_t e = cudaSuccess;
 #define PKV_SIMT(TYPE, NPL)                                                                          \
@@ -1039,7 +1073,7 @@ extern "C" int pkv_decode_attention_noalloc(const pkv_pool* pool, int32_t layer,
   if (!tc_eligible(P)) {
     // the CUDA-core kernel needs no scratch at all
     const int d = g.d_head;
-    const size_t smem = sizeof(float) * (SIMT_WARPS * GPAD * 2 + SIMT_WARPS * GPAD * d);
+    const size_t smem = sizeof(float) * (SIMT_WARPS * G * 2 + SIMT_WARPS * G * static_cast<size_t>(d));
     const int pairs = n_seq * g.H_kv;
     const int npl = (d + 31) / 32;
 #define PKV_NA_SIMT(TYPE, NPL)                                                                       \

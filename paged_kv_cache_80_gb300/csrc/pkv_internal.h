@@ -101,6 +101,7 @@ enum DeviceErr : int32_t {
   DERR_DECODE_LEN = 2,      // seq_len < 0 or > W * B
   DERR_DECODE_BLOCK = 3,    // block id out of range in a table
   DERR_DECODE_TIMEOUT = 4,  // a bounded mbarrier wait gave up
+  DERR_SELFTEST_TIMEOUT = 5,  // the self-test's wait gave up (expected)
 };
 
 }  // namespace pkv
