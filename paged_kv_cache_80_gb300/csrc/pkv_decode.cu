@@ -55,6 +55,7 @@ namespace {
 constexpr int TILE = 16;   // tokens per tile (the mma M dimension)
 constexpr int GPAD = 8;    // query heads per mma N dimension
 constexpr int kHdrBytes = 256;
+constexpr int kPlanSmemInts = 8192;  // prefix entries the plan kernel keeps in shared memory
 constexpr uint64_t kWaitNs = 2000000000ull;  // a tile load that takes 2 s is a fault: give up
 
 struct DecodeArgs {
@@ -136,6 +137,13 @@ __global__ void __launch_bounds__(1024) plan_kernel(const DecodeArgs a) {
         reinterpret_cast<int4*>(static_cast<char*>(a.out) + static_cast<int64_t>(s) * row16 * 16)[k] =
             make_int4(0, 0, 0, 0);
   __syncthreads();  // the prefix array is complete (global writes of this block are visible)
+  // the prefix in shared memory for the searches below, when it fits
+  extern __shared__ int32_t q_smem[];
+  const bool in_smem = a.n_seq + 1 <= kPlanSmemInts;
+  if (in_smem)
+    for (int k = tid; k <= a.n_seq; k += blockDim.x) q_smem[k] = a.tile_prefix[k];
+  __syncthreads();
+  const int32_t* Qp = in_smem ? q_smem : a.tile_prefix;
   // each warp's first tile: sequence s (largest with H_kv*Q[s] <= start), KV head, tile, tiles of pair
   const int total = run_total_from(a);
   const int R = (total + a.total_warps - 1) / a.total_warps;
@@ -148,10 +156,10 @@ __global__ void __launch_bounds__(1024) plan_kernel(const DecodeArgs a) {
     int lo = 0, hi = a.n_seq - 1;
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
-      if (a.H_kv * a.tile_prefix[mid] <= start) lo = mid; else hi = mid - 1;
+      if (a.H_kv * Qp[mid] <= start) lo = mid; else hi = mid - 1;
     }
-    const int nt = a.tile_prefix[lo + 1] - a.tile_prefix[lo];
-    const int within = start - a.H_kv * a.tile_prefix[lo];
+    const int nt = Qp[lo + 1] - Qp[lo];
+    const int within = start - a.H_kv * Qp[lo];
     a.wstart[w] = make_int4(lo, within / nt, within - (within / nt) * nt, nt);
   }
 }
@@ -202,32 +210,41 @@ __device__ __forceinline__ void merge_pair(const DecodeArgs& a, int s, int g, in
                                            int lane) {
   using C = TcCfg<D>;
   const int h0 = 2 * (lane & 3);
-  float M0 = -INFINITY, M1 = -INFINITY;
-  for (int w = wa; w <= wb; ++w) {
-    const int slot = (w == wa && pbeg != wa * R) ? 1 : 0;
-    const float* p = a.partials + static_cast<int64_t>(w * 2 + slot) * C::PSTRIDE + C::NKC * 128;
-    M0 = fmaxf(M0, __ldcg(p + h0));
-    M1 = fmaxf(M1, __ldcg(p + h0 + 1));
-  }
-  float L0 = 0.f, L1 = 0.f;
+  float M0 = -INFINITY, M1 = -INFINITY, L0 = 0.f, L1 = 0.f;
   float4 acc[C::NKC];
 #pragma unroll
   for (int c = 0; c < C::NKC; ++c) acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int w = wa; w <= wb; ++w) {
-    const int slot = (w == wa && pbeg != wa * R) ? 1 : 0;
-    const float* p = a.partials + static_cast<int64_t>(w * 2 + slot) * C::PSTRIDE;
-    const float e0 = exp2f(__ldcg(p + C::NKC * 128 + h0) - M0);
-    const float e1 = exp2f(__ldcg(p + C::NKC * 128 + h0 + 1) - M1);
-    L0 += __ldcg(p + C::NKC * 128 + GPAD + h0) * e0;
-    L1 += __ldcg(p + C::NKC * 128 + GPAD + h0 + 1) * e1;
+  // two contributors per round: all their loads are issued before any use
+  for (int w = wa; w <= wb; w += 2) {
+    const bool two = w + 1 <= wb;
+    const float* p0 = a.partials + static_cast<int64_t>(w * 2 + ((w == wa && pbeg != wa * R) ? 1 : 0)) * C::PSTRIDE;
+    const float* p1 = two ? a.partials + static_cast<int64_t>((w + 1) * 2) * C::PSTRIDE : p0;
+    const float ma0 = __ldcg(p0 + C::NKC * 128 + h0), ma1 = __ldcg(p0 + C::NKC * 128 + h0 + 1);
+    const float la0 = __ldcg(p0 + C::NKC * 128 + GPAD + h0), la1 = __ldcg(p0 + C::NKC * 128 + GPAD + h0 + 1);
+    float mb0 = __ldcg(p1 + C::NKC * 128 + h0), mb1 = __ldcg(p1 + C::NKC * 128 + h0 + 1);
+    const float lb0 = __ldcg(p1 + C::NKC * 128 + GPAD + h0), lb1 = __ldcg(p1 + C::NKC * 128 + GPAD + h0 + 1);
+    float4 va[C::NKC], vb[C::NKC];
 #pragma unroll
     for (int c = 0; c < C::NKC; ++c) {
-      const float4 v = __ldcg(reinterpret_cast<const float4*>(p) + c * 32 + lane);
-      acc[c].x += v.x * e0;
-      acc[c].y += v.y * e1;
-      acc[c].z += v.z * e0;
-      acc[c].w += v.w * e1;
+      va[c] = __ldcg(reinterpret_cast<const float4*>(p0) + c * 32 + lane);
+      vb[c] = __ldcg(reinterpret_cast<const float4*>(p1) + c * 32 + lane);
     }
+    if (!two) mb0 = mb1 = -INFINITY;
+    const float n0 = fmaxf(M0, fmaxf(ma0, mb0)), n1 = fmaxf(M1, fmaxf(ma1, mb1));
+    const float r0 = exp2f(M0 - n0), r1 = exp2f(M1 - n1);
+    const float ea0 = exp2f(ma0 - n0), ea1 = exp2f(ma1 - n1);
+    const float eb0 = two ? exp2f(mb0 - n0) : 0.f, eb1 = two ? exp2f(mb1 - n1) : 0.f;
+    L0 = L0 * r0 + la0 * ea0 + lb0 * eb0;
+    L1 = L1 * r1 + la1 * ea1 + lb1 * eb1;
+#pragma unroll
+    for (int c = 0; c < C::NKC; ++c) {
+      acc[c].x = acc[c].x * r0 + va[c].x * ea0 + vb[c].x * eb0;
+      acc[c].y = acc[c].y * r1 + va[c].y * ea1 + vb[c].y * eb1;
+      acc[c].z = acc[c].z * r0 + va[c].z * ea0 + vb[c].z * eb0;
+      acc[c].w = acc[c].w * r1 + va[c].w * ea1 + vb[c].w * eb1;
+    }
+    M0 = n0;
+    M1 = n1;
   }
   const float i0 = 1.f / L0, i1 = 1.f / L1;
   T* out = static_cast<T*>(a.out) + (static_cast<int64_t>(s) * a.H_q + g * a.G) * D;
@@ -508,11 +525,14 @@ __global__ void __launch_bounds__(NW * 32) decode_tc_kernel(const __grid_constan
           ps[C::NKC * 128 + GPAD + h0 + 1] = L1;
         }
         // the warp that writes a split pair's last partial merges it ("Chunked prefill
-        // mechanics" rule): publish, count, and let the last arrival read everyone's
-        __threadfence();
+        // mechanics" rule): publish (the warp barrier orders every lane's writes before
+        // lane 0's cumulative fence), count, and let the last arrival read everyone's
         __syncwarp();
         int arrived = 0;
-        if (lane == 0) arrived = atomicAdd(&a.counters[cur_pair], 1);
+        if (lane == 0) {
+          __threadfence();
+          arrived = atomicAdd(&a.counters[cur_pair], 1);
+        }
         arrived = __shfl_sync(0xffffffffu, arrived, 0);
         const int nt = Q[s + 1] - Q[s];
         const int pbeg = a.H_kv * Q[s] + g * nt;
@@ -813,7 +833,8 @@ WsLayout ws_layout(int n_seq, int H_kv, int64_t total_warps, int D) {
 // and wait (griddepcontrol.wait) before reading the plan's outputs.
 int launch_tc_sequence(DecodeArgs& a, CUtensorMap* maps, KernelPtr k, int grid, int nw, int smem,
                        cudaStream_t st) {
-  plan_kernel<<<1, 1024, 0, st>>>(a);
+  const size_t plan_smem = a.n_seq + 1 <= kPlanSmemInts ? sizeof(int32_t) * (a.n_seq + 1) : 0;
+  plan_kernel<<<1, 1024, plan_smem, st>>>(a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return fail(PKV_ERR_CUDA, std::string("plan launch: ") + cudaGetErrorString(e));
   cudaLaunchConfig_t cfg = {};
