@@ -46,8 +46,8 @@ METRIC = "paged decode attention KV GB/s & tokens/s (% of 8 TB/s HBM); swap GB/s
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per algorithmic byte
 # of the decode call, from an ncu capture of the kernels built from the sources
 # with this digest (summary in profiles/).  Reported only while the sources match.
-TRAFFIC_RECORD = {"sources_sha256": "047a427e88ba5f0a3f31ba90c0a134a7f22cc1da8de6e532bad7ff0dc6ec40af",
-                  "ratio": 1.0114}  # 817.14 MB DRAM / 807.91 MB algorithmic, agent 48 x 4,096 capture
+TRAFFIC_RECORD = {"sources_sha256": "512a01d8c25f3eb410590f6a29eb77f916efb5f5e7e6dfbd10d708dab58073e6",
+                  "ratio": 1.0110}  # 816.8 MB DRAM / 807.9 MB algorithmic, agent 48 x 4,096 capture
 
 
 def decode_sources_digest() -> str:
