@@ -688,6 +688,108 @@ def run_swap(args, torch, pkv, dev, world, rank):
     return line, None
 
 
+def run_overlap(args, torch, pkv, dev, world, rank):
+    """Reload of paused sequences (copy engines, own stream) overlapped with decode
+    attention of a resident batch (another stream).  Phases: decode alone, reload
+    alone, both at once; hidden = (T_dec + T_swap - T_both) / T_swap."""
+    L, n_res, ctx, n_paused, plen = 8, 32, 8192, 64, 1024
+    seed = W.SEEDS["swap"] + 1
+    blocks_res, blocks_p = n_res * ctx // 16, n_paused * plen // 16
+    N = blocks_res + 2 * blocks_p + 64
+    g = W.Geometry(L=L, H_q=64, H_kv=8, d_head=128, block_size=16, dtype="bf16", num_blocks=N)
+    pool = pkv.pkv_pool_create(g.L, g.H_q, g.H_kv, g.d_head, g.block_size, g.dtype, N,
+                               W.permutation(seed, "overlap_fo", N))
+    pkv.pkv_pool_set_swap_engine(pool, args.swap_engine)
+    res = [pkv.pkv_seq_create(pool) for _ in range(n_res)]
+    pkv.pkv_plan_append(pool, res, [ctx] * n_res)
+    paused = [pkv.pkv_seq_create(pool) for _ in range(n_paused)]
+    pkv.pkv_plan_append(pool, paused, [plen] * n_paused)
+    kp = W.device_normal(seed, "k_pool", g.pool_shape(), g.dtype, dev)
+    vp = W.device_normal(seed, "v_pool", g.pool_shape(), g.dtype, dev)
+    frame = 2 * g.L * g.H_kv * g.block_size * g.d_head * g.elem_bytes
+    per = plen // 16
+    host = torch.empty(blocks_p * frame, dtype=torch.uint8, pin_memory=True)
+    frames = {s: np.arange(i * per, (i + 1) * per, dtype=np.int64) for i, s in enumerate(paused)}
+    Wd = ctx // 16
+    tables, lens = pkv.pkv_export_tables(pool, res, Wd)
+    d_tables, d_lens = torch.from_numpy(tables.copy()).to(dev), torch.from_numpy(lens.copy()).to(dev)
+    q = W.device_normal(seed, "q", (g.L, n_res, g.H_q, g.d_head), g.dtype, dev)
+    out = torch.empty((n_res, g.H_q, g.d_head), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(pkv.pkv_decode_workspace_size(pool, n_res), dtype=torch.uint8, device=dev)
+    s_dec, s_swap = torch.cuda.Stream(), torch.cuda.Stream()
+    scale = 1.0 / math.sqrt(g.d_head)
+
+    def evict():
+        for s_ in paused:
+            pkv.pkv_swap_out(pool, s_, kp, vp, host, blocks_p, frames[s_], stream=s_swap)
+        torch.cuda.synchronize()
+
+    def decode_steps(k):
+        for _ in range(k):
+            for layer in range(g.L):
+                pkv.pkv_decode_attention(pool, layer, q[layer], kp, vp, d_tables, d_lens, scale, out, ws,
+                                         stream=s_dec)
+
+    def reload():
+        for s_ in paused:
+            pkv.pkv_swap_in(pool, s_, host, blocks_p, per, kp, vp, stream=s_swap)
+
+    def timed(fn_dec, fn_swap):
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        torch.cuda.synchronize()
+        ev[0].record(s_dec)
+        s_swap.wait_event(ev[0])
+        if fn_dec:
+            fn_dec()
+        ev[1].record(s_dec)
+        if fn_swap:
+            fn_swap()
+        ev[2].record(s_swap)
+        torch.cuda.synchronize()
+        return ev[0].elapsed_time(ev[1]) / 1e3, ev[0].elapsed_time(ev[2]) / 1e3
+
+    evict()
+    k = args.steps
+    decode_steps(args.warmup)
+    reload()
+    evict()
+    clocks = clock_sampler(torch, dev)
+    clocks.start()
+    l0 = pkv.pkv_launch_count()
+    t_dec, _ = timed(lambda: decode_steps(k), None)
+    _, t_swap = timed(None, reload)
+    evict()
+    t_dec_b, t_swap_b = timed(lambda: decode_steps(k), reload)
+    launches = pkv.pkv_launch_count() - l0
+    clk = clocks.stop()
+    pkv.pkv_check_device_error()
+    t_both = max(t_dec_b, t_swap_b)
+    kv = int(lens.astype(np.int64).sum()) * g.H_kv * g.d_head * 2 * 2 * g.L * k
+    sw = blocks_p * frame
+    peak, _ = load_peaks()
+    hidden = (t_dec + t_swap - t_both) / t_swap
+    return {
+        "metric": METRIC, "value": round(kv / t_dec_b / 1e9, 2), "unit": "GB/s", "n_gpus": world, "steps": k,
+        "warmup": args.warmup, "ms_per_step": round(t_both / k * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "overlap: decode of 32 x 8,192-token sequences over 8 layers on one stream while 64 "
+                               "paused 1,024-token sequences (2.1 GB) reload from pinned host memory on another",
+                   "engine": "copy engines" if args.swap_engine else "SM kernel",
+                   "l2": "inputs larger than L2", "parallelism": "replicas (no collectives)"},
+        "decode_gbs_alone": round(kv / t_dec / 1e9, 1), "decode_gbs_overlapped": round(kv / t_dec_b / 1e9, 1),
+        "swap_in_gbs_alone": round(sw / t_swap / 1e9, 1), "swap_in_gbs_overlapped": round(sw / t_swap_b / 1e9, 1),
+        "hidden_reload_fraction": round(hidden, 3),
+        "ms": {"decode_alone": round(t_dec * 1e3, 3), "reload_alone": round(t_swap * 1e3, 3),
+               "both": round(t_both * 1e3, 3)},
+        "roofline": {"bound": "hbm", "achieved": round(kv / t_dec_b / 1e9, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(kv / t_dec_b / 1e9 / peak, 4), "traffic": None,
+                     "kernel": "pkv_decode_attention while a reload runs"},
+        "e2e": {"value": round(kv / t_dec_b / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": int(sw / k),
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": int(launches), "clocks": clk,
+    }, None
+
+
 # ------------------------------------------------------------------ CPU baseline (the oracle)
 
 
@@ -745,7 +847,7 @@ def reference_arm(args, world, rank):
     if rank != 0:
         return None
     cores = oracle.hardware_threads()
-    if args.workload == "swap":
+    if args.workload in ("swap", "overlap"):
         wl = W.swap(n_chunks=16)
         g = wl.geometry
         nb = 64
@@ -841,7 +943,8 @@ def main():
     ap.add_argument("--steps", type=int, default=None, help="timed steps (default 100; swap 4)")
     ap.add_argument("--warmup", type=int, default=None, help="warm-up steps (default 10; swap 3)")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["agent32k", "chat", "forked", "swap", "tiny"], default="agent32k")
+    ap.add_argument("--workload", choices=["agent32k", "chat", "forked", "swap", "tiny", "overlap"],
+                    default="agent32k")
     ap.add_argument("--swap-engine", type=int, default=0, help="swap workload: 0 SM kernel, 1 copy engines")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--context", type=int, default=0, help="agent workload: tokens per sequence (default 32768)")
@@ -850,7 +953,7 @@ def main():
                     help="ncu dram bytes per decode launch, if captured for this kernel version")
     args = ap.parse_args()
     if args.steps is None:
-        args.steps = 4 if args.workload == "swap" else 100
+        args.steps = {"swap": 4, "overlap": 8}.get(args.workload, 100)
     if args.warmup is None:
         args.warmup = 3 if args.workload == "swap" else 10
     if args.warmup < 3:
@@ -879,6 +982,8 @@ def main():
         dist.init_process_group("nccl", device_id=dev)
     if args.workload == "swap":
         line, runner = run_swap(args, torch, pkv, dev, world, rank)
+    elif args.workload == "overlap":
+        line, runner = run_overlap(args, torch, pkv, dev, world, rank)
     else:
         line, runner = run_decode(args, torch, pkv, dev, world, rank)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -890,6 +995,7 @@ def main():
         else:
             ref = reference_arm(argparse.Namespace(workload="swap", steps=2, warmup=1), 1, 0)
             line["cpu_baseline"] = dict(ref["cpu_baseline"])
+            line["cpu_baseline"]["sample"] += " (host-tier copy baseline)"
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -263,6 +263,15 @@ int pkv_swap_out(pkv_pool* pool, int32_t seq, const void* k_pool, const void* v_
 int pkv_swap_in(pkv_pool* pool, int32_t seq, const void* host, int64_t host_frames, int32_t n, void* k_pool,
                 void* v_pool, int32_t* new_block_ids, pkv_stream_t stream);
 
+/* Residency of a sequence's blocks (the dual-residency table of [KVM] "Asynchronous
+ * paged swapping"): PKV_TIER_HBM while its blocks are in the pool, PKV_TIER_HOST
+ * after pkv_swap_out until pkv_swap_in.  A swap-in may run on its own stream (with
+ * the copy engines, pkv_pool_set_swap_engine(pool, 1), so the SMs stay with
+ * attention) while other sequences decode; record an event after it and make the
+ * stream that decodes the restored sequence wait on that event. */
+enum pkv_tier { PKV_TIER_HBM = 0, PKV_TIER_HOST = 1 };
+int pkv_seq_residency(const pkv_pool* pool, int32_t seq, int32_t* tier);
+
 /* Host frames recorded for a swapped-out sequence: HOST int64 [capacity], *n = count. */
 int pkv_seq_host_slots(const pkv_pool* pool, int32_t seq, int64_t* out, int32_t capacity, int32_t* n);
 

@@ -22,7 +22,7 @@ __all__ = [
     "pkv_append_kv", "pkv_decode_workspace_size", "pkv_decode_attention", "pkv_decode_attention_noalloc",
     "pkv_decode_step",
     "pkv_copy_blocks", "pkv_swap_out",
-    "pkv_swap_in", "pkv_seq_host_slots", "pkv_pool_set_swap_engine", "pkv_check_device_error", "pkv_launch_count",
+    "pkv_swap_in", "pkv_seq_host_slots", "pkv_seq_residency", "TIER_HBM", "TIER_HOST", "pkv_pool_set_swap_engine", "pkv_check_device_error", "pkv_launch_count",
     "pkv_selftest_bounded_wait",
 ]
 
@@ -87,6 +87,7 @@ def _L():
             "pkv_swap_out": ([vp, i32, vp, vp, vp, i64, P64, i32, P32, vp], ctypes.c_int),
             "pkv_swap_in": ([vp, i32, vp, i64, i32, vp, vp, P32, vp], ctypes.c_int),
             "pkv_seq_host_slots": ([vp, i32, P64, i32, P32], ctypes.c_int),
+            "pkv_seq_residency": ([vp, i32, P32], ctypes.c_int),
             "pkv_pool_set_swap_engine": ([vp, i32], ctypes.c_int),
             "pkv_check_device_error": ([vp, P32, P64], ctypes.c_int),
             "pkv_launch_count": ([], ctypes.c_uint64),
@@ -281,6 +282,15 @@ def pkv_free_list(pool: PoolLike) -> np.ndarray:
 
 def pkv_pool_set_swap_engine(pool: PoolLike, engine: int) -> None:
     _check(_L().pkv_pool_set_swap_engine(_h(pool), engine), "pkv_pool_set_swap_engine")
+
+
+TIER_HBM, TIER_HOST = 0, 1
+
+
+def pkv_seq_residency(pool: PoolLike, seq: int) -> int:
+    out = ctypes.c_int32()
+    _check(_L().pkv_seq_residency(_h(pool), seq, ctypes.byref(out)), "pkv_seq_residency")
+    return out.value
 
 
 def pkv_seq_host_slots(pool: PoolLike, seq: int) -> np.ndarray:

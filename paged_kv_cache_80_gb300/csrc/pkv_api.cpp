@@ -532,6 +532,16 @@ int pkv_swap_in(pkv_pool* pool, int32_t seq, const void* host, int64_t host_fram
   return PKV_OK;
 }
 
+int pkv_seq_residency(const pkv_pool* pool, int32_t seq, int32_t* tier) {
+  pkv::clear_error();
+  if (!pool || !tier) return fail(PKV_ERR_INVALID_ARG, "NULL argument");
+  const Pool& P = *as_pool(pool);
+  const SeqState* s = find_seq(P, seq);
+  if (!s) return unknown_seq(P, seq);
+  *tier = s->swapped ? PKV_TIER_HOST : PKV_TIER_HBM;
+  return PKV_OK;
+}
+
 int pkv_seq_host_slots(const pkv_pool* pool, int32_t seq, int64_t* out, int32_t capacity, int32_t* n) {
   pkv::clear_error();
   if (!pool || !n || capacity < 0) return fail(PKV_ERR_INVALID_ARG, "bad arguments");
