@@ -59,6 +59,9 @@ def lib():
         L.orc_decode_attention.argtypes = [ctypes.c_int] * 6 + [i64, ctypes.c_int, vp, vp, vp, P32, ctypes.c_int,
                                                                  P32, ctypes.c_int, dbl, ctypes.POINTER(dbl),
                                                                  ctypes.c_int]
+        L.orc_prefill_attention.argtypes = [ctypes.c_int] * 6 + [i64, ctypes.c_int, vp, P32, vp, vp, P32,
+                                                                  ctypes.c_int, P32, ctypes.c_int, dbl,
+                                                                  ctypes.POINTER(dbl), ctypes.c_int]
         L.orc_hardware_threads.restype = ctypes.c_int
         _lib = L
     return _lib
@@ -224,6 +227,26 @@ def decode_attention(g, layer: int, q: np.ndarray, k_pool: np.ndarray, v_pool: n
                                       _p32(sl), n_seq, float(scale),
                                       out.ctypes.data_as(ctypes.POINTER(ctypes.c_double)), int(n_threads))
     _check(code, "decode_attention")
+    return out
+
+
+def prefill_attention(g, layer: int, q: np.ndarray, q_offsets: np.ndarray, k_pool: np.ndarray,
+                      v_pool: np.ndarray, tables: np.ndarray, seq_lens: np.ndarray, scale: float,
+                      n_threads: int = 0) -> np.ndarray:
+    """Chunked-prefill attention in float64; q is [n_tok][H_q][d] raw storage, the
+    chunk of sequence s is rows q_offsets[s]..q_offsets[s+1] (its last tokens)."""
+    q = np.ascontiguousarray(q)
+    qo = np.ascontiguousarray(q_offsets, dtype=np.int32)
+    tb = np.ascontiguousarray(tables, dtype=np.int32)
+    sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    n_seq = len(sl)
+    W = tb.shape[1] if tb.ndim == 2 else 0
+    out = np.zeros((int(qo[-1]), g.H_q, g.d_head), np.float64)
+    code = lib().orc_prefill_attention(g.L, g.H_q, g.H_kv, g.d_head, g.block_size, DTYPE_CODE[g.dtype],
+                                       g.num_blocks, layer, _vp(q), _p32(qo), _vp(k_pool), _vp(v_pool), _p32(tb), W,
+                                       _p32(sl), n_seq, float(scale),
+                                       out.ctypes.data_as(ctypes.POINTER(ctypes.c_double)), int(n_threads))
+    _check(code, "prefill_attention")
     return out
 
 

@@ -482,6 +482,82 @@ int orc_decode_attention(int L, int H_q, int H_kv, int d, int B, int dtype, int6
   return ORC_OK;
 }
 
+// Chunked-prefill attention [KVM, "Chunked prefill mechanics"]: the queries of
+// chunk k attend to the cached keys of earlier chunks in full and to the keys of
+// their own chunk causally:  O_k = Softmax(Q_k K_<=k^T / sqrt(d) + M_k) V_<=k.
+// Here the chunk of sequence s is its last C_s = q_offsets[s+1] - q_offsets[s]
+// tokens (already written to the pool, so seq_lens[s] counts them); query i of the
+// chunk sits at position P_s + i with P_s = seq_lens[s] - C_s and sees positions
+// t <= P_s + i.  q and out are [n_tok][H_q][d], row q_offsets[s] + i.
+int orc_prefill_attention(int L, int H_q, int H_kv, int d, int B, int dtype, int64_t num_blocks, int layer,
+                          const void* q, const int32_t* q_offsets, const void* k_pool, const void* v_pool,
+                          const int32_t* tables, int W, const int32_t* seq_lens, int n_seq, double scale,
+                          double* out, int n_threads) {
+  if (H_kv <= 0 || H_q % H_kv != 0 || layer < 0 || layer >= L) return ORC_INVALID_ARG;
+  const int G = H_q / H_kv;
+  for (int s = 0; s < n_seq; ++s) {
+    const int64_t C = q_offsets[s + 1] - q_offsets[s];
+    if (C < 0 || seq_lens[s] < C || static_cast<int64_t>(seq_lens[s]) > static_cast<int64_t>(W) * B)
+      return ORC_INVALID_ARG;
+    for (int64_t l = 0; l * B < seq_lens[s]; ++l) {
+      int32_t p = tables[static_cast<int64_t>(s) * W + l];
+      if (p < 0 || p >= num_blocks) return ORC_BAD_BLOCK_ID;
+    }
+  }
+  auto one_pair = [&](int s, int g) {
+    const int64_t len = seq_lens[s];
+    const int64_t C = q_offsets[s + 1] - q_offsets[s];
+    const int64_t P = len - C;
+    std::vector<double> K(len * d), V(len * d);
+    for (int64_t t = 0; t < len; ++t) {
+      int64_t p = tables[static_cast<int64_t>(s) * W + t / B];
+      int64_t base = (((p * L + layer) * H_kv + g) * B + t % B) * d;
+      for (int i = 0; i < d; ++i) {
+        K[t * d + i] = decode(k_pool, base + i, dtype);
+        V[t * d + i] = decode(v_pool, base + i, dtype);
+      }
+    }
+    std::vector<double> z(len), qv(d);
+    for (int64_t qi = 0; qi < C; ++qi) {
+      const int64_t visible = P + qi + 1;  // mask M_k: history in full, own chunk causally
+      const int64_t row = q_offsets[s] + qi;
+      for (int hh = 0; hh < G; ++hh) {
+        const int h = g * G + hh;
+        double* o = out + (row * H_q + h) * d;
+        for (int i = 0; i < d; ++i) o[i] = 0.0;
+        for (int i = 0; i < d; ++i) qv[i] = decode(q, (row * H_q + h) * d + i, dtype);
+        double zmax = -INFINITY;
+        for (int64_t t = 0; t < visible; ++t) {
+          double acc = 0.0;
+          for (int i = 0; i < d; ++i) acc += qv[i] * K[t * d + i];
+          z[t] = scale * acc;
+          zmax = std::max(zmax, z[t]);
+        }
+        double denom = 0.0;
+        for (int64_t t = 0; t < visible; ++t) denom += std::exp(z[t] - zmax);
+        for (int64_t t = 0; t < visible; ++t) {
+          double w = std::exp(z[t] - zmax) / denom;
+          for (int i = 0; i < d; ++i) o[i] += w * V[t * d + i];
+        }
+      }
+    }
+  };
+  const int64_t n_pairs = static_cast<int64_t>(n_seq) * H_kv;
+  int nt = n_threads > 0 ? n_threads : static_cast<int>(std::thread::hardware_concurrency());
+  if (nt < 1) nt = 1;
+  if (nt > n_pairs) nt = static_cast<int>(std::max<int64_t>(n_pairs, 1));
+  std::atomic<int64_t> next(0);
+  auto worker = [&]() {
+    for (int64_t k = next.fetch_add(1); k < n_pairs; k = next.fetch_add(1))
+      one_pair(static_cast<int>(k / H_kv), static_cast<int>(k % H_kv));
+  };
+  std::vector<std::thread> pool;
+  for (int i = 1; i < nt; ++i) pool.emplace_back(worker);
+  worker();
+  for (auto& th : pool) th.join();
+  return ORC_OK;
+}
+
 int orc_hardware_threads() { return static_cast<int>(std::thread::hardware_concurrency()); }
 
 }  // extern "C"

@@ -41,6 +41,8 @@ MUTANTS = {
     "write_skips_value": ("std::memcpy(static_cast<char*>(v_pool) + dst, static_cast<const char*>(v_new) + src, row);",
                           "(void)v_new;"),
     "softmax_not_normalised": ("double w = std::exp(z[t] - zmax) / denom;", "double w = std::exp(z[t] - zmax);"),
+    "prefill_sees_one_less": ("const int64_t visible = P + qi + 1;", "const int64_t visible = P + qi;"),
+    "prefill_forgets_history": ("const int64_t visible = P + qi + 1;", "const int64_t visible = qi + 1;"),
     "swap_in_lifo": ("    allocate_block(P, &p);\n    s.table.push_back(p);",
                      "    p = P.free_fifo.back(); P.free_fifo.pop_back(); P.ref[p] = 1;\n    s.table.push_back(p);"),
 }
@@ -48,7 +50,8 @@ MUTANTS = {
 
 def _run_mutant(name, old, new, tmp):
     src = open(SRC).read()
-    assert src.count(old) == 1, f"mutant {name}: anchor not unique/found"
+    # a slip in a line the two attention functions share is planted in both
+    assert src.count(old) >= 1, f"mutant {name}: anchor not found"
     mdir = os.path.join(tmp, name)
     os.makedirs(mdir)
     cpp = os.path.join(mdir, "m.cpp")

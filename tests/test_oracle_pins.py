@@ -487,3 +487,68 @@ def test_threads_do_not_change_the_result():
     a = oracle.decode_attention(g, 0, q, kp, vp, tables, seq_lens, 0.2, n_threads=1)
     b = oracle.decode_attention(g, 0, q, kp, vp, tables, seq_lens, 0.2, n_threads=7)
     assert np.array_equal(a, b)
+
+
+# ------------------------------------------------------------------ chunked prefill
+
+
+def _sdpa_causal(g, q_rows, k, v, scale):
+    """torch SDPA, float64, causal over a whole sequence (the monolithic forward pass)."""
+    G = g.H_q // g.H_kv
+    qt = torch.from_numpy(W.to_float64(q_rows, g.dtype)).permute(1, 0, 2)[None]
+    kt = torch.from_numpy(W.to_float64(k, g.dtype)).permute(1, 0, 2).repeat_interleave(G, dim=0)[None]
+    vt = torch.from_numpy(W.to_float64(v, g.dtype)).permute(1, 0, 2).repeat_interleave(G, dim=0)[None]
+    o = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, is_causal=True, scale=scale)
+    return o[0].permute(1, 0, 2).numpy()
+
+
+@pytest.mark.parametrize("dtype,B", [("bf16", 16), ("f32", 4), ("f16", 1)])
+def test_chunked_prefill_equals_monolithic_causal_attention(dtype, B):
+    """"Chunked prefill mechanics": chunk k's queries attend to the cached history in
+    full and causally within the chunk, which must equal one causal pass over the
+    whole prompt.  Three sequences, each split into ragged chunks; every chunk of
+    every sequence is computed in one oracle call per round."""
+    g = W.Geometry(L=1, H_q=8, H_kv=2, d_head=16, block_size=B, dtype=dtype, num_blocks=200)
+    lens = [37, 70, 5]
+    cuts = [[0, 10, 11, 37], [0, 64, 70], [0, 5]]
+    pool, ids, kp, vp, ks, vs, _, _, _ = build_case(g, lens, 71, W.permutation(71, "fo", g.num_blocks))
+    qs = [W.normal(71, f"qp{i}", (n, g.H_q, g.d_head), dtype) for i, n in enumerate(lens)]
+    scale = 0.25
+    Wd = max(-(-n // B) for n in lens)
+    tables, _ = pool.tables(ids, Wd)
+    got = [np.zeros((n, g.H_q, g.d_head)) for n in lens]
+    for rnd in range(max(len(c) - 1 for c in cuts)):
+        rows, offs, cur = [], [0], []
+        for i, c in enumerate(cuts):
+            if rnd + 1 < len(c):
+                a, b = c[rnd], c[rnd + 1]
+                rows.append(qs[i][a:b])
+                cur.append(b)
+            else:
+                cur.append(lens[i])  # empty chunk
+            offs.append(offs[-1] + (len(rows[-1]) if rnd + 1 < len(c) else 0))
+        q = np.concatenate(rows)
+        out = oracle.prefill_attention(g, 0, q, np.array(offs), kp, vp, tables, np.array(cur, np.int32), scale)
+        for i, c in enumerate(cuts):
+            if rnd + 1 < len(c):
+                got[i][c[rnd]:c[rnd + 1]] = out[offs[i]:offs[i + 1]]
+    for i in range(len(lens)):
+        ref = _sdpa_causal(g, qs[i], ks[i], vs[i], scale)
+        np.testing.assert_allclose(got[i], ref, rtol=1e-12, atol=1e-13)
+
+
+def test_prefill_last_query_is_the_decode_query_and_bad_chunks_are_rejected():
+    g = W.Geometry(L=1, H_q=4, H_kv=1, d_head=8, block_size=4, dtype="f32", num_blocks=16)
+    pool, ids, kp, vp, ks, vs, q, tables, lens = build_case(g, [13], 72)
+    qrow = W.normal(72, "qq", (3, 4, 8), "f32")
+    out = oracle.prefill_attention(g, 0, qrow, np.array([0, 3]), kp, vp, tables, lens, 0.5)
+    # the chunk's last query sees every token: an ordinary decode query
+    dec = oracle.decode_attention(g, 0, qrow[2:3], kp, vp, tables, lens, 0.5)
+    np.testing.assert_allclose(out[2], dec[0], rtol=1e-13)
+    # its first query sees all but the last two tokens
+    dec2 = oracle.decode_attention(g, 0, qrow[0:1], kp, vp, tables, lens - 2, 0.5)
+    np.testing.assert_allclose(out[0], dec2[0], rtol=1e-13)
+    with pytest.raises(oracle.OracleError) as e:
+        oracle.prefill_attention(g, 0, np.zeros((20, 4, 8), np.float32), np.array([0, 20]), kp, vp, tables, lens,
+                                 0.5)
+    assert e.value.status == "INVALID_ARG"
