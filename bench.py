@@ -790,6 +790,95 @@ def run_overlap(args, torch, pkv, dev, world, rank):
     }, None
 
 
+def run_prefill(args, torch, pkv, dev, world, rank):
+    """Chunked prefill: 8 sequences with 16,384 cached tokens each take a 512-token chunk.
+    Each step forks the 8 histories (no data moves), plans and writes the chunks'
+    keys/values, and runs chunked-prefill attention (history in full, causal within
+    the chunk)."""
+    n, hist, C = 8, 16384, 512
+    seed = W.SEEDS["agent32k"] + 11
+    total = args.warmup + args.steps
+    N = n * hist // 16 + total * n * (C // 16) + 64
+    g = W.Geometry(L=1, H_q=64, H_kv=8, d_head=128, block_size=16, dtype="bf16", num_blocks=N)
+    pool = pkv.pkv_pool_create(g.L, g.H_q, g.H_kv, g.d_head, g.block_size, g.dtype, N,
+                               W.permutation(seed, "prefill_fo", N))
+    base = [pkv.pkv_seq_create(pool) for _ in range(n)]
+    pkv.pkv_plan_append(pool, base, [hist] * n)
+    kp = W.device_normal(seed, "k_pool", g.pool_shape(), g.dtype, dev)
+    vp = W.device_normal(seed, "v_pool", g.pool_shape(), g.dtype, dev)
+    q = W.device_normal(seed, "q", (total, n * C, g.H_q, g.d_head), g.dtype, dev)
+    kn = W.device_normal(seed, "kn", (total, n * C, g.H_kv, g.d_head), g.dtype, dev)
+    vn = W.device_normal(seed, "vn", (total, n * C, g.H_kv, g.d_head), g.dtype, dev)
+    out = torch.empty((n * C, g.H_q, g.d_head), dtype=torch.bfloat16, device=dev)
+    offs = torch.arange(0, n * C + 1, C, dtype=torch.int32, device=dev)
+    Wd = (hist + C) // 16
+    scale = 1.0 / math.sqrt(g.d_head)
+    ev = []
+
+    def step(t, timed):
+        kids = [pkv.pkv_seq_fork(pool, b) for b in base]
+        slots, cows = pkv.pkv_plan_append(pool, kids, [C] * n)
+        tables, lens = pkv.pkv_export_tables(pool, kids, Wd)
+        d_slots = torch.from_numpy(slots).to(dev, non_blocking=True)
+        d_tab = torch.from_numpy(tables.copy()).to(dev, non_blocking=True)
+        d_len = torch.from_numpy(lens.copy()).to(dev, non_blocking=True)
+        if len(cows):
+            pkv.pkv_copy_blocks(pool, cows, kp, vp)
+        pkv.pkv_append_kv(pool, 0, kn[t], vn[t], d_slots, kp, vp)
+        e = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) if timed else None
+        if e:
+            e[0].record()
+        pkv.pkv_prefill_attention(pool, 0, q[t], offs, C, kp, vp, d_tab, d_len, scale, out)
+        if e:
+            e[1].record()
+            ev.append(e)
+        return kids
+
+    for t in range(args.warmup):
+        step(t, False)
+    torch.cuda.synchronize()
+    pkv.pkv_check_device_error()
+    clocks = clock_sampler(torch, dev)
+    clocks.start()
+    l0 = pkv.pkv_launch_count()
+    es, ee = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    es.record()
+    for t in range(args.warmup, total):
+        step(t, True)
+    ee.record()
+    torch.cuda.synchronize()
+    launches = pkv.pkv_launch_count() - l0
+    clk = clocks.stop()
+    pkv.pkv_check_device_error()
+    ms = es.elapsed_time(ee) / args.steps
+    att = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    flop = sum(4.0 * g.H_q * g.d_head * (hist + i + 1) for i in range(C)) * n
+    kvb = n * (hist + C) * g.H_kv * g.d_head * 2 * 2
+    tflops = flop / (att / 1e3) / 1e12
+    peak = 1916.4
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peak = float(json.load(f)["bf16_tflops"])
+    except Exception:
+        pass
+    return {
+        "metric": METRIC, "value": round(flop / (ms / 1e3) / 1e12, 2), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "prefill: 8 sequences x 16,384 cached tokens, a 512-token chunk each (forked "
+                               "histories), 64 query / 8 KV heads, d_head 128, bf16, 16-token blocks",
+                   "l2": "inputs larger than L2 (1.1 GB of K/V per step)", "parallelism": "replicas (no collectives)"},
+        "tokens_per_s": round(n * C / (ms / 1e3), 1),
+        "roofline": {"bound": "tensor", "achieved": round(tflops, 1), "peak": peak, "unit": "TFLOP/s",
+                     "frac": round(tflops / peak, 4), "traffic": None,
+                     "kernel": "pkv_prefill_attention (mma.sync m16n8k16)", "avg_launch_ms": round(att, 4),
+                     "kv_bytes_per_launch": kvb},
+        "e2e": {"value": round(flop / (ms / 1e3) / 1e12, 2), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": int(n * Wd * 4 + n * C * 4), "d2h_bytes_per_step": 0},
+        "gpu_launches": int(launches), "clocks": clk,
+    }, None
+
+
 # ------------------------------------------------------------------ CPU baseline (the oracle)
 
 
@@ -847,6 +936,33 @@ def reference_arm(args, world, rank):
     if rank != 0:
         return None
     cores = oracle.hardware_threads()
+    if args.workload == "prefill":
+        hist, C = 16384, 32
+        g = W.Geometry(L=1, H_q=64, H_kv=8, d_head=128, block_size=16, dtype="bf16", num_blocks=(hist + C) // 16)
+        kp = W.normal(1, "ref_k", g.pool_shape(), "bf16")
+        vp = W.normal(1, "ref_v", g.pool_shape(), "bf16")
+        tables = W.permutation(1, "ref_perm", g.num_blocks).reshape(1, -1)
+        q = W.normal(1, "ref_q", (C, g.H_q, g.d_head), "bf16")
+        lens = np.array([hist + C], np.int32)
+        times = []
+        for step in range(args.warmup + args.steps):
+            t0 = time.perf_counter()
+            oracle.prefill_attention(g, 0, q, np.array([0, C], np.int32), kp, vp, tables, lens, 1 / math.sqrt(128))
+            if step >= args.warmup:
+                times.append(time.perf_counter() - t0)
+        flop = sum(4.0 * g.H_q * g.d_head * (hist + i + 1) for i in range(C))
+        t_step = statistics.mean(times)
+        value = flop / t_step / 1e12
+        return {
+            "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(t_step * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": "prefill (sampled: one sequence, 32 chunk queries over 16,384 cached tokens)"},
+            "impl": "reference",
+            "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                             "sample": "oracle chunked-prefill attention, 1 sequence x 32 queries x 16,416 keys"},
+            "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        }
     if args.workload in ("swap", "overlap"):
         wl = W.swap(n_chunks=16)
         g = wl.geometry
@@ -943,7 +1059,7 @@ def main():
     ap.add_argument("--steps", type=int, default=None, help="timed steps (default 100; swap 4)")
     ap.add_argument("--warmup", type=int, default=None, help="warm-up steps (default 10; swap 3)")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["agent32k", "chat", "forked", "swap", "tiny", "overlap"],
+    ap.add_argument("--workload", choices=["agent32k", "chat", "forked", "swap", "tiny", "overlap", "prefill"],
                     default="agent32k")
     ap.add_argument("--swap-engine", type=int, default=0, help="swap workload: 0 SM kernel, 1 copy engines")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -953,7 +1069,7 @@ def main():
                     help="ncu dram bytes per decode launch, if captured for this kernel version")
     args = ap.parse_args()
     if args.steps is None:
-        args.steps = {"swap": 4, "overlap": 8}.get(args.workload, 100)
+        args.steps = {"swap": 4, "overlap": 8, "prefill": 20}.get(args.workload, 100)
     if args.warmup is None:
         args.warmup = 3 if args.workload == "swap" else 10
     if args.warmup < 3:
@@ -984,6 +1100,8 @@ def main():
         line, runner = run_swap(args, torch, pkv, dev, world, rank)
     elif args.workload == "overlap":
         line, runner = run_overlap(args, torch, pkv, dev, world, rank)
+    elif args.workload == "prefill":
+        line, runner = run_prefill(args, torch, pkv, dev, world, rank)
     else:
         line, runner = run_decode(args, torch, pkv, dev, world, rank)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -992,6 +1110,9 @@ def main():
             v, dt, desc = oracle_sample_decode(runner, n_sample)
             line["cpu_baseline"] = {"value": round(v, 4), "unit": "GB/s", "cores": __import__("oracle").hardware_threads(),
                                     "kind": "oracle", "sample": desc + f", {dt:.2f} s"}
+        elif args.workload == "prefill":
+            ref = reference_arm(argparse.Namespace(workload="prefill", steps=1, warmup=0), 1, 0)
+            line["cpu_baseline"] = dict(ref["cpu_baseline"])
         else:
             ref = reference_arm(argparse.Namespace(workload="swap", steps=2, warmup=1), 1, 0)
             line["cpu_baseline"] = dict(ref["cpu_baseline"])

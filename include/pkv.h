@@ -234,6 +234,25 @@ int pkv_decode_attention_noalloc(const pkv_pool* pool, int32_t layer, const void
                                  const void* v_pool, const int32_t* block_tables, int32_t W, const int32_t* seq_lens,
                                  int32_t n_seq, float scale, void* out, pkv_stream_t stream);
 
+/* Chunked-prefill attention ([KVM] "Chunked prefill mechanics"): the queries of a
+ * chunk attend to the cached history in full and to their own chunk causally,
+ *   O_k = Softmax(Q_k K_<=k^T * scale + M_k) V_<=k.
+ * The chunk of sequence s is its last C_s = q_offsets[s+1] - q_offsets[s] tokens,
+ * already written to the pool (pkv_plan_append + pkv_append_kv), so seq_lens[s]
+ * counts them: query i sits at position seq_lens[s] - C_s + i and sees positions
+ * 0 .. that position.  Decode is the case C_s = 1.
+ *   q, out     : device [n_tok][H_q][d_head], row q_offsets[s] + i (16-byte aligned).
+ *   q_offsets  : device int32 [n_seq + 1], q_offsets[0] = 0, q_offsets[n_seq] = n_tok.
+ *   max_q      : host int, >= every C_s (a longer chunk records code 6 in the device
+ *                error word and its extra rows are not computed).
+ *   block_tables, W, seq_lens: as for pkv_decode_attention (C_s <= len_s <= W*B).
+ * bf16/f16 with d_head 64 or 128 and B a multiple of 16 run on tensor cores (one CTA
+ * per 128 (query, head) rows, 64-key tiles staged by TMA); other geometries on CUDA
+ * cores.  No workspace. */
+int pkv_prefill_attention(const pkv_pool* pool, int32_t layer, const void* q, const int32_t* q_offsets, int32_t n_tok,
+                          int32_t max_q, const void* k_pool, const void* v_pool, const int32_t* block_tables, int32_t W,
+                          const int32_t* seq_lens, int32_t n_seq, float scale, void* out, pkv_stream_t stream);
+
 /* Copy-on-write data step ([KVM] "copies the B tokens from the shared block into
  * p_new"): for each (src, dst) in pairs (HOST int32 [n][2]), copy every slot of
  * every layer of block src into block dst, for K and V.  Pairs are passed to the

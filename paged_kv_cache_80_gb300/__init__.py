@@ -20,7 +20,7 @@ __all__ = [
     "pkv_version", "pkv_pool_create", "pkv_pool_destroy", "pkv_pool_geometry", "pkv_seq_create", "pkv_seq_fork",
     "pkv_seq_free", "pkv_seq_len", "pkv_plan_append", "pkv_export_tables", "pkv_refcounts", "pkv_free_list",
     "pkv_append_kv", "pkv_decode_workspace_size", "pkv_decode_attention", "pkv_decode_attention_noalloc",
-    "pkv_decode_step",
+    "pkv_decode_step", "pkv_prefill_attention",
     "pkv_copy_blocks", "pkv_swap_out",
     "pkv_swap_in", "pkv_seq_host_slots", "pkv_seq_residency", "TIER_HBM", "TIER_HOST", "pkv_pool_set_swap_engine", "pkv_check_device_error", "pkv_launch_count",
     "pkv_selftest_bounded_wait",
@@ -82,6 +82,8 @@ def _L():
             "pkv_decode_attention_noalloc": ([vp, i32, vp, vp, vp, vp, i32, vp, i32, ctypes.c_float, vp, vp],
                                              ctypes.c_int),
             "pkv_copy_blocks": ([vp, P32, i32, vp, vp, vp], ctypes.c_int),
+            "pkv_prefill_attention": ([vp, i32, vp, vp, i32, i32, vp, vp, vp, i32, vp, i32, ctypes.c_float, vp, vp],
+                                      ctypes.c_int),
             "pkv_decode_step": ([vp, i32, P32, i32, i32, vp, vp, vp, vp, vp, ctypes.c_float, vp, vp, vp, vp,
                                  ctypes.c_size_t, vp, vp, vp], ctypes.c_int),
             "pkv_swap_out": ([vp, i32, vp, vp, vp, i64, P64, i32, P32, vp], ctypes.c_int),
@@ -359,6 +361,17 @@ def pkv_decode_step(pool: PoolLike, layer: int, seq_ids, W: int, q, k_new, v_new
                                 _dev(out, "out"), _host_ptr(meta_host, "meta_host"), _dev(meta_dev, "meta_dev"),
                                 _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(), ev0, ev1,
                                 _stream(stream)), "pkv_decode_step")
+
+
+def pkv_prefill_attention(pool: PoolLike, layer: int, q, q_offsets, max_q: int, k_pool, v_pool, block_tables,
+                          seq_lens, scale: float, out, stream=None) -> None:
+    """Chunked-prefill attention; q/out are [n_tok][H_q][d], q_offsets device int32 [n_seq+1]."""
+    n_seq = int(seq_lens.numel())
+    W = int(block_tables.shape[1]) if block_tables.dim() == 2 else 0
+    _check(_L().pkv_prefill_attention(_h(pool), layer, _dev(q, "q"), _dev(q_offsets, "q_offsets"), int(q.shape[0]),
+                                      int(max_q), _dev(k_pool, "k_pool"), _dev(v_pool, "v_pool"),
+                                      _dev(block_tables, "block_tables"), W, _dev(seq_lens, "seq_lens"), n_seq,
+                                      float(scale), _dev(out, "out"), _stream(stream)), "pkv_prefill_attention")
 
 
 def pkv_copy_blocks(pool: PoolLike, pairs, k_pool, v_pool, stream=None) -> None:

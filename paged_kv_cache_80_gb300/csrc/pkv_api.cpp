@@ -414,6 +414,23 @@ int pkv_decode_attention(const pkv_pool* pool, int32_t layer, const void* q, con
                             out, workspace, ws_bytes, stream);
 }
 
+int pkv_prefill_attention(const pkv_pool* pool, int32_t layer, const void* q, const int32_t* q_offsets, int32_t n_tok,
+                          int32_t max_q, const void* k_pool, const void* v_pool, const int32_t* block_tables, int32_t W,
+                          const int32_t* seq_lens, int32_t n_seq, float scale, void* out, pkv_stream_t stream) {
+  pkv::clear_error();
+  if (!pool || n_seq < 0 || W < 0 || n_tok < 0 || max_q < 0)
+    return fail(PKV_ERR_INVALID_ARG, "bad arguments to pkv_prefill_attention");
+  const Pool& P = *as_pool(pool);
+  if (layer < 0 || layer >= P.geo.L) return fail(PKV_ERR_INVALID_ARG, "layer out of range");
+  if (n_seq == 0 || n_tok == 0) return PKV_OK;
+  if (n_seq > 65535) return fail(PKV_ERR_INVALID_ARG, "at most 65535 sequences per call");
+  if (!q || !q_offsets || !k_pool || !v_pool || !block_tables || !seq_lens || !out)
+    return fail(PKV_ERR_INVALID_ARG, "NULL buffer");
+  if (P.geo.H_q / P.geo.H_kv > 128) return fail(PKV_ERR_UNSUPPORTED, "more than 128 query heads per KV head");
+  return pkv::launch_prefill(const_cast<Pool&>(P), layer, q, q_offsets, n_tok, max_q, k_pool, v_pool, block_tables,
+                             W, seq_lens, n_seq, scale, out, stream);
+}
+
 int pkv_copy_blocks(const pkv_pool* pool, const int32_t* pairs, int32_t n, void* k_pool, void* v_pool,
                     pkv_stream_t stream) {
   pkv::clear_error();

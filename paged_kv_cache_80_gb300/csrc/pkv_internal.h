@@ -92,6 +92,9 @@ int decode_workspace_bytes(const Pool& P, int32_t n_seq, size_t* bytes);
 int launch_decode(Pool& P, int32_t layer, const void* q, const void* k_pool, const void* v_pool,
                   const int32_t* tables, int32_t W, const int32_t* seq_lens, int32_t n_seq, float scale, void* out,
                   void* ws, size_t ws_bytes, void* stream);
+int launch_prefill(Pool& P, int32_t layer, const void* q, const int32_t* q_off, int32_t n_tok, int32_t max_q,
+                   const void* k_pool, const void* v_pool, const int32_t* tables, int32_t W, const int32_t* seq_lens,
+                   int32_t n_seq, float scale, void* out, void* stream);
 void destroy_tensor_maps(Pool& P);
 
 // Device error codes recorded by kernels (the `code` of pkv_check_device_error).
@@ -102,6 +105,7 @@ enum DeviceErr : int32_t {
   DERR_DECODE_BLOCK = 3,    // block id out of range in a table
   DERR_DECODE_TIMEOUT = 4,  // a bounded mbarrier wait gave up
   DERR_SELFTEST_TIMEOUT = 5,  // the self-test's wait gave up (expected)
+  DERR_PREFILL_CHUNK = 6,     // a chunk longer than max_q
 };
 
 }  // namespace pkv

@@ -1,0 +1,76 @@
+"""Chunked-prefill attention on the GPU against the oracle ("KV Cache Management",
+"Chunked prefill mechanics": history in full, causal within the chunk)."""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+import paged_kv_cache_80_gb300 as pkv
+import workloads as W
+from helpers import PagedBatch, check_attention, out_f64, to_dev, torch_dtype
+
+pytestmark = pytest.mark.gpu
+
+
+def run_prefill(g, history, chunks, seed, max_q=None, free_order=None):
+    import torch
+
+    b = PagedBatch(g, free_order if free_order is not None else W.permutation(seed, "fo", g.num_blocks), seed=seed)
+    ids = b.new_seqs(len(history))
+    b.append(ids, history, "hist")
+    b.append(ids, chunks, "chunk")  # the chunk's keys/values are written first
+    tables, lens = b.tables(ids)
+    offs = np.concatenate([[0], np.cumsum(chunks)]).astype(np.int32)
+    n_tok = int(offs[-1])
+    q = W.normal(seed, "qchunk", (n_tok, g.H_q, g.d_head), g.dtype)
+    out = torch.full((n_tok, g.H_q, g.d_head), float("nan"), dtype=torch_dtype(g.dtype), device="cuda")
+    scale = 1.0 / math.sqrt(g.d_head)
+    pkv.pkv_prefill_attention(b.lib, 0, to_dev(q, g.dtype), torch.from_numpy(offs).cuda(),
+                              max(chunks) if max_q is None else max_q, b.kp, b.vp, torch.from_numpy(tables).cuda(),
+                              torch.from_numpy(lens).cuda(), scale, out)
+    pkv.pkv_check_device_error()
+    ref = oracle.prefill_attention(g, 0, q, offs, b.hk, b.hv, tables, lens, scale)
+    return check_attention(out_f64(out, g.dtype), ref, g.dtype)
+
+
+@pytest.mark.parametrize("H_q,H_kv,d,B,dtype", [
+    (64, 8, 128, 16, "bf16"),
+    (64, 8, 64, 16, "bf16"),
+    (64, 8, 128, 16, "f16"),
+    (32, 8, 128, 16, "bf16"),   # G = 4
+    (8, 8, 128, 32, "bf16"),    # G = 1, B = 32
+    (48, 4, 128, 16, "bf16"),   # G = 12: rows of a warp span queries
+    (12, 12, 64, 16, "f32"),    # CUDA-core path
+    (16, 2, 96, 16, "bf16"),    # CUDA-core path
+])
+def test_prefill_geometries(H_q, H_kv, d, B, dtype):
+    g = W.Geometry(L=1, H_q=H_q, H_kv=H_kv, d_head=d, block_size=B, dtype=dtype, num_blocks=800)
+    run_prefill(g, [0, 5, 64, 1000, 37, 300], [17, 1, 100, 40, 130, 16], 81)
+
+
+def test_prefill_ragged_chunks_and_empty_chunk():
+    g = W.Geometry(L=1, H_q=64, H_kv=8, d_head=128, block_size=16, dtype="bf16", num_blocks=1200)
+    run_prefill(g, [3000, 0, 200, 15, 999], [512, 300, 0, 1, 33], 82)
+
+
+def test_prefill_whole_prompt_is_causal_attention():
+    g = W.Geometry(L=1, H_q=64, H_kv=8, d_head=128, block_size=16, dtype="bf16", num_blocks=600)
+    run_prefill(g, [0, 0], [1000, 257], 83)
+
+
+def test_prefill_chunk_longer_than_max_q_is_recorded():
+    import torch
+
+    g = W.Geometry(L=1, H_q=64, H_kv=8, d_head=128, block_size=16, dtype="bf16", num_blocks=64)
+    b = PagedBatch(g, None, seed=84)
+    ids = b.new_seqs(1)
+    b.append(ids, [40], "c")
+    tables, lens = b.tables(ids)
+    q = torch.zeros((40, 64, 128), dtype=torch.bfloat16, device="cuda")
+    out = torch.zeros_like(q)
+    pkv.pkv_prefill_attention(b.lib, 0, q, torch.tensor([0, 40], dtype=torch.int32, device="cuda"), 16, b.kp, b.vp,
+                              torch.from_numpy(tables).cuda(), torch.from_numpy(lens).cuda(), 0.1, out)
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.pkv_check_device_error()
+    assert "code 6" in str(e.value)
