@@ -21,7 +21,7 @@ import numpy as np
 from . import build as _build
 
 STATUS = {0: "OK", 1: "INVALID_ARG", 2: "OUT_OF_BLOCKS", 3: "DOUBLE_FREE", 4: "BAD_BLOCK_ID"}
-DTYPE_CODE = {"f32": 0, "f16": 1, "bf16": 2}
+DTYPE_CODE = {"f32": 0, "f16": 1, "bf16": 2, "e4m3": 3}
 
 _lib = None
 
@@ -56,11 +56,15 @@ def lib():
         L.orc_copy_blocks.argtypes = geo + [P32, i64, vp, vp]
         L.orc_swap_out_data.argtypes = geo + [P32, P64, i64, vp, vp, vp]
         L.orc_swap_in_data.argtypes = geo + [P32, P64, i64, vp, vp, vp]
-        L.orc_decode_attention.argtypes = [ctypes.c_int] * 6 + [i64, ctypes.c_int, vp, vp, vp, P32, ctypes.c_int,
-                                                                 P32, ctypes.c_int, dbl, ctypes.POINTER(dbl),
-                                                                 ctypes.c_int]
-        L.orc_prefill_attention.argtypes = [ctypes.c_int] * 6 + [i64, ctypes.c_int, vp, P32, vp, vp, P32,
-                                                                  ctypes.c_int, P32, ctypes.c_int, dbl,
+        L.orc_write_slots_e4m3.argtypes = [ctypes.c_int] * 4 + [i64, ctypes.c_int, vp, vp, P32, i64,
+                                                                 ctypes.c_float, ctypes.c_float, vp, vp]
+        L.orc_e4m3_encode.argtypes = [vp, i64, vp]
+        L.orc_e4m3_decode.argtypes = [vp, i64, vp]
+        L.orc_decode_attention.argtypes = [ctypes.c_int] * 6 + [i64, ctypes.c_int, vp, ctypes.c_int, vp, vp, dbl,
+                                                                 dbl, P32, ctypes.c_int, P32, ctypes.c_int, dbl,
+                                                                 ctypes.POINTER(dbl), ctypes.c_int]
+        L.orc_prefill_attention.argtypes = [ctypes.c_int] * 6 + [i64, ctypes.c_int, vp, ctypes.c_int, P32, vp, vp,
+                                                                  dbl, dbl, P32, ctypes.c_int, P32, ctypes.c_int, dbl,
                                                                   ctypes.POINTER(dbl), ctypes.c_int]
         L.orc_hardware_threads.restype = ctypes.c_int
         _lib = L
@@ -184,12 +188,41 @@ def _geo(g):
     return (g.L, g.H_kv, g.d_head, g.block_size, DTYPE_CODE[g.dtype], g.num_blocks)
 
 
+def q_dtype(g) -> str:
+    """Element type of the activations (q, out, new keys/values) around a pool:
+    bfloat16 for an FP8 pool, the pool's own type otherwise."""
+    return "bf16" if g.dtype == "e4m3" else g.dtype
+
+
+def e4m3_encode(x: np.ndarray) -> np.ndarray:
+    """E4M3 codes (uint8) of float32 values: nearest, ties to even, saturating at 448."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty(x.shape, np.uint8)
+    lib().orc_e4m3_encode(_vp(x), x.size, _vp(out))
+    return out
+
+
+def e4m3_decode(codes: np.ndarray) -> np.ndarray:
+    """float64 values of E4M3 codes."""
+    c = np.ascontiguousarray(codes, dtype=np.uint8)
+    out = np.empty(c.shape, np.float64)
+    lib().orc_e4m3_decode(_vp(c), c.size, _vp(out))
+    return out
+
+
 def write_slots(g, layer: int, k_new: np.ndarray, v_new: np.ndarray, slot_mapping: np.ndarray,
-                k_pool: np.ndarray, v_pool: np.ndarray) -> None:
+                k_pool: np.ndarray, v_pool: np.ndarray, k_scale: float = 1.0, v_scale: float = 1.0) -> None:
+    """Write new keys/values at their slots.  For an FP8 pool k_new/v_new are bf16
+    (uint16 storage) and are quantised with the pool scales; otherwise bytes move."""
     sm = np.ascontiguousarray(slot_mapping, dtype=np.int32)
     assert k_pool.flags.c_contiguous and v_pool.flags.c_contiguous
     k_new = np.ascontiguousarray(k_new)
     v_new = np.ascontiguousarray(v_new)
+    if g.dtype == "e4m3":
+        _check(lib().orc_write_slots_e4m3(g.L, g.H_kv, g.d_head, g.block_size, g.num_blocks, layer, _vp(k_new),
+                                          _vp(v_new), _p32(sm), len(sm), float(k_scale), float(v_scale),
+                                          _vp(k_pool), _vp(v_pool)), "write_slots_e4m3")
+        return
     _check(lib().orc_write_slots(*_geo(g), layer, _vp(k_new), _vp(v_new), _p32(sm), len(sm), _vp(k_pool),
                                  _vp(v_pool)), "write_slots")
 
@@ -214,8 +247,10 @@ def swap_in_data(g, new_ids, host_slots, host, k_pool, v_pool) -> None:
 
 
 def decode_attention(g, layer: int, q: np.ndarray, k_pool: np.ndarray, v_pool: np.ndarray, tables: np.ndarray,
-                     seq_lens: np.ndarray, scale: float, n_threads: int = 0) -> np.ndarray:
-    """Plain softmax attention in float64; q is [n_seq][H_q][d] raw storage."""
+                     seq_lens: np.ndarray, scale: float, n_threads: int = 0, k_scale: float = 1.0,
+                     v_scale: float = 1.0) -> np.ndarray:
+    """Plain softmax attention in float64; q is [n_seq][H_q][d] raw storage of
+    ``q_dtype(g)``; stored keys/values are read as scale * element."""
     q = np.ascontiguousarray(q)
     tb = np.ascontiguousarray(tables, dtype=np.int32)
     sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
@@ -223,7 +258,8 @@ def decode_attention(g, layer: int, q: np.ndarray, k_pool: np.ndarray, v_pool: n
     W = tb.shape[1] if tb.ndim == 2 else 0
     out = np.zeros((n_seq, g.H_q, g.d_head), np.float64)
     code = lib().orc_decode_attention(g.L, g.H_q, g.H_kv, g.d_head, g.block_size, DTYPE_CODE[g.dtype],
-                                      g.num_blocks, layer, _vp(q), _vp(k_pool), _vp(v_pool), _p32(tb), W,
+                                      g.num_blocks, layer, _vp(q), DTYPE_CODE[q_dtype(g)], _vp(k_pool),
+                                      _vp(v_pool), float(k_scale), float(v_scale), _p32(tb), W,
                                       _p32(sl), n_seq, float(scale),
                                       out.ctypes.data_as(ctypes.POINTER(ctypes.c_double)), int(n_threads))
     _check(code, "decode_attention")
@@ -232,7 +268,7 @@ def decode_attention(g, layer: int, q: np.ndarray, k_pool: np.ndarray, v_pool: n
 
 def prefill_attention(g, layer: int, q: np.ndarray, q_offsets: np.ndarray, k_pool: np.ndarray,
                       v_pool: np.ndarray, tables: np.ndarray, seq_lens: np.ndarray, scale: float,
-                      n_threads: int = 0) -> np.ndarray:
+                      n_threads: int = 0, k_scale: float = 1.0, v_scale: float = 1.0) -> np.ndarray:
     """Chunked-prefill attention in float64; q is [n_tok][H_q][d] raw storage, the
     chunk of sequence s is rows q_offsets[s]..q_offsets[s+1] (its last tokens)."""
     q = np.ascontiguousarray(q)
@@ -243,7 +279,8 @@ def prefill_attention(g, layer: int, q: np.ndarray, q_offsets: np.ndarray, k_poo
     W = tb.shape[1] if tb.ndim == 2 else 0
     out = np.zeros((int(qo[-1]), g.H_q, g.d_head), np.float64)
     code = lib().orc_prefill_attention(g.L, g.H_q, g.H_kv, g.d_head, g.block_size, DTYPE_CODE[g.dtype],
-                                       g.num_blocks, layer, _vp(q), _p32(qo), _vp(k_pool), _vp(v_pool), _p32(tb), W,
+                                       g.num_blocks, layer, _vp(q), DTYPE_CODE[q_dtype(g)], _p32(qo), _vp(k_pool),
+                                       _vp(v_pool), float(k_scale), float(v_scale), _p32(tb), W,
                                        _p32(sl), n_seq, float(scale),
                                        out.ctypes.data_as(ctypes.POINTER(ctypes.c_double)), int(n_threads))
     _check(code, "prefill_attention")

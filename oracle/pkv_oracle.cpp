@@ -40,7 +40,13 @@
 //     sequence's tokens in position order;
 //   * CoW copies the whole block (every slot, every layer, K and V);
 //   * query head h reads KV head floor(h / G), G = H_q / H_kv;
-//   * a sequence of length 0 attends to nothing and yields a zero output.
+//   * a sequence of length 0 attends to nothing and yields a zero output;
+//   * FP8 storage ([KVM] b_elem = 1 "for FP8") is the OCP E4M3 format with one
+//     scale per pool for K and one for V: a value x is stored as the E4M3 code
+//     nearest to x / scale (binary32 quotient, ties to an even fraction, values
+//     beyond the largest finite 448 stored as 448) and read back as code * scale;
+//     the activations around such a pool (new keys/values, queries, outputs) are
+//     bfloat16.
 //
 // Pool data layout (both K and V): [num_blocks][L][H_kv][B][d_head] elements.
 // Host tier layout: [slot][2 (K, V)][L][H_kv][B][d_head] elements.
@@ -102,10 +108,51 @@ int release_block(Pool& P, int32_t p) {
   return ORC_OK;
 }
 
-size_t elem_bytes(int dtype) { return dtype == 0 ? 4 : 2; }  // 0 f32, 1 f16, 2 bf16
+// 0 f32, 1 f16, 2 bf16, 3 FP8 E4M3
+size_t elem_bytes(int dtype) { return dtype == 0 ? 4 : (dtype == 3 ? 1 : 2); }
+
+// Value of an FP8 E4M3 code (OCP 8-bit floating point, "E4M3"): 1 sign bit, 4
+// exponent bits with bias 7, 3 fraction bits; exponent 0 is subnormal
+// (frac/8 * 2^-6); there are no infinities and only S.1111.111 is NaN, so the
+// largest finite magnitude is 1.75 * 2^8 = 448.
+double e4m3_value(uint8_t c) {
+  int sign = c >> 7;
+  int expo = (c >> 3) & 0xf;
+  int frac = c & 7;
+  double v;
+  if (expo == 0) {
+    v = std::ldexp(static_cast<double>(frac), -9);  // frac/8 * 2^(1-7)
+  } else if (expo == 15 && frac == 7) {
+    v = NAN;
+  } else {
+    v = std::ldexp(1.0 + frac / 8.0, expo - 7);
+  }
+  return sign ? -v : v;
+}
+
+// The E4M3 code nearest to x: every finite non-negative code is tried in increasing
+// order of value; on a tie the code with the even fraction wins (round to nearest,
+// ties to even); magnitudes beyond 448 get 448 (saturation to the largest finite
+// value).  The sign is kept, so a negative value that rounds to zero is -0.
+uint8_t e4m3_encode(float x) {
+  if (std::isnan(x)) return 0x7f;
+  const uint8_t sign = std::signbit(x) ? 0x80 : 0x00;
+  const double a = std::fabs(static_cast<double>(x));
+  int best = 0;
+  double best_err = INFINITY;
+  for (int c = 0; c <= 0x7e; ++c) {
+    const double err = std::fabs(e4m3_value(static_cast<uint8_t>(c)) - a);
+    if (err < best_err || (err == best_err && (c & 1) == 0)) {
+      best = c;
+      best_err = err;
+    }
+  }
+  return static_cast<uint8_t>(sign | best);
+}
 
 // Exact decode of one stored element to double.
 double decode(const void* base, int64_t index, int dtype) {
+  if (dtype == 3) return e4m3_value(static_cast<const uint8_t*>(base)[index]);
   if (dtype == 0) {
     float f;
     std::memcpy(&f, static_cast<const char*>(base) + index * 4, 4);
@@ -362,6 +409,54 @@ int orc_write_slots(int L, int H_kv, int d, int B, int dtype, int64_t num_blocks
   return ORC_OK;
 }
 
+// The E4M3 codes of n binary32 values (test access to the encoder above).
+void orc_e4m3_encode(const float* x, int64_t n, uint8_t* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = e4m3_encode(x[i]);
+}
+
+// Value of each of n E4M3 codes.
+void orc_e4m3_decode(const uint8_t* codes, int64_t n, double* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = e4m3_value(codes[i]);
+}
+
+// Write into an FP8 pool ([KVM] M_block with b_elem = 1): as orc_write_slots, but
+// k_new and v_new hold bfloat16 values and each element x of a key is stored as
+// the E4M3 code of the binary32 quotient x / k_scale (x / v_scale for a value).
+int orc_write_slots_e4m3(int L, int H_kv, int d, int B, int64_t num_blocks, int layer, const void* k_new,
+                         const void* v_new, const int32_t* slot_mapping, int64_t n_tok, float k_scale, float v_scale,
+                         void* k_pool, void* v_pool) {
+  for (int64_t i = 0; i < n_tok; ++i)
+    if (slot_mapping[i] < 0 || slot_mapping[i] >= num_blocks * B) return ORC_BAD_BLOCK_ID;
+  auto bf16_at = [](const void* base, int64_t idx) {
+    uint16_t h;
+    std::memcpy(&h, static_cast<const char*>(base) + idx * 2, 2);
+    uint32_t bits = static_cast<uint32_t>(h) << 16;
+    float f;
+    std::memcpy(&f, &bits, 4);
+    return f;
+  };
+  int l0 = layer < 0 ? 0 : layer;
+  int l1 = layer < 0 ? L : layer + 1;
+  for (int l = l0; l < l1; ++l) {
+    int64_t src_layer = layer < 0 ? l : 0;
+    for (int64_t i = 0; i < n_tok; ++i) {
+      int64_t p = slot_mapping[i] / B;
+      int64_t o = slot_mapping[i] % B;
+      for (int h = 0; h < H_kv; ++h) {
+        int64_t src = ((src_layer * n_tok + i) * H_kv + h) * d;
+        int64_t dst = (((p * L + l) * H_kv + h) * B + o) * d;
+        for (int e = 0; e < d; ++e) {
+          const float kq = bf16_at(k_new, src + e) / k_scale;
+          const float vq = bf16_at(v_new, src + e) / v_scale;
+          static_cast<uint8_t*>(k_pool)[dst + e] = e4m3_encode(kq);
+          static_cast<uint8_t*>(v_pool)[dst + e] = e4m3_encode(vq);
+        }
+      }
+    }
+  }
+  return ORC_OK;
+}
+
 // Copy-on-write data step [KVM, CoW branching]: copy every slot of every layer of
 // block src into block dst, for K and for V, for each (src, dst) pair in order.
 int orc_copy_blocks(int L, int H_kv, int d, int B, int dtype, int64_t num_blocks, const int32_t* pairs,
@@ -415,11 +510,14 @@ int orc_swap_in_data(int L, int H_kv, int d, int B, int dtype, int64_t num_block
 //   w_t    = exp(z_t - max_u z_u) / sum_u exp(z_u - max_u z_u)
 //   out[s][h][:] = sum_t w_t * V_s[t][:]
 // computed in double precision from the exact stored input values.  A sequence
-// with len_s == 0 gives out = 0.  q is [n_seq][H_q][d]; tables are [n_seq][W].
+// with len_s == 0 gives out = 0.  q is [n_seq][H_q][d] of q_dtype; tables are
+// [n_seq][W].  Stored keys are read as k_scale * element, values as v_scale *
+// element (1 and 1 for 16/32-bit pools; the pool scales for an FP8 pool).
 // Work is split over (s, g) pairs across n_threads threads (0 = all cores).
 int orc_decode_attention(int L, int H_q, int H_kv, int d, int B, int dtype, int64_t num_blocks, int layer,
-                         const void* q, const void* k_pool, const void* v_pool, const int32_t* tables, int W,
-                         const int32_t* seq_lens, int n_seq, double scale, double* out, int n_threads) {
+                         const void* q, int q_dtype, const void* k_pool, const void* v_pool, double k_scale,
+                         double v_scale, const int32_t* tables, int W, const int32_t* seq_lens, int n_seq,
+                         double scale, double* out, int n_threads) {
   if (H_kv <= 0 || H_q % H_kv != 0 || layer < 0 || layer >= L) return ORC_INVALID_ARG;
   const int G = H_q / H_kv;
   for (int s = 0; s < n_seq; ++s) {
@@ -438,8 +536,8 @@ int orc_decode_attention(int L, int H_q, int H_kv, int d, int B, int dtype, int6
       int64_t p = tables[static_cast<int64_t>(s) * W + t / B];
       int64_t base = (((p * L + layer) * H_kv + g) * B + t % B) * d;
       for (int i = 0; i < d; ++i) {
-        K[t * d + i] = decode(k_pool, base + i, dtype);
-        V[t * d + i] = decode(v_pool, base + i, dtype);
+        K[t * d + i] = k_scale * decode(k_pool, base + i, dtype);
+        V[t * d + i] = v_scale * decode(v_pool, base + i, dtype);
       }
     }
     std::vector<double> z(len);
@@ -449,7 +547,7 @@ int orc_decode_attention(int L, int H_q, int H_kv, int d, int B, int dtype, int6
       for (int i = 0; i < d; ++i) o[i] = 0.0;
       if (len == 0) continue;
       std::vector<double> qv(d);
-      for (int i = 0; i < d; ++i) qv[i] = decode(q, (static_cast<int64_t>(s) * H_q + h) * d + i, dtype);
+      for (int i = 0; i < d; ++i) qv[i] = decode(q, (static_cast<int64_t>(s) * H_q + h) * d + i, q_dtype);
       double zmax = -INFINITY;
       for (int64_t t = 0; t < len; ++t) {
         double acc = 0.0;
@@ -488,11 +586,12 @@ int orc_decode_attention(int L, int H_q, int H_kv, int d, int B, int dtype, int6
 // Here the chunk of sequence s is its last C_s = q_offsets[s+1] - q_offsets[s]
 // tokens (already written to the pool, so seq_lens[s] counts them); query i of the
 // chunk sits at position P_s + i with P_s = seq_lens[s] - C_s and sees positions
-// t <= P_s + i.  q and out are [n_tok][H_q][d], row q_offsets[s] + i.
+// t <= P_s + i.  q (of q_dtype) and out are [n_tok][H_q][d], row q_offsets[s] + i;
+// keys and values are read as in orc_decode_attention.
 int orc_prefill_attention(int L, int H_q, int H_kv, int d, int B, int dtype, int64_t num_blocks, int layer,
-                          const void* q, const int32_t* q_offsets, const void* k_pool, const void* v_pool,
-                          const int32_t* tables, int W, const int32_t* seq_lens, int n_seq, double scale,
-                          double* out, int n_threads) {
+                          const void* q, int q_dtype, const int32_t* q_offsets, const void* k_pool,
+                          const void* v_pool, double k_scale, double v_scale, const int32_t* tables, int W,
+                          const int32_t* seq_lens, int n_seq, double scale, double* out, int n_threads) {
   if (H_kv <= 0 || H_q % H_kv != 0 || layer < 0 || layer >= L) return ORC_INVALID_ARG;
   const int G = H_q / H_kv;
   for (int s = 0; s < n_seq; ++s) {
@@ -513,8 +612,8 @@ int orc_prefill_attention(int L, int H_q, int H_kv, int d, int B, int dtype, int
       int64_t p = tables[static_cast<int64_t>(s) * W + t / B];
       int64_t base = (((p * L + layer) * H_kv + g) * B + t % B) * d;
       for (int i = 0; i < d; ++i) {
-        K[t * d + i] = decode(k_pool, base + i, dtype);
-        V[t * d + i] = decode(v_pool, base + i, dtype);
+        K[t * d + i] = k_scale * decode(k_pool, base + i, dtype);
+        V[t * d + i] = v_scale * decode(v_pool, base + i, dtype);
       }
     }
     std::vector<double> z(len), qv(d);
@@ -525,7 +624,7 @@ int orc_prefill_attention(int L, int H_q, int H_kv, int d, int B, int dtype, int
         const int h = g * G + hh;
         double* o = out + (row * H_q + h) * d;
         for (int i = 0; i < d; ++i) o[i] = 0.0;
-        for (int i = 0; i < d; ++i) qv[i] = decode(q, (row * H_q + h) * d + i, dtype);
+        for (int i = 0; i < d; ++i) qv[i] = decode(q, (row * H_q + h) * d + i, q_dtype);
         double zmax = -INFINITY;
         for (int64_t t = 0; t < visible; ++t) {
           double acc = 0.0;

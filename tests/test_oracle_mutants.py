@@ -43,6 +43,15 @@ MUTANTS = {
     "softmax_not_normalised": ("double w = std::exp(z[t] - zmax) / denom;", "double w = std::exp(z[t] - zmax);"),
     "prefill_sees_one_less": ("const int64_t visible = P + qi + 1;", "const int64_t visible = P + qi;"),
     "prefill_forgets_history": ("const int64_t visible = P + qi + 1;", "const int64_t visible = qi + 1;"),
+    "e4m3_bias_8": ("v = std::ldexp(1.0 + frac / 8.0, expo - 7);", "v = std::ldexp(1.0 + frac / 8.0, expo - 8);"),
+    "e4m3_subnormal_step": ("v = std::ldexp(static_cast<double>(frac), -9);",
+                            "v = std::ldexp(static_cast<double>(frac), -10);"),
+    "e4m3_ties_upward": ("if (err < best_err || (err == best_err && (c & 1) == 0)) {", "if (err <= best_err) {"),
+    "e4m3_no_448": ("for (int c = 0; c <= 0x7e; ++c) {", "for (int c = 0; c < 0x7e; ++c) {"),
+    "quantise_by_product": ("const float kq = bf16_at(k_new, src + e) / k_scale;",
+                            "const float kq = bf16_at(k_new, src + e) * k_scale;"),
+    "key_scale_dropped": ("K[t * d + i] = k_scale * decode(k_pool, base + i, dtype);",
+                          "K[t * d + i] = decode(k_pool, base + i, dtype);"),
     "swap_in_lifo": ("    allocate_block(P, &p);\n    s.table.push_back(p);",
                      "    p = P.free_fifo.back(); P.free_fifo.pop_back(); P.ref[p] = 1;\n    s.table.push_back(p);"),
 }

@@ -552,3 +552,145 @@ def test_prefill_last_query_is_the_decode_query_and_bad_chunks_are_rejected():
         oracle.prefill_attention(g, 0, np.zeros((20, 4, 8), np.float32), np.array([0, 20]), kp, vp, tables, lens,
                                  0.5)
     assert e.value.status == "INVALID_ARG"
+
+
+# ------------------------------------------------------------------ FP8 (E4M3) storage
+#
+# "KV Cache Management" (cs249r vol. 3 ch. 5), "The PagedAttention virtual memory
+# model": M_block = 2 L H_kv B d_head b_elem with b_elem = 1 byte for FP8.  The
+# format is OCP E4M3; torch's float8_e4m3fn is an independent implementation of it.
+
+
+def _torch_e4m3_values(codes: np.ndarray) -> np.ndarray:
+    return torch.from_numpy(np.ascontiguousarray(codes, np.uint8)).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+
+
+def _torch_e4m3_codes(x: np.ndarray) -> np.ndarray:
+    return torch.from_numpy(np.ascontiguousarray(x, np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def test_e4m3_values_match_torch_and_closed_forms():
+    codes = np.arange(256, dtype=np.uint8)
+    mine = oracle.e4m3_decode(codes)
+    ref = _torch_e4m3_values(codes)
+    assert np.array_equal(np.isnan(mine), np.isnan(ref))
+    assert set(np.flatnonzero(np.isnan(mine)).tolist()) == {0x7F, 0xFF}
+    ok = ~np.isnan(ref)
+    assert np.array_equal(mine[ok], ref[ok]) and np.array_equal(np.signbit(mine[ok]), np.signbit(ref[ok]))
+    # closed forms of the format: bias 7, 3 fraction bits, largest finite 1.75 * 2^8
+    assert mine[0x7E] == 448.0 and mine[0xFE] == -448.0
+    assert mine[0x38] == 1.0 and mine[0xC0] == -2.0
+    assert mine[0x08] == 2.0 ** -6 and mine[0x01] == 2.0 ** -9 and mine[0x07] == 7 * 2.0 ** -9
+    assert mine[0x00] == 0.0 and np.signbit(mine[0x80])
+
+
+def test_e4m3_encode_round_trip_ties_to_even_and_saturation():
+    finite = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], np.uint8)
+    vals = oracle.e4m3_decode(finite).astype(np.float32)
+    assert np.array_equal(oracle.e4m3_encode(vals), finite)  # every value maps to its own code (-0 too)
+    pos = np.arange(0, 0x7F, dtype=np.uint8)  # 0 .. 448 in increasing order
+    pv = oracle.e4m3_decode(pos)
+    assert np.all(np.diff(pv) > 0)
+    mid = ((pv[:-1] + pv[1:]) / 2).astype(np.float32)  # exact: five significant bits
+    assert np.array_equal(mid.astype(np.float64), (pv[:-1] + pv[1:]) / 2)
+    even = np.where(pos[:-1] % 2 == 0, pos[:-1], pos[1:])
+    assert np.array_equal(oracle.e4m3_encode(mid), even)
+    assert np.array_equal(oracle.e4m3_encode(np.nextafter(mid, np.float32(np.inf))), pos[1:])
+    assert np.array_equal(oracle.e4m3_encode(np.nextafter(mid, np.float32(0))), pos[:-1])
+    assert np.array_equal(oracle.e4m3_encode(-mid), even | 0x80)
+    big = np.array([448, 460, 464, 1e4, 3e38, -500, -3e38], np.float32)
+    assert oracle.e4m3_encode(big).tolist() == [0x7E] * 5 + [0xFE] * 2
+    tiny = np.array([2.0 ** -10, 2.0 ** -10 * 1.001, -(2.0 ** -11), 2.0 ** -9 * 1.5], np.float32)
+    assert oracle.e4m3_encode(tiny).tolist() == [0x00, 0x01, 0x80, 0x02]
+    # against torch's conversion (round to nearest even) inside the finite range
+    x = np.concatenate([W.substream(31, f"e4m3_{s}").standard_normal(20000).astype(np.float32) * s
+                        for s in (1e-3, 0.05, 1.0, 30.0, 140.0)])
+    x = x[np.abs(x) < 448]
+    assert np.array_equal(oracle.e4m3_encode(x), _torch_e4m3_codes(x))
+
+
+def _fp8_case(g, lens, seed, k_scale, v_scale, free_order=None):
+    """Sequences written into an FP8 pool through the oracle's quantised write; K/V
+    drawn in bf16.  Returns the codes' values dequantised by torch."""
+    pool = oracle.Pool(g.num_blocks, g.block_size, free_order)
+    kp = np.zeros(g.pool_shape(), np.uint8)
+    vp = np.zeros(g.pool_shape(), np.uint8)
+    ids = [pool.seq_create() for _ in lens]
+    kd, vd = [], []
+    for i, (sid, n) in enumerate(zip(ids, lens)):
+        k = W.normal(seed, f"k{i}", (n, g.H_kv, g.d_head), "bf16")
+        v = W.normal(seed, f"v{i}", (n, g.H_kv, g.d_head), "bf16")
+        if n:
+            slots, _ = pool.append([sid], [n])
+            oracle.write_slots(g, 0, k, v, slots, kp, vp, k_scale, v_scale)
+            # the stored codes, read back through the table by plain indexing
+            blk = np.array([pool.table(sid)[t // g.block_size] for t in range(n)])
+            off = np.arange(n) % g.block_size
+            kd.append(_torch_e4m3_values(kp[blk, 0, :, off, :]) * k_scale)
+            vd.append(_torch_e4m3_values(vp[blk, 0, :, off, :]) * v_scale)
+        else:
+            kd.append(np.zeros((0, g.H_kv, g.d_head)))
+            vd.append(np.zeros((0, g.H_kv, g.d_head)))
+    Wt = max([-(-n // g.block_size) for n in lens] + [1])
+    tables, seq_lens = pool.tables(ids, Wt)
+    return pool, ids, kp, vp, kd, vd, tables, seq_lens
+
+
+def test_quantised_write_stores_the_code_of_the_binary32_quotient():
+    g = W.Geometry(L=2, H_q=4, H_kv=2, d_head=16, block_size=4, dtype="e4m3", num_blocks=8)
+    k = W.normal(41, "k", (g.L, 6, g.H_kv, g.d_head), "bf16")
+    v = W.normal(41, "v", (g.L, 6, g.H_kv, g.d_head), "bf16")
+    v[0, 0, 0, :4] = W.f32_to_bf16_bits(np.array([900.0, -5000.0, 1e-4, -1e-4], np.float32))  # saturate / flush
+    slots = np.array([0, 5, 6, 13, 31, 20], np.int32)
+    for ks, vs in ((1.0, 1.0), (0.0173, 0.5), (3.0, 0.011)):
+        kp = np.zeros(g.pool_shape(), np.uint8)
+        vp = np.zeros(g.pool_shape(), np.uint8)
+        oracle.write_slots(g, -1, k, v, slots, kp, vp, ks, vs)
+        kq = W.bf16_bits_to_f32(k) / np.float32(ks)
+        vq = W.bf16_bits_to_f32(v) / np.float32(vs)
+        vq_codes = _torch_e4m3_codes(np.clip(vq, -448, 448))
+        for i, sl in enumerate(slots):
+            p, o = divmod(int(sl), g.block_size)
+            for l in range(g.L):
+                assert np.array_equal(kp[p, l, :, o, :], _torch_e4m3_codes(kq[l, i]))
+                assert np.array_equal(vp[p, l, :, o, :], vq_codes[l, i])
+        mask = np.zeros(g.num_blocks * g.block_size, bool)
+        mask[slots] = True
+        assert np.all(kp.transpose(0, 3, 1, 2, 4).reshape(g.num_blocks * g.block_size, -1)[~mask] == 0)
+    # the page's byte count with b_elem = 1: one block of K plus V
+    assert 2 * kp[0].nbytes == 2 * g.L * g.H_kv * g.block_size * g.d_head * 1
+
+
+@pytest.mark.parametrize("B", [1, 4, 16])
+def test_fp8_attention_matches_sdpa_on_dequantised_keys_and_values(B):
+    """Attention over an FP8 pool equals torch's SDPA (float64) over the stored codes'
+    values times the pool scales, with bf16 queries."""
+    g = W.Geometry(L=1, H_q=8, H_kv=2, d_head=16, block_size=B, dtype="e4m3", num_blocks=96)
+    lens = [1, 2, 5, 8, 17, 0, 33][: 7 if B >= 4 else 5]
+    k_scale, v_scale = 0.0173, 0.25
+    pool, ids, kp, vp, kd, vd, tables, seq_lens = _fp8_case(g, lens, 43, k_scale, v_scale,
+                                                            W.permutation(43, f"fo{B}", g.num_blocks))
+    q = W.normal(43, "q", (len(lens), g.H_q, g.d_head), "bf16")
+    out = oracle.decode_attention(g, 0, q, kp, vp, tables, seq_lens, 0.3, k_scale=k_scale, v_scale=v_scale)
+    G = g.H_q // g.H_kv
+    for s in range(len(lens)):
+        if lens[s] == 0:
+            assert np.all(out[s] == 0)
+            continue
+        qt = torch.from_numpy(W.to_float64(q[s], "bf16")).view(1, g.H_q, 1, g.d_head)
+        kt = torch.from_numpy(kd[s]).permute(1, 0, 2).repeat_interleave(G, dim=0)[None]
+        vt = torch.from_numpy(vd[s]).permute(1, 0, 2).repeat_interleave(G, dim=0)[None]
+        ref = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, scale=0.3)[0, :, 0, :].numpy()
+        np.testing.assert_allclose(out[s], ref, rtol=1e-12, atol=1e-13)
+    # chunked prefill over the same pool: the last 5 tokens of sequence 4 as a chunk
+    s = 4
+    qs = W.normal(43, "qc", (5, g.H_q, g.d_head), "bf16")
+    got = oracle.prefill_attention(g, 0, qs, np.array([0, 5], np.int32), kp, vp, tables[s:s + 1],
+                                   seq_lens[s:s + 1], 0.3, k_scale=k_scale, v_scale=v_scale)
+    P = lens[s] - 5
+    for i in range(5):
+        qt = torch.from_numpy(W.to_float64(qs[i], "bf16")).view(1, g.H_q, 1, g.d_head)
+        kt = torch.from_numpy(kd[s][: P + i + 1]).permute(1, 0, 2).repeat_interleave(G, dim=0)[None]
+        vt = torch.from_numpy(vd[s][: P + i + 1]).permute(1, 0, 2).repeat_interleave(G, dim=0)[None]
+        ref = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, scale=0.3)[0, :, 0, :].numpy()
+        np.testing.assert_allclose(got[i], ref, rtol=1e-12, atol=1e-13)

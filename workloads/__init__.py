@@ -33,7 +33,7 @@ from typing import Optional
 import numpy as np
 
 # dtype names used throughout (element bytes in parentheses)
-DTYPE_BYTES = {"f32": 4, "f16": 2, "bf16": 2}
+DTYPE_BYTES = {"f32": 4, "f16": 2, "bf16": 2, "e4m3": 1}
 
 # seed = workload index * 1000 + 7
 SEEDS = {"tiny": 1007, "chat": 2007, "agent32k": 3007, "forked": 4007, "swap": 5007}
