@@ -46,8 +46,12 @@ METRIC = "paged decode attention KV GB/s & tokens/s (% of 8 TB/s HBM); swap GB/s
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per algorithmic byte
 # of the decode call, from an ncu capture of the kernels built from the sources
 # with this digest (summary in profiles/).  Reported only while the sources match.
-TRAFFIC_RECORD = {"sources_sha256": "512a01d8c25f3eb410590f6a29eb77f916efb5f5e7e6dfbd10d708dab58073e6",
-                  "ratio": 1.0110}  # 816.8 MB DRAM / 807.9 MB algorithmic, agent 48 x 4,096 capture
+# ncu DRAM bytes / algorithmic bytes of one decode launch, per stored K/V type, valid
+# while the decode sources hash to sources_sha256
+TRAFFIC_RECORD = {
+    "bf16": {"sources_sha256": "512a01d8c25f3eb410590f6a29eb77f916efb5f5e7e6dfbd10d708dab58073e6",
+             "ratio": 1.0110},  # 816.8 MB DRAM / 807.9 MB algorithmic, agent 48 x 4,096 capture
+}
 
 
 def decode_sources_digest() -> str:
@@ -241,9 +245,24 @@ class DecodeRunner:
     # subclasses set: g, pool, ids (live batch in order), kp, vp, Wd, scale,
     # q/kn/vn device tensors [steps][n_max][...], and implement running(t)
 
+    def _set_geometry(self, g, kv_scales=(1.0, 1.0)):
+        """g.dtype is the stored K/V type; q, out and new keys/values are bf16 around
+        an FP8 pool."""
+        self.g = g
+        self.act = "bf16" if g.dtype == "e4m3" else g.dtype
+        self.act_bytes = W.DTYPE_BYTES[self.act]
+        self.kv_scales = kv_scales
+
+    def _new_pool(self, free_order):
+        g, pkv = self.g, self.pkv
+        pool = pkv.pkv_pool_create(g.L, g.H_q, g.H_kv, g.d_head, g.block_size, g.dtype, g.num_blocks, free_order)
+        if g.dtype == "e4m3":
+            pkv.pkv_pool_set_kv_scales(pool, *self.kv_scales)
+        return pool
+
     def _alloc_common(self, n_max: int):
         torch, g = self.torch, self.g
-        td = {"bf16": torch.bfloat16, "f16": torch.float16, "f32": torch.float32}[g.dtype]
+        td = {"bf16": torch.bfloat16, "f16": torch.float16, "f32": torch.float32}[self.act]
         self.td = td
         self.out = torch.empty((n_max, g.H_q, g.d_head), dtype=td, device=self.dev)
         self.ws = torch.empty(self.pkv.pkv_decode_workspace_size(self.pool, n_max), dtype=torch.uint8,
@@ -316,15 +335,15 @@ class DecodeRunner:
             tok = int(lens.sum(dtype=np.int64))
             kvb = tok * g.H_kv * g.d_head * g.elem_bytes * 2
             self.kv_bytes.append(kvb)
-            qo = 2 * n * g.H_q * g.d_head * g.elem_bytes
+            qo = 2 * n * g.H_q * g.d_head * self.act_bytes
             self.alg_bytes.append(kvb + qo + n * self.Wd * 4 + n * 4)
             self.tokens.append(n)
             self.h2d_meta += nbytes
         if host_inputs is not None:
             self.out_host[:n].copy_(self.out[:n], non_blocking=True)
             torch.cuda.current_stream().synchronize()  # the step's result is read on the host
-            self.e2e_in_bytes += nbytes + (q.numel() + kn.numel() + vn.numel()) * g.elem_bytes
-            self.e2e_out_bytes += n * g.H_q * g.d_head * g.elem_bytes
+            self.e2e_in_bytes += nbytes + (q.numel() + kn.numel() + vn.numel()) * self.act_bytes
+            self.e2e_out_bytes += n * g.H_q * g.d_head * self.act_bytes
         self.after_step(t, ids)
 
     def _refresh_handle(self):
@@ -355,23 +374,24 @@ class DecodeRunner:
     def inputs_for_steps(self, tag):
         torch, g = self.torch, self.g
         n = self.n_max
-        self.q = W.device_normal(self.seed, f"{tag}_q", (self.total_steps, n, g.H_q, g.d_head), g.dtype, self.dev)
-        self.kn = W.device_normal(self.seed, f"{tag}_k", (self.total_steps, n, g.H_kv, g.d_head), g.dtype, self.dev)
-        self.vn = W.device_normal(self.seed, f"{tag}_v", (self.total_steps, n, g.H_kv, g.d_head), g.dtype, self.dev)
+        a = self.act
+        self.q = W.device_normal(self.seed, f"{tag}_q", (self.total_steps, n, g.H_q, g.d_head), a, self.dev)
+        self.kn = W.device_normal(self.seed, f"{tag}_k", (self.total_steps, n, g.H_kv, g.d_head), a, self.dev)
+        self.vn = W.device_normal(self.seed, f"{tag}_v", (self.total_steps, n, g.H_kv, g.d_head), a, self.dev)
 
 
 class AgentRunner(DecodeRunner):
     name = "agent32k"
 
-    def __init__(self, torch, pkv, dev, total_steps, n_seq=48, context=32768):
+    def __init__(self, torch, pkv, dev, total_steps, n_seq=48, context=32768, kv_dtype="bf16"):
         super().__init__(torch, pkv, dev, total_steps)
         wl = W.agent(n_seq, context, spare_steps=total_steps + 16)
-        self.wl, self.g, self.seed = wl, wl.geometry, wl.seed
+        self.wl, self.seed = wl, wl.seed
+        self._set_geometry(with_kv_dtype(wl.geometry, kv_dtype))
         g = self.g
         self.n_max = n_seq
         self.scale = wl.scale
-        self.pool = pkv.pkv_pool_create(g.L, g.H_q, g.H_kv, g.d_head, g.block_size, g.dtype, g.num_blocks,
-                                        wl.free_order)
+        self.pool = self._new_pool(wl.free_order)
         self.ids = [pkv.pkv_seq_create(self.pool) for _ in range(n_seq)]
         self.ids_np = np.array(self.ids, np.int32)
         pkv.pkv_plan_append(self.pool, self.ids, [context] * n_seq)
@@ -382,10 +402,11 @@ class AgentRunner(DecodeRunner):
         self.inputs_for_steps("agent")
         self._alloc_common(n_seq)
         self.config = {"workload": f"agent{context // 1024}k: {n_seq} sequences x {context} tokens, 64 query / "
-                                   f"8 KV heads, d_head 128, bf16, 16-token blocks, permuted block ids",
+                                   f"8 KV heads, d_head 128, {kv_desc(g)}, 16-token blocks, permuted block ids",
                        "n_seq": n_seq, "context": context, "H_q": g.H_q, "H_kv": g.H_kv, "d_head": g.d_head,
                        "block_size": g.block_size, "pool_blocks": g.num_blocks,
-                       "l2": f"inputs larger than L2 ({n_seq * context * 4096 / 1e9:.2f} GB of K/V per step)",
+                       "l2": f"inputs larger than L2 ({n_seq * context * 2048 * g.elem_bytes / 1e9:.2f} GB of K/V "
+                             f"per step)",
                        "parallelism": "replicas (no collectives)"}
 
     def running(self, t):
@@ -395,10 +416,11 @@ class AgentRunner(DecodeRunner):
 class ChatRunner(DecodeRunner):
     name = "chat"
 
-    def __init__(self, torch, pkv, dev, total_steps, n_seq=256):
+    def __init__(self, torch, pkv, dev, total_steps, n_seq=256, kv_dtype="bf16"):
         super().__init__(torch, pkv, dev, total_steps)
         wl = W.chat(n_seq=n_seq)
-        self.wl, self.g, self.seed = wl, wl.geometry, wl.seed
+        self.wl, self.seed = wl, wl.seed
+        self._set_geometry(with_kv_dtype(wl.geometry, kv_dtype))
         g = self.g
         self.n_max = n_seq
         self.scale = wl.scale
@@ -417,7 +439,7 @@ class ChatRunner(DecodeRunner):
         self.inputs_for_steps("chat")
         self._alloc_common(n_seq)
         self.config = {"workload": "chat: 256 sequences, lognormal prompt (mean 217) + generated (mean 154) "
-                                   "lengths <= 1024, 64 query / 8 KV heads, d_head 128, bf16, 16-token blocks, "
+                                   f"lengths <= 1024, 64 query / 8 KV heads, d_head 128, {kv_desc(g)}, 16-token blocks, "
                                    "32,768-block pool in shuffled order, 64-step schedule",
                        "n_seq": n_seq, "H_q": g.H_q, "H_kv": g.H_kv, "d_head": g.d_head,
                        "block_size": g.block_size, "pool_blocks": g.num_blocks,
@@ -425,9 +447,8 @@ class ChatRunner(DecodeRunner):
                        "parallelism": "replicas (no collectives)"}
 
     def _fresh_state(self):
-        g, pkv = self.g, self.pkv
-        pool = pkv.pkv_pool_create(g.L, g.H_q, g.H_kv, g.d_head, g.block_size, g.dtype, g.num_blocks,
-                                   self.wl.free_order)
+        pkv = self.pkv
+        pool = self._new_pool(self.wl.free_order)
         ids = [pkv.pkv_seq_create(pool) for _ in range(self.n_max if hasattr(self, "n_max") else 256)]
         pkv.pkv_plan_append(pool, ids, self.prompt)
         return (pool, ids)
@@ -446,15 +467,15 @@ class ChatRunner(DecodeRunner):
 class ForkedRunner(DecodeRunner):
     name = "forked"
 
-    def __init__(self, torch, pkv, dev, total_steps, n_branch=64):
+    def __init__(self, torch, pkv, dev, total_steps, n_branch=64, kv_dtype="bf16"):
         super().__init__(torch, pkv, dev, total_steps)
         wl = W.forked(n_branch=n_branch)
-        self.wl, self.g, self.seed = wl, wl.geometry, wl.seed
+        self.wl, self.seed = wl, wl.seed
+        self._set_geometry(with_kv_dtype(wl.geometry, kv_dtype))
         g = self.g
         self.n_max = n_branch
         self.scale = wl.scale
-        self.pool = pkv.pkv_pool_create(g.L, g.H_q, g.H_kv, g.d_head, g.block_size, g.dtype, g.num_blocks,
-                                        wl.free_order)
+        self.pool = self._new_pool(wl.free_order)
         self.kp = W.device_normal(self.seed, "k_pool", g.pool_shape(), g.dtype, dev)
         self.vp = W.device_normal(self.seed, "v_pool", g.pool_shape(), g.dtype, dev)
         parent = pkv.pkv_seq_create(self.pool)
@@ -464,8 +485,8 @@ class ForkedRunner(DecodeRunner):
         slots, cows = pkv.pkv_plan_append(self.pool, self.ids, suffix)
         pkv.pkv_copy_blocks(self.pool, cows, self.kp, self.vp)
         if len(slots):
-            kn = W.device_normal(self.seed, "suffix_k", (len(slots), g.H_kv, g.d_head), g.dtype, dev)
-            vn = W.device_normal(self.seed, "suffix_v", (len(slots), g.H_kv, g.d_head), g.dtype, dev)
+            kn = W.device_normal(self.seed, "suffix_k", (len(slots), g.H_kv, g.d_head), self.act, dev)
+            vn = W.device_normal(self.seed, "suffix_v", (len(slots), g.H_kv, g.d_head), self.act, dev)
             pkv.pkv_append_kv(self.pool, 0, kn, vn, torch.from_numpy(slots).to(dev), self.kp, self.vp)
         self.unique_tokens = int(wl.lengths[0]) + sum(suffix)
         self.ids_np = np.array(self.ids, np.int32)
@@ -473,7 +494,8 @@ class ForkedRunner(DecodeRunner):
         self.inputs_for_steps("forked")
         self._alloc_common(n_branch)
         self.config = {"workload": "forked: 16,376-token prefix forked into 64 branches (refcount 65) with "
-                                   "U[0,2048] suffixes, 64 query / 8 KV heads, d_head 128, bf16, 16-token blocks",
+                                   f"U[0,2048] suffixes, 64 query / 8 KV heads, d_head 128, {kv_desc(g)}, 16-token "
+                                   "blocks",
                        "n_seq": n_branch, "prefix": int(wl.lengths[0]), "H_q": g.H_q, "H_kv": g.H_kv,
                        "d_head": g.d_head, "block_size": g.block_size,
                        "l2": "logical K/V per step 4.5 GB > L2; the 67 MB shared prefix is re-read by every branch",
@@ -489,7 +511,8 @@ class TinyRunner(DecodeRunner):
     def __init__(self, torch, pkv, dev, total_steps):
         super().__init__(torch, pkv, dev, total_steps)
         wl = W.tiny()
-        self.wl, self.g, self.seed = wl, wl.geometry, wl.seed
+        self.wl, self.seed = wl, wl.seed
+        self._set_geometry(wl.geometry)
         g = self.g
         self.n_max = len(wl.lengths)
         self.scale = wl.scale
@@ -512,15 +535,24 @@ class TinyRunner(DecodeRunner):
         return self.ids_np
 
 
+def with_kv_dtype(g, kv_dtype):
+    return W.Geometry(g.L, g.H_q, g.H_kv, g.d_head, g.block_size, kv_dtype, g.num_blocks)
+
+
+def kv_desc(g):
+    return "FP8 E4M3 K/V (bf16 q/out)" if g.dtype == "e4m3" else g.dtype
+
+
 RUNNERS = {"agent32k": AgentRunner, "chat": ChatRunner, "forked": ForkedRunner, "tiny": TinyRunner}
 
 
 def run_decode(args, torch, pkv, dev, world, rank):
     total = args.warmup + args.steps + 2 + args.steps  # timed region, then e2e warm-up + e2e steps
+    kw = {} if args.workload == "tiny" else {"kv_dtype": args.kv_dtype}
     if args.workload == "agent32k" and (args.context or args.n_seq):
-        r = AgentRunner(torch, pkv, dev, total, n_seq=args.n_seq or 48, context=args.context or 32768)
+        r = AgentRunner(torch, pkv, dev, total, n_seq=args.n_seq or 48, context=args.context or 32768, **kw)
     else:
-        r = RUNNERS[args.workload](torch, pkv, dev, total)
+        r = RUNNERS[args.workload](torch, pkv, dev, total, **kw)
     g = r.g
     launches0 = None
     for t in range(args.warmup):
@@ -571,8 +603,9 @@ def run_decode(args, torch, pkv, dev, world, rank):
     peak, peak_kind = load_peaks()
     value = world * kv_total / (ms_max / 1e3) / 1e9
     traffic = args.traffic
-    if traffic is None and TRAFFIC_RECORD["ratio"] and TRAFFIC_RECORD["sources_sha256"] == decode_sources_digest():
-        traffic = round(TRAFFIC_RECORD["ratio"] * alg_avg)
+    rec = TRAFFIC_RECORD.get(g.dtype)
+    if traffic is None and rec and rec["sources_sha256"] == decode_sources_digest():
+        traffic = round(rec["ratio"] * alg_avg)
     achieved = alg_avg / (dec_avg / 1e3) / 1e9
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -903,7 +936,7 @@ def oracle_sample_decode(runner, n_sample: int, reps: int = 1):
     used = sorted({int(b) for i in range(len(ids)) for b in tables[i, : -(-int(lens[i]) // g.block_size)]})
     remap = {b: j for j, b in enumerate(used)}
     idx = torch.tensor(used, dtype=torch.long, device=runner.kp.device)
-    store = {"bf16": np.uint16, "f16": np.float16, "f32": np.float32}[g.dtype]
+    store = {"bf16": np.uint16, "f16": np.float16, "f32": np.float32}[runner.act]
 
     def host_copy(t):
         x = t.index_select(0, idx).cpu().contiguous()
@@ -917,10 +950,11 @@ def oracle_sample_decode(runner, n_sample: int, reps: int = 1):
     for i in range(len(ids)):
         nb = -(-int(lens[i]) // g.block_size)
         ct[i, :nb] = [remap[int(b)] for b in tables[i, :nb]]
-    q = W.normal(runner.seed, "oracle_q", (len(ids), g.H_q, g.d_head), g.dtype).astype(store)
+    q = W.normal(runner.seed, "oracle_q", (len(ids), g.H_q, g.d_head), runner.act).astype(store)
     t0 = time.perf_counter()
     for _ in range(reps):
-        oracle.decode_attention(gc, 0, q, hk, hv, ct, lens, runner.scale)
+        oracle.decode_attention(gc, 0, q, hk, hv, ct, lens, runner.scale, k_scale=runner.kv_scales[0],
+                                v_scale=runner.kv_scales[1])
     dt = (time.perf_counter() - t0) / reps
     kvb = int(lens.astype(np.int64).sum()) * g.H_kv * g.d_head * g.elem_bytes * 2
     return kvb / dt / 1e9, dt, f"oracle attention over {len(ids)} of the batch's sequences " \
@@ -992,15 +1026,20 @@ def reference_arm(args, world, rank):
                 "forked": (lambda: W.forked(), 4),
                 "tiny": (lambda: W.tiny(), 8)}[args.workload]
         wl, n_s = spec[0](), spec[1]
-        g = wl.geometry
+        g = wl.geometry if args.workload == "tiny" else with_kv_dtype(wl.geometry, args.kv_dtype)
+        act = oracle.q_dtype(g)
         lens = np.array([int(x) for x in wl.lengths[:n_s]], np.int32) if args.workload != "forked" else \
             np.array([int(wl.lengths[0]) + int(s) for s in wl.extra["suffix"][:n_s]], np.int32)
         if args.workload == "chat":
             lens = np.array([int(wl.lengths[i]) + 1 for i in range(n_s)], np.int32)
         nblk = [-(-int(x) // g.block_size) for x in lens]
         gs = W.Geometry(g.L, g.H_q, g.H_kv, g.d_head, g.block_size, g.dtype, sum(nblk))
-        kp = W.normal(wl.seed, "ref_k", gs.pool_shape(), g.dtype)
-        vp = W.normal(wl.seed, "ref_v", gs.pool_shape(), g.dtype)
+        if g.dtype == "e4m3":  # codes of N(0,1) draws
+            kp = oracle.e4m3_encode(W.normal(wl.seed, "ref_k", gs.pool_shape(), "f32"))
+            vp = oracle.e4m3_encode(W.normal(wl.seed, "ref_v", gs.pool_shape(), "f32"))
+        else:
+            kp = W.normal(wl.seed, "ref_k", gs.pool_shape(), g.dtype)
+            vp = W.normal(wl.seed, "ref_v", gs.pool_shape(), g.dtype)
         perm = W.permutation(wl.seed, "ref_perm", sum(nblk))
         Wd = max(nblk)
         tables = np.zeros((n_s, Wd), np.int32)
@@ -1008,7 +1047,7 @@ def reference_arm(args, world, rank):
         for i, nb in enumerate(nblk):
             tables[i, :nb] = perm[o:o + nb]
             o += nb
-        q = W.normal(wl.seed, "ref_q", (n_s, g.H_q, g.d_head), g.dtype)
+        q = W.normal(wl.seed, "ref_q", (n_s, g.H_q, g.d_head), act)
         times = []
         for step in range(args.warmup + args.steps):
             t0 = time.perf_counter()
@@ -1065,6 +1104,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--context", type=int, default=0, help="agent workload: tokens per sequence (default 32768)")
     ap.add_argument("--n-seq", type=int, default=0, help="agent workload: sequences (default 48)")
+    ap.add_argument("--kv-dtype", choices=["bf16", "e4m3"], default="bf16",
+                    help="decode workloads: stored K/V type (e4m3 = FP8 pool, bf16 q/out)")
     ap.add_argument("--traffic", type=float, default=None,
                     help="ncu dram bytes per decode launch, if captured for this kernel version")
     args = ap.parse_args()

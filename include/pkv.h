@@ -42,6 +42,18 @@
  *   block_tables   : int32 [n_seq][W]; entry l is the physical block of logical
  *                    block l = floor(t / block_size) ([KVM] Definition 0.1).
  *   Query head h reads KV head floor(h / G), G = H_q / H_kv.
+ *
+ * FP8 pools (dtype PKV_E4M3; [KVM] PagedAttention model: b_elem = 1 byte for FP8)
+ *   K and V are stored as OCP FP8 E4M3 bytes (1 sign, 4 exponent bits with bias 7,
+ *   3 fraction bits, largest finite 448) and read as code * k_scale (keys) or
+ *   code * v_scale (values), one scale of each per pool (pkv_pool_set_kv_scales).
+ *   Everything around such a pool is bfloat16: k_new / v_new of pkv_append_kv and
+ *   pkv_decode_step, q and out.  An append stores the E4M3 code nearest to the
+ *   binary32 quotient x / scale (ties to even; magnitudes beyond 448 stored as 448;
+ *   a negative value that rounds to zero is stored as -0).  d_head must be a
+ *   multiple of 8.  The tensor-core attention path computes q K^T and P V with
+ *   binary16 operands, so |q| must stay below 65504 there; the codes convert to
+ *   binary16 exactly.
  */
 #ifndef PKV_H
 #define PKV_H
@@ -70,7 +82,7 @@ enum pkv_status {
   PKV_ERR_UNSUPPORTED = 8    /* geometry or dtype this build does not handle */
 };
 
-enum pkv_dtype { PKV_F32 = 0, PKV_F16 = 1, PKV_BF16 = 2 };
+enum pkv_dtype { PKV_F32 = 0, PKV_F16 = 1, PKV_BF16 = 2, PKV_E4M3 = 3 };
 
 /* Pool geometry ([KVM] Eq. 1: m_token = 2 * L * H_kv * d_head * b). */
 typedef struct pkv_geometry {
@@ -103,6 +115,13 @@ const char* pkv_status_name(int status);
 int pkv_pool_create(const pkv_geometry* geometry, const int32_t* initial_free_order, pkv_pool** out);
 int pkv_pool_destroy(pkv_pool* pool);
 int pkv_pool_geometry(const pkv_pool* pool, pkv_geometry* out);
+
+/* Scales of an FP8 pool (see "FP8 pools" above): stored keys read as code * k_scale,
+ * values as code * v_scale; both start at 1.  Later appends and attention calls use
+ * the new values; codes already stored are not rewritten.  Errors: INVALID_ARG (a
+ * scale that is not finite and > 0), UNSUPPORTED (a 16/32-bit pool). */
+int pkv_pool_set_kv_scales(pkv_pool* pool, float k_scale, float v_scale);
+int pkv_pool_kv_scales(const pkv_pool* pool, float* k_scale, float* v_scale);
 
 /* New empty sequence. */
 int pkv_seq_create(pkv_pool* pool, int32_t* seq_id);
@@ -181,8 +200,9 @@ int pkv_decode_workspace_size(const pkv_pool* pool, int32_t n_seq, size_t* bytes
  *   workspace   : device, >= pkv_decode_workspace_size bytes, 256-byte aligned;
  *                 no state survives between calls.
  * Calls on one workspace must not overlap on the GPU.
- * bf16/f16 with d_head 64 or 128, G <= 8 and B a multiple of 16 run on the
- * tensor-core path (TMA-staged tiles, mma.sync); other geometries on CUDA cores. */
+ * bf16/f16 with d_head 64 or 128, and FP8 with d_head 128, with G <= 8 and B a
+ * multiple of 16 run on the tensor-core path (TMA-staged tiles, mma.sync); other
+ * geometries on CUDA cores. */
 int pkv_decode_attention(const pkv_pool* pool, int32_t layer, const void* q, const void* k_pool,
                          const void* v_pool, const int32_t* block_tables, int32_t W, const int32_t* seq_lens,
                          int32_t n_seq, float scale, void* out, void* workspace, size_t ws_bytes,
@@ -247,8 +267,8 @@ int pkv_decode_attention_noalloc(const pkv_pool* pool, int32_t layer, const void
  *                error word and its extra rows are not computed).
  *   block_tables, W, seq_lens: as for pkv_decode_attention (C_s <= len_s <= W*B).
  * bf16/f16 with d_head 64 or 128 and B a multiple of 16 run on tensor cores (one CTA
- * per 128 (query, head) rows, 64-key tiles staged by TMA); other geometries on CUDA
- * cores.  No workspace. */
+ * per 128 (query, head) rows, 64-key tiles staged by TMA); other geometries, and FP8
+ * pools, on CUDA cores.  No workspace. */
 int pkv_prefill_attention(const pkv_pool* pool, int32_t layer, const void* q, const int32_t* q_offsets, int32_t n_tok,
                           int32_t max_q, const void* k_pool, const void* v_pool, const int32_t* block_tables, int32_t W,
                           const int32_t* seq_lens, int32_t n_seq, float scale, void* out, pkv_stream_t stream);

@@ -23,11 +23,11 @@ __all__ = [
     "pkv_decode_step", "pkv_prefill_attention",
     "pkv_copy_blocks", "pkv_swap_out",
     "pkv_swap_in", "pkv_seq_host_slots", "pkv_seq_residency", "TIER_HBM", "TIER_HOST", "pkv_pool_set_swap_engine", "pkv_check_device_error", "pkv_launch_count",
-    "pkv_selftest_bounded_wait",
+    "pkv_selftest_bounded_wait", "pkv_pool_set_kv_scales", "pkv_pool_kv_scales",
 ]
 
-F32, F16, BF16 = 0, 1, 2
-DTYPES = {"f32": F32, "f16": F16, "bf16": BF16}
+F32, F16, BF16, E4M3 = 0, 1, 2, 3
+DTYPES = {"f32": F32, "f16": F16, "bf16": BF16, "e4m3": E4M3}
 _HERE = os.path.dirname(os.path.abspath(__file__))
 
 
@@ -91,6 +91,8 @@ def _L():
             "pkv_seq_host_slots": ([vp, i32, P64, i32, P32], ctypes.c_int),
             "pkv_seq_residency": ([vp, i32, P32], ctypes.c_int),
             "pkv_pool_set_swap_engine": ([vp, i32], ctypes.c_int),
+            "pkv_pool_set_kv_scales": ([vp, ctypes.c_float, ctypes.c_float], ctypes.c_int),
+            "pkv_pool_kv_scales": ([vp, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_float)], ctypes.c_int),
             "pkv_check_device_error": ([vp, P32, P64], ctypes.c_int),
             "pkv_launch_count": ([], ctypes.c_uint64),
             "pkv_selftest_bounded_wait": ([i64, vp], ctypes.c_int),
@@ -284,6 +286,17 @@ def pkv_free_list(pool: PoolLike) -> np.ndarray:
 
 def pkv_pool_set_swap_engine(pool: PoolLike, engine: int) -> None:
     _check(_L().pkv_pool_set_swap_engine(_h(pool), engine), "pkv_pool_set_swap_engine")
+
+
+def pkv_pool_set_kv_scales(pool: PoolLike, k_scale: float, v_scale: float) -> None:
+    """FP8 pools: stored keys read as code * k_scale, values as code * v_scale."""
+    _check(_L().pkv_pool_set_kv_scales(_h(pool), k_scale, v_scale), "pkv_pool_set_kv_scales")
+
+
+def pkv_pool_kv_scales(pool: PoolLike):
+    k, v = ctypes.c_float(), ctypes.c_float()
+    _check(_L().pkv_pool_kv_scales(_h(pool), ctypes.byref(k), ctypes.byref(v)), "pkv_pool_kv_scales")
+    return k.value, v.value
 
 
 TIER_HBM, TIER_HOST = 0, 1

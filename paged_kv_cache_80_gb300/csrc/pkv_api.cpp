@@ -16,6 +16,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cmath>
 #include <cstring>
 #include <string>
 #include <unordered_map>
@@ -72,8 +73,10 @@ int check_geometry(const pkv_geometry* g) {
     return fail(PKV_ERR_INVALID_ARG, "geometry fields must be positive");
   if (g->H_q % g->H_kv) return fail(PKV_ERR_INVALID_ARG, "H_q must be a multiple of H_kv");
   if (g->d_head % 2 || g->d_head > 256) return fail(PKV_ERR_INVALID_ARG, "d_head must be even and <= 256");
-  if (g->dtype != PKV_F32 && g->dtype != PKV_F16 && g->dtype != PKV_BF16)
-    return fail(PKV_ERR_UNSUPPORTED, "dtype must be PKV_F32, PKV_F16 or PKV_BF16");
+  if (g->dtype != PKV_F32 && g->dtype != PKV_F16 && g->dtype != PKV_BF16 && g->dtype != PKV_E4M3)
+    return fail(PKV_ERR_UNSUPPORTED, "dtype must be PKV_F32, PKV_F16, PKV_BF16 or PKV_E4M3");
+  if (g->dtype == PKV_E4M3 && g->d_head % 8)
+    return fail(PKV_ERR_UNSUPPORTED, "an FP8 pool needs d_head a multiple of 8");
   if (g->num_blocks >= (int64_t(1) << 31)) return fail(PKV_ERR_INVALID_ARG, "num_blocks must be < 2^31");
   if (g->num_blocks * g->block_size >= (int64_t(1) << 31))
     return fail(PKV_ERR_INVALID_ARG, "num_blocks * block_size must be < 2^31 (int32 slots)");
@@ -371,6 +374,26 @@ int pkv_free_list(const pkv_pool* pool, int32_t* out, int64_t* n) {
   const Pool& P = *as_pool(pool);
   for (int64_t i = 0; i < P.free.size(); ++i) out[i] = P.free.front_at(i);
   *n = P.free.size();
+  return PKV_OK;
+}
+
+int pkv_pool_set_kv_scales(pkv_pool* pool, float k_scale, float v_scale) {
+  pkv::clear_error();
+  if (!pool) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
+  Pool& P = *as_pool(pool);
+  if (P.geo.dtype != PKV_E4M3) return fail(PKV_ERR_UNSUPPORTED, "scales apply to FP8 (PKV_E4M3) pools only");
+  if (!(std::isfinite(k_scale) && k_scale > 0.f && std::isfinite(v_scale) && v_scale > 0.f))
+    return fail(PKV_ERR_INVALID_ARG, "scales must be finite and > 0");
+  P.k_scale = k_scale;
+  P.v_scale = v_scale;
+  return PKV_OK;
+}
+
+int pkv_pool_kv_scales(const pkv_pool* pool, float* k_scale, float* v_scale) {
+  pkv::clear_error();
+  if (!pool || !k_scale || !v_scale) return fail(PKV_ERR_INVALID_ARG, "NULL argument");
+  *k_scale = as_pool(pool)->k_scale;
+  *v_scale = as_pool(pool)->v_scale;
   return PKV_OK;
 }
 

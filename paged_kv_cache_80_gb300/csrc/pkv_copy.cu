@@ -9,6 +9,7 @@
 // "Asynchronous paged swapping" (block frames move between HBM and pinned host
 // DRAM).  All of these are pure byte streams: the kernels use 16-byte vector
 // loads and stores with several transactions in flight per thread.
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -99,6 +100,46 @@ __global__ void __launch_bounds__(256) append_kernel(const AppendArgs a) {
   }
 }
 
+// Append into an FP8 pool ("KV Cache Management", PagedAttention model: b_elem = 1
+// for FP8): one thread per 8 elements of a (layer, token, head) row -- 16 bytes of
+// bf16 in, 8 bytes of E4M3 codes out.  Each code is the E4M3 value nearest to the
+// binary32 quotient x / scale (IEEE division, then round to nearest even with
+// saturation to the largest finite value, 448).
+__device__ __forceinline__ uint32_t quant4(uint32_t w0, uint32_t w1, float s) {
+  const float x[4] = {__uint_as_float(w0 << 16), __uint_as_float(w0 & 0xffff0000u), __uint_as_float(w1 << 16),
+                      __uint_as_float(w1 & 0xffff0000u)};
+  uint32_t r = 0;
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    r |= static_cast<uint32_t>(__nv_cvt_float_to_fp8(__fdiv_rn(x[j], s), __NV_SATFINITE, __NV_E4M3)) << (8 * j);
+  return r;
+}
+
+__global__ void __launch_bounds__(256) append_e4m3_kernel(const AppendArgs a, float k_scale, float v_scale) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < a.total; idx += stride) {
+    int64_t r = idx / a.vec_per_row;
+    const int c = static_cast<int>(idx - r * a.vec_per_row);
+    const int h = static_cast<int>(r % a.H_kv);
+    r /= a.H_kv;
+    const int i = static_cast<int>(r % a.n_tok);
+    const int l = static_cast<int>(r / a.n_tok);
+    const int32_t slot = a.slots[i];
+    if (slot < 0 || slot >= a.n_slots) {
+      if (c == 0 && h == 0 && l == 0) record_error(a.err, DERR_APPEND_SLOT, slot);
+      continue;
+    }
+    const int layer = a.layer < 0 ? l : a.layer;
+    const int64_t blk = slot / a.B, off = slot - blk * a.B;
+    const int64_t src = ((static_cast<int64_t>(l) * a.n_tok + i) * a.H_kv + h) * a.vec_per_row + c;
+    const int64_t dst = (((blk * a.L + layer) * a.H_kv + h) * a.B + off) * a.vec_per_row + c;
+    const uint4 k = reinterpret_cast<const uint4*>(a.k_new)[src];
+    const uint4 v = reinterpret_cast<const uint4*>(a.v_new)[src];
+    reinterpret_cast<uint2*>(a.k_pool)[dst] = make_uint2(quant4(k.x, k.y, k_scale), quant4(k.z, k.w, k_scale));
+    reinterpret_cast<uint2*>(a.v_pool)[dst] = make_uint2(quant4(v.x, v.y, v_scale), quant4(v.z, v.w, v_scale));
+  }
+}
+
 static int vec_width(int64_t row_bytes, const void* const* ptrs, int n) {
   uintptr_t m = static_cast<uintptr_t>(row_bytes);
   for (int i = 0; i < n; ++i) m |= reinterpret_cast<uintptr_t>(ptrs[i]);
@@ -125,10 +166,14 @@ int launch_append(const Pool& P, int32_t layer, const void* k_new, const void* v
   void* err = nullptr;
   if (int rc = device_error_word(&err)) return rc;
   const auto& g = P.geo;
+  const bool fp8 = g.dtype == PKV_E4M3;
   const int64_t row = static_cast<int64_t>(g.d_head) * elem_size(g.dtype);
   const void* ptrs[4] = {k_new, v_new, k_pool, v_pool};
   const int vec = vec_width(row, ptrs, 4);
   if (vec < 2) return fail(PKV_ERR_INVALID_ARG, "append: buffers must be 2-byte aligned");
+  if (fp8 && ((reinterpret_cast<uintptr_t>(k_new) | reinterpret_cast<uintptr_t>(v_new)) & 15 ||
+              (reinterpret_cast<uintptr_t>(k_pool) | reinterpret_cast<uintptr_t>(v_pool)) & 7))
+    return fail(PKV_ERR_INVALID_ARG, "append to an FP8 pool: k_new/v_new must be 16-byte and the pools 8-byte aligned");
   AppendArgs a;
   a.k_new = static_cast<const char*>(k_new);
   a.v_new = static_cast<const char*>(v_new);
@@ -141,7 +186,7 @@ int launch_append(const Pool& P, int32_t layer, const void* k_new, const void* v
   a.B = g.block_size;
   a.L = g.L;
   a.layer = layer;
-  a.vec_per_row = static_cast<int32_t>(row / vec);
+  a.vec_per_row = fp8 ? g.d_head / 8 : static_cast<int32_t>(row / vec);
   a.n_slots = g.num_blocks * g.block_size;
   const int layers = layer < 0 ? g.L : 1;
   a.total = static_cast<int64_t>(layers) * n_tok * g.H_kv * a.vec_per_row;
@@ -149,7 +194,8 @@ int launch_append(const Pool& P, int32_t layer, const void* k_new, const void* v
   const int64_t want = (a.total + threads - 1) / threads;
   const int blocks = static_cast<int>(std::min<int64_t>(want, static_cast<int64_t>(sm_count()) * 16));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  switch (vec) {
+  if (fp8) append_e4m3_kernel<<<blocks, threads, 0, s>>>(a, P.k_scale, P.v_scale);
+  else switch (vec) {
     case 16: append_kernel<16><<<blocks, threads, 0, s>>>(a); break;
     case 8: append_kernel<8><<<blocks, threads, 0, s>>>(a); break;
     case 4: append_kernel<4><<<blocks, threads, 0, s>>>(a); break;

@@ -29,11 +29,20 @@
 //   * A pair fully inside one warp's range is normalised and written directly; a
 //     pair split across warps leaves (m, l, O) partials that a merge kernel
 //     combines with the same rule.
+// FP8 pools (E4M3 codes, "KV Cache Management" b_elem = 1): the same kernel with
+//   16 x 128-byte tiles (one TMA box each); every lane reads its operand bytes with
+//   16-byte shared loads and converts code pairs to binary16 (exact), so the mma
+//   runs on f16 operands (q rounded to f16 once per pair).  The contraction index of
+//   q K^T is permuted so that a lane's K bytes are contiguous (lane c of a quad owns
+//   d = 32c .. 32c+31), and the d rows of V^T so that a lane's V bytes are (quad row
+//   g owns d = 16g .. 16g+15); the k_scale is folded into the softmax scale and the
+//   v_scale into the final normalisation.
 // CUDA-core path (fp32, or other geometries): one CTA per (sequence, KV head),
 // warps stride over tokens with an online softmax per head, then merge in smem.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
@@ -51,6 +60,10 @@
 namespace pkv {
 
 namespace {
+
+struct E4M3 {  // one stored OCP FP8 E4M3 element
+  uint8_t bits;
+};
 
 constexpr int TILE = 16;   // tokens per tile (the mma M dimension)
 constexpr int GPAD = 8;    // query heads per mma N dimension
@@ -72,8 +85,9 @@ struct DecodeArgs {
   int* err;
   int64_t num_blocks;
   int32_t n_seq, W, H_q, H_kv, G, L, layer, B;
-  int32_t D, elem;   // head dimension, bytes per element
-  float scale_log2;  // scale * log2(e)
+  int32_t D, elem;   // head dimension, bytes per activation element (q, out)
+  float scale_log2;  // scale * log2(e) (* k_scale for an FP8 pool)
+  float v_mul;       // 1, or v_scale for an FP8 pool
   int32_t total_warps;
 };
 
@@ -166,20 +180,21 @@ __global__ void __launch_bounds__(1024) plan_kernel(const DecodeArgs a) {
 
 // --------------------------------------------------------------------------- tensor-core path
 
-template <int D>
+template <int D, int EB = 2>  // EB: bytes per stored K/V element
 struct TcCfg {
-  static constexpr int KV_TILE_BYTES = TILE * D * 2;      // one 16 x D tile of K (or V)
-  static constexpr int Q_BYTES = GPAD * D * 2;             // up to 8 query rows
+  static constexpr int KV_TILE_BYTES = TILE * D * EB;     // one 16 x D tile of K (or V)
+  static constexpr int Q_BYTES = GPAD * D * 2;             // up to 8 query rows (16-bit)
   static constexpr int STAGE_BYTES = 2 * KV_TILE_BYTES + Q_BYTES;
-  static constexpr int NBOX = D / 64;                      // 128-byte TMA boxes per tile row
+  static constexpr int NBOX = D * EB / 128;                // 128-byte TMA boxes per tile row
+  static constexpr int BOX_ELEMS = 128 / EB;
   static constexpr int NKC = D / 16;                       // 16-wide chunks of d_head
   static constexpr int PSTRIDE = NKC * 32 * 4 + 2 * GPAD;  // floats per partial slot
   static_assert(STAGE_BYTES % 1024 == 0, "stages must keep 1024-byte alignment for the swizzle");
 };
 
-template <int D, int S, int NW>
+template <int D, int EB, int S, int NW>
 struct TcSmem {
-  static constexpr int WARP_BYTES = S * TcCfg<D>::STAGE_BYTES + 64 * 16 + S * 8 + 8;
+  static constexpr int WARP_BYTES = S * TcCfg<D, EB>::STAGE_BYTES + 64 * 16 + S * 8 + 8;
   static constexpr int WARP_STRIDE = (WARP_BYTES + 1023) / 1024 * 1024;
   static constexpr int TOTAL = NW * WARP_STRIDE + 1024;  // + alignment slack
 };
@@ -202,10 +217,76 @@ __device__ __forceinline__ __nv_bfloat16 from_float<__nv_bfloat16>(float x) { re
 template <>
 __device__ __forceinline__ __half from_float<__half>(float x) { return __float2half_rn(x); }
 
+// Two E4M3 codes (low byte first) to two binary16 values (exact).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t b16) {
+  const __half2_raw r = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(b16 & 0xffffu), __NV_E4M3);
+  return static_cast<uint32_t>(r.x) | (static_cast<uint32_t>(r.y) << 16);
+}
+
+// Two bfloat16 values (low half first) to two binary16 values (round to nearest).
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
+  __half2 h = __floats2half2_rn(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+
+__device__ __forceinline__ uint32_t word_of(const uint4& v, int i) {
+  return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
+}
+
+// Write the G output rows of one (sequence, KV head) pair from a lane's accumulator
+// fragment acc[c] (the O^T fragment of d-chunk c), scaled by i0 (head h0) and i1
+// (head h0 + 1).  16-bit pools: chunk c, quad row r holds d = 16c + r (x, y) and
+// d + 8 (z, w).  FP8 pools: quad row r holds d = 16r + 2c (x, y) and d + 1 (z, w),
+// so a lane has 16 consecutive d of its two heads (two 16-byte stores per head).
+template <typename TO, int D, bool F8>
+__device__ __forceinline__ void store_group(TO* out, const float4 (&acc)[D / 16], float i0, float i1, int lane,
+                                            int G) {
+  const int h0 = 2 * (lane & 3), trow = lane >> 2;
+  if constexpr (F8) {
+    static_assert(D == 128, "FP8 tiles are 128 bytes wide");
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      if (h0 + hh >= G) continue;
+      const float sc = hh ? i1 : i0;
+      uint32_t w[8];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        __nv_bfloat162 v = __floats2bfloat162_rn((hh ? acc[c].y : acc[c].x) * sc, (hh ? acc[c].w : acc[c].z) * sc);
+        w[c] = *reinterpret_cast<uint32_t*>(&v);
+      }
+      uint4* dst = reinterpret_cast<uint4*>(out + (h0 + hh) * D + 16 * trow);
+      dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+      dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+    }
+  } else {
+#pragma unroll
+    for (int c = 0; c < D / 16; ++c) {
+      const int dd = 16 * c + trow;
+      if (h0 < G) {
+        out[h0 * D + dd] = from_float<TO>(acc[c].x * i0);
+        out[h0 * D + dd + 8] = from_float<TO>(acc[c].z * i0);
+      }
+      if (h0 + 1 < G) {
+        out[(h0 + 1) * D + dd] = from_float<TO>(acc[c].y * i1);
+        out[(h0 + 1) * D + dd + 8] = from_float<TO>(acc[c].w * i1);
+      }
+    }
+  }
+}
+
 // Merge the partials of one split pair (contributing warps wa..wb) and write its
 // G output rows.  Run by one whole warp; lane l owns float4 l of every d-chunk.
 // Partials are read through L2 (ld.global.cg): other SMs wrote them.
-template <typename T, int D>
+template <typename TO, int D, bool F8>
 __device__ __forceinline__ void merge_pair(const DecodeArgs& a, int s, int g, int pbeg, int wa, int wb, int R,
                                            int lane) {
   using C = TcCfg<D>;
@@ -246,21 +327,9 @@ __device__ __forceinline__ void merge_pair(const DecodeArgs& a, int s, int g, in
     M0 = n0;
     M1 = n1;
   }
-  const float i0 = 1.f / L0, i1 = 1.f / L1;
-  T* out = static_cast<T*>(a.out) + (static_cast<int64_t>(s) * a.H_q + g * a.G) * D;
-  const int trow = lane >> 2;
-#pragma unroll
-  for (int c = 0; c < C::NKC; ++c) {
-    const int dd = 16 * c + trow;
-    if (h0 < a.G) {
-      out[h0 * D + dd] = from_float<T>(acc[c].x * i0);
-      out[h0 * D + dd + 8] = from_float<T>(acc[c].z * i0);
-    }
-    if (h0 + 1 < a.G) {
-      out[(h0 + 1) * D + dd] = from_float<T>(acc[c].y * i1);
-      out[(h0 + 1) * D + dd + 8] = from_float<T>(acc[c].w * i1);
-    }
-  }
+  const float i0 = a.v_mul / L0, i1 = a.v_mul / L1;
+  TO* out = static_cast<TO*>(a.out) + (static_cast<int64_t>(s) * a.H_q + g * a.G) * D;
+  store_group<TO, D, F8>(out, acc, i0, i1, lane, a.G);
 }
 
 // Descriptor of one tile, built by the warp a batch at a time:
@@ -272,9 +341,14 @@ template <typename T, int D, int S, int NW>
 __global__ void __launch_bounds__(NW * 32) decode_tc_kernel(const __grid_constant__ CUtensorMap tmk,
                                                             const __grid_constant__ CUtensorMap tmv,
                                                             const DecodeArgs a) {
-  using C = TcCfg<D>;
-  using SM = TcSmem<D, S, NW>;
-  constexpr bool BF16 = std::is_same<T, __nv_bfloat16>::value;
+  // T = stored K/V element; TA = q / out element; TM = mma operand type
+  constexpr bool F8 = std::is_same<T, E4M3>::value;
+  using TA = typename std::conditional<F8, __nv_bfloat16, T>::type;
+  using TM = typename std::conditional<F8, __half, T>::type;
+  constexpr bool BF16 = std::is_same<TM, __nv_bfloat16>::value;
+  constexpr int EB = F8 ? 1 : 2;
+  using C = TcCfg<D, EB>;
+  using SM = TcSmem<D, EB, S, NW>;
   extern __shared__ uint8_t smem_raw[];
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -361,12 +435,12 @@ __global__ void __launch_bounds__(NW * 32) decode_tc_kernel(const __grid_constan
     mbar_arrive_expect_tx(bar, 2 * C::KV_TILE_BYTES + (newpair ? a.G * D * 2 : 0));
 #pragma unroll
     for (int b = 0; b < C::NBOX; ++b) {
-      tma_load_2d(sk + b * (TILE * 128), &tmk, b * 64, d.x, bar);
-      tma_load_2d(sv + b * (TILE * 128), &tmv, b * 64, d.x, bar);
+      tma_load_2d(sk + b * (TILE * 128), &tmk, b * C::BOX_ELEMS, d.x, bar);
+      tma_load_2d(sv + b * (TILE * 128), &tmv, b * C::BOX_ELEMS, d.x, bar);
     }
     if (newpair) {
       const int s = d.y / a.H_kv, g = d.y - (d.y / a.H_kv) * a.H_kv;
-      const T* qsrc = static_cast<const T*>(a.q) + (static_cast<int64_t>(s) * a.H_q + g * a.G) * D;
+      const TA* qsrc = static_cast<const TA*>(a.q) + (static_cast<int64_t>(s) * a.H_q + g * a.G) * D;
       bulk_load(sk + 2 * C::KV_TILE_BYTES, qsrc, a.G * D * 2, bar);
     }
   };
@@ -382,6 +456,7 @@ __global__ void __launch_bounds__(NW * 32) decode_tc_kernel(const __grid_constan
   const int v_row = r8 + 8 * (mi >> 1), v_add = mi & 1;  // PV: A = V^T via .trans
   const int h0 = 2 * (lane & 3);                         // heads of this lane's columns
   const int trow = lane >> 2;                            // token row of c0/c1 (c2/c3: +8)
+  const int c4 = lane & 3;
 
   float o[C::NKC][4];
   uint32_t qf[C::NKC][2];
@@ -413,24 +488,51 @@ __global__ void __launch_bounds__(NW * 32) decode_tc_kernel(const __grid_constan
       for (int c = 0; c < C::NKC; ++c) o[c][0] = o[c][1] = o[c][2] = o[c][3] = 0.f;
       const uint8_t* qs = region + st * C::STAGE_BYTES + 2 * C::KV_TILE_BYTES;
       const bool live = trow < a.G;
+      if constexpr (F8) {
+        // step c of q K^T covers d = 32 c4 + 4c .. +3: (b0, b1) the first two, (b2, b3) the last two
 #pragma unroll
-      for (int c = 0; c < C::NKC; ++c) {
-        const uint32_t* p = reinterpret_cast<const uint32_t*>(qs + trow * D * 2 + (16 * c + h0) * 2);
-        qf[c][0] = live ? p[0] : 0u;
-        qf[c][1] = live ? p[4] : 0u;
+        for (int c = 0; c < C::NKC; ++c) {
+          const uint2 w = *reinterpret_cast<const uint2*>(qs + (trow * D + (D / 4) * c4 + 4 * c) * 2);
+          qf[c][0] = live ? bf16x2_to_f16x2(w.x) : 0u;
+          qf[c][1] = live ? bf16x2_to_f16x2(w.y) : 0u;
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < C::NKC; ++c) {
+          const uint32_t* p = reinterpret_cast<const uint32_t*>(qs + trow * D * 2 + (16 * c + h0) * 2);
+          qf[c][0] = live ? p[0] : 0u;
+          qf[c][1] = live ? p[4] : 0u;
+        }
       }
     }
 
     // ---- S^T = K q^T  (16 tokens x 8 heads), two accumulation chains
     float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+    if constexpr (F8) {
+      // K rows trow and trow + 8, bytes 32 c4 .. 32 c4 + 31 (16-byte chunks 2c4, 2c4 + 1; swizzle
+      // XOR = row & 7 = trow); step c takes bytes 4c .. 4c + 3 of each row
+      const uint4 ka0 = lds128(sk + trow * 128 + (((2 * c4) ^ trow) << 4));
+      const uint4 ka1 = lds128(sk + trow * 128 + (((2 * c4 + 1) ^ trow) << 4));
+      const uint4 kb0 = lds128(sk + (trow + 8) * 128 + (((2 * c4) ^ trow) << 4));
+      const uint4 kb1 = lds128(sk + (trow + 8) * 128 + (((2 * c4 + 1) ^ trow) << 4));
 #pragma unroll
-    for (int c = 0; c < C::NKC; ++c) {
-      const int chunk = 2 * (c & 3) + k_add;
-      const uint32_t addr = sk + (c >> 2) * (TILE * 128) + k_row * 128 + ((chunk ^ r8) << 4);
-      uint32_t a0, a1, a2, a3;
-      ldmatrix_x4(addr, a0, a1, a2, a3);
-      if (c & 1) mma_16816<BF16>(sb, a0, a1, a2, a3, qf[c][0], qf[c][1]);
-      else mma_16816<BF16>(sa, a0, a1, a2, a3, qf[c][0], qf[c][1]);
+      for (int c = 0; c < C::NKC; ++c) {
+        const uint32_t wa = word_of(c < 4 ? ka0 : ka1, c & 3), wb = word_of(c < 4 ? kb0 : kb1, c & 3);
+        const uint32_t a0 = e4m3x2_to_f16x2(wa), a1 = e4m3x2_to_f16x2(wb);
+        const uint32_t a2 = e4m3x2_to_f16x2(wa >> 16), a3 = e4m3x2_to_f16x2(wb >> 16);
+        if (c & 1) mma_16816<BF16>(sb, a0, a1, a2, a3, qf[c][0], qf[c][1]);
+        else mma_16816<BF16>(sa, a0, a1, a2, a3, qf[c][0], qf[c][1]);
+      }
+    } else {
+#pragma unroll
+      for (int c = 0; c < C::NKC; ++c) {
+        const int chunk = 2 * (c & 3) + k_add;
+        const uint32_t addr = sk + (c >> 2) * (TILE * 128) + k_row * 128 + ((chunk ^ r8) << 4);
+        uint32_t a0, a1, a2, a3;
+        ldmatrix_x4(addr, a0, a1, a2, a3);
+        if (c & 1) mma_16816<BF16>(sb, a0, a1, a2, a3, qf[c][0], qf[c][1]);
+        else mma_16816<BF16>(sa, a0, a1, a2, a3, qf[c][0], qf[c][1]);
+      }
     }
     float s0 = (sa[0] + sb[0]) * a.scale_log2, s1 = (sa[1] + sb[1]) * a.scale_log2;
     float s2 = (sa[2] + sb[2]) * a.scale_log2, s3 = (sa[3] + sb[3]) * a.scale_log2;
@@ -472,17 +574,36 @@ __global__ void __launch_bounds__(NW * 32) decode_tc_kernel(const __grid_constan
       o[c][3] *= c1;
     }
     // P^T (16 tokens x 8 heads) from the accumulator layout into the B-operand layout
-    const uint32_t pb0 = movmatrix_trans(pack2<T>(p0, p1));
-    const uint32_t pb1 = movmatrix_trans(pack2<T>(p2, p3));
+    const uint32_t pb0 = movmatrix_trans(pack2<TM>(p0, p1));
+    const uint32_t pb1 = movmatrix_trans(pack2<TM>(p2, p3));
 
     // ---- O^T += V^T P^T  (d_head x 8 heads)
+    if constexpr (F8) {
+      // token rows 2c4, 2c4 + 1, 2c4 + 8, 2c4 + 9, bytes 16 trow .. 16 trow + 15 of each (chunk trow;
+      // swizzle XOR = row & 7); step c takes d = 16 trow + 2c (A rows trow) and + 1 (rows trow + 8)
+      const int r0 = 2 * c4;
+      const uint4 v0 = lds128(sv + r0 * 128 + ((trow ^ r0) << 4));
+      const uint4 v1 = lds128(sv + (r0 + 1) * 128 + ((trow ^ (r0 + 1)) << 4));
+      const uint4 v2 = lds128(sv + (r0 + 8) * 128 + ((trow ^ r0) << 4));
+      const uint4 v3 = lds128(sv + (r0 + 9) * 128 + ((trow ^ (r0 + 1)) << 4));
 #pragma unroll
-    for (int c = 0; c < C::NKC; ++c) {
-      const int chunk = 2 * (c & 3) + v_add;
-      const uint32_t addr = sv + (c >> 2) * (TILE * 128) + v_row * 128 + ((chunk ^ r8) << 4);
-      uint32_t a0, a1, a2, a3;
-      ldmatrix_x4_trans(addr, a0, a1, a2, a3);
-      mma_16816<BF16>(o[c], a0, a1, a2, a3, pb0, pb1);
+      for (int c = 0; c < C::NKC; ++c) {
+        // bytes 2c, 2c + 1 of the 16: word c / 2, byte 2 (c & 1); interleave tokens (2c4, 2c4 + 1)
+        const unsigned sel = (c & 1) ? 0x7362u : 0x5140u;
+        const uint32_t x = __byte_perm(word_of(v0, c >> 1), word_of(v1, c >> 1), sel);
+        const uint32_t y = __byte_perm(word_of(v2, c >> 1), word_of(v3, c >> 1), sel);
+        mma_16816<BF16>(o[c], e4m3x2_to_f16x2(x), e4m3x2_to_f16x2(x >> 16), e4m3x2_to_f16x2(y),
+                        e4m3x2_to_f16x2(y >> 16), pb0, pb1);
+      }
+    } else {
+#pragma unroll
+      for (int c = 0; c < C::NKC; ++c) {
+        const int chunk = 2 * (c & 3) + v_add;
+        const uint32_t addr = sv + (c >> 2) * (TILE * 128) + v_row * 128 + ((chunk ^ r8) << 4);
+        uint32_t a0, a1, a2, a3;
+        ldmatrix_x4_trans(addr, a0, a1, a2, a3);
+        mma_16816<BF16>(o[c], a0, a1, a2, a3, pb0, pb1);
+      }
     }
 
     __syncwarp();  // every lane is done with this stage
@@ -498,20 +619,12 @@ __global__ void __launch_bounds__(NW * 32) decode_tc_kernel(const __grid_constan
       }
       const int s = cur_pair / a.H_kv, g = cur_pair - (cur_pair / a.H_kv) * a.H_kv;
       if (cur_started && (d.z & F_LAST)) {
-        const float i0 = 1.f / L0, i1 = 1.f / L1;
-        T* out = static_cast<T*>(a.out) + (static_cast<int64_t>(s) * a.H_q + g * a.G) * D;
+        const float i0 = a.v_mul / L0, i1 = a.v_mul / L1;
+        TA* out = static_cast<TA*>(a.out) + (static_cast<int64_t>(s) * a.H_q + g * a.G) * D;
+        float4 acc4[C::NKC];
 #pragma unroll
-        for (int c = 0; c < C::NKC; ++c) {
-          const int dd = 16 * c + trow;
-          if (h0 < a.G) {
-            out[h0 * D + dd] = from_float<T>(o[c][0] * i0);
-            out[h0 * D + dd + 8] = from_float<T>(o[c][2] * i0);
-          }
-          if (h0 + 1 < a.G) {
-            out[(h0 + 1) * D + dd] = from_float<T>(o[c][1] * i1);
-            out[(h0 + 1) * D + dd + 8] = from_float<T>(o[c][3] * i1);
-          }
-        }
+        for (int c = 0; c < C::NKC; ++c) acc4[c] = make_float4(o[c][0], o[c][1], o[c][2], o[c][3]);
+        store_group<TA, D, F8>(out, acc4, i0, i1, lane, a.G);
       } else {
         const int slot = cur_first_in_range ? 0 : 1;
         float* ps = a.partials + static_cast<int64_t>(gw * 2 + slot) * C::PSTRIDE;
@@ -539,7 +652,7 @@ __global__ void __launch_bounds__(NW * 32) decode_tc_kernel(const __grid_constan
         const int wa = pbeg / R, wb = (pbeg + nt - 1) / R;
         if (arrived == wb - wa) {
           __threadfence();
-          merge_pair<T, D>(a, s, g, pbeg, wa, wb, R, lane);
+          merge_pair<TA, D, F8>(a, s, g, pbeg, wa, wb, R, lane);
         }
       }
     }
@@ -809,6 +922,10 @@ template <>
 __device__ __forceinline__ float to_f<__half>(__half x) { return __half2float(x); }
 template <>
 __device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 x) { return __bfloat162float(x); }
+template <>
+__device__ __forceinline__ float to_f<E4M3>(E4M3 x) {
+  return __half2float(__half(__nv_cvt_fp8_to_halfraw(x.bits, __NV_E4M3)));
+}
 
 template <typename T>
 __device__ __forceinline__ T f_to(float x);
@@ -828,10 +945,12 @@ constexpr int SIMT_WARPS = 8;
 // into the running (m, l, O) of each head with one rescale per chunk.  The warps
 // are merged in shared memory at the end.
 // Attention of the G query rows at q (contiguous, d apart) over the first len tokens
-// of sequence s, KV head g; writes G rows at out.  Run by the whole CTA.
-template <typename T, int NPL>
-__device__ __forceinline__ void simt_attend(const DecodeArgs& a, const T* __restrict__ kp, const T* __restrict__ vp,
-                                            int d, int s, int g, int len, const T* q, T* out) {
+// of sequence s, KV head g; writes G rows at out.  Run by the whole CTA.  TS is the
+// stored K/V element, TA the q / out element.
+template <typename TS, typename TA, int NPL>
+__device__ __forceinline__ void simt_attend(const DecodeArgs& a, const TS* __restrict__ kp,
+                                            const TS* __restrict__ vp, int d, int s, int g, int len, const TA* q,
+                                            TA* out) {
   constexpr int TOK = NPL >= 8 ? 2 : (NPL >= 4 ? 4 : 8);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int G = a.G;
@@ -937,13 +1056,13 @@ __device__ __forceinline__ void simt_attend(const DecodeArgs& a, const T* __rest
         acc += so[(w * G + h) * d + e] * e2;
       }
     }
-    out[h * d + e] = f_to<T>(L > 0.f ? acc / L : 0.f);
+    out[h * d + e] = f_to<TA>(L > 0.f ? acc / L * a.v_mul : 0.f);
   }
 }
 
-template <typename T, int NPL>
-__global__ void __launch_bounds__(SIMT_WARPS * 32) decode_simt_kernel(const DecodeArgs a, const T* __restrict__ kp,
-                                                                        const T* __restrict__ vp, int d) {
+template <typename TS, typename TA, int NPL>
+__global__ void __launch_bounds__(SIMT_WARPS * 32) decode_simt_kernel(const DecodeArgs a, const TS* __restrict__ kp,
+                                                                        const TS* __restrict__ vp, int d) {
   const int pair = blockIdx.x;
   const int s = pair / a.H_kv, g = pair - (pair / a.H_kv) * a.H_kv;
   int len = a.seq_lens[s];
@@ -953,16 +1072,17 @@ __global__ void __launch_bounds__(SIMT_WARPS * 32) decode_simt_kernel(const Deco
     len = len < 0 ? 0 : static_cast<int>(maxlen);
   }
   const int64_t row = (static_cast<int64_t>(s) * a.H_q + g * a.G) * d;
-  simt_attend<T, NPL>(a, kp, vp, d, s, g, len, static_cast<const T*>(a.q) + row, static_cast<T*>(a.out) + row);
+  simt_attend<TS, TA, NPL>(a, kp, vp, d, s, g, len, static_cast<const TA*>(a.q) + row,
+                           static_cast<TA*>(a.out) + row);
 }
 
 // Chunked prefill on CUDA cores: one CTA per (query row, KV head).  The row's
 // sequence s is found in q_off; its position is len_s - C_s + (row - q_off[s]) and it
 // attends to every token up to and including that position.
-template <typename T, int NPL>
+template <typename TS, typename TA, int NPL>
 __global__ void __launch_bounds__(SIMT_WARPS * 32) prefill_simt_kernel(const DecodeArgs a, const int32_t* q_off,
-                                                                         const T* __restrict__ kp,
-                                                                         const T* __restrict__ vp, int d) {
+                                                                         const TS* __restrict__ kp,
+                                                                         const TS* __restrict__ vp, int d) {
   const int row = blockIdx.x, g = blockIdx.y;
   int lo = 0, hi = a.n_seq - 1;
   while (lo < hi) {
@@ -975,11 +1095,12 @@ __global__ void __launch_bounds__(SIMT_WARPS * 32) prefill_simt_kernel(const Dec
   const int64_t base = (static_cast<int64_t>(row) * a.H_q + g * a.G) * d;
   if (C < 0 || len < C || len > static_cast<int64_t>(a.W) * a.B) {
     if (threadIdx.x == 0 && g == 0 && row == q_off[s]) record_error(a.err, DERR_DECODE_LEN, s);
-    for (int k = threadIdx.x; k < a.G * d; k += blockDim.x) static_cast<T*>(a.out)[base + k] = f_to<T>(0.f);
+    for (int k = threadIdx.x; k < a.G * d; k += blockDim.x) static_cast<TA*>(a.out)[base + k] = f_to<TA>(0.f);
     return;
   }
   const int pos = len - C + (row - q_off[s]);
-  simt_attend<T, NPL>(a, kp, vp, d, s, g, pos + 1, static_cast<const T*>(a.q) + base, static_cast<T*>(a.out) + base);
+  simt_attend<TS, TA, NPL>(a, kp, vp, d, s, g, pos + 1, static_cast<const TA*>(a.q) + base,
+                           static_cast<TA*>(a.out) + base);
 }
 
 // --------------------------------------------------------------------------- host side
@@ -1004,11 +1125,13 @@ struct TcVariant {
   int stages, warps;
 };
 
-// Pipeline depth and warps per CTA; PKV_TC_VARIANT selects another for tuning.
-TcVariant tc_variant() {
-  static const TcVariant table[] = {{2, 4}, {3, 4}, {4, 4}, {2, 8}, {3, 2}};
-  int idx = 0;
-  if (const char* e = std::getenv("PKV_TC_VARIANT")) idx = std::max(0, std::min(4, std::atoi(e)));
+// Pipeline depth and warps per CTA; PKV_TC_VARIANT selects another for tuning.  An
+// FP8 tile carries half the bytes of a 16-bit one, so its default pipeline is twice
+// as deep (the same bytes in flight per SM).
+TcVariant tc_variant(const Pool& P) {
+  static const TcVariant table[] = {{2, 4}, {3, 4}, {4, 4}, {2, 8}, {3, 2}, {6, 4}};
+  int idx = P.geo.dtype == PKV_E4M3 ? 2 : 0;
+  if (const char* e = std::getenv("PKV_TC_VARIANT")) idx = std::max(0, std::min(5, std::atoi(e)));
   return table[idx];
 }
 
@@ -1016,8 +1139,9 @@ bool tc_eligible(const Pool& P) {
   const auto& g = P.geo;
   const int G = g.H_q / g.H_kv;
   const int64_t rows = g.num_blocks * g.L * g.H_kv * g.block_size;
-  return (g.dtype == PKV_BF16 || g.dtype == PKV_F16) && (g.d_head == 64 || g.d_head == 128) && G <= GPAD &&
-         g.block_size % TILE == 0 && rows < (int64_t(1) << 31) && encode_fn() != nullptr;
+  const bool dt = ((g.dtype == PKV_BF16 || g.dtype == PKV_F16) && (g.d_head == 64 || g.d_head == 128)) ||
+                  (g.dtype == PKV_E4M3 && g.d_head == 128);
+  return dt && G <= GPAD && g.block_size % TILE == 0 && rows < (int64_t(1) << 31) && encode_fn() != nullptr;
 }
 
 int device_sm_count(int* n) {
@@ -1037,9 +1161,10 @@ using KernelPtr = const void*;
 
 template <typename T, int D>
 KernelPtr pick_tc(const TcVariant& v, int* smem) {
+  constexpr int EB = std::is_same<T, E4M3>::value ? 1 : 2;
 #define PKV_TC_CASE(S_, NW_)                           \
   if (v.stages == S_ && v.warps == NW_) {              \
-    *smem = TcSmem<D, S_, NW_>::TOTAL;                 \
+    *smem = TcSmem<D, EB, S_, NW_>::TOTAL;             \
     return tc_kernel_ptr<T, D, S_, NW_>();             \
   }
   PKV_TC_CASE(2, 4)
@@ -1047,13 +1172,15 @@ KernelPtr pick_tc(const TcVariant& v, int* smem) {
   PKV_TC_CASE(4, 4)
   PKV_TC_CASE(2, 8)
   PKV_TC_CASE(3, 2)
+  if constexpr (EB == 1) PKV_TC_CASE(6, 4)
 #undef PKV_TC_CASE
-  *smem = TcSmem<D, 2, 4>::TOTAL;
+  *smem = TcSmem<D, EB, 2, 4>::TOTAL;
   return tc_kernel_ptr<T, D, 2, 4>();
 }
 
 KernelPtr tc_kernel_for(const Pool& P, int* smem) {
-  const TcVariant v = tc_variant();
+  const TcVariant v = tc_variant(P);
+  if (P.geo.dtype == PKV_E4M3) return pick_tc<E4M3, 128>(v, smem);
   const bool bf = P.geo.dtype == PKV_BF16;
   if (P.geo.d_head == 128) return bf ? pick_tc<__nv_bfloat16, 128>(v, smem) : pick_tc<__half, 128>(v, smem);
   return bf ? pick_tc<__nv_bfloat16, 64>(v, smem) : pick_tc<__half, 64>(v, smem);
@@ -1076,14 +1203,14 @@ int tc_grid(const Pool& P, int* grid, int* warps, int* smem) {
     for (const auto& kn : known)
       if (kn.dev == dev && kn.k == k) {
         *grid = kn.grid;
-        *warps = tc_variant().warps;
+        *warps = tc_variant(P).warps;
         return PKV_OK;
       }
   }
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, *smem);
   if (e != cudaSuccess) return fail(PKV_ERR_CUDA, std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e));
   int per_sm = 0;
-  const int nw = tc_variant().warps;
+  const int nw = tc_variant(P).warps;
   e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, nw * 32, *smem);
   if (e != cudaSuccess || per_sm < 1)
     return fail(PKV_ERR_CUDA, std::string("occupancy query: ") + cudaGetErrorString(e));
@@ -1112,6 +1239,97 @@ WsLayout ws_layout(int n_seq, int H_kv, int64_t total_warps, int D) {
   const int pstride = (D / 16) * 32 * 4 + 2 * GPAD;
   w.total = w.partials + align256(sizeof(float) * total_warps * 2 * pstride);
   return w;
+}
+
+// Fields of DecodeArgs shared by every attention launch.  For an FP8 pool the key
+// scale is folded into the softmax scale and the value scale into the final
+// normalisation (stored code * scale is the element's value).
+int fill_args(const Pool& P, int32_t layer, const void* q, void* out, const int32_t* tables, int32_t W,
+              const int32_t* seq_lens, int32_t n_seq, float scale, DecodeArgs* a) {
+  const auto& g = P.geo;
+  void* err = nullptr;
+  if (int rc = device_error_word(&err)) return rc;
+  *a = DecodeArgs{};
+  a->q = q;
+  a->out = out;
+  a->tables = tables;
+  a->seq_lens = seq_lens;
+  a->err = static_cast<int*>(err);
+  a->num_blocks = g.num_blocks;
+  a->n_seq = n_seq;
+  a->W = W;
+  a->H_q = g.H_q;
+  a->H_kv = g.H_kv;
+  a->G = g.H_q / g.H_kv;
+  a->L = g.L;
+  a->layer = layer;
+  a->B = g.block_size;
+  a->D = g.d_head;
+  a->elem = static_cast<int32_t>(act_size(g.dtype));
+  const bool fp8 = g.dtype == PKV_E4M3;
+  a->scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634 * (fp8 ? P.k_scale : 1.0));
+  a->v_mul = fp8 ? P.v_scale : 1.f;
+  return PKV_OK;
+}
+
+// The CUDA-core decode kernel for the pool's element types: one CTA per (sequence, KV head).
+template <typename TS, typename TA>
+void simt_decode_t(const DecodeArgs& a, const void* kp, const void* vp, int grid, size_t smem, cudaStream_t st) {
+  const int d = a.D;
+#define PKV_SIMT(NPL)                                                                                \
+  {                                                                                                  \
+    auto kern = decode_simt_kernel<TS, TA, NPL>;                                                     \
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)); \
+    kern<<<grid, SIMT_WARPS * 32, smem, st>>>(a, static_cast<const TS*>(kp), static_cast<const TS*>(vp), d); \
+  }
+  switch ((d + 31) / 32) {
+    case 1: PKV_SIMT(1) break;
+    case 2: PKV_SIMT(2) break;
+    case 3: case 4: PKV_SIMT(4) break;
+    default: PKV_SIMT(8) break;
+  }
+#undef PKV_SIMT
+}
+
+int launch_simt_decode(const Pool& P, const DecodeArgs& a, const void* kp, const void* vp, cudaStream_t st) {
+  const auto& g = P.geo;
+  const size_t smem = sizeof(float) * (SIMT_WARPS * a.G * 2 + SIMT_WARPS * a.G * static_cast<size_t>(g.d_head));
+  const int pairs = a.n_seq * g.H_kv;
+  switch (g.dtype) {
+    case PKV_F32: simt_decode_t<float, float>(a, kp, vp, pairs, smem, st); break;
+    case PKV_F16: simt_decode_t<__half, __half>(a, kp, vp, pairs, smem, st); break;
+    case PKV_BF16: simt_decode_t<__nv_bfloat16, __nv_bfloat16>(a, kp, vp, pairs, smem, st); break;
+    default: simt_decode_t<E4M3, __nv_bfloat16>(a, kp, vp, pairs, smem, st); break;
+  }
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(PKV_ERR_CUDA, std::string("decode launch: ") + cudaGetErrorString(e));
+  count_launch();
+  return PKV_OK;
+}
+
+// TMA descriptors of the K and V pools as 2-D arrays {d_head, all rows}: 16-token
+// boxes 128 bytes wide (64 16-bit or 128 FP8 elements), 128-byte swizzle.
+int encode_kv_maps(const pkv_geometry& g, const void* k, const void* v, CUtensorMap* tk, CUtensorMap* tv) {
+  if ((reinterpret_cast<uintptr_t>(k) & 15) || (reinterpret_cast<uintptr_t>(v) & 15))
+    return fail(PKV_ERR_INVALID_ARG, "k_pool and v_pool must be 16-byte aligned");
+  const int eb = static_cast<int>(elem_size(g.dtype));
+  const CUtensorMapDataType dt = g.dtype == PKV_E4M3  ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                 : g.dtype == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                       : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(g.d_head),
+                        static_cast<cuuint64_t>(g.num_blocks) * g.L * g.H_kv * g.block_size};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(g.d_head) * eb};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / eb), TILE};
+  cuuint32_t estr[2] = {1, 1};
+  auto fn = encode_fn();
+  if (!fn) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+  for (int which = 0; which < 2; ++which) {
+    CUresult r = fn(which ? tv : tk, dt, 2, const_cast<void*>(which ? v : k), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled failed: " + std::to_string(r));
+  }
+  return PKV_OK;
 }
 
 // plan_kernel, then the attention kernel as a programmatic dependent launch: its
@@ -1169,26 +1387,11 @@ static int get_tensor_maps(Pool& P, const void* k, const void* v, CUtensorMap* t
       *tv = e.tv;
       return PKV_OK;
     }
-  const auto& g = P.geo;
-  if ((reinterpret_cast<uintptr_t>(k) & 15) || (reinterpret_cast<uintptr_t>(v) & 15))
-    return fail(PKV_ERR_INVALID_ARG, "k_pool and v_pool must be 16-byte aligned");
   TensorMaps::Entry ent;
   ent.device = dev;
   ent.k = k;
   ent.v = v;
-  const CUtensorMapDataType dt = g.dtype == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(g.d_head),
-                        static_cast<cuuint64_t>(g.num_blocks) * g.L * g.H_kv * g.block_size};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(g.d_head) * 2};
-  cuuint32_t box[2] = {64, TILE};
-  cuuint32_t estr[2] = {1, 1};
-  auto fn = encode_fn();
-  for (int which = 0; which < 2; ++which) {
-    CUresult r = fn(which ? &ent.tv : &ent.tk, dt, 2, const_cast<void*>(which ? v : k), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled failed: " + std::to_string(r));
-  }
+  if (int rc = encode_kv_maps(P.geo, k, v, &ent.tk, &ent.tv)) return rc;
   if (es.size() >= 8) es.erase(es.begin());
   es.push_back(ent);
   *tk = ent.tk;
@@ -1217,35 +1420,17 @@ int launch_decode(Pool& P, int32_t layer, const void* q, const void* k_pool, con
   if (static_cast<int64_t>(n_seq) * g.H_kv * ((static_cast<int64_t>(W) * g.block_size + TILE - 1) / TILE) >=
       (int64_t(1) << 31))
     return fail(PKV_ERR_INVALID_ARG, "batch too large (tile count must stay below 2^31)");
-  void* err = nullptr;
-  if (int rc = device_error_word(&err)) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-
-  DecodeArgs a{};
-  a.q = q;
-  a.out = out;
-  a.tables = tables;
-  a.seq_lens = seq_lens;
-  a.err = static_cast<int*>(err);
-  a.num_blocks = g.num_blocks;
-  a.n_seq = n_seq;
-  a.W = W;
-  a.H_q = g.H_q;
-  a.H_kv = g.H_kv;
-  a.G = G;
-  a.L = g.L;
-  a.layer = layer;
-  a.B = g.block_size;
-  a.D = g.d_head;
-  a.elem = static_cast<int32_t>(elem_size(g.dtype));
-  a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  DecodeArgs a;
+  if (int rc = fill_args(P, layer, q, out, tables, W, seq_lens, n_seq, scale, &a)) return rc;
 
   if (tc_eligible(P)) {
     int grid = 0, nw = 0, smem = 0;
     if (int rc = tc_grid(P, &grid, &nw, &smem)) return rc;
     const WsLayout L = ws_layout(n_seq, g.H_kv, static_cast<int64_t>(grid) * nw, g.d_head);
     if (ws_bytes < L.total) return fail(PKV_ERR_INVALID_ARG, "workspace too small: need " + std::to_string(L.total));
-    if ((reinterpret_cast<uintptr_t>(q) & 15)) return fail(PKV_ERR_INVALID_ARG, "q must be 16-byte aligned");
+    if ((reinterpret_cast<uintptr_t>(q) & 15) || (reinterpret_cast<uintptr_t>(out) & 15))
+      return fail(PKV_ERR_INVALID_ARG, "q and out must be 16-byte aligned");
     CUtensorMap tk, tv;
     if (int rc = get_tensor_maps(P, k_pool, v_pool, &tk, &tv)) return rc;
     char* w = static_cast<char*>(ws);
@@ -1260,39 +1445,27 @@ int launch_decode(Pool& P, int32_t layer, const void* q, const void* k_pool, con
     return launch_tc_sequence(a, maps, tc_kernel_for(P, &smem), grid, nw, smem, st);
   }
 
-  // CUDA-core path
-  const int d = g.d_head;
-  const int npl = (d + 31) / 32;
-  const size_t smem = sizeof(float) * (SIMT_WARPS * G * 2 + SIMT_WARPS * G * static_cast<size_t>(d));
-  const int pairs = n_seq * g.H_kv;
-  cudaError_t e = cudaSuccess;
-#define PKV_SIMT(TYPE, NPL)                                                                          \
+  return launch_simt_decode(P, a, k_pool, v_pool, st);
+}
+
+// The CUDA-core prefill kernel for the pool's element types: one CTA per (query row, KV head).
+template <typename TS, typename TA>
+void simt_prefill_t(const DecodeArgs& a, const int32_t* q_off, const void* kp, const void* vp, dim3 grid, size_t smem,
+                    cudaStream_t st) {
+  const int d = a.D;
+#define PKV_PF_SIMT(NPL)                                                                             \
   {                                                                                                  \
-    auto kern = decode_simt_kernel<TYPE, NPL>;                                                       \
+    auto kern = prefill_simt_kernel<TS, TA, NPL>;                                                    \
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)); \
-    kern<<<pairs, SIMT_WARPS * 32, smem, st>>>(a, static_cast<const TYPE*>(k_pool),                  \
-                                               static_cast<const TYPE*>(v_pool), d);                 \
+    kern<<<grid, SIMT_WARPS * 32, smem, st>>>(a, q_off, static_cast<const TS*>(kp), static_cast<const TS*>(vp), d); \
   }
-#define PKV_SIMT_T(TYPE)                         \
-  switch (npl) {                                 \
-    case 1: PKV_SIMT(TYPE, 1) break;             \
-    case 2: PKV_SIMT(TYPE, 2) break;             \
-    case 3: case 4: PKV_SIMT(TYPE, 4) break;     \
-    default: PKV_SIMT(TYPE, 8) break;            \
+  switch ((d + 31) / 32) {
+    case 1: PKV_PF_SIMT(1) break;
+    case 2: PKV_PF_SIMT(2) break;
+    case 3: case 4: PKV_PF_SIMT(4) break;
+    default: PKV_PF_SIMT(8) break;
   }
-  if (g.dtype == PKV_F32) {
-    PKV_SIMT_T(float)
-  } else if (g.dtype == PKV_F16) {
-    PKV_SIMT_T(__half)
-  } else {
-    PKV_SIMT_T(__nv_bfloat16)
-  }
-#undef PKV_SIMT_T
-#undef PKV_SIMT
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return fail(PKV_ERR_CUDA, std::string("decode launch: ") + cudaGetErrorString(e));
-  count_launch();
-  return PKV_OK;
+#undef PKV_PF_SIMT
 }
 
 int launch_prefill(Pool& P, int32_t layer, const void* q, const int32_t* q_off, int32_t n_tok, int32_t max_q,
@@ -1300,27 +1473,9 @@ int launch_prefill(Pool& P, int32_t layer, const void* q, const int32_t* q_off, 
                    int32_t n_seq, float scale, void* out, void* stream) {
   const auto& g = P.geo;
   const int G = g.H_q / g.H_kv;
-  void* err = nullptr;
-  if (int rc = device_error_word(&err)) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  DecodeArgs a{};
-  a.q = q;
-  a.out = out;
-  a.tables = tables;
-  a.seq_lens = seq_lens;
-  a.err = static_cast<int*>(err);
-  a.num_blocks = g.num_blocks;
-  a.n_seq = n_seq;
-  a.W = W;
-  a.H_q = g.H_q;
-  a.H_kv = g.H_kv;
-  a.G = G;
-  a.L = g.L;
-  a.layer = layer;
-  a.B = g.block_size;
-  a.D = g.d_head;
-  a.elem = static_cast<int32_t>(elem_size(g.dtype));
-  a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  DecodeArgs a;
+  if (int rc = fill_args(P, layer, q, out, tables, W, seq_lens, n_seq, scale, &a)) return rc;
   cudaError_t e = cudaSuccess;
   const int64_t rows = g.num_blocks * g.L * g.H_kv * g.block_size;
   const bool tc = (g.dtype == PKV_BF16 || g.dtype == PKV_F16) && (g.d_head == 64 || g.d_head == 128) &&
@@ -1351,33 +1506,14 @@ int launch_prefill(Pool& P, int32_t layer, const void* q, const int32_t* q_off, 
     count_launch();
     return PKV_OK;
   }
-  const int d = g.d_head;
-  const int npl = (d + 31) / 32;
-  const size_t smem = sizeof(float) * (SIMT_WARPS * G * 2 + SIMT_WARPS * G * static_cast<size_t>(d));
-  dim3 grid(n_tok, g.H_kv);
-#define PKV_PF_SIMT(TYPE, NPL)                                                                       \
-  {                                                                                                  \
-    auto kern = prefill_simt_kernel<TYPE, NPL>;                                                      \
-    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)); \
-    kern<<<grid, SIMT_WARPS * 32, smem, st>>>(a, q_off, static_cast<const TYPE*>(k_pool),            \
-                                              static_cast<const TYPE*>(v_pool), d);                  \
+  const size_t smem = sizeof(float) * (SIMT_WARPS * G * 2 + SIMT_WARPS * G * static_cast<size_t>(g.d_head));
+  const dim3 grid(n_tok, g.H_kv);
+  switch (g.dtype) {
+    case PKV_F32: simt_prefill_t<float, float>(a, q_off, k_pool, v_pool, grid, smem, st); break;
+    case PKV_F16: simt_prefill_t<__half, __half>(a, q_off, k_pool, v_pool, grid, smem, st); break;
+    case PKV_BF16: simt_prefill_t<__nv_bfloat16, __nv_bfloat16>(a, q_off, k_pool, v_pool, grid, smem, st); break;
+    default: simt_prefill_t<E4M3, __nv_bfloat16>(a, q_off, k_pool, v_pool, grid, smem, st); break;
   }
-#define PKV_PF_SIMT_T(TYPE)                      \
-  switch (npl) {                                 \
-    case 1: PKV_PF_SIMT(TYPE, 1) break;          \
-    case 2: PKV_PF_SIMT(TYPE, 2) break;          \
-    case 3: case 4: PKV_PF_SIMT(TYPE, 4) break;  \
-    default: PKV_PF_SIMT(TYPE, 8) break;         \
-  }
-  if (g.dtype == PKV_F32) {
-    PKV_PF_SIMT_T(float)
-  } else if (g.dtype == PKV_F16) {
-    PKV_PF_SIMT_T(__half)
-  } else {
-    PKV_PF_SIMT_T(__nv_bfloat16)
-  }
-#undef PKV_PF_SIMT_T
-#undef PKV_PF_SIMT
   e = cudaGetLastError();
   if (e != cudaSuccess) return fail(PKV_ERR_CUDA, std::string("prefill launch: ") + cudaGetErrorString(e));
   count_launch();
@@ -1444,62 +1580,13 @@ extern "C" int pkv_decode_attention_noalloc(const pkv_pool* pool, int32_t layer,
   if (static_cast<int64_t>(n_seq) * g.H_kv * ((static_cast<int64_t>(W) * g.block_size + TILE - 1) / TILE) >=
       (int64_t(1) << 31))
     return fail(PKV_ERR_INVALID_ARG, "batch too large (tile count must stay below 2^31)");
-  void* err = nullptr;
-  if (int rc = device_error_word(&err)) return rc;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-
-  DecodeArgs a{};
-  a.q = q;
-  a.out = out;
-  a.tables = block_tables;
-  a.seq_lens = seq_lens;
-  a.err = static_cast<int*>(err);
-  a.num_blocks = g.num_blocks;
-  a.n_seq = n_seq;
-  a.W = W;
-  a.H_q = g.H_q;
-  a.H_kv = g.H_kv;
-  a.G = G;
-  a.L = g.L;
-  a.layer = layer;
-  a.B = g.block_size;
-  a.D = g.d_head;
-  a.elem = static_cast<int32_t>(elem_size(g.dtype));
-  a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  DecodeArgs a;
+  if (int rc = fill_args(P, layer, q, out, block_tables, W, seq_lens, n_seq, scale, &a)) return rc;
 
   if (!tc_eligible(P)) {
     // the CUDA-core kernel needs no scratch at all
-    const int d = g.d_head;
-    const size_t smem = sizeof(float) * (SIMT_WARPS * G * 2 + SIMT_WARPS * G * static_cast<size_t>(d));
-    const int pairs = n_seq * g.H_kv;
-    const int npl = (d + 31) / 32;
-#define PKV_NA_SIMT(TYPE, NPL)                                                                       \
-  {                                                                                                  \
-    auto kern = decode_simt_kernel<TYPE, NPL>;                                                       \
-    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)); \
-    kern<<<pairs, SIMT_WARPS * 32, smem, st>>>(a, static_cast<const TYPE*>(k_pool),                  \
-                                               static_cast<const TYPE*>(v_pool), d);                 \
-  }
-#define PKV_NA_SIMT_T(TYPE)                      \
-  switch (npl) {                                 \
-    case 1: PKV_NA_SIMT(TYPE, 1) break;          \
-    case 2: PKV_NA_SIMT(TYPE, 2) break;          \
-    case 3: case 4: PKV_NA_SIMT(TYPE, 4) break;  \
-    default: PKV_NA_SIMT(TYPE, 8) break;         \
-  }
-    if (g.dtype == PKV_F32) {
-      PKV_NA_SIMT_T(float)
-    } else if (g.dtype == PKV_F16) {
-      PKV_NA_SIMT_T(__half)
-    } else {
-      PKV_NA_SIMT_T(__nv_bfloat16)
-    }
-#undef PKV_NA_SIMT_T
-#undef PKV_NA_SIMT
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return fail(PKV_ERR_CUDA, std::string("decode launch: ") + cudaGetErrorString(e));
-    count_launch();
-    return PKV_OK;
+    return launch_simt_decode(P, a, k_pool, v_pool, st);
   }
 
   // persistent grid, computed here without any cache
@@ -1508,7 +1595,7 @@ extern "C" int pkv_decode_attention_noalloc(const pkv_pool* pool, int32_t layer,
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return fail(PKV_ERR_CUDA, std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e));
   int per_sm = 0, sms = 0, dev = 0;
-  const int nw = tc_variant().warps;
+  const int nw = tc_variant(P).warps;
   e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, nw * 32, smem);
   if (e == cudaSuccess) e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -1520,26 +1607,14 @@ extern "C" int pkv_decode_attention_noalloc(const pkv_pool* pool, int32_t layer,
                                          " bytes of scratch, more than the static " +
                                          std::to_string(kNoallocScratchBytes) +
                                          "; use pkv_decode_attention with a caller workspace");
-  if (reinterpret_cast<uintptr_t>(q) & 15) return fail(PKV_ERR_INVALID_ARG, "q must be 16-byte aligned");
-  if ((reinterpret_cast<uintptr_t>(k_pool) & 15) || (reinterpret_cast<uintptr_t>(v_pool) & 15))
-    return fail(PKV_ERR_INVALID_ARG, "k_pool and v_pool must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(q) & 15) || (reinterpret_cast<uintptr_t>(out) & 15))
+    return fail(PKV_ERR_INVALID_ARG, "q and out must be 16-byte aligned");
   void* ws = nullptr;
   if (int rc = noalloc_scratch(&ws)) return rc;
 
   // tensor maps encoded on the stack (no cache)
   CUtensorMap maps[2];
-  const CUtensorMapDataType dt = g.dtype == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(g.d_head),
-                        static_cast<cuuint64_t>(g.num_blocks) * g.L * g.H_kv * g.block_size};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(g.d_head) * 2};
-  cuuint32_t box[2] = {64, TILE};
-  cuuint32_t estr[2] = {1, 1};
-  for (int which = 0; which < 2; ++which) {
-    CUresult r = encode_fn()(&maps[which], dt, 2, const_cast<void*>(which ? v_pool : k_pool), dims, strides, box, estr,
-                             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled failed: " + std::to_string(r));
-  }
+  if (int rc = encode_kv_maps(g, k_pool, v_pool, &maps[0], &maps[1])) return rc;
   // every field the kernels read is written earlier in the same call: the plan
   // kernel writes the header, prefix, clamped lengths, warp starts and zeroes the
   // split-pair counters; the attention kernel writes a partial before counting it

@@ -59,12 +59,16 @@ struct Pool {
   std::vector<int64_t> first_tok;  // scratch: caller offsets of one append
   int32_t next_id = 0;
   int32_t swap_engine = 0;  // 0 SM kernel, 1 copy engine
+  float k_scale = 1.f, v_scale = 1.f;  // FP8 pools: stored code * scale
 
   std::mutex tmap_mu;
   TensorMaps* tmaps = nullptr;
 };
 
-inline int64_t elem_size(int32_t dtype) { return dtype == PKV_F32 ? 4 : 2; }
+// Bytes of one stored pool element.
+inline int64_t elem_size(int32_t dtype) { return dtype == PKV_F32 ? 4 : (dtype == PKV_E4M3 ? 1 : 2); }
+// Bytes of one activation element (q, out, new keys/values): bf16 around an FP8 pool.
+inline int64_t act_size(int32_t dtype) { return dtype == PKV_E4M3 ? 2 : elem_size(dtype); }
 
 // ------------------------------------------------------------------ device side
 

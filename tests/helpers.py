@@ -8,13 +8,18 @@ import oracle
 import paged_kv_cache_80_gb300 as pkv
 import workloads as W
 
-NP_STORE = {"f32": np.float32, "f16": np.float16, "bf16": np.uint16}
+NP_STORE = {"f32": np.float32, "f16": np.float16, "bf16": np.uint16, "e4m3": np.uint8}
 
 
 def torch_dtype(dtype):
     import torch
 
-    return {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[dtype]
+    return {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16, "e4m3": torch.uint8}[dtype]
+
+
+def act(g) -> str:
+    """Element type of q, out and new keys/values around the pool (bf16 for FP8)."""
+    return oracle.q_dtype(g)
 
 
 def to_dev(raw: np.ndarray, dtype: str, device="cuda"):
@@ -58,11 +63,14 @@ class PagedBatch:
     """A library pool on the device and an oracle pool on the host, advanced together."""
 
     def __init__(self, g: W.Geometry, free_order=None, seed: int = 0, host_pool: bool = True, device="cuda",
-                 fill_device=None):
+                 fill_device=None, kv_scales=(1.0, 1.0)):
         import torch
 
         self.g, self.seed, self.device = g, seed, device
         self.lib = pkv.pkv_pool_create(g.L, g.H_q, g.H_kv, g.d_head, g.block_size, g.dtype, g.num_blocks, free_order)
+        self.k_scale, self.v_scale = (float(np.float32(kv_scales[0])), float(np.float32(kv_scales[1])))
+        if g.dtype == "e4m3":
+            pkv.pkv_pool_set_kv_scales(self.lib, self.k_scale, self.v_scale)
         self.orc = oracle.Pool(g.num_blocks, g.block_size, free_order)
         td = torch_dtype(g.dtype)
         if fill_device is None:
@@ -115,12 +123,13 @@ class PagedBatch:
             return slots, cows
         lay = g.L if layer < 0 else 1
         shape = (lay, len(slots), g.H_kv, g.d_head) if layer < 0 else (len(slots), g.H_kv, g.d_head)
-        k = W.normal(self.seed, f"k_{tag}", shape, g.dtype)
-        v = W.normal(self.seed, f"v_{tag}", shape, g.dtype)
-        pkv.pkv_append_kv(self.lib, layer, to_dev(k, g.dtype, self.device), to_dev(v, g.dtype, self.device),
+        a = act(g)
+        k = W.normal(self.seed, f"k_{tag}", shape, a)
+        v = W.normal(self.seed, f"v_{tag}", shape, a)
+        pkv.pkv_append_kv(self.lib, layer, to_dev(k, a, self.device), to_dev(v, a, self.device),
                           torch.from_numpy(slots).to(self.device), self.kp, self.vp)
         if write_host and self.hk is not None:
-            oracle.write_slots(g, layer, k, v, slots, self.hk, self.hv)
+            oracle.write_slots(g, layer, k, v, slots, self.hk, self.hv, self.k_scale, self.v_scale)
         return slots, cows
 
     def tables(self, seq_ids, W_=None):
@@ -145,15 +154,16 @@ class PagedBatch:
         g = self.g
         if tables is None:
             tables, lens = self.tables(seq_ids, W_)
-        out = torch.full((len(seq_ids), g.H_q, g.d_head), float("nan"), dtype=torch_dtype(g.dtype),
+        out = torch.full((len(seq_ids), g.H_q, g.d_head), float("nan"), dtype=torch_dtype(act(g)),
                          device=self.device)
         ws = torch.empty(pkv.pkv_decode_workspace_size(self.lib, len(seq_ids)), dtype=torch.uint8,
                          device=self.device)
-        pkv.pkv_decode_attention(self.lib, layer, to_dev(q_raw, g.dtype, self.device), self.kp, self.vp,
+        pkv.pkv_decode_attention(self.lib, layer, to_dev(q_raw, act(g), self.device), self.kp, self.vp,
                                  torch.from_numpy(np.ascontiguousarray(tables)).to(self.device),
                                  torch.from_numpy(np.ascontiguousarray(lens)).to(self.device), scale, out, ws)
         pkv.pkv_check_device_error()
-        return out_f64(out, g.dtype), tables, lens
+        return out_f64(out, act(g)), tables, lens
 
     def decode_ref(self, q_raw, tables, lens, scale, layer=0):
-        return oracle.decode_attention(self.g, layer, q_raw, self.hk, self.hv, tables, lens, scale)
+        return oracle.decode_attention(self.g, layer, q_raw, self.hk, self.hv, tables, lens, scale,
+                                       k_scale=self.k_scale, v_scale=self.v_scale)

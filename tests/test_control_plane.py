@@ -152,3 +152,22 @@ def test_invalid_arguments_are_rejected_without_change():
     rc = pkv._L().pkv_swap_in(lib.handle, a, host.ctypes.data, 1, 0, None, None, None, None)
     assert pkv._L().pkv_status_name(rc).decode() == "PKV_ERR_INVALID_ARG"
     assert pkv.pkv_seq_len(lib, a) == 9
+
+
+def test_fp8_pool_scales_and_geometry_checks():
+    p = pkv.pkv_pool_create(2, 8, 2, 128, 16, "e4m3", 64)
+    assert pkv.pkv_pool_geometry(p).dtype == pkv.E4M3
+    assert pkv.pkv_pool_kv_scales(p) == (1.0, 1.0)
+    pkv.pkv_pool_set_kv_scales(p, 0.25, 0.5)
+    assert pkv.pkv_pool_kv_scales(p) == (0.25, 0.5)
+    for bad in [(0.0, 1.0), (1.0, -2.0), (float("inf"), 1.0), (1.0, float("nan"))]:
+        with pytest.raises(pkv.PkvError) as e:
+            pkv.pkv_pool_set_kv_scales(p, *bad)
+        assert e.value.name == "PKV_ERR_INVALID_ARG"
+    assert pkv.pkv_pool_kv_scales(p) == (0.25, 0.5)
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.pkv_pool_set_kv_scales(pkv.pkv_pool_create(1, 2, 2, 8, 4, "bf16", 4), 0.5, 0.5)
+    assert e.value.name == "PKV_ERR_UNSUPPORTED"
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.pkv_pool_create(1, 2, 2, 12, 4, "e4m3", 4)  # d_head not a multiple of 8
+    assert e.value.name == "PKV_ERR_UNSUPPORTED"

@@ -93,14 +93,16 @@ def device_normal(seed: int, tag: str, shape, dtype: str, device):
     h = int.from_bytes(hashlib.sha256(tag.encode()).digest()[:6], "little")
     gen = torch.Generator(device=device)
     gen.manual_seed((seed * 1_000_003 + h) % (2**63 - 1))
-    tdt = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[dtype]
-    out = torch.empty(shape, dtype=tdt, device=device)
+    tdt = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16, "e4m3": torch.float8_e4m3fn}[dtype]
+    # FP8 draws are returned as their uint8 codes (the pool's storage)
+    out = torch.empty(shape, dtype=torch.uint8 if dtype == "e4m3" else tdt, device=device)
     # fill in slabs to bound the float32 temporary
     flat = out.view(-1)
     step = 1 << 28
     for i in range(0, flat.numel(), step):
         n = min(step, flat.numel() - i)
-        flat[i : i + n] = torch.randn(n, generator=gen, device=device, dtype=torch.float32).to(tdt)
+        x = torch.randn(n, generator=gen, device=device, dtype=torch.float32).to(tdt)
+        flat[i : i + n] = x.view(torch.uint8) if dtype == "e4m3" else x
     return out
 
 
