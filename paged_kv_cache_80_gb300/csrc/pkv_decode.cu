@@ -217,10 +217,13 @@ __device__ __forceinline__ __nv_bfloat16 from_float<__nv_bfloat16>(float x) { re
 template <>
 __device__ __forceinline__ __half from_float<__half>(float x) { return __float2half_rn(x); }
 
-// Two E4M3 codes (low byte first) to two binary16 values (exact).
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t b16) {
-  const __half2_raw r = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(b16 & 0xffffu), __NV_E4M3);
-  return static_cast<uint32_t>(r.x) | (static_cast<uint32_t>(r.y) << 16);
+// Four E4M3 codes (bytes 0..3 of w) to binary16 pairs (exact): lo = (b0, b1), hi = (b2, b3),
+// the first of each pair in the low half.
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, l;\n\tcvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
 }
 
 // Two bfloat16 values (low half first) to two binary16 values (round to nearest).
@@ -518,8 +521,9 @@ __global__ void __launch_bounds__(NW * 32) decode_tc_kernel(const __grid_constan
 #pragma unroll
       for (int c = 0; c < C::NKC; ++c) {
         const uint32_t wa = word_of(c < 4 ? ka0 : ka1, c & 3), wb = word_of(c < 4 ? kb0 : kb1, c & 3);
-        const uint32_t a0 = e4m3x2_to_f16x2(wa), a1 = e4m3x2_to_f16x2(wb);
-        const uint32_t a2 = e4m3x2_to_f16x2(wa >> 16), a3 = e4m3x2_to_f16x2(wb >> 16);
+        uint32_t a0, a1, a2, a3;
+        e4m3x4_to_f16x2x2(wa, a0, a2);
+        e4m3x4_to_f16x2x2(wb, a1, a3);
         if (c & 1) mma_16816<BF16>(sb, a0, a1, a2, a3, qf[c][0], qf[c][1]);
         else mma_16816<BF16>(sa, a0, a1, a2, a3, qf[c][0], qf[c][1]);
       }
@@ -592,8 +596,10 @@ __global__ void __launch_bounds__(NW * 32) decode_tc_kernel(const __grid_constan
         const unsigned sel = (c & 1) ? 0x7362u : 0x5140u;
         const uint32_t x = __byte_perm(word_of(v0, c >> 1), word_of(v1, c >> 1), sel);
         const uint32_t y = __byte_perm(word_of(v2, c >> 1), word_of(v3, c >> 1), sel);
-        mma_16816<BF16>(o[c], e4m3x2_to_f16x2(x), e4m3x2_to_f16x2(x >> 16), e4m3x2_to_f16x2(y),
-                        e4m3x2_to_f16x2(y >> 16), pb0, pb1);
+        uint32_t a0, a1, a2, a3;
+        e4m3x4_to_f16x2x2(x, a0, a1);
+        e4m3x4_to_f16x2x2(y, a2, a3);
+        mma_16816<BF16>(o[c], a0, a1, a2, a3, pb0, pb1);
       }
     } else {
 #pragma unroll
@@ -1126,12 +1132,13 @@ struct TcVariant {
 };
 
 // Pipeline depth and warps per CTA; PKV_TC_VARIANT selects another for tuning.  An
-// FP8 tile carries half the bytes of a 16-bit one, so its default pipeline is twice
-// as deep (the same bytes in flight per SM).
+// FP8 tile carries half the bytes of a 16-bit one and more instructions, so its
+// default pipeline is twice as deep and its CTAs smaller: 4 stages x 2 warps, 8 CTAs
+// (16 warps) per SM, the same bytes in flight with twice the warps to hide latency.
 TcVariant tc_variant(const Pool& P) {
-  static const TcVariant table[] = {{2, 4}, {3, 4}, {4, 4}, {2, 8}, {3, 2}, {6, 4}};
-  int idx = P.geo.dtype == PKV_E4M3 ? 2 : 0;
-  if (const char* e = std::getenv("PKV_TC_VARIANT")) idx = std::max(0, std::min(5, std::atoi(e)));
+  static const TcVariant table[] = {{2, 4}, {3, 4}, {4, 4}, {2, 8}, {3, 2}, {6, 4}, {2, 2}, {4, 2}, {3, 1}};
+  int idx = P.geo.dtype == PKV_E4M3 ? 7 : 0;
+  if (const char* e = std::getenv("PKV_TC_VARIANT")) idx = std::max(0, std::min(8, std::atoi(e)));
   return table[idx];
 }
 
@@ -1172,7 +1179,12 @@ KernelPtr pick_tc(const TcVariant& v, int* smem) {
   PKV_TC_CASE(4, 4)
   PKV_TC_CASE(2, 8)
   PKV_TC_CASE(3, 2)
-  if constexpr (EB == 1) PKV_TC_CASE(6, 4)
+  if constexpr (EB == 1) {
+    PKV_TC_CASE(6, 4)
+    PKV_TC_CASE(2, 2)
+    PKV_TC_CASE(4, 2)
+    PKV_TC_CASE(3, 1)
+  }
 #undef PKV_TC_CASE
   *smem = TcSmem<D, EB, 2, 4>::TOTAL;
   return tc_kernel_ptr<T, D, 2, 4>();
