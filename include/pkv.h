@@ -317,6 +317,79 @@ int pkv_seq_host_slots(const pkv_pool* pool, int32_t seq, int64_t* out, int32_t 
 /* 0 = swap with SM kernels (default), 1 = with cudaMemcpyAsync on the copy engines. */
 int pkv_pool_set_swap_engine(pkv_pool* pool, int32_t engine);
 
+/* ---------------------------------------------------------------- radix prefix cache (host only)
+ *
+ * [KVM] "Prefix Caching Across Turns": a radix tree over the pool that indexes physical
+ * blocks by the tokens they hold (Table 4, Definition 0.2), so that a new request whose
+ * prompt starts with cached tokens reuses those blocks instead of recomputing them.
+ *   - Only whole blocks are shared ("Longest prefix matching": block-aligned truncation,
+ *     S_usable = floor(S_match / B) * B); the tree's edges hold whole blocks and a node's
+ *     children are keyed by the B tokens of their first block.
+ *   - The cache holds one owner reference on every block it indexes, so the blocks of a
+ *     finished request stay resident ("dormant") after pkv_seq_free.
+ *   - A node's reference count is the number of attached requests whose matched path runs
+ *     through it (ref >= 1: pinned, never evicted).  Every operation advances a clock and
+ *     stamps the nodes it traverses (last_access).
+ *   - pkv_prefix_evict removes dormant leaves (ref 0, no children), least recently used
+ *     first (ties: the older node), releasing all of a leaf's blocks; a parent left with no
+ *     children and ref 0 becomes a candidate ("Dynamic radix eviction", leaf-first LRU).
+ * Destroy every cache of a pool before the pool (pkv_pool_destroy refuses otherwise).
+ * Not thread-safe: serialise calls with the pool's other control-plane calls. */
+typedef struct pkv_prefix_cache pkv_prefix_cache;
+typedef struct pkv_prefix_stats {
+  int64_t nodes;           /* nodes other than the root */
+  int64_t blocks;          /* blocks indexed (one owner reference each) */
+  int64_t pinned_nodes;    /* reference count >= 1 */
+  int64_t dormant_leaves;  /* reference count 0 and no children: eviction candidates */
+  int64_t prompt_tokens;   /* sum of the prompt lengths given to pkv_prefix_attach */
+  int64_t matched_tokens;  /* sum of the whole-block matches it served ([KVM] Eq. 2 hit rate =
+                              matched_tokens / prompt_tokens) */
+} pkv_prefix_stats;
+
+int pkv_prefix_cache_create(pkv_pool* pool, pkv_prefix_cache** out);
+/* Drops the cache's reference on every indexed block (blocks left with no owner go to the
+ * FIFO back, tree preorder). */
+int pkv_prefix_cache_destroy(pkv_prefix_cache* cache);
+
+/* Longest cached whole-block prefix of tokens[0, n): *n_matched tokens (a multiple of B),
+ * and, if block_ids is not NULL, its blocks (capacity n / B) in order.  Changes nothing. */
+int pkv_prefix_match(const pkv_prefix_cache* cache, const int32_t* tokens, int64_t n, int64_t* n_matched,
+                     int32_t* block_ids);
+
+/* Serve a new request with prompt tokens[0, n): match as above, split a node matched only in
+ * part at the match end, create a sequence (*seq) whose table is the matched blocks (each
+ * gains one owner) and whose length is *n_matched, and pin the matched path (every node from
+ * the deepest matched one to the root gains a reference and is stamped).  The caller appends
+ * the remaining n - *n_matched prompt tokens with pkv_plan_append (a fresh block: the last
+ * matched block is full). */
+int pkv_prefix_attach(pkv_prefix_cache* cache, const int32_t* tokens, int64_t n, int32_t* seq, int64_t* n_matched);
+
+/* Index the whole blocks of resident sequence seq under its tokens[0, n) (n <= its length;
+ * floor(n / B) blocks): blocks whose token path is already cached are not adopted (the
+ * sequence keeps its own); the rest become a new leaf, each block gaining the cache as an
+ * owner.  A node that diverges (or ends) inside an edge is split at that block boundary.
+ * Errors: INVALID_ARG (unknown, released or swapped-out sequence, n > length). */
+int pkv_prefix_insert(pkv_prefix_cache* cache, int32_t seq, const int32_t* tokens, int64_t n);
+
+/* Drop the pins pkv_prefix_attach took for seq (each node from its deepest matched node to
+ * the root loses a reference and is stamped).  Call before or after pkv_seq_free; the cache
+ * keeps the blocks.  Errors: INVALID_ARG (seq holds no pins). */
+int pkv_prefix_release(pkv_prefix_cache* cache, int32_t seq);
+
+/* Evict dormant leaves, least recently used first, while the pool's free list holds fewer
+ * than target_free blocks and a candidate is left.  *n_released = blocks whose cache
+ * reference was dropped (a block also owned by a live sequence stays allocated). */
+int pkv_prefix_evict(pkv_prefix_cache* cache, int64_t target_free, int64_t* n_released);
+
+int pkv_prefix_get_stats(const pkv_prefix_cache* cache, pkv_prefix_stats* out);
+
+/* The tree in preorder, children in ascending order of their first block's tokens:
+ * nodes int64 [stats.nodes][5] = (parent row or -1 for the root, blocks, ref, last_access,
+ * creation serial); blocks int32 [stats.blocks] and tokens int32 [stats.blocks * B], node
+ * after node. */
+int pkv_prefix_export(const pkv_prefix_cache* cache, int64_t* nodes, int32_t* tokens, int32_t* blocks,
+                      int64_t cap_nodes, int64_t cap_blocks);
+
 /* Failure-path self-test: launch one warp that waits on an mbarrier nothing will
  * complete, bounded by timeout_ns (<= 10 s) of the GPU's global timer -- the same
  * bounded wait the decode kernel uses for its tile loads.  When the bound runs out

@@ -49,6 +49,9 @@ def lib():
         L.orc_refcounts.argtypes = [vp, P32]
         L.orc_free_list.restype = i64
         L.orc_free_list.argtypes = [vp, P32]
+        L.orc_seq_adopt.argtypes = [vp, P32, i64, i64, P32]
+        L.orc_block_retain.argtypes = [vp, i32]
+        L.orc_block_release.argtypes = [vp, i32]
         L.orc_swap_out.argtypes = [vp, i32, P64, P32]
         L.orc_swap_in.argtypes = [vp, i32, P32, P64]
         geo = [ctypes.c_int] * 5 + [i64]
@@ -125,6 +128,20 @@ class Pool:
 
     def seq_free(self, seq: int) -> None:
         _check(lib().orc_seq_free(self._h, seq), "seq_free")
+
+    def seq_adopt(self, blocks: Sequence[int], length: int) -> int:
+        """New sequence over the given (allocated) blocks, each gaining an owner."""
+        b = np.ascontiguousarray(blocks, dtype=np.int32)
+        out = np.zeros(1, np.int32)
+        _check(lib().orc_seq_adopt(self._h, _p32(b) if len(b) else None, len(b), int(length), _p32(out)),
+               "seq_adopt")
+        return int(out[0])
+
+    def block_retain(self, p: int) -> None:
+        _check(lib().orc_block_retain(self._h, int(p)), "block_retain")
+
+    def block_release(self, p: int) -> None:
+        _check(lib().orc_block_release(self._h, int(p)), "block_release")
 
     def append(self, seq_ids: Sequence[int], n_new: Sequence[int]):
         """Returns (slot_mapping int32[sum n_new], cow_pairs int32[n_cow, 2])."""

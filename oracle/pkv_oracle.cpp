@@ -232,6 +232,38 @@ int orc_seq_fork(void* h, int32_t parent, int32_t* child) {
   return ORC_OK;
 }
 
+// A new sequence whose table is the given blocks, each gaining one owner, with length
+// len: a request served from the prefix cache starts as the cached blocks it matched
+// [KVM, "Prefix Caching Across Turns": matched blocks are re-attached to the request].
+int orc_seq_adopt(void* h, const int32_t* blocks, int64_t n, int64_t len, int32_t* seq_id) {
+  Pool& P = *static_cast<Pool*>(h);
+  for (int64_t i = 0; i < n; ++i)
+    if (blocks[i] < 0 || blocks[i] >= P.num_blocks || P.ref[blocks[i]] <= 0) return ORC_BAD_BLOCK_ID;
+  Sequence s;
+  s.table.assign(blocks, blocks + n);
+  s.len = len;
+  for (int32_t p : s.table) P.ref[p] += 1;
+  int32_t id = P.next_id++;
+  P.seqs[id] = s;
+  *seq_id = id;
+  return ORC_OK;
+}
+
+// One more owner of an allocated block (the prefix cache holding it).
+int orc_block_retain(void* h, int32_t p) {
+  Pool& P = *static_cast<Pool*>(h);
+  if (p < 0 || p >= P.num_blocks || P.ref[p] <= 0) return ORC_BAD_BLOCK_ID;
+  P.ref[p] += 1;
+  return ORC_OK;
+}
+
+// One owner fewer (the prefix cache evicting it); at zero the block goes to the FIFO back.
+int orc_block_release(void* h, int32_t p) {
+  Pool& P = *static_cast<Pool*>(h);
+  if (p < 0 || p >= P.num_blocks || P.ref[p] <= 0) return ORC_BAD_BLOCK_ID;
+  return release_block(P, p);
+}
+
 // Release [KVM, release_sequence_blocks]: walk the table in order, drop one owner
 // of each block, push blocks that reach zero to the FIFO, clear the table.
 int orc_seq_free(void* h, int32_t seq) {

@@ -24,6 +24,8 @@ __all__ = [
     "pkv_copy_blocks", "pkv_swap_out",
     "pkv_swap_in", "pkv_seq_host_slots", "pkv_seq_residency", "TIER_HBM", "TIER_HOST", "pkv_pool_set_swap_engine", "pkv_check_device_error", "pkv_launch_count",
     "pkv_selftest_bounded_wait", "pkv_pool_set_kv_scales", "pkv_pool_kv_scales",
+    "PrefixStats", "pkv_prefix_cache_create", "pkv_prefix_cache_destroy", "pkv_prefix_match", "pkv_prefix_attach",
+    "pkv_prefix_insert", "pkv_prefix_release", "pkv_prefix_evict", "pkv_prefix_get_stats", "pkv_prefix_export",
 ]
 
 F32, F16, BF16, E4M3 = 0, 1, 2, 3
@@ -46,6 +48,12 @@ class Geometry(ctypes.Structure):
     _fields_ = [("L", ctypes.c_int32), ("H_q", ctypes.c_int32), ("H_kv", ctypes.c_int32),
                 ("d_head", ctypes.c_int32), ("block_size", ctypes.c_int32), ("dtype", ctypes.c_int32),
                 ("num_blocks", ctypes.c_int64)]
+
+
+class PrefixStats(ctypes.Structure):
+    _fields_ = [("nodes", ctypes.c_int64), ("blocks", ctypes.c_int64), ("pinned_nodes", ctypes.c_int64),
+                ("dormant_leaves", ctypes.c_int64), ("prompt_tokens", ctypes.c_int64),
+                ("matched_tokens", ctypes.c_int64)]
 
 
 _lib = None
@@ -96,6 +104,15 @@ def _L():
             "pkv_check_device_error": ([vp, P32, P64], ctypes.c_int),
             "pkv_launch_count": ([], ctypes.c_uint64),
             "pkv_selftest_bounded_wait": ([i64, vp], ctypes.c_int),
+            "pkv_prefix_cache_create": ([vp, ctypes.POINTER(vp)], ctypes.c_int),
+            "pkv_prefix_cache_destroy": ([vp], ctypes.c_int),
+            "pkv_prefix_match": ([vp, P32, i64, P64, P32], ctypes.c_int),
+            "pkv_prefix_attach": ([vp, P32, i64, P32, P64], ctypes.c_int),
+            "pkv_prefix_insert": ([vp, i32, P32, i64], ctypes.c_int),
+            "pkv_prefix_release": ([vp, i32], ctypes.c_int),
+            "pkv_prefix_evict": ([vp, i64, P64], ctypes.c_int),
+            "pkv_prefix_get_stats": ([vp, ctypes.POINTER(PrefixStats)], ctypes.c_int),
+            "pkv_prefix_export": ([vp, P64, P32, P32, i64, i64], ctypes.c_int),
         }
         for name, (args, res) in sig.items():
             f = getattr(L, name)
@@ -426,3 +443,97 @@ def pkv_check_device_error(stream=None):
     rc = _L().pkv_check_device_error(_stream(stream), ctypes.byref(code), ctypes.byref(detail))
     _check(rc, "pkv_check_device_error")
     return code.value, detail.value
+
+
+# ------------------------------------------------------------------ radix prefix cache (host)
+
+
+class PrefixCache:
+    """Owner of a pkv_prefix_cache handle; keeps its pool alive and is destroyed first."""
+
+    def __init__(self, handle: ctypes.c_void_p, pool: PoolLike):
+        self.handle = handle
+        self.pool = pool
+
+    def __del__(self):
+        h = getattr(self, "handle", None)
+        if h and _lib is not None:
+            _lib.pkv_prefix_cache_destroy(h)
+            self.handle = None
+
+
+def _c(cache) -> ctypes.c_void_p:
+    return cache.handle if isinstance(cache, PrefixCache) else cache
+
+
+def pkv_prefix_cache_create(pool: PoolLike) -> PrefixCache:
+    h = ctypes.c_void_p()
+    _check(_L().pkv_prefix_cache_create(_h(pool), ctypes.byref(h)), "pkv_prefix_cache_create")
+    return PrefixCache(h, pool)
+
+
+def pkv_prefix_cache_destroy(cache: PrefixCache) -> None:
+    _check(_L().pkv_prefix_cache_destroy(_c(cache)), "pkv_prefix_cache_destroy")
+    cache.handle = None
+
+
+def pkv_prefix_match(cache, tokens):
+    """(matched tokens, their blocks) for a prompt; changes nothing."""
+    t = _i32(tokens)
+    n = ctypes.c_int64()
+    out = np.zeros(max(len(t), 1), np.int32)
+    _check(_L().pkv_prefix_match(_c(cache), _p32(t), len(t), ctypes.byref(n), _p32(out)), "pkv_prefix_match")
+    B = _pool_block_size(cache)
+    return n.value, out[: n.value // B].copy()
+
+
+def _pool_block_size(cache) -> int:
+    return pkv_pool_geometry(cache.pool).block_size
+
+
+def pkv_prefix_attach(cache, tokens):
+    """Serve a prompt from the cache: (new sequence id, matched tokens)."""
+    t = _i32(tokens)
+    seq = ctypes.c_int32()
+    n = ctypes.c_int64()
+    _check(_L().pkv_prefix_attach(_c(cache), _p32(t), len(t), ctypes.byref(seq), ctypes.byref(n)),
+           "pkv_prefix_attach")
+    return seq.value, n.value
+
+
+def pkv_prefix_insert(cache, seq: int, tokens) -> None:
+    t = _i32(tokens)
+    _check(_L().pkv_prefix_insert(_c(cache), seq, _p32(t), len(t)), "pkv_prefix_insert")
+
+
+def pkv_prefix_release(cache, seq: int) -> None:
+    _check(_L().pkv_prefix_release(_c(cache), seq), "pkv_prefix_release")
+
+
+def pkv_prefix_evict(cache, target_free: int) -> int:
+    n = ctypes.c_int64()
+    _check(_L().pkv_prefix_evict(_c(cache), int(target_free), ctypes.byref(n)), "pkv_prefix_evict")
+    return n.value
+
+
+def pkv_prefix_get_stats(cache) -> PrefixStats:
+    st = PrefixStats()
+    _check(_L().pkv_prefix_get_stats(_c(cache), ctypes.byref(st)), "pkv_prefix_get_stats")
+    return st
+
+
+def pkv_prefix_export(cache):
+    """Preorder rows (parent row, blocks, ref, last_access, serial, tokens, block ids)."""
+    st = pkv_prefix_get_stats(cache)
+    B = _pool_block_size(cache)
+    nodes = np.zeros((max(st.nodes, 1), 5), np.int64)
+    toks = np.zeros(max(st.blocks * B, 1), np.int32)
+    blks = np.zeros(max(st.blocks, 1), np.int32)
+    _check(_L().pkv_prefix_export(_c(cache), nodes.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), _p32(toks),
+                                  _p32(blks), st.nodes, st.blocks), "pkv_prefix_export")
+    rows, off = [], 0
+    for r in range(st.nodes):
+        parent, nb, ref, last, serial = (int(x) for x in nodes[r])
+        rows.append((parent, nb, ref, last, serial, toks[off * B:(off + nb) * B].tolist(), blks[off:off + nb].tolist()))
+        off += nb
+    return rows

@@ -189,6 +189,7 @@ int pkv_pool_destroy(pkv_pool* pool) {
   pkv::clear_error();
   if (!pool) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
   Pool* P = as_pool(pool);
+  if (P->n_prefix_caches > 0) return fail(PKV_ERR_INVALID_ARG, "destroy the pool's prefix caches first");
   pkv::destroy_tensor_maps(*P);
   delete P;
   return PKV_OK;

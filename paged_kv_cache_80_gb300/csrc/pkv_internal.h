@@ -60,6 +60,7 @@ struct Pool {
   int32_t next_id = 0;
   int32_t swap_engine = 0;  // 0 SM kernel, 1 copy engine
   float k_scale = 1.f, v_scale = 1.f;  // FP8 pools: stored code * scale
+  int32_t n_prefix_caches = 0;         // live radix prefix caches holding references
 
   std::mutex tmap_mu;
   TensorMaps* tmaps = nullptr;
