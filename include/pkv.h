@@ -390,6 +390,39 @@ int pkv_prefix_get_stats(const pkv_prefix_cache* cache, pkv_prefix_stats* out);
 int pkv_prefix_export(const pkv_prefix_cache* cache, int64_t* nodes, int32_t* tokens, int32_t* blocks,
                       int64_t cap_nodes, int64_t cap_blocks);
 
+/* ---------------------------------------------------------------- admission simulator (host only)
+ *
+ * [PA] "The policy is where it succeeds or fails": how many steps a decode loop needs to
+ * finish a saturated queue of requests under an admission policy, using this pool's own
+ * allocator (reservations and paged growth are pkv_seq_create / pkv_plan_append /
+ * pkv_seq_free calls).  Every step, each running sequence emits one token (prefill is
+ * free).  Requests are admitted from the queue head while the policy allows:
+ *   PKV_SIM_RESERVE_MAX      reserve max_context tokens per sequence;
+ *   PKV_SIM_RESERVE_DECLARED reserve prompt + declared[i] tokens;
+ *   PKV_SIM_PAGED            allocate the prompt's blocks if, after they are taken, at least
+ *                            watermark * num_blocks blocks are still free; a token that opens
+ *                            a block with none free preempts the newest running sequence (its
+ *                            blocks are freed, it returns to the queue head and is readmitted
+ *                            with blocks for its prompt and the tokens it had generated).
+ * Sequences are processed oldest first within a step; a finished one frees its blocks at once.
+ * charged_steps = steps + recompute_steps * preemptions.  The pool must have every block
+ * free; it is left that way.  Errors: INVALID_ARG (lengths: answer >= 1, prompt + answer <=
+ * max_context, declared >= answer), OUT_OF_BLOCKS (a request cannot be admitted into the empty
+ * pool: its blocks, plus the watermark for PKV_SIM_PAGED, exceed the pool). */
+enum pkv_sim_policy { PKV_SIM_RESERVE_MAX = 0, PKV_SIM_RESERVE_DECLARED = 1, PKV_SIM_PAGED = 2 };
+typedef struct pkv_sim_config {
+  int32_t policy;          /* enum pkv_sim_policy */
+  int32_t max_context;     /* tokens */
+  double watermark;        /* PKV_SIM_PAGED: free fraction kept after an admission, in [0, 1) */
+  int32_t recompute_steps; /* charged per preemption */
+} pkv_sim_config;
+typedef struct pkv_sim_result {
+  int64_t steps, charged_steps, preemptions, completed, max_running;
+  double mean_running;     /* running sequences per step, averaged over steps */
+} pkv_sim_result;
+int pkv_sim_run(pkv_pool* pool, const pkv_sim_config* cfg, const int32_t* prompt, const int32_t* answer,
+                const int32_t* declared, int32_t n_req, pkv_sim_result* out);
+
 /* Failure-path self-test: launch one warp that waits on an mbarrier nothing will
  * complete, bounded by timeout_ns (<= 10 s) of the GPU's global timer -- the same
  * bounded wait the decode kernel uses for its tile loads.  When the bound runs out

@@ -50,6 +50,8 @@ def lib():
         L.orc_free_list.restype = i64
         L.orc_free_list.argtypes = [vp, P32]
         L.orc_seq_adopt.argtypes = [vp, P32, i64, i64, P32]
+        L.orc_free_count.restype = i64
+        L.orc_free_count.argtypes = [vp]
         L.orc_block_retain.argtypes = [vp, i32]
         L.orc_block_release.argtypes = [vp, i32]
         L.orc_swap_out.argtypes = [vp, i32, P64, P32]
@@ -170,6 +172,9 @@ class Pool:
         out = np.zeros(self.num_blocks, np.int32)
         lib().orc_refcounts(self._h, _p32(out))
         return out
+
+    def free_count(self) -> int:
+        return int(lib().orc_free_count(self._h))
 
     def free_list(self) -> np.ndarray:
         out = np.zeros(self.num_blocks, np.int32)

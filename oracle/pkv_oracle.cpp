@@ -249,6 +249,9 @@ int orc_seq_adopt(void* h, const int32_t* blocks, int64_t n, int64_t len, int32_
   return ORC_OK;
 }
 
+// Number of blocks on the free list.
+int64_t orc_free_count(void* h) { return static_cast<int64_t>(static_cast<Pool*>(h)->free_fifo.size()); }
+
 // One more owner of an allocated block (the prefix cache holding it).
 int orc_block_retain(void* h, int32_t p) {
   Pool& P = *static_cast<Pool*>(h);

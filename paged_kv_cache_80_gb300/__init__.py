@@ -26,6 +26,7 @@ __all__ = [
     "pkv_selftest_bounded_wait", "pkv_pool_set_kv_scales", "pkv_pool_kv_scales",
     "PrefixStats", "pkv_prefix_cache_create", "pkv_prefix_cache_destroy", "pkv_prefix_match", "pkv_prefix_attach",
     "pkv_prefix_insert", "pkv_prefix_release", "pkv_prefix_evict", "pkv_prefix_get_stats", "pkv_prefix_export",
+    "SimConfig", "SimResult", "SIM_POLICIES", "pkv_sim_run",
 ]
 
 F32, F16, BF16, E4M3 = 0, 1, 2, 3
@@ -55,6 +56,18 @@ class PrefixStats(ctypes.Structure):
                 ("dormant_leaves", ctypes.c_int64), ("prompt_tokens", ctypes.c_int64),
                 ("matched_tokens", ctypes.c_int64)]
 
+
+class SimConfig(ctypes.Structure):
+    _fields_ = [("policy", ctypes.c_int32), ("max_context", ctypes.c_int32), ("watermark", ctypes.c_double),
+                ("recompute_steps", ctypes.c_int32)]
+
+
+class SimResult(ctypes.Structure):
+    _fields_ = [("steps", ctypes.c_int64), ("charged_steps", ctypes.c_int64), ("preemptions", ctypes.c_int64),
+                ("completed", ctypes.c_int64), ("max_running", ctypes.c_int64), ("mean_running", ctypes.c_double)]
+
+
+SIM_POLICIES = {"reserve_max": 0, "reserve_declared": 1, "paged": 2}
 
 _lib = None
 
@@ -113,6 +126,8 @@ def _L():
             "pkv_prefix_evict": ([vp, i64, P64], ctypes.c_int),
             "pkv_prefix_get_stats": ([vp, ctypes.POINTER(PrefixStats)], ctypes.c_int),
             "pkv_prefix_export": ([vp, P64, P32, P32, i64, i64], ctypes.c_int),
+            "pkv_sim_run": ([vp, ctypes.POINTER(SimConfig), P32, P32, P32, i32, ctypes.POINTER(SimResult)],
+                            ctypes.c_int),
         }
         for name, (args, res) in sig.items():
             f = getattr(L, name)
@@ -537,3 +552,18 @@ def pkv_prefix_export(cache):
         rows.append((parent, nb, ref, last, serial, toks[off * B:(off + nb) * B].tolist(), blks[off:off + nb].tolist()))
         off += nb
     return rows
+
+
+# ------------------------------------------------------------------ admission simulator (host)
+
+
+def pkv_sim_run(pool: PoolLike, policy: str, prompt, answer, declared=None, max_context: int = 1024,
+                watermark: float = 0.0, recompute_steps: int = 4) -> dict:
+    """Steps to serve a saturated queue under an admission policy (see pkv.h)."""
+    cfg = SimConfig(SIM_POLICIES[policy], max_context, watermark, recompute_steps)
+    p, a = _i32(prompt), _i32(answer)
+    d = _i32(declared) if declared is not None else None
+    res = SimResult()
+    _check(_L().pkv_sim_run(_h(pool), ctypes.byref(cfg), _p32(p), _p32(a), _p32(d) if d is not None else None, len(p),
+                            ctypes.byref(res)), "pkv_sim_run")
+    return {k: getattr(res, k) for k, _ in SimResult._fields_}

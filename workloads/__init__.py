@@ -36,7 +36,7 @@ import numpy as np
 DTYPE_BYTES = {"f32": 4, "f16": 2, "bf16": 2, "e4m3": 1}
 
 # seed = workload index * 1000 + 7
-SEEDS = {"tiny": 1007, "chat": 2007, "agent32k": 3007, "forked": 4007, "swap": 5007}
+SEEDS = {"tiny": 1007, "chat": 2007, "agent32k": 3007, "forked": 4007, "swap": 5007, "admission": 6007}
 
 
 def substream(seed: int, tag: str) -> np.random.Generator:
@@ -210,3 +210,21 @@ def swap(n_chunks: int = 512, chunk_blocks: int = 16, num_blocks: int = 12288, L
     return Workload("swap", g, s, permutation(s, "free_order", num_blocks),
                     np.full(n_chunks, chunk_blocks * 16, dtype=np.int64),
                     {"evict_order": evict_order, "restore": restore, "chunk_blocks": chunk_blocks})
+
+
+# (mean prompt, mean answer) of the admission-simulator workloads: "chat-like" is the chat
+# length mix above; "long prompt" and "long answer" are not parameterised on the page.
+ADMISSION_KINDS = {"chat": (217.0, 154.0), "long_prompt": (600.0, 60.0), "long_answer": (40.0, 500.0)}
+
+
+def admission(kind: str = "chat", n: int = 3000, max_context: int = 1024):
+    """Request lengths for the admission simulator: lognormal prompt and answer (sigma 1,
+    the given means), prompt clipped to [1, max_context - 1], answer to [1, max_context -
+    prompt]; each request declares an output limit of twice its answer, capped by the
+    context.  Returns int32 arrays (prompt, answer, declared)."""
+    s = SEEDS["admission"]
+    mp, ma = ADMISSION_KINDS[kind]
+    prompt = np.clip(lognormal_lengths(s, f"{kind}_prompt", mp, n), 1, max_context - 1)
+    answer = np.clip(lognormal_lengths(s, f"{kind}_answer", ma, n), 1, max_context - prompt)
+    declared = np.minimum(max_context - prompt, 2 * answer)
+    return prompt.astype(np.int32), answer.astype(np.int32), declared.astype(np.int32)
