@@ -60,7 +60,7 @@ def decode_sources_digest() -> str:
     import hashlib
 
     h = hashlib.sha256()
-    for f in ("pkv_decode.cu", "pkv_device.cuh"):
+    for f in ("pkv_decode.cu", "pkv_attn.cuh", "pkv_device.cuh"):
         with open(os.path.join(ROOT, "paged_kv_cache_80_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()

@@ -13,8 +13,8 @@ CSRC = os.path.join(HERE, "csrc")
 ROOT = os.path.dirname(HERE)
 LIB = os.path.join(HERE, "libpkv.so")
 BUILD_DIR = os.path.join(ROOT, "_build")
-SOURCES = ["pkv_api.cpp", "pkv_copy.cu", "pkv_decode.cu", "pkv_prefix.cpp", "pkv_sim.cpp"]
-HEADERS = ["pkv_internal.h", "pkv_device.cuh"]
+SOURCES = ["pkv_api.cpp", "pkv_copy.cu", "pkv_decode.cu", "pkv_prefill.cu", "pkv_prefix.cpp", "pkv_sim.cpp"]
+HEADERS = ["pkv_internal.h", "pkv_device.cuh", "pkv_attn.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

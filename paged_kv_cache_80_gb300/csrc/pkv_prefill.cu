@@ -1,0 +1,376 @@
+// Chunked-prefill paged attention for one layer ("KV Cache Management", cs249r vol. 3
+// ch. 5, "Chunked prefill mechanics"): the queries of a chunk attend to the cached keys of
+// earlier chunks in full and to their own chunk causally.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <string>
+
+#include "pkv_attn.cuh"
+#include "pkv_device.cuh"
+#include "pkv_internal.h"
+
+namespace pkv {
+
+namespace {
+
+// --------------------------------------------------------------------------- chunked prefill (tensor cores)
+//
+// "KV Cache Management", "Chunked prefill mechanics": the queries of a chunk attend to
+// the cached keys of earlier chunks in full and to their own chunk causally,
+// O_k = Softmax(Q_k K_<=k^T / sqrt(d) + M_k) V_<=k; the chunk's keys/values are already
+// in the pool, so query i of sequence s (position P_s + i, P_s = len_s - C_s) sees the
+// paged keys 0 .. P_s + i.
+// One CTA per (query block, KV head, sequence): 8 warps x 16 rows = 128 rows, a row
+// being one (query, head of the group) pair, so every K/V tile staged in shared memory
+// serves all of them.  Keys stream in tiles of 64 (four 16-token slabs, each from its
+// own pool block, TMA with 128-byte swizzle, two stages).  S = Q K^T and O += P V are
+// mma.sync m16n8k16 with the accumulator of S reused as the A operand of P V.
+
+constexpr int PF_WARPS = 8;
+constexpr int PF_ROWS = PF_WARPS * 16;
+constexpr int PF_KEYS = 64;
+constexpr int PF_SLABS = PF_KEYS / TILE;
+
+template <int D>
+struct PfCfg {
+  static constexpr int SLAB = TILE * D * 2;          // one 16-token slab of K (or V)
+  static constexpr int STAGE = 2 * PF_SLABS * SLAB;  // K slabs then V slabs
+  static constexpr int NKC = D / 16;                 // 16-wide chunks of d
+  static constexpr int NDG = D / 8;                  // 8-wide groups of d (PV n8 tiles)
+  static constexpr int NBOX = D / 64;
+};
+
+template <typename T, int D>
+__global__ void __launch_bounds__(PF_WARPS * 32, 1) prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk,
+                                                                       const __grid_constant__ CUtensorMap tmv,
+                                                                       const DecodeArgs a, const int32_t* q_off,
+                                                                       int blk_cap) {
+  using C = PfCfg<D>;
+  constexpr bool BF16 = std::is_same<T, __nv_bfloat16>::value;
+  extern __shared__ uint8_t smem_raw[];
+  const int qb = blockIdx.x, g = blockIdx.y, s = blockIdx.z;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int G = a.G;
+  const int QB = PF_ROWS / G;  // queries per CTA
+  const int qbeg = q_off[s];
+  const int Cs = q_off[s + 1] - qbeg;
+  const int i0 = qb * QB;
+  if (qb == gridDim.x - 1 && tid == 0 && g == 0 && Cs > i0 + QB) record_error(a.err, DERR_PREFILL_CHUNK, s);
+  if (i0 >= Cs) return;  // uniform over the CTA
+  const int i1 = min(Cs, i0 + QB);
+  const int len = a.seq_lens[s];
+  if (Cs < 0 || len < Cs || len > static_cast<int64_t>(a.W) * a.B) {
+    if (tid == 0 && qb == 0 && g == 0) record_error(a.err, DERR_DECODE_LEN, s);
+    return;
+  }
+  const int P = len - Cs;
+  const int pmin = P + i0, pmax = P + i1 - 1;
+  const int nkeys = pmax + 1;
+  const int ntiles = (nkeys + PF_KEYS - 1) / PF_KEYS;
+  const int nblk = (nkeys + a.B - 1) / a.B;
+  if (nblk > blk_cap) {  // the host sizes blk_cap from W: cannot happen for valid lengths
+    if (tid == 0) record_error(a.err, DERR_DECODE_LEN, s);
+    return;
+  }
+
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t stage0 = smem_u32(base);
+  int32_t* blks = reinterpret_cast<int32_t*>(base + 2 * C::STAGE);
+  const uint32_t bar0 = smem_u32(base + 2 * C::STAGE + ((blk_cap * 4 + 15) / 16) * 16);
+
+  for (int k = tid; k < nblk; k += blockDim.x) {
+    int b = a.tables[static_cast<int64_t>(s) * a.W + k];
+    if (b < 0 || b >= a.num_blocks) {
+      record_error(a.err, DERR_DECODE_BLOCK, b);
+      b = 0;
+    }
+    blks[k] = b;
+  }
+  if (tid == 0) {
+    mbar_init(bar0, 1);
+    mbar_init(bar0 + 8, 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  auto issue = [&](int kt) {  // thread 0 only
+    const int st = kt & 1;
+    const uint32_t bar = bar0 + 8 * st;
+    const uint32_t sk = stage0 + st * C::STAGE;
+    int n = 0;
+    for (int j = 0; j < PF_SLABS; ++j) n += (kt * PF_KEYS + j * TILE < nkeys) ? 1 : 0;
+    fence_proxy_async();
+    mbar_arrive_expect_tx(bar, 2 * n * C::SLAB);
+    for (int j = 0; j < n; ++j) {
+      const int t0 = kt * PF_KEYS + j * TILE;
+      const int lb = t0 / a.B;
+      const int row = ((blks[lb] * a.L + a.layer) * a.H_kv + g) * a.B + (t0 - lb * a.B);
+#pragma unroll
+      for (int b = 0; b < C::NBOX; ++b) {
+        tma_load_2d(sk + j * C::SLAB + b * (TILE * 128), &tmk, b * 64, row, bar);
+        tma_load_2d(sk + (PF_SLABS + j) * C::SLAB + b * (TILE * 128), &tmv, b * 64, row, bar);
+      }
+    }
+  };
+  if (tid == 0) {
+    issue(0);
+    if (ntiles > 1) issue(1);
+  }
+
+  // this warp's rows: r0 = warp*16 + lane/4, r1 = r0 + 8; row r = (query r / G, head r % G)
+  const int r0 = warp * 16 + (lane >> 2), r1 = r0 + 8;
+  const int qi0 = i0 + r0 / G, qi1 = i0 + r1 / G;
+  const bool v0 = r0 < QB * G && qi0 < i1, v1 = r1 < QB * G && qi1 < i1;
+  const int p0 = v0 ? P + qi0 : pmax, p1 = v1 ? P + qi1 : pmax;  // last visible key
+  const int64_t qrow0 = (static_cast<int64_t>(qbeg + qi0) * a.H_q + g * G + r0 % G) * D;
+  const int64_t qrow1 = (static_cast<int64_t>(qbeg + qi1) * a.H_q + g * G + r1 % G) * D;
+  const int c2 = 2 * (lane & 3);
+  uint32_t qa[C::NKC][4];
+  {
+    const T* q = static_cast<const T*>(a.q);
+#pragma unroll
+    for (int c = 0; c < C::NKC; ++c) {
+      qa[c][0] = v0 ? *reinterpret_cast<const uint32_t*>(q + qrow0 + 16 * c + c2) : 0u;
+      qa[c][1] = v1 ? *reinterpret_cast<const uint32_t*>(q + qrow1 + 16 * c + c2) : 0u;
+      qa[c][2] = v0 ? *reinterpret_cast<const uint32_t*>(q + qrow0 + 16 * c + 8 + c2) : 0u;
+      qa[c][3] = v1 ? *reinterpret_cast<const uint32_t*>(q + qrow1 + 16 * c + 8 + c2) : 0u;
+    }
+  }
+  float o[C::NDG][4];
+#pragma unroll
+  for (int n = 0; n < C::NDG; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+  const int r8 = lane & 7, mi = lane >> 3;
+
+  for (int kt = 0; kt < ntiles; ++kt) {
+    const int st = kt & 1;
+    const uint32_t sk = stage0 + st * C::STAGE;
+    const uint32_t sv = sk + PF_SLABS * C::SLAB;
+    if (!mbar_wait_bounded(bar0 + 8 * st, (kt >> 1) & 1, kWaitNs)) {
+      if (lane == 0) record_error(a.err, DERR_DECODE_TIMEOUT, kt);
+      if (tid == 0 && kt + 1 < ntiles) mbar_wait_bounded(bar0 + 8 * ((kt + 1) & 1), ((kt + 1) >> 1) & 1, kWaitNs);
+      return;
+    }
+    const int kbase = kt * PF_KEYS;
+    const int nvalid = min(PF_KEYS, nkeys - kbase);  // keys of this tile that exist
+    if (nvalid < PF_KEYS && (nvalid & (TILE - 1))) {
+      // zero the V rows past the last key of the last loaded slab (0 * stale could be NaN)
+      const int js = nvalid / TILE, r_from = nvalid - js * TILE;
+      uint8_t* vrows = base + st * C::STAGE + (PF_SLABS + js) * C::SLAB;
+      for (int k = tid; k < (TILE - r_from) * 8 * C::NBOX; k += blockDim.x) {
+        const int b = k / ((TILE - r_from) * 8);
+        const int rem = k - b * (TILE - r_from) * 8;
+        *reinterpret_cast<int4*>(vrows + b * (TILE * 128) + (r_from + rem / 8) * 128 + (rem & 7) * 16) =
+            make_int4(0, 0, 0, 0);
+      }
+      __syncthreads();
+    }
+    // ---- S = Q K^T over the tile's 64 keys: 8 groups of 8 keys
+    float sf[PF_KEYS / 8][4];
+#pragma unroll
+    for (int grp = 0; grp < PF_KEYS / 8; ++grp) {
+      sf[grp][0] = sf[grp][1] = sf[grp][2] = sf[grp][3] = 0.f;
+      if (grp * 8 >= nvalid) continue;
+      const int slab = grp >> 1, krow = (grp & 1) * 8 + r8;
+#pragma unroll
+      for (int c = 0; c < C::NKC; c += 2) {
+        const int doff = 16 * c + 8 * mi;
+        const int chunk = (doff & 63) >> 3;
+        const uint32_t addr = sk + slab * C::SLAB + (doff >> 6) * (TILE * 128) + krow * 128 + ((chunk ^ r8) << 4);
+        uint32_t b0, b1, b2, b3;
+        ldmatrix_x4(addr, b0, b1, b2, b3);
+        mma_16816<BF16>(sf[grp], qa[c][0], qa[c][1], qa[c][2], qa[c][3], b0, b1);
+        mma_16816<BF16>(sf[grp], qa[c + 1][0], qa[c + 1][1], qa[c + 1][2], qa[c + 1][3], b2, b3);
+      }
+    }
+    // ---- scale, causal mask, online softmax (rows r0: c0/c1, r1: c2/c3)
+    const bool need_mask = kbase + PF_KEYS - 1 > pmin;
+    float x0 = -INFINITY, x1 = -INFINITY;
+#pragma unroll
+    for (int grp = 0; grp < PF_KEYS / 8; ++grp) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        float v = sf[grp][e] * a.scale_log2;
+        if (need_mask) {
+          const int t = kbase + grp * 8 + c2 + (e & 1);
+          if (t > ((e < 2) ? p0 : p1)) v = -INFINITY;
+        }
+        sf[grp][e] = v;
+      }
+      x0 = fmaxf(x0, fmaxf(sf[grp][0], sf[grp][1]));
+      x1 = fmaxf(x1, fmaxf(sf[grp][2], sf[grp][3]));
+    }
+    x0 = fmaxf(x0, __shfl_xor_sync(0xffffffffu, x0, 1));
+    x0 = fmaxf(x0, __shfl_xor_sync(0xffffffffu, x0, 2));
+    x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, 1));
+    x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, 2));
+    const float n0 = fmaxf(m0, x0), n1 = fmaxf(m1, x1);  // finite: key 0 is visible to every row
+    const float cr0 = exp2f(m0 - n0), cr1 = exp2f(m1 - n1);
+    m0 = n0;
+    m1 = n1;
+    float ps0 = 0.f, ps1 = 0.f;
+#pragma unroll
+    for (int grp = 0; grp < PF_KEYS / 8; ++grp) {
+      sf[grp][0] = exp2f(sf[grp][0] - n0);
+      sf[grp][1] = exp2f(sf[grp][1] - n0);
+      sf[grp][2] = exp2f(sf[grp][2] - n1);
+      sf[grp][3] = exp2f(sf[grp][3] - n1);
+      ps0 += sf[grp][0] + sf[grp][1];
+      ps1 += sf[grp][2] + sf[grp][3];
+    }
+    l0 = l0 * cr0 + ps0;
+    l1 = l1 * cr1 + ps1;
+#pragma unroll
+    for (int n = 0; n < C::NDG; ++n) {
+      o[n][0] *= cr0;
+      o[n][1] *= cr0;
+      o[n][2] *= cr1;
+      o[n][3] *= cr1;
+    }
+    // ---- O += P V: one k16 step per slab; P's accumulator layout is the A operand
+#pragma unroll
+    for (int j = 0; j < PF_SLABS; ++j) {
+      if (j * TILE >= nvalid) continue;
+      const uint32_t pa0 = pack2<T>(sf[2 * j][0], sf[2 * j][1]);
+      const uint32_t pa1 = pack2<T>(sf[2 * j][2], sf[2 * j][3]);
+      const uint32_t pa2 = pack2<T>(sf[2 * j + 1][0], sf[2 * j + 1][1]);
+      const uint32_t pa3 = pack2<T>(sf[2 * j + 1][2], sf[2 * j + 1][3]);
+      const int vrow = 8 * (mi & 1) + r8;
+#pragma unroll
+      for (int n = 0; n < C::NDG; n += 2) {
+        const int doff = 8 * (n + (mi >> 1));
+        const int chunk = (doff & 63) >> 3;
+        const uint32_t addr = sv + j * C::SLAB + (doff >> 6) * (TILE * 128) + vrow * 128 + ((chunk ^ r8) << 4);
+        uint32_t b0, b1, b2, b3;
+        ldmatrix_x4_trans(addr, b0, b1, b2, b3);
+        mma_16816<BF16>(o[n], pa0, pa1, pa2, pa3, b0, b1);
+        mma_16816<BF16>(o[n + 1], pa0, pa1, pa2, pa3, b2, b3);
+      }
+    }
+    __syncthreads();  // every warp is done with this stage
+    if (tid == 0 && kt + 2 < ntiles) issue(kt + 2);
+  }
+
+  // ---- normalise and write the valid rows
+  l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+  l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+  l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+  l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+  const float inv0 = 1.f / l0, inv1 = 1.f / l1;
+  T* out = static_cast<T*>(a.out);
+#pragma unroll
+  for (int n = 0; n < C::NDG; ++n) {
+    const int dd = 8 * n + c2;
+    if (v0) *reinterpret_cast<uint32_t*>(out + qrow0 + dd) = pack2<T>(o[n][0] * inv0, o[n][1] * inv0);
+    if (v1) *reinterpret_cast<uint32_t*>(out + qrow1 + dd) = pack2<T>(o[n][2] * inv1, o[n][3] * inv1);
+  }
+}
+
+// Chunked prefill on CUDA cores: one CTA per (query row, KV head).  The row's
+// sequence s is found in q_off; its position is len_s - C_s + (row - q_off[s]) and it
+// attends to every token up to and including that position.
+template <typename TS, typename TA, int NPL>
+__global__ void __launch_bounds__(SIMT_WARPS * 32) prefill_simt_kernel(const DecodeArgs a, const int32_t* q_off,
+                                                                         const TS* __restrict__ kp,
+                                                                         const TS* __restrict__ vp, int d) {
+  const int row = blockIdx.x, g = blockIdx.y;
+  int lo = 0, hi = a.n_seq - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (q_off[mid] <= row) lo = mid; else hi = mid - 1;
+  }
+  const int s = lo;
+  const int C = q_off[s + 1] - q_off[s];
+  const int len = a.seq_lens[s];
+  const int64_t base = (static_cast<int64_t>(row) * a.H_q + g * a.G) * d;
+  if (C < 0 || len < C || len > static_cast<int64_t>(a.W) * a.B) {
+    if (threadIdx.x == 0 && g == 0 && row == q_off[s]) record_error(a.err, DERR_DECODE_LEN, s);
+    for (int k = threadIdx.x; k < a.G * d; k += blockDim.x) static_cast<TA*>(a.out)[base + k] = f_to<TA>(0.f);
+    return;
+  }
+  const int pos = len - C + (row - q_off[s]);
+  simt_attend<TS, TA, NPL>(a, kp, vp, d, s, g, pos + 1, static_cast<const TA*>(a.q) + base,
+                           static_cast<TA*>(a.out) + base);
+}
+
+// The CUDA-core prefill kernel for the pool's element types: one CTA per (query row, KV head).
+template <typename TS, typename TA>
+void simt_prefill_t(const DecodeArgs& a, const int32_t* q_off, const void* kp, const void* vp, dim3 grid, size_t smem,
+                    cudaStream_t st) {
+  const int d = a.D;
+#define PKV_PF_SIMT(NPL)                                                                             \
+  {                                                                                                  \
+    auto kern = prefill_simt_kernel<TS, TA, NPL>;                                                    \
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)); \
+    kern<<<grid, SIMT_WARPS * 32, smem, st>>>(a, q_off, static_cast<const TS*>(kp), static_cast<const TS*>(vp), d); \
+  }
+  switch ((d + 31) / 32) {
+    case 1: PKV_PF_SIMT(1) break;
+    case 2: PKV_PF_SIMT(2) break;
+    case 3: case 4: PKV_PF_SIMT(4) break;
+    default: PKV_PF_SIMT(8) break;
+  }
+#undef PKV_PF_SIMT
+}
+
+}  // namespace
+
+int launch_prefill(Pool& P, int32_t layer, const void* q, const int32_t* q_off, int32_t n_tok, int32_t max_q,
+                   const void* k_pool, const void* v_pool, const int32_t* tables, int32_t W, const int32_t* seq_lens,
+                   int32_t n_seq, float scale, void* out, void* stream) {
+  const auto& g = P.geo;
+  const int G = g.H_q / g.H_kv;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  DecodeArgs a;
+  if (int rc = fill_args(P, layer, q, out, tables, W, seq_lens, n_seq, scale, &a)) return rc;
+  cudaError_t e = cudaSuccess;
+  const int64_t rows = g.num_blocks * g.L * g.H_kv * g.block_size;
+  const bool tc = (g.dtype == PKV_BF16 || g.dtype == PKV_F16) && (g.d_head == 64 || g.d_head == 128) &&
+                  G <= PF_ROWS && g.block_size % TILE == 0 && rows < (int64_t(1) << 31) && encode_fn() != nullptr;
+  if (!tc && G > GPAD) return fail(PKV_ERR_UNSUPPORTED, "more than 8 query heads per KV head on the CUDA-core path");
+  if (tc) {
+    if ((reinterpret_cast<uintptr_t>(q) & 15) || (reinterpret_cast<uintptr_t>(out) & 15))
+      return fail(PKV_ERR_INVALID_ARG, "q and out must be 16-byte aligned");
+    CUtensorMap maps[2];
+    if (int rc = get_tensor_maps(P, k_pool, v_pool, &maps[0], &maps[1])) return rc;
+    const int stage = 2 * PF_SLABS * TILE * g.d_head * 2;
+    const int blk_cap = W;
+    const size_t smem = 1024 + 2 * static_cast<size_t>(stage) + ((blk_cap * 4 + 15) / 16) * 16 + 16;
+    if (smem > 227 * 1024) return fail(PKV_ERR_UNSUPPORTED, "block table too wide for the prefill kernel");
+    const int QB = PF_ROWS / G;
+    dim3 grid((max_q + QB - 1) / QB, g.H_kv, n_seq);
+    const bool bf = g.dtype == PKV_BF16;
+    const void* k = g.d_head == 128 ? (bf ? reinterpret_cast<const void*>(&prefill_tc_kernel<__nv_bfloat16, 128>)
+                                          : reinterpret_cast<const void*>(&prefill_tc_kernel<__half, 128>))
+                                    : (bf ? reinterpret_cast<const void*>(&prefill_tc_kernel<__nv_bfloat16, 64>)
+                                          : reinterpret_cast<const void*>(&prefill_tc_kernel<__half, 64>));
+    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return fail(PKV_ERR_CUDA, std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e));
+    int cap = blk_cap;
+    void* args[] = {&maps[0], &maps[1], &a, const_cast<int32_t**>(&q_off), &cap};
+    e = cudaLaunchKernel(k, grid, dim3(PF_WARPS * 32), args, smem, st);
+    if (e != cudaSuccess) return fail(PKV_ERR_CUDA, std::string("prefill launch: ") + cudaGetErrorString(e));
+    count_launch();
+    return PKV_OK;
+  }
+  const size_t smem = sizeof(float) * (SIMT_WARPS * G * 2 + SIMT_WARPS * G * static_cast<size_t>(g.d_head));
+  const dim3 grid(n_tok, g.H_kv);
+  switch (g.dtype) {
+    case PKV_F32: simt_prefill_t<float, float>(a, q_off, k_pool, v_pool, grid, smem, st); break;
+    case PKV_F16: simt_prefill_t<__half, __half>(a, q_off, k_pool, v_pool, grid, smem, st); break;
+    case PKV_BF16: simt_prefill_t<__nv_bfloat16, __nv_bfloat16>(a, q_off, k_pool, v_pool, grid, smem, st); break;
+    default: simt_prefill_t<E4M3, __nv_bfloat16>(a, q_off, k_pool, v_pool, grid, smem, st); break;
+  }
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(PKV_ERR_CUDA, std::string("prefill launch: ") + cudaGetErrorString(e));
+  count_launch();
+  return PKV_OK;
+}
+
+
+}  // namespace pkv
