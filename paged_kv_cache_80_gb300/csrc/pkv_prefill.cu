@@ -8,6 +8,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <cstdlib>
 #include <string>
 
 #include "pkv_attn.cuh"
@@ -271,6 +272,325 @@ __global__ void __launch_bounds__(PF_WARPS * 32, 1) prefill_tc_kernel(const __gr
   }
 }
 
+// --------------------------------------------------------------------------- chunked prefill (tcgen05)
+//
+// Same work split (one CTA per (query block, KV head, sequence), M = 128 (query, head)
+// rows, row r = query r / G, head r % G), on the 5th-generation tensor cores:
+//   * warps 0-3 (softmax): one thread per row, which is also its TMEM lane; reads S with
+//     tcgen05.ld, keeps the row's running max m and sum l, writes P (16-bit) back to TMEM,
+//     and at the end reads O, divides by l and stores the row;
+//   * warp 4 (producer, TMEM owner): TMA loads of Q (two 3-D boxes whose rows land as
+//     (query, head)) and of 128-key K and V tiles (8 slabs of 16 tokens, each from its own
+//     pool block) into rings of 3 (K) and 2 (V) 32 KB slots, slab i at 2 KB stride so the
+//     8-row groups are uniformly 1 KB apart; it zeroes the V rows past the sequence end in
+//     the last tile so that P = 0 never meets a non-finite value;
+//   * warp 5 (one thread): S = Q K^T (tcgen05.mma kind::f16, both K-major, 128-byte
+//     swizzle, M = 128, N = 128, 8 x K = 16) into one of two S buffers, and O += P V with P
+//     read from TMEM and V as an MN-major operand (N = d).  QK^T of tile j + 1 runs on the
+//     tensor cores while the softmax of tile j runs.
+// TMEM (512 columns): S0 [0, 128), S1 [128, 256), P0 [256, 320), P1 [320, 384), O [384, 512).
+// The online softmax ("Chunked prefill mechanics": m_new = max(m, m_blk), l and O scaled by
+// e^{m - m_new}) rescales O in TMEM only when a row's max grows by more than 2^8; otherwise
+// the old max stays the reference, which is exact because P and l use the same reference.
+
+constexpr int UM_KEYS = 128;
+constexpr int UM_SLABS = UM_KEYS / TILE;
+constexpr int UM_KS = 3, UM_VS = 2;
+constexpr int UM_THREADS = 192;
+constexpr int UM_TILE_BYTES = 128 * 128 * 2;  // Q, or one K or V tile (128 rows x d 128, 16-bit)
+constexpr int UM_BARS = 1 + 2 * UM_KS + 2 * UM_VS + 2 + 2 + 2 + 1;
+constexpr int UM_SMEM = 1024 + (1 + UM_KS + UM_VS) * UM_TILE_BYTES + UM_BARS * 8 + 16;
+constexpr uint32_t UM_S_COL = 0, UM_P_COL = 256, UM_O_COL = 384;
+
+template <typename T>
+__global__ void __launch_bounds__(UM_THREADS, 1) prefill_umma_kernel(const __grid_constant__ CUtensorMap tmq,
+                                                                      const __grid_constant__ CUtensorMap tmk,
+                                                                      const __grid_constant__ CUtensorMap tmv,
+                                                                      const DecodeArgs a, const int32_t* q_off) {
+  constexpr int D = 128;
+  constexpr bool BF16 = std::is_same<T, __nv_bfloat16>::value;
+  extern __shared__ uint8_t smem_raw[];
+  const int qb = blockIdx.x, g = blockIdx.y, s = blockIdx.z;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int G = a.G;
+  const int QB = 128 / G;
+  const int qbeg = q_off[s];
+  const int Cs = q_off[s + 1] - qbeg;
+  const int i0 = qb * QB;
+  if (qb == gridDim.x - 1 && tid == 0 && g == 0 && Cs > i0 + QB) record_error(a.err, DERR_PREFILL_CHUNK, s);
+  if (i0 >= Cs) return;  // uniform over the CTA, before any barrier or TMEM use
+  const int len = a.seq_lens[s];
+  if (Cs < 0 || len < Cs || len > static_cast<int64_t>(a.W) * a.B) {
+    if (tid == 0 && qb == 0 && g == 0) record_error(a.err, DERR_DECODE_LEN, s);
+    return;
+  }
+  const int i1 = min(Cs, i0 + QB);
+  const int P = len - Cs;
+  const int pmax = P + i1 - 1;
+  const int nkeys = pmax + 1;
+  const int nt = (nkeys + UM_KEYS - 1) / UM_KEYS;
+  const bool tail = nkeys < nt * UM_KEYS;  // the last tile has keys past the sequence end
+
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t qs = smem_u32(base);
+  const uint32_t ks0 = qs + UM_TILE_BYTES, vs0 = ks0 + UM_KS * UM_TILE_BYTES;
+  uint8_t* bar_p = base + (1 + UM_KS + UM_VS) * UM_TILE_BYTES;
+  const uint32_t bars = smem_u32(bar_p);
+  const uint32_t q_full = bars;
+  const uint32_t k_full = bars + 8, k_empty = k_full + 8 * UM_KS;
+  const uint32_t v_full = k_empty + 8 * UM_KS, v_empty = v_full + 8 * UM_VS;
+  const uint32_t s_full = v_empty + 8 * UM_VS, p_full = s_full + 16, o_done = p_full + 16, vz = o_done + 16;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar_p + UM_BARS * 8);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bar_p + UM_BARS * 8 + 4);
+
+  if (tid == 0) {
+    mbar_init(q_full, 1);
+    for (int k = 0; k < UM_KS; ++k) {
+      mbar_init(k_full + 8 * k, 1);
+      mbar_init(k_empty + 8 * k, 1);
+    }
+    for (int k = 0; k < UM_VS; ++k) {
+      mbar_init(v_full + 8 * k, 1);
+      mbar_init(v_empty + 8 * k, 1);
+    }
+    for (int k = 0; k < 2; ++k) {
+      mbar_init(s_full + 8 * k, 1);
+      mbar_init(p_full + 8 * k, 128);
+      mbar_init(o_done + 8 * k, 1);
+    }
+    mbar_init(vz, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 4) tmem_alloc(smem_u32(tslot), 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tslot;
+
+  // bounded wait that also gives up once another role has given up
+  auto wait = [&](uint32_t bar, uint32_t parity, int where) -> bool {
+    const uint64_t t0 = global_ns();
+    for (;;) {
+      for (int k = 0; k < 32; ++k)
+        if (mbar_try_wait(bar, parity)) return true;
+      if (*abort_flag) return false;
+      if (global_ns() - t0 > kWaitNs) {
+        *abort_flag = 1;
+        record_error(a.err, DERR_DECODE_TIMEOUT, where);
+        return false;
+      }
+    }
+  };
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      fence_proxy_async();
+      mbar_arrive_expect_tx(q_full, 2 * 64 * G * QB * 2);
+      tma_load_3d(qs, &tmq, 0, g * G, qbeg + i0, q_full);
+      tma_load_3d(qs + 16384, &tmq, 64, g * G, qbeg + i0, q_full);
+    }
+    auto load = [&](int j, bool is_k) -> bool {  // whole warp; lane 0 issues
+      int row = 0;
+      const int t0 = j * UM_KEYS + lane * TILE;
+      if (lane < UM_SLABS && t0 < nkeys) {
+        const int lb = t0 / a.B;
+        int blk = a.tables[static_cast<int64_t>(s) * a.W + lb];
+        if (blk < 0 || blk >= a.num_blocks) {
+          record_error(a.err, DERR_DECODE_BLOCK, blk);
+          blk = 0;
+        }
+        row = ((blk * a.L + a.layer) * a.H_kv + g) * a.B + (t0 - lb * a.B);
+      }
+      const int nv = min(UM_SLABS, (nkeys - j * UM_KEYS + TILE - 1) / TILE);
+      bool ok = true;
+      if (lane == 0) {
+        const int slot = is_k ? j % UM_KS : j % UM_VS;
+        const int depth = is_k ? UM_KS : UM_VS;
+        const uint32_t full = (is_k ? k_full : v_full) + 8 * slot, empty = (is_k ? k_empty : v_empty) + 8 * slot;
+        if (j >= depth) ok = wait(empty, ((j / depth) - 1) & 1, 100 + j);
+        if (ok) {
+          mbar_arrive_expect_tx(full, nv * 2 * TILE * 128);
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      if (!ok) return false;
+      const int slot = is_k ? j % UM_KS : j % UM_VS;
+      const uint32_t dst = (is_k ? ks0 : vs0) + slot * UM_TILE_BYTES;
+      const uint32_t full = (is_k ? k_full : v_full) + 8 * slot;
+      for (int i = 0; i < nv; ++i) {
+        const int r = __shfl_sync(0xffffffffu, row, i);
+        if (lane == 0) {
+          tma_load_2d(dst + i * TILE * 128, is_k ? &tmk : &tmv, 0, r, full);
+          tma_load_2d(dst + 16384 + i * TILE * 128, is_k ? &tmk : &tmv, 64, r, full);
+        }
+      }
+      return true;
+    };
+    bool ok = load(0, true);
+    for (int j = 0; j < nt && ok; ++j) {
+      if (j + 1 < nt) ok = load(j + 1, true);
+      if (ok) ok = load(j, false);
+      if (ok && tail && j == nt - 1) {
+        // zero the V rows past the sequence end once the tile has landed
+        const int slot = j % UM_VS;
+        bool landed = true;
+        if (lane == 0) landed = wait(v_full + 8 * slot, (j / UM_VS) & 1, 200);
+        landed = __shfl_sync(0xffffffffu, landed ? 1 : 0, 0) != 0;
+        if (landed) {
+          uint8_t* vt = base + (1 + UM_KS + slot) * UM_TILE_BYTES;
+          const int r0 = nkeys - j * UM_KEYS;
+          for (int k = lane; k < (UM_KEYS - r0) * 16; k += 32) {  // 16-byte pieces, both d chunks
+            const int r = r0 + k / 16, c = k % 16;
+            *reinterpret_cast<int4*>(vt + (c / 8) * 16384 + r * 128 + (c % 8) * 16) = make_int4(0, 0, 0, 0);
+          }
+          fence_proxy_async();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(vz);
+        }
+      }
+    }
+  } else if (warp == 5) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc_s = umma_idesc_f16(BF16, 128, UM_KEYS, false);
+      const uint32_t idesc_o = umma_idesc_f16(BF16, 128, D, true);
+      bool ok = wait(q_full, 0, 1);
+      auto qk = [&](int j) -> bool {
+        const int slot = j % UM_KS;
+        if (!wait(k_full + 8 * slot, (j / UM_KS) & 1, 300 + j)) return false;
+        tc_fence_after();
+        const uint32_t kb = ks0 + slot * UM_TILE_BYTES;
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
+          umma_ss(tmem + UM_S_COL + (j & 1) * 128, umma_desc_sw128(qs + off, 16, 1024),
+                  umma_desc_sw128(kb + off, 16, 1024), idesc_s, k > 0);
+        }
+        umma_commit(s_full + 8 * (j & 1));
+        umma_commit(k_empty + 8 * slot);
+        return true;
+      };
+      if (ok) ok = qk(0);
+      if (ok && nt > 1) ok = qk(1);
+      for (int j = 0; j < nt && ok; ++j) {
+        ok = wait(p_full + 8 * (j & 1), (j >> 1) & 1, 400 + j);
+        const int vslot = j % UM_VS;
+        if (ok) ok = wait(v_full + 8 * vslot, (j / UM_VS) & 1, 500 + j);
+        if (ok && tail && j == nt - 1) ok = wait(vz, 0, 600);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t vb = vs0 + vslot * UM_TILE_BYTES;
+#pragma unroll
+        for (int k = 0; k < UM_KEYS / 16; ++k)
+          umma_ts(tmem + UM_O_COL, tmem + UM_P_COL + (j & 1) * 64 + 8 * k,
+                  umma_desc_sw128(vb + k * 16 * 128, 16384, 1024), idesc_o, (j > 0 || k > 0) ? 1u : 0u);
+        umma_commit(o_done + 8 * (j & 1));
+        umma_commit(v_empty + 8 * vslot);
+        if (j + 2 < nt) ok = qk(j + 2);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ softmax and epilogue (warps 0-3)
+    const int r = tid;
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const int qi = i0 + r / G, h = r % G;
+    const bool valid = r < QB * G && qi < i1;
+    const int lim = valid ? P + qi : pmax;  // last visible key
+    float m = -INFINITY, l = 0.f;
+    bool ok = true;
+    // tcgen05.ld / st are warp-collective: every decision below is uniform over the warp
+    for (int j = 0; j < nt && ok; ++j) {
+      ok = __all_sync(0xffffffffu, wait(s_full + 8 * (j & 1), (j >> 1) & 1, 700 + j));
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t sv[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld32(lane_addr + UM_S_COL + (j & 1) * 128 + 32 * c, sv[c]);
+      tmem_ld_wait();
+      const int k0 = j * UM_KEYS;
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          float x = __uint_as_float(sv[c][e]) * a.scale_log2;
+          if (k0 + 32 * c + e > lim) x = -INFINITY;
+          sv[c][e] = __float_as_uint(x);
+          mx = fmaxf(mx, x);
+        }
+      const float m_new = fmaxf(m, mx);
+      if (__any_sync(0xffffffffu, m_new > m + 8.f)) {  // the reference max moves: rescale l and O so far
+        const float alpha = exp2f(m - m_new);
+        if (j > 0) {
+          ok = __all_sync(0xffffffffu, wait(o_done + 8 * ((j - 1) & 1), ((j - 1) >> 1) & 1, 800 + j));
+          if (!ok) break;
+          tc_fence_after();
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32(lane_addr + UM_O_COL + 32 * c, o);
+            tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            tmem_st32(lane_addr + UM_O_COL + 32 * c, o);
+          }
+        }
+        l *= alpha;
+        m = m_new;
+      }
+      // P = 2^(x - m), 16-bit, two keys per TMEM column
+      uint32_t pw[2][32];
+      float ls = 0.f;
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const float p0 = exp2f(__uint_as_float(sv[c][2 * e]) - m);
+          const float p1 = exp2f(__uint_as_float(sv[c][2 * e + 1]) - m);
+          ls += p0 + p1;
+          pw[c >> 1][(c & 1) * 16 + e] = pack2<T>(p0, p1);
+        }
+      l += ls;
+      if (j >= 2) {  // P buffer j & 1 was last read by PV(j - 2)
+        ok = __all_sync(0xffffffffu, wait(o_done + 8 * (j & 1), ((j - 2) >> 1) & 1, 900 + j));
+        if (!ok) break;
+        tc_fence_after();
+      }
+      tmem_st32(lane_addr + UM_P_COL + (j & 1) * 64, pw[0]);
+      tmem_st32(lane_addr + UM_P_COL + (j & 1) * 64 + 32, pw[1]);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(p_full + 8 * (j & 1));
+    }
+    if (ok) ok = __all_sync(0xffffffffu, wait(o_done + 8 * ((nt - 1) & 1), ((nt - 1) >> 1) & 1, 1000));
+    if (ok) {
+      tc_fence_after();
+      const float inv = 1.f / l;
+      T* out = static_cast<T*>(a.out) + (static_cast<int64_t>(qbeg + qi) * a.H_q + g * G + h) * D;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+        tmem_ld32(lane_addr + UM_O_COL + 32 * c, o);
+        tmem_ld_wait();
+        if (valid) {
+          uint4* dst = reinterpret_cast<uint4*>(out + 32 * c);
+#pragma unroll
+          for (int v = 0; v < 4; ++v)
+            dst[v] = make_uint4(pack2<T>(__uint_as_float(o[8 * v]) * inv, __uint_as_float(o[8 * v + 1]) * inv),
+                                pack2<T>(__uint_as_float(o[8 * v + 2]) * inv, __uint_as_float(o[8 * v + 3]) * inv),
+                                pack2<T>(__uint_as_float(o[8 * v + 4]) * inv, __uint_as_float(o[8 * v + 5]) * inv),
+                                pack2<T>(__uint_as_float(o[8 * v + 6]) * inv, __uint_as_float(o[8 * v + 7]) * inv));
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 4) tmem_dealloc(tmem, 512);
+}
+
 // Chunked prefill on CUDA cores: one CTA per (query row, KV head).  The row's
 // sequence s is found in q_off; its position is len_s - C_s + (row - q_off[s]) and it
 // attends to every token up to and including that position.
@@ -332,6 +652,35 @@ int launch_prefill(Pool& P, int32_t layer, const void* q, const int32_t* q_off, 
   const int64_t rows = g.num_blocks * g.L * g.H_kv * g.block_size;
   const bool tc = (g.dtype == PKV_BF16 || g.dtype == PKV_F16) && (g.d_head == 64 || g.d_head == 128) &&
                   G <= PF_ROWS && g.block_size % TILE == 0 && rows < (int64_t(1) << 31) && encode_fn() != nullptr;
+  static const bool force_mma_sync = std::getenv("PKV_PREFILL_MMA_SYNC") != nullptr;
+  if (tc && g.d_head == 128 && !force_mma_sync) {
+    if ((reinterpret_cast<uintptr_t>(q) & 15) || (reinterpret_cast<uintptr_t>(out) & 15))
+      return fail(PKV_ERR_INVALID_ARG, "q and out must be 16-byte aligned");
+    CUtensorMap maps[3];
+    if (int rc = get_tensor_maps(P, k_pool, v_pool, &maps[1], &maps[2])) return rc;
+    // q as {d, H_q, n_tok}: a box of {64, G, 128 / G} lands as 128 (query, head) rows of 128 bytes
+    const int QB = 128 / G;
+    const CUtensorMapDataType dt = g.dtype == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    cuuint64_t dims[3] = {128, static_cast<cuuint64_t>(g.H_q), static_cast<cuuint64_t>(std::max(n_tok, 1))};
+    cuuint64_t strides[2] = {256, static_cast<cuuint64_t>(g.H_q) * 256};
+    cuuint32_t box[3] = {64, static_cast<cuuint32_t>(G), static_cast<cuuint32_t>(QB)};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = encode_fn()(&maps[0], dt, 3, const_cast<void*>(q), dims, strides, box, estr,
+                             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled (q) failed: " + std::to_string(r));
+    const bool bf = g.dtype == PKV_BF16;
+    const void* k = bf ? reinterpret_cast<const void*>(&prefill_umma_kernel<__nv_bfloat16>)
+                       : reinterpret_cast<const void*>(&prefill_umma_kernel<__half>);
+    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, UM_SMEM);
+    if (e != cudaSuccess) return fail(PKV_ERR_CUDA, std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e));
+    dim3 grid((max_q + QB - 1) / QB, g.H_kv, n_seq);
+    void* args[] = {&maps[0], &maps[1], &maps[2], &a, const_cast<int32_t**>(&q_off)};
+    e = cudaLaunchKernel(k, grid, dim3(UM_THREADS), args, UM_SMEM, st);
+    if (e != cudaSuccess) return fail(PKV_ERR_CUDA, std::string("prefill launch: ") + cudaGetErrorString(e));
+    count_launch();
+    return PKV_OK;
+  }
   if (!tc && G > GPAD) return fail(PKV_ERR_UNSUPPORTED, "more than 8 query heads per KV head on the CUDA-core path");
   if (tc) {
     if ((reinterpret_cast<uintptr_t>(q) & 15) || (reinterpret_cast<uintptr_t>(out) & 15))
