@@ -830,7 +830,7 @@ def run_prefill(args, torch, pkv, dev, world, rank):
     Each step forks the 8 histories (no data moves), plans and writes the chunks'
     keys/values, and runs chunked-prefill attention (history in full, causal within
     the chunk)."""
-    n, hist, C = 8, 16384, 512
+    n, hist, C = 8, args.context or 16384, 512
     seed = W.SEEDS["agent32k"] + 11
     total = args.warmup + args.steps
     N = n * hist // 16 + total * n * (C // 16) + 64
@@ -900,13 +900,16 @@ def run_prefill(args, torch, pkv, dev, world, rank):
         "metric": METRIC, "value": round(flop / (ms / 1e3) / 1e12, 2), "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": "prefill: 8 sequences x 16,384 cached tokens, a 512-token chunk each (forked "
+        "config": {"workload": f"prefill: {n} sequences x {hist:,} cached tokens, a {C}-token chunk each (forked "
                                "histories), 64 query / 8 KV heads, d_head 128, bf16, 16-token blocks",
-                   "l2": "inputs larger than L2 (1.1 GB of K/V per step)", "parallelism": "replicas (no collectives)"},
+                   "l2": f"inputs larger than L2 ({kvb / 1e9:.2f} GB of K/V per step)",
+                   "parallelism": "replicas (no collectives)"},
         "tokens_per_s": round(n * C / (ms / 1e3), 1),
         "roofline": {"bound": "tensor", "achieved": round(tflops, 1), "peak": peak, "unit": "TFLOP/s",
                      "frac": round(tflops / peak, 4), "traffic": None,
-                     "kernel": "pkv_prefill_attention (mma.sync m16n8k16)", "avg_launch_ms": round(att, 4),
+                     "kernel": "pkv_prefill_attention (" + ("mma.sync m16n8k16" if os.environ.get("PKV_PREFILL_MMA_SYNC")
+                                                           else "tcgen05.mma kind::f16, TMEM accumulators") + ")",
+                     "avg_launch_ms": round(att, 4),
                      "kv_bytes_per_launch": kvb},
         "e2e": {"value": round(flop / (ms / 1e3) / 1e12, 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": int(n * Wd * 4 + n * C * 4), "d2h_bytes_per_step": 0},

@@ -296,16 +296,17 @@ __global__ void __launch_bounds__(PF_WARPS * 32, 1) prefill_tc_kernel(const __gr
 constexpr int UM_KEYS = 128;
 constexpr int UM_SLABS = UM_KEYS / TILE;
 constexpr int UM_KS = 3, UM_VS = 2;
-constexpr int UM_THREADS = 192;
+constexpr int UM_THREADS = 224;
 constexpr int UM_TILE_BYTES = 128 * 128 * 2;  // Q, or one K or V tile (128 rows x d 128, 16-bit)
 constexpr int UM_BARS = 1 + 2 * UM_KS + 2 * UM_VS + 2 + 2 + 2 + 1;
-constexpr int UM_SMEM = 1024 + (1 + UM_KS + UM_VS) * UM_TILE_BYTES + UM_BARS * 8 + 16;
+constexpr int UM_TBL = 4096;  // block-table entries staged in shared memory (65,536 tokens at B = 16)
+constexpr int UM_SMEM = 1024 + (1 + UM_KS + UM_VS) * UM_TILE_BYTES + UM_BARS * 8 + 16 + UM_TBL * 4;
 constexpr uint32_t UM_S_COL = 0, UM_P_COL = 256, UM_O_COL = 384;
 
 template <typename T>
 __global__ void __launch_bounds__(UM_THREADS, 1) prefill_umma_kernel(const __grid_constant__ CUtensorMap tmq,
                                                                       const __grid_constant__ CUtensorMap tmk,
-                                                                      const __grid_constant__ CUtensorMap tmv,
+                                                                      const __grid_constant__ CUtensorMap tmv3,
                                                                       const DecodeArgs a, const int32_t* q_off) {
   constexpr int D = 128;
   constexpr bool BF16 = std::is_same<T, __nv_bfloat16>::value;
@@ -342,6 +343,9 @@ __global__ void __launch_bounds__(UM_THREADS, 1) prefill_umma_kernel(const __gri
   const uint32_t s_full = v_empty + 8 * UM_VS, p_full = s_full + 16, o_done = p_full + 16, vz = o_done + 16;
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bar_p + UM_BARS * 8);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bar_p + UM_BARS * 8 + 4);
+  int32_t* tbl = reinterpret_cast<int32_t*>(bar_p + UM_BARS * 8 + 16);
+  const int nblk = (nkeys + a.B - 1) / a.B;
+  const bool tbl_in_smem = nblk <= UM_TBL;
 
   if (tid == 0) {
     mbar_init(q_full, 1);
@@ -383,24 +387,33 @@ __global__ void __launch_bounds__(UM_THREADS, 1) prefill_umma_kernel(const __gri
     }
   };
 
-  if (warp == 4) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
+  if (warp == 4 || warp == 6) {
+    // ------------------------------------------------------------ producers: warp 4 K (and Q), warp 6 V
+    const bool kw = warp == 4;
+    if (kw && lane == 0) {
       fence_proxy_async();
       mbar_arrive_expect_tx(q_full, 2 * 64 * G * QB * 2);
       tma_load_3d(qs, &tmq, 0, g * G, qbeg + i0, q_full);
       tma_load_3d(qs + 16384, &tmq, 64, g * G, qbeg + i0, q_full);
     }
-    auto load = [&](int j, bool is_k) -> bool {  // whole warp; lane 0 issues
+    auto block_at = [&](int lb) -> int {
+      int blk = a.tables[static_cast<int64_t>(s) * a.W + lb];
+      if (blk < 0 || blk >= a.num_blocks) {
+        record_error(a.err, DERR_DECODE_BLOCK, blk);
+        blk = 0;
+      }
+      return blk;
+    };
+    if (tbl_in_smem) {  // the sequence's table slice, once
+      for (int k = lane; k < nblk; k += 32) tbl[k] = block_at(k);
+      __syncwarp();
+    }
+    auto load = [&](int j, bool is_k) -> bool {  // whole warp: lane i < 8 issues slab i
       int row = 0;
       const int t0 = j * UM_KEYS + lane * TILE;
       if (lane < UM_SLABS && t0 < nkeys) {
         const int lb = t0 / a.B;
-        int blk = a.tables[static_cast<int64_t>(s) * a.W + lb];
-        if (blk < 0 || blk >= a.num_blocks) {
-          record_error(a.err, DERR_DECODE_BLOCK, blk);
-          blk = 0;
-        }
+        const int blk = tbl_in_smem ? tbl[lb] : block_at(lb);
         row = ((blk * a.L + a.layer) * a.H_kv + g) * a.B + (t0 - lb * a.B);
       }
       const int nv = min(UM_SLABS, (nkeys - j * UM_KEYS + TILE - 1) / TILE);
@@ -414,25 +427,25 @@ __global__ void __launch_bounds__(UM_THREADS, 1) prefill_umma_kernel(const __gri
           mbar_arrive_expect_tx(full, nv * 2 * TILE * 128);
         }
       }
-      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;  // also orders the expect_tx before the copies
       if (!ok) return false;
       const int slot = is_k ? j % UM_KS : j % UM_VS;
       const uint32_t dst = (is_k ? ks0 : vs0) + slot * UM_TILE_BYTES;
       const uint32_t full = (is_k ? k_full : v_full) + 8 * slot;
-      for (int i = 0; i < nv; ++i) {
-        const int r = __shfl_sync(0xffffffffu, row, i);
-        if (lane == 0) {
-          tma_load_2d(dst + i * TILE * 128, is_k ? &tmk : &tmv, 0, r, full);
-          tma_load_2d(dst + 16384 + i * TILE * 128, is_k ? &tmk : &tmv, 64, r, full);
+      if (lane < nv) {
+        if (is_k) {  // K slab i: two 2 KB boxes, one per d chunk ([chunk][128 keys][128 B])
+          tma_load_2d(dst + lane * TILE * 128, &tmk, 0, row, full);
+          tma_load_2d(dst + 16384 + lane * TILE * 128, &tmk, 64, row, full);
+        } else {  // V slab i: one 4 KB box of both d chunks ([slab][chunk][16 keys][128 B])
+          tma_load_3d(dst + lane * 2 * TILE * 128, &tmv3, 0, row, 0, full);
         }
       }
       return true;
     };
-    bool ok = load(0, true);
+    bool ok = true;
     for (int j = 0; j < nt && ok; ++j) {
-      if (j + 1 < nt) ok = load(j + 1, true);
-      if (ok) ok = load(j, false);
-      if (ok && tail && j == nt - 1) {
+      ok = load(j, kw);
+      if (!kw && ok && tail && j == nt - 1) {
         // zero the V rows past the sequence end once the tile has landed
         const int slot = j % UM_VS;
         bool landed = true;
@@ -443,7 +456,8 @@ __global__ void __launch_bounds__(UM_THREADS, 1) prefill_umma_kernel(const __gri
           const int r0 = nkeys - j * UM_KEYS;
           for (int k = lane; k < (UM_KEYS - r0) * 16; k += 32) {  // 16-byte pieces, both d chunks
             const int r = r0 + k / 16, c = k % 16;
-            *reinterpret_cast<int4*>(vt + (c / 8) * 16384 + r * 128 + (c % 8) * 16) = make_int4(0, 0, 0, 0);
+            *reinterpret_cast<int4*>(vt + (r / TILE) * 4096 + (c / 8) * 2048 + (r % TILE) * 128 + (c % 8) * 16) =
+                make_int4(0, 0, 0, 0);
           }
           fence_proxy_async();
           __syncwarp();
@@ -485,7 +499,7 @@ __global__ void __launch_bounds__(UM_THREADS, 1) prefill_umma_kernel(const __gri
 #pragma unroll
         for (int k = 0; k < UM_KEYS / 16; ++k)
           umma_ts(tmem + UM_O_COL, tmem + UM_P_COL + (j & 1) * 64 + 8 * k,
-                  umma_desc_sw128(vb + k * 16 * 128, 16384, 1024), idesc_o, (j > 0 || k > 0) ? 1u : 0u);
+                  umma_desc_sw128(vb + k * 4096, 2048, 1024), idesc_o, (j > 0 || k > 0) ? 1u : 0u);
         umma_commit(o_done + 8 * (j & 1));
         umma_commit(v_empty + 8 * vslot);
         if (j + 2 < nt) ok = qk(j + 2);
@@ -510,24 +524,33 @@ __global__ void __launch_bounds__(UM_THREADS, 1) prefill_umma_kernel(const __gri
       for (int c = 0; c < 4; ++c) tmem_ld32(lane_addr + UM_S_COL + (j & 1) * 128 + 32 * c, sv[c]);
       tmem_ld_wait();
       const int k0 = j * UM_KEYS;
-      float mx = -INFINITY;
+      // mask only tiles where some row of the warp meets the causal edge or the sequence end
+      if (__any_sync(0xffffffffu, k0 + UM_KEYS - 1 > lim)) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (k0 + 32 * c + e > lim) sv[c][e] = __float_as_uint(-INFINITY);
+      }
+      // row max on the raw scores (the scale is positive), 8 independent chains
+      float mx8[8];
+#pragma unroll
+      for (int t = 0; t < 8; ++t) mx8[t] = -INFINITY;
 #pragma unroll
       for (int c = 0; c < 4; ++c)
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          float x = __uint_as_float(sv[c][e]) * a.scale_log2;
-          if (k0 + 32 * c + e > lim) x = -INFINITY;
-          sv[c][e] = __float_as_uint(x);
-          mx = fmaxf(mx, x);
-        }
-      const float m_new = fmaxf(m, mx);
+        for (int e = 0; e < 32; ++e) mx8[e & 7] = fmaxf(mx8[e & 7], __uint_as_float(sv[c][e]));
+      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      const float sl = a.scale_log2;
+      const float m_new = fmaxf(m, mx * sl);
       if (__any_sync(0xffffffffu, m_new > m + 8.f)) {  // the reference max moves: rescale l and O so far
-        const float alpha = exp2f(m - m_new);
+        const float alpha = fast_exp2(m - m_new);
         if (j > 0) {
           ok = __all_sync(0xffffffffu, wait(o_done + 8 * ((j - 1) & 1), ((j - 1) >> 1) & 1, 800 + j));
           if (!ok) break;
           tc_fence_after();
-#pragma unroll
+#pragma unroll 1
           for (int c = 0; c < D / 32; ++c) {
             uint32_t o[32];
             tmem_ld32(lane_addr + UM_O_COL + 32 * c, o);
@@ -540,19 +563,22 @@ __global__ void __launch_bounds__(UM_THREADS, 1) prefill_umma_kernel(const __gri
         l *= alpha;
         m = m_new;
       }
-      // P = 2^(x - m), 16-bit, two keys per TMEM column
+      // P = 2^(scale * s - m), 16-bit, two keys per TMEM column; 8 partial sums
+      const float neg_m = -m;
       uint32_t pw[2][32];
-      float ls = 0.f;
+      float ls8[8];
+#pragma unroll
+      for (int t = 0; t < 8; ++t) ls8[t] = 0.f;
 #pragma unroll
       for (int c = 0; c < 4; ++c)
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          const float p0 = exp2f(__uint_as_float(sv[c][2 * e]) - m);
-          const float p1 = exp2f(__uint_as_float(sv[c][2 * e + 1]) - m);
-          ls += p0 + p1;
+          const float p0 = fast_exp2(fmaf(__uint_as_float(sv[c][2 * e]), sl, neg_m));
+          const float p1 = fast_exp2(fmaf(__uint_as_float(sv[c][2 * e + 1]), sl, neg_m));
+          ls8[e & 7] += p0 + p1;
           pw[c >> 1][(c & 1) * 16 + e] = pack2<T>(p0, p1);
         }
-      l += ls;
+      l += ((ls8[0] + ls8[1]) + (ls8[2] + ls8[3])) + ((ls8[4] + ls8[5]) + (ls8[6] + ls8[7]));
       if (j >= 2) {  // P buffer j & 1 was last read by PV(j - 2)
         ok = __all_sync(0xffffffffu, wait(o_done + 8 * (j & 1), ((j - 2) >> 1) & 1, 900 + j));
         if (!ok) break;
@@ -658,6 +684,19 @@ int launch_prefill(Pool& P, int32_t layer, const void* q, const int32_t* q_off, 
       return fail(PKV_ERR_INVALID_ARG, "q and out must be 16-byte aligned");
     CUtensorMap maps[3];
     if (int rc = get_tensor_maps(P, k_pool, v_pool, &maps[1], &maps[2])) return rc;
+    // V as {64, rows, 2 d chunks}: a {64, 16, 2} box is one 16-token slab, both chunks, 4 KB
+    {
+      cuuint64_t vd[3] = {64, static_cast<cuuint64_t>(g.num_blocks) * g.L * g.H_kv * g.block_size, 2};
+      cuuint64_t vs[2] = {256, 128};
+      cuuint32_t vb[3] = {64, TILE, 2};
+      cuuint32_t ve[3] = {1, 1, 1};
+      const CUtensorMapDataType vt =
+          g.dtype == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+      CUresult r = encode_fn()(&maps[2], vt, 3, const_cast<void*>(v_pool), vd, vs, vb, ve, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+      if (r != CUDA_SUCCESS) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled (v slabs) failed: " + std::to_string(r));
+    }
     // q as {d, H_q, n_tok}: a box of {64, G, 128 / G} lands as 128 (query, head) rows of 128 bytes
     const int QB = 128 / G;
     const CUtensorMapDataType dt = g.dtype == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
