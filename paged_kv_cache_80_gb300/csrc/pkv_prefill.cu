@@ -288,7 +288,10 @@ __global__ void __launch_bounds__(PF_WARPS * 32, 1) prefill_tc_kernel(const __gr
 //     swizzle, M = 128, N = 128, 8 x K = 16) into one of two S buffers, and O += P V with P
 //     read from TMEM and V as an MN-major operand (N = d).  QK^T of tile j + 1 runs on the
 //     tensor cores while the softmax of tile j runs.
-// TMEM (512 columns): S0 [0, 128), S1 [128, 256), P0 [256, 320), P1 [320, 384), O [384, 512).
+// TMEM (512 columns): S0 [0, 128), S1 [128, 256), S2 [256, 384), O [384, 512); the softmax
+// writes P (16-bit pairs) over the first 64 columns of the S buffer it read, and QK^T runs two
+// tiles ahead (S(j + 2) goes into the buffer of P(j - 1) once PV(j - 1) is complete), so the
+// softmax never waits for the tensor cores.
 // The online softmax ("Chunked prefill mechanics": m_new = max(m, m_blk), l and O scaled by
 // e^{m - m_new}) rescales O in TMEM only when a row's max grows by more than 2^8; otherwise
 // the old max stays the reference, which is exact because P and l use the same reference.
@@ -296,12 +299,12 @@ __global__ void __launch_bounds__(PF_WARPS * 32, 1) prefill_tc_kernel(const __gr
 constexpr int UM_KEYS = 128;
 constexpr int UM_SLABS = UM_KEYS / TILE;
 constexpr int UM_KS = 3, UM_VS = 2;
-constexpr int UM_THREADS = 224;
+constexpr int UM_THREADS = 256;  // softmax x 4, K producer, PV issuer, V producer, QK issuer
 constexpr int UM_TILE_BYTES = 128 * 128 * 2;  // Q, or one K or V tile (128 rows x d 128, 16-bit)
-constexpr int UM_BARS = 1 + 2 * UM_KS + 2 * UM_VS + 2 + 2 + 2 + 1;
+constexpr int UM_BARS = 1 + 2 * UM_KS + 2 * UM_VS + 3 + 3 + 3 + 1 + 2;
 constexpr int UM_TBL = 4096;  // block-table entries staged in shared memory (65,536 tokens at B = 16)
 constexpr int UM_SMEM = 1024 + (1 + UM_KS + UM_VS) * UM_TILE_BYTES + UM_BARS * 8 + 16 + UM_TBL * 4;
-constexpr uint32_t UM_S_COL = 0, UM_P_COL = 256, UM_O_COL = 384;
+constexpr uint32_t UM_O_COL = 384;
 
 template <typename T>
 __global__ void __launch_bounds__(UM_THREADS, 1) prefill_umma_kernel(const __grid_constant__ CUtensorMap tmq,
@@ -340,7 +343,8 @@ __global__ void __launch_bounds__(UM_THREADS, 1) prefill_umma_kernel(const __gri
   const uint32_t q_full = bars;
   const uint32_t k_full = bars + 8, k_empty = k_full + 8 * UM_KS;
   const uint32_t v_full = k_empty + 8 * UM_KS, v_empty = v_full + 8 * UM_VS;
-  const uint32_t s_full = v_empty + 8 * UM_VS, p_full = s_full + 16, o_done = p_full + 16, vz = o_done + 16;
+  const uint32_t s_full = v_empty + 8 * UM_VS, p_full = s_full + 24, o_done = p_full + 24, vz = o_done + 24;
+  const uint32_t drain = vz + 8;  // two barriers: the issuers' last commits after an abort
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bar_p + UM_BARS * 8);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bar_p + UM_BARS * 8 + 4);
   int32_t* tbl = reinterpret_cast<int32_t*>(bar_p + UM_BARS * 8 + 16);
@@ -357,12 +361,14 @@ __global__ void __launch_bounds__(UM_THREADS, 1) prefill_umma_kernel(const __gri
       mbar_init(v_full + 8 * k, 1);
       mbar_init(v_empty + 8 * k, 1);
     }
-    for (int k = 0; k < 2; ++k) {
+    for (int k = 0; k < 3; ++k) {
       mbar_init(s_full + 8 * k, 1);
       mbar_init(p_full + 8 * k, 128);
       mbar_init(o_done + 8 * k, 1);
     }
     mbar_init(vz, 1);
+    mbar_init(drain, 1);
+    mbar_init(drain + 8, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -374,6 +380,7 @@ __global__ void __launch_bounds__(UM_THREADS, 1) prefill_umma_kernel(const __gri
 
   // bounded wait that also gives up once another role has given up
   auto wait = [&](uint32_t bar, uint32_t parity, int where) -> bool {
+    if (mbar_try_wait(bar, parity)) return true;  // fast path: no timer read
     const uint64_t t0 = global_ns();
     for (;;) {
       for (int k = 0; k < 32; ++k)
@@ -384,6 +391,12 @@ __global__ void __launch_bounds__(UM_THREADS, 1) prefill_umma_kernel(const __gri
         record_error(a.err, DERR_DECODE_TIMEOUT, where);
         return false;
       }
+    }
+  };
+  // after an abort: bounded wait for work this thread already started (copies or MMAs)
+  auto settle = [&](uint32_t bar, uint32_t parity) {
+    const uint64_t t0 = global_ns();
+    while (!mbar_try_wait(bar, parity) && global_ns() - t0 < kWaitNs) {
     }
   };
 
@@ -443,8 +456,10 @@ __global__ void __launch_bounds__(UM_THREADS, 1) prefill_umma_kernel(const __gri
       return true;
     };
     bool ok = true;
+    int issued = 0;
     for (int j = 0; j < nt && ok; ++j) {
       ok = load(j, kw);
+      issued += ok ? 1 : 0;
       if (!kw && ok && tail && j == nt - 1) {
         // zero the V rows past the sequence end once the tile has landed
         const int slot = j % UM_VS;
@@ -465,44 +480,61 @@ __global__ void __launch_bounds__(UM_THREADS, 1) prefill_umma_kernel(const __gri
         }
       }
     }
-  } else if (warp == 5) {
-    // ------------------------------------------------------------ MMA issuer
+    if (*abort_flag && lane == 0) {  // the last ring's copies may still be landing
+      const int depth = kw ? UM_KS : UM_VS;
+      for (int jj = max(0, issued - depth); jj < issued; ++jj)
+        settle((kw ? k_full : v_full) + 8 * (jj % depth), (jj / depth) & 1);
+    }
+  } else if (warp == 7) {
+    // ------------------------------------------------------------ QK^T issuer (up to three S buffers ahead)
     if (lane == 0) {
       const uint32_t idesc_s = umma_idesc_f16(BF16, 128, UM_KEYS, false);
-      const uint32_t idesc_o = umma_idesc_f16(BF16, 128, D, true);
       bool ok = wait(q_full, 0, 1);
-      auto qk = [&](int j) -> bool {
+      for (int j = 0; j < nt && ok; ++j) {
+        // buffer j % 3 held P(j - 3): its PV must be complete
+        if (j >= 3) ok = wait(o_done + 8 * ((j - 3) % 3), ((j - 3) / 3) & 1, 450 + j);
         const int slot = j % UM_KS;
-        if (!wait(k_full + 8 * slot, (j / UM_KS) & 1, 300 + j)) return false;
+        if (ok) ok = wait(k_full + 8 * slot, (j / UM_KS) & 1, 300 + j);
+        if (!ok) break;
         tc_fence_after();
         const uint32_t kb = ks0 + slot * UM_TILE_BYTES;
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
-          umma_ss(tmem + UM_S_COL + (j & 1) * 128, umma_desc_sw128(qs + off, 16, 1024),
-                  umma_desc_sw128(kb + off, 16, 1024), idesc_s, k > 0);
+          umma_ss(tmem + (j % 3) * 128, umma_desc_sw128(qs + off, 16, 1024), umma_desc_sw128(kb + off, 16, 1024),
+                  idesc_s, k > 0);
         }
-        umma_commit(s_full + 8 * (j & 1));
+        umma_commit(s_full + 8 * (j % 3));
         umma_commit(k_empty + 8 * slot);
-        return true;
-      };
-      if (ok) ok = qk(0);
-      if (ok && nt > 1) ok = qk(1);
+      }
+      if (*abort_flag) {
+        umma_commit(drain);
+        settle(drain, 0);
+      }
+    }
+  } else if (warp == 5) {
+    // ------------------------------------------------------------ PV issuer
+    if (lane == 0) {
+      const uint32_t idesc_o = umma_idesc_f16(BF16, 128, D, true);
+      bool ok = true;
       for (int j = 0; j < nt && ok; ++j) {
-        ok = wait(p_full + 8 * (j & 1), (j >> 1) & 1, 400 + j);
         const int vslot = j % UM_VS;
-        if (ok) ok = wait(v_full + 8 * vslot, (j / UM_VS) & 1, 500 + j);
+        ok = wait(v_full + 8 * vslot, (j / UM_VS) & 1, 500 + j);
         if (ok && tail && j == nt - 1) ok = wait(vz, 0, 600);
+        if (ok) ok = wait(p_full + 8 * (j % 3), (j / 3) & 1, 400 + j);
         if (!ok) break;
         tc_fence_after();
         const uint32_t vb = vs0 + vslot * UM_TILE_BYTES;
 #pragma unroll
         for (int k = 0; k < UM_KEYS / 16; ++k)
-          umma_ts(tmem + UM_O_COL, tmem + UM_P_COL + (j & 1) * 64 + 8 * k,
-                  umma_desc_sw128(vb + k * 4096, 2048, 1024), idesc_o, (j > 0 || k > 0) ? 1u : 0u);
-        umma_commit(o_done + 8 * (j & 1));
+          umma_ts(tmem + UM_O_COL, tmem + (j % 3) * 128 + 8 * k, umma_desc_sw128(vb + k * 4096, 2048, 1024), idesc_o,
+                  (j > 0 || k > 0) ? 1u : 0u);
+        umma_commit(o_done + 8 * (j % 3));
         umma_commit(v_empty + 8 * vslot);
-        if (j + 2 < nt) ok = qk(j + 2);
+      }
+      if (*abort_flag) {
+        umma_commit(drain + 8);
+        settle(drain + 8, 0);
       }
     }
   } else {
@@ -516,12 +548,13 @@ __global__ void __launch_bounds__(UM_THREADS, 1) prefill_umma_kernel(const __gri
     bool ok = true;
     // tcgen05.ld / st are warp-collective: every decision below is uniform over the warp
     for (int j = 0; j < nt && ok; ++j) {
-      ok = __all_sync(0xffffffffu, wait(s_full + 8 * (j & 1), (j >> 1) & 1, 700 + j));
+      ok = __all_sync(0xffffffffu, wait(s_full + 8 * (j % 3), (j / 3) & 1, 700 + j));
       if (!ok) break;
       tc_fence_after();
+      const uint32_t s_addr = lane_addr + (j % 3) * 128;
       uint32_t sv[4][32];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(lane_addr + UM_S_COL + (j & 1) * 128 + 32 * c, sv[c]);
+      for (int c = 0; c < 4; ++c) tmem_ld32(s_addr + 32 * c, sv[c]);
       tmem_ld_wait();
       const int k0 = j * UM_KEYS;
       // mask only tiles where some row of the warp meets the causal edge or the sequence end
@@ -547,7 +580,7 @@ __global__ void __launch_bounds__(UM_THREADS, 1) prefill_umma_kernel(const __gri
       if (__any_sync(0xffffffffu, m_new > m + 8.f)) {  // the reference max moves: rescale l and O so far
         const float alpha = fast_exp2(m - m_new);
         if (j > 0) {
-          ok = __all_sync(0xffffffffu, wait(o_done + 8 * ((j - 1) & 1), ((j - 1) >> 1) & 1, 800 + j));
+          ok = __all_sync(0xffffffffu, wait(o_done + 8 * ((j - 1) % 3), ((j - 1) / 3) & 1, 800 + j));
           if (!ok) break;
           tc_fence_after();
 #pragma unroll 1
@@ -579,18 +612,14 @@ __global__ void __launch_bounds__(UM_THREADS, 1) prefill_umma_kernel(const __gri
           pw[c >> 1][(c & 1) * 16 + e] = pack2<T>(p0, p1);
         }
       l += ((ls8[0] + ls8[1]) + (ls8[2] + ls8[3])) + ((ls8[4] + ls8[5]) + (ls8[6] + ls8[7]));
-      if (j >= 2) {  // P buffer j & 1 was last read by PV(j - 2)
-        ok = __all_sync(0xffffffffu, wait(o_done + 8 * (j & 1), ((j - 2) >> 1) & 1, 900 + j));
-        if (!ok) break;
-        tc_fence_after();
-      }
-      tmem_st32(lane_addr + UM_P_COL + (j & 1) * 64, pw[0]);
-      tmem_st32(lane_addr + UM_P_COL + (j & 1) * 64 + 32, pw[1]);
+      // P over the S buffer just read (this lane's row only: its S is in registers)
+      tmem_st32(s_addr, pw[0]);
+      tmem_st32(s_addr + 32, pw[1]);
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(p_full + 8 * (j & 1));
+      mbar_arrive(p_full + 8 * (j % 3));
     }
-    if (ok) ok = __all_sync(0xffffffffu, wait(o_done + 8 * ((nt - 1) & 1), ((nt - 1) >> 1) & 1, 1000));
+    if (ok) ok = __all_sync(0xffffffffu, wait(o_done + 8 * ((nt - 1) % 3), ((nt - 1) / 3) & 1, 1000));
     if (ok) {
       tc_fence_after();
       const float inv = 1.f / l;
