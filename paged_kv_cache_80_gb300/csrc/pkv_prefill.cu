@@ -274,37 +274,64 @@ __global__ void __launch_bounds__(PF_WARPS * 32, 1) prefill_tc_kernel(const __gr
 
 // --------------------------------------------------------------------------- chunked prefill (tcgen05)
 //
-// Same work split (one CTA per (query block, KV head, sequence), M = 128 (query, head)
-// rows, row r = query r / G, head r % G), on the 5th-generation tensor cores:
-//   * warps 0-3 (softmax): one thread per row, which is also its TMEM lane; reads S with
-//     tcgen05.ld, keeps the row's running max m and sum l, writes P (16-bit) back to TMEM,
-//     and at the end reads O, divides by l and stores the row;
-//   * warp 4 (producer, TMEM owner): TMA loads of Q (two 3-D boxes whose rows land as
-//     (query, head)) and of 128-key K and V tiles (8 slabs of 16 tokens, each from its own
-//     pool block) into rings of 3 (K) and 2 (V) 32 KB slots, slab i at 2 KB stride so the
-//     8-row groups are uniformly 1 KB apart; it zeroes the V rows past the sequence end in
-//     the last tile so that P = 0 never meets a non-finite value;
-//   * warp 5 (one thread): S = Q K^T (tcgen05.mma kind::f16, both K-major, 128-byte
-//     swizzle, M = 128, N = 128, 8 x K = 16) into one of two S buffers, and O += P V with P
-//     read from TMEM and V as an MN-major operand (N = d).  QK^T of tile j + 1 runs on the
-//     tensor cores while the softmax of tile j runs.
-// TMEM (512 columns): S0 [0, 128), S1 [128, 256), S2 [256, 384), O [384, 512); the softmax
-// writes P (16-bit pairs) over the first 64 columns of the S buffer it read, and QK^T runs two
-// tiles ahead (S(j + 2) goes into the buffer of P(j - 1) once PV(j - 1) is complete), so the
-// softmax never waits for the tensor cores.
+// One CTA per (pair of query blocks, KV head, sequence).  Its rows are two M = 128 tiles of
+// (query, head) pairs, A and B (row r = query r / G, head r % G; B holds the 128 / G queries
+// after A's), and both tiles use every K and V tile the CTA loads: against one tile per CTA
+// this halves the L2-to-SM bytes and the TMA copies per multiply-add, and it gives the tensor
+// cores a second chain of products to run while one tile's softmax is on the CUDA cores.
+//   * warps 0-3 (softmax of A) and 4-7 (softmax of B): one thread per row, which is also its
+//     TMEM lane; reads S with tcgen05.ld, keeps the row's running max m and sum l, writes P
+//     (16-bit) back over S, and at the end reads O, divides by l and stores the row;
+//   * warps 8 and 10 (producers; warp 8 owns TMEM): TMA loads of Q (3-D boxes whose rows land
+//     as (query, head)) and of the 128-key K (warp 8) and V (warp 10) tiles, 8 slabs of 16
+//     tokens, each from its own pool block.  Lane i copies K slab i as two boxes, one per
+//     64-wide d chunk, at 2 KB stride so that the 8-row groups are uniformly 1 KB apart, or V
+//     slab i as one 4 KB box of both chunks.  Warp 10 zeroes the V rows past the sequence end
+//     in the last tile so that P = 0 never meets a non-finite value;
+//   * warps 9 and 11 (one thread each): the tensor-core issuers of A and of B: S = Q K^T
+//     (tcgen05.mma kind::f16, both K-major, 128-byte swizzle, M = 128, N = 128, 8 x K = 16)
+//     and O += P V with P read from TMEM and V as an MN-major operand (N = d).
+// TMEM (512 columns): S_A [0, 128), S_B [128, 256), O_A [256, 384), O_B [384, 512).  The
+// softmax writes P (16-bit pairs) over the first 64 columns of the S it read; S = Q K^T of the
+// next key tile goes into the same columns once P V is complete, so each tile's chain is
+// QK^T -> softmax -> PV.  The two softmaxes take turns (A of key tile j, then B of j, then A
+// of j + 1), so that one tile's products run on the tensor cores while the other tile's
+// exponentials run on the CUDA cores.
 // The online softmax ("Chunked prefill mechanics": m_new = max(m, m_blk), l and O scaled by
 // e^{m - m_new}) rescales O in TMEM only when a row's max grows by more than 2^8; otherwise
 // the old max stays the reference, which is exact because P and l use the same reference.
 
+// mbarrier wait that suspends the thread until the phase completes or `hint_ns` passes, so
+// that waiting warps leave the issue slots of their SM sub-partition to the softmax warps
+__device__ __forceinline__ bool mbar_wait_suspend(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n"
+      ".reg .pred p;\n"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+      "selp.u32 %0, 1, 0, p;\n"
+      "}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 constexpr int UM_KEYS = 128;
 constexpr int UM_SLABS = UM_KEYS / TILE;
-constexpr int UM_KS = 3, UM_VS = 2;
-constexpr int UM_THREADS = 256;  // softmax x 4, K producer, PV issuer, V producer, QK issuer
-constexpr int UM_TILE_BYTES = 128 * 128 * 2;  // Q, or one K or V tile (128 rows x d 128, 16-bit)
-constexpr int UM_BARS = 1 + 2 * UM_KS + 2 * UM_VS + 3 + 3 + 3 + 1 + 2;
+constexpr int UM_KS = 2, UM_VS = 2;  // K and V rings of equal depth (one slot index)
+static_assert(UM_KS == UM_VS, "one slot index serves both rings");
+constexpr int UM_THREADS = 384;  // softmax 2 x 4 warps; K producer, issuer A, V producer, issuer B
+// Registers: launched at 65,536 / 384 = 168 a thread (12 warps, 3 per SM sub-partition); the
+// producer warpgroup gives back down to 56 and the softmax warpgroups take 208:
+// 4 x 32 x 56 + 8 x 32 x 208 = 60,416 <= 384 x 168 = 64,512.
+constexpr int UM_REGS_LOW = 56, UM_REGS_HIGH = 208;
+static_assert(4 * 32 * UM_REGS_LOW + 8 * 32 * UM_REGS_HIGH <= UM_THREADS * 168, "register split");
+constexpr int UM_TILE_BYTES = 128 * 128 * 2;  // one Q, K or V tile (128 rows x d 128, 16-bit)
+// barriers: q; the K and V rings; (S, P, O, turn) per tile; vz; two drains
+constexpr int UM_BARS = 1 + 2 * UM_KS + 2 * UM_VS + 4 * 2 + 1 + 2;
 constexpr int UM_TBL = 4096;  // block-table entries staged in shared memory (65,536 tokens at B = 16)
-constexpr int UM_SMEM = 1024 + (1 + UM_KS + UM_VS) * UM_TILE_BYTES + UM_BARS * 8 + 16 + UM_TBL * 4;
-constexpr uint32_t UM_O_COL = 384;
+constexpr int UM_SMEM = 1024 + (2 + UM_KS + UM_VS) * UM_TILE_BYTES + UM_BARS * 8 + 16 + UM_TBL * 4;
 
 template <typename T>
 __global__ void __launch_bounds__(UM_THREADS, 1) prefill_umma_kernel(const __grid_constant__ CUtensorMap tmq,
@@ -317,18 +344,19 @@ __global__ void __launch_bounds__(UM_THREADS, 1) prefill_umma_kernel(const __gri
   const int qb = blockIdx.x, g = blockIdx.y, s = blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int G = a.G;
-  const int QB = 128 / G;
+  const int QB = 128 / G;  // queries per tile
   const int qbeg = q_off[s];
   const int Cs = q_off[s + 1] - qbeg;
-  const int i0 = qb * QB;
-  if (qb == gridDim.x - 1 && tid == 0 && g == 0 && Cs > i0 + QB) record_error(a.err, DERR_PREFILL_CHUNK, s);
+  const int i0 = qb * 2 * QB;  // first query of tile A
+  if (qb == gridDim.x - 1 && tid == 0 && g == 0 && Cs > i0 + 2 * QB) record_error(a.err, DERR_PREFILL_CHUNK, s);
   if (i0 >= Cs) return;  // uniform over the CTA, before any barrier or TMEM use
   const int len = a.seq_lens[s];
   if (Cs < 0 || len < Cs || len > static_cast<int64_t>(a.W) * a.B) {
     if (tid == 0 && qb == 0 && g == 0) record_error(a.err, DERR_DECODE_LEN, s);
     return;
   }
-  const int i1 = min(Cs, i0 + QB);
+  const int nq = i0 + QB < Cs ? 2 : 1;  // tiles with rows in the chunk
+  const int i1 = min(Cs, i0 + nq * QB);
   const int P = len - Cs;
   const int pmax = P + i1 - 1;
   const int nkeys = pmax + 1;
@@ -337,14 +365,15 @@ __global__ void __launch_bounds__(UM_THREADS, 1) prefill_umma_kernel(const __gri
 
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t qs = smem_u32(base);
-  const uint32_t ks0 = qs + UM_TILE_BYTES, vs0 = ks0 + UM_KS * UM_TILE_BYTES;
-  uint8_t* bar_p = base + (1 + UM_KS + UM_VS) * UM_TILE_BYTES;
+  const uint32_t ks0 = qs + 2 * UM_TILE_BYTES, vs0 = ks0 + UM_KS * UM_TILE_BYTES;
+  uint8_t* bar_p = base + (2 + UM_KS + UM_VS) * UM_TILE_BYTES;
   const uint32_t bars = smem_u32(bar_p);
   const uint32_t q_full = bars;
   const uint32_t k_full = bars + 8, k_empty = k_full + 8 * UM_KS;
   const uint32_t v_full = k_empty + 8 * UM_KS, v_empty = v_full + 8 * UM_VS;
-  const uint32_t s_full = v_empty + 8 * UM_VS, p_full = s_full + 24, o_done = p_full + 24, vz = o_done + 24;
+  const uint32_t s_full = v_empty + 8 * UM_VS, p_full = s_full + 16, o_done = p_full + 16, vz = o_done + 16;
   const uint32_t drain = vz + 8;  // two barriers: the issuers' last commits after an abort
+  const uint32_t turn = drain + 16;  // per tile: its softmax of the current key tile is done
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bar_p + UM_BARS * 8);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bar_p + UM_BARS * 8 + 4);
   int32_t* tbl = reinterpret_cast<int32_t*>(bar_p + UM_BARS * 8 + 16);
@@ -355,24 +384,24 @@ __global__ void __launch_bounds__(UM_THREADS, 1) prefill_umma_kernel(const __gri
     mbar_init(q_full, 1);
     for (int k = 0; k < UM_KS; ++k) {
       mbar_init(k_full + 8 * k, 1);
-      mbar_init(k_empty + 8 * k, 1);
+      mbar_init(k_empty + 8 * k, nq);  // released by every tile's QK^T
     }
     for (int k = 0; k < UM_VS; ++k) {
       mbar_init(v_full + 8 * k, 1);
-      mbar_init(v_empty + 8 * k, 1);
+      mbar_init(v_empty + 8 * k, nq);
     }
-    for (int k = 0; k < 3; ++k) {
-      mbar_init(s_full + 8 * k, 1);
-      mbar_init(p_full + 8 * k, 128);
-      mbar_init(o_done + 8 * k, 1);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(s_full + 8 * x, 1);
+      mbar_init(p_full + 8 * x, 128);
+      mbar_init(o_done + 8 * x, 1);
+      mbar_init(drain + 8 * x, 1);
+      mbar_init(turn + 8 * x, 4);  // one arrival per softmax warp
     }
     mbar_init(vz, 1);
-    mbar_init(drain, 1);
-    mbar_init(drain + 8, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == 4) tmem_alloc(smem_u32(tslot), 512);
+  if (warp == 8) tmem_alloc(smem_u32(tslot), 512);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -383,8 +412,7 @@ __global__ void __launch_bounds__(UM_THREADS, 1) prefill_umma_kernel(const __gri
     if (mbar_try_wait(bar, parity)) return true;  // fast path: no timer read
     const uint64_t t0 = global_ns();
     for (;;) {
-      for (int k = 0; k < 32; ++k)
-        if (mbar_try_wait(bar, parity)) return true;
+      if (mbar_wait_suspend(bar, parity, 20000)) return true;
       if (*abort_flag) return false;
       if (global_ns() - t0 > kWaitNs) {
         *abort_flag = 1;
@@ -400,250 +428,241 @@ __global__ void __launch_bounds__(UM_THREADS, 1) prefill_umma_kernel(const __gri
     }
   };
 
-  if (warp == 4 || warp == 6) {
-    // ------------------------------------------------------------ producers: warp 4 K (and Q), warp 6 V
-    const bool kw = warp == 4;
-    if (kw && lane == 0) {
-      fence_proxy_async();
-      mbar_arrive_expect_tx(q_full, 2 * 64 * G * QB * 2);
-      tma_load_3d(qs, &tmq, 0, g * G, qbeg + i0, q_full);
-      tma_load_3d(qs + 16384, &tmq, 64, g * G, qbeg + i0, q_full);
-    }
-    auto block_at = [&](int lb) -> int {
-      int blk = a.tables[static_cast<int64_t>(s) * a.W + lb];
-      if (blk < 0 || blk >= a.num_blocks) {
-        record_error(a.err, DERR_DECODE_BLOCK, blk);
-        blk = 0;
+  if (warp >= 8) {
+    // each warpgroup sets its register count once, before its warps go their own ways
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(UM_REGS_LOW));
+    if (warp == 8 || warp == 10) {
+      // ------------------------------------------------------------ producers: warp 8 Q and K, warp 10 V
+      const bool kw = warp == 8;
+      if (kw && lane == 0) {
+        fence_proxy_async();
+        mbar_arrive_expect_tx(q_full, nq * 2 * 64 * G * QB * 2);  // G * QB rows per tile (126 for G = 3)
+        for (int x = 0; x < nq; ++x) {
+          tma_load_3d(qs + x * UM_TILE_BYTES, &tmq, 0, g * G, qbeg + i0 + x * QB, q_full);
+          tma_load_3d(qs + x * UM_TILE_BYTES + 16384, &tmq, 64, g * G, qbeg + i0 + x * QB, q_full);
+        }
       }
-      return blk;
-    };
-    if (tbl_in_smem) {  // the sequence's table slice, once
-      for (int k = lane; k < nblk; k += 32) tbl[k] = block_at(k);
-      __syncwarp();
-    }
-    auto load = [&](int j, bool is_k) -> bool {  // whole warp: lane i < 8 issues slab i
-      int row = 0;
-      const int t0 = j * UM_KEYS + lane * TILE;
-      if (lane < UM_SLABS && t0 < nkeys) {
-        const int lb = t0 / a.B;
-        const int blk = tbl_in_smem ? tbl[lb] : block_at(lb);
-        row = ((blk * a.L + a.layer) * a.H_kv + g) * a.B + (t0 - lb * a.B);
+      auto block_at = [&](int lb) -> int {
+        int blk = a.tables[static_cast<int64_t>(s) * a.W + lb];
+        if (blk < 0 || blk >= a.num_blocks) {
+          record_error(a.err, DERR_DECODE_BLOCK, blk);
+          blk = 0;
+        }
+        return blk;
+      };
+      if (tbl_in_smem) {  // the sequence's table slice, once (both warps write the same values)
+        for (int k = lane; k < nblk; k += 32) tbl[k] = block_at(k);
+        __syncwarp();
       }
-      const int nv = min(UM_SLABS, (nkeys - j * UM_KEYS + TILE - 1) / TILE);
+      const uint32_t full0 = kw ? k_full : v_full, empty0 = kw ? k_empty : v_empty;
       bool ok = true;
-      if (lane == 0) {
-        const int slot = is_k ? j % UM_KS : j % UM_VS;
-        const int depth = is_k ? UM_KS : UM_VS;
-        const uint32_t full = (is_k ? k_full : v_full) + 8 * slot, empty = (is_k ? k_empty : v_empty) + 8 * slot;
-        if (j >= depth) ok = wait(empty, ((j / depth) - 1) & 1, 100 + j);
-        if (ok) {
-          mbar_arrive_expect_tx(full, nv * 2 * TILE * 128);
-        }
-      }
-      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;  // also orders the expect_tx before the copies
-      if (!ok) return false;
-      const int slot = is_k ? j % UM_KS : j % UM_VS;
-      const uint32_t dst = (is_k ? ks0 : vs0) + slot * UM_TILE_BYTES;
-      const uint32_t full = (is_k ? k_full : v_full) + 8 * slot;
-      if (lane < nv) {
-        if (is_k) {  // K slab i: two 2 KB boxes, one per d chunk ([chunk][128 keys][128 B])
-          tma_load_2d(dst + lane * TILE * 128, &tmk, 0, row, full);
-          tma_load_2d(dst + 16384 + lane * TILE * 128, &tmk, 64, row, full);
-        } else {  // V slab i: one 4 KB box of both d chunks ([slab][chunk][16 keys][128 B])
-          tma_load_3d(dst + lane * 2 * TILE * 128, &tmv3, 0, row, 0, full);
-        }
-      }
-      return true;
-    };
-    bool ok = true;
-    int issued = 0;
-    for (int j = 0; j < nt && ok; ++j) {
-      ok = load(j, kw);
-      issued += ok ? 1 : 0;
-      if (!kw && ok && tail && j == nt - 1) {
-        // zero the V rows past the sequence end once the tile has landed
-        const int slot = j % UM_VS;
-        bool landed = true;
-        if (lane == 0) landed = wait(v_full + 8 * slot, (j / UM_VS) & 1, 200);
-        landed = __shfl_sync(0xffffffffu, landed ? 1 : 0, 0) != 0;
-        if (landed) {
-          uint8_t* vt = base + (1 + UM_KS + slot) * UM_TILE_BYTES;
-          const int r0 = nkeys - j * UM_KEYS;
-          for (int k = lane; k < (UM_KEYS - r0) * 16; k += 32) {  // 16-byte pieces, both d chunks
-            const int r = r0 + k / 16, c = k % 16;
-            *reinterpret_cast<int4*>(vt + (r / TILE) * 4096 + (c / 8) * 2048 + (r % TILE) * 128 + (c % 8) * 16) =
-                make_int4(0, 0, 0, 0);
-          }
-          fence_proxy_async();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(vz);
-        }
-      }
-    }
-    if (*abort_flag && lane == 0) {  // the last ring's copies may still be landing
-      const int depth = kw ? UM_KS : UM_VS;
-      for (int jj = max(0, issued - depth); jj < issued; ++jj)
-        settle((kw ? k_full : v_full) + 8 * (jj % depth), (jj / depth) & 1);
-    }
-  } else if (warp == 7) {
-    // ------------------------------------------------------------ QK^T issuer (up to three S buffers ahead)
-    if (lane == 0) {
-      const uint32_t idesc_s = umma_idesc_f16(BF16, 128, UM_KEYS, false);
-      bool ok = wait(q_full, 0, 1);
+      int issued = 0;
       for (int j = 0; j < nt && ok; ++j) {
-        // buffer j % 3 held P(j - 3): its PV must be complete
-        if (j >= 3) ok = wait(o_done + 8 * ((j - 3) % 3), ((j - 3) / 3) & 1, 450 + j);
+        int row = 0;
+        const int t0 = j * UM_KEYS + lane * TILE;
+        if (lane < UM_SLABS && t0 < nkeys) {
+          const int lb = t0 / a.B;
+          const int blk = tbl_in_smem ? tbl[lb] : block_at(lb);
+          row = ((blk * a.L + a.layer) * a.H_kv + g) * a.B + (t0 - lb * a.B);
+        }
+        const int nv = min(UM_SLABS, (nkeys - j * UM_KEYS + TILE - 1) / TILE);
         const int slot = j % UM_KS;
-        if (ok) ok = wait(k_full + 8 * slot, (j / UM_KS) & 1, 300 + j);
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t kb = ks0 + slot * UM_TILE_BYTES;
-#pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-          const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
-          umma_ss(tmem + (j % 3) * 128, umma_desc_sw128(qs + off, 16, 1024), umma_desc_sw128(kb + off, 16, 1024),
-                  idesc_s, k > 0);
+        if (lane == 0) {
+          if (j >= UM_KS) ok = wait(empty0 + 8 * slot, ((j / UM_KS) - 1) & 1, 100 + j);
+          if (ok) mbar_arrive_expect_tx(full0 + 8 * slot, nv * 2 * TILE * 128);
         }
-        umma_commit(s_full + 8 * (j % 3));
-        umma_commit(k_empty + 8 * slot);
-      }
-      if (*abort_flag) {
-        umma_commit(drain);
-        settle(drain, 0);
-      }
-    }
-  } else if (warp == 5) {
-    // ------------------------------------------------------------ PV issuer
-    if (lane == 0) {
-      const uint32_t idesc_o = umma_idesc_f16(BF16, 128, D, true);
-      bool ok = true;
-      for (int j = 0; j < nt && ok; ++j) {
-        const int vslot = j % UM_VS;
-        ok = wait(v_full + 8 * vslot, (j / UM_VS) & 1, 500 + j);
-        if (ok && tail && j == nt - 1) ok = wait(vz, 0, 600);
-        if (ok) ok = wait(p_full + 8 * (j % 3), (j / 3) & 1, 400 + j);
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;  // also orders the expect_tx before the copies
         if (!ok) break;
-        tc_fence_after();
-        const uint32_t vb = vs0 + vslot * UM_TILE_BYTES;
-#pragma unroll
-        for (int k = 0; k < UM_KEYS / 16; ++k)
-          umma_ts(tmem + UM_O_COL, tmem + (j % 3) * 128 + 8 * k, umma_desc_sw128(vb + k * 4096, 2048, 1024), idesc_o,
-                  (j > 0 || k > 0) ? 1u : 0u);
-        umma_commit(o_done + 8 * (j % 3));
-        umma_commit(v_empty + 8 * vslot);
+        issued += 1;
+        if (lane < nv) {
+          if (kw) {  // K slab i: two 2 KB boxes, one per d chunk ([chunk][128 keys][128 B])
+            const uint32_t dst = ks0 + slot * UM_TILE_BYTES + lane * TILE * 128;
+            tma_load_2d(dst, &tmk, 0, row, k_full + 8 * slot);
+            tma_load_2d(dst + 16384, &tmk, 64, row, k_full + 8 * slot);
+          } else {  // V slab i: one 4 KB box of both d chunks ([slab][chunk][16 keys][128 B])
+            tma_load_3d(vs0 + slot * UM_TILE_BYTES + lane * 2 * TILE * 128, &tmv3, 0, row, 0, v_full + 8 * slot);
+          }
+        }
+        if (!kw && tail && j == nt - 1) {
+          // zero the V rows past the sequence end once the tile has landed
+          bool landed = true;
+          if (lane == 0) landed = wait(v_full + 8 * slot, (j / UM_KS) & 1, 200);
+          landed = __shfl_sync(0xffffffffu, landed ? 1 : 0, 0) != 0;
+          if (landed) {
+            uint8_t* vt = base + (2 + UM_KS + slot) * UM_TILE_BYTES;
+            const int r0 = nkeys - j * UM_KEYS;
+            for (int k = lane; k < (UM_KEYS - r0) * 16; k += 32) {  // 16-byte pieces, both d chunks
+              const int r = r0 + k / 16, c = k % 16;
+              *reinterpret_cast<int4*>(vt + (r / TILE) * 4096 + (c / 8) * 2048 + (r % TILE) * 128 + (c % 8) * 16) =
+                  make_int4(0, 0, 0, 0);
+            }
+            fence_proxy_async();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(vz);
+          }
+        }
       }
-      if (*abort_flag) {
-        umma_commit(drain + 8);
-        settle(drain + 8, 0);
+      if (*abort_flag && lane == 0) {  // the last ring's copies may still be landing
+        for (int jj = max(0, issued - UM_KS); jj < issued; ++jj) settle(full0 + 8 * (jj % UM_KS), (jj / UM_KS) & 1);
+      }
+    } else {
+      // ------------------------------------------------------------ tensor-core issuer of tile X (warp 9 A, warp 11 B)
+      const int X = warp == 9 ? 0 : 1;
+      if (lane == 0 && X < nq) {
+        const uint32_t idesc_s = umma_idesc_f16(BF16, 128, UM_KEYS, false);
+        const uint32_t idesc_o = umma_idesc_f16(BF16, 128, D, true);
+        const uint32_t qx = qs + X * UM_TILE_BYTES;
+        const uint32_t sx = tmem + 128 * X, ox = tmem + 256 + 128 * X;
+        bool ok = wait(q_full, 0, 1);
+        for (int j = 0; j < nt && ok; ++j) {
+          const int slot = j % UM_KS;
+          // S_X holds P_X(j - 1) until its P V is complete
+          if (j >= 1) ok = wait(o_done + 8 * X, (j - 1) & 1, 450 + j);
+          if (ok) ok = wait(k_full + 8 * slot, (j / UM_KS) & 1, 300 + j);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t kb = ks0 + slot * UM_TILE_BYTES;
+#pragma unroll
+          for (int k = 0; k < D / 16; ++k) {
+            const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
+            umma_ss(sx, umma_desc_sw128(qx + off, 16, 1024), umma_desc_sw128(kb + off, 16, 1024), idesc_s, k > 0);
+          }
+          umma_commit(s_full + 8 * X);
+          umma_commit(k_empty + 8 * slot);
+          ok = wait(v_full + 8 * slot, (j / UM_KS) & 1, 500 + j);
+          if (ok && tail && j == nt - 1) ok = wait(vz, 0, 600);
+          if (ok) ok = wait(p_full + 8 * X, j & 1, 400 + j);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t vb = vs0 + slot * UM_TILE_BYTES;
+#pragma unroll
+          for (int k = 0; k < UM_KEYS / 16; ++k)
+            umma_ts(ox, sx + 8 * k, umma_desc_sw128(vb + k * 4096, 2048, 1024), idesc_o, (j > 0 || k > 0) ? 1u : 0u);
+          umma_commit(o_done + 8 * X);
+          umma_commit(v_empty + 8 * slot);
+        }
+        if (*abort_flag) {
+          umma_commit(drain + 8 * X);
+          settle(drain + 8 * X, 0);
+        }
       }
     }
   } else {
-    // ------------------------------------------------------------ softmax and epilogue (warps 0-3)
-    const int r = tid;
-    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-    const int qi = i0 + r / G, h = r % G;
-    const bool valid = r < QB * G && qi < i1;
-    const int lim = valid ? P + qi : pmax;  // last visible key
-    float m = -INFINITY, l = 0.f;
-    bool ok = true;
-    // tcgen05.ld / st are warp-collective: every decision below is uniform over the warp
-    for (int j = 0; j < nt && ok; ++j) {
-      ok = __all_sync(0xffffffffu, wait(s_full + 8 * (j % 3), (j / 3) & 1, 700 + j));
-      if (!ok) break;
-      tc_fence_after();
-      const uint32_t s_addr = lane_addr + (j % 3) * 128;
-      uint32_t sv[4][32];
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(UM_REGS_HIGH));
+    if (warp / 4 < nq) {
+      // ---------------------------------------------------------- softmax and epilogue of tile X (warps 4X .. 4X + 3)
+      const int X = warp / 4;
+      const int r = tid & 127;
+      const uint32_t lane_addr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+      const uint32_t s_addr = lane_addr + 128 * X, o_addr = lane_addr + 256 + 128 * X;
+      const int qi = i0 + X * QB + r / G, h = r % G;
+      const bool valid = r < QB * G && qi < i1;
+      const int lim = valid ? P + qi : pmax;  // last visible key
+      float m = -INFINITY, l = 0.f;
+      bool ok = true;
+      // tcgen05.ld / st are warp-collective: every decision below is uniform over the warp
+      for (int j = 0; j < nt && ok; ++j) {
+        ok = __all_sync(0xffffffffu, wait(s_full + 8 * X, j & 1, 700 + j));
+        // the two tiles' softmaxes alternate (A of key tile j, B of j, A of j + 1, ...), so that
+        // one tile's products run on the tensor cores while the other's exponentials run
+        if (ok && X == 0 && nq == 2 && j > 0) ok = __all_sync(0xffffffffu, wait(turn + 8, (j - 1) & 1, 900 + j));
+        if (ok && X == 1) ok = __all_sync(0xffffffffu, wait(turn, j & 1, 900 + j));
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t sv[4][32];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(s_addr + 32 * c, sv[c]);
-      tmem_ld_wait();
-      const int k0 = j * UM_KEYS;
-      // mask only tiles where some row of the warp meets the causal edge or the sequence end
-      if (__any_sync(0xffffffffu, k0 + UM_KEYS - 1 > lim)) {
+        for (int c = 0; c < 4; ++c) tmem_ld32(s_addr + 32 * c, sv[c]);
+        tmem_ld_wait();
+        const int k0 = j * UM_KEYS;
+        // mask only tiles where some row of the warp meets the causal edge or the sequence end
+        if (__any_sync(0xffffffffu, k0 + UM_KEYS - 1 > lim)) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              if (k0 + 32 * c + e > lim) sv[c][e] = __float_as_uint(-INFINITY);
+        }
+        // row max on the raw scores (the scale is positive), 8 independent chains
+        float mx8[8];
+#pragma unroll
+        for (int t = 0; t < 8; ++t) mx8[t] = -INFINITY;
 #pragma unroll
         for (int c = 0; c < 4; ++c)
 #pragma unroll
-          for (int e = 0; e < 32; ++e)
-            if (k0 + 32 * c + e > lim) sv[c][e] = __float_as_uint(-INFINITY);
-      }
-      // row max on the raw scores (the scale is positive), 8 independent chains
-      float mx8[8];
-#pragma unroll
-      for (int t = 0; t < 8; ++t) mx8[t] = -INFINITY;
-#pragma unroll
-      for (int c = 0; c < 4; ++c)
-#pragma unroll
-        for (int e = 0; e < 32; ++e) mx8[e & 7] = fmaxf(mx8[e & 7], __uint_as_float(sv[c][e]));
-      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-      const float sl = a.scale_log2;
-      const float m_new = fmaxf(m, mx * sl);
-      if (__any_sync(0xffffffffu, m_new > m + 8.f)) {  // the reference max moves: rescale l and O so far
-        const float alpha = fast_exp2(m - m_new);
-        if (j > 0) {
-          ok = __all_sync(0xffffffffu, wait(o_done + 8 * ((j - 1) % 3), ((j - 1) / 3) & 1, 800 + j));
-          if (!ok) break;
-          tc_fence_after();
+          for (int e = 0; e < 32; ++e) mx8[e & 7] = fmaxf(mx8[e & 7], __uint_as_float(sv[c][e]));
+        const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+        const float sl = a.scale_log2;
+        const float m_new = fmaxf(m, mx * sl);
+        if (__any_sync(0xffffffffu, m_new > m + 8.f)) {  // the reference max moves: rescale l and O so far
+          const float alpha = fast_exp2(m - m_new);
+          if (j > 0) {
+            ok = __all_sync(0xffffffffu, wait(o_done + 8 * X, (j - 1) & 1, 800 + j));
+            if (!ok) break;
+            tc_fence_after();
 #pragma unroll 1
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t o[32];
-            tmem_ld32(lane_addr + UM_O_COL + 32 * c, o);
-            tmem_ld_wait();
+            for (int c = 0; c < D / 32; ++c) {
+              uint32_t o[32];
+              tmem_ld32(o_addr + 32 * c, o);
+              tmem_ld_wait();
 #pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-            tmem_st32(lane_addr + UM_O_COL + 32 * c, o);
+              for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+              tmem_st32(o_addr + 32 * c, o);
+            }
           }
+          l *= alpha;
+          m = m_new;
         }
-        l *= alpha;
-        m = m_new;
+        // P = 2^(scale * s - m), 16-bit, two keys per TMEM column, written over the S just
+        // read (this lane's row only: its S is in registers); 8 partial sums
+        const float neg_m = -m;
+        float ls8[8];
+#pragma unroll
+        for (int t = 0; t < 8; ++t) ls8[t] = 0.f;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {  // 32 keys -> 16 columns
+          uint32_t pw[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const float p0 = fast_exp2(fmaf(__uint_as_float(sv[c][2 * e]), sl, neg_m));
+            const float p1 = fast_exp2(fmaf(__uint_as_float(sv[c][2 * e + 1]), sl, neg_m));
+            ls8[e & 7] += p0 + p1;
+            pw[e] = pack2<T>(p0, p1);
+          }
+          tmem_st16(s_addr + 16 * c, pw);
+        }
+        l += ((ls8[0] + ls8[1]) + (ls8[2] + ls8[3])) + ((ls8[4] + ls8[5]) + (ls8[6] + ls8[7]));
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(p_full + 8 * X);
+        if (lane == 0) mbar_arrive(turn + 8 * X);
       }
-      // P = 2^(scale * s - m), 16-bit, two keys per TMEM column; 8 partial sums
-      const float neg_m = -m;
-      uint32_t pw[2][32];
-      float ls8[8];
+      if (ok) ok = __all_sync(0xffffffffu, wait(o_done + 8 * X, (nt - 1) & 1, 1000));
+      if (ok) {
+        tc_fence_after();
+        const float inv = 1.f / l;
+        T* out = static_cast<T*>(a.out) + (static_cast<int64_t>(qbeg + qi) * a.H_q + g * G + h) * D;
 #pragma unroll
-      for (int t = 0; t < 8; ++t) ls8[t] = 0.f;
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(o_addr + 32 * c, o);
+          tmem_ld_wait();
+          if (valid) {
+            uint4* dst = reinterpret_cast<uint4*>(out + 32 * c);
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const float p0 = fast_exp2(fmaf(__uint_as_float(sv[c][2 * e]), sl, neg_m));
-          const float p1 = fast_exp2(fmaf(__uint_as_float(sv[c][2 * e + 1]), sl, neg_m));
-          ls8[e & 7] += p0 + p1;
-          pw[c >> 1][(c & 1) * 16 + e] = pack2<T>(p0, p1);
-        }
-      l += ((ls8[0] + ls8[1]) + (ls8[2] + ls8[3])) + ((ls8[4] + ls8[5]) + (ls8[6] + ls8[7]));
-      // P over the S buffer just read (this lane's row only: its S is in registers)
-      tmem_st32(s_addr, pw[0]);
-      tmem_st32(s_addr + 32, pw[1]);
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(p_full + 8 * (j % 3));
-    }
-    if (ok) ok = __all_sync(0xffffffffu, wait(o_done + 8 * ((nt - 1) % 3), ((nt - 1) / 3) & 1, 1000));
-    if (ok) {
-      tc_fence_after();
-      const float inv = 1.f / l;
-      T* out = static_cast<T*>(a.out) + (static_cast<int64_t>(qbeg + qi) * a.H_q + g * G + h) * D;
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t o[32];
-        tmem_ld32(lane_addr + UM_O_COL + 32 * c, o);
-        tmem_ld_wait();
-        if (valid) {
-          uint4* dst = reinterpret_cast<uint4*>(out + 32 * c);
-#pragma unroll
-          for (int v = 0; v < 4; ++v)
-            dst[v] = make_uint4(pack2<T>(__uint_as_float(o[8 * v]) * inv, __uint_as_float(o[8 * v + 1]) * inv),
-                                pack2<T>(__uint_as_float(o[8 * v + 2]) * inv, __uint_as_float(o[8 * v + 3]) * inv),
-                                pack2<T>(__uint_as_float(o[8 * v + 4]) * inv, __uint_as_float(o[8 * v + 5]) * inv),
-                                pack2<T>(__uint_as_float(o[8 * v + 6]) * inv, __uint_as_float(o[8 * v + 7]) * inv));
+            for (int v = 0; v < 4; ++v)
+              dst[v] = make_uint4(pack2<T>(__uint_as_float(o[8 * v]) * inv, __uint_as_float(o[8 * v + 1]) * inv),
+                                  pack2<T>(__uint_as_float(o[8 * v + 2]) * inv, __uint_as_float(o[8 * v + 3]) * inv),
+                                  pack2<T>(__uint_as_float(o[8 * v + 4]) * inv, __uint_as_float(o[8 * v + 5]) * inv),
+                                  pack2<T>(__uint_as_float(o[8 * v + 6]) * inv, __uint_as_float(o[8 * v + 7]) * inv));
+          }
         }
       }
     }
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 4) tmem_dealloc(tmem, 512);
+  if (warp == 8) tmem_dealloc(tmem, 512);
 }
 
 // Chunked prefill on CUDA cores: one CTA per (query row, KV head).  The row's
@@ -742,7 +761,7 @@ int launch_prefill(Pool& P, int32_t layer, const void* q, const int32_t* q_off, 
                        : reinterpret_cast<const void*>(&prefill_umma_kernel<__half>);
     e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, UM_SMEM);
     if (e != cudaSuccess) return fail(PKV_ERR_CUDA, std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e));
-    dim3 grid((max_q + QB - 1) / QB, g.H_kv, n_seq);
+    dim3 grid((max_q + 2 * QB - 1) / (2 * QB), g.H_kv, n_seq);
     void* args[] = {&maps[0], &maps[1], &maps[2], &a, const_cast<int32_t**>(&q_off)};
     e = cudaLaunchKernel(k, grid, dim3(UM_THREADS), args, UM_SMEM, st);
     if (e != cudaSuccess) return fail(PKV_ERR_CUDA, std::string("prefill launch: ") + cudaGetErrorString(e));
