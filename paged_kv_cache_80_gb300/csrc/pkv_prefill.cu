@@ -283,20 +283,21 @@ __global__ void __launch_bounds__(PF_WARPS * 32, 1) prefill_tc_kernel(const __gr
 //     TMEM lane; reads S with tcgen05.ld, keeps the row's running max m and sum l, writes P
 //     (16-bit) back over S, and at the end reads O, divides by l and stores the row;
 //   * warps 8 and 10 (producers; warp 8 owns TMEM): TMA loads of Q (3-D boxes whose rows land
-//     as (query, head)) and of the 128-key K (warp 8) and V (warp 10) tiles, 8 slabs of 16
-//     tokens, each from its own pool block.  Lane i copies K slab i as two boxes, one per
-//     64-wide d chunk, at 2 KB stride so that the 8-row groups are uniformly 1 KB apart, or V
-//     slab i as one 4 KB box of both chunks.  Warp 10 zeroes the V rows past the sequence end
-//     in the last tile so that P = 0 never meets a non-finite value;
+//     as (query, head)) and of the 64-key K (warp 8) and V (warp 10) tiles, 4 slabs of 16
+//     tokens, each from its own pool block, into rings of 4.  Lane i copies K slab i as two
+//     boxes, one per 64-wide d chunk, at 2 KB stride so that the 8-row groups are uniformly
+//     1 KB apart, or V slab i as one 4 KB box of both chunks.  Warp 10 zeroes the V rows past
+//     the sequence end in the last tile so that P = 0 never meets a non-finite value;
 //   * warps 9 and 11 (one thread each): the tensor-core issuers of A and of B: S = Q K^T
-//     (tcgen05.mma kind::f16, both K-major, 128-byte swizzle, M = 128, N = 128, 8 x K = 16)
-//     and O += P V with P read from TMEM and V as an MN-major operand (N = d).
-// TMEM (512 columns): S_A [0, 128), S_B [128, 256), O_A [256, 384), O_B [384, 512).  The
-// softmax writes P (16-bit pairs) over the first 64 columns of the S it read; S = Q K^T of the
-// next key tile goes into the same columns once P V is complete, so each tile's chain is
-// QK^T -> softmax -> PV.  The two softmaxes take turns (A of key tile j, then B of j, then A
-// of j + 1), so that one tile's products run on the tensor cores while the other tile's
-// exponentials run on the CUDA cores.
+//     (tcgen05.mma kind::f16, both K-major, 128-byte swizzle, M = 128, N = 64, 8 x K = 16)
+//     and O += P V (4 x K = 16) with P read from TMEM and V as an MN-major operand (N = d).
+// TMEM (512 columns): tile X has two 64-column S buffers at [128 X, 128 X + 128) and O at
+// [256 + 128 X, 384 + 128 X).  The softmax writes P (16-bit pairs) over the first 32 columns
+// of the S it read; S = Q K^T of key tile j + 1 goes into the other buffer, so it runs on the
+// tensor cores while the softmax of key tile j runs, and a buffer is reused once the P V that
+// read it is complete.  The two softmaxes take turns (A of key tile j, then B of j, then A of
+// j + 1), so that each has the CUDA cores of the SM to itself while the other tile's products
+// run.
 // The online softmax ("Chunked prefill mechanics": m_new = max(m, m_blk), l and O scaled by
 // e^{m - m_new}) rescales O in TMEM only when a row's max grows by more than 2^8; otherwise
 // the old max stays the reference, which is exact because P and l use the same reference.
@@ -317,9 +318,24 @@ __device__ __forceinline__ bool mbar_wait_suspend(uint32_t bar, uint32_t parity,
   return ok != 0;
 }
 
-constexpr int UM_KEYS = 128;
+// non-blocking test of an mbarrier phase
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n"
+      ".reg .pred p;\n"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      "selp.u32 %0, 1, 0, p;\n"
+      "}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+constexpr int UM_KEYS = 64;  // keys per tile: S of both tiles, double-buffered, fits in TMEM
 constexpr int UM_SLABS = UM_KEYS / TILE;
-constexpr int UM_KS = 2, UM_VS = 2;  // K and V rings of equal depth (one slot index)
+constexpr int UM_KS = 4, UM_VS = 4;  // K and V rings of equal depth (one slot index)
 static_assert(UM_KS == UM_VS, "one slot index serves both rings");
 constexpr int UM_THREADS = 384;  // softmax 2 x 4 warps; K producer, issuer A, V producer, issuer B
 // Registers: launched at 65,536 / 384 = 168 a thread (12 warps, 3 per SM sub-partition); the
@@ -327,11 +343,12 @@ constexpr int UM_THREADS = 384;  // softmax 2 x 4 warps; K producer, issuer A, V
 // 4 x 32 x 56 + 8 x 32 x 208 = 60,416 <= 384 x 168 = 64,512.
 constexpr int UM_REGS_LOW = 56, UM_REGS_HIGH = 208;
 static_assert(4 * 32 * UM_REGS_LOW + 8 * 32 * UM_REGS_HIGH <= UM_THREADS * 168, "register split");
-constexpr int UM_TILE_BYTES = 128 * 128 * 2;  // one Q, K or V tile (128 rows x d 128, 16-bit)
-// barriers: q; the K and V rings; (S, P, O, turn) per tile; vz; two drains
-constexpr int UM_BARS = 1 + 2 * UM_KS + 2 * UM_VS + 4 * 2 + 1 + 2;
+constexpr int UM_TILE_BYTES = 128 * 128 * 2;     // one Q tile (128 rows x d 128, 16-bit)
+constexpr int UM_KV_BYTES = UM_KEYS * 128 * 2;   // one K or V tile
+// barriers: q; the K and V rings; (S, P, O) per tile and S buffer; turn per tile; vz; two drains
+constexpr int UM_BARS = 1 + 2 * UM_KS + 2 * UM_VS + 3 * 4 + 2 + 1 + 2;
 constexpr int UM_TBL = 4096;  // block-table entries staged in shared memory (65,536 tokens at B = 16)
-constexpr int UM_SMEM = 1024 + (2 + UM_KS + UM_VS) * UM_TILE_BYTES + UM_BARS * 8 + 16 + UM_TBL * 4;
+constexpr int UM_SMEM = 1024 + 2 * UM_TILE_BYTES + (UM_KS + UM_VS) * UM_KV_BYTES + UM_BARS * 8 + 16 + UM_TBL * 4;
 
 template <typename T>
 __global__ void __launch_bounds__(UM_THREADS, 1) prefill_umma_kernel(const __grid_constant__ CUtensorMap tmq,
@@ -365,13 +382,14 @@ __global__ void __launch_bounds__(UM_THREADS, 1) prefill_umma_kernel(const __gri
 
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t qs = smem_u32(base);
-  const uint32_t ks0 = qs + 2 * UM_TILE_BYTES, vs0 = ks0 + UM_KS * UM_TILE_BYTES;
-  uint8_t* bar_p = base + (2 + UM_KS + UM_VS) * UM_TILE_BYTES;
+  const uint32_t ks0 = qs + 2 * UM_TILE_BYTES, vs0 = ks0 + UM_KS * UM_KV_BYTES;
+  uint8_t* bar_p = base + 2 * UM_TILE_BYTES + (UM_KS + UM_VS) * UM_KV_BYTES;
   const uint32_t bars = smem_u32(bar_p);
   const uint32_t q_full = bars;
   const uint32_t k_full = bars + 8, k_empty = k_full + 8 * UM_KS;
   const uint32_t v_full = k_empty + 8 * UM_KS, v_empty = v_full + 8 * UM_VS;
-  const uint32_t s_full = v_empty + 8 * UM_VS, p_full = s_full + 16, o_done = p_full + 16, vz = o_done + 16;
+  // S, P and O barriers are indexed by 2 X + b: tile X, S buffer b
+  const uint32_t s_full = v_empty + 8 * UM_VS, p_full = s_full + 32, o_done = p_full + 32, vz = o_done + 32;
   const uint32_t drain = vz + 8;  // two barriers: the issuers' last commits after an abort
   const uint32_t turn = drain + 16;  // per tile: its softmax of the current key tile is done
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bar_p + UM_BARS * 8);
@@ -390,10 +408,12 @@ __global__ void __launch_bounds__(UM_THREADS, 1) prefill_umma_kernel(const __gri
       mbar_init(v_full + 8 * k, 1);
       mbar_init(v_empty + 8 * k, nq);
     }
+    for (int i = 0; i < 4; ++i) {
+      mbar_init(s_full + 8 * i, 1);
+      mbar_init(p_full + 8 * i, 128);
+      mbar_init(o_done + 8 * i, 1);
+    }
     for (int x = 0; x < 2; ++x) {
-      mbar_init(s_full + 8 * x, 1);
-      mbar_init(p_full + 8 * x, 128);
-      mbar_init(o_done + 8 * x, 1);
       mbar_init(drain + 8 * x, 1);
       mbar_init(turn + 8 * x, 4);  // one arrival per softmax warp
     }
@@ -475,12 +495,12 @@ __global__ void __launch_bounds__(UM_THREADS, 1) prefill_umma_kernel(const __gri
         if (!ok) break;
         issued += 1;
         if (lane < nv) {
-          if (kw) {  // K slab i: two 2 KB boxes, one per d chunk ([chunk][128 keys][128 B])
-            const uint32_t dst = ks0 + slot * UM_TILE_BYTES + lane * TILE * 128;
+          if (kw) {  // K slab i: two 2 KB boxes, one per d chunk ([chunk][64 keys][128 B])
+            const uint32_t dst = ks0 + slot * UM_KV_BYTES + lane * TILE * 128;
             tma_load_2d(dst, &tmk, 0, row, k_full + 8 * slot);
-            tma_load_2d(dst + 16384, &tmk, 64, row, k_full + 8 * slot);
+            tma_load_2d(dst + UM_KEYS * 128, &tmk, 64, row, k_full + 8 * slot);
           } else {  // V slab i: one 4 KB box of both d chunks ([slab][chunk][16 keys][128 B])
-            tma_load_3d(vs0 + slot * UM_TILE_BYTES + lane * 2 * TILE * 128, &tmv3, 0, row, 0, v_full + 8 * slot);
+            tma_load_3d(vs0 + slot * UM_KV_BYTES + lane * 2 * TILE * 128, &tmv3, 0, row, 0, v_full + 8 * slot);
           }
         }
         if (!kw && tail && j == nt - 1) {
@@ -489,7 +509,7 @@ __global__ void __launch_bounds__(UM_THREADS, 1) prefill_umma_kernel(const __gri
           if (lane == 0) landed = wait(v_full + 8 * slot, (j / UM_KS) & 1, 200);
           landed = __shfl_sync(0xffffffffu, landed ? 1 : 0, 0) != 0;
           if (landed) {
-            uint8_t* vt = base + (2 + UM_KS + slot) * UM_TILE_BYTES;
+            uint8_t* vt = base + 2 * UM_TILE_BYTES + (UM_KS + slot) * UM_KV_BYTES;
             const int r0 = nkeys - j * UM_KEYS;
             for (int k = lane; k < (UM_KEYS - r0) * 16; k += 32) {  // 16-byte pieces, both d chunks
               const int r = r0 + k / 16, c = k % 16;
@@ -513,33 +533,55 @@ __global__ void __launch_bounds__(UM_THREADS, 1) prefill_umma_kernel(const __gri
         const uint32_t idesc_o = umma_idesc_f16(BF16, 128, D, true);
         const uint32_t qx = qs + X * UM_TILE_BYTES;
         const uint32_t sx = tmem + 128 * X, ox = tmem + 256 + 128 * X;
-        bool ok = wait(q_full, 0, 1);
-        for (int j = 0; j < nt && ok; ++j) {
-          const int slot = j % UM_KS;
-          // S_X holds P_X(j - 1) until its P V is complete
-          if (j >= 1) ok = wait(o_done + 8 * X, (j - 1) & 1, 450 + j);
-          if (ok) ok = wait(k_full + 8 * slot, (j / UM_KS) & 1, 300 + j);
-          if (!ok) break;
-          tc_fence_after();
-          const uint32_t kb = ks0 + slot * UM_TILE_BYTES;
+        // S = Q K^T of key tile i into S buffer i & 1 (which held P(i - 2) until its P V was
+        // complete) and O += P V of key tile j are two in-order streams with their own inputs;
+        // the thread starts whichever is ready, so neither waits behind the other.
+        auto qk = [&](int i) {
+          const uint32_t kb = ks0 + (i % UM_KS) * UM_KV_BYTES;
 #pragma unroll
           for (int k = 0; k < D / 16; ++k) {
-            const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
-            umma_ss(sx, umma_desc_sw128(qx + off, 16, 1024), umma_desc_sw128(kb + off, 16, 1024), idesc_s, k > 0);
+            const uint32_t kin = (k & 3) * 32;  // 16 elements = 32 bytes along the swizzled 128-byte row
+            umma_ss(sx + UM_KEYS * (i & 1), umma_desc_sw128(qx + (k >> 2) * 16384 + kin, 16, 1024),
+                    umma_desc_sw128(kb + (k >> 2) * (UM_KEYS * 128) + kin, 16, 1024), idesc_s, k > 0);
           }
-          umma_commit(s_full + 8 * X);
-          umma_commit(k_empty + 8 * slot);
-          ok = wait(v_full + 8 * slot, (j / UM_KS) & 1, 500 + j);
-          if (ok && tail && j == nt - 1) ok = wait(vz, 0, 600);
-          if (ok) ok = wait(p_full + 8 * X, j & 1, 400 + j);
-          if (!ok) break;
-          tc_fence_after();
-          const uint32_t vb = vs0 + slot * UM_TILE_BYTES;
+          umma_commit(s_full + 8 * (2 * X + (i & 1)));
+          umma_commit(k_empty + 8 * (i % UM_KS));
+        };
+        auto pv = [&](int j) {
+          const uint32_t vb = vs0 + (j % UM_VS) * UM_KV_BYTES;
 #pragma unroll
           for (int k = 0; k < UM_KEYS / 16; ++k)
-            umma_ts(ox, sx + 8 * k, umma_desc_sw128(vb + k * 4096, 2048, 1024), idesc_o, (j > 0 || k > 0) ? 1u : 0u);
-          umma_commit(o_done + 8 * X);
-          umma_commit(v_empty + 8 * slot);
+            umma_ts(ox, sx + UM_KEYS * (j & 1) + 8 * k, umma_desc_sw128(vb + k * 4096, 2048, 1024), idesc_o,
+                    (j > 0 || k > 0) ? 1u : 0u);
+          umma_commit(o_done + 8 * (2 * X + (j & 1)));
+          umma_commit(v_empty + 8 * (j % UM_VS));
+        };
+        bool ok = wait(q_full, 0, 1);
+        int i = 0, j = 0;  // next S = Q K^T, next P V
+        uint64_t t_last = global_ns();
+        while (ok && j < nt) {
+          bool progressed = false;
+          if (i < nt && i <= j + 1 && (i < 2 || mbar_test(o_done + 8 * (2 * X + (i & 1)), ((i - 2) >> 1) & 1)) &&
+              mbar_test(k_full + 8 * (i % UM_KS), (i / UM_KS) & 1)) {
+            tc_fence_after();
+            qk(i++);
+            progressed = true;
+          }
+          if (j < i && mbar_test(p_full + 8 * (2 * X + (j & 1)), (j >> 1) & 1) &&
+              mbar_test(v_full + 8 * (j % UM_VS), (j / UM_VS) & 1) && (!tail || j < nt - 1 || mbar_test(vz, 0))) {
+            tc_fence_after();
+            pv(j++);
+            progressed = true;
+          }
+          if (progressed) {
+            t_last = global_ns();
+          } else if (*abort_flag) {
+            ok = false;
+          } else if (global_ns() - t_last > kWaitNs) {
+            *abort_flag = 1;
+            record_error(a.err, DERR_DECODE_TIMEOUT, 400 + j);
+            ok = false;
+          }
         }
         if (*abort_flag) {
           umma_commit(drain + 8 * X);
@@ -554,7 +596,7 @@ __global__ void __launch_bounds__(UM_THREADS, 1) prefill_umma_kernel(const __gri
       const int X = warp / 4;
       const int r = tid & 127;
       const uint32_t lane_addr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
-      const uint32_t s_addr = lane_addr + 128 * X, o_addr = lane_addr + 256 + 128 * X;
+      const uint32_t o_addr = lane_addr + 256 + 128 * X;
       const int qi = i0 + X * QB + r / G, h = r % G;
       const bool valid = r < QB * G && qi < i1;
       const int lim = valid ? P + qi : pmax;  // last visible key
@@ -562,22 +604,25 @@ __global__ void __launch_bounds__(UM_THREADS, 1) prefill_umma_kernel(const __gri
       bool ok = true;
       // tcgen05.ld / st are warp-collective: every decision below is uniform over the warp
       for (int j = 0; j < nt && ok; ++j) {
-        ok = __all_sync(0xffffffffu, wait(s_full + 8 * X, j & 1, 700 + j));
+        const int b = j & 1;
+        const uint32_t s_addr = lane_addr + 128 * X + UM_KEYS * b;
+        ok = __all_sync(0xffffffffu, wait(s_full + 8 * (2 * X + b), (j >> 1) & 1, 700 + j));
         // the two tiles' softmaxes alternate (A of key tile j, B of j, A of j + 1, ...), so that
         // one tile's products run on the tensor cores while the other's exponentials run
         if (ok && X == 0 && nq == 2 && j > 0) ok = __all_sync(0xffffffffu, wait(turn + 8, (j - 1) & 1, 900 + j));
         if (ok && X == 1) ok = __all_sync(0xffffffffu, wait(turn, j & 1, 900 + j));
         if (!ok) break;
         tc_fence_after();
-        uint32_t sv[4][32];
+        constexpr int NC = UM_KEYS / 32;
+        uint32_t sv[NC][32];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld32(s_addr + 32 * c, sv[c]);
+        for (int c = 0; c < NC; ++c) tmem_ld32(s_addr + 32 * c, sv[c]);
         tmem_ld_wait();
         const int k0 = j * UM_KEYS;
         // mask only tiles where some row of the warp meets the causal edge or the sequence end
         if (__any_sync(0xffffffffu, k0 + UM_KEYS - 1 > lim)) {
 #pragma unroll
-          for (int c = 0; c < 4; ++c)
+          for (int c = 0; c < NC; ++c)
 #pragma unroll
             for (int e = 0; e < 32; ++e)
               if (k0 + 32 * c + e > lim) sv[c][e] = __float_as_uint(-INFINITY);
@@ -587,7 +632,7 @@ __global__ void __launch_bounds__(UM_THREADS, 1) prefill_umma_kernel(const __gri
 #pragma unroll
         for (int t = 0; t < 8; ++t) mx8[t] = -INFINITY;
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
+        for (int c = 0; c < NC; ++c)
 #pragma unroll
           for (int e = 0; e < 32; ++e) mx8[e & 7] = fmaxf(mx8[e & 7], __uint_as_float(sv[c][e]));
         const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
@@ -597,7 +642,7 @@ __global__ void __launch_bounds__(UM_THREADS, 1) prefill_umma_kernel(const __gri
         if (__any_sync(0xffffffffu, m_new > m + 8.f)) {  // the reference max moves: rescale l and O so far
           const float alpha = fast_exp2(m - m_new);
           if (j > 0) {
-            ok = __all_sync(0xffffffffu, wait(o_done + 8 * X, (j - 1) & 1, 800 + j));
+            ok = __all_sync(0xffffffffu, wait(o_done + 8 * (2 * X + ((j - 1) & 1)), ((j - 1) >> 1) & 1, 800 + j));
             if (!ok) break;
             tc_fence_after();
 #pragma unroll 1
@@ -620,7 +665,7 @@ __global__ void __launch_bounds__(UM_THREADS, 1) prefill_umma_kernel(const __gri
 #pragma unroll
         for (int t = 0; t < 8; ++t) ls8[t] = 0.f;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {  // 32 keys -> 16 columns
+        for (int c = 0; c < NC; ++c) {  // 32 keys -> 16 columns
           uint32_t pw[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
@@ -634,10 +679,10 @@ __global__ void __launch_bounds__(UM_THREADS, 1) prefill_umma_kernel(const __gri
         l += ((ls8[0] + ls8[1]) + (ls8[2] + ls8[3])) + ((ls8[4] + ls8[5]) + (ls8[6] + ls8[7]));
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(p_full + 8 * X);
+        mbar_arrive(p_full + 8 * (2 * X + b));
         if (lane == 0) mbar_arrive(turn + 8 * X);
       }
-      if (ok) ok = __all_sync(0xffffffffu, wait(o_done + 8 * X, (nt - 1) & 1, 1000));
+      if (ok) ok = __all_sync(0xffffffffu, wait(o_done + 8 * (2 * X + ((nt - 1) & 1)), ((nt - 1) >> 1) & 1, 1000));
       if (ok) {
         tc_fence_after();
         const float inv = 1.f / l;
