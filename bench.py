@@ -834,16 +834,18 @@ def run_prefill(args, torch, pkv, dev, world, rank):
     seed = W.SEEDS["agent32k"] + 11
     total = args.warmup + args.steps
     N = n * hist // 16 + total * n * (C // 16) + 64
-    g = W.Geometry(L=1, H_q=64, H_kv=8, d_head=128, block_size=16, dtype="bf16", num_blocks=N)
+    kvd = getattr(args, "kv_dtype", "bf16") or "bf16"
+    g = W.Geometry(L=1, H_q=64, H_kv=8, d_head=128, block_size=16, dtype=kvd, num_blocks=N)
     pool = pkv.pkv_pool_create(g.L, g.H_q, g.H_kv, g.d_head, g.block_size, g.dtype, N,
                                W.permutation(seed, "prefill_fo", N))
     base = [pkv.pkv_seq_create(pool) for _ in range(n)]
     pkv.pkv_plan_append(pool, base, [hist] * n)
     kp = W.device_normal(seed, "k_pool", g.pool_shape(), g.dtype, dev)
     vp = W.device_normal(seed, "v_pool", g.pool_shape(), g.dtype, dev)
-    q = W.device_normal(seed, "q", (total, n * C, g.H_q, g.d_head), g.dtype, dev)
-    kn = W.device_normal(seed, "kn", (total, n * C, g.H_kv, g.d_head), g.dtype, dev)
-    vn = W.device_normal(seed, "vn", (total, n * C, g.H_kv, g.d_head), g.dtype, dev)
+    act = "bf16" if kvd == "e4m3" else g.dtype  # q, out and new keys/values around an E4M3 pool: bf16
+    q = W.device_normal(seed, "q", (total, n * C, g.H_q, g.d_head), act, dev)
+    kn = W.device_normal(seed, "kn", (total, n * C, g.H_kv, g.d_head), act, dev)
+    vn = W.device_normal(seed, "vn", (total, n * C, g.H_kv, g.d_head), act, dev)
     out = torch.empty((n * C, g.H_q, g.d_head), dtype=torch.bfloat16, device=dev)
     offs = torch.arange(0, n * C + 1, C, dtype=torch.int32, device=dev)
     Wd = (hist + C) // 16
@@ -888,7 +890,7 @@ def run_prefill(args, torch, pkv, dev, world, rank):
     ms = es.elapsed_time(ee) / args.steps
     att = statistics.mean(a.elapsed_time(b) for a, b in ev)
     flop = sum(4.0 * g.H_q * g.d_head * (hist + i + 1) for i in range(C)) * n
-    kvb = n * (hist + C) * g.H_kv * g.d_head * 2 * 2
+    kvb = n * (hist + C) * g.H_kv * g.d_head * W.DTYPE_BYTES[g.dtype] * 2
     tflops = flop / (att / 1e3) / 1e12
     peak = 1916.4
     try:
@@ -899,9 +901,10 @@ def run_prefill(args, torch, pkv, dev, world, rank):
     return {
         "metric": METRIC, "value": round(flop / (ms / 1e3) / 1e12, 2), "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None, "dtype": "f16 (E4M3 K/V)" if kvd == "e4m3" else "bf16",
+        "data": "synthetic",
         "config": {"workload": f"prefill: {n} sequences x {hist:,} cached tokens, a {C}-token chunk each (forked "
-                               "histories), 64 query / 8 KV heads, d_head 128, bf16, 16-token blocks",
+                               f"histories), 64 query / 8 KV heads, d_head 128, {kv_desc(g)}, 16-token blocks",
                    "l2": f"inputs larger than L2 ({kvb / 1e9:.2f} GB of K/V per step)",
                    "parallelism": "replicas (no collectives)"},
         "tokens_per_s": round(n * C / (ms / 1e3), 1),

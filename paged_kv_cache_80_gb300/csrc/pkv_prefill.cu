@@ -335,8 +335,6 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
 
 constexpr int UM_KEYS = 64;  // keys per tile: S of both tiles, double-buffered, fits in TMEM
 constexpr int UM_SLABS = UM_KEYS / TILE;
-constexpr int UM_KS = 4, UM_VS = 4;  // K and V rings of equal depth (one slot index)
-static_assert(UM_KS == UM_VS, "one slot index serves both rings");
 constexpr int UM_THREADS = 384;  // softmax 2 x 4 warps; K producer, issuer A, V producer, issuer B
 // Registers: launched at 65,536 / 384 = 168 a thread (12 warps, 3 per SM sub-partition); the
 // producer warpgroup gives back down to 56 and the softmax warpgroups take 208:
@@ -344,19 +342,45 @@ constexpr int UM_THREADS = 384;  // softmax 2 x 4 warps; K producer, issuer A, V
 constexpr int UM_REGS_LOW = 56, UM_REGS_HIGH = 208;
 static_assert(4 * 32 * UM_REGS_LOW + 8 * 32 * UM_REGS_HIGH <= UM_THREADS * 168, "register split");
 constexpr int UM_TILE_BYTES = 128 * 128 * 2;     // one Q tile (128 rows x d 128, 16-bit)
-constexpr int UM_KV_BYTES = UM_KEYS * 128 * 2;   // one K or V tile
-// barriers: q; the K and V rings; (S, P, O) per tile and S buffer; turn per tile; vz; two drains
-constexpr int UM_BARS = 1 + 2 * UM_KS + 2 * UM_VS + 3 * 4 + 2 + 1 + 2;
+constexpr int UM_KV_BYTES = UM_KEYS * 128 * 2;   // one K or V tile (16-bit operands)
+constexpr int UM_STG_BYTES = UM_KEYS * 128;      // one E4M3 K or V tile as stored (1 byte per element)
+constexpr int UM_FS = 2;                         // E4M3 staging ring depth
+// K and V operand rings: 4 deep for 16-bit pools, 3 for E4M3 pools (whose staging needs the rest)
+__host__ __device__ constexpr int um_ks(bool kv8) { return kv8 ? 3 : 4; }
+// barriers: q; the K and V rings (at most 4 deep); (S, P, O) per tile and S buffer; vz; two drains;
+// turn per tile; the E4M3 staging rings; Q converted
+constexpr int UM_BARS = 1 + 4 * 4 + 3 * 4 + 1 + 2 + 2 + 2 * UM_FS + 1;
 constexpr int UM_TBL = 4096;  // block-table entries staged in shared memory (65,536 tokens at B = 16)
-constexpr int UM_SMEM = 1024 + 2 * UM_TILE_BYTES + (UM_KS + UM_VS) * UM_KV_BYTES + UM_BARS * 8 + 16 + UM_TBL * 4;
+constexpr int um_smem(bool kv8) {
+  return 1024 + 2 * UM_TILE_BYTES + 2 * um_ks(kv8) * UM_KV_BYTES + (kv8 ? 2 * UM_FS * UM_STG_BYTES : 0) + UM_BARS * 8 +
+         16 + UM_TBL * 4;
+}
+static_assert(um_smem(false) <= 232448 && um_smem(true) <= 232448, "shared memory per CTA");
 
-template <typename T>
+// two E4M3 codes per 16-bit half of w to two binary16 pairs (exact), the first of each pair low
+__device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, l;\n\tcvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
+}
+// two bfloat16 values (low half first) rounded to binary16
+__device__ __forceinline__ uint32_t bf16x2_rn_f16x2(uint32_t w) {
+  __half2 h = __floats2half2_rn(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// T: the type of q and out; KV8: an E4M3 pool, whose products run on binary16 operands (the
+// codes convert exactly; q is rounded to binary16 as on the FP8 decode path).
+template <typename T, bool KV8>
 __global__ void __launch_bounds__(UM_THREADS, 1) prefill_umma_kernel(const __grid_constant__ CUtensorMap tmq,
                                                                       const __grid_constant__ CUtensorMap tmk,
                                                                       const __grid_constant__ CUtensorMap tmv3,
                                                                       const DecodeArgs a, const int32_t* q_off) {
   constexpr int D = 128;
-  constexpr bool BF16 = std::is_same<T, __nv_bfloat16>::value;
+  constexpr bool BF16 = std::is_same<T, __nv_bfloat16>::value && !KV8;  // operand type of the products
+  using TP = typename std::conditional<BF16, __nv_bfloat16, __half>::type;  // type of P
+  constexpr int KS = um_ks(KV8);
   extern __shared__ uint8_t smem_raw[];
   const int qb = blockIdx.x, g = blockIdx.y, s = blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -382,16 +406,19 @@ __global__ void __launch_bounds__(UM_THREADS, 1) prefill_umma_kernel(const __gri
 
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t qs = smem_u32(base);
-  const uint32_t ks0 = qs + 2 * UM_TILE_BYTES, vs0 = ks0 + UM_KS * UM_KV_BYTES;
-  uint8_t* bar_p = base + 2 * UM_TILE_BYTES + (UM_KS + UM_VS) * UM_KV_BYTES;
+  const uint32_t ks0 = qs + 2 * UM_TILE_BYTES, vs0 = ks0 + KS * UM_KV_BYTES;
+  const int stg_off = 2 * UM_TILE_BYTES + 2 * KS * UM_KV_BYTES;  // E4M3 staging: K ring, then V ring
+  uint8_t* bar_p = base + stg_off + (KV8 ? 2 * UM_FS * UM_STG_BYTES : 0);
   const uint32_t bars = smem_u32(bar_p);
   const uint32_t q_full = bars;
-  const uint32_t k_full = bars + 8, k_empty = k_full + 8 * UM_KS;
-  const uint32_t v_full = k_empty + 8 * UM_KS, v_empty = v_full + 8 * UM_VS;
+  const uint32_t k_full = bars + 8, k_empty = k_full + 8 * KS;
+  const uint32_t v_full = k_empty + 8 * KS, v_empty = v_full + 8 * KS;
   // S, P and O barriers are indexed by 2 X + b: tile X, S buffer b
-  const uint32_t s_full = v_empty + 8 * UM_VS, p_full = s_full + 32, o_done = p_full + 32, vz = o_done + 32;
+  const uint32_t s_full = v_empty + 8 * KS, p_full = s_full + 32, o_done = p_full + 32, vz = o_done + 32;
   const uint32_t drain = vz + 8;  // two barriers: the issuers' last commits after an abort
   const uint32_t turn = drain + 16;  // per tile: its softmax of the current key tile is done
+  const uint32_t sk_full = turn + 16, sv_full = sk_full + 8 * UM_FS;  // E4M3 staging landed
+  const uint32_t q_ready = sv_full + 8 * UM_FS;                        // E4M3 pools: q in binary16
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bar_p + UM_BARS * 8);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bar_p + UM_BARS * 8 + 4);
   int32_t* tbl = reinterpret_cast<int32_t*>(bar_p + UM_BARS * 8 + 16);
@@ -400,14 +427,17 @@ __global__ void __launch_bounds__(UM_THREADS, 1) prefill_umma_kernel(const __gri
 
   if (tid == 0) {
     mbar_init(q_full, 1);
-    for (int k = 0; k < UM_KS; ++k) {
+    for (int k = 0; k < KS; ++k) {
       mbar_init(k_full + 8 * k, 1);
       mbar_init(k_empty + 8 * k, nq);  // released by every tile's QK^T
-    }
-    for (int k = 0; k < UM_VS; ++k) {
       mbar_init(v_full + 8 * k, 1);
       mbar_init(v_empty + 8 * k, nq);
     }
+    for (int f = 0; f < UM_FS; ++f) {
+      mbar_init(sk_full + 8 * f, 1);
+      mbar_init(sv_full + 8 * f, 1);
+    }
+    mbar_init(q_ready, nq);
     for (int i = 0; i < 4; ++i) {
       mbar_init(s_full + 8 * i, 1);
       mbar_init(p_full + 8 * i, 128);
@@ -475,55 +505,144 @@ __global__ void __launch_bounds__(UM_THREADS, 1) prefill_umma_kernel(const __gri
         __syncwarp();
       }
       const uint32_t full0 = kw ? k_full : v_full, empty0 = kw ? k_empty : v_empty;
-      bool ok = true;
-      int issued = 0;
-      for (int j = 0; j < nt && ok; ++j) {
-        int row = 0;
-        const int t0 = j * UM_KEYS + lane * TILE;
-        if (lane < UM_SLABS && t0 < nkeys) {
-          const int lb = t0 / a.B;
-          const int blk = tbl_in_smem ? tbl[lb] : block_at(lb);
-          row = ((blk * a.L + a.layer) * a.H_kv + g) * a.B + (t0 - lb * a.B);
-        }
-        const int nv = min(UM_SLABS, (nkeys - j * UM_KEYS + TILE - 1) / TILE);
-        const int slot = j % UM_KS;
-        if (lane == 0) {
-          if (j >= UM_KS) ok = wait(empty0 + 8 * slot, ((j / UM_KS) - 1) & 1, 100 + j);
-          if (ok) mbar_arrive_expect_tx(full0 + 8 * slot, nv * 2 * TILE * 128);
-        }
-        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;  // also orders the expect_tx before the copies
-        if (!ok) break;
-        issued += 1;
-        if (lane < nv) {
-          if (kw) {  // K slab i: two 2 KB boxes, one per d chunk ([chunk][64 keys][128 B])
-            const uint32_t dst = ks0 + slot * UM_KV_BYTES + lane * TILE * 128;
-            tma_load_2d(dst, &tmk, 0, row, k_full + 8 * slot);
-            tma_load_2d(dst + UM_KEYS * 128, &tmk, 64, row, k_full + 8 * slot);
-          } else {  // V slab i: one 4 KB box of both d chunks ([slab][chunk][16 keys][128 B])
-            tma_load_3d(vs0 + slot * UM_KV_BYTES + lane * 2 * TILE * 128, &tmv3, 0, row, 0, v_full + 8 * slot);
+      if constexpr (KV8) {
+        // E4M3 pool: lane i < 4 copies slab i of a 64-key tile (one 2 KB box of codes, 128-byte
+        // swizzle) into a staging ring; the warp converts each tile to binary16 in the operand
+        // layout of the 16-bit path and zeroes the V rows past the sequence end.
+        const uint32_t sfull0 = kw ? sk_full : sv_full;
+        const int stg = stg_off + (kw ? 0 : UM_FS * UM_STG_BYTES);
+        const CUtensorMap* map = kw ? &tmk : &tmv3;
+        auto issue = [&](int j) {
+          int row = 0;
+          const int t0 = j * UM_KEYS + lane * TILE;
+          if (lane < UM_SLABS && t0 < nkeys) {
+            const int lb = t0 / a.B;
+            const int blk = tbl_in_smem ? tbl[lb] : block_at(lb);
+            row = ((blk * a.L + a.layer) * a.H_kv + g) * a.B + (t0 - lb * a.B);
           }
-        }
-        if (!kw && tail && j == nt - 1) {
-          // zero the V rows past the sequence end once the tile has landed
-          bool landed = true;
-          if (lane == 0) landed = wait(v_full + 8 * slot, (j / UM_KS) & 1, 200);
-          landed = __shfl_sync(0xffffffffu, landed ? 1 : 0, 0) != 0;
-          if (landed) {
-            uint8_t* vt = base + 2 * UM_TILE_BYTES + (UM_KS + slot) * UM_KV_BYTES;
-            const int r0 = nkeys - j * UM_KEYS;
-            for (int k = lane; k < (UM_KEYS - r0) * 16; k += 32) {  // 16-byte pieces, both d chunks
-              const int r = r0 + k / 16, c = k % 16;
-              *reinterpret_cast<int4*>(vt + (r / TILE) * 4096 + (c / 8) * 2048 + (r % TILE) * 128 + (c % 8) * 16) =
-                  make_int4(0, 0, 0, 0);
+          const int nv = min(UM_SLABS, (nkeys - j * UM_KEYS + TILE - 1) / TILE);
+          const uint32_t bar = sfull0 + 8 * (j % UM_FS);
+          if (lane == 0) {
+            fence_proxy_async();  // this warp's reads of the slot come before the copy overwrites it
+            mbar_arrive_expect_tx(bar, nv * TILE * 128);
+          }
+          __syncwarp();
+          if (lane < nv) tma_load_2d(qs + stg + (j % UM_FS) * UM_STG_BYTES + lane * TILE * 128, map, 0, row, bar);
+        };
+        issue(0);
+        if (nt > 1) issue(1);
+        int issued = min(nt, UM_FS);
+        bool ok = true;
+        // q of this warp's tile (warp 8: A, warp 10: B) to binary16 in place once it has landed
+        const int xq = kw ? 0 : 1;
+        if (xq < nq) {
+          if (lane == 0) ok = wait(q_full, 0, 1);
+          ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+          if (ok) {
+            uint4* qt = reinterpret_cast<uint4*>(base + xq * UM_TILE_BYTES);
+            for (int k = lane; k < UM_TILE_BYTES / 16; k += 32) {
+              uint4 w = qt[k];
+              w = make_uint4(bf16x2_rn_f16x2(w.x), bf16x2_rn_f16x2(w.y), bf16x2_rn_f16x2(w.z), bf16x2_rn_f16x2(w.w));
+              qt[k] = w;
             }
             fence_proxy_async();
             __syncwarp();
-            if (lane == 0) mbar_arrive(vz);
+            if (lane == 0) mbar_arrive(q_ready);
           }
         }
-      }
-      if (*abort_flag && lane == 0) {  // the last ring's copies may still be landing
-        for (int jj = max(0, issued - UM_KS); jj < issued; ++jj) settle(full0 + 8 * (jj % UM_KS), (jj / UM_KS) & 1);
+        for (int j = 0; j < nt && ok; ++j) {
+          const int slot = j % KS, f = j % UM_FS;
+          if (lane == 0) {
+            ok = wait(sfull0 + 8 * f, (j / UM_FS) & 1, 120 + j);
+            if (ok && j >= KS) ok = wait(empty0 + 8 * slot, ((j / KS) - 1) & 1, 100 + j);
+          }
+          ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+          if (!ok) break;
+          // staging row r of slab i holds d = 16 u .. 16 u + 15 in 16-byte unit u ^ (r & 7); the
+          // operand rows hold d in two 64-wide chunks of eight 16-byte units, unit t at t ^ (row & 7)
+          const uint8_t* src = base + stg + f * UM_STG_BYTES;
+          uint8_t* dst = base + 2 * UM_TILE_BYTES + ((kw ? 0 : KS) + slot) * UM_KV_BYTES;
+          const int r0 = nkeys - j * UM_KEYS;  // tile rows at or past r0 are past the sequence end
+#pragma unroll 2
+          for (int k = 0; k < UM_STG_BYTES / 16 / 32; ++k) {
+            const int idx = lane + 32 * k;
+            const int i = idx >> 7, r = (idx >> 3) & 15, u = idx & 7, R = TILE * i + r;
+            const uint4 w = *reinterpret_cast<const uint4*>(src + i * (TILE * 128) + r * 128 + ((u ^ (r & 7)) << 4));
+            uint4 o0 = make_uint4(0, 0, 0, 0), o1 = make_uint4(0, 0, 0, 0);
+            if (kw || R < r0) {
+              e4m3x4_to_f16x4(w.x, o0.x, o0.y);
+              e4m3x4_to_f16x4(w.y, o0.z, o0.w);
+              e4m3x4_to_f16x4(w.z, o1.x, o1.y);
+              e4m3x4_to_f16x4(w.w, o1.z, o1.w);
+            }
+            const int c = u >> 2, t = (u & 3) * 2, sw = R & 7;
+            // K: [chunk][64 keys][128 B]; V: [slab][chunk][16 keys][128 B]
+            uint8_t* rowp = kw ? dst + c * (UM_KEYS * 128) + R * 128 : dst + i * 4096 + c * 2048 + r * 128;
+            *reinterpret_cast<uint4*>(rowp + ((t ^ sw) << 4)) = o0;
+            *reinterpret_cast<uint4*>(rowp + (((t + 1) ^ sw) << 4)) = o1;
+          }
+          fence_proxy_async();  // the generic-proxy writes, before the tensor cores read them
+          __syncwarp();
+          if (lane == 0) mbar_arrive(full0 + 8 * slot);
+          if (j + UM_FS < nt) {
+            issue(j + UM_FS);
+            ++issued;
+          }
+        }
+        if (*abort_flag && lane == 0) {  // copies into the staging ring may still be landing
+          for (int jj = max(0, issued - UM_FS); jj < issued; ++jj) settle(sfull0 + 8 * (jj % UM_FS), (jj / UM_FS) & 1);
+        }
+      } else {
+        bool ok = true;
+        int issued = 0;
+        for (int j = 0; j < nt && ok; ++j) {
+          int row = 0;
+          const int t0 = j * UM_KEYS + lane * TILE;
+          if (lane < UM_SLABS && t0 < nkeys) {
+            const int lb = t0 / a.B;
+            const int blk = tbl_in_smem ? tbl[lb] : block_at(lb);
+            row = ((blk * a.L + a.layer) * a.H_kv + g) * a.B + (t0 - lb * a.B);
+          }
+          const int nv = min(UM_SLABS, (nkeys - j * UM_KEYS + TILE - 1) / TILE);
+          const int slot = j % KS;
+          if (lane == 0) {
+            if (j >= KS) ok = wait(empty0 + 8 * slot, ((j / KS) - 1) & 1, 100 + j);
+            if (ok) mbar_arrive_expect_tx(full0 + 8 * slot, nv * 2 * TILE * 128);
+          }
+          ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;  // also orders the expect_tx before the copies
+          if (!ok) break;
+          issued += 1;
+          if (lane < nv) {
+            if (kw) {  // K slab i: two 2 KB boxes, one per d chunk ([chunk][64 keys][128 B])
+              const uint32_t dst = ks0 + slot * UM_KV_BYTES + lane * TILE * 128;
+              tma_load_2d(dst, &tmk, 0, row, k_full + 8 * slot);
+              tma_load_2d(dst + UM_KEYS * 128, &tmk, 64, row, k_full + 8 * slot);
+            } else {  // V slab i: one 4 KB box of both d chunks ([slab][chunk][16 keys][128 B])
+              tma_load_3d(vs0 + slot * UM_KV_BYTES + lane * 2 * TILE * 128, &tmv3, 0, row, 0, v_full + 8 * slot);
+            }
+          }
+          if (!kw && tail && j == nt - 1) {
+            // zero the V rows past the sequence end once the tile has landed
+            bool landed = true;
+            if (lane == 0) landed = wait(v_full + 8 * slot, (j / KS) & 1, 200);
+            landed = __shfl_sync(0xffffffffu, landed ? 1 : 0, 0) != 0;
+            if (landed) {
+              uint8_t* vt = base + 2 * UM_TILE_BYTES + (KS + slot) * UM_KV_BYTES;
+              const int r0 = nkeys - j * UM_KEYS;
+              for (int k = lane; k < (UM_KEYS - r0) * 16; k += 32) {  // 16-byte pieces, both d chunks
+                const int r = r0 + k / 16, c = k % 16;
+                *reinterpret_cast<int4*>(vt + (r / TILE) * 4096 + (c / 8) * 2048 + (r % TILE) * 128 + (c % 8) * 16) =
+                    make_int4(0, 0, 0, 0);
+              }
+              fence_proxy_async();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(vz);
+            }
+          }
+        }
+        if (*abort_flag && lane == 0) {  // the last ring's copies may still be landing
+          for (int jj = max(0, issued - KS); jj < issued; ++jj) settle(full0 + 8 * (jj % KS), (jj / KS) & 1);
+        }
       }
     } else {
       // ------------------------------------------------------------ tensor-core issuer of tile X (warp 9 A, warp 11 B)
@@ -537,7 +656,7 @@ __global__ void __launch_bounds__(UM_THREADS, 1) prefill_umma_kernel(const __gri
         // complete) and O += P V of key tile j are two in-order streams with their own inputs;
         // the thread starts whichever is ready, so neither waits behind the other.
         auto qk = [&](int i) {
-          const uint32_t kb = ks0 + (i % UM_KS) * UM_KV_BYTES;
+          const uint32_t kb = ks0 + (i % KS) * UM_KV_BYTES;
 #pragma unroll
           for (int k = 0; k < D / 16; ++k) {
             const uint32_t kin = (k & 3) * 32;  // 16 elements = 32 bytes along the swizzled 128-byte row
@@ -545,30 +664,30 @@ __global__ void __launch_bounds__(UM_THREADS, 1) prefill_umma_kernel(const __gri
                     umma_desc_sw128(kb + (k >> 2) * (UM_KEYS * 128) + kin, 16, 1024), idesc_s, k > 0);
           }
           umma_commit(s_full + 8 * (2 * X + (i & 1)));
-          umma_commit(k_empty + 8 * (i % UM_KS));
+          umma_commit(k_empty + 8 * (i % KS));
         };
         auto pv = [&](int j) {
-          const uint32_t vb = vs0 + (j % UM_VS) * UM_KV_BYTES;
+          const uint32_t vb = vs0 + (j % KS) * UM_KV_BYTES;
 #pragma unroll
           for (int k = 0; k < UM_KEYS / 16; ++k)
             umma_ts(ox, sx + UM_KEYS * (j & 1) + 8 * k, umma_desc_sw128(vb + k * 4096, 2048, 1024), idesc_o,
                     (j > 0 || k > 0) ? 1u : 0u);
           umma_commit(o_done + 8 * (2 * X + (j & 1)));
-          umma_commit(v_empty + 8 * (j % UM_VS));
+          umma_commit(v_empty + 8 * (j % KS));
         };
-        bool ok = wait(q_full, 0, 1);
+        bool ok = wait(KV8 ? q_ready : q_full, 0, 1);
         int i = 0, j = 0;  // next S = Q K^T, next P V
         uint64_t t_last = global_ns();
         while (ok && j < nt) {
           bool progressed = false;
           if (i < nt && i <= j + 1 && (i < 2 || mbar_test(o_done + 8 * (2 * X + (i & 1)), ((i - 2) >> 1) & 1)) &&
-              mbar_test(k_full + 8 * (i % UM_KS), (i / UM_KS) & 1)) {
+              mbar_test(k_full + 8 * (i % KS), (i / KS) & 1)) {
             tc_fence_after();
             qk(i++);
             progressed = true;
           }
           if (j < i && mbar_test(p_full + 8 * (2 * X + (j & 1)), (j >> 1) & 1) &&
-              mbar_test(v_full + 8 * (j % UM_VS), (j / UM_VS) & 1) && (!tail || j < nt - 1 || mbar_test(vz, 0))) {
+              mbar_test(v_full + 8 * (j % KS), (j / KS) & 1) && (KV8 || !tail || j < nt - 1 || mbar_test(vz, 0))) {
             tc_fence_after();
             pv(j++);
             progressed = true;
@@ -672,7 +791,7 @@ __global__ void __launch_bounds__(UM_THREADS, 1) prefill_umma_kernel(const __gri
             const float p0 = fast_exp2(fmaf(__uint_as_float(sv[c][2 * e]), sl, neg_m));
             const float p1 = fast_exp2(fmaf(__uint_as_float(sv[c][2 * e + 1]), sl, neg_m));
             ls8[e & 7] += p0 + p1;
-            pw[e] = pack2<T>(p0, p1);
+            pw[e] = pack2<TP>(p0, p1);
           }
           tmem_st16(s_addr + 16 * c, pw);
         }
@@ -685,7 +804,7 @@ __global__ void __launch_bounds__(UM_THREADS, 1) prefill_umma_kernel(const __gri
       if (ok) ok = __all_sync(0xffffffffu, wait(o_done + 8 * (2 * X + ((nt - 1) & 1)), ((nt - 1) >> 1) & 1, 1000));
       if (ok) {
         tc_fence_after();
-        const float inv = 1.f / l;
+        const float inv = a.v_mul / l;  // v_scale of an E4M3 pool, else 1
         T* out = static_cast<T*>(a.out) + (static_cast<int64_t>(qbeg + qi) * a.H_q + g * G + h) * D;
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
@@ -772,13 +891,17 @@ int launch_prefill(Pool& P, int32_t layer, const void* q, const int32_t* q_off, 
   const bool tc = (g.dtype == PKV_BF16 || g.dtype == PKV_F16) && (g.d_head == 64 || g.d_head == 128) &&
                   G <= PF_ROWS && g.block_size % TILE == 0 && rows < (int64_t(1) << 31) && encode_fn() != nullptr;
   static const bool force_mma_sync = std::getenv("PKV_PREFILL_MMA_SYNC") != nullptr;
-  if (tc && g.d_head == 128 && !force_mma_sync) {
+  // E4M3 pools with d_head 128: the same tcgen05 kernel on binary16 operands converted in shared memory
+  const bool tc8 = g.dtype == PKV_E4M3 && g.d_head == 128 && G <= PF_ROWS && g.block_size % TILE == 0 &&
+                   rows < (int64_t(1) << 31) && encode_fn() != nullptr;
+  if ((tc && g.d_head == 128 && !force_mma_sync) || tc8) {
     if ((reinterpret_cast<uintptr_t>(q) & 15) || (reinterpret_cast<uintptr_t>(out) & 15))
       return fail(PKV_ERR_INVALID_ARG, "q and out must be 16-byte aligned");
     CUtensorMap maps[3];
     if (int rc = get_tensor_maps(P, k_pool, v_pool, &maps[1], &maps[2])) return rc;
     // V as {64, rows, 2 d chunks}: a {64, 16, 2} box is one 16-token slab, both chunks, 4 KB
-    {
+    // (E4M3 pools copy slabs of codes with the 2-D maps and convert them in the kernel)
+    if (!tc8) {
       cuuint64_t vd[3] = {64, static_cast<cuuint64_t>(g.num_blocks) * g.L * g.H_kv * g.block_size, 2};
       cuuint64_t vs[2] = {256, 128};
       cuuint32_t vb[3] = {64, TILE, 2};
@@ -792,7 +915,8 @@ int launch_prefill(Pool& P, int32_t layer, const void* q, const int32_t* q_off, 
     }
     // q as {d, H_q, n_tok}: a box of {64, G, 128 / G} lands as 128 (query, head) rows of 128 bytes
     const int QB = 128 / G;
-    const CUtensorMapDataType dt = g.dtype == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const CUtensorMapDataType dt =
+        g.dtype == PKV_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;  // q: bf16 for E4M3
     cuuint64_t dims[3] = {128, static_cast<cuuint64_t>(g.H_q), static_cast<cuuint64_t>(std::max(n_tok, 1))};
     cuuint64_t strides[2] = {256, static_cast<cuuint64_t>(g.H_q) * 256};
     cuuint32_t box[3] = {64, static_cast<cuuint32_t>(G), static_cast<cuuint32_t>(QB)};
@@ -801,14 +925,15 @@ int launch_prefill(Pool& P, int32_t layer, const void* q, const int32_t* q_off, 
                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled (q) failed: " + std::to_string(r));
-    const bool bf = g.dtype == PKV_BF16;
-    const void* k = bf ? reinterpret_cast<const void*>(&prefill_umma_kernel<__nv_bfloat16>)
-                       : reinterpret_cast<const void*>(&prefill_umma_kernel<__half>);
-    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, UM_SMEM);
+    const void* k = tc8 ? reinterpret_cast<const void*>(&prefill_umma_kernel<__nv_bfloat16, true>)
+                    : g.dtype == PKV_BF16 ? reinterpret_cast<const void*>(&prefill_umma_kernel<__nv_bfloat16, false>)
+                                          : reinterpret_cast<const void*>(&prefill_umma_kernel<__half, false>);
+    const int smem = um_smem(tc8);
+    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return fail(PKV_ERR_CUDA, std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e));
     dim3 grid((max_q + 2 * QB - 1) / (2 * QB), g.H_kv, n_seq);
     void* args[] = {&maps[0], &maps[1], &maps[2], &a, const_cast<int32_t**>(&q_off)};
-    e = cudaLaunchKernel(k, grid, dim3(UM_THREADS), args, UM_SMEM, st);
+    e = cudaLaunchKernel(k, grid, dim3(UM_THREADS), args, smem, st);
     if (e != cudaSuccess) return fail(PKV_ERR_CUDA, std::string("prefill launch: ") + cudaGetErrorString(e));
     count_launch();
     return PKV_OK;

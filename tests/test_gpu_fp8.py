@@ -125,25 +125,37 @@ def test_fp8_noalloc_equals_workspace_call():
     check_attention(got, b.decode_ref(q, tables, lens, 0.09), "bf16")
 
 
-def test_fp8_prefill_on_cuda_cores():
+def _fp8_prefill(H_q, H_kv, d, history, chunks, seed, scales, num_blocks):
     import torch
 
-    g = W.Geometry(L=1, H_q=16, H_kv=4, d_head=128, block_size=16, dtype="e4m3", num_blocks=200)
-    b = PagedBatch(g, W.permutation(56, "fo", g.num_blocks), seed=56, kv_scales=(0.1, 0.4))
-    ids = b.new_seqs(3)
-    b.append(ids, [100, 0, 700], "history")
-    chunks = [37, 16, 5]
+    g = W.Geometry(L=1, H_q=H_q, H_kv=H_kv, d_head=d, block_size=16, dtype="e4m3", num_blocks=num_blocks)
+    b = PagedBatch(g, W.permutation(seed, "fo", g.num_blocks), seed=seed, kv_scales=scales)
+    ids = b.new_seqs(len(history))
+    b.append(ids, history, "history")
     b.append(ids, chunks, "chunk")
     tables, lens = b.tables(ids)
     qo = np.concatenate([[0], np.cumsum(chunks)]).astype(np.int32)
-    q = W.normal(56, "q", (int(qo[-1]), g.H_q, g.d_head), "bf16")
+    q = W.normal(seed, "q", (int(qo[-1]), g.H_q, g.d_head), "bf16")
     out = torch.full((int(qo[-1]), g.H_q, g.d_head), float("nan"), dtype=torch.bfloat16, device="cuda")
+    scale = 1.0 / math.sqrt(d)
     pkv.pkv_prefill_attention(b.lib, 0, to_dev(q, "bf16"), torch.from_numpy(qo).cuda(), max(chunks), b.kp, b.vp,
-                              torch.from_numpy(tables).cuda(), torch.from_numpy(lens).cuda(), 0.088, out)
+                              torch.from_numpy(tables).cuda(), torch.from_numpy(lens).cuda(), scale, out)
     pkv.pkv_check_device_error()
-    ref = oracle.prefill_attention(g, 0, q, qo, b.hk, b.hv, tables, lens, 0.088, k_scale=b.k_scale,
+    ref = oracle.prefill_attention(g, 0, q, qo, b.hk, b.hv, tables, lens, scale, k_scale=b.k_scale,
                                    v_scale=b.v_scale)
     check_attention(out_f64(out, "bf16"), ref, "bf16")
+
+
+@pytest.mark.parametrize("H_q,H_kv", [(64, 8), (16, 4), (48, 4), (8, 8)])
+def test_fp8_prefill_tensor_cores(H_q, H_kv):
+    # d_head 128: tcgen05 kernel on binary16 operands converted from the codes in shared memory;
+    # ragged chunks (one query, a 16-query tile, 512), empty and long histories, ragged tails
+    _fp8_prefill(H_q, H_kv, 128, [0, 5, 64, 1000, 37, 300, 3000], [17, 1, 100, 40, 130, 16, 512], 56, (0.1, 0.4), 400)
+
+
+def test_fp8_prefill_on_cuda_cores():
+    # d_head 64 over an E4M3 pool runs on the CUDA-core kernel
+    _fp8_prefill(16, 4, 64, [100, 0, 700], [37, 16, 5], 58, (0.2, 0.3), 200)
 
 
 @pytest.mark.parametrize("engine", [0, 1])
