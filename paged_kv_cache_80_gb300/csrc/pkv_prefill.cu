@@ -348,8 +348,8 @@ constexpr int UM_FS = 2;                         // E4M3 staging ring depth
 // K and V operand rings: 4 deep for 16-bit pools, 3 for E4M3 pools (whose staging needs the rest)
 __host__ __device__ constexpr int um_ks(bool kv8) { return kv8 ? 3 : 4; }
 // barriers: q; the K and V rings (at most 4 deep); (S, P, O) per tile and S buffer; vz; two drains;
-// turn per tile; the E4M3 staging rings; Q converted
-constexpr int UM_BARS = 1 + 4 * 4 + 3 * 4 + 1 + 2 + 2 + 2 * UM_FS + 1;
+// turn per tile; the E4M3 staging rings (full, free); Q converted
+constexpr int UM_BARS = 1 + 4 * 4 + 3 * 4 + 1 + 2 + 2 + 4 * UM_FS + 1;
 constexpr int UM_TBL = 4096;  // block-table entries staged in shared memory (65,536 tokens at B = 16)
 constexpr int um_smem(bool kv8) {
   return 1024 + 2 * UM_TILE_BYTES + 2 * um_ks(kv8) * UM_KV_BYTES + (kv8 ? 2 * UM_FS * UM_STG_BYTES : 0) + UM_BARS * 8 +
@@ -418,7 +418,8 @@ __global__ void __launch_bounds__(UM_THREADS, 1) prefill_umma_kernel(const __gri
   const uint32_t drain = vz + 8;  // two barriers: the issuers' last commits after an abort
   const uint32_t turn = drain + 16;  // per tile: its softmax of the current key tile is done
   const uint32_t sk_full = turn + 16, sv_full = sk_full + 8 * UM_FS;  // E4M3 staging landed
-  const uint32_t q_ready = sv_full + 8 * UM_FS;                        // E4M3 pools: q in binary16
+  const uint32_t sk_free = sv_full + 8 * UM_FS, sv_free = sk_free + 8 * UM_FS;  // staging read
+  const uint32_t q_ready = sv_free + 8 * UM_FS;                                  // E4M3: q in binary16
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bar_p + UM_BARS * 8);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bar_p + UM_BARS * 8 + 4);
   int32_t* tbl = reinterpret_cast<int32_t*>(bar_p + UM_BARS * 8 + 16);
@@ -428,14 +429,16 @@ __global__ void __launch_bounds__(UM_THREADS, 1) prefill_umma_kernel(const __gri
   if (tid == 0) {
     mbar_init(q_full, 1);
     for (int k = 0; k < KS; ++k) {
-      mbar_init(k_full + 8 * k, 1);
-      mbar_init(k_empty + 8 * k, nq);  // released by every tile's QK^T
-      mbar_init(v_full + 8 * k, 1);
+      mbar_init(k_full + 8 * k, KV8 ? 128 : 1);  // E4M3: the 128 threads of the converting warpgroup
+      mbar_init(k_empty + 8 * k, nq);            // released by every tile's QK^T
+      mbar_init(v_full + 8 * k, KV8 ? 128 : 1);
       mbar_init(v_empty + 8 * k, nq);
     }
     for (int f = 0; f < UM_FS; ++f) {
       mbar_init(sk_full + 8 * f, 1);
       mbar_init(sv_full + 8 * f, 1);
+      mbar_init(sk_free + 8 * f, 128);
+      mbar_init(sv_free + 8 * f, 128);
     }
     mbar_init(q_ready, nq);
     for (int i = 0; i < 4; ++i) {
@@ -506,32 +509,11 @@ __global__ void __launch_bounds__(UM_THREADS, 1) prefill_umma_kernel(const __gri
       }
       const uint32_t full0 = kw ? k_full : v_full, empty0 = kw ? k_empty : v_empty;
       if constexpr (KV8) {
-        // E4M3 pool: lane i < 4 copies slab i of a 64-key tile (one 2 KB box of codes, 128-byte
-        // swizzle) into a staging ring; the warp converts each tile to binary16 in the operand
-        // layout of the 16-bit path and zeroes the V rows past the sequence end.
-        const uint32_t sfull0 = kw ? sk_full : sv_full;
+        // E4M3 pool: lane i < 4 copies slab i of a 64-key tile of codes (one 2 KB box, 128-byte
+        // swizzle) into a staging ring; a softmax warpgroup converts it (see there)
+        const uint32_t sfull0 = kw ? sk_full : sv_full, sfree0 = kw ? sk_free : sv_free;
         const int stg = stg_off + (kw ? 0 : UM_FS * UM_STG_BYTES);
         const CUtensorMap* map = kw ? &tmk : &tmv3;
-        auto issue = [&](int j) {
-          int row = 0;
-          const int t0 = j * UM_KEYS + lane * TILE;
-          if (lane < UM_SLABS && t0 < nkeys) {
-            const int lb = t0 / a.B;
-            const int blk = tbl_in_smem ? tbl[lb] : block_at(lb);
-            row = ((blk * a.L + a.layer) * a.H_kv + g) * a.B + (t0 - lb * a.B);
-          }
-          const int nv = min(UM_SLABS, (nkeys - j * UM_KEYS + TILE - 1) / TILE);
-          const uint32_t bar = sfull0 + 8 * (j % UM_FS);
-          if (lane == 0) {
-            fence_proxy_async();  // this warp's reads of the slot come before the copy overwrites it
-            mbar_arrive_expect_tx(bar, nv * TILE * 128);
-          }
-          __syncwarp();
-          if (lane < nv) tma_load_2d(qs + stg + (j % UM_FS) * UM_STG_BYTES + lane * TILE * 128, map, 0, row, bar);
-        };
-        issue(0);
-        if (nt > 1) issue(1);
-        int issued = min(nt, UM_FS);
         bool ok = true;
         // q of this warp's tile (warp 8: A, warp 10: B) to binary16 in place once it has landed
         const int xq = kw ? 0 : 1;
@@ -550,44 +532,25 @@ __global__ void __launch_bounds__(UM_THREADS, 1) prefill_umma_kernel(const __gri
             if (lane == 0) mbar_arrive(q_ready);
           }
         }
+        int issued = 0;
         for (int j = 0; j < nt && ok; ++j) {
-          const int slot = j % KS, f = j % UM_FS;
+          int row = 0;
+          const int t0 = j * UM_KEYS + lane * TILE;
+          if (lane < UM_SLABS && t0 < nkeys) {
+            const int lb = t0 / a.B;
+            const int blk = tbl_in_smem ? tbl[lb] : block_at(lb);
+            row = ((blk * a.L + a.layer) * a.H_kv + g) * a.B + (t0 - lb * a.B);
+          }
+          const int nv = min(UM_SLABS, (nkeys - j * UM_KEYS + TILE - 1) / TILE);
+          const int f = j % UM_FS;
           if (lane == 0) {
-            ok = wait(sfull0 + 8 * f, (j / UM_FS) & 1, 120 + j);
-            if (ok && j >= KS) ok = wait(empty0 + 8 * slot, ((j / KS) - 1) & 1, 100 + j);
+            if (j >= UM_FS) ok = wait(sfree0 + 8 * f, ((j / UM_FS) - 1) & 1, 110 + j);
+            if (ok) mbar_arrive_expect_tx(sfull0 + 8 * f, nv * TILE * 128);
           }
-          ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+          ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;  // also orders the expect_tx before the copies
           if (!ok) break;
-          // staging row r of slab i holds d = 16 u .. 16 u + 15 in 16-byte unit u ^ (r & 7); the
-          // operand rows hold d in two 64-wide chunks of eight 16-byte units, unit t at t ^ (row & 7)
-          const uint8_t* src = base + stg + f * UM_STG_BYTES;
-          uint8_t* dst = base + 2 * UM_TILE_BYTES + ((kw ? 0 : KS) + slot) * UM_KV_BYTES;
-          const int r0 = nkeys - j * UM_KEYS;  // tile rows at or past r0 are past the sequence end
-#pragma unroll 2
-          for (int k = 0; k < UM_STG_BYTES / 16 / 32; ++k) {
-            const int idx = lane + 32 * k;
-            const int i = idx >> 7, r = (idx >> 3) & 15, u = idx & 7, R = TILE * i + r;
-            const uint4 w = *reinterpret_cast<const uint4*>(src + i * (TILE * 128) + r * 128 + ((u ^ (r & 7)) << 4));
-            uint4 o0 = make_uint4(0, 0, 0, 0), o1 = make_uint4(0, 0, 0, 0);
-            if (kw || R < r0) {
-              e4m3x4_to_f16x4(w.x, o0.x, o0.y);
-              e4m3x4_to_f16x4(w.y, o0.z, o0.w);
-              e4m3x4_to_f16x4(w.z, o1.x, o1.y);
-              e4m3x4_to_f16x4(w.w, o1.z, o1.w);
-            }
-            const int c = u >> 2, t = (u & 3) * 2, sw = R & 7;
-            // K: [chunk][64 keys][128 B]; V: [slab][chunk][16 keys][128 B]
-            uint8_t* rowp = kw ? dst + c * (UM_KEYS * 128) + R * 128 : dst + i * 4096 + c * 2048 + r * 128;
-            *reinterpret_cast<uint4*>(rowp + ((t ^ sw) << 4)) = o0;
-            *reinterpret_cast<uint4*>(rowp + (((t + 1) ^ sw) << 4)) = o1;
-          }
-          fence_proxy_async();  // the generic-proxy writes, before the tensor cores read them
-          __syncwarp();
-          if (lane == 0) mbar_arrive(full0 + 8 * slot);
-          if (j + UM_FS < nt) {
-            issue(j + UM_FS);
-            ++issued;
-          }
+          ++issued;
+          if (lane < nv) tma_load_2d(qs + stg + f * UM_STG_BYTES + lane * TILE * 128, map, 0, row, sfull0 + 8 * f);
         }
         if (*abort_flag && lane == 0) {  // copies into the staging ring may still be landing
           for (int jj = max(0, issued - UM_FS); jj < issued; ++jj) settle(sfull0 + 8 * (jj % UM_FS), (jj / UM_FS) & 1);
@@ -721,6 +684,48 @@ __global__ void __launch_bounds__(UM_THREADS, 1) prefill_umma_kernel(const __gri
       const int lim = valid ? P + qi : pmax;  // last visible key
       float m = -INFINITY, l = 0.f;
       bool ok = true;
+      // E4M3 pools: this warpgroup converts a staged tile of codes (K or V of key tile c) into
+      // the binary16 operand ring while the other warpgroup has its softmax turn.  Staging row r
+      // of slab i holds d = 16 u .. 16 u + 15 in 16-byte unit u ^ (r & 7); the operand rows hold
+      // d in two 64-wide chunks of eight 16-byte units, unit t at t ^ (row & 7).  V rows past the
+      // sequence end are written as zeros.
+      auto convert = [&](int c, bool is_k) -> bool {
+        const int f = c % UM_FS, slot = c % KS;
+        bool ok2 = wait((is_k ? sk_full : sv_full) + 8 * f, (c / UM_FS) & 1, 130 + c);
+        if (ok2 && c >= KS) ok2 = wait((is_k ? k_empty : v_empty) + 8 * slot, ((c / KS) - 1) & 1, 140 + c);
+        if (!__all_sync(0xffffffffu, ok2)) return false;
+        const uint8_t* src = base + stg_off + ((is_k ? 0 : UM_FS) + f) * UM_STG_BYTES;
+        uint8_t* dst = base + 2 * UM_TILE_BYTES + ((is_k ? 0 : KS) + slot) * UM_KV_BYTES;
+        const int r0 = nkeys - c * UM_KEYS;  // tile rows at or past r0 are past the sequence end
+#pragma unroll
+        for (int k = 0; k < UM_STG_BYTES / 16 / 128; ++k) {
+          const int idx = r + 128 * k;
+          const int i = idx >> 7, rr = (idx >> 3) & 15, u = idx & 7, R = TILE * i + rr;
+          const uint4 w = *reinterpret_cast<const uint4*>(src + i * (TILE * 128) + rr * 128 + ((u ^ (rr & 7)) << 4));
+          uint4 o0 = make_uint4(0, 0, 0, 0), o1 = make_uint4(0, 0, 0, 0);
+          if (is_k || R < r0) {
+            e4m3x4_to_f16x4(w.x, o0.x, o0.y);
+            e4m3x4_to_f16x4(w.y, o0.z, o0.w);
+            e4m3x4_to_f16x4(w.z, o1.x, o1.y);
+            e4m3x4_to_f16x4(w.w, o1.z, o1.w);
+          }
+          const int cc = u >> 2, t = (u & 3) * 2, sw = R & 7;
+          // K: [chunk][64 keys][128 B]; V: [slab][chunk][16 keys][128 B]
+          uint8_t* rowp = is_k ? dst + cc * (UM_KEYS * 128) + R * 128 : dst + i * 4096 + cc * 2048 + rr * 128;
+          *reinterpret_cast<uint4*>(rowp + ((t ^ sw) << 4)) = o0;
+          *reinterpret_cast<uint4*>(rowp + (((t + 1) ^ sw) << 4)) = o1;
+        }
+        fence_proxy_async();  // the generic-proxy writes and reads, before the async proxy's use
+        mbar_arrive((is_k ? k_full : v_full) + 8 * slot);
+        mbar_arrive((is_k ? sk_free : sv_free) + 8 * f);
+        return true;
+      };
+      // A converts K, B converts V (A both when the CTA has one tile): K(0 .. 2) and V(0, 1)
+      // first, then after its softmax of key tile j, K(j + 3) in the slot that QK^T(j) freed
+      // and V(j + 2) in the slot that P V(j - 1) freed.
+      const bool conv_k = KV8 && X == 0, conv_v = KV8 && (X == 1 || nq == 1);
+      for (int c = 0; c < min(nt, KS) && ok && conv_k; ++c) ok = convert(c, true);
+      for (int c = 0; c < min(nt, 2) && ok && conv_v; ++c) ok = convert(c, false);
       // tcgen05.ld / st are warp-collective: every decision below is uniform over the warp
       for (int j = 0; j < nt && ok; ++j) {
         const int b = j & 1;
@@ -800,6 +805,8 @@ __global__ void __launch_bounds__(UM_THREADS, 1) prefill_umma_kernel(const __gri
         tc_fence_before();
         mbar_arrive(p_full + 8 * (2 * X + b));
         if (lane == 0) mbar_arrive(turn + 8 * X);
+        if (conv_k && j + KS < nt) ok = convert(j + KS, true);
+        if (ok && conv_v && j + 2 < nt) ok = convert(j + 2, false);
       }
       if (ok) ok = __all_sync(0xffffffffu, wait(o_done + 8 * (2 * X + ((nt - 1) & 1)), ((nt - 1) >> 1) & 1, 1000));
       if (ok) {
