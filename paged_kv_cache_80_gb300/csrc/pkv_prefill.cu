@@ -301,6 +301,11 @@ __global__ void __launch_bounds__(PF_WARPS * 32, 1) prefill_tc_kernel(const __gr
 // The online softmax ("Chunked prefill mechanics": m_new = max(m, m_blk), l and O scaled by
 // e^{m - m_new}) rescales O in TMEM only when a row's max grows by more than 2^8; otherwise
 // the old max stays the reference, which is exact because P and l use the same reference.
+// E4M3 pools ("KV Cache Management", b_elem = 1): the producers copy 2 KB slabs of codes into
+// 2-deep staging rings instead, warps 8 and 10 round their tile's q to binary16 in place, and
+// the softmax warpgroups convert each staged tile into the binary16 operand rings (3 deep)
+// during the other group's turn; the products run on binary16 operands, k_scale folds into the
+// softmax scale and v_scale into the final 1 / l.
 
 // mbarrier wait that suspends the thread until the phase completes or `hint_ns` passes, so
 // that waiting warps leave the issue slots of their SM sub-partition to the softmax warps
