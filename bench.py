@@ -905,7 +905,8 @@ def run_prefill(args, torch, pkv, dev, world, rank):
         "data": "synthetic",
         "config": {"workload": f"prefill: {n} sequences x {hist:,} cached tokens, a {C}-token chunk each (forked "
                                f"histories), 64 query / 8 KV heads, d_head 128, {kv_desc(g)}, 16-token blocks",
-                   "l2": f"inputs larger than L2 ({kvb / 1e9:.2f} GB of K/V per step)",
+                   "l2": (f"inputs larger than L2 ({kvb / 1e9:.2f} GB of K/V per step)" if kvb > 129e6 else
+                          f"K/V smaller than L2 ({kvb / 1e9:.2f} GB per step), not flushed: a diagnostic size"),
                    "parallelism": "replicas (no collectives)"},
         "tokens_per_s": round(n * C / (ms / 1e3), 1),
         "roofline": {"bound": "tensor", "achieved": round(tflops, 1), "peak": peak, "unit": "TFLOP/s",
