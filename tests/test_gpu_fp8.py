@@ -153,6 +153,10 @@ def test_fp8_prefill_tensor_cores(H_q, H_kv):
     _fp8_prefill(H_q, H_kv, 128, [0, 5, 64, 1000, 37, 300, 3000], [17, 1, 100, 40, 130, 16, 512], 56, (0.1, 0.4), 400)
 
 
+def test_fp8_prefill_history_longer_than_the_staged_table():
+    _fp8_prefill(16, 2, 128, [66000, 100], [40, 200], 59, (0.1, 0.2), 4400)
+
+
 def test_fp8_prefill_on_cuda_cores():
     # d_head 64 over an E4M3 pool runs on the CUDA-core kernel
     _fp8_prefill(16, 4, 64, [100, 0, 700], [37, 16, 5], 58, (0.2, 0.3), 200)

@@ -59,6 +59,13 @@ def test_prefill_whole_prompt_is_causal_attention():
     run_prefill(g, [0, 0], [1000, 257], 83)
 
 
+def test_prefill_history_longer_than_the_staged_table():
+    # 4,128 blocks of history: more than the 4,096 table entries the tensor-core kernel stages in
+    # shared memory, so its producers read block ids from the table in global memory
+    g = W.Geometry(L=1, H_q=16, H_kv=2, d_head=128, block_size=16, dtype="bf16", num_blocks=4400)
+    run_prefill(g, [66000, 100], [40, 200], 85)
+
+
 def test_prefill_chunk_longer_than_max_q_is_recorded():
     import torch
 
