@@ -804,12 +804,16 @@ __global__ void __launch_bounds__(UM_THREADS, 1) prefill_umma_kernel(const __gri
             pw[e] = pack2<TP>(p0, p1);
           }
           tmem_st16(s_addr + 16 * c, pw);
+          // the other tile's turn starts halfway through these exponentials, so that its S load
+          // and row max (no special-function work) overlap the second half (16-bit pools; with
+          // E4M3 pools, whose softmax warpgroups also convert, at the end of the exponentials)
+          if (!KV8 && c == NC / 2 - 1 && lane == 0) mbar_arrive(turn + 8 * X);
         }
+        if (KV8 && lane == 0) mbar_arrive(turn + 8 * X);
         l += ((ls8[0] + ls8[1]) + (ls8[2] + ls8[3])) + ((ls8[4] + ls8[5]) + (ls8[6] + ls8[7]));
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(p_full + 8 * (2 * X + b));
-        if (lane == 0) mbar_arrive(turn + 8 * X);
         if (conv_k && j + KS < nt) ok = convert(j + KS, true);
         if (ok && conv_v && j + 2 < nt) ok = convert(j + 2, false);
       }
