@@ -8,7 +8,7 @@ import pytest
 import oracle
 import paged_kv_cache_80_gb300 as pkv
 import workloads as W
-from helpers import PagedBatch, check_attention, out_f64, to_dev, torch_dtype
+from helpers import PagedBatch, check_attention, out_f64, to_dev, to_raw, torch_dtype
 
 pytestmark = pytest.mark.gpu
 
@@ -81,3 +81,61 @@ def test_prefill_chunk_longer_than_max_q_is_recorded():
     with pytest.raises(pkv.PkvError) as e:
         pkv.pkv_check_device_error()
     assert "code 6" in str(e.value)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "e4m3"])
+def test_prefill_bench_size_sampled(dtype):
+    """The prefill bench's workload -- 8 sequences of 16,384 cached tokens each take a 512-token
+    chunk; 64 query / 8 KV heads, d 128; the tcgen05 kernel -- checked on sampled query rows.  A
+    chunk row attends to exactly the keys up to its own position, so the oracle's decode attention
+    over that prefix is its reference ("Chunked prefill mechanics": the chunked result equals a
+    monolithic pass).  The oracle reads host copies of the sampled sequences' blocks taken from
+    the seeded pool before any library kernel ran, with the chunk's keys/values written on the host."""
+    import torch
+
+    n, hist, C = 8, 16384, 512
+    seed = 7101
+    N = n * (hist + C) // 16 + 64
+    g = W.Geometry(L=1, H_q=64, H_kv=8, d_head=128, block_size=16, dtype=dtype, num_blocks=N)
+    kp = W.device_normal(seed, "pf_k_pool", g.pool_shape(), g.dtype, "cuda")
+    vp = W.device_normal(seed, "pf_v_pool", g.pool_shape(), g.dtype, "cuda")
+    b = PagedBatch(g, W.permutation(seed, "pf_fo", N), seed=seed, host_pool=False, fill_device=(kp, vp))
+    ids = b.new_seqs(n)
+    b.append(ids, [hist] * n, "hist", plan_only=True)  # the seeded pool holds the histories
+    slots, cows = pkv.pkv_plan_append(b.lib, ids, [C] * n)
+    oslots, ocows = b.orc.append(ids, [C] * n)
+    assert np.array_equal(slots, oslots) and len(cows) == 0
+    tables, lens = b.tables(ids)
+    sample_seqs = [0, 3, 7]
+    used = sorted({int(x) for s in sample_seqs for x in tables[s, : -(-int(lens[s]) // 16)]})
+    remap = {blk: j for j, blk in enumerate(used)}
+    idx = torch.tensor(used, dtype=torch.long, device="cuda")
+    hk = to_raw(kp.index_select(0, idx), g.dtype)
+    hv = to_raw(vp.index_select(0, idx), g.dtype)
+    a = "bf16"  # q, out and the new keys/values (bf16 also around an E4M3 pool)
+    kn = W.normal(seed, "pf_kn", (n * C, g.H_kv, g.d_head), a)
+    vn = W.normal(seed, "pf_vn", (n * C, g.H_kv, g.d_head), a)
+    pkv.pkv_append_kv(b.lib, 0, to_dev(kn, a), to_dev(vn, a), torch.from_numpy(slots).cuda(), kp, vp)
+    q = W.normal(seed, "pf_q", (n * C, g.H_q, g.d_head), a)
+    offs = np.arange(0, n * C + 1, C, dtype=np.int32)
+    out = torch.full((n * C, g.H_q, g.d_head), float("nan"), dtype=torch.bfloat16, device="cuda")
+    scale = 1.0 / math.sqrt(g.d_head)
+    pkv.pkv_prefill_attention(b.lib, 0, to_dev(q, a), torch.from_numpy(offs).cuda(), C, kp, vp,
+                              torch.from_numpy(tables).cuda(), torch.from_numpy(lens).cuda(), scale, out)
+    pkv.pkv_check_device_error()
+    got = out_f64(out, a)
+    assert np.all(np.isfinite(got))
+    gc = W.Geometry(1, g.H_q, g.H_kv, g.d_head, 16, g.dtype, len(used))
+    rows = [s * C + i for s in sample_seqs for i in range(C)]
+    cslots = np.array([remap[int(slots[r]) // 16] * 16 + int(slots[r]) % 16 for r in rows], np.int32)
+    oracle.write_slots(gc, 0, kn[rows], vn[rows], cslots, hk, hv, b.k_scale, b.v_scale)
+    samples = [(s, i) for s in sample_seqs for i in (0, 1, 17, 255, 256, 510, 511)]
+    ct = np.zeros((len(samples), tables.shape[1]), np.int32)
+    sl = np.zeros(len(samples), np.int32)
+    for k, (s, i) in enumerate(samples):
+        nb = -(-int(lens[s]) // 16)
+        ct[k, :nb] = [remap[int(x)] for x in tables[s, :nb]]
+        sl[k] = hist + i + 1
+    picked = [s * C + i for s, i in samples]
+    ref = oracle.decode_attention(gc, 0, q[picked], hk, hv, ct, sl, scale, k_scale=b.k_scale, v_scale=b.v_scale)
+    check_attention(got[picked], ref, a)
