@@ -313,13 +313,12 @@ class DecodeRunner:
         self.last_ids = ids
         k, hnp, hbuf, dmeta = self.staging.next()
         if host_inputs is not None:
-            # end to end: the public binding, inputs copied from pinned host memory
+            # end to end: the public host-buffer call; it copies the inputs from pinned host
+            # memory, runs the step and copies the result back
             q, kn, vn = self.q_e2e[:n], self.kn_e2e[:n], self.vn_e2e[:n]
-            q.copy_(host_inputs[0][t][:n], non_blocking=True)
-            kn.copy_(host_inputs[1][t][:n], non_blocking=True)
-            vn.copy_(host_inputs[2][t][:n], non_blocking=True)
-            pkv.pkv_decode_step(self.pool, 0, ids, self.Wd, q, kn, vn, self.kp, self.vp, self.scale, self.out[:n],
-                                hbuf, dmeta, self.ws, attn_events=events)
+            pkv.pkv_decode_step_host(self.pool, 0, ids, self.Wd, host_inputs[0][t][:n], host_inputs[1][t][:n],
+                                     host_inputs[2][t][:n], self.out_host[:n], q, kn, vn, self.out[:n], self.kp,
+                                     self.vp, self.scale, hbuf, dmeta, self.ws, attn_events=events)
         else:
             kp, vp, outp, wsp, wsb = self.ptrs
             h = self.handle if self.pool is self._fast_pool else self._refresh_handle()
@@ -342,7 +341,6 @@ class DecodeRunner:
             self.tokens.append(n)
             self.h2d_meta += nbytes
         if host_inputs is not None:
-            self.out_host[:n].copy_(self.out[:n], non_blocking=True)
             torch.cuda.current_stream().synchronize()  # the step's result is read on the host
             self.e2e_in_bytes += nbytes + (q.numel() + kn.numel() + vn.numel()) * self.act_bytes
             self.e2e_out_bytes += n * g.H_q * g.d_head * self.act_bytes

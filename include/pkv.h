@@ -232,6 +232,27 @@ int pkv_decode_step(pkv_pool* pool, int32_t layer, const int32_t* seq_ids, int32
                     int32_t* meta_host, int32_t* meta_dev, void* workspace, size_t ws_bytes, pkv_event_t attn_begin,
                     pkv_event_t attn_end, pkv_stream_t stream);
 
+/* pkv_decode_step with the step's inputs and result in HOST memory.  (The pages
+ * have no counterpart of this call; it is the step for callers whose per-step
+ * inputs arrive in, and whose result is read from, host memory.)  On the stream:
+ * copies q_host, k_new_host and v_new_host into the caller's device staging
+ * buffers q_dev, k_new_dev, v_new_dev (one cudaMemcpyAsync each), runs
+ * pkv_decode_step on them with out_dev as its output, then copies out_dev to
+ * out_host.  The caller synchronises the stream before reading out_host.
+ *   q_host, out_host         : host [n][H_q][d_head];
+ *   k_new_host, v_new_host   : host [n][H_kv][d_head] (the activation type: bf16
+ *                              for an E4M3 pool); page-locked for the copies to
+ *                              be asynchronous;
+ *   q_dev, k_new_dev, v_new_dev, out_dev: device buffers of at least those sizes.
+ * Every other argument is as for pkv_decode_step.  If the step's validation fails,
+ * the staging copies may already be queued (caller-owned scratch); no pool state
+ * changes. */
+int pkv_decode_step_host(pkv_pool* pool, int32_t layer, const int32_t* seq_ids, int32_t n, int32_t W,
+                         const void* q_host, const void* k_new_host, const void* v_new_host, void* out_host,
+                         void* q_dev, void* k_new_dev, void* v_new_dev, void* out_dev, void* k_pool, void* v_pool,
+                         float scale, int32_t* meta_host, int32_t* meta_dev, void* workspace, size_t ws_bytes,
+                         pkv_event_t attn_begin, pkv_event_t attn_end, pkv_stream_t stream);
+
 /* Decode attention that allocates nothing.  (The pages have no counterpart of
  * this call; it exists for callers of this library.)
  * Same arguments and result as pkv_decode_attention, minus the workspace: the

@@ -20,7 +20,7 @@ __all__ = [
     "pkv_version", "pkv_pool_create", "pkv_pool_destroy", "pkv_pool_geometry", "pkv_seq_create", "pkv_seq_fork",
     "pkv_seq_free", "pkv_seq_len", "pkv_plan_append", "pkv_export_tables", "pkv_refcounts", "pkv_free_list",
     "pkv_append_kv", "pkv_decode_workspace_size", "pkv_decode_attention", "pkv_decode_attention_noalloc",
-    "pkv_decode_step", "pkv_prefill_attention",
+    "pkv_decode_step", "pkv_decode_step_host", "pkv_prefill_attention",
     "pkv_copy_blocks", "pkv_swap_out",
     "pkv_swap_in", "pkv_seq_host_slots", "pkv_seq_residency", "TIER_HBM", "TIER_HOST", "pkv_pool_set_swap_engine", "pkv_check_device_error", "pkv_launch_count",
     "pkv_selftest_bounded_wait", "pkv_pool_set_kv_scales", "pkv_pool_kv_scales",
@@ -107,6 +107,8 @@ def _L():
                                       ctypes.c_int),
             "pkv_decode_step": ([vp, i32, P32, i32, i32, vp, vp, vp, vp, vp, ctypes.c_float, vp, vp, vp, vp,
                                  ctypes.c_size_t, vp, vp, vp], ctypes.c_int),
+            "pkv_decode_step_host": ([vp, i32, P32, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_float,
+                                      vp, vp, vp, ctypes.c_size_t, vp, vp, vp], ctypes.c_int),
             "pkv_swap_out": ([vp, i32, vp, vp, vp, i64, P64, i32, P32, vp], ctypes.c_int),
             "pkv_swap_in": ([vp, i32, vp, i64, i32, vp, vp, P32, vp], ctypes.c_int),
             "pkv_seq_host_slots": ([vp, i32, P64, i32, P32], ctypes.c_int),
@@ -406,6 +408,36 @@ def pkv_decode_step(pool: PoolLike, layer: int, seq_ids, W: int, q, k_new, v_new
                                 _dev(out, "out"), _host_ptr(meta_host, "meta_host"), _dev(meta_dev, "meta_dev"),
                                 _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(), ev0, ev1,
                                 _stream(stream)), "pkv_decode_step")
+
+
+def pkv_decode_step_host(pool: PoolLike, layer: int, seq_ids, W: int, q_host, k_new_host, v_new_host, out_host,
+                         q_dev, k_new_dev, v_new_dev, out_dev, k_pool, v_pool, scale: float, meta_host, meta_dev,
+                         workspace, attn_events=None, stream=None) -> None:
+    """pkv_decode_step with q / k_new / v_new read from, and out written to, host
+    tensors (page-locked for asynchronous copies) through the *_dev staging tensors;
+    synchronise the stream before reading out_host."""
+    ids = _i32(seq_ids)
+    n = ids.size
+    if meta_host.numel() < n * (W + 2) or meta_dev.numel() < n * (W + 2):
+        raise ValueError("metadata buffers smaller than n * (W + 2)")
+    for t, d, what in ((q_host, q_dev, "q"), (k_new_host, k_new_dev, "k_new"), (v_new_host, v_new_dev, "v_new"),
+                       (out_host, out_dev, "out")):
+        if t.numel() < n * t[0].numel() or d.numel() < n * t[0].numel():
+            raise ValueError(f"{what} buffers hold fewer than n rows")
+    ev0 = ev1 = None
+    if attn_events is not None:
+        for ev in attn_events:
+            if not ev.cuda_event:  # torch creates its CUDA event at the first record
+                ev.record()
+        ev0, ev1 = attn_events[0].cuda_event, attn_events[1].cuda_event
+    _check(_L().pkv_decode_step_host(_h(pool), layer, _p32(ids), n, W, _host_ptr(q_host, "q_host"),
+                                     _host_ptr(k_new_host, "k_new_host"), _host_ptr(v_new_host, "v_new_host"),
+                                     _host_ptr(out_host, "out_host"), _dev(q_dev, "q_dev"), _dev(k_new_dev, "k_new_dev"),
+                                     _dev(v_new_dev, "v_new_dev"), _dev(out_dev, "out_dev"), _dev(k_pool, "k_pool"),
+                                     _dev(v_pool, "v_pool"), float(scale), _host_ptr(meta_host, "meta_host"),
+                                     _dev(meta_dev, "meta_dev"), _dev(workspace, "workspace"),
+                                     workspace.numel() * workspace.element_size(), ev0, ev1, _stream(stream)),
+           "pkv_decode_step_host")
 
 
 def pkv_prefill_attention(pool: PoolLike, layer: int, q, q_offsets, max_q: int, k_pool, v_pool, block_tables,

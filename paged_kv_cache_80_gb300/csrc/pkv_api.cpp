@@ -646,4 +646,35 @@ int pkv_decode_step(pkv_pool* pool, int32_t layer, const int32_t* seq_ids, int32
   return PKV_OK;
 }
 
+int pkv_decode_step_host(pkv_pool* pool, int32_t layer, const int32_t* seq_ids, int32_t n, int32_t W,
+                         const void* q_host, const void* k_new_host, const void* v_new_host, void* out_host,
+                         void* q_dev, void* k_new_dev, void* v_new_dev, void* out_dev, void* k_pool, void* v_pool,
+                         float scale, int32_t* meta_host, int32_t* meta_dev, void* workspace, size_t ws_bytes,
+                         pkv_event_t attn_begin, pkv_event_t attn_end, pkv_stream_t stream) {
+  pkv::clear_error();
+  if (!pool || n < 0 || W <= 0) return fail(PKV_ERR_INVALID_ARG, "bad arguments to pkv_decode_step_host");
+  if (n == 0) return PKV_OK;
+  if (!q_host || !k_new_host || !v_new_host || !out_host || !q_dev || !k_new_dev || !v_new_dev || !out_dev)
+    return fail(PKV_ERR_INVALID_ARG, "NULL buffer");
+  const pkv_geometry& g = as_pool(pool)->geo;
+  const size_t ab = static_cast<size_t>(pkv::act_size(g.dtype));
+  const size_t qb = ab * n * g.H_q * g.d_head, kb = ab * n * g.H_kv * g.d_head;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const struct {
+    void* dst;
+    const void* src;
+    size_t bytes;
+  } in[3] = {{q_dev, q_host, qb}, {k_new_dev, k_new_host, kb}, {v_new_dev, v_new_host, kb}};
+  for (const auto& c : in) {
+    const cudaError_t e = cudaMemcpyAsync(c.dst, c.src, c.bytes, cudaMemcpyHostToDevice, st);
+    if (e != cudaSuccess) return fail(PKV_ERR_CUDA, std::string("cudaMemcpyAsync (step input): ") + cudaGetErrorString(e));
+  }
+  if (int rc = pkv_decode_step(pool, layer, seq_ids, n, W, q_dev, k_new_dev, v_new_dev, k_pool, v_pool, scale, out_dev,
+                               meta_host, meta_dev, workspace, ws_bytes, attn_begin, attn_end, stream))
+    return rc;
+  const cudaError_t e = cudaMemcpyAsync(out_host, out_dev, qb, cudaMemcpyDeviceToHost, st);
+  if (e != cudaSuccess) return fail(PKV_ERR_CUDA, std::string("cudaMemcpyAsync (step result): ") + cudaGetErrorString(e));
+  return PKV_OK;
+}
+
 }  // extern "C"

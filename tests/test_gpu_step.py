@@ -72,3 +72,46 @@ def test_decode_step_rejects_a_narrow_table_without_change():
     assert e.value.name == "PKV_ERR_INVALID_ARG"
     assert np.array_equal(before[0], pkv.pkv_refcounts(b.lib)) and np.array_equal(before[1], pkv.pkv_free_list(b.lib))
     assert pkv.pkv_seq_len(b.lib, ids[0]) == 32
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "e4m3"])
+def test_decode_step_host_buffers_match_oracle(dtype):
+    """pkv_decode_step_host: inputs in page-locked host memory, result copied back by the call."""
+    import torch
+
+    g = W.Geometry(L=1, H_q=64, H_kv=8, d_head=128, block_size=16, dtype=dtype, num_blocks=256)
+    b = PagedBatch(g, W.permutation(43, "fo", g.num_blocks), seed=43,
+                   kv_scales=(0.5, 0.25) if dtype == "e4m3" else (1.0, 1.0))
+    ids = b.new_seqs(5)
+    b.append(ids, [15, 16, 100, 0, 333], "prompt")
+    kid = b.fork(ids[2])
+    run = np.array(ids + [kid], np.int32)
+    n, Wd = len(run), 24
+    meta_host = torch.zeros(n * (Wd + 2), dtype=torch.int32).pin_memory()
+    meta_dev = torch.zeros(n * (Wd + 2), dtype=torch.int32, device="cuda")
+    ws = torch.empty(pkv.pkv_decode_workspace_size(b.lib, n), dtype=torch.uint8, device="cuda")
+    q_dev = torch.empty((n, g.H_q, g.d_head), dtype=torch.bfloat16, device="cuda")
+    k_dev = torch.empty((n, g.H_kv, g.d_head), dtype=torch.bfloat16, device="cuda")
+    v_dev = torch.empty_like(k_dev)
+    o_dev = torch.empty_like(q_dev)
+    scale = 1.0 / math.sqrt(g.d_head)
+    for step in range(3):
+        q = W.normal(43, f"q{step}", (n, g.H_q, g.d_head), "bf16")
+        kn = W.normal(43, f"k{step}", (n, g.H_kv, g.d_head), "bf16")
+        vn = W.normal(43, f"v{step}", (n, g.H_kv, g.d_head), "bf16")
+        pin = lambda x: torch.from_numpy(x.copy()).pin_memory()
+        out_host = torch.full((n, g.H_q, g.d_head), float("nan"), dtype=torch.bfloat16).pin_memory()
+        pkv.pkv_decode_step_host(b.lib, 0, run, Wd, pin(q).view(torch.bfloat16), pin(kn).view(torch.bfloat16),
+                                 pin(vn).view(torch.bfloat16), out_host, q_dev, k_dev, v_dev, o_dev, b.kp, b.vp, scale,
+                                 meta_host, meta_dev, ws)
+        torch.cuda.synchronize()
+        oslots, ocows = b.orc.append(run.tolist(), [1] * n)
+        if len(ocows):
+            oracle.copy_blocks(g, ocows, b.hk, b.hv)
+        oracle.write_slots(g, 0, kn, vn, oslots, b.hk, b.hv, b.k_scale, b.v_scale)
+        pkv.pkv_check_device_error()
+        tables, lens = b.tables(run.tolist(), Wd)
+        ref = b.decode_ref(q, tables, lens, scale)
+        check_attention(out_host.double().numpy(), ref, "bf16")
+        b.check_state()
+    b.check_pools_bitexact()
