@@ -146,7 +146,7 @@ def _fp8_prefill(H_q, H_kv, d, history, chunks, seed, scales, num_blocks):
     check_attention(out_f64(out, "bf16"), ref, "bf16")
 
 
-@pytest.mark.parametrize("H_q,H_kv", [(64, 8), (16, 4), (48, 4), (8, 8)])
+@pytest.mark.parametrize("H_q,H_kv", [(64, 8), (16, 4), (48, 4), (8, 8), (128, 8)])
 def test_fp8_prefill_tensor_cores(H_q, H_kv):
     # d_head 128: tcgen05 kernel on binary16 operands converted from the codes in shared memory;
     # ragged chunks (one query, a 16-query tile, 512), empty and long histories, ragged tails

@@ -41,6 +41,8 @@ def run_prefill(g, history, chunks, seed, max_q=None, free_order=None):
     (32, 8, 128, 16, "bf16"),   # G = 4
     (8, 8, 128, 32, "bf16"),    # G = 1, B = 32
     (48, 4, 128, 16, "bf16"),   # G = 12: rows of a warp span queries
+    (128, 8, 128, 16, "bf16"),  # G = 16: 8 queries per 128-row tile
+    (64, 1, 128, 16, "bf16"),   # G = 64 (one KV head): 2 queries per tile
     (12, 12, 64, 16, "f32"),    # CUDA-core path
     (16, 2, 96, 16, "bf16"),    # CUDA-core path
 ])
