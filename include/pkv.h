@@ -287,9 +287,11 @@ int pkv_decode_attention_noalloc(const pkv_pool* pool, int32_t layer, const void
  *   max_q      : host int, >= every C_s (a longer chunk records code 6 in the device
  *                error word and its extra rows are not computed).
  *   block_tables, W, seq_lens: as for pkv_decode_attention (C_s <= len_s <= W*B).
- * bf16/f16 with d_head 64 or 128 and B a multiple of 16 run on tensor cores (one CTA
- * per 128 (query, head) rows, 64-key tiles staged by TMA); other geometries, and FP8
- * pools, on CUDA cores.  No workspace. */
+ * bf16/f16 and FP8 (E4M3) pools with d_head 128 and B a multiple of 16 run on the
+ * 5th-generation tensor cores (tcgen05, TMEM accumulators; one CTA per 2 x 128
+ * (query, head) rows, 64-key tiles staged by TMA; E4M3 codes are converted to
+ * binary16 in shared memory and q is rounded to binary16); bf16/f16 with d_head 64 on
+ * mma.sync tensor cores; other geometries on CUDA cores.  No workspace. */
 int pkv_prefill_attention(const pkv_pool* pool, int32_t layer, const void* q, const int32_t* q_offsets, int32_t n_tok,
                           int32_t max_q, const void* k_pool, const void* v_pool, const int32_t* block_tables, int32_t W,
                           const int32_t* seq_lens, int32_t n_seq, float scale, void* out, pkv_stream_t stream);
