@@ -303,8 +303,8 @@ class DecodeRunner:
             b.record()
         return evs
 
-    def step(self, t: int, timed: bool = False, host_inputs=None, events=None):
-        """Plan, CoW copy, append and attend through one pkv_decode_step call."""
+    def step(self, t: int, timed: bool = False, events=None):
+        """Plan, CoW copy, append and attend through one pkv_decode_step call (device inputs)."""
         torch, pkv, g = self.torch, self.pkv, self.g
         ids = self.running(t)
         n = len(ids)
@@ -312,23 +312,15 @@ class DecodeRunner:
             return
         self.last_ids = ids
         k, hnp, hbuf, dmeta = self.staging.next()
-        if host_inputs is not None:
-            # end to end: the public host-buffer call; it copies the inputs from pinned host
-            # memory, runs the step and copies the result back
-            q, kn, vn = self.q_e2e[:n], self.kn_e2e[:n], self.vn_e2e[:n]
-            pkv.pkv_decode_step_host(self.pool, 0, ids, self.Wd, host_inputs[0][t][:n], host_inputs[1][t][:n],
-                                     host_inputs[2][t][:n], self.out_host[:n], q, kn, vn, self.out[:n], self.kp,
-                                     self.vp, self.scale, hbuf, dmeta, self.ws, attn_events=events)
-        else:
-            kp, vp, outp, wsp, wsb = self.ptrs
-            h = self.handle if self.pool is self._fast_pool else self._refresh_handle()
-            rc = self.raw_step(h, 0, ids.ctypes.data, n, self.Wd, self.q_base + t * self.q_stride,
-                               self.k_base + t * self.k_stride, self.v_base + t * self.v_stride, kp, vp,
-                               self.scale, outp, hbuf.data_ptr(), dmeta.data_ptr(), wsp, wsb,
-                               events[0].cuda_event if events else None, events[1].cuda_event if events else None,
-                               self.stream)
-            if rc:
-                pkv._check(rc, "pkv_decode_step")
+        kp, vp, outp, wsp, wsb = self.ptrs
+        h = self.handle if self.pool is self._fast_pool else self._refresh_handle()
+        rc = self.raw_step(h, 0, ids.ctypes.data, n, self.Wd, self.q_base + t * self.q_stride,
+                           self.k_base + t * self.k_stride, self.v_base + t * self.v_stride, kp, vp,
+                           self.scale, outp, hbuf.data_ptr(), dmeta.data_ptr(), wsp, wsb,
+                           events[0].cuda_event if events else None, events[1].cuda_event if events else None,
+                           self.stream)
+        if rc:
+            pkv._check(rc, "pkv_decode_step")
         nbytes = self.staging.mark(k, n * (self.Wd + 2))
         if timed:
             self.decode_ms.append(events)
@@ -340,11 +332,55 @@ class DecodeRunner:
             self.alg_bytes.append(kvb + qo + n * self.Wd * 4 + n * 4)
             self.tokens.append(n)
             self.h2d_meta += nbytes
-        if host_inputs is not None:
+        self.after_step(t, ids)
+
+    def e2e_steps(self, host, t0: int, steps: int, events=None, timed: bool = False):
+        """End to end through the public host-buffer calls: each step's inputs come from pinned
+        host memory and its result is read on the host before the next step's inputs are
+        sent.  The host half of step t + 1 (pkv_step_plan: slots, tables, CoW pairs -- it needs
+        no result of step t) runs while step t is on the GPU, as a serving loop's scheduler
+        does; the device half (pkv_step_launch_host) copies the inputs in, runs the step and
+        copies the result out."""
+        torch, pkv, g = self.torch, self.pkv, self.g
+
+        def plan(t):
+            ids = self.running(t)
+            if len(ids) == 0:
+                return None
+            k, hnp, hbuf, dmeta = self.staging.next()
+            cows = pkv.pkv_step_plan(self.pool, ids, self.Wd, hbuf)
+            return ids, self.pool, k, hnp, hbuf, dmeta, cows
+
+        nxt = plan(t0)
+        for i in range(steps):
+            t = t0 + i
+            cur, nxt = nxt, None
+            if cur is not None:
+                ids, pool, k, hnp, hbuf, dmeta, cows = cur
+                n = len(ids)
+                q, kn, vn = self.q_e2e[:n], self.kn_e2e[:n], self.vn_e2e[:n]
+                pkv.pkv_step_launch_host(pool, 0, n, self.Wd, cows, host[0][t][:n], host[1][t][:n], host[2][t][:n],
+                                         self.out_host[:n], q, kn, vn, self.out[:n], self.kp, self.vp, self.scale,
+                                         hbuf, dmeta, self.ws, attn_events=events[i] if events else None)
+                nbytes = self.staging.mark(k, n * (self.Wd + 2))
+                self.pool = pool
+                self.after_step(t, ids)
+            if i + 1 < steps:
+                nxt = plan(t + 1)  # the next step's host half, while this step runs
             torch.cuda.current_stream().synchronize()  # the step's result is read on the host
+            if cur is None:
+                continue
+            self.last_ids = ids
+            if timed:
+                self.decode_ms.append(events[i])
+                lens = hnp[n + n * self.Wd:n + n * self.Wd + n]
+                kvb = int(lens.sum(dtype=np.int64)) * g.H_kv * g.d_head * g.elem_bytes * 2
+                self.kv_bytes.append(kvb)
+                self.alg_bytes.append(kvb + 2 * n * g.H_q * g.d_head * self.act_bytes + n * self.Wd * 4 + n * 4)
+                self.tokens.append(n)
+                self.h2d_meta += nbytes
             self.e2e_in_bytes += nbytes + (q.numel() + kn.numel() + vn.numel()) * self.act_bytes
             self.e2e_out_bytes += n * g.H_q * g.d_head * self.act_bytes
-        self.after_step(t, ids)
 
     def _refresh_handle(self):
         self._fast_pool = self.pool
@@ -585,8 +621,7 @@ def run_decode(args, torch, pkv, dev, world, rank):
     # end to end: inputs from pinned host memory each step, result read back each step
     host = r.prepare_e2e()
     t0 = args.warmup + args.steps
-    for t in range(t0, t0 + 2):
-        r.step(t, host_inputs=host)
+    r.e2e_steps(host, t0, 2)
     r.e2e_in_bytes = r.e2e_out_bytes = 0
     kv_before = len(r.kv_bytes)
     barrier(world)
@@ -594,8 +629,7 @@ def run_decode(args, torch, pkv, dev, world, rank):
     evs2 = r.make_events(args.steps)
     torch.cuda.synchronize()
     h0 = time.perf_counter()
-    for i, t in enumerate(range(t0 + 2, t0 + 2 + args.steps)):
-        r.step(t, timed=True, host_inputs=host, events=evs2[i])
+    r.e2e_steps(host, t0 + 2, args.steps, events=evs2, timed=True)
     torch.cuda.synchronize()
     e2e_s = reduce_max(torch, world, (time.perf_counter() - h0) * 1e3) / 1e3
     e2e_kv = sum(r.kv_bytes[kv_before:])

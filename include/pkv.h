@@ -232,6 +232,34 @@ int pkv_decode_step(pkv_pool* pool, int32_t layer, const int32_t* seq_ids, int32
                     int32_t* meta_host, int32_t* meta_dev, void* workspace, size_t ws_bytes, pkv_event_t attn_begin,
                     pkv_event_t attn_end, pkv_stream_t stream);
 
+/* pkv_decode_step in two halves, so that a caller can plan step t + 1 on the host
+ * while step t runs on the GPU (the plan of a step needs no result of the previous
+ * one).  (The pages have no counterpart of these calls.)
+ * pkv_step_plan: the host half -- checks the sequences as pkv_decode_step does, then
+ *   plans one new token per sequence (pkv_plan_append) and writes the slot mapping,
+ *   tables and lengths into meta_host (host int32 [n * (W + 2)], as for
+ *   pkv_decode_step) and the copy-on-write pairs into cow_pairs (host int32 [2 n];
+ *   their count in *n_cow).  On failure nothing changes.
+ * pkv_step_launch: the device half, on the stream: copies meta_host to meta_dev,
+ *   copies the shared blocks, appends k_new / v_new at the planned slots and attends
+ *   (arguments as for pkv_decode_step; n, W, cow_pairs and meta_host from the plan,
+ *   meta_host page-locked and untouched until the copy has run).  Its argument
+ *   errors do not undo the plan.
+ * pkv_step_launch_host: pkv_step_launch with q / k_new / v_new read from, and out
+ *   written to, host memory through the caller's device staging buffers, as for
+ *   pkv_decode_step_host. */
+int pkv_step_plan(pkv_pool* pool, const int32_t* seq_ids, int32_t n, int32_t W, int32_t* meta_host,
+                  int32_t* cow_pairs, int32_t* n_cow);
+int pkv_step_launch(pkv_pool* pool, int32_t layer, int32_t n, int32_t W, const int32_t* cow_pairs, int32_t n_cow,
+                    const void* q, const void* k_new, const void* v_new, void* k_pool, void* v_pool, float scale,
+                    void* out, const int32_t* meta_host, int32_t* meta_dev, void* workspace, size_t ws_bytes,
+                    pkv_event_t attn_begin, pkv_event_t attn_end, pkv_stream_t stream);
+int pkv_step_launch_host(pkv_pool* pool, int32_t layer, int32_t n, int32_t W, const int32_t* cow_pairs,
+                         int32_t n_cow, const void* q_host, const void* k_new_host, const void* v_new_host,
+                         void* out_host, void* q_dev, void* k_new_dev, void* v_new_dev, void* out_dev, void* k_pool,
+                         void* v_pool, float scale, const int32_t* meta_host, int32_t* meta_dev, void* workspace,
+                         size_t ws_bytes, pkv_event_t attn_begin, pkv_event_t attn_end, pkv_stream_t stream);
+
 /* pkv_decode_step with the step's inputs and result in HOST memory.  (The pages
  * have no counterpart of this call; it is the step for callers whose per-step
  * inputs arrive in, and whose result is read from, host memory.)  On the stream:

@@ -20,7 +20,8 @@ __all__ = [
     "pkv_version", "pkv_pool_create", "pkv_pool_destroy", "pkv_pool_geometry", "pkv_seq_create", "pkv_seq_fork",
     "pkv_seq_free", "pkv_seq_len", "pkv_plan_append", "pkv_export_tables", "pkv_refcounts", "pkv_free_list",
     "pkv_append_kv", "pkv_decode_workspace_size", "pkv_decode_attention", "pkv_decode_attention_noalloc",
-    "pkv_decode_step", "pkv_decode_step_host", "pkv_prefill_attention",
+    "pkv_decode_step", "pkv_decode_step_host", "pkv_step_plan", "pkv_step_launch", "pkv_step_launch_host",
+    "pkv_prefill_attention",
     "pkv_copy_blocks", "pkv_swap_out",
     "pkv_swap_in", "pkv_seq_host_slots", "pkv_seq_residency", "TIER_HBM", "TIER_HOST", "pkv_pool_set_swap_engine", "pkv_check_device_error", "pkv_launch_count",
     "pkv_selftest_bounded_wait", "pkv_pool_set_kv_scales", "pkv_pool_kv_scales",
@@ -109,6 +110,11 @@ def _L():
                                  ctypes.c_size_t, vp, vp, vp], ctypes.c_int),
             "pkv_decode_step_host": ([vp, i32, P32, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_float,
                                       vp, vp, vp, ctypes.c_size_t, vp, vp, vp], ctypes.c_int),
+            "pkv_step_plan": ([vp, P32, i32, i32, vp, P32, P32], ctypes.c_int),
+            "pkv_step_launch": ([vp, i32, i32, i32, P32, i32, vp, vp, vp, vp, vp, ctypes.c_float, vp, vp, vp, vp,
+                                 ctypes.c_size_t, vp, vp, vp], ctypes.c_int),
+            "pkv_step_launch_host": ([vp, i32, i32, i32, P32, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                      ctypes.c_float, vp, vp, vp, ctypes.c_size_t, vp, vp, vp], ctypes.c_int),
             "pkv_swap_out": ([vp, i32, vp, vp, vp, i64, P64, i32, P32, vp], ctypes.c_int),
             "pkv_swap_in": ([vp, i32, vp, i64, i32, vp, vp, P32, vp], ctypes.c_int),
             "pkv_seq_host_slots": ([vp, i32, P64, i32, P32], ctypes.c_int),
@@ -438,6 +444,57 @@ def pkv_decode_step_host(pool: PoolLike, layer: int, seq_ids, W: int, q_host, k_
                                      _dev(meta_dev, "meta_dev"), _dev(workspace, "workspace"),
                                      workspace.numel() * workspace.element_size(), ev0, ev1, _stream(stream)),
            "pkv_decode_step_host")
+
+
+def pkv_step_plan(pool: PoolLike, seq_ids, W: int, meta_host) -> np.ndarray:
+    """The host half of a decode step: plan one token per sequence into meta_host
+    (pinned int32, >= n*(W+2)); returns the copy-on-write pairs [n_cow][2]."""
+    ids = _i32(seq_ids)
+    n = ids.size
+    if meta_host.numel() < n * (W + 2):
+        raise ValueError("meta_host smaller than n * (W + 2)")
+    cows = np.zeros(max(2 * n, 2), np.int32)
+    n_cow = ctypes.c_int32(0)
+    _check(_L().pkv_step_plan(_h(pool), _p32(ids), n, W, _host_ptr(meta_host, "meta_host"), _p32(cows),
+                              ctypes.byref(n_cow)), "pkv_step_plan")
+    return cows[: 2 * n_cow.value].reshape(-1, 2)
+
+
+def _events(attn_events):
+    if attn_events is None:
+        return None, None
+    for ev in attn_events:
+        if not ev.cuda_event:  # torch creates its CUDA event at the first record
+            ev.record()
+    return attn_events[0].cuda_event, attn_events[1].cuda_event
+
+
+def pkv_step_launch(pool: PoolLike, layer: int, n: int, W: int, cow_pairs, q, k_new, v_new, k_pool, v_pool,
+                    scale: float, out, meta_host, meta_dev, workspace, attn_events=None, stream=None) -> None:
+    """The device half of a decode step planned by pkv_step_plan (device q / k_new / v_new / out)."""
+    cp = _i32(cow_pairs).reshape(-1)
+    ev0, ev1 = _events(attn_events)
+    _check(_L().pkv_step_launch(_h(pool), layer, n, W, _p32(cp), cp.size // 2, _dev(q, "q"), _dev(k_new, "k_new"),
+                                _dev(v_new, "v_new"), _dev(k_pool, "k_pool"), _dev(v_pool, "v_pool"), float(scale),
+                                _dev(out, "out"), _host_ptr(meta_host, "meta_host"), _dev(meta_dev, "meta_dev"),
+                                _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(), ev0, ev1,
+                                _stream(stream)), "pkv_step_launch")
+
+
+def pkv_step_launch_host(pool: PoolLike, layer: int, n: int, W: int, cow_pairs, q_host, k_new_host, v_new_host,
+                         out_host, q_dev, k_new_dev, v_new_dev, out_dev, k_pool, v_pool, scale: float, meta_host,
+                         meta_dev, workspace, attn_events=None, stream=None) -> None:
+    """pkv_step_launch with host input and result tensors (page-locked) copied inside the call."""
+    cp = _i32(cow_pairs).reshape(-1)
+    ev0, ev1 = _events(attn_events)
+    _check(_L().pkv_step_launch_host(_h(pool), layer, n, W, _p32(cp), cp.size // 2, _host_ptr(q_host, "q_host"),
+                                     _host_ptr(k_new_host, "k_new_host"), _host_ptr(v_new_host, "v_new_host"),
+                                     _host_ptr(out_host, "out_host"), _dev(q_dev, "q_dev"), _dev(k_new_dev, "k_new_dev"),
+                                     _dev(v_new_dev, "v_new_dev"), _dev(out_dev, "out_dev"), _dev(k_pool, "k_pool"),
+                                     _dev(v_pool, "v_pool"), float(scale), _host_ptr(meta_host, "meta_host"),
+                                     _dev(meta_dev, "meta_dev"), _dev(workspace, "workspace"),
+                                     workspace.numel() * workspace.element_size(), ev0, ev1, _stream(stream)),
+           "pkv_step_launch_host")
 
 
 def pkv_prefill_attention(pool: PoolLike, layer: int, q, q_offsets, max_q: int, k_pool, v_pool, block_tables,

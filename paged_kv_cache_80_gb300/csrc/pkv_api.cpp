@@ -596,19 +596,11 @@ int pkv_seq_host_slots(const pkv_pool* pool, int32_t seq, int64_t* out, int32_t 
   return PKV_OK;
 }
 
-int pkv_decode_step(pkv_pool* pool, int32_t layer, const int32_t* seq_ids, int32_t n, int32_t W, const void* q,
-                    const void* k_new, const void* v_new, void* k_pool, void* v_pool, float scale, void* out,
-                    int32_t* meta_host, int32_t* meta_dev, void* workspace, size_t ws_bytes, pkv_event_t attn_begin,
-                    pkv_event_t attn_end, pkv_stream_t stream) {
-  pkv::clear_error();
-  if (!pool || n < 0 || W <= 0) return fail(PKV_ERR_INVALID_ARG, "bad arguments to pkv_decode_step");
-  if (n == 0) return PKV_OK;
-  if (!seq_ids || !q || !k_new || !v_new || !k_pool || !v_pool || !out || !meta_host || !meta_dev || !workspace)
-    return fail(PKV_ERR_INVALID_ARG, "NULL buffer");
-  Pool& P = *as_pool(pool);
-  const Pool& CP = P;
-  if (layer < 0 || layer >= P.geo.L) return fail(PKV_ERR_INVALID_ARG, "layer out of range");
-  const int64_t B = P.geo.block_size;
+// The checks pkv_decode_step makes before anything changes: resident, unswapped sequences whose
+// tables still fit W after one more token.
+static int step_check(pkv_pool* pool, const int32_t* seq_ids, int32_t n, int32_t W) {
+  const Pool& CP = *as_pool(pool);
+  const int64_t B = CP.geo.block_size;
   for (int32_t i = 0; i < n; ++i) {
     const SeqState* s = find_seq(CP, seq_ids[i]);
     if (!s) return unknown_seq(CP, seq_ids[i]);
@@ -617,25 +609,51 @@ int pkv_decode_step(pkv_pool* pool, int32_t layer, const int32_t* seq_ids, int32
       return fail(PKV_ERR_INVALID_ARG, "W = " + std::to_string(W) + " cannot hold sequence " +
                                            std::to_string(seq_ids[i]) + " after the step");
   }
-  size_t need = 0;
-  if (int rc = pkv::decode_workspace_bytes(P, n, &need)) return rc;
-  if (ws_bytes < need) return fail(PKV_ERR_INVALID_ARG, "workspace too small: need " + std::to_string(need));
+  return PKV_OK;
+}
 
-  static thread_local std::vector<int32_t> ones, cows;
+static int step_workspace_check(pkv_pool* pool, int32_t n, size_t ws_bytes) {
+  size_t need = 0;
+  if (int rc = pkv::decode_workspace_bytes(*as_pool(pool), n, &need)) return rc;
+  if (ws_bytes < need) return fail(PKV_ERR_INVALID_ARG, "workspace too small: need " + std::to_string(need));
+  return PKV_OK;
+}
+
+int pkv_step_plan(pkv_pool* pool, const int32_t* seq_ids, int32_t n, int32_t W, int32_t* meta_host,
+                  int32_t* cow_pairs, int32_t* n_cow) {
+  pkv::clear_error();
+  if (!pool || n < 0 || W <= 0 || !n_cow) return fail(PKV_ERR_INVALID_ARG, "bad arguments to pkv_step_plan");
+  *n_cow = 0;
+  if (n == 0) return PKV_OK;
+  if (!seq_ids || !meta_host || !cow_pairs) return fail(PKV_ERR_INVALID_ARG, "NULL buffer");
+  if (int rc = step_check(pool, seq_ids, n, W)) return rc;
+  static thread_local std::vector<int32_t> ones;
   if (static_cast<int32_t>(ones.size()) < n) ones.assign(n, 1);
-  if (static_cast<int32_t>(cows.size()) < 2 * n) cows.resize(2 * n);
-  int32_t n_cow = 0;
   int32_t* slots = meta_host;
   int32_t* tables = meta_host + n;
   int32_t* lens = meta_host + n + static_cast<int64_t>(n) * W;
-  if (int rc = pkv_plan_append(pool, seq_ids, ones.data(), n, slots, cows.data(), &n_cow)) return rc;
-  if (int rc = pkv_export_tables(pool, seq_ids, n, tables, W, lens)) return rc;
+  if (int rc = pkv_plan_append(pool, seq_ids, ones.data(), n, slots, cow_pairs, n_cow)) return rc;
+  return pkv_export_tables(pool, seq_ids, n, tables, W, lens);
+}
+
+int pkv_step_launch(pkv_pool* pool, int32_t layer, int32_t n, int32_t W, const int32_t* cow_pairs, int32_t n_cow,
+                    const void* q, const void* k_new, const void* v_new, void* k_pool, void* v_pool, float scale,
+                    void* out, const int32_t* meta_host, int32_t* meta_dev, void* workspace, size_t ws_bytes,
+                    pkv_event_t attn_begin, pkv_event_t attn_end, pkv_stream_t stream) {
+  pkv::clear_error();
+  if (!pool || n < 0 || W <= 0 || n_cow < 0) return fail(PKV_ERR_INVALID_ARG, "bad arguments to pkv_step_launch");
+  if (n == 0) return PKV_OK;
+  if (!q || !k_new || !v_new || !k_pool || !v_pool || !out || !meta_host || !meta_dev || !workspace ||
+      (n_cow > 0 && !cow_pairs))
+    return fail(PKV_ERR_INVALID_ARG, "NULL buffer");
+  if (layer < 0 || layer >= as_pool(pool)->geo.L) return fail(PKV_ERR_INVALID_ARG, "layer out of range");
+  if (int rc = step_workspace_check(pool, n, ws_bytes)) return rc;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const size_t meta_bytes = sizeof(int32_t) * static_cast<size_t>(n) * (W + 2);
   cudaError_t e = cudaMemcpyAsync(meta_dev, meta_host, meta_bytes, cudaMemcpyHostToDevice, st);
   if (e != cudaSuccess) return fail(PKV_ERR_CUDA, std::string("cudaMemcpyAsync (step metadata): ") + cudaGetErrorString(e));
   if (n_cow > 0)
-    if (int rc = pkv_copy_blocks(pool, cows.data(), n_cow, k_pool, v_pool, stream)) return rc;
+    if (int rc = pkv_copy_blocks(pool, cow_pairs, n_cow, k_pool, v_pool, stream)) return rc;
   if (int rc = pkv_append_kv(pool, layer, k_new, v_new, meta_dev, n, k_pool, v_pool, stream)) return rc;
   if (attn_begin) cudaEventRecord(reinterpret_cast<cudaEvent_t>(attn_begin), st);
   if (int rc = pkv_decode_attention(pool, layer, q, k_pool, v_pool, meta_dev + n, W,
@@ -646,13 +664,13 @@ int pkv_decode_step(pkv_pool* pool, int32_t layer, const int32_t* seq_ids, int32
   return PKV_OK;
 }
 
-int pkv_decode_step_host(pkv_pool* pool, int32_t layer, const int32_t* seq_ids, int32_t n, int32_t W,
-                         const void* q_host, const void* k_new_host, const void* v_new_host, void* out_host,
-                         void* q_dev, void* k_new_dev, void* v_new_dev, void* out_dev, void* k_pool, void* v_pool,
-                         float scale, int32_t* meta_host, int32_t* meta_dev, void* workspace, size_t ws_bytes,
-                         pkv_event_t attn_begin, pkv_event_t attn_end, pkv_stream_t stream) {
+int pkv_step_launch_host(pkv_pool* pool, int32_t layer, int32_t n, int32_t W, const int32_t* cow_pairs,
+                         int32_t n_cow, const void* q_host, const void* k_new_host, const void* v_new_host,
+                         void* out_host, void* q_dev, void* k_new_dev, void* v_new_dev, void* out_dev, void* k_pool,
+                         void* v_pool, float scale, const int32_t* meta_host, int32_t* meta_dev, void* workspace,
+                         size_t ws_bytes, pkv_event_t attn_begin, pkv_event_t attn_end, pkv_stream_t stream) {
   pkv::clear_error();
-  if (!pool || n < 0 || W <= 0) return fail(PKV_ERR_INVALID_ARG, "bad arguments to pkv_decode_step_host");
+  if (!pool || n < 0 || W <= 0) return fail(PKV_ERR_INVALID_ARG, "bad arguments to pkv_step_launch_host");
   if (n == 0) return PKV_OK;
   if (!q_host || !k_new_host || !v_new_host || !out_host || !q_dev || !k_new_dev || !v_new_dev || !out_dev)
     return fail(PKV_ERR_INVALID_ARG, "NULL buffer");
@@ -669,12 +687,56 @@ int pkv_decode_step_host(pkv_pool* pool, int32_t layer, const int32_t* seq_ids, 
     const cudaError_t e = cudaMemcpyAsync(c.dst, c.src, c.bytes, cudaMemcpyHostToDevice, st);
     if (e != cudaSuccess) return fail(PKV_ERR_CUDA, std::string("cudaMemcpyAsync (step input): ") + cudaGetErrorString(e));
   }
-  if (int rc = pkv_decode_step(pool, layer, seq_ids, n, W, q_dev, k_new_dev, v_new_dev, k_pool, v_pool, scale, out_dev,
-                               meta_host, meta_dev, workspace, ws_bytes, attn_begin, attn_end, stream))
+  if (int rc = pkv_step_launch(pool, layer, n, W, cow_pairs, n_cow, q_dev, k_new_dev, v_new_dev, k_pool, v_pool, scale,
+                               out_dev, meta_host, meta_dev, workspace, ws_bytes, attn_begin, attn_end, stream))
     return rc;
   const cudaError_t e = cudaMemcpyAsync(out_host, out_dev, qb, cudaMemcpyDeviceToHost, st);
   if (e != cudaSuccess) return fail(PKV_ERR_CUDA, std::string("cudaMemcpyAsync (step result): ") + cudaGetErrorString(e));
   return PKV_OK;
+}
+
+int pkv_decode_step(pkv_pool* pool, int32_t layer, const int32_t* seq_ids, int32_t n, int32_t W, const void* q,
+                    const void* k_new, const void* v_new, void* k_pool, void* v_pool, float scale, void* out,
+                    int32_t* meta_host, int32_t* meta_dev, void* workspace, size_t ws_bytes, pkv_event_t attn_begin,
+                    pkv_event_t attn_end, pkv_stream_t stream) {
+  pkv::clear_error();
+  if (!pool || n < 0 || W <= 0) return fail(PKV_ERR_INVALID_ARG, "bad arguments to pkv_decode_step");
+  if (n == 0) return PKV_OK;
+  if (!seq_ids || !q || !k_new || !v_new || !k_pool || !v_pool || !out || !meta_host || !meta_dev || !workspace)
+    return fail(PKV_ERR_INVALID_ARG, "NULL buffer");
+  if (layer < 0 || layer >= as_pool(pool)->geo.L) return fail(PKV_ERR_INVALID_ARG, "layer out of range");
+  // everything is validated before the plan changes any state
+  if (int rc = step_check(pool, seq_ids, n, W)) return rc;
+  if (int rc = step_workspace_check(pool, n, ws_bytes)) return rc;
+  static thread_local std::vector<int32_t> cows;
+  if (static_cast<int32_t>(cows.size()) < 2 * n) cows.resize(2 * n);
+  int32_t n_cow = 0;
+  if (int rc = pkv_step_plan(pool, seq_ids, n, W, meta_host, cows.data(), &n_cow)) return rc;
+  return pkv_step_launch(pool, layer, n, W, cows.data(), n_cow, q, k_new, v_new, k_pool, v_pool, scale, out,
+                         meta_host, meta_dev, workspace, ws_bytes, attn_begin, attn_end, stream);
+}
+
+int pkv_decode_step_host(pkv_pool* pool, int32_t layer, const int32_t* seq_ids, int32_t n, int32_t W,
+                         const void* q_host, const void* k_new_host, const void* v_new_host, void* out_host,
+                         void* q_dev, void* k_new_dev, void* v_new_dev, void* out_dev, void* k_pool, void* v_pool,
+                         float scale, int32_t* meta_host, int32_t* meta_dev, void* workspace, size_t ws_bytes,
+                         pkv_event_t attn_begin, pkv_event_t attn_end, pkv_stream_t stream) {
+  pkv::clear_error();
+  if (!pool || n < 0 || W <= 0) return fail(PKV_ERR_INVALID_ARG, "bad arguments to pkv_decode_step_host");
+  if (n == 0) return PKV_OK;
+  if (!seq_ids || !q_host || !k_new_host || !v_new_host || !out_host || !q_dev || !k_new_dev || !v_new_dev ||
+      !out_dev || !k_pool || !v_pool || !meta_host || !meta_dev || !workspace)
+    return fail(PKV_ERR_INVALID_ARG, "NULL buffer");
+  if (layer < 0 || layer >= as_pool(pool)->geo.L) return fail(PKV_ERR_INVALID_ARG, "layer out of range");
+  if (int rc = step_check(pool, seq_ids, n, W)) return rc;
+  if (int rc = step_workspace_check(pool, n, ws_bytes)) return rc;
+  static thread_local std::vector<int32_t> cows;
+  if (static_cast<int32_t>(cows.size()) < 2 * n) cows.resize(2 * n);
+  int32_t n_cow = 0;
+  if (int rc = pkv_step_plan(pool, seq_ids, n, W, meta_host, cows.data(), &n_cow)) return rc;
+  return pkv_step_launch_host(pool, layer, n, W, cows.data(), n_cow, q_host, k_new_host, v_new_host, out_host, q_dev,
+                              k_new_dev, v_new_dev, out_dev, k_pool, v_pool, scale, meta_host, meta_dev, workspace,
+                              ws_bytes, attn_begin, attn_end, stream);
 }
 
 }  // extern "C"

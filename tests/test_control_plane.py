@@ -171,3 +171,37 @@ def test_fp8_pool_scales_and_geometry_checks():
     with pytest.raises(pkv.PkvError) as e:
         pkv.pkv_pool_create(1, 2, 2, 12, 4, "e4m3", 4)  # d_head not a multiple of 8
     assert e.value.name == "PKV_ERR_UNSUPPORTED"
+
+
+def test_step_plan_matches_the_oracle_and_rejects_without_change():
+    """pkv_step_plan (the host half of a decode step): one token per sequence, slot mapping,
+    tables and lengths in the metadata buffer and the copy-on-write pairs, as the oracle plans
+    them; a sequence whose table would overflow W is rejected with nothing changed."""
+    import torch
+
+    g = W.Geometry(L=2, H_q=8, H_kv=2, d_head=64, block_size=16, dtype="bf16", num_blocks=96)
+    fo = W.permutation(91, "fo", g.num_blocks)
+    lib = pkv.pkv_pool_create(g.L, g.H_q, g.H_kv, g.d_head, g.block_size, g.dtype, g.num_blocks, fo)
+    orc = oracle.Pool(g.num_blocks, g.block_size, fo)
+    ids = [pkv.pkv_seq_create(lib) for _ in range(4)]
+    assert ids == [orc.seq_create() for _ in range(4)]
+    pkv.pkv_plan_append(lib, ids, [15, 16, 40, 0])
+    orc.append(ids, [15, 16, 40, 0])
+    kids = [pkv.pkv_seq_fork(lib, ids[2]), pkv.pkv_seq_fork(lib, ids[0])]
+    assert kids == [orc.seq_fork(ids[2]), orc.seq_fork(ids[0])]
+    run = ids + kids
+    n, Wd = len(run), 8
+    meta = torch.zeros(n * (Wd + 2), dtype=torch.int32)
+    for step in range(20):
+        cows = pkv.pkv_step_plan(lib, run, Wd, meta)
+        oslots, ocows = orc.append(run, [1] * n)
+        t2, l2 = orc.tables(run, Wd)
+        m = meta.numpy()
+        assert np.array_equal(m[:n], oslots) and np.array_equal(cows, ocows)
+        assert np.array_equal(m[n:n + n * Wd].reshape(n, Wd), t2) and np.array_equal(m[n + n * Wd:n + n * Wd + n], l2)
+    same_state(lib, orc, run)
+    before = (pkv.pkv_refcounts(lib).copy(), pkv.pkv_free_list(lib).copy())
+    with pytest.raises(pkv.PkvError) as e:  # 40 + 20 tokens fit 4 blocks: W = 3 cannot hold the next one
+        pkv.pkv_step_plan(lib, run, 3, meta)
+    assert e.value.name == "PKV_ERR_INVALID_ARG"
+    assert np.array_equal(before[0], pkv.pkv_refcounts(lib)) and np.array_equal(before[1], pkv.pkv_free_list(lib))

@@ -115,3 +115,60 @@ def test_decode_step_host_buffers_match_oracle(dtype):
         check_attention(out_host.double().numpy(), ref, "bf16")
         b.check_state()
     b.check_pools_bitexact()
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "e4m3"])
+def test_step_plan_ahead_then_launch_host_match_oracle(dtype):
+    """pkv_step_plan of step t + 1 runs while step t (pkv_step_launch_host) is on the GPU, as a
+    serving loop's scheduler would; every step's result matches the oracle and the pools and
+    control-plane state stay identical to the oracle's."""
+    import torch
+
+    g = W.Geometry(L=1, H_q=64, H_kv=8, d_head=128, block_size=16, dtype=dtype, num_blocks=256)
+    b = PagedBatch(g, W.permutation(44, "fo", g.num_blocks), seed=44,
+                   kv_scales=(0.5, 0.25) if dtype == "e4m3" else (1.0, 1.0))
+    ids = b.new_seqs(4)
+    b.append(ids, [16, 31, 200, 1], "prompt")
+    kids = [b.fork(ids[1]), b.fork(ids[2])]  # the first step copies their shared tail blocks
+    run = np.array(ids + kids, np.int32)
+    n, Wd, steps = len(run), 24, 5
+    metas = [torch.zeros(n * (Wd + 2), dtype=torch.int32).pin_memory() for _ in range(2)]
+    mdev = [torch.zeros(n * (Wd + 2), dtype=torch.int32, device="cuda") for _ in range(2)]
+    ws = torch.empty(pkv.pkv_decode_workspace_size(b.lib, n), dtype=torch.uint8, device="cuda")
+    q_dev = torch.empty((n, g.H_q, g.d_head), dtype=torch.bfloat16, device="cuda")
+    k_dev = torch.empty((n, g.H_kv, g.d_head), dtype=torch.bfloat16, device="cuda")
+    v_dev = torch.empty_like(k_dev)
+    o_dev = torch.empty_like(q_dev)
+    out_host = torch.empty((n, g.H_q, g.d_head), dtype=torch.bfloat16).pin_memory()
+    scale = 1.0 / math.sqrt(g.d_head)
+    pin = lambda x: torch.from_numpy(x.copy()).pin_memory().view(torch.bfloat16)
+    plans = {}
+
+    def plan(t):
+        m = metas[t % 2]
+        cows = pkv.pkv_step_plan(b.lib, run, Wd, m)
+        oslots, ocows = b.orc.append(run.tolist(), [1] * n)
+        mn = m.numpy()
+        assert np.array_equal(mn[:n], oslots) and np.array_equal(cows, ocows)
+        plans[t] = (cows, oslots, mn[n:n + n * Wd].reshape(n, Wd).copy(), mn[n + n * Wd:n + n * Wd + n].copy())
+
+    plan(0)
+    for t in range(steps):
+        q = W.normal(44, f"q{t}", (n, g.H_q, g.d_head), "bf16")
+        kn = W.normal(44, f"k{t}", (n, g.H_kv, g.d_head), "bf16")
+        vn = W.normal(44, f"v{t}", (n, g.H_kv, g.d_head), "bf16")
+        cows, oslots, tab, lens = plans[t]
+        out_host.fill_(float("nan"))
+        pkv.pkv_step_launch_host(b.lib, 0, n, Wd, cows, pin(q), pin(kn), pin(vn), out_host, q_dev, k_dev, v_dev, o_dev,
+                                 b.kp, b.vp, scale, metas[t % 2], mdev[t % 2], ws)
+        if len(cows):
+            oracle.copy_blocks(g, cows, b.hk, b.hv)
+        oracle.write_slots(g, 0, kn, vn, oslots, b.hk, b.hv, b.k_scale, b.v_scale)
+        if t + 1 < steps:
+            plan(t + 1)  # the host half of the next step while this one runs
+        torch.cuda.synchronize()
+        pkv.pkv_check_device_error()
+        ref = b.decode_ref(q, tab, lens, scale)
+        check_attention(out_host.double().numpy(), ref, "bf16")
+    b.check_state()
+    b.check_pools_bitexact()
