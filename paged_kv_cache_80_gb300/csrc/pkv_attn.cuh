@@ -25,6 +25,7 @@ struct E4M3 {  // one stored OCP FP8 E4M3 element
 
 constexpr int TILE = 16;   // tokens per tile (the mma M dimension)
 constexpr int GPAD = 8;    // query heads per mma N dimension
+constexpr int SIMT_GMAX = 16;  // query heads per KV head on the CUDA-core kernels (16 only for d_head <= 128)
 constexpr uint64_t kWaitNs = 2000000000ull;  // a tile load that takes 2 s is a fault: give up
 
 struct DecodeArgs {
@@ -98,17 +99,18 @@ constexpr int SIMT_WARPS = 8;
 // are merged in shared memory at the end.
 // Attention of the G query rows at q (contiguous, d apart) over the first len tokens
 // of sequence s, KV head g; writes G rows at out.  Run by the whole CTA.  TS is the
-// stored K/V element, TA the q / out element.
-template <typename TS, typename TA, int NPL>
+// stored K/V element, TA the q / out element; HP >= G is the head capacity (8, or 16
+// for wider groups).
+template <typename TS, typename TA, int NPL, int HP = GPAD>
 __device__ __forceinline__ void simt_attend(const DecodeArgs& a, const TS* __restrict__ kp,
                                             const TS* __restrict__ vp, int d, int s, int g, int len, const TA* q,
                                             TA* out) {
   constexpr int TOK = NPL >= 8 ? 2 : (NPL >= 4 ? 4 : 8);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int G = a.G;
-  float qv[GPAD][NPL], o[GPAD][NPL], m[GPAD], l[GPAD];
+  float qv[HP][NPL], o[HP][NPL], m[HP], l[HP];
 #pragma unroll
-  for (int h = 0; h < GPAD; ++h) {
+  for (int h = 0; h < HP; ++h) {
     m[h] = -INFINITY;
     l[h] = 0.f;
 #pragma unroll
@@ -143,7 +145,7 @@ __device__ __forceinline__ void simt_attend(const DecodeArgs& a, const TS* __res
       }
     }
 #pragma unroll
-    for (int h = 0; h < GPAD; ++h) {
+    for (int h = 0; h < HP; ++h) {
       if (h >= G) break;
       float sc[TOK];
 #pragma unroll
@@ -181,7 +183,7 @@ __device__ __forceinline__ void simt_attend(const DecodeArgs& a, const TS* __res
   float* sml = sm;                          // SIMT_WARPS * G * 2
   float* so = sm + SIMT_WARPS * G * 2;      // SIMT_WARPS * G * d
 #pragma unroll
-  for (int h = 0; h < GPAD; ++h) {
+  for (int h = 0; h < HP; ++h) {
     if (h >= G) break;
     if (lane == 0) {
       sml[(warp * G + h) * 2] = m[h];

@@ -622,7 +622,7 @@ __global__ void __launch_bounds__(NW * 32) decode_tc_kernel(const __grid_constan
 
 // --------------------------------------------------------------------------- CUDA-core path
 
-template <typename TS, typename TA, int NPL>
+template <typename TS, typename TA, int NPL, int HP>
 __global__ void __launch_bounds__(SIMT_WARPS * 32) decode_simt_kernel(const DecodeArgs a, const TS* __restrict__ kp,
                                                                         const TS* __restrict__ vp, int d) {
   const int pair = blockIdx.x;
@@ -634,8 +634,8 @@ __global__ void __launch_bounds__(SIMT_WARPS * 32) decode_simt_kernel(const Deco
     len = len < 0 ? 0 : static_cast<int>(maxlen);
   }
   const int64_t row = (static_cast<int64_t>(s) * a.H_q + g * a.G) * d;
-  simt_attend<TS, TA, NPL>(a, kp, vp, d, s, g, len, static_cast<const TA*>(a.q) + row,
-                           static_cast<TA*>(a.out) + row);
+  simt_attend<TS, TA, NPL, HP>(a, kp, vp, d, s, g, len, static_cast<const TA*>(a.q) + row,
+                               static_cast<TA*>(a.out) + row);
 }
 
 // --------------------------------------------------------------------------- host side
@@ -770,17 +770,25 @@ WsLayout ws_layout(int n_seq, int H_kv, int64_t total_warps, int D) {
 template <typename TS, typename TA>
 void simt_decode_t(const DecodeArgs& a, const void* kp, const void* vp, int grid, size_t smem, cudaStream_t st) {
   const int d = a.D;
-#define PKV_SIMT(NPL)                                                                                \
+#define PKV_SIMT(NPL, HP)                                                                            \
   {                                                                                                  \
-    auto kern = decode_simt_kernel<TS, TA, NPL>;                                                     \
+    auto kern = decode_simt_kernel<TS, TA, NPL, HP>;                                                 \
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)); \
     kern<<<grid, SIMT_WARPS * 32, smem, st>>>(a, static_cast<const TS*>(kp), static_cast<const TS*>(vp), d); \
   }
-  switch ((d + 31) / 32) {
-    case 1: PKV_SIMT(1) break;
-    case 2: PKV_SIMT(2) break;
-    case 3: case 4: PKV_SIMT(4) break;
-    default: PKV_SIMT(8) break;
+  if (a.G > GPAD) {  // 9 .. 16 query heads per KV head, d_head <= 128
+    switch ((d + 31) / 32) {
+      case 1: PKV_SIMT(1, SIMT_GMAX) break;
+      case 2: PKV_SIMT(2, SIMT_GMAX) break;
+      default: PKV_SIMT(4, SIMT_GMAX) break;
+    }
+  } else {
+    switch ((d + 31) / 32) {
+      case 1: PKV_SIMT(1, GPAD) break;
+      case 2: PKV_SIMT(2, GPAD) break;
+      case 3: case 4: PKV_SIMT(4, GPAD) break;
+      default: PKV_SIMT(8, GPAD) break;
+    }
   }
 #undef PKV_SIMT
 }
@@ -956,7 +964,8 @@ int launch_decode(Pool& P, int32_t layer, const void* q, const void* k_pool, con
                   void* ws, size_t ws_bytes, void* stream) {
   const auto& g = P.geo;
   const int G = g.H_q / g.H_kv;
-  if (G > GPAD) return fail(PKV_ERR_UNSUPPORTED, "more than 8 query heads per KV head");
+  if (G > SIMT_GMAX || (G > GPAD && g.d_head > 128))
+    return fail(PKV_ERR_UNSUPPORTED, "more than 16 query heads per KV head, or more than 8 with d_head > 128");
   if (reinterpret_cast<uintptr_t>(ws) & 255) return fail(PKV_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
   if (static_cast<int64_t>(n_seq) * g.H_kv * ((static_cast<int64_t>(W) * g.block_size + TILE - 1) / TILE) >=
       (int64_t(1) << 31))
@@ -1045,7 +1054,8 @@ extern "C" int pkv_decode_attention_noalloc(const pkv_pool* pool, int32_t layer,
   if (n_seq == 0) return PKV_OK;
   if (!q || !k_pool || !v_pool || !block_tables || !seq_lens || !out) return fail(PKV_ERR_INVALID_ARG, "NULL buffer");
   const int G = g.H_q / g.H_kv;
-  if (G > GPAD) return fail(PKV_ERR_UNSUPPORTED, "more than 8 query heads per KV head");
+  if (G > SIMT_GMAX || (G > GPAD && g.d_head > 128))
+    return fail(PKV_ERR_UNSUPPORTED, "more than 16 query heads per KV head, or more than 8 with d_head > 128");
   if (static_cast<int64_t>(n_seq) * g.H_kv * ((static_cast<int64_t>(W) * g.block_size + TILE - 1) / TILE) >=
       (int64_t(1) << 31))
     return fail(PKV_ERR_INVALID_ARG, "batch too large (tile count must stay below 2^31)");

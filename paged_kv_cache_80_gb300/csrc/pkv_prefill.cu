@@ -848,7 +848,7 @@ __global__ void __launch_bounds__(UM_THREADS, 1) prefill_umma_kernel(const __gri
 // Chunked prefill on CUDA cores: one CTA per (query row, KV head).  The row's
 // sequence s is found in q_off; its position is len_s - C_s + (row - q_off[s]) and it
 // attends to every token up to and including that position.
-template <typename TS, typename TA, int NPL>
+template <typename TS, typename TA, int NPL, int HP>
 __global__ void __launch_bounds__(SIMT_WARPS * 32) prefill_simt_kernel(const DecodeArgs a, const int32_t* q_off,
                                                                          const TS* __restrict__ kp,
                                                                          const TS* __restrict__ vp, int d) {
@@ -868,8 +868,8 @@ __global__ void __launch_bounds__(SIMT_WARPS * 32) prefill_simt_kernel(const Dec
     return;
   }
   const int pos = len - C + (row - q_off[s]);
-  simt_attend<TS, TA, NPL>(a, kp, vp, d, s, g, pos + 1, static_cast<const TA*>(a.q) + base,
-                           static_cast<TA*>(a.out) + base);
+  simt_attend<TS, TA, NPL, HP>(a, kp, vp, d, s, g, pos + 1, static_cast<const TA*>(a.q) + base,
+                               static_cast<TA*>(a.out) + base);
 }
 
 // The CUDA-core prefill kernel for the pool's element types: one CTA per (query row, KV head).
@@ -877,17 +877,25 @@ template <typename TS, typename TA>
 void simt_prefill_t(const DecodeArgs& a, const int32_t* q_off, const void* kp, const void* vp, dim3 grid, size_t smem,
                     cudaStream_t st) {
   const int d = a.D;
-#define PKV_PF_SIMT(NPL)                                                                             \
+#define PKV_PF_SIMT(NPL, HP)                                                                         \
   {                                                                                                  \
-    auto kern = prefill_simt_kernel<TS, TA, NPL>;                                                    \
+    auto kern = prefill_simt_kernel<TS, TA, NPL, HP>;                                                \
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)); \
     kern<<<grid, SIMT_WARPS * 32, smem, st>>>(a, q_off, static_cast<const TS*>(kp), static_cast<const TS*>(vp), d); \
   }
-  switch ((d + 31) / 32) {
-    case 1: PKV_PF_SIMT(1) break;
-    case 2: PKV_PF_SIMT(2) break;
-    case 3: case 4: PKV_PF_SIMT(4) break;
-    default: PKV_PF_SIMT(8) break;
+  if (a.G > GPAD) {  // 9 .. 16 query heads per KV head, d_head <= 128
+    switch ((d + 31) / 32) {
+      case 1: PKV_PF_SIMT(1, SIMT_GMAX) break;
+      case 2: PKV_PF_SIMT(2, SIMT_GMAX) break;
+      default: PKV_PF_SIMT(4, SIMT_GMAX) break;
+    }
+  } else {
+    switch ((d + 31) / 32) {
+      case 1: PKV_PF_SIMT(1, GPAD) break;
+      case 2: PKV_PF_SIMT(2, GPAD) break;
+      case 3: case 4: PKV_PF_SIMT(4, GPAD) break;
+      default: PKV_PF_SIMT(8, GPAD) break;
+    }
   }
 #undef PKV_PF_SIMT
 }
@@ -954,7 +962,8 @@ int launch_prefill(Pool& P, int32_t layer, const void* q, const int32_t* q_off, 
     count_launch();
     return PKV_OK;
   }
-  if (!tc && G > GPAD) return fail(PKV_ERR_UNSUPPORTED, "more than 8 query heads per KV head on the CUDA-core path");
+  if (!tc && !tc8 && (G > SIMT_GMAX || (G > GPAD && g.d_head > 128)))
+    return fail(PKV_ERR_UNSUPPORTED, "on the CUDA-core path: more than 16 query heads per KV head, or more than 8 with d_head > 128");
   if (tc) {
     if ((reinterpret_cast<uintptr_t>(q) & 15) || (reinterpret_cast<uintptr_t>(out) & 15))
       return fail(PKV_ERR_INVALID_ARG, "q and out must be 16-byte aligned");

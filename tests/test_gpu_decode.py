@@ -56,6 +56,8 @@ def test_gqa_bf16_ragged_lengths(lens):
     (16, 2, 96, 16, "bf16"),    # d = 96: CUDA-core path
     (12, 12, 64, 16, "f32"),
     (16, 4, 128, 16, "f32"),
+    (32, 2, 128, 16, "bf16"),   # G = 16: CUDA-core path
+    (48, 4, 64, 16, "f16"),     # G = 12: CUDA-core path
 ])
 def test_geometries(H_q, H_kv, d, B, dtype):
     g = W.Geometry(L=2, H_q=H_q, H_kv=H_kv, d_head=d, block_size=B, dtype=dtype, num_blocks=600)

@@ -54,10 +54,12 @@ def test_quantised_append_saturates_and_keeps_signed_zero():
     assert (codes == 0x7E).any() and (codes == 0xFE).any() and (codes == 0x80).any() and (codes == 0x00).any()
 
 
-@pytest.mark.parametrize("H_q,H_kv,d", [(64, 8, 128), (16, 16, 128), (32, 8, 128), (16, 4, 64), (24, 2, 64), (8, 2, 96)])
+@pytest.mark.parametrize("H_q,H_kv,d", [(64, 8, 128), (16, 16, 128), (32, 8, 128), (16, 4, 64), (24, 2, 64), (8, 2, 96),
+                                        (32, 2, 128), (16, 1, 256)])
 def test_fp8_decode_matches_oracle(H_q, H_kv, d):
     """Ragged lengths (0, 1, tails of 1..15 tokens, multi-block), permuted blocks.
-    d 128 with G <= 8 runs on tensor cores; the rest on CUDA cores."""
+    d 128 with G <= 8 runs on tensor cores; the rest on CUDA cores (G 12 and 16 there;
+    more than 8 heads with d_head 256 is refused)."""
     g = W.Geometry(L=2, H_q=H_q, H_kv=H_kv, d_head=d, block_size=16, dtype="e4m3", num_blocks=700)
     b = PagedBatch(g, W.permutation(53, f"fo{H_q}{d}", g.num_blocks), seed=53, kv_scales=(0.0173, 0.25))
     lens = [0, 1, 15, 16, 17, 31, 64, 100, 257, 1000, 2049, 3, 500, 0, 33, 4095]
@@ -67,7 +69,7 @@ def test_fp8_decode_matches_oracle(H_q, H_kv, d):
     b.append(ids, lens, "p", layer=1)
     b.append(ids, [1] * len(ids), "t", layer=1)
     q = W.normal(53, "q", (len(ids), g.H_q, g.d_head), "bf16")
-    if H_q // H_kv > 8:
+    if H_q // H_kv > 8 and d > 128:
         with pytest.raises(pkv.PkvError) as e:
             b.decode_gpu(ids, q, 1 / math.sqrt(d), layer=1)
         assert e.value.name == "PKV_ERR_UNSUPPORTED"

@@ -45,6 +45,7 @@ def run_prefill(g, history, chunks, seed, max_q=None, free_order=None):
     (64, 1, 128, 16, "bf16"),   # G = 64 (one KV head): 2 queries per tile
     (12, 12, 64, 16, "f32"),    # CUDA-core path
     (16, 2, 96, 16, "bf16"),    # CUDA-core path
+    (32, 2, 96, 16, "bf16"),    # CUDA-core path, G = 16
 ])
 def test_prefill_geometries(H_q, H_kv, d, B, dtype):
     g = W.Geometry(L=1, H_q=H_q, H_kv=H_kv, d_head=d, block_size=B, dtype=dtype, num_blocks=800)
