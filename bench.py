@@ -44,15 +44,14 @@ import workloads as W  # noqa: E402
 METRIC = "paged decode attention KV GB/s & tokens/s (% of 8 TB/s HBM); swap GB/s vs host link"
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per algorithmic byte
-# of the decode call, from an ncu capture of the kernels built from the sources
-# with this digest (summary in profiles/).  Reported only while the sources match.
-# ncu DRAM bytes / algorithmic bytes of one decode launch, per stored K/V type, valid
-# while the decode sources hash to sources_sha256
+# of one decode launch, per (stored K/V type, query heads per KV head), from ncu
+# captures of agent 48 x 4,096 (summary in profiles/) of the kernels built from the
+# sources with this digest.  Reported only while the sources hash to TRAFFIC_SOURCES_SHA256.
+TRAFFIC_SOURCES_SHA256 = "67d79765b0f2906f356190f872eadd0b84d69d51b5a40b1fe1204d12def797cc"
 TRAFFIC_RECORD = {
-    "bf16": {"sources_sha256": "29ed0f4ea1697f34cfbe16b64e859bfe40a2e77f9b4520338e67f74fa4dc7c1d",
-             "ratio": 1.0103},  # 816.2 MB DRAM / 807.8 MB algorithmic, agent 48 x 4,096 capture
-    "e4m3": {"sources_sha256": "29ed0f4ea1697f34cfbe16b64e859bfe40a2e77f9b4520338e67f74fa4dc7c1d",
-             "ratio": 1.0164},  # 411.4 MB DRAM / 404.7 MB algorithmic, agent 48 x 4,096 capture
+    ("bf16", 8): 1.0104,   # 811.6 + 4.7 MB DRAM for 807.9 MB algorithmic
+    ("e4m3", 8): 1.0163,   # 407.0 + 4.4 MB for 404.8 MB
+    ("bf16", 16): 1.0137,  # 814.4 + 6.2 MB for 809.5 MB
 }
 
 
@@ -419,11 +418,14 @@ class DecodeRunner:
 class AgentRunner(DecodeRunner):
     name = "agent32k"
 
-    def __init__(self, torch, pkv, dev, total_steps, n_seq=48, context=32768, kv_dtype="bf16"):
+    def __init__(self, torch, pkv, dev, total_steps, n_seq=48, context=32768, kv_dtype="bf16", q_heads=0):
         super().__init__(torch, pkv, dev, total_steps)
         wl = W.agent(n_seq, context, spare_steps=total_steps + 16)
         self.wl, self.seed = wl, wl.seed
-        self._set_geometry(with_kv_dtype(wl.geometry, kv_dtype))
+        g0 = with_kv_dtype(wl.geometry, kv_dtype)
+        if q_heads:  # another query-head count over the same 8 KV heads (group size q_heads / 8)
+            g0 = W.Geometry(g0.L, q_heads, g0.H_kv, g0.d_head, g0.block_size, g0.dtype, g0.num_blocks)
+        self._set_geometry(g0)
         g = self.g
         self.n_max = n_seq
         self.scale = wl.scale
@@ -437,8 +439,8 @@ class AgentRunner(DecodeRunner):
         self.Wd = -(-(context + total_steps + 1) // g.block_size)
         self.inputs_for_steps("agent")
         self._alloc_common(n_seq)
-        self.config = {"workload": f"agent{context // 1024}k: {n_seq} sequences x {context} tokens, 64 query / "
-                                   f"8 KV heads, d_head 128, {kv_desc(g)}, 16-token blocks, permuted block ids",
+        self.config = {"workload": f"agent{context // 1024}k: {n_seq} sequences x {context} tokens, {g.H_q} query / "
+                                   f"{g.H_kv} KV heads, d_head 128, {kv_desc(g)}, 16-token blocks, permuted block ids",
                        "n_seq": n_seq, "context": context, "H_q": g.H_q, "H_kv": g.H_kv, "d_head": g.d_head,
                        "block_size": g.block_size, "pool_blocks": g.num_blocks,
                        "l2": f"inputs larger than L2 ({n_seq * context * 2048 * g.elem_bytes / 1e9:.2f} GB of K/V "
@@ -585,8 +587,9 @@ RUNNERS = {"agent32k": AgentRunner, "chat": ChatRunner, "forked": ForkedRunner, 
 def run_decode(args, torch, pkv, dev, world, rank):
     total = args.warmup + args.steps + 2 + args.steps  # timed region, then e2e warm-up + e2e steps
     kw = {} if args.workload == "tiny" else {"kv_dtype": args.kv_dtype}
-    if args.workload == "agent32k" and (args.context or args.n_seq):
-        r = AgentRunner(torch, pkv, dev, total, n_seq=args.n_seq or 48, context=args.context or 32768, **kw)
+    if args.workload == "agent32k" and (args.context or args.n_seq or args.q_heads):
+        r = AgentRunner(torch, pkv, dev, total, n_seq=args.n_seq or 48, context=args.context or 32768,
+                        q_heads=args.q_heads, **kw)
     else:
         r = RUNNERS[args.workload](torch, pkv, dev, total, **kw)
     g = r.g
@@ -637,9 +640,9 @@ def run_decode(args, torch, pkv, dev, world, rank):
     peak, peak_kind = load_peaks()
     value = world * kv_total / (ms_max / 1e3) / 1e9
     traffic = args.traffic
-    rec = TRAFFIC_RECORD.get(g.dtype)
-    if traffic is None and rec and rec["sources_sha256"] == decode_sources_digest():
-        traffic = round(rec["ratio"] * alg_avg)
+    ratio = TRAFFIC_RECORD.get((g.dtype, g.H_q // g.H_kv))
+    if traffic is None and ratio and TRAFFIC_SOURCES_SHA256 == decode_sources_digest():
+        traffic = round(ratio * alg_avg)
     achieved = alg_avg / (dec_avg / 1e3) / 1e9
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -1145,6 +1148,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--context", type=int, default=0, help="agent workload: tokens per sequence (default 32768)")
     ap.add_argument("--n-seq", type=int, default=0, help="agent workload: sequences (default 48)")
+    ap.add_argument("--q-heads", type=int, default=0,
+                    help="agent workload: query heads over its 8 KV heads (default 64; 128 = groups of 16)")
     ap.add_argument("--kv-dtype", choices=["bf16", "e4m3"], default="bf16",
                     help="decode workloads: stored K/V type (e4m3 = FP8 pool, bf16 q/out)")
     ap.add_argument("--traffic", type=float, default=None,

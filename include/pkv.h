@@ -200,9 +200,10 @@ int pkv_decode_workspace_size(const pkv_pool* pool, int32_t n_seq, size_t* bytes
  *   workspace   : device, >= pkv_decode_workspace_size bytes, 256-byte aligned;
  *                 no state survives between calls.
  * Calls on one workspace must not overlap on the GPU.
- * bf16/f16 with d_head 64 or 128, and FP8 with d_head 128, with G <= 8 and B a
- * multiple of 16 run on the tensor-core path (TMA-staged tiles, mma.sync); other
- * geometries on CUDA cores (G <= 16; G <= 8 when d_head > 128; wider groups return
+ * bf16/f16 with d_head 64 or 128, and FP8 with d_head 128, with G <= 16 and B a
+ * multiple of 16 run on the tensor-core path (TMA-staged tiles, mma.sync; groups
+ * of 9 to 16 query heads as two 8-head column blocks); other geometries on CUDA
+ * cores (G <= 16; G <= 8 when d_head > 128; wider groups return
  * PKV_ERR_UNSUPPORTED). */
 int pkv_decode_attention(const pkv_pool* pool, int32_t layer, const void* q, const void* k_pool,
                          const void* v_pool, const int32_t* block_tables, int32_t W, const int32_t* seq_lens,
@@ -285,7 +286,7 @@ int pkv_decode_step_host(pkv_pool* pool, int32_t layer, const int32_t* seq_ids, 
 /* Decode attention that allocates nothing.  (The pages have no counterpart of
  * this call; it exists for callers of this library.)
  * Same arguments and result as pkv_decode_attention, minus the workspace: the
- * scratch is a 12 MiB array compiled into the library (a static __device__
+ * scratch is a 24 MiB array compiled into the library (a static __device__
  * variable, held by every GPU that loads the library until the process exits).
  * It is for callers that cannot call cudaMalloc: e.g. a serving engine that sized
  * its KV block pool to fill the device at start-up, so a later allocation would
@@ -293,9 +294,10 @@ int pkv_decode_step_host(pkv_pool* pool, int32_t layer, const int32_t* seq_ids, 
  *   - The first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call
  *     before any stream capture.
- *   - A batch that needs more scratch than 12 MiB is rejected with
- *     PKV_ERR_INVALID_ARG (about 10 MB are the partials of one persistent grid on
- *     a 152-SM GB300; each sequence adds 8 bytes).
+ *   - A batch that needs more scratch than 24 MiB is rejected with
+ *     PKV_ERR_INVALID_ARG (the partials of one persistent grid on a 152-SM GB300
+ *     take about 10 MB for groups of up to 8 query heads and 20 MB for 9 to 16;
+ *     each sequence adds 8 + 4 * H_kv bytes).
  *   - Every call on a device shares the one array and leaves its contents behind;
  *     nothing in it needs to start at zero.  Calls whose GPU work overlaps (two
  *     streams, or two threads) race on it: order them on one stream.

@@ -386,7 +386,7 @@ def pkv_decode_attention(pool: PoolLike, layer: int, q, k_pool, v_pool, block_ta
 def pkv_decode_attention_noalloc(pool: PoolLike, layer: int, q, k_pool, v_pool, block_tables, seq_lens,
                                  scale: float, out, stream=None) -> None:
     """Decode attention without a workspace: for callers that cannot allocate device
-    memory (the library's own static 12 MiB scratch is used instead)."""
+    memory (the library's own static 24 MiB scratch is used instead)."""
     n_seq = int(seq_lens.numel())
     W = int(block_tables.shape[1]) if block_tables.dim() == 2 else 0
     _check(_L().pkv_decode_attention_noalloc(_h(pool), layer, _dev(q, "q"), _dev(k_pool, "k_pool"),

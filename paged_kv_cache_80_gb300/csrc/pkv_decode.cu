@@ -153,21 +153,26 @@ __global__ void __launch_bounds__(1024) plan_kernel(const DecodeArgs a) {
 
 // --------------------------------------------------------------------------- tensor-core path
 
-template <int D, int EB = 2>  // EB: bytes per stored K/V element
+// EB: bytes per stored K/V element; NB: 8-head column blocks of the mma N dimension (1 for
+// G <= 8, 2 for 9 <= G <= 16: every K/V fragment loaded from shared memory feeds NB mmas).
+template <int D, int EB = 2, int NB = 1>
 struct TcCfg {
+  static constexpr int GP = GPAD * NB;                     // query rows held per group (padded)
   static constexpr int KV_TILE_BYTES = TILE * D * EB;     // one 16 x D tile of K (or V)
-  static constexpr int Q_BYTES = GPAD * D * 2;             // up to 8 query rows (16-bit)
+  static constexpr int Q_BYTES = GP * D * 2;               // up to GP query rows (16-bit)
   static constexpr int STAGE_BYTES = 2 * KV_TILE_BYTES + Q_BYTES;
   static constexpr int NBOX = D * EB / 128;                // 128-byte TMA boxes per tile row
   static constexpr int BOX_ELEMS = 128 / EB;
   static constexpr int NKC = D / 16;                       // 16-wide chunks of d_head
-  static constexpr int PSTRIDE = NKC * 32 * 4 + 2 * GPAD;  // floats per partial slot
+  static constexpr int OFL = NKC * 32 * 4;                 // floats of one head block's O^T fragments
+  // floats per partial slot: the O^T fragments of each head block, then m[GP], then l[GP]
+  static constexpr int PSTRIDE = NB * OFL + 2 * GP;
   static_assert(STAGE_BYTES % 1024 == 0, "stages must keep 1024-byte alignment for the swizzle");
 };
 
-template <int D, int EB, int S, int NW>
+template <int D, int EB, int S, int NW, int NB = 1>
 struct TcSmem {
-  static constexpr int WARP_BYTES = S * TcCfg<D, EB>::STAGE_BYTES + 64 * 16 + S * 8 + 8;
+  static constexpr int WARP_BYTES = S * TcCfg<D, EB, NB>::STAGE_BYTES + 64 * 16 + S * 8 + 8;
   static constexpr int WARP_STRIDE = (WARP_BYTES + 1023) / 1024 * 1024;
   static constexpr int TOTAL = NW * WARP_STRIDE + 1024;  // + alignment slack
 };
@@ -242,52 +247,59 @@ __device__ __forceinline__ void store_group(TO* out, const float4 (&acc)[D / 16]
 }
 
 // Merge the partials of one split pair (contributing warps wa..wb) and write its
-// G output rows.  Run by one whole warp; lane l owns float4 l of every d-chunk.
-// Partials are read through L2 (ld.global.cg): other SMs wrote them.
-template <typename TO, int D, bool F8>
+// G output rows.  Run by one whole warp; lane l owns float4 l of every d-chunk of
+// each head block, merged one block at a time.  Partials are read through L2
+// (ld.global.cg): other SMs wrote them.
+template <typename TO, int D, bool F8, int NB>
 __device__ __forceinline__ void merge_pair(const DecodeArgs& a, int s, int g, int pbeg, int wa, int wb, int R,
                                            int lane) {
-  using C = TcCfg<D>;
+  using C = TcCfg<D, 2, NB>;
   const int h0 = 2 * (lane & 3);
-  float M0 = -INFINITY, M1 = -INFINITY, L0 = 0.f, L1 = 0.f;
-  float4 acc[C::NKC];
-#pragma unroll
-  for (int c = 0; c < C::NKC; ++c) acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
-  // two contributors per round: all their loads are issued before any use
-  for (int w = wa; w <= wb; w += 2) {
-    const bool two = w + 1 <= wb;
-    const float* p0 = a.partials + static_cast<int64_t>(w * 2 + ((w == wa && pbeg != wa * R) ? 1 : 0)) * C::PSTRIDE;
-    const float* p1 = two ? a.partials + static_cast<int64_t>((w + 1) * 2) * C::PSTRIDE : p0;
-    const float ma0 = __ldcg(p0 + C::NKC * 128 + h0), ma1 = __ldcg(p0 + C::NKC * 128 + h0 + 1);
-    const float la0 = __ldcg(p0 + C::NKC * 128 + GPAD + h0), la1 = __ldcg(p0 + C::NKC * 128 + GPAD + h0 + 1);
-    float mb0 = __ldcg(p1 + C::NKC * 128 + h0), mb1 = __ldcg(p1 + C::NKC * 128 + h0 + 1);
-    const float lb0 = __ldcg(p1 + C::NKC * 128 + GPAD + h0), lb1 = __ldcg(p1 + C::NKC * 128 + GPAD + h0 + 1);
-    float4 va[C::NKC], vb[C::NKC];
-#pragma unroll
-    for (int c = 0; c < C::NKC; ++c) {
-      va[c] = __ldcg(reinterpret_cast<const float4*>(p0) + c * 32 + lane);
-      vb[c] = __ldcg(reinterpret_cast<const float4*>(p1) + c * 32 + lane);
-    }
-    if (!two) mb0 = mb1 = -INFINITY;
-    const float n0 = fmaxf(M0, fmaxf(ma0, mb0)), n1 = fmaxf(M1, fmaxf(ma1, mb1));
-    const float r0 = exp2f(M0 - n0), r1 = exp2f(M1 - n1);
-    const float ea0 = exp2f(ma0 - n0), ea1 = exp2f(ma1 - n1);
-    const float eb0 = two ? exp2f(mb0 - n0) : 0.f, eb1 = two ? exp2f(mb1 - n1) : 0.f;
-    L0 = L0 * r0 + la0 * ea0 + lb0 * eb0;
-    L1 = L1 * r1 + la1 * ea1 + lb1 * eb1;
-#pragma unroll
-    for (int c = 0; c < C::NKC; ++c) {
-      acc[c].x = acc[c].x * r0 + va[c].x * ea0 + vb[c].x * eb0;
-      acc[c].y = acc[c].y * r1 + va[c].y * ea1 + vb[c].y * eb1;
-      acc[c].z = acc[c].z * r0 + va[c].z * ea0 + vb[c].z * eb0;
-      acc[c].w = acc[c].w * r1 + va[c].w * ea1 + vb[c].w * eb1;
-    }
-    M0 = n0;
-    M1 = n1;
-  }
-  const float i0 = a.v_mul / L0, i1 = a.v_mul / L1;
   TO* out = static_cast<TO*>(a.out) + (static_cast<int64_t>(s) * a.H_q + g * a.G) * D;
-  store_group<TO, D, F8>(out, acc, i0, i1, lane, a.G);
+#pragma unroll 1
+  for (int nb = 0; nb < NB; ++nb) {
+    if (GPAD * nb >= a.G) break;
+    const int hm = NB * C::OFL + GPAD * nb + h0;  // m of heads h0, h0 + 1 of this block; l is GP further
+    float M0 = -INFINITY, M1 = -INFINITY, L0 = 0.f, L1 = 0.f;
+    float4 acc[C::NKC];
+#pragma unroll
+    for (int c = 0; c < C::NKC; ++c) acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+    // two contributors per round: all their loads are issued before any use
+    for (int w = wa; w <= wb; w += 2) {
+      const bool two = w + 1 <= wb;
+      const float* p0 =
+          a.partials + static_cast<int64_t>(w * 2 + ((w == wa && pbeg != wa * R) ? 1 : 0)) * C::PSTRIDE;
+      const float* p1 = two ? a.partials + static_cast<int64_t>((w + 1) * 2) * C::PSTRIDE : p0;
+      const float ma0 = __ldcg(p0 + hm), ma1 = __ldcg(p0 + hm + 1);
+      const float la0 = __ldcg(p0 + hm + C::GP), la1 = __ldcg(p0 + hm + C::GP + 1);
+      float mb0 = __ldcg(p1 + hm), mb1 = __ldcg(p1 + hm + 1);
+      const float lb0 = __ldcg(p1 + hm + C::GP), lb1 = __ldcg(p1 + hm + C::GP + 1);
+      float4 va[C::NKC], vb[C::NKC];
+#pragma unroll
+      for (int c = 0; c < C::NKC; ++c) {
+        va[c] = __ldcg(reinterpret_cast<const float4*>(p0 + nb * C::OFL) + c * 32 + lane);
+        vb[c] = __ldcg(reinterpret_cast<const float4*>(p1 + nb * C::OFL) + c * 32 + lane);
+      }
+      if (!two) mb0 = mb1 = -INFINITY;
+      const float n0 = fmaxf(M0, fmaxf(ma0, mb0)), n1 = fmaxf(M1, fmaxf(ma1, mb1));
+      const float r0 = exp2f(M0 - n0), r1 = exp2f(M1 - n1);
+      const float ea0 = exp2f(ma0 - n0), ea1 = exp2f(ma1 - n1);
+      const float eb0 = two ? exp2f(mb0 - n0) : 0.f, eb1 = two ? exp2f(mb1 - n1) : 0.f;
+      L0 = L0 * r0 + la0 * ea0 + lb0 * eb0;
+      L1 = L1 * r1 + la1 * ea1 + lb1 * eb1;
+#pragma unroll
+      for (int c = 0; c < C::NKC; ++c) {
+        acc[c].x = acc[c].x * r0 + va[c].x * ea0 + vb[c].x * eb0;
+        acc[c].y = acc[c].y * r1 + va[c].y * ea1 + vb[c].y * eb1;
+        acc[c].z = acc[c].z * r0 + va[c].z * ea0 + vb[c].z * eb0;
+        acc[c].w = acc[c].w * r1 + va[c].w * ea1 + vb[c].w * eb1;
+      }
+      M0 = n0;
+      M1 = n1;
+    }
+    const float i0 = a.v_mul / L0, i1 = a.v_mul / L1;
+    store_group<TO, D, F8>(out + GPAD * nb * D, acc, i0, i1, lane, a.G - GPAD * nb);
+  }
 }
 
 // Descriptor of one tile, built by the warp a batch at a time:
@@ -295,7 +307,7 @@ __device__ __forceinline__ void merge_pair(const DecodeArgs& a, int s, int g, in
 //   z = valid tokens | first-of-pair << 8 | last-of-pair << 9 | new-pair-in-range << 10.
 constexpr int F_FIRST = 1 << 8, F_LAST = 1 << 9, F_NEWPAIR = 1 << 10;
 
-template <typename T, int D, int S, int NW>
+template <typename T, int D, int S, int NW, int NB>
 __global__ void __launch_bounds__(NW * 32) decode_tc_kernel(const __grid_constant__ CUtensorMap tmk,
                                                             const __grid_constant__ CUtensorMap tmv,
                                                             const DecodeArgs a) {
@@ -305,8 +317,8 @@ __global__ void __launch_bounds__(NW * 32) decode_tc_kernel(const __grid_constan
   using TM = typename std::conditional<F8, __half, T>::type;
   constexpr bool BF16 = std::is_same<TM, __nv_bfloat16>::value;
   constexpr int EB = F8 ? 1 : 2;
-  using C = TcCfg<D, EB>;
-  using SM = TcSmem<D, EB, S, NW>;
+  using C = TcCfg<D, EB, NB>;
+  using SM = TcSmem<D, EB, S, NW, NB>;
   extern __shared__ uint8_t smem_raw[];
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -416,9 +428,10 @@ __global__ void __launch_bounds__(NW * 32) decode_tc_kernel(const __grid_constan
   const int trow = lane >> 2;                            // token row of c0/c1 (c2/c3: +8)
   const int c4 = lane & 3;
 
-  float o[C::NKC][4];
-  uint32_t qf[C::NKC][2];
-  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+  // per head block nb: O^T fragments, q fragments, running max and sum of heads 8nb + h0, 8nb + h0 + 1
+  float o[NB][C::NKC][4];
+  uint32_t qf[NB][C::NKC][2];
+  float m[NB][2], l[NB][2];
   int cur_pair = -1;
   bool cur_started = false, cur_first_in_range = false;
 
@@ -440,32 +453,40 @@ __global__ void __launch_bounds__(NW * 32) decode_tc_kernel(const __grid_constan
       cur_pair = d.y;
       cur_started = d.z & F_FIRST;
       cur_first_in_range = (i == 0);
-      m0 = m1 = -INFINITY;
-      l0 = l1 = 0.f;
 #pragma unroll
-      for (int c = 0; c < C::NKC; ++c) o[c][0] = o[c][1] = o[c][2] = o[c][3] = 0.f;
-      const uint8_t* qs = region + st * C::STAGE_BYTES + 2 * C::KV_TILE_BYTES;
-      const bool live = trow < a.G;
-      if constexpr (F8) {
-        // step c of q K^T covers d = 32 c4 + 4c .. +3: (b0, b1) the first two, (b2, b3) the last two
+      for (int nb = 0; nb < NB; ++nb) {
+        m[nb][0] = m[nb][1] = -INFINITY;
+        l[nb][0] = l[nb][1] = 0.f;
 #pragma unroll
-        for (int c = 0; c < C::NKC; ++c) {
-          const uint2 w = *reinterpret_cast<const uint2*>(qs + (trow * D + (D / 4) * c4 + 4 * c) * 2);
-          qf[c][0] = live ? bf16x2_to_f16x2(w.x) : 0u;
-          qf[c][1] = live ? bf16x2_to_f16x2(w.y) : 0u;
-        }
-      } else {
+        for (int c = 0; c < C::NKC; ++c) o[nb][c][0] = o[nb][c][1] = o[nb][c][2] = o[nb][c][3] = 0.f;
+        const uint8_t* qs = region + st * C::STAGE_BYTES + 2 * C::KV_TILE_BYTES;
+        const int hq = trow + GPAD * nb;  // this lane's query row (B-operand column) in block nb
+        const bool live = hq < a.G;
+        if constexpr (F8) {
+          // step c of q K^T covers d = 32 c4 + 4c .. +3: (b0, b1) the first two, (b2, b3) the last two
 #pragma unroll
-        for (int c = 0; c < C::NKC; ++c) {
-          const uint32_t* p = reinterpret_cast<const uint32_t*>(qs + trow * D * 2 + (16 * c + h0) * 2);
-          qf[c][0] = live ? p[0] : 0u;
-          qf[c][1] = live ? p[4] : 0u;
+          for (int c = 0; c < C::NKC; ++c) {
+            const uint2 w = *reinterpret_cast<const uint2*>(qs + (hq * D + (D / 4) * c4 + 4 * c) * 2);
+            qf[nb][c][0] = live ? bf16x2_to_f16x2(w.x) : 0u;
+            qf[nb][c][1] = live ? bf16x2_to_f16x2(w.y) : 0u;
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < C::NKC; ++c) {
+            const uint32_t* p = reinterpret_cast<const uint32_t*>(qs + hq * D * 2 + (16 * c + h0) * 2);
+            qf[nb][c][0] = live ? p[0] : 0u;
+            qf[nb][c][1] = live ? p[4] : 0u;
+          }
         }
       }
     }
 
-    // ---- S^T = K q^T  (16 tokens x 8 heads), two accumulation chains
-    float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+    // ---- S^T = K q^T  (16 tokens x 8 heads per block), two accumulation chains per block
+    float sa[NB][4], sb[NB][4];
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+      for (int r = 0; r < 4; ++r) sa[nb][r] = sb[nb][r] = 0.f;
     if constexpr (F8) {
       // K rows trow and trow + 8, bytes 32 c4 .. 32 c4 + 31 (16-byte chunks 2c4, 2c4 + 1; swizzle
       // XOR = row & 7 = trow); step c takes bytes 4c .. 4c + 3 of each row
@@ -479,8 +500,11 @@ __global__ void __launch_bounds__(NW * 32) decode_tc_kernel(const __grid_constan
         uint32_t a0, a1, a2, a3;
         e4m3x4_to_f16x2x2(wa, a0, a2);
         e4m3x4_to_f16x2x2(wb, a1, a3);
-        if (c & 1) mma_16816<BF16>(sb, a0, a1, a2, a3, qf[c][0], qf[c][1]);
-        else mma_16816<BF16>(sa, a0, a1, a2, a3, qf[c][0], qf[c][1]);
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) {
+          if (c & 1) mma_16816<BF16>(sb[nb], a0, a1, a2, a3, qf[nb][c][0], qf[nb][c][1]);
+          else mma_16816<BF16>(sa[nb], a0, a1, a2, a3, qf[nb][c][0], qf[nb][c][1]);
+        }
       }
     } else {
 #pragma unroll
@@ -489,16 +513,25 @@ __global__ void __launch_bounds__(NW * 32) decode_tc_kernel(const __grid_constan
         const uint32_t addr = sk + (c >> 2) * (TILE * 128) + k_row * 128 + ((chunk ^ r8) << 4);
         uint32_t a0, a1, a2, a3;
         ldmatrix_x4(addr, a0, a1, a2, a3);
-        if (c & 1) mma_16816<BF16>(sb, a0, a1, a2, a3, qf[c][0], qf[c][1]);
-        else mma_16816<BF16>(sa, a0, a1, a2, a3, qf[c][0], qf[c][1]);
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) {
+          if (c & 1) mma_16816<BF16>(sb[nb], a0, a1, a2, a3, qf[nb][c][0], qf[nb][c][1]);
+          else mma_16816<BF16>(sa[nb], a0, a1, a2, a3, qf[nb][c][0], qf[nb][c][1]);
+        }
       }
     }
-    float s0 = (sa[0] + sb[0]) * a.scale_log2, s1 = (sa[1] + sb[1]) * a.scale_log2;
-    float s2 = (sa[2] + sb[2]) * a.scale_log2, s3 = (sa[3] + sb[3]) * a.scale_log2;
+    float sc[NB][4];  // scores (base-2 logits): c0, c1 token trow, heads h0, h0 + 1; c2, c3 token trow + 8
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+      for (int r = 0; r < 4; ++r) sc[nb][r] = (sa[nb][r] + sb[nb][r]) * a.scale_log2;
     const int valid = d.z & 0xff;
     if (valid < TILE) {
-      if (trow >= valid) s0 = s1 = -INFINITY;
-      if (trow + 8 >= valid) s2 = s3 = -INFINITY;
+#pragma unroll
+      for (int nb = 0; nb < NB; ++nb) {
+        if (trow >= valid) sc[nb][0] = sc[nb][1] = -INFINITY;
+        if (trow + 8 >= valid) sc[nb][2] = sc[nb][3] = -INFINITY;
+      }
       // zero the V rows past the end so that 0 * (stale value) cannot make NaN
       uint8_t* vrows = region + st * C::STAGE_BYTES + C::KV_TILE_BYTES;
       for (int k = lane; k < (TILE - valid) * 8 * C::NBOX; k += 32) {
@@ -510,33 +543,37 @@ __global__ void __launch_bounds__(NW * 32) decode_tc_kernel(const __grid_constan
       __syncwarp();
     }
 
-    // ---- online softmax over this tile (per head: columns h0, h0 + 1)
-    float x0 = fmaxf(s0, s2), x1 = fmaxf(s1, s3);
+    // ---- online softmax over this tile (per head: columns h0, h0 + 1 of each block)
+    uint32_t pb[NB][2];
 #pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-      x0 = fmaxf(x0, __shfl_xor_sync(0xffffffffu, x0, off));
-      x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, off));
-    }
-    const float n0 = fmaxf(m0, x0), n1 = fmaxf(m1, x1);
-    const float c0 = exp2f(m0 - n0), c1 = exp2f(m1 - n1);
-    m0 = n0;
-    m1 = n1;
-    const float p0 = exp2f(s0 - n0), p2 = exp2f(s2 - n0);
-    const float p1 = exp2f(s1 - n1), p3 = exp2f(s3 - n1);
-    l0 = l0 * c0 + (p0 + p2);
-    l1 = l1 * c1 + (p1 + p3);
+    for (int nb = 0; nb < NB; ++nb) {
+      float x0 = fmaxf(sc[nb][0], sc[nb][2]), x1 = fmaxf(sc[nb][1], sc[nb][3]);
 #pragma unroll
-    for (int c = 0; c < C::NKC; ++c) {
-      o[c][0] *= c0;
-      o[c][1] *= c1;
-      o[c][2] *= c0;
-      o[c][3] *= c1;
+      for (int off = 4; off < 32; off <<= 1) {
+        x0 = fmaxf(x0, __shfl_xor_sync(0xffffffffu, x0, off));
+        x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, off));
+      }
+      const float n0 = fmaxf(m[nb][0], x0), n1 = fmaxf(m[nb][1], x1);
+      const float c0 = exp2f(m[nb][0] - n0), c1 = exp2f(m[nb][1] - n1);
+      m[nb][0] = n0;
+      m[nb][1] = n1;
+      const float p0 = exp2f(sc[nb][0] - n0), p2 = exp2f(sc[nb][2] - n0);
+      const float p1 = exp2f(sc[nb][1] - n1), p3 = exp2f(sc[nb][3] - n1);
+      l[nb][0] = l[nb][0] * c0 + (p0 + p2);
+      l[nb][1] = l[nb][1] * c1 + (p1 + p3);
+#pragma unroll
+      for (int c = 0; c < C::NKC; ++c) {
+        o[nb][c][0] *= c0;
+        o[nb][c][1] *= c1;
+        o[nb][c][2] *= c0;
+        o[nb][c][3] *= c1;
+      }
+      // P^T (16 tokens x 8 heads) from the accumulator layout into the B-operand layout
+      pb[nb][0] = movmatrix_trans(pack2<TM>(p0, p1));
+      pb[nb][1] = movmatrix_trans(pack2<TM>(p2, p3));
     }
-    // P^T (16 tokens x 8 heads) from the accumulator layout into the B-operand layout
-    const uint32_t pb0 = movmatrix_trans(pack2<TM>(p0, p1));
-    const uint32_t pb1 = movmatrix_trans(pack2<TM>(p2, p3));
 
-    // ---- O^T += V^T P^T  (d_head x 8 heads)
+    // ---- O^T += V^T P^T  (d_head x 8 heads per block)
     if constexpr (F8) {
       // token rows 2c4, 2c4 + 1, 2c4 + 8, 2c4 + 9, bytes 16 trow .. 16 trow + 15 of each (chunk trow;
       // swizzle XOR = row & 7); step c takes d = 16 trow + 2c (A rows trow) and + 1 (rows trow + 8)
@@ -554,7 +591,8 @@ __global__ void __launch_bounds__(NW * 32) decode_tc_kernel(const __grid_constan
         uint32_t a0, a1, a2, a3;
         e4m3x4_to_f16x2x2(x, a0, a1);
         e4m3x4_to_f16x2x2(y, a2, a3);
-        mma_16816<BF16>(o[c], a0, a1, a2, a3, pb0, pb1);
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) mma_16816<BF16>(o[nb][c], a0, a1, a2, a3, pb[nb][0], pb[nb][1]);
       }
     } else {
 #pragma unroll
@@ -563,7 +601,8 @@ __global__ void __launch_bounds__(NW * 32) decode_tc_kernel(const __grid_constan
         const uint32_t addr = sv + (c >> 2) * (TILE * 128) + v_row * 128 + ((chunk ^ r8) << 4);
         uint32_t a0, a1, a2, a3;
         ldmatrix_x4_trans(addr, a0, a1, a2, a3);
-        mma_16816<BF16>(o[c], a0, a1, a2, a3, pb0, pb1);
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) mma_16816<BF16>(o[nb][c], a0, a1, a2, a3, pb[nb][0], pb[nb][1]);
       }
     }
 
@@ -572,31 +611,46 @@ __global__ void __launch_bounds__(NW * 32) decode_tc_kernel(const __grid_constan
 
     // ---- end of this pair within the range: write the result or a partial
     if ((d.z & F_LAST) || i == n_my - 1) {
-      float L0 = l0, L1 = l1;
+      float Ls[NB][2];
 #pragma unroll
-      for (int off = 4; off < 32; off <<= 1) {
-        L0 += __shfl_xor_sync(0xffffffffu, L0, off);
-        L1 += __shfl_xor_sync(0xffffffffu, L1, off);
+      for (int nb = 0; nb < NB; ++nb) {
+        float L0 = l[nb][0], L1 = l[nb][1];
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+          L0 += __shfl_xor_sync(0xffffffffu, L0, off);
+          L1 += __shfl_xor_sync(0xffffffffu, L1, off);
+        }
+        Ls[nb][0] = L0;
+        Ls[nb][1] = L1;
       }
       const int s = cur_pair / a.H_kv, g = cur_pair - (cur_pair / a.H_kv) * a.H_kv;
       if (cur_started && (d.z & F_LAST)) {
-        const float i0 = a.v_mul / L0, i1 = a.v_mul / L1;
         TA* out = static_cast<TA*>(a.out) + (static_cast<int64_t>(s) * a.H_q + g * a.G) * D;
-        float4 acc4[C::NKC];
 #pragma unroll
-        for (int c = 0; c < C::NKC; ++c) acc4[c] = make_float4(o[c][0], o[c][1], o[c][2], o[c][3]);
-        store_group<TA, D, F8>(out, acc4, i0, i1, lane, a.G);
+        for (int nb = 0; nb < NB; ++nb) {
+          if (GPAD * nb >= a.G) break;
+          const float i0 = a.v_mul / Ls[nb][0], i1 = a.v_mul / Ls[nb][1];
+          float4 acc4[C::NKC];
+#pragma unroll
+          for (int c = 0; c < C::NKC; ++c) acc4[c] = make_float4(o[nb][c][0], o[nb][c][1], o[nb][c][2], o[nb][c][3]);
+          store_group<TA, D, F8>(out + GPAD * nb * D, acc4, i0, i1, lane, a.G - GPAD * nb);
+        }
       } else {
         const int slot = cur_first_in_range ? 0 : 1;
         float* ps = a.partials + static_cast<int64_t>(gw * 2 + slot) * C::PSTRIDE;
 #pragma unroll
-        for (int c = 0; c < C::NKC; ++c)
-          reinterpret_cast<float4*>(ps)[c * 32 + lane] = make_float4(o[c][0], o[c][1], o[c][2], o[c][3]);
-        if (lane < 4) {
-          ps[C::NKC * 128 + h0] = m0;
-          ps[C::NKC * 128 + h0 + 1] = m1;
-          ps[C::NKC * 128 + GPAD + h0] = L0;
-          ps[C::NKC * 128 + GPAD + h0 + 1] = L1;
+        for (int nb = 0; nb < NB; ++nb) {
+#pragma unroll
+          for (int c = 0; c < C::NKC; ++c)
+            reinterpret_cast<float4*>(ps + nb * C::OFL)[c * 32 + lane] =
+                make_float4(o[nb][c][0], o[nb][c][1], o[nb][c][2], o[nb][c][3]);
+          if (lane < 4) {
+            const int hm = NB * C::OFL + GPAD * nb + h0;
+            ps[hm] = m[nb][0];
+            ps[hm + 1] = m[nb][1];
+            ps[hm + C::GP] = Ls[nb][0];
+            ps[hm + C::GP + 1] = Ls[nb][1];
+          }
         }
         // the warp that writes a split pair's last partial merges it ("Chunked prefill
         // mechanics" rule): publish (the warp barrier orders every lane's writes before
@@ -613,7 +667,7 @@ __global__ void __launch_bounds__(NW * 32) decode_tc_kernel(const __grid_constan
         const int wa = pbeg / R, wb = (pbeg + nt - 1) / R;
         if (arrived == wb - wa) {
           __threadfence();
-          merge_pair<TA, D, F8>(a, s, g, pbeg, wa, wb, R, lane);
+          merge_pair<TA, D, F8, NB>(a, s, g, pbeg, wa, wb, R, lane);
         }
       }
     }
@@ -648,10 +702,18 @@ struct TcVariant {
 // FP8 tile carries half the bytes of a 16-bit one and more instructions, so its
 // default pipeline is twice as deep and its CTAs smaller: 4 stages x 2 warps, 4 CTAs
 // (8 warps) per SM, the same bytes in flight as the 16-bit default.
+// Groups of 9 to 16 query heads (two head blocks) hold twice the accumulators (255
+// registers a thread), so at most 8 warps fit an SM: every pool type takes 2 stages x
+// 4 warps there (FP8, agent 48 x 32,768 with 16-head groups: 0.81 of the copy peak, against
+// 0.79 for 3 x 2 and 0.61 for 4 x 2, which fits only 6 warps); FP8 is built in 3 x 2 as well.
 TcVariant tc_variant(const Pool& P) {
   static const TcVariant table[] = {{2, 4}, {3, 4}, {4, 4}, {2, 8}, {3, 2}, {6, 4}, {2, 2}, {4, 2}, {3, 1}};
-  int idx = P.geo.dtype == PKV_E4M3 ? 7 : 0;
-  if (const char* e = std::getenv("PKV_TC_VARIANT")) idx = std::max(0, std::min(8, std::atoi(e)));
+  const bool fp8 = P.geo.dtype == PKV_E4M3, wide = P.geo.H_q / P.geo.H_kv > GPAD;
+  int idx = fp8 && !wide ? 7 : 0;
+  if (const char* e = std::getenv("PKV_TC_VARIANT")) {
+    const int v = std::max(0, std::min(8, std::atoi(e)));
+    if (!wide || (fp8 && (v == 0 || v == 4))) idx = v;
+  }
   return table[idx];
 }
 
@@ -661,7 +723,7 @@ bool tc_eligible(const Pool& P) {
   const int64_t rows = g.num_blocks * g.L * g.H_kv * g.block_size;
   const bool dt = ((g.dtype == PKV_BF16 || g.dtype == PKV_F16) && (g.d_head == 64 || g.d_head == 128)) ||
                   (g.dtype == PKV_E4M3 && g.d_head == 128);
-  return dt && G <= GPAD && g.block_size % TILE == 0 && rows < (int64_t(1) << 31) && encode_fn() != nullptr;
+  return dt && G <= 2 * GPAD && g.block_size % TILE == 0 && rows < (int64_t(1) << 31) && encode_fn() != nullptr;
 }
 
 int device_sm_count(int* n) {
@@ -672,16 +734,26 @@ int device_sm_count(int* n) {
   return PKV_OK;
 }
 
-template <typename T, int D, int S, int NW>
+template <typename T, int D, int S, int NW, int NB = 1>
 const void* tc_kernel_ptr() {
-  return reinterpret_cast<const void*>(&decode_tc_kernel<T, D, S, NW>);
+  return reinterpret_cast<const void*>(&decode_tc_kernel<T, D, S, NW, NB>);
 }
 
 using KernelPtr = const void*;
 
 template <typename T, int D>
-KernelPtr pick_tc(const TcVariant& v, int* smem) {
+KernelPtr pick_tc(const TcVariant& v, int G, int* smem) {
   constexpr int EB = std::is_same<T, E4M3>::value ? 1 : 2;
+  if (G > GPAD) {  // two head blocks (the variants tc_variant allows for them)
+    if constexpr (EB == 1) {
+      if (v.stages == 3 && v.warps == 2) {
+        *smem = TcSmem<D, EB, 3, 2, 2>::TOTAL;
+        return tc_kernel_ptr<T, D, 3, 2, 2>();
+      }
+    }
+    *smem = TcSmem<D, EB, 2, 4, 2>::TOTAL;
+    return tc_kernel_ptr<T, D, 2, 4, 2>();
+  }
 #define PKV_TC_CASE(S_, NW_)                           \
   if (v.stages == S_ && v.warps == NW_) {              \
     *smem = TcSmem<D, EB, S_, NW_>::TOTAL;             \
@@ -705,10 +777,11 @@ KernelPtr pick_tc(const TcVariant& v, int* smem) {
 
 KernelPtr tc_kernel_for(const Pool& P, int* smem) {
   const TcVariant v = tc_variant(P);
-  if (P.geo.dtype == PKV_E4M3) return pick_tc<E4M3, 128>(v, smem);
+  const int G = P.geo.H_q / P.geo.H_kv;
+  if (P.geo.dtype == PKV_E4M3) return pick_tc<E4M3, 128>(v, G, smem);
   const bool bf = P.geo.dtype == PKV_BF16;
-  if (P.geo.d_head == 128) return bf ? pick_tc<__nv_bfloat16, 128>(v, smem) : pick_tc<__half, 128>(v, smem);
-  return bf ? pick_tc<__nv_bfloat16, 64>(v, smem) : pick_tc<__half, 64>(v, smem);
+  if (P.geo.d_head == 128) return bf ? pick_tc<__nv_bfloat16, 128>(v, G, smem) : pick_tc<__half, 128>(v, G, smem);
+  return bf ? pick_tc<__nv_bfloat16, 64>(v, G, smem) : pick_tc<__half, 64>(v, G, smem);
 }
 
 // Persistent grid for the tensor-core kernel: resident CTAs per SM x SM count.
@@ -754,14 +827,15 @@ struct WsLayout {
   size_t prefix, lens, counters, wstart, partials, total;
 };
 
-WsLayout ws_layout(int n_seq, int H_kv, int64_t total_warps, int D) {
+WsLayout ws_layout(int n_seq, int H_kv, int64_t total_warps, int D, int G) {
   WsLayout w;
   w.prefix = kHdrBytes;
   w.lens = w.prefix + align256(sizeof(int32_t) * (n_seq + 1));
   w.counters = w.lens + align256(sizeof(int32_t) * n_seq);
   w.wstart = w.counters + align256(sizeof(int32_t) * static_cast<size_t>(n_seq) * H_kv);
   w.partials = w.wstart + align256(sizeof(int4) * total_warps);
-  const int pstride = (D / 16) * 32 * 4 + 2 * GPAD;
+  const int nb = G > GPAD ? 2 : 1;  // head blocks (the kernel's TcCfg::PSTRIDE)
+  const int pstride = nb * (D / 16) * 32 * 4 + 2 * GPAD * nb;
   w.total = w.partials + align256(sizeof(float) * total_warps * 2 * pstride);
   return w;
 }
@@ -955,7 +1029,7 @@ int decode_workspace_bytes(const Pool& P, int32_t n_seq, size_t* bytes) {
     if (int rc = tc_grid(P, &grid, &nw, &smem)) return rc;
     warps_total = static_cast<int64_t>(grid) * nw;
   }
-  *bytes = ws_layout(n_seq, P.geo.H_kv, warps_total, P.geo.d_head).total;
+  *bytes = ws_layout(n_seq, P.geo.H_kv, warps_total, P.geo.d_head, P.geo.H_q / P.geo.H_kv).total;
   return PKV_OK;
 }
 
@@ -977,7 +1051,7 @@ int launch_decode(Pool& P, int32_t layer, const void* q, const void* k_pool, con
   if (tc_eligible(P)) {
     int grid = 0, nw = 0, smem = 0;
     if (int rc = tc_grid(P, &grid, &nw, &smem)) return rc;
-    const WsLayout L = ws_layout(n_seq, g.H_kv, static_cast<int64_t>(grid) * nw, g.d_head);
+    const WsLayout L = ws_layout(n_seq, g.H_kv, static_cast<int64_t>(grid) * nw, g.d_head, G);
     if (ws_bytes < L.total) return fail(PKV_ERR_INVALID_ARG, "workspace too small: need " + std::to_string(L.total));
     if ((reinterpret_cast<uintptr_t>(q) & 15) || (reinterpret_cast<uintptr_t>(out) & 15))
       return fail(PKV_ERR_INVALID_ARG, "q and out must be 16-byte aligned");
@@ -1011,10 +1085,11 @@ int launch_decode(Pool& P, int32_t layer, const void* q, const void* k_pool, con
 namespace pkv {
 namespace {
 
-// 12 MiB: the stream-K partials of one persistent grid (about 10 MB on a 152-SM
-// GB300) plus per-sequence prefix and length arrays.  Held by every GPU that loads
-// the library until the process exits.
-constexpr size_t kNoallocScratchBytes = size_t(12) << 20;
+// 24 MiB: the stream-K partials of one persistent grid (about 10 MB on a 152-SM
+// GB300 for groups of up to 8 query heads, about 20 MB for 9 to 16) plus
+// per-sequence prefix and length arrays.  Held by every GPU that loads the library
+// until the process exits.
+constexpr size_t kNoallocScratchBytes = size_t(24) << 20;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
 
 // Device address of g_noalloc_scratch on the current device, looked up once per
@@ -1080,7 +1155,7 @@ extern "C" int pkv_decode_attention_noalloc(const pkv_pool* pool, int32_t layer,
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess || per_sm < 1) return fail(PKV_ERR_CUDA, std::string("grid query: ") + cudaGetErrorString(e));
   const int grid = per_sm * sms;
-  const WsLayout L = ws_layout(n_seq, g.H_kv, static_cast<int64_t>(grid) * nw, g.d_head);
+  const WsLayout L = ws_layout(n_seq, g.H_kv, static_cast<int64_t>(grid) * nw, g.d_head, G);
   if (L.total > kNoallocScratchBytes)
     return fail(PKV_ERR_INVALID_ARG, "pkv_decode_attention_noalloc: this batch needs " + std::to_string(L.total) +
                                          " bytes of scratch, more than the static " +

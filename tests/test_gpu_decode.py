@@ -56,12 +56,40 @@ def test_gqa_bf16_ragged_lengths(lens):
     (16, 2, 96, 16, "bf16"),    # d = 96: CUDA-core path
     (12, 12, 64, 16, "f32"),
     (16, 4, 128, 16, "f32"),
-    (32, 2, 128, 16, "bf16"),   # G = 16: CUDA-core path
-    (48, 4, 64, 16, "f16"),     # G = 12: CUDA-core path
+    (32, 2, 128, 16, "bf16"),   # G = 16 on tensor cores (two 8-head blocks)
+    (48, 4, 64, 16, "f16"),     # G = 12 on tensor cores
+    (32, 2, 96, 16, "f16"),     # G = 16, d = 96: CUDA-core path
+    (16, 1, 64, 16, "f32"),     # G = 16, fp32: CUDA-core path
 ])
 def test_geometries(H_q, H_kv, d, B, dtype):
     g = W.Geometry(L=2, H_q=H_q, H_kv=H_kv, d_head=d, block_size=B, dtype=dtype, num_blocks=600)
     run_case(g, [3, 40, 129, 700, 1], 11, steps=1)
+
+
+@pytest.mark.parametrize("H_q,H_kv,d,dtype", [
+    (32, 2, 128, "bf16"),   # G = 16
+    (72, 8, 128, "bf16"),   # G = 9: seven padded heads in the second block
+    (48, 4, 64, "f16"),     # G = 12
+    (128, 8, 128, "bf16"),  # G = 16 with 8 KV heads (a 128-query-head layer)
+    (80, 8, 64, "bf16"),    # G = 10
+])
+def test_wide_groups_on_tensor_cores(H_q, H_kv, d, dtype):
+    """9 to 16 query heads per KV head run on the tensor-core kernel with two 8-head
+    column blocks (a plan launch and an attention launch per call); the lengths make
+    pairs that end inside one warp's range and pairs split across warps (merged
+    partials), ragged tails and an empty sequence."""
+    g = W.Geometry(L=2, H_q=H_q, H_kv=H_kv, d_head=d, block_size=16, dtype=dtype, num_blocks=1500)
+    b = PagedBatch(g, W.permutation(61, f"fo{H_q}{d}", g.num_blocks), seed=61)
+    lens = [3, 40, 129, 700, 1, 0, 4000, 17, 2049, 15, 16, 300]
+    ids = b.new_seqs(len(lens))
+    b.append(ids, lens, "p", layer=1)
+    b.append(ids, [1] * len(ids), "t", layer=1)
+    for step, scale in enumerate([1 / math.sqrt(d), 0.3]):
+        q = W.normal(61, f"q{step}", (len(ids), g.H_q, g.d_head), dtype)
+        before = pkv.pkv_launch_count()
+        got, tables, sl = b.decode_gpu(ids, q, scale, layer=1)
+        assert pkv.pkv_launch_count() - before == 2  # plan + tensor-core attention
+        check_attention(got, b.decode_ref(q, tables, sl, scale, layer=1), dtype)
 
 
 def test_long_single_sequence_split_across_many_warps():
