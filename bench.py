@@ -242,6 +242,19 @@ class DecodeRunner:
         self.h2d_meta = 0
         self.e2e_in_bytes = 0
         self.e2e_out_bytes = 0
+        self.l2_flush = None  # a device buffer larger than L2, rewritten after every step when set
+
+    def enable_l2_flush(self):
+        """Write 256 MB (twice the L2) after every step, so that no step finds the previous
+        step's K/V in L2.  The write runs inside the whole-step time; the decode call's own
+        CUDA events do not include it."""
+        self.l2_flush = self.torch.empty(64 << 20, dtype=self.torch.int32, device=self.dev)
+        self.config["l2"] = ("flushed: 256 MB written after every step (inside the whole-step time, outside "
+                             "the decode call's events); " + self.config.get("l2", ""))
+
+    def flush_l2(self, t):
+        if self.l2_flush is not None:
+            self.l2_flush.fill_(t)
 
     # subclasses set: g, pool, ids (live batch in order), kp, vp, Wd, scale,
     # q/kn/vn device tensors [steps][n_max][...], and implement running(t)
@@ -320,6 +333,7 @@ class DecodeRunner:
                            self.stream)
         if rc:
             pkv._check(rc, "pkv_decode_step")
+        self.flush_l2(t)
         nbytes = self.staging.mark(k, n * (self.Wd + 2))
         if timed:
             self.decode_ms.append(events)
@@ -361,6 +375,7 @@ class DecodeRunner:
                 pkv.pkv_step_launch_host(pool, 0, n, self.Wd, cows, host[0][t][:n], host[1][t][:n], host[2][t][:n],
                                          self.out_host[:n], q, kn, vn, self.out[:n], self.kp, self.vp, self.scale,
                                          hbuf, dmeta, self.ws, attn_events=events[i] if events else None)
+                self.flush_l2(t)
                 nbytes = self.staging.mark(k, n * (self.Wd + 2))
                 self.pool = pool
                 self.after_step(t, ids)
@@ -592,6 +607,8 @@ def run_decode(args, torch, pkv, dev, world, rank):
                         q_heads=args.q_heads, **kw)
     else:
         r = RUNNERS[args.workload](torch, pkv, dev, total, **kw)
+    if args.l2_flush:
+        r.enable_l2_flush()
     g = r.g
     launches0 = None
     for t in range(args.warmup):
@@ -1148,6 +1165,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--context", type=int, default=0, help="agent workload: tokens per sequence (default 32768)")
     ap.add_argument("--n-seq", type=int, default=0, help="agent workload: sequences (default 48)")
+    ap.add_argument("--l2-flush", action="store_true",
+                    help="decode workloads: overwrite a 256 MB buffer after every step (forked: the prefix "
+                         "then comes from HBM at each step's first read)")
     ap.add_argument("--q-heads", type=int, default=0,
                     help="agent workload: query heads over its 8 KV heads (default 64; 128 = groups of 16)")
     ap.add_argument("--kv-dtype", choices=["bf16", "e4m3"], default="bf16",

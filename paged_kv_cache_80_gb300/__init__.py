@@ -403,12 +403,7 @@ def pkv_decode_step(pool: PoolLike, layer: int, seq_ids, W: int, q, k_new, v_new
     n = ids.size
     if meta_host.numel() < n * (W + 2) or meta_dev.numel() < n * (W + 2):
         raise ValueError("metadata buffers smaller than n * (W + 2)")
-    ev0 = ev1 = None
-    if attn_events is not None:
-        for ev in attn_events:
-            if not ev.cuda_event:  # torch creates its CUDA event at the first record
-                ev.record()
-        ev0, ev1 = attn_events[0].cuda_event, attn_events[1].cuda_event
+    ev0, ev1 = _events(attn_events)
     _check(_L().pkv_decode_step(_h(pool), layer, _p32(ids), n, W, _dev(q, "q"), _dev(k_new, "k_new"),
                                 _dev(v_new, "v_new"), _dev(k_pool, "k_pool"), _dev(v_pool, "v_pool"), float(scale),
                                 _dev(out, "out"), _host_ptr(meta_host, "meta_host"), _dev(meta_dev, "meta_dev"),
@@ -428,14 +423,10 @@ def pkv_decode_step_host(pool: PoolLike, layer: int, seq_ids, W: int, q_host, k_
         raise ValueError("metadata buffers smaller than n * (W + 2)")
     for t, d, what in ((q_host, q_dev, "q"), (k_new_host, k_new_dev, "k_new"), (v_new_host, v_new_dev, "v_new"),
                        (out_host, out_dev, "out")):
-        if t.numel() < n * t[0].numel() or d.numel() < n * t[0].numel():
+        row = t[0].numel() if t.dim() > 0 and t.shape[0] > 0 else 0
+        if t.dim() == 0 or t.shape[0] < n or d.dim() == 0 or d.shape[0] < n or d.numel() < n * row:
             raise ValueError(f"{what} buffers hold fewer than n rows")
-    ev0 = ev1 = None
-    if attn_events is not None:
-        for ev in attn_events:
-            if not ev.cuda_event:  # torch creates its CUDA event at the first record
-                ev.record()
-        ev0, ev1 = attn_events[0].cuda_event, attn_events[1].cuda_event
+    ev0, ev1 = _events(attn_events)
     _check(_L().pkv_decode_step_host(_h(pool), layer, _p32(ids), n, W, _host_ptr(q_host, "q_host"),
                                      _host_ptr(k_new_host, "k_new_host"), _host_ptr(v_new_host, "v_new_host"),
                                      _host_ptr(out_host, "out_host"), _dev(q_dev, "q_dev"), _dev(k_new_dev, "k_new_dev"),
