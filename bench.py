@@ -454,13 +454,7 @@ class AgentRunner(DecodeRunner):
         self.Wd = -(-(context + total_steps + 1) // g.block_size)
         self.inputs_for_steps("agent")
         self._alloc_common(n_seq)
-        self.config = {"workload": f"agent{context // 1024}k: {n_seq} sequences x {context} tokens, {g.H_q} query / "
-                                   f"{g.H_kv} KV heads, d_head 128, {kv_desc(g)}, 16-token blocks, permuted block ids",
-                       "n_seq": n_seq, "context": context, "H_q": g.H_q, "H_kv": g.H_kv, "d_head": g.d_head,
-                       "block_size": g.block_size, "pool_blocks": g.num_blocks,
-                       "l2": f"inputs larger than L2 ({n_seq * context * 2048 * g.elem_bytes / 1e9:.2f} GB of K/V "
-                             f"per step)",
-                       "parallelism": "replicas (no collectives)"}
+        self.config = dict(workload_config("agent32k", g, n_seq, context), pool_blocks=g.num_blocks)
 
     def running(self, t):
         return self.ids_np
@@ -491,13 +485,7 @@ class ChatRunner(DecodeRunner):
         self.pool = self.states[0][0]
         self.inputs_for_steps("chat")
         self._alloc_common(n_seq)
-        self.config = {"workload": "chat: 256 sequences, lognormal prompt (mean 217) + generated (mean 154) "
-                                   f"lengths <= 1024, 64 query / 8 KV heads, d_head 128, {kv_desc(g)}, 16-token blocks, "
-                                   "32,768-block pool in shuffled order, 64-step schedule",
-                       "n_seq": n_seq, "H_q": g.H_q, "H_kv": g.H_kv, "d_head": g.d_head,
-                       "block_size": g.block_size, "pool_blocks": g.num_blocks,
-                       "l2": "inputs larger than L2 (0.2-0.3 GB of K/V per step)",
-                       "parallelism": "replicas (no collectives)"}
+        self.config = dict(workload_config("chat", g, n_seq), pool_blocks=g.num_blocks)
 
     def _fresh_state(self):
         pkv = self.pkv
@@ -546,13 +534,7 @@ class ForkedRunner(DecodeRunner):
         self.Wd = -(-(int(wl.lengths[0]) + 2048 + total_steps + 1) // g.block_size)
         self.inputs_for_steps("forked")
         self._alloc_common(n_branch)
-        self.config = {"workload": "forked: 16,376-token prefix forked into 64 branches (refcount 65) with "
-                                   f"U[0,2048] suffixes, 64 query / 8 KV heads, d_head 128, {kv_desc(g)}, 16-token "
-                                   "blocks",
-                       "n_seq": n_branch, "prefix": int(wl.lengths[0]), "H_q": g.H_q, "H_kv": g.H_kv,
-                       "d_head": g.d_head, "block_size": g.block_size,
-                       "l2": "logical K/V per step 4.5 GB > L2; the 67 MB shared prefix is re-read by every branch",
-                       "parallelism": "replicas (no collectives)"}
+        self.config = workload_config("forked", g, n_branch, prefix=int(wl.lengths[0]))
 
     def running(self, t):
         return self.ids_np
@@ -579,10 +561,7 @@ class TinyRunner(DecodeRunner):
         self.Wd = -(-(512 + total_steps + 1) // g.block_size)
         self.inputs_for_steps("tiny")
         self._alloc_common(self.n_max)
-        self.config = {"workload": "tiny: GPT-2-small geometry (12 heads, d_head 64, fp32), 8 sequences of "
-                                   "U[1,512] tokens, 512-block permuted pool",
-                       "n_seq": self.n_max, "l2": "inputs smaller than L2 (launch-bound case)",
-                       "parallelism": "replicas (no collectives)"}
+        self.config = workload_config("tiny", self.g, self.n_max)
 
     def running(self, t):
         return self.ids_np
@@ -594,6 +573,34 @@ def with_kv_dtype(g, kv_dtype):
 
 def kv_desc(g):
     return "FP8 E4M3 K/V (bf16 q/out)" if g.dtype == "e4m3" else g.dtype
+
+
+def workload_config(name, g, n_seq, context=0, prefix=0):
+    """The bench line's config for a decode workload (both arms print the same one)."""
+    rep = "replicas (no collectives)"
+    if name == "agent32k":
+        return {"workload": f"agent{context // 1024}k: {n_seq} sequences x {context} tokens, {g.H_q} query / "
+                            f"{g.H_kv} KV heads, d_head 128, {kv_desc(g)}, 16-token blocks, permuted block ids",
+                "n_seq": n_seq, "context": context, "H_q": g.H_q, "H_kv": g.H_kv, "d_head": g.d_head,
+                "block_size": g.block_size,
+                "l2": f"inputs larger than L2 ({n_seq * context * 2048 * g.elem_bytes / 1e9:.2f} GB of K/V per step)",
+                "parallelism": rep}
+    if name == "chat":
+        return {"workload": "chat: 256 sequences, lognormal prompt (mean 217) + generated (mean 154) "
+                            f"lengths <= 1024, 64 query / 8 KV heads, d_head 128, {kv_desc(g)}, 16-token blocks, "
+                            "32,768-block pool in shuffled order, 64-step schedule",
+                "n_seq": n_seq, "H_q": g.H_q, "H_kv": g.H_kv, "d_head": g.d_head, "block_size": g.block_size,
+                "l2": "inputs larger than L2 (0.2-0.3 GB of K/V per step)", "parallelism": rep}
+    if name == "forked":
+        return {"workload": "forked: 16,376-token prefix forked into 64 branches (refcount 65) with "
+                            f"U[0,2048] suffixes, 64 query / 8 KV heads, d_head 128, {kv_desc(g)}, 16-token blocks",
+                "n_seq": n_seq, "prefix": prefix, "H_q": g.H_q, "H_kv": g.H_kv, "d_head": g.d_head,
+                "block_size": g.block_size,
+                "l2": "logical K/V per step 4.5 GB > L2; the 67 MB shared prefix is re-read by every branch",
+                "parallelism": rep}
+    return {"workload": "tiny: GPT-2-small geometry (12 heads, d_head 64, fp32), 8 sequences of "
+                        "U[1,512] tokens, 512-block permuted pool",
+            "n_seq": n_seq, "l2": "inputs smaller than L2 (launch-bound case)", "parallelism": rep}
 
 
 RUNNERS = {"agent32k": AgentRunner, "chat": ChatRunner, "forked": ForkedRunner, "tiny": TinyRunner}
@@ -1082,7 +1089,7 @@ def reference_arm(args, world, rank):
         config = {"workload": "swap: 80-layer 70B GQA geometry, 5 MiB blocks (sampled)"}
         dtype = "bf16"
     else:
-        spec = {"agent32k": (lambda: W.agent(48, 32768, 256), 2),
+        spec = {"agent32k": (lambda: W.agent(args.n_seq or 48, args.context or 32768, 256), 2),
                 "chat": (lambda: W.chat(), 64),
                 "forked": (lambda: W.forked(), 4),
                 "tiny": (lambda: W.tiny(), 8)}[args.workload]
@@ -1118,7 +1125,11 @@ def reference_arm(args, world, rank):
         bytes_step = int(lens.astype(np.int64).sum()) * g.H_kv * g.d_head * g.elem_bytes * 2
         value = bytes_step / statistics.mean(times) / 1e9
         desc = f"oracle attention over {n_s} sequences ({int(lens.sum())} tokens) of the {args.workload} workload"
-        config = {"workload": args.workload, "sampled_sequences": n_s}
+        # the same config as this workload's line from the library arm, plus the sample size
+        n_full = {"agent32k": args.n_seq or 48, "chat": 256, "forked": 64, "tiny": 8}[args.workload]
+        config = dict(workload_config(args.workload, g, n_full, context=args.context or 32768,
+                                      prefix=int(wl.lengths[0]) if args.workload == "forked" else 0),
+                      sampled_sequences=n_s)
         dtype = g.dtype
     t_step = statistics.mean(times)
     return {
