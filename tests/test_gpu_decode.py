@@ -66,19 +66,20 @@ def test_geometries(H_q, H_kv, d, B, dtype):
     run_case(g, [3, 40, 129, 700, 1], 11, steps=1)
 
 
-@pytest.mark.parametrize("H_q,H_kv,d,dtype", [
-    (32, 2, 128, "bf16"),   # G = 16
-    (72, 8, 128, "bf16"),   # G = 9: seven padded heads in the second block
-    (48, 4, 64, "f16"),     # G = 12
-    (128, 8, 128, "bf16"),  # G = 16 with 8 KV heads (a 128-query-head layer)
-    (80, 8, 64, "bf16"),    # G = 10
+@pytest.mark.parametrize("H_q,H_kv,d,dtype,B", [
+    (32, 2, 128, "bf16", 16),   # G = 16
+    (72, 8, 128, "bf16", 16),   # G = 9: seven padded heads in the second block
+    (48, 4, 64, "f16", 16),     # G = 12
+    (128, 8, 128, "bf16", 16),  # G = 16 with 8 KV heads (a 128-query-head layer)
+    (80, 8, 64, "bf16", 16),    # G = 10
+    (32, 2, 128, "f16", 32),    # G = 16, 32-token blocks
 ])
-def test_wide_groups_on_tensor_cores(H_q, H_kv, d, dtype):
+def test_wide_groups_on_tensor_cores(H_q, H_kv, d, dtype, B):
     """9 to 16 query heads per KV head run on the tensor-core kernel with two 8-head
     column blocks (a plan launch and an attention launch per call); the lengths make
     pairs that end inside one warp's range and pairs split across warps (merged
     partials), ragged tails and an empty sequence."""
-    g = W.Geometry(L=2, H_q=H_q, H_kv=H_kv, d_head=d, block_size=16, dtype=dtype, num_blocks=1500)
+    g = W.Geometry(L=2, H_q=H_q, H_kv=H_kv, d_head=d, block_size=B, dtype=dtype, num_blocks=1500)
     b = PagedBatch(g, W.permutation(61, f"fo{H_q}{d}", g.num_blocks), seed=61)
     lens = [3, 40, 129, 700, 1, 0, 4000, 17, 2049, 15, 16, 300]
     ids = b.new_seqs(len(lens))
