@@ -106,14 +106,14 @@ def _L():
             "pkv_copy_blocks": ([vp, P32, i32, vp, vp, vp], ctypes.c_int),
             "pkv_prefill_attention": ([vp, i32, vp, vp, i32, i32, vp, vp, vp, i32, vp, i32, ctypes.c_float, vp, vp],
                                       ctypes.c_int),
-            "pkv_decode_step": ([vp, i32, P32, i32, i32, vp, vp, vp, vp, vp, ctypes.c_float, vp, vp, vp, vp,
+            "pkv_decode_step": ([vp, i32, vp, i32, i32, vp, vp, vp, vp, vp, ctypes.c_float, vp, vp, vp, vp,
                                  ctypes.c_size_t, vp, vp, vp], ctypes.c_int),
-            "pkv_decode_step_host": ([vp, i32, P32, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_float,
+            "pkv_decode_step_host": ([vp, i32, vp, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_float,
                                       vp, vp, vp, ctypes.c_size_t, vp, vp, vp], ctypes.c_int),
-            "pkv_step_plan": ([vp, P32, i32, i32, vp, P32, P32], ctypes.c_int),
-            "pkv_step_launch": ([vp, i32, i32, i32, P32, i32, vp, vp, vp, vp, vp, ctypes.c_float, vp, vp, vp, vp,
+            "pkv_step_plan": ([vp, vp, i32, i32, vp, vp, P32], ctypes.c_int),
+            "pkv_step_launch": ([vp, i32, i32, i32, vp, i32, vp, vp, vp, vp, vp, ctypes.c_float, vp, vp, vp, vp,
                                  ctypes.c_size_t, vp, vp, vp], ctypes.c_int),
-            "pkv_step_launch_host": ([vp, i32, i32, i32, P32, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+            "pkv_step_launch_host": ([vp, i32, i32, i32, vp, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                       ctypes.c_float, vp, vp, vp, ctypes.c_size_t, vp, vp, vp], ctypes.c_int),
             "pkv_swap_out": ([vp, i32, vp, vp, vp, i64, P64, i32, P32, vp], ctypes.c_int),
             "pkv_swap_in": ([vp, i32, vp, i64, i32, vp, vp, P32, vp], ctypes.c_int),
@@ -165,6 +165,12 @@ def _p32(a: np.ndarray):
 
 def _p64(a: np.ndarray):
     return a.ctypes.data_as(ctypes.POINTER(ctypes.c_int64))
+
+
+def _a(a: np.ndarray) -> int:
+    """Address of a contiguous numpy array, for parameters declared as void pointers (the
+    per-step calls: cheaper than building a typed ctypes pointer)."""
+    return a.ctypes.data
 
 
 def _dev(t, what: str) -> int:
@@ -404,7 +410,7 @@ def pkv_decode_step(pool: PoolLike, layer: int, seq_ids, W: int, q, k_new, v_new
     if meta_host.numel() < n * (W + 2) or meta_dev.numel() < n * (W + 2):
         raise ValueError("metadata buffers smaller than n * (W + 2)")
     ev0, ev1 = _events(attn_events)
-    _check(_L().pkv_decode_step(_h(pool), layer, _p32(ids), n, W, _dev(q, "q"), _dev(k_new, "k_new"),
+    _check(_L().pkv_decode_step(_h(pool), layer, _a(ids), n, W, _dev(q, "q"), _dev(k_new, "k_new"),
                                 _dev(v_new, "v_new"), _dev(k_pool, "k_pool"), _dev(v_pool, "v_pool"), float(scale),
                                 _dev(out, "out"), _host_ptr(meta_host, "meta_host"), _dev(meta_dev, "meta_dev"),
                                 _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(), ev0, ev1,
@@ -427,7 +433,7 @@ def pkv_decode_step_host(pool: PoolLike, layer: int, seq_ids, W: int, q_host, k_
         if t.dim() == 0 or t.shape[0] < n or d.dim() == 0 or d.shape[0] < n or d.numel() < n * row:
             raise ValueError(f"{what} buffers hold fewer than n rows")
     ev0, ev1 = _events(attn_events)
-    _check(_L().pkv_decode_step_host(_h(pool), layer, _p32(ids), n, W, _host_ptr(q_host, "q_host"),
+    _check(_L().pkv_decode_step_host(_h(pool), layer, _a(ids), n, W, _host_ptr(q_host, "q_host"),
                                      _host_ptr(k_new_host, "k_new_host"), _host_ptr(v_new_host, "v_new_host"),
                                      _host_ptr(out_host, "out_host"), _dev(q_dev, "q_dev"), _dev(k_new_dev, "k_new_dev"),
                                      _dev(v_new_dev, "v_new_dev"), _dev(out_dev, "out_dev"), _dev(k_pool, "k_pool"),
@@ -446,7 +452,7 @@ def pkv_step_plan(pool: PoolLike, seq_ids, W: int, meta_host) -> np.ndarray:
         raise ValueError("meta_host smaller than n * (W + 2)")
     cows = np.zeros(max(2 * n, 2), np.int32)
     n_cow = ctypes.c_int32(0)
-    _check(_L().pkv_step_plan(_h(pool), _p32(ids), n, W, _host_ptr(meta_host, "meta_host"), _p32(cows),
+    _check(_L().pkv_step_plan(_h(pool), _a(ids), n, W, _host_ptr(meta_host, "meta_host"), _a(cows),
                               ctypes.byref(n_cow)), "pkv_step_plan")
     return cows[: 2 * n_cow.value].reshape(-1, 2)
 
@@ -465,7 +471,7 @@ def pkv_step_launch(pool: PoolLike, layer: int, n: int, W: int, cow_pairs, q, k_
     """The device half of a decode step planned by pkv_step_plan (device q / k_new / v_new / out)."""
     cp = _i32(cow_pairs).reshape(-1)
     ev0, ev1 = _events(attn_events)
-    _check(_L().pkv_step_launch(_h(pool), layer, n, W, _p32(cp), cp.size // 2, _dev(q, "q"), _dev(k_new, "k_new"),
+    _check(_L().pkv_step_launch(_h(pool), layer, n, W, _a(cp), cp.size // 2, _dev(q, "q"), _dev(k_new, "k_new"),
                                 _dev(v_new, "v_new"), _dev(k_pool, "k_pool"), _dev(v_pool, "v_pool"), float(scale),
                                 _dev(out, "out"), _host_ptr(meta_host, "meta_host"), _dev(meta_dev, "meta_dev"),
                                 _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(), ev0, ev1,
@@ -478,7 +484,7 @@ def pkv_step_launch_host(pool: PoolLike, layer: int, n: int, W: int, cow_pairs, 
     """pkv_step_launch with host input and result tensors (page-locked) copied inside the call."""
     cp = _i32(cow_pairs).reshape(-1)
     ev0, ev1 = _events(attn_events)
-    _check(_L().pkv_step_launch_host(_h(pool), layer, n, W, _p32(cp), cp.size // 2, _host_ptr(q_host, "q_host"),
+    _check(_L().pkv_step_launch_host(_h(pool), layer, n, W, _a(cp), cp.size // 2, _host_ptr(q_host, "q_host"),
                                      _host_ptr(k_new_host, "k_new_host"), _host_ptr(v_new_host, "v_new_host"),
                                      _host_ptr(out_host, "out_host"), _dev(q_dev, "q_dev"), _dev(k_new_dev, "k_new_dev"),
                                      _dev(v_new_dev, "v_new_dev"), _dev(out_dev, "out_dev"), _dev(k_pool, "k_pool"),
