@@ -20,8 +20,8 @@ from helpers import PagedBatch, check_attention, out_f64, to_dev, torch_dtype
 pytestmark = pytest.mark.gpu
 
 
-def _batch():
-    g = W.Geometry(L=1, H_q=64, H_kv=8, d_head=128, block_size=16, dtype="bf16", num_blocks=4096)
+def _batch(H_q=64):
+    g = W.Geometry(L=1, H_q=H_q, H_kv=8, d_head=128, block_size=16, dtype="bf16", num_blocks=4096)
     b = PagedBatch(g, W.permutation(31, "fo", g.num_blocks), seed=31, host_pool=False)
     lens = [int(x) for x in W.uniform_int(31, "lens", 0, 700, 40)] + [20000, 1, 16, 17]
     ids = b.new_seqs(len(lens))
@@ -30,10 +30,11 @@ def _batch():
     return b, ids
 
 
-def test_noalloc_matches_workspace_entry_point_twice():
+@pytest.mark.parametrize("H_q", [64, 128])  # groups of 8, and of 16 (twice the partials)
+def test_noalloc_matches_workspace_entry_point_twice(H_q):
     import torch
 
-    b, ids = _batch()
+    b, ids = _batch(H_q)
     g = b.g
     tables, lens = b.tables(ids)
     d_tables = torch.from_numpy(tables).cuda()
