@@ -352,7 +352,8 @@ class DecodeRunner:
         host memory and its result is read on the host before the next step's inputs are
         sent.  The host half of step t + 1 (pkv_step_plan: slots, tables, CoW pairs -- it needs
         no result of step t) runs while step t is on the GPU, as a serving loop's scheduler
-        does; the device half (pkv_step_launch_host) copies the inputs in, runs the step and
+        does; the device half (pkv_step_launch_host through a StepLauncher, which binds the
+        buffers that stay the same from step to step) copies the inputs in, runs the step and
         copies the result out."""
         torch, pkv, g = self.torch, self.pkv, self.g
 
@@ -376,10 +377,8 @@ class DecodeRunner:
                     return x if x.shape[0] == n else x[:n]
 
                 q, kn, vn = rows(self.q_e2e), rows(self.kn_e2e), rows(self.vn_e2e)
-                pkv.pkv_step_launch_host(pool, 0, n, self.Wd, cows, rows(host[0][t]), rows(host[1][t]),
-                                         rows(host[2][t]), rows(self.out_host), q, kn, vn, rows(self.out), self.kp,
-                                         self.vp, self.scale, hbuf, dmeta, self.ws,
-                                         attn_events=events[i] if events else None)
+                self.launcher_for(pool)(n, self.Wd, cows, rows(host[0][t]), rows(host[1][t]), rows(host[2][t]),
+                                        rows(self.out_host), hbuf, dmeta, attn_events=events[i] if events else None)
                 self.flush_l2(t)
                 nbytes = self.staging.mark(k, n * (self.Wd + 2))
                 self.pool = pool
@@ -401,6 +400,17 @@ class DecodeRunner:
                 self.h2d_meta += nbytes
             self.e2e_in_bytes += nbytes + (q.numel() + kn.numel() + vn.numel()) * self.act_bytes
             self.e2e_out_bytes += n * g.H_q * g.d_head * self.act_bytes
+
+    def launcher_for(self, pool):
+        """pkv_step_launch_host with this runner's device staging, pools, scale and workspace
+        bound once (a StepLauncher per control-plane state)."""
+        if not hasattr(self, "_launchers"):
+            self._launchers = {}
+        key = id(pool)
+        if key not in self._launchers:
+            self._launchers[key] = self.pkv.StepLauncher(pool, 0, self.q_e2e, self.kn_e2e, self.vn_e2e, self.out,
+                                                         self.kp, self.vp, self.scale, self.ws)
+        return self._launchers[key]
 
     def _refresh_handle(self):
         self._fast_pool = self.pool

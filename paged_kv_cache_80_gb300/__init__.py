@@ -21,6 +21,7 @@ __all__ = [
     "pkv_seq_free", "pkv_seq_len", "pkv_plan_append", "pkv_export_tables", "pkv_refcounts", "pkv_free_list",
     "pkv_append_kv", "pkv_decode_workspace_size", "pkv_decode_attention", "pkv_decode_attention_noalloc",
     "pkv_decode_step", "pkv_decode_step_host", "pkv_step_plan", "pkv_step_launch", "pkv_step_launch_host",
+    "StepLauncher",
     "pkv_prefill_attention",
     "pkv_copy_blocks", "pkv_swap_out",
     "pkv_swap_in", "pkv_seq_host_slots", "pkv_seq_residency", "TIER_HBM", "TIER_HOST", "pkv_pool_set_swap_engine", "pkv_check_device_error", "pkv_launch_count",
@@ -492,6 +493,40 @@ def pkv_step_launch_host(pool: PoolLike, layer: int, n: int, W: int, cow_pairs, 
                                      _dev(meta_dev, "meta_dev"), _dev(workspace, "workspace"),
                                      workspace.numel() * workspace.element_size(), ev0, ev1, _stream(stream)),
            "pkv_step_launch_host")
+
+
+class StepLauncher:
+    """pkv_step_launch_host with the buffers that stay the same from step to step bound once:
+    the device staging tensors (q, k_new, v_new, out: the first n rows are used), the pools,
+    the workspace, the scale and the stream (torch's current stream at construction when
+    None).  Each call then takes only what changes per step, so a serving loop's host side
+    is shorter; the result is the same as pkv_step_launch_host's."""
+
+    def __init__(self, pool: PoolLike, layer: int, q_dev, k_new_dev, v_new_dev, out_dev, k_pool, v_pool,
+                 scale: float, workspace, stream=None):
+        self._h = _h(pool)
+        self._layer = int(layer)
+        self._rows = min(int(t.shape[0]) for t in (q_dev, k_new_dev, v_new_dev, out_dev))
+        self._dev = (_dev(q_dev, "q_dev"), _dev(k_new_dev, "k_new_dev"), _dev(v_new_dev, "v_new_dev"),
+                     _dev(out_dev, "out_dev"), _dev(k_pool, "k_pool"), _dev(v_pool, "v_pool"))
+        self._scale = float(scale)
+        self._ws = (_dev(workspace, "workspace"), workspace.numel() * workspace.element_size())
+        self._stream = _stream(stream)
+        self._f = _L().pkv_step_launch_host
+        self._keep = (q_dev, k_new_dev, v_new_dev, out_dev, k_pool, v_pool, workspace)  # keep them alive
+
+    def __call__(self, n: int, W: int, cow_pairs, q_host, k_new_host, v_new_host, out_host, meta_host, meta_dev,
+                 attn_events=None) -> None:
+        if n > self._rows:
+            raise ValueError(f"n = {n} exceeds the {self._rows} rows of the bound device buffers")
+        cp = _i32(cow_pairs).reshape(-1)
+        ev0, ev1 = _events(attn_events)
+        q, k, v, o, kp, vp = self._dev
+        _check(self._f(self._h, self._layer, n, W, _a(cp), cp.size // 2, _host_ptr(q_host, "q_host"),
+                       _host_ptr(k_new_host, "k_new_host"), _host_ptr(v_new_host, "v_new_host"),
+                       _host_ptr(out_host, "out_host"), q, k, v, o, kp, vp, self._scale,
+                       _host_ptr(meta_host, "meta_host"), _dev(meta_dev, "meta_dev"), self._ws[0], self._ws[1], ev0,
+                       ev1, self._stream), "pkv_step_launch_host")
 
 
 def pkv_prefill_attention(pool: PoolLike, layer: int, q, q_offsets, max_q: int, k_pool, v_pool, block_tables,

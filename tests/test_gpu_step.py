@@ -117,11 +117,12 @@ def test_decode_step_host_buffers_match_oracle(dtype):
     b.check_pools_bitexact()
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "e4m3"])
-def test_step_plan_ahead_then_launch_host_match_oracle(dtype):
-    """pkv_step_plan of step t + 1 runs while step t (pkv_step_launch_host) is on the GPU, as a
-    serving loop's scheduler would; every step's result matches the oracle and the pools and
-    control-plane state stay identical to the oracle's."""
+@pytest.mark.parametrize("dtype,api", [("bf16", "function"), ("e4m3", "function"), ("bf16", "launcher")])
+def test_step_plan_ahead_then_launch_host_match_oracle(dtype, api):
+    """pkv_step_plan of step t + 1 runs while step t (pkv_step_launch_host, or a StepLauncher
+    with the fixed buffers bound once) is on the GPU, as a serving loop's scheduler would; every
+    step's result matches the oracle and the pools and control-plane state stay identical to the
+    oracle's."""
     import torch
 
     g = W.Geometry(L=1, H_q=64, H_kv=8, d_head=128, block_size=16, dtype=dtype, num_blocks=256)
@@ -143,6 +144,7 @@ def test_step_plan_ahead_then_launch_host_match_oracle(dtype):
     scale = 1.0 / math.sqrt(g.d_head)
     pin = lambda x: torch.from_numpy(x.copy()).pin_memory().view(torch.bfloat16)
     plans = {}
+    launcher = pkv.StepLauncher(b.lib, 0, q_dev, k_dev, v_dev, o_dev, b.kp, b.vp, scale, ws)
 
     def plan(t):
         m = metas[t % 2]
@@ -159,8 +161,11 @@ def test_step_plan_ahead_then_launch_host_match_oracle(dtype):
         vn = W.normal(44, f"v{t}", (n, g.H_kv, g.d_head), "bf16")
         cows, oslots, tab, lens = plans[t]
         out_host.fill_(float("nan"))
-        pkv.pkv_step_launch_host(b.lib, 0, n, Wd, cows, pin(q), pin(kn), pin(vn), out_host, q_dev, k_dev, v_dev, o_dev,
-                                 b.kp, b.vp, scale, metas[t % 2], mdev[t % 2], ws)
+        if api == "launcher":
+            launcher(n, Wd, cows, pin(q), pin(kn), pin(vn), out_host, metas[t % 2], mdev[t % 2])
+        else:
+            pkv.pkv_step_launch_host(b.lib, 0, n, Wd, cows, pin(q), pin(kn), pin(vn), out_host, q_dev, k_dev, v_dev,
+                                     o_dev, b.kp, b.vp, scale, metas[t % 2], mdev[t % 2], ws)
         if len(cows):
             oracle.copy_blocks(g, cows, b.hk, b.hv)
         oracle.write_slots(g, 0, kn, vn, oslots, b.hk, b.hv, b.k_scale, b.v_scale)
