@@ -403,13 +403,16 @@ class DecodeRunner:
 
     def launcher_for(self, pool):
         """pkv_step_launch_host with this runner's device staging, pools, scale and workspace
-        bound once (a StepLauncher per control-plane state)."""
+        bound once: a StepLauncher per (control-plane state, stream).  The key holds the Pool
+        object itself (it stays alive while cached) and the stream the launcher is fixed to,
+        torch's current stream."""
         if not hasattr(self, "_launchers"):
             self._launchers = {}
-        key = id(pool)
+        stream = self.torch.cuda.current_stream().cuda_stream
+        key = (pool, stream)
         if key not in self._launchers:
             self._launchers[key] = self.pkv.StepLauncher(pool, 0, self.q_e2e, self.kn_e2e, self.vn_e2e, self.out,
-                                                         self.kp, self.vp, self.scale, self.ws)
+                                                         self.kp, self.vp, self.scale, self.ws, stream=stream)
         return self._launchers[key]
 
     def _refresh_handle(self):

@@ -488,6 +488,12 @@ int pkv_selftest_bounded_wait(int64_t timeout_ns, pkv_stream_t stream);
 /* Number of kernels this library has launched in this process (all devices). */
 uint64_t pkv_launch_count(void);
 
+/* Device code of this library as the runtime loaded it on the current device:
+ * *binary_version and *ptx_version are cudaFuncAttributes' binaryVersion and ptxVersion
+ * (major * 10 + minor) of the append kernel, e.g. 103 for sm_103a machine code.  Either
+ * output pointer may be NULL.  Needs a CUDA device (PKV_ERR_CUDA otherwise). */
+int pkv_device_code_version(int32_t* binary_version, int32_t* ptx_version);
+
 /* Synchronize the stream, then read and clear the current device's error word.
  * Returns DEVICE_CHECK if a kernel recorded a bad index since the last check;
  * *code (kernel-specific, nonzero) and *detail (the offending value) describe it.

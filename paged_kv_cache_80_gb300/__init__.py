@@ -25,7 +25,7 @@ __all__ = [
     "pkv_prefill_attention",
     "pkv_copy_blocks", "pkv_swap_out",
     "pkv_swap_in", "pkv_seq_host_slots", "pkv_seq_residency", "TIER_HBM", "TIER_HOST", "pkv_pool_set_swap_engine", "pkv_check_device_error", "pkv_launch_count",
-    "pkv_selftest_bounded_wait", "pkv_pool_set_kv_scales", "pkv_pool_kv_scales",
+    "pkv_selftest_bounded_wait", "pkv_device_code_version", "pkv_pool_set_kv_scales", "pkv_pool_kv_scales",
     "PrefixStats", "pkv_prefix_cache_create", "pkv_prefix_cache_destroy", "pkv_prefix_match", "pkv_prefix_attach",
     "pkv_prefix_insert", "pkv_prefix_release", "pkv_prefix_evict", "pkv_prefix_get_stats", "pkv_prefix_export",
     "SimConfig", "SimResult", "SIM_POLICIES", "pkv_sim_run",
@@ -125,6 +125,7 @@ def _L():
             "pkv_pool_kv_scales": ([vp, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_float)], ctypes.c_int),
             "pkv_check_device_error": ([vp, P32, P64], ctypes.c_int),
             "pkv_launch_count": ([], ctypes.c_uint64),
+            "pkv_device_code_version": ([P32, P32], ctypes.c_int),
             "pkv_selftest_bounded_wait": ([i64, vp], ctypes.c_int),
             "pkv_prefix_cache_create": ([vp, ctypes.POINTER(vp)], ctypes.c_int),
             "pkv_prefix_cache_destroy": ([vp], ctypes.c_int),
@@ -229,6 +230,30 @@ PoolLike = Union[Pool, ctypes.c_void_p]
 
 def _h(pool: PoolLike):
     return pool.handle if isinstance(pool, Pool) else pool
+
+
+def _nbytes(t) -> int:
+    """Size in bytes of a numpy array or torch tensor."""
+    return int(t.nbytes) if isinstance(t, np.ndarray) else t.numel() * t.element_size()
+
+
+def _step_bytes(pool: PoolLike, n: int, W: int):
+    """Bytes a decode step of n sequences reads or writes in each buffer: metadata
+    (n*(W+2) int32), q / out rows (n*H_q*d_head activations), k_new / v_new rows
+    (n*H_kv*d_head activations; activations are bf16 around an FP8 pool)."""
+    g = pool.geometry if isinstance(pool, Pool) else pkv_pool_geometry(pool)
+    ab = {F32: 4, F16: 2, BF16: 2, E4M3: 2}[g.dtype]
+    return 4 * n * (W + 2), ab * n * g.H_q * g.d_head, ab * n * g.H_kv * g.d_head
+
+
+def _require_bytes(*bufs):
+    """Raise ValueError for the first (buffer, bytes needed, name) whose buffer is smaller:
+    the library copies fixed byte counts into and out of these buffers and cannot see
+    their sizes."""
+    for t, need, what in bufs:
+        have = _nbytes(t)
+        if have < need:
+            raise ValueError(f"{what} holds {have} bytes; this step needs {need}")
 
 
 # ------------------------------------------------------------------ library
@@ -408,8 +433,9 @@ def pkv_decode_step(pool: PoolLike, layer: int, seq_ids, W: int, q, k_new, v_new
     meta_host: pinned CPU int32 tensor, meta_dev: CUDA int32 tensor, each >= n*(W+2)."""
     ids = _i32(seq_ids)
     n = ids.size
-    if meta_host.numel() < n * (W + 2) or meta_dev.numel() < n * (W + 2):
-        raise ValueError("metadata buffers smaller than n * (W + 2)")
+    mb, qb, kb = _step_bytes(pool, n, W)
+    _require_bytes((meta_host, mb, "meta_host"), (meta_dev, mb, "meta_dev"), (q, qb, "q"), (k_new, kb, "k_new"),
+                   (v_new, kb, "v_new"), (out, qb, "out"))
     ev0, ev1 = _events(attn_events)
     _check(_L().pkv_decode_step(_h(pool), layer, _a(ids), n, W, _dev(q, "q"), _dev(k_new, "k_new"),
                                 _dev(v_new, "v_new"), _dev(k_pool, "k_pool"), _dev(v_pool, "v_pool"), float(scale),
@@ -426,13 +452,11 @@ def pkv_decode_step_host(pool: PoolLike, layer: int, seq_ids, W: int, q_host, k_
     synchronise the stream before reading out_host."""
     ids = _i32(seq_ids)
     n = ids.size
-    if meta_host.numel() < n * (W + 2) or meta_dev.numel() < n * (W + 2):
-        raise ValueError("metadata buffers smaller than n * (W + 2)")
-    for t, d, what in ((q_host, q_dev, "q"), (k_new_host, k_new_dev, "k_new"), (v_new_host, v_new_dev, "v_new"),
-                       (out_host, out_dev, "out")):
-        row = t[0].numel() if t.dim() > 0 and t.shape[0] > 0 else 0
-        if t.dim() == 0 or t.shape[0] < n or d.dim() == 0 or d.shape[0] < n or d.numel() < n * row:
-            raise ValueError(f"{what} buffers hold fewer than n rows")
+    mb, qb, kb = _step_bytes(pool, n, W)
+    _require_bytes((meta_host, mb, "meta_host"), (meta_dev, mb, "meta_dev"), (q_host, qb, "q_host"),
+                   (k_new_host, kb, "k_new_host"), (v_new_host, kb, "v_new_host"), (out_host, qb, "out_host"),
+                   (q_dev, qb, "q_dev"), (k_new_dev, kb, "k_new_dev"), (v_new_dev, kb, "v_new_dev"),
+                   (out_dev, qb, "out_dev"))
     ev0, ev1 = _events(attn_events)
     _check(_L().pkv_decode_step_host(_h(pool), layer, _a(ids), n, W, _host_ptr(q_host, "q_host"),
                                      _host_ptr(k_new_host, "k_new_host"), _host_ptr(v_new_host, "v_new_host"),
@@ -449,8 +473,7 @@ def pkv_step_plan(pool: PoolLike, seq_ids, W: int, meta_host) -> np.ndarray:
     (pinned int32, >= n*(W+2)); returns the copy-on-write pairs [n_cow][2]."""
     ids = _i32(seq_ids)
     n = ids.size
-    if meta_host.numel() < n * (W + 2):
-        raise ValueError("meta_host smaller than n * (W + 2)")
+    _require_bytes((meta_host, 4 * n * (W + 2), "meta_host"))
     cows = np.zeros(max(2 * n, 2), np.int32)
     n_cow = ctypes.c_int32(0)
     _check(_L().pkv_step_plan(_h(pool), _a(ids), n, W, _host_ptr(meta_host, "meta_host"), _a(cows),
@@ -470,6 +493,9 @@ def _events(attn_events):
 def pkv_step_launch(pool: PoolLike, layer: int, n: int, W: int, cow_pairs, q, k_new, v_new, k_pool, v_pool,
                     scale: float, out, meta_host, meta_dev, workspace, attn_events=None, stream=None) -> None:
     """The device half of a decode step planned by pkv_step_plan (device q / k_new / v_new / out)."""
+    mb, qb, kb = _step_bytes(pool, n, W)
+    _require_bytes((meta_host, mb, "meta_host"), (meta_dev, mb, "meta_dev"), (q, qb, "q"), (k_new, kb, "k_new"),
+                   (v_new, kb, "v_new"), (out, qb, "out"))
     cp = _i32(cow_pairs).reshape(-1)
     ev0, ev1 = _events(attn_events)
     _check(_L().pkv_step_launch(_h(pool), layer, n, W, _a(cp), cp.size // 2, _dev(q, "q"), _dev(k_new, "k_new"),
@@ -483,6 +509,11 @@ def pkv_step_launch_host(pool: PoolLike, layer: int, n: int, W: int, cow_pairs, 
                          out_host, q_dev, k_new_dev, v_new_dev, out_dev, k_pool, v_pool, scale: float, meta_host,
                          meta_dev, workspace, attn_events=None, stream=None) -> None:
     """pkv_step_launch with host input and result tensors (page-locked) copied inside the call."""
+    mb, qb, kb = _step_bytes(pool, n, W)
+    _require_bytes((meta_host, mb, "meta_host"), (meta_dev, mb, "meta_dev"), (q_host, qb, "q_host"),
+                   (k_new_host, kb, "k_new_host"), (v_new_host, kb, "v_new_host"), (out_host, qb, "out_host"),
+                   (q_dev, qb, "q_dev"), (k_new_dev, kb, "k_new_dev"), (v_new_dev, kb, "v_new_dev"),
+                   (out_dev, qb, "out_dev"))
     cp = _i32(cow_pairs).reshape(-1)
     ev0, ev1 = _events(attn_events)
     _check(_L().pkv_step_launch_host(_h(pool), layer, n, W, _a(cp), cp.size // 2, _host_ptr(q_host, "q_host"),
@@ -497,32 +528,48 @@ def pkv_step_launch_host(pool: PoolLike, layer: int, n: int, W: int, cow_pairs, 
 
 class StepLauncher:
     """pkv_step_launch_host with the buffers that stay the same from step to step bound once:
-    the device staging tensors (q, k_new, v_new, out: the first n rows are used), the pools,
-    the workspace, the scale and the stream (torch's current stream at construction when
-    None).  Each call then takes only what changes per step, so a serving loop's host side
-    is shorter; the result is the same as pkv_step_launch_host's."""
+    the device staging tensors (q, k_new, v_new, out: their leading rows are used), the pools,
+    the workspace, the scale and the stream.  The stream is fixed at construction (torch's
+    current stream then, when None): calls made later under another torch stream still
+    launch on it.  Each call then takes only what changes per step, so a serving loop's host
+    side is shorter; the result is the same as pkv_step_launch_host's.  The launcher holds
+    references to the pool and every bound buffer, so none is freed while it lives, and each
+    call checks that its host and metadata buffers hold what the step copies."""
 
     def __init__(self, pool: PoolLike, layer: int, q_dev, k_new_dev, v_new_dev, out_dev, k_pool, v_pool,
                  scale: float, workspace, stream=None):
-        self._h = _h(pool)
+        self._pool = pool
         self._layer = int(layer)
-        self._rows = min(int(t.shape[0]) for t in (q_dev, k_new_dev, v_new_dev, out_dev))
+        g = pool.geometry if isinstance(pool, Pool) else pkv_pool_geometry(pool)
+        ab = {F32: 4, F16: 2, BF16: 2, E4M3: 2}[g.dtype]
+        self._row_q, self._row_k = ab * g.H_q * g.d_head, ab * g.H_kv * g.d_head
+        # rows that every bound device buffer can take
+        self._rows = min(_nbytes(q_dev) // self._row_q, _nbytes(k_new_dev) // self._row_k,
+                         _nbytes(v_new_dev) // self._row_k, _nbytes(out_dev) // self._row_q)
         self._dev = (_dev(q_dev, "q_dev"), _dev(k_new_dev, "k_new_dev"), _dev(v_new_dev, "v_new_dev"),
                      _dev(out_dev, "out_dev"), _dev(k_pool, "k_pool"), _dev(v_pool, "v_pool"))
         self._scale = float(scale)
         self._ws = (_dev(workspace, "workspace"), workspace.numel() * workspace.element_size())
         self._stream = _stream(stream)
         self._f = _L().pkv_step_launch_host
-        self._keep = (q_dev, k_new_dev, v_new_dev, out_dev, k_pool, v_pool, workspace)  # keep them alive
+        self._keep = (pool, q_dev, k_new_dev, v_new_dev, out_dev, k_pool, v_pool, workspace)  # keep them alive
+
+    @property
+    def stream(self) -> int:
+        """The CUDA stream (as an integer handle) every call launches on."""
+        return self._stream
 
     def __call__(self, n: int, W: int, cow_pairs, q_host, k_new_host, v_new_host, out_host, meta_host, meta_dev,
                  attn_events=None) -> None:
         if n > self._rows:
             raise ValueError(f"n = {n} exceeds the {self._rows} rows of the bound device buffers")
+        mb, qb, kb = 4 * n * (W + 2), n * self._row_q, n * self._row_k
+        _require_bytes((meta_host, mb, "meta_host"), (meta_dev, mb, "meta_dev"), (q_host, qb, "q_host"),
+                       (k_new_host, kb, "k_new_host"), (v_new_host, kb, "v_new_host"), (out_host, qb, "out_host"))
         cp = _i32(cow_pairs).reshape(-1)
         ev0, ev1 = _events(attn_events)
         q, k, v, o, kp, vp = self._dev
-        _check(self._f(self._h, self._layer, n, W, _a(cp), cp.size // 2, _host_ptr(q_host, "q_host"),
+        _check(self._f(_h(self._pool), self._layer, n, W, _a(cp), cp.size // 2, _host_ptr(q_host, "q_host"),
                        _host_ptr(k_new_host, "k_new_host"), _host_ptr(v_new_host, "v_new_host"),
                        _host_ptr(out_host, "out_host"), q, k, v, o, kp, vp, self._scale,
                        _host_ptr(meta_host, "meta_host"), _dev(meta_dev, "meta_dev"), self._ws[0], self._ws[1], ev0,
@@ -569,6 +616,14 @@ def pkv_selftest_bounded_wait(timeout_ns: int, stream=None) -> None:
 
 def pkv_launch_count() -> int:
     return int(_L().pkv_launch_count())
+
+
+def pkv_device_code_version():
+    """(binaryVersion, ptxVersion) of the library's device code as loaded on the current
+    device (needs a GPU)."""
+    b, p = ctypes.c_int32(), ctypes.c_int32()
+    _check(_L().pkv_device_code_version(ctypes.byref(b), ctypes.byref(p)), "pkv_device_code_version")
+    return b.value, p.value
 
 
 def pkv_check_device_error(stream=None):

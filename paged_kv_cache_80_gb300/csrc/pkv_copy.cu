@@ -312,6 +312,16 @@ extern "C" int pkv_selftest_bounded_wait(int64_t timeout_ns, pkv_stream_t stream
 
 extern "C" uint64_t pkv_launch_count(void) { return pkv::g_launches.load(std::memory_order_relaxed); }
 
+extern "C" int pkv_device_code_version(int32_t* binary_version, int32_t* ptx_version) {
+  pkv::clear_error();
+  cudaFuncAttributes attr{};
+  const cudaError_t e = cudaFuncGetAttributes(&attr, pkv::append_kernel<4>);
+  if (e != cudaSuccess) return pkv::fail(PKV_ERR_CUDA, std::string("cudaFuncGetAttributes: ") + cudaGetErrorString(e));
+  if (binary_version) *binary_version = attr.binaryVersion;
+  if (ptx_version) *ptx_version = attr.ptxVersion;
+  return PKV_OK;
+}
+
 extern "C" int pkv_check_device_error(pkv_stream_t stream, int32_t* code, int64_t* detail) {
   pkv::clear_error();
   if (code) *code = 0;

@@ -34,13 +34,18 @@ def test_every_declared_symbol_is_exported():
     assert set(declared_functions()) <= exported
 
 
-def test_library_is_the_sm103a_build():
-    # the only device code in the library is sm_103a machine code
-    out = subprocess.run(["cuobjdump", "--list-elf", pkv.library_path()], capture_output=True, text=True)
-    if out.returncode != 0:
-        pytest.skip("cuobjdump unavailable")
-    arches = set(re.findall(r"sm_(\d+a?)", out.stdout))
-    assert arches == {"103a"}, arches
+def test_library_is_built_for_sm103a_only():
+    # the build compiles every source with exactly one -gencode: sm_103a machine code
+    from paged_kv_cache_80_gb300 import build
+
+    assert build.ARCH == ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+
+@pytest.mark.gpu
+def test_loaded_device_code_is_sm103():
+    # what the runtime loaded for this device: sm_103a machine code (binaryVersion 103)
+    binary, ptx = pkv.pkv_device_code_version()
+    assert binary == 103, binary
 
 
 def test_version_and_status_names():

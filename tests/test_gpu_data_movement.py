@@ -110,10 +110,11 @@ def test_swap_round_trip_bit_exact(engine):
     b.append([ids[1]], [40], "reuse", layer=-1)
     for s in [3, 2]:
         n = len(before[s])
+        front = pkv.pkv_free_list(b.lib)[:n].copy()
         got = pkv.pkv_swap_in(b.lib, s, host, 16, n, b.kp, b.vp)
         exp, hs = b.orc.swap_in(s, n)
         assert np.array_equal(got, exp)
-        assert not set(got.tolist()) & set(before[s].tolist()) or True
+        assert np.array_equal(got, front)  # the restored blocks are the FIFO's first n ids, in order
         oracle.swap_in_data(g, exp, hs, ohost, b.hk, b.hv)
     b.check_pools_bitexact()
     b.check_state()

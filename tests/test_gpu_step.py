@@ -177,3 +177,43 @@ def test_step_plan_ahead_then_launch_host_match_oracle(dtype, api):
         check_attention(out_host.double().numpy(), ref, "bf16")
     b.check_state()
     b.check_pools_bitexact()
+
+
+def test_step_launcher_keeps_its_pool_and_checks_host_buffers():
+    """A StepLauncher holds the pool it was built on (dropping the caller's last reference
+    does not destroy it under the launcher) and rejects host buffers shorter than the step
+    copies, before any copy is issued."""
+    import gc
+
+    import torch
+
+    g = W.Geometry(L=1, H_q=16, H_kv=2, d_head=128, block_size=16, dtype="bf16", num_blocks=64)
+    pool = pkv.pkv_pool_create(g.L, g.H_q, g.H_kv, g.d_head, g.block_size, g.dtype, g.num_blocks)
+    ids = np.array([pkv.pkv_seq_create(pool) for _ in range(2)], np.int32)
+    pkv.pkv_plan_append(pool, ids, [10, 40])
+    kp = torch.zeros(g.pool_shape(), dtype=torch.bfloat16, device="cuda")
+    vp = torch.zeros_like(kp)
+    n, Wd = 2, 4
+    ws = torch.empty(pkv.pkv_decode_workspace_size(pool, n), dtype=torch.uint8, device="cuda")
+    q_dev = torch.empty((n, g.H_q, g.d_head), dtype=torch.bfloat16, device="cuda")
+    k_dev = torch.empty((n, g.H_kv, g.d_head), dtype=torch.bfloat16, device="cuda")
+    launcher = pkv.StepLauncher(pool, 0, q_dev, k_dev, k_dev.clone(), q_dev.clone(), kp, vp, 0.1, ws)
+    del pool
+    gc.collect()
+    meta_host = torch.zeros(n * (Wd + 2), dtype=torch.int32).pin_memory()
+    meta_dev = torch.zeros(n * (Wd + 2), dtype=torch.int32, device="cuda")
+    pool = launcher._pool
+    cows = pkv.pkv_step_plan(pool, ids, Wd, meta_host)
+    qh = torch.zeros((n, g.H_q, g.d_head), dtype=torch.bfloat16).pin_memory()
+    kh = torch.zeros((n, g.H_kv, g.d_head), dtype=torch.bfloat16).pin_memory()
+    oh = torch.full((n, g.H_q, g.d_head), float("nan"), dtype=torch.bfloat16).pin_memory()
+    with pytest.raises(ValueError, match="out_host"):
+        launcher(n, Wd, cows, qh, kh, kh, oh[:1], meta_host, meta_dev)
+    with pytest.raises(ValueError, match="meta_dev"):
+        launcher(n, Wd, cows, qh, kh, kh, oh, meta_host, meta_dev[:-1])
+    with pytest.raises(ValueError, match="exceeds"):
+        launcher(n + 1, Wd, cows, qh, kh, kh, oh, meta_host, meta_dev)
+    launcher(n, Wd, cows, qh, kh, kh, oh, meta_host, meta_dev)  # zero q and keys: outputs are means of zero V
+    torch.cuda.synchronize()
+    pkv.pkv_check_device_error()
+    assert torch.all(oh == 0)

@@ -38,10 +38,7 @@ def test_chat_64_steps_full():
         tables, lens = b.tables(run)
         q = W.normal(wl.seed, f"q{k}", (len(run), g.H_q, g.d_head), g.dtype)
         got, _, _ = b.decode_gpu(run, q, wl.scale, tables=tables, lens=lens)
-        if k % 9 == 0 or k == wl.extra["steps"] - 1:
-            check_attention(got, b.decode_ref(q, tables, lens, wl.scale), g.dtype)
-        else:
-            assert np.all(np.isfinite(got))
+        check_attention(got, b.decode_ref(q, tables, lens, wl.scale), g.dtype)  # every step, every sequence
         for s in run:
             if gen[s] == k + 1:
                 b.free(s)
@@ -136,10 +133,16 @@ def test_forked_prefix_with_cow_full():
     b.check_pools_bitexact()
 
 
-def test_swap_full_size_sampled():
+def test_swap_full_size_every_image():
     """80-layer geometry (5 MiB blocks): 512 chunk sequences of 16 blocks (42.9 GB)
     evicted to pinned host frames in a seeded order, then a seeded half restored into
-    different blocks.  Bookkeeping exact; sampled images bit-exact both ways."""
+    different blocks.  Bookkeeping exact; every host frame and every restored block
+    bit-exact against the pool's bytes from before the first eviction.
+
+    The expected bytes are a copy of the seeded pool taken on the device before any
+    library kernel ran (the pool and its copy fit in HBM; host copies of 43 GB would
+    not fit a test's time budget); the comparisons are whole-tensor equality, chunk by
+    chunk (16 frames, 80 MiB at a time)."""
     import torch
 
     wl = W.swap()
@@ -148,18 +151,12 @@ def test_swap_full_size_sampled():
     nchunk = len(wl.lengths)
     kp = W.device_normal(wl.seed, "k_pool", g.pool_shape(), g.dtype, "cuda")
     vp = W.device_normal(wl.seed, "v_pool", g.pool_shape(), g.dtype, "cuda")
+    kp0, vp0 = kp.clone(), vp.clone()  # the pool before any library kernel
     b = PagedBatch(g, wl.free_order, seed=wl.seed, host_pool=False, fill_device=(kp, vp))
     ids = b.new_seqs(nchunk)
     b.append(ids, [int(x) for x in wl.lengths], "chunks", plan_only=True)  # the seeded pool holds the data
     restore = [int(x) for x in wl.extra["restore"]]
-    kept_out = sorted(set(range(nchunk)) - set(restore))
-    rng = W.substream(wl.seed, "sample")
-    sampled = sorted([int(x) for x in rng.choice(restore, size=3, replace=False)] +
-                     [int(x) for x in rng.choice(kept_out, size=3, replace=False)])
-    snap = {}
-    for s in sampled:
-        t = torch.from_numpy(b.orc.table(s).astype(np.int64)).cuda()
-        snap[s] = (to_raw(kp.index_select(0, t), g.dtype), to_raw(vp.index_select(0, t), g.dtype))
+    before = {s: b.orc.table(s).astype(np.int64) for s in ids}
     frame = 2 * g.L * g.H_kv * g.block_size * g.d_head * g.elem_bytes
     assert frame == 16 * 327680
     host = torch.empty(nchunk * cb * frame, dtype=torch.uint8, pin_memory=True)
@@ -171,13 +168,19 @@ def test_swap_full_size_sampled():
         assert np.array_equal(got, b.orc.swap_out(s, frames))
         old_ids.update(got.tolist())
     torch.cuda.synchronize()
+    pkv.pkv_check_device_error()
     b.check_state()
-    hview = host.numpy().reshape(nchunk * cb, 2, -1)
-    for s in sampled:
-        i = order.index(s)
-        for j in range(cb):
-            assert np.array_equal(hview[i * cb + j, 0], snap[s][0][j].reshape(-1).view(np.uint8))
-            assert np.array_equal(hview[i * cb + j, 1], snap[s][1][j].reshape(-1).view(np.uint8))
+
+    def image(pool, blocks):  # [n][L*H_kv*B*d] raw bytes of the given blocks
+        return pool.index_select(0, blocks).view(len(blocks), -1).view(torch.uint8)
+
+    # every host frame: [K image | V image] of the block it was evicted from
+    hview = host.view(nchunk * cb, 2, -1)
+    for i, s in enumerate(order):
+        t = torch.from_numpy(before[s]).cuda()
+        got = hview[i * cb:(i + 1) * cb].to("cuda", non_blocking=True)
+        assert torch.equal(got[:, 0], image(kp0, t)), f"K frames of chunk {s}"
+        assert torch.equal(got[:, 1], image(vp0, t)), f"V frames of chunk {s}"
     for s in restore:
         got = pkv.pkv_swap_in(b.lib, s, host, nchunk * cb, cb, kp, vp)
         exp, _ = b.orc.swap_in(s, cb)
@@ -186,8 +189,9 @@ def test_swap_full_size_sampled():
     torch.cuda.synchronize()
     pkv.pkv_check_device_error()
     b.check_state()
-    for s in sampled:
-        if s in restore:
-            t = torch.from_numpy(b.orc.table(s).astype(np.int64)).cuda()
-            assert np.array_equal(to_raw(kp.index_select(0, t), g.dtype), snap[s][0])
-            assert np.array_equal(to_raw(vp.index_select(0, t), g.dtype), snap[s][1])
+    # every restored block equals the block its frame was evicted from
+    for s in restore:
+        new = torch.from_numpy(b.orc.table(s).astype(np.int64)).cuda()
+        old = torch.from_numpy(before[s]).cuda()
+        assert torch.equal(image(kp, new), image(kp0, old)), f"restored K of chunk {s}"
+        assert torch.equal(image(vp, new), image(vp0, old)), f"restored V of chunk {s}"
