@@ -342,7 +342,8 @@ class DecodeRunner:
             kvb = tok * g.H_kv * g.d_head * g.elem_bytes * 2
             self.kv_bytes.append(kvb)
             qo = 2 * n * g.H_q * g.d_head * self.act_bytes
-            self.alg_bytes.append(kvb + qo + n * self.Wd * 4 + n * 4)
+            app = 2 * n * g.H_kv * g.d_head * (self.act_bytes + g.elem_bytes)  # new keys/values in, slots out
+            self.alg_bytes.append(kvb + qo + app + n * self.Wd * 4 + n * 4)
             self.tokens.append(n)
             self.h2d_meta += nbytes
         self.after_step(t, ids)
@@ -395,7 +396,8 @@ class DecodeRunner:
                 lens = hnp[n + n * self.Wd:n + n * self.Wd + n]
                 kvb = int(lens.sum(dtype=np.int64)) * g.H_kv * g.d_head * g.elem_bytes * 2
                 self.kv_bytes.append(kvb)
-                self.alg_bytes.append(kvb + 2 * n * g.H_q * g.d_head * self.act_bytes + n * self.Wd * 4 + n * 4)
+                self.alg_bytes.append(kvb + 2 * n * g.H_q * g.d_head * self.act_bytes + n * self.Wd * 4 + n * 4 +
+                                      2 * n * g.H_kv * g.d_head * (self.act_bytes + g.elem_bytes))
                 self.tokens.append(n)
                 self.h2d_meta += nbytes
             self.e2e_in_bytes += nbytes + (q.numel() + kn.numel() + vn.numel()) * self.act_bytes
@@ -693,7 +695,7 @@ def run_decode(args, torch, pkv, dev, world, rank):
         "hbm_frac_of_8tbs": round(value / world / NOMINAL_HBM_GBS, 4),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "kernel": "pkv_decode_attention (plan + stream-K attention + merge)",
+                     "kernel": "decode step device work: append (programmatic primary) + stream-K attention planned in-kernel + merge",
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
                      else "fallback 6.8 TB/s",
                      "alg_bytes_per_launch": int(alg_avg), "avg_launch_ms": round(dec_avg, 4)},

@@ -654,11 +654,13 @@ int pkv_step_launch(pkv_pool* pool, int32_t layer, int32_t n, int32_t W, const i
   if (e != cudaSuccess) return fail(PKV_ERR_CUDA, std::string("cudaMemcpyAsync (step metadata): ") + cudaGetErrorString(e));
   if (n_cow > 0)
     if (int rc = pkv_copy_blocks(pool, cow_pairs, n_cow, k_pool, v_pool, stream)) return rc;
-  if (int rc = pkv_append_kv(pool, layer, k_new, v_new, meta_dev, n, k_pool, v_pool, stream)) return rc;
+  // append and attention in one launch on the tensor-core path (the kernel writes each new
+  // token before it loads the tile that holds it); the append kernel first otherwise
   if (attn_begin) cudaEventRecord(reinterpret_cast<cudaEvent_t>(attn_begin), st);
-  if (int rc = pkv_decode_attention(pool, layer, q, k_pool, v_pool, meta_dev + n, W,
-                                    meta_dev + n + static_cast<int64_t>(n) * W, n, scale, out, workspace, ws_bytes,
-                                    stream))
+  const pkv::AppendFuse fuse{k_new, v_new, meta_dev, k_pool, v_pool};
+  if (int rc = pkv::launch_decode(*as_pool(pool), layer, q, k_pool, v_pool, meta_dev + n, W,
+                                  meta_dev + n + static_cast<int64_t>(n) * W, n, scale, out, workspace, ws_bytes,
+                                  stream, &fuse))
     return rc;
   if (attn_end) cudaEventRecord(reinterpret_cast<cudaEvent_t>(attn_end), st);
   return PKV_OK;

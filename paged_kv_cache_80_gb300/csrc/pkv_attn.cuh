@@ -36,7 +36,10 @@ struct DecodeArgs {
   int32_t* tile_prefix;  // [n_seq + 1]: tiles of sequences before s (per KV head)
   int32_t* lens_c;       // [n_seq]: lengths clamped to [0, W*B]
   int32_t* hdr;          // [0] = total tiles over all pairs
-  int32_t* counters;     // [n_seq * H_kv]: partials written so far for a split pair
+  // [total_warps]: arrivals at the split pair whose first tile lies in warp w's range, as
+  // (epoch << 16) | count; a word carrying another launch's epoch counts as zero, so the
+  // array needs no clearing between launches
+  unsigned long long* counters;
   int4* wstart;          // [total_warps]: (sequence, KV head, tile, tiles of pair) at each warp's first tile
   float* partials;
   int* err;
@@ -46,6 +49,8 @@ struct DecodeArgs {
   float scale_log2;  // scale * log2(e) (* k_scale for an FP8 pool)
   float v_mul;       // 1, or v_scale for an FP8 pool
   int32_t total_warps;
+  int32_t self_plan;           // 1: every CTA plans its own warps from seq_lens (no plan kernel)
+  unsigned long long epoch;    // 48-bit tag of this launch (nonzero, unique in the process)
 };
 
 template <typename T>

@@ -60,6 +60,7 @@ struct AppendArgs {
   int64_t n_slots;      // num_blocks * B
   int32_t n_tok, H_kv, B, L, layer;  // layer < 0: all layers
   int32_t vec_per_row;  // row bytes / VEC
+  int32_t lets_dependents;  // let a programmatic dependent launched next start now
 };
 
 template <int VEC>
@@ -78,6 +79,7 @@ struct VecT<2> { using T = short; };
 template <int VEC>
 __global__ void __launch_bounds__(256) append_kernel(const AppendArgs a) {
   using V = typename VecT<VEC>::T;
+  if (a.lets_dependents) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   for (int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < a.total; idx += stride) {
     int64_t r = idx / a.vec_per_row;
@@ -102,20 +104,9 @@ __global__ void __launch_bounds__(256) append_kernel(const AppendArgs a) {
 
 // Append into an FP8 pool ("KV Cache Management", PagedAttention model: b_elem = 1
 // for FP8): one thread per 8 elements of a (layer, token, head) row -- 16 bytes of
-// bf16 in, 8 bytes of E4M3 codes out.  Each code is the E4M3 value nearest to the
-// binary32 quotient x / scale (IEEE division, then round to nearest even with
-// saturation to the largest finite value, 448).
-__device__ __forceinline__ uint32_t quant4(uint32_t w0, uint32_t w1, float s) {
-  const float x[4] = {__uint_as_float(w0 << 16), __uint_as_float(w0 & 0xffff0000u), __uint_as_float(w1 << 16),
-                      __uint_as_float(w1 & 0xffff0000u)};
-  uint32_t r = 0;
-#pragma unroll
-  for (int j = 0; j < 4; ++j)
-    r |= static_cast<uint32_t>(__nv_cvt_float_to_fp8(__fdiv_rn(x[j], s), __NV_SATFINITE, __NV_E4M3)) << (8 * j);
-  return r;
-}
-
+// bf16 in, 8 bytes of E4M3 codes out (quant4_e4m3: the code nearest x / scale).
 __global__ void __launch_bounds__(256) append_e4m3_kernel(const AppendArgs a, float k_scale, float v_scale) {
+  if (a.lets_dependents) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   for (int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < a.total; idx += stride) {
     int64_t r = idx / a.vec_per_row;
@@ -135,8 +126,8 @@ __global__ void __launch_bounds__(256) append_e4m3_kernel(const AppendArgs a, fl
     const int64_t dst = (((blk * a.L + layer) * a.H_kv + h) * a.B + off) * a.vec_per_row + c;
     const uint4 k = reinterpret_cast<const uint4*>(a.k_new)[src];
     const uint4 v = reinterpret_cast<const uint4*>(a.v_new)[src];
-    reinterpret_cast<uint2*>(a.k_pool)[dst] = make_uint2(quant4(k.x, k.y, k_scale), quant4(k.z, k.w, k_scale));
-    reinterpret_cast<uint2*>(a.v_pool)[dst] = make_uint2(quant4(v.x, v.y, v_scale), quant4(v.z, v.w, v_scale));
+    reinterpret_cast<uint2*>(a.k_pool)[dst] = make_uint2(quant4_e4m3(k.x, k.y, k_scale), quant4_e4m3(k.z, k.w, k_scale));
+    reinterpret_cast<uint2*>(a.v_pool)[dst] = make_uint2(quant4_e4m3(v.x, v.y, v_scale), quant4_e4m3(v.z, v.w, v_scale));
   }
 }
 
@@ -161,7 +152,7 @@ static int sm_count() {
 }
 
 int launch_append(const Pool& P, int32_t layer, const void* k_new, const void* v_new, const int32_t* slots,
-                  int32_t n_tok, void* k_pool, void* v_pool, void* stream) {
+                  int32_t n_tok, void* k_pool, void* v_pool, void* stream, bool lets_dependents) {
   if (n_tok == 0) return PKV_OK;
   void* err = nullptr;
   if (int rc = device_error_word(&err)) return rc;
@@ -188,6 +179,7 @@ int launch_append(const Pool& P, int32_t layer, const void* k_new, const void* v
   a.layer = layer;
   a.vec_per_row = fp8 ? g.d_head / 8 : static_cast<int32_t>(row / vec);
   a.n_slots = g.num_blocks * g.block_size;
+  a.lets_dependents = lets_dependents ? 1 : 0;
   const int layers = layer < 0 ? g.L : 1;
   a.total = static_cast<int64_t>(layers) * n_tok * g.H_kv * a.vec_per_row;
   const int threads = 256;

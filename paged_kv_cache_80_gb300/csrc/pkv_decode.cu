@@ -46,7 +46,11 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <unistd.h>
+
 #include <algorithm>
+#include <atomic>
+#include <chrono>
 #include <cmath>
 #include <cstdlib>
 #include <cstring>
@@ -114,8 +118,6 @@ __global__ void __launch_bounds__(1024) plan_kernel(const DecodeArgs a) {
     a.tile_prefix[a.n_seq] = run;
     a.hdr[0] = run * a.H_kv;
   }
-  // counters of split pairs start at zero
-  for (int p = tid; p < a.n_seq * a.H_kv; p += blockDim.x) a.counters[p] = 0;
   // an empty sequence attends to nothing: zero output (16-byte stores; H_q*D*b is a multiple of 16)
   const int row16 = a.H_q * a.D * a.elem / 16;
   for (int s = s0; s < s1; ++s)
@@ -149,6 +151,86 @@ __global__ void __launch_bounds__(1024) plan_kernel(const DecodeArgs a) {
     const int within = start - a.H_kv * Qp[lo];
     a.wstart[w] = make_int4(lo, within / nt, within - (within / nt) * nt, nt);
   }
+}
+
+// --------------------------------------------------------------------------- in-kernel plan
+
+// Sequences up to which every CTA of the attention kernel plans its own warps (no plan kernel).
+constexpr int kSelfPlanMaxSeqs = 4096;
+
+// Length of sequence s clamped to the table's capacity [0, W*B]; `record` reports a bad one.
+__device__ __forceinline__ int32_t clamped_len(const DecodeArgs& a, int s, bool record) {
+  int32_t len = a.seq_lens[s];
+  const int64_t maxlen = static_cast<int64_t>(a.W) * a.B;
+  if (len < 0 || len > maxlen) {
+    if (record) record_error(a.err, DERR_DECODE_LEN, s);
+    len = len < 0 ? 0 : static_cast<int32_t>(maxlen);
+  }
+  return len;
+}
+
+// The plan kernel's work for this CTA's NW warps only, from the lengths: tiles per
+// sequence, their block-wide exclusive prefix, the total, and each warp's first tile
+// (sequence, KV head, tile, tiles of the pair) with the prefix of its sequence.  Every
+// CTA reads all n_seq lengths (n_seq <= kSelfPlanMaxSeqs) and gets the same total; the
+// thread whose chunk of sequences holds a warp's start finds it.  CTA 0 records bad
+// lengths; CTA (s mod grid) zeroes the output of an empty sequence s.  Ends with a CTA
+// barrier, so it is called by every thread before any warp leaves.
+template <int NW>
+__device__ void self_plan(const DecodeArgs& a, int4* s_start, int32_t* s_q, int32_t* s_total) {
+  __shared__ int32_t wsum[NW];
+  constexpr int NT = NW * 32;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int per = (a.n_seq + NT - 1) / NT;
+  const int s0 = min(a.n_seq, tid * per), s1 = min(a.n_seq, s0 + per);
+  const int row16 = a.H_q * a.D * a.elem / 16;
+  int32_t local = 0;
+  for (int s = s0; s < s1; ++s) {
+    const int32_t len = clamped_len(a, s, blockIdx.x == 0);
+    local += (len + TILE - 1) / TILE;
+    if (len == 0 && s % gridDim.x == blockIdx.x)  // an empty sequence attends to nothing: zero output
+      for (int k = 0; k < row16; ++k)
+        reinterpret_cast<int4*>(static_cast<char*>(a.out) + static_cast<int64_t>(s) * row16 * 16)[k] =
+            make_int4(0, 0, 0, 0);
+  }
+  int32_t incl = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) wsum[warp] = incl;
+  __syncthreads();
+  int32_t before = 0, tot = 0;
+#pragma unroll
+  for (int w = 0; w < NW; ++w) {
+    before += w < warp ? wsum[w] : 0;
+    tot += wsum[w];
+  }
+  const int32_t excl = before + incl - local;
+  const int total = tot * a.H_kv;
+  const int R = (total + a.total_warps - 1) / a.total_warps;
+#pragma unroll 1
+  for (int w = 0; w < NW; ++w) {
+    const int start = (blockIdx.x * NW + w) * R;
+    if (start >= total) {
+      if (tid == 0) s_start[w] = make_int4(-1, 0, 0, 0);
+    } else if (local > 0 && a.H_kv * excl <= start && start < a.H_kv * (excl + local)) {
+      int32_t q = excl;
+      for (int s = s0; s < s1; ++s) {
+        const int nt = (clamped_len(a, s, false) + TILE - 1) / TILE;
+        if (a.H_kv * (q + nt) > start) {
+          const int within = start - a.H_kv * q;
+          s_start[w] = make_int4(s, within / nt, within - (within / nt) * nt, nt);
+          s_q[w] = q;
+          break;
+        }
+        q += nt;
+      }
+    }
+  }
+  if (tid == 0) *s_total = total;
+  __syncthreads();
 }
 
 // --------------------------------------------------------------------------- tensor-core path
@@ -304,7 +386,8 @@ __device__ __forceinline__ void merge_pair(const DecodeArgs& a, int s, int g, in
 
 // Descriptor of one tile, built by the warp a batch at a time:
 //   x = TMA row coordinate of the slab, y = pair id (s * H_kv + g),
-//   z = valid tokens | first-of-pair << 8 | last-of-pair << 9 | new-pair-in-range << 10.
+//   z = valid tokens | first-of-pair << 8 | last-of-pair << 9 | new-pair-in-range << 10,
+//   w = tiles of the sequences before s (the pair's place in the batch's tile order).
 constexpr int F_FIRST = 1 << 8, F_LAST = 1 << 9, F_NEWPAIR = 1 << 10;
 
 template <typename T, int D, int S, int NW, int NB>
@@ -336,29 +419,48 @@ __global__ void __launch_bounds__(NW * 32) decode_tc_kernel(const __grid_constan
   }
   __syncwarp();
 
-  // everything above overlaps the plan kernel; its outputs are read from here on
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int total = a.hdr[0];
+  // ---- this warp's range of the batch's tiles and its first tile: planned here by every CTA
+  // (small batches), or read from the plan kernel, which this kernel then follows as a
+  // programmatic dependent (everything above overlaps it).  A self-planning launch may itself
+  // follow a decode step's append kernel as a programmatic dependent: it reads only lengths and
+  // tables before its first tile load, and waits for the append's grid just before that load.
+  __shared__ int4 s_start[NW];
+  __shared__ int32_t s_q[NW];
+  __shared__ int32_t s_total;
+  int total, cq;
+  int4 w0;
+  if (a.self_plan) {
+    self_plan<NW>(a, s_start, s_q, &s_total);
+    total = s_total;
+    w0 = s_start[warp];
+    cq = s_q[warp];
+  } else {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    total = a.hdr[0];
+    w0 = a.wstart[gw];
+    cq = w0.x >= 0 ? a.tile_prefix[w0.x] : 0;
+  }
   const int R = (total + a.total_warps - 1) / a.total_warps;
   const int my_start = gw * R;
   const int my_end = min(total, my_start + R);
-  if (my_start >= my_end) return;  // the whole warp leaves; no block-level barriers are used
+  if (my_start >= my_end) return;  // the whole warp leaves; no block-level barriers follow
   const int n_my = my_end - my_start;
 
-  // ---- tile walk state: (sequence, KV head, tile within pair, tiles of the pair), from the plan
-  const int32_t* Q = a.tile_prefix;
-  const int4 w0 = a.wstart[gw];
+  // ---- tile walk state: (sequence, KV head, tile within pair, tiles of the pair, tiles before
+  // the sequence)
   int cs = w0.x, ch = w0.y, cj = w0.z, cn = w0.w;
+  auto tiles_of = [&](int s) { return (clamped_len(a, s, false) + TILE - 1) / TILE; };
 
   // Fill descriptors for range tiles [t0, t0 + 32) into ring slots (t & 63).
   auto fill = [&](int t0) {
-    int ss = cs, hh = ch, jj = cj + lane, nn = cn;
+    int ss = cs, hh = ch, jj = cj + lane, nn = cn, qq = cq;
     while (jj >= nn && ss < a.n_seq) {
       jj -= nn;
       if (++hh == a.H_kv) {
         hh = 0;
+        qq += nn;
         ++ss;
-        nn = ss < a.n_seq ? Q[ss + 1] - Q[ss] : 0;
+        nn = ss < a.n_seq ? tiles_of(ss) : 0;
       }
     }
     const int t = t0 + lane;
@@ -371,26 +473,28 @@ __global__ void __launch_bounds__(NW * 32) decode_tc_kernel(const __grid_constan
         record_error(a.err, DERR_DECODE_BLOCK, blk);
         blk = 0;
       }
-      const int valid = min(TILE, a.lens_c[ss] - tok0);
+      const int valid = min(TILE, clamped_len(a, ss, false) - tok0);
       int flags = valid;
       if (jj == 0) flags |= F_FIRST;
       if (jj == nn - 1) flags |= F_LAST;
       if (jj == 0 || t == 0) flags |= F_NEWPAIR;
       const int row = ((blk * a.L + a.layer) * a.H_kv + hh) * a.B + sub;
-      desc[t & 63] = make_int4(row, ss * a.H_kv + hh, flags, 0);
+      desc[t & 63] = make_int4(row, ss * a.H_kv + hh, flags, qq);
     }
     // carry = position of tile t0 + 32 (one past lane 31's tile)
     int ns = __shfl_sync(0xffffffffu, ss, 31), nh = __shfl_sync(0xffffffffu, hh, 31);
     int nj = __shfl_sync(0xffffffffu, jj, 31) + 1, nnn = __shfl_sync(0xffffffffu, nn, 31);
+    int nq = __shfl_sync(0xffffffffu, qq, 31);
     while (nj >= nnn && ns < a.n_seq) {
       nj -= nnn;
       if (++nh == a.H_kv) {
         nh = 0;
+        nq += nnn;
         ++ns;
-        nnn = ns < a.n_seq ? Q[ns + 1] - Q[ns] : 0;
+        nnn = ns < a.n_seq ? tiles_of(ns) : 0;
       }
     }
-    cs = ns; ch = nh; cj = nj; cn = nnn;
+    cs = ns; ch = nh; cj = nj; cn = nnn; cq = nq;
     __syncwarp();
   };
 
@@ -417,6 +521,7 @@ __global__ void __launch_bounds__(NW * 32) decode_tc_kernel(const __grid_constan
 
   fill(0);
   if (n_my > 32) fill(32);
+  if (a.self_plan) asm volatile("griddepcontrol.wait;" ::: "memory");  // the append's K/V are written
   if (lane == 0)
     for (int t = 0; t < S && t < n_my; ++t) issue(t);
 
@@ -434,6 +539,8 @@ __global__ void __launch_bounds__(NW * 32) decode_tc_kernel(const __grid_constan
   float m[NB][2], l[NB][2];
   int cur_pair = -1;
   bool cur_started = false, cur_first_in_range = false;
+  // split pairs whose partial this warp wrote: one that ended inside the range, one at its end
+  int pend_pair = -1, pend_pbeg = 0, pend_nt = 0, end_pair = -1, end_pbeg = 0, end_nt = 0;
 
   for (int i = 0; i < n_my; ++i) {
     if (i >= 32 && (i & 31) == 0 && i + 32 < n_my) fill(i + 32);
@@ -652,25 +759,58 @@ __global__ void __launch_bounds__(NW * 32) decode_tc_kernel(const __grid_constan
             ps[hm + C::GP + 1] = Ls[nb][1];
           }
         }
-        // the warp that writes a split pair's last partial merges it ("Chunked prefill
-        // mechanics" rule): publish (the warp barrier orders every lane's writes before
-        // lane 0's cumulative fence), count, and let the last arrival read everyone's
-        __syncwarp();
-        int arrived = 0;
-        if (lane == 0) {
-          __threadfence();
-          arrived = atomicAdd(&a.counters[cur_pair], 1);
-        }
-        arrived = __shfl_sync(0xffffffffu, arrived, 0);
-        const int nt = Q[s + 1] - Q[s];
-        const int pbeg = a.H_kv * Q[s] + g * nt;
-        const int wa = pbeg / R, wb = (pbeg + nt - 1) / R;
-        if (arrived == wb - wa) {
-          __threadfence();
-          merge_pair<TA, D, F8, NB>(a, s, g, pbeg, wa, wb, R, lane);
+        // this warp's share of a split pair: arrive at the pair's counter once the range is done
+        // (a pair that ends before the range does waits there, so no fence stalls the tiles)
+        const int nt = tiles_of(s);
+        const int pbeg = a.H_kv * d.w + g * nt;
+        if (i != n_my - 1) {
+          pend_pair = cur_pair;
+          pend_pbeg = pbeg;
+          pend_nt = nt;
+        } else {
+          end_pair = cur_pair;
+          end_pbeg = pbeg;
+          end_nt = nt;
         }
       }
     }
+  }
+
+  // ---- end of the range: publish this warp's partials, count them, merge what is complete.
+  // The warp that writes a split pair's last partial merges it ("Chunked prefill mechanics"
+  // rule): publish (the warp barrier orders every lane's writes before lane 0's cumulative
+  // fence), count, and let the last arrival read everyone's.  The pair's counter is that of
+  // the first warp of its range (a warp's range ends with at most one split pair), tagged
+  // with this launch's epoch: a word left by an earlier launch (or never written) counts as
+  // no arrival.
+  if (pend_pair >= 0 || end_pair >= 0) {
+    __syncwarp();
+    if (lane == 0) __threadfence();
+    auto arrive = [&](int pair, int pbeg, int nt) {
+      const int s = pair / a.H_kv, g = pair - (pair / a.H_kv) * a.H_kv;
+      const int wa = pbeg / R, wb = (pbeg + nt - 1) / R;
+      int arrived = 0;
+      if (lane == 0) {
+        unsigned long long* c = a.counters + wa;
+        unsigned long long cur = *reinterpret_cast<volatile unsigned long long*>(c);
+        for (;;) {
+          const bool ours = (cur >> 16) == a.epoch;
+          const unsigned long long prev = atomicCAS(c, cur, ours ? cur + 1 : ((a.epoch << 16) | 1ull));
+          if (prev == cur) {
+            arrived = ours ? static_cast<int>(cur & 0xffffull) : 0;
+            break;
+          }
+          cur = prev;
+        }
+      }
+      arrived = __shfl_sync(0xffffffffu, arrived, 0);
+      if (arrived == wb - wa) {
+        __threadfence();
+        merge_pair<TA, D, F8, NB>(a, s, g, pbeg, wa, wb, R, lane);
+      }
+    };
+    if (pend_pair >= 0) arrive(pend_pair, pend_pbeg, pend_nt);
+    if (end_pair >= 0) arrive(end_pair, end_pbeg, end_nt);
   }
 }
 
@@ -711,8 +851,10 @@ TcVariant tc_variant(const Pool& P) {
   const bool fp8 = P.geo.dtype == PKV_E4M3, wide = P.geo.H_q / P.geo.H_kv > GPAD;
   int idx = fp8 && !wide ? 7 : 0;
   if (const char* e = std::getenv("PKV_TC_VARIANT")) {
+    // only variants built for this pool type: 0-4 for 16-bit pools, 0-8 for FP8; 0 (and 4
+    // for FP8) with groups of 9 to 16 heads (pick_tc builds no others)
     const int v = std::max(0, std::min(8, std::atoi(e)));
-    if (!wide || (fp8 && (v == 0 || v == 4))) idx = v;
+    if (wide ? (fp8 && (v == 0 || v == 4)) : (fp8 || v <= 4)) idx = v;
   }
   return table[idx];
 }
@@ -828,11 +970,12 @@ struct WsLayout {
 };
 
 WsLayout ws_layout(int n_seq, int H_kv, int64_t total_warps, int D, int G) {
+  (void)H_kv;
   WsLayout w;
   w.prefix = kHdrBytes;
   w.lens = w.prefix + align256(sizeof(int32_t) * (n_seq + 1));
   w.counters = w.lens + align256(sizeof(int32_t) * n_seq);
-  w.wstart = w.counters + align256(sizeof(int32_t) * static_cast<size_t>(n_seq) * H_kv);
+  w.wstart = w.counters + align256(sizeof(unsigned long long) * total_warps);
   w.partials = w.wstart + align256(sizeof(int4) * total_warps);
   const int nb = G > GPAD ? 2 : 1;  // head blocks (the kernel's TcCfg::PSTRIDE)
   const int pstride = nb * (D / 16) * 32 * 4 + 2 * GPAD * nb;
@@ -908,15 +1051,42 @@ int encode_kv_maps(const pkv_geometry& g, const void* k, const void* v, CUtensor
   return PKV_OK;
 }
 
-// plan_kernel, then the attention kernel as a programmatic dependent launch: its
-// CTAs become resident and initialise their barriers while the plan kernel runs,
-// and wait (griddepcontrol.wait) before reading the plan's outputs.
+// A 48-bit tag for one attention launch, unique within the process (never 0): the
+// split-pair counters it leaves behind carry it, so the next launch needs no clearing pass.
+unsigned long long next_epoch() {
+  static std::atomic<unsigned long long> ctr{[] {
+    // start at an arbitrary point so that leftovers of another process are unlikely to match
+    unsigned long long z = static_cast<unsigned long long>(
+        std::chrono::steady_clock::now().time_since_epoch().count()) ^
+        (static_cast<unsigned long long>(getpid()) << 24);
+    z += 0x9e3779b97f4a7c15ull;
+    z = (z ^ (z >> 30)) * 0xbf58476d1ce4e5b9ull;
+    z = (z ^ (z >> 27)) * 0x94d049bb133111ebull;
+    return z ^ (z >> 31);
+  }()};
+  for (;;) {
+    const unsigned long long e = ctr.fetch_add(1, std::memory_order_relaxed) & ((1ull << 48) - 1);
+    if (e != 0) return e;
+  }
+}
+
+// The attention launch.  Up to kSelfPlanMaxSeqs sequences, every CTA plans its own warps
+// (one launch; after_append: as the programmatic dependent of the decode step's append
+// kernel launched just before, which lets it start).  Beyond that, plan_kernel first and the
+// attention kernel as its programmatic dependent: its CTAs become resident and initialise
+// their barriers while the plan kernel runs, and wait (griddepcontrol.wait) before reading
+// the plan's outputs.
 int launch_tc_sequence(DecodeArgs& a, CUtensorMap* maps, KernelPtr k, int grid, int nw, int smem,
-                       cudaStream_t st) {
-  const size_t plan_smem = a.n_seq + 1 <= kPlanSmemInts ? sizeof(int32_t) * (a.n_seq + 1) : 0;
-  plan_kernel<<<1, 1024, plan_smem, st>>>(a);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return fail(PKV_ERR_CUDA, std::string("plan launch: ") + cudaGetErrorString(e));
+                       cudaStream_t st, bool after_append = false) {
+  a.epoch = next_epoch();
+  a.self_plan = a.n_seq <= kSelfPlanMaxSeqs ? 1 : 0;
+  cudaError_t e;
+  if (!a.self_plan) {
+    const size_t plan_smem = a.n_seq + 1 <= kPlanSmemInts ? sizeof(int32_t) * (a.n_seq + 1) : 0;
+    plan_kernel<<<1, 1024, plan_smem, st>>>(a);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(PKV_ERR_CUDA, std::string("plan launch: ") + cudaGetErrorString(e));
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(nw * 32);
@@ -926,11 +1096,11 @@ int launch_tc_sequence(DecodeArgs& a, CUtensorMap* maps, KernelPtr k, int grid, 
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = (a.self_plan && !after_append) ? 0 : 1;
   void* args[] = {&maps[0], &maps[1], &a};
   e = cudaLaunchKernelExC(&cfg, k, args);
   if (e != cudaSuccess) return fail(PKV_ERR_CUDA, std::string("decode launch: ") + cudaGetErrorString(e));
-  count_launch(2);
+  count_launch(a.self_plan ? 1 : 2);
   return PKV_OK;
 }
 
@@ -1035,7 +1205,7 @@ int decode_workspace_bytes(const Pool& P, int32_t n_seq, size_t* bytes) {
 
 int launch_decode(Pool& P, int32_t layer, const void* q, const void* k_pool, const void* v_pool,
                   const int32_t* tables, int32_t W, const int32_t* seq_lens, int32_t n_seq, float scale, void* out,
-                  void* ws, size_t ws_bytes, void* stream) {
+                  void* ws, size_t ws_bytes, void* stream, const AppendFuse* fuse) {
   const auto& g = P.geo;
   const int G = g.H_q / g.H_kv;
   if (G > SIMT_GMAX || (G > GPAD && g.d_head > 128))
@@ -1061,14 +1231,25 @@ int launch_decode(Pool& P, int32_t layer, const void* q, const void* k_pool, con
     a.hdr = reinterpret_cast<int32_t*>(w);
     a.tile_prefix = reinterpret_cast<int32_t*>(w + L.prefix);
     a.lens_c = reinterpret_cast<int32_t*>(w + L.lens);
-    a.counters = reinterpret_cast<int32_t*>(w + L.counters);
+    a.counters = reinterpret_cast<unsigned long long*>(w + L.counters);
     a.wstart = reinterpret_cast<int4*>(w + L.wstart);
     a.partials = reinterpret_cast<float*>(w + L.partials);
     a.total_warps = grid * nw;
     CUtensorMap maps[2] = {tk, tv};
-    return launch_tc_sequence(a, maps, tc_kernel_for(P, &smem), grid, nw, smem, st);
+    bool after_append = false;
+    if (fuse) {  // the step's append kernel first, letting the attention launch start under it
+      after_append = n_seq <= kSelfPlanMaxSeqs;
+      if (int rc = launch_append(P, layer, fuse->k_new, fuse->v_new, fuse->slots, n_seq, fuse->k_pool, fuse->v_pool,
+                                 stream, after_append))
+        return rc;
+    }
+    return launch_tc_sequence(a, maps, tc_kernel_for(P, &smem), grid, nw, smem, st, after_append);
   }
 
+  if (fuse)
+    if (int rc = launch_append(P, layer, fuse->k_new, fuse->v_new, fuse->slots, n_seq, fuse->k_pool, fuse->v_pool,
+                               stream))
+      return rc;
   return launch_simt_decode(P, a, k_pool, v_pool, st);
 }
 
@@ -1169,14 +1350,15 @@ extern "C" int pkv_decode_attention_noalloc(const pkv_pool* pool, int32_t layer,
   // tensor maps encoded on the stack (no cache)
   CUtensorMap maps[2];
   if (int rc = encode_kv_maps(g, k_pool, v_pool, &maps[0], &maps[1])) return rc;
-  // every field the kernels read is written earlier in the same call: the plan
-  // kernel writes the header, prefix, clamped lengths, warp starts and zeroes the
-  // split-pair counters; the attention kernel writes a partial before counting it
+  // every field the kernels read is written earlier in the same call (the plan kernel's
+  // header, prefix, clamped lengths and warp starts; each partial before it is counted),
+  // except the split-pair counters, whose words carry the launch's epoch: a word left by an
+  // earlier call counts as zero
   char* w = static_cast<char*>(ws);
   a.hdr = reinterpret_cast<int32_t*>(w);
   a.tile_prefix = reinterpret_cast<int32_t*>(w + L.prefix);
   a.lens_c = reinterpret_cast<int32_t*>(w + L.lens);
-  a.counters = reinterpret_cast<int32_t*>(w + L.counters);
+  a.counters = reinterpret_cast<unsigned long long*>(w + L.counters);
   a.wstart = reinterpret_cast<int4*>(w + L.wstart);
   a.partials = reinterpret_cast<float*>(w + L.partials);
   a.total_warps = grid * nw;

@@ -3,9 +3,24 @@
 // tcgen05 MMA / TMEM, ldmatrix, movmatrix, mma.sync).
 #pragma once
 
+#include <cuda_fp8.h>
+
 #include <cstdint>
 
 namespace pkv {
+
+// Four bf16 values (two 32-bit words, low half first) to four OCP FP8 E4M3 codes (byte j =
+// value j): each code is the E4M3 value nearest to the binary32 quotient x / s (IEEE
+// division, round to nearest even, saturating to the largest finite value, 448).
+__device__ __forceinline__ uint32_t quant4_e4m3(uint32_t w0, uint32_t w1, float s) {
+  const float x[4] = {__uint_as_float(w0 << 16), __uint_as_float(w0 & 0xffff0000u), __uint_as_float(w1 << 16),
+                      __uint_as_float(w1 & 0xffff0000u)};
+  uint32_t r = 0;
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    r |= static_cast<uint32_t>(__nv_cvt_float_to_fp8(__fdiv_rn(x[j], s), __NV_SATFINITE, __NV_E4M3)) << (8 * j);
+  return r;
+}
 
 // Error word layout: int32 code at [0], int64 detail at byte 8.  The first error
 // recorded wins; later ones are dropped until the host reads and clears it.

@@ -85,8 +85,10 @@ struct CopyItem {
   int64_t dst_off;
 };
 
+// lets_dependents: the kernel lets a programmatic dependent launched right after it start
+// before it completes (the decode step's attention, which waits for it before loading K/V).
 int launch_append(const Pool& P, int32_t layer, const void* k_new, const void* v_new, const int32_t* slots,
-                  int32_t n_tok, void* k_pool, void* v_pool, void* stream);
+                  int32_t n_tok, void* k_pool, void* v_pool, void* stream, bool lets_dependents = false);
 
 // Copy `n` contiguous images of `bytes` bytes each, image i from src_base +
 // items[i].src_off to dst_base + items[i].dst_off (device-accessible pointers).
@@ -94,9 +96,19 @@ int launch_copy_images(const void* src_base, void* dst_base, const CopyItem* ite
                        void* stream);
 
 int decode_workspace_bytes(const Pool& P, int32_t n_seq, size_t* bytes);
+// The new token of each sequence of a decode step (k_new / v_new rows [n_seq][H_kv][d], slot
+// slots[s]), written by the append kernel launched first; on the tensor-core path the
+// attention kernel follows it as a programmatic dependent (its start overlaps the append).
+struct AppendFuse {
+  const void* k_new;
+  const void* v_new;
+  const int32_t* slots;
+  void* k_pool;
+  void* v_pool;
+};
 int launch_decode(Pool& P, int32_t layer, const void* q, const void* k_pool, const void* v_pool,
                   const int32_t* tables, int32_t W, const int32_t* seq_lens, int32_t n_seq, float scale, void* out,
-                  void* ws, size_t ws_bytes, void* stream);
+                  void* ws, size_t ws_bytes, void* stream, const AppendFuse* fuse = nullptr);
 int launch_prefill(Pool& P, int32_t layer, const void* q, const int32_t* q_off, int32_t n_tok, int32_t max_q,
                    const void* k_pool, const void* v_pool, const int32_t* tables, int32_t W, const int32_t* seq_lens,
                    int32_t n_seq, float scale, void* out, void* stream);

@@ -76,7 +76,7 @@ def test_geometries(H_q, H_kv, d, B, dtype):
 ])
 def test_wide_groups_on_tensor_cores(H_q, H_kv, d, dtype, B):
     """9 to 16 query heads per KV head run on the tensor-core kernel with two 8-head
-    column blocks (a plan launch and an attention launch per call); the lengths make
+    column blocks (one launch per call: every CTA plans its own warps); the lengths make
     pairs that end inside one warp's range and pairs split across warps (merged
     partials), ragged tails and an empty sequence."""
     g = W.Geometry(L=2, H_q=H_q, H_kv=H_kv, d_head=d, block_size=B, dtype=dtype, num_blocks=1500)
@@ -89,7 +89,7 @@ def test_wide_groups_on_tensor_cores(H_q, H_kv, d, dtype, B):
         q = W.normal(61, f"q{step}", (len(ids), g.H_q, g.d_head), dtype)
         before = pkv.pkv_launch_count()
         got, tables, sl = b.decode_gpu(ids, q, scale, layer=1)
-        assert pkv.pkv_launch_count() - before == 2  # plan + tensor-core attention
+        assert pkv.pkv_launch_count() - before == 1  # the tensor-core attention, planned in the kernel
         check_attention(got, b.decode_ref(q, tables, sl, scale, layer=1), dtype)
 
 
@@ -158,3 +158,53 @@ def test_workspace_too_small_is_rejected():
         pkv.pkv_decode_attention(b.lib, 0, out, b.kp, b.vp, torch.from_numpy(tables).cuda(),
                                  torch.from_numpy(lens).cuda(), 0.1, out, ws)
     assert e.value.name == "PKV_ERR_INVALID_ARG"
+
+
+def test_plan_kernel_path_beyond_in_kernel_planning():
+    """More than 4,096 sequences: a plan kernel computes the warps' first tiles and the
+    attention kernel follows it as a programmatic dependent (two launches); lengths 0-40
+    give many pairs split across warps and empty sequences."""
+    g = W.Geometry(L=1, H_q=64, H_kv=8, d_head=128, block_size=16, dtype="bf16", num_blocks=10000)
+    b = PagedBatch(g, W.permutation(18, "fo", g.num_blocks), seed=18)
+    lens = [int(x) for x in W.uniform_int(18, "lens", 0, 40, 4500)]
+    ids = b.new_seqs(len(lens))
+    b.append(ids, lens, "prompt")
+    tables, sl = b.tables(ids)
+    sl[::97] = 0  # a few empty sequences: zero output
+    q = W.normal(18, "q", (len(ids), g.H_q, g.d_head), "bf16")
+    before = pkv.pkv_launch_count()
+    got, _, _ = b.decode_gpu(ids, q, 0.09, tables=tables, lens=sl)
+    assert pkv.pkv_launch_count() - before == 2
+    check_attention(got, b.decode_ref(q, tables, sl, 0.09), "bf16")
+    assert np.all(got[::97] == 0)
+
+
+def test_workspace_contents_do_not_matter():
+    """The split-pair counters in the workspace carry each launch's tag, so a workspace
+    holding anything -- random bytes, all ones, another batch's leftovers -- gives the
+    same result without clearing: three calls on one workspace, two batches."""
+    import torch
+
+    g = W.Geometry(L=1, H_q=64, H_kv=8, d_head=128, block_size=16, dtype="bf16", num_blocks=3000)
+    batches = []
+    for seed, lens in ((19, [20000, 3, 700, 1]), (20, [5000, 5000, 0, 12000, 31])):
+        b = PagedBatch(g, W.permutation(seed, "fo", g.num_blocks), seed=seed)
+        ids = b.new_seqs(len(lens))
+        b.append(ids, lens, "prompt")
+        batches.append((b, ids))
+    n_max = max(len(ids) for _, ids in batches)
+    ws = torch.empty(pkv.pkv_decode_workspace_size(batches[0][0].lib, n_max), dtype=torch.uint8, device="cuda")
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(21)
+    fills = [lambda: ws.random_(0, 256, generator=gen), lambda: ws.fill_(255), lambda: None]
+    for k, fill in enumerate(fills):
+        b, ids = batches[k % 2]
+        fill()
+        tables, sl = b.tables(ids)
+        q = W.normal(21, f"q{k}", (len(ids), g.H_q, g.d_head), "bf16")
+        out = torch.full((len(ids), g.H_q, g.d_head), float("nan"), dtype=torch.bfloat16, device="cuda")
+        pkv.pkv_decode_attention(b.lib, 0, to_dev(q, "bf16"), b.kp, b.vp, torch.from_numpy(tables).cuda(),
+                                 torch.from_numpy(sl).cuda(), 0.088, out, ws)
+        pkv.pkv_check_device_error()
+        got = out.double().cpu().numpy()
+        check_attention(got, b.decode_ref(q, tables, sl, 0.088), "bf16")

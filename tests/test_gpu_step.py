@@ -217,3 +217,53 @@ def test_step_launcher_keeps_its_pool_and_checks_host_buffers():
     torch.cuda.synchronize()
     pkv.pkv_check_device_error()
     assert torch.all(oh == 0)
+
+
+@pytest.mark.parametrize("H_q,H_kv,d,B,dtype", [
+    (64, 8, 128, 16, "bf16"),
+    (48, 4, 64, 16, "f16"),     # G = 12 (two head blocks), d 64
+    (32, 2, 128, 32, "bf16"),   # G = 16, 32-token blocks
+    (64, 8, 128, 16, "e4m3"),   # FP8 pool: the kernel quantises the new token
+    (12, 12, 64, 16, "f32"),    # CUDA-core path: the append kernel runs first
+    (16, 2, 96, 16, "bf16"),    # d 96: CUDA-core path
+])
+def test_decode_step_appends_inside_the_attention_launch(H_q, H_kv, d, B, dtype):
+    """On the tensor-core path pkv_decode_step writes each new token from inside the
+    attention kernel (one launch for append and attention); elsewhere the append kernel
+    runs first.  Either way the pools stay bit-exact with the oracle's and every output
+    matches the oracle, over steps whose new tokens open blocks, fill them and copy
+    shared tails."""
+    import torch
+
+    g = W.Geometry(L=2, H_q=H_q, H_kv=H_kv, d_head=d, block_size=B, dtype=dtype, num_blocks=400)
+    b = PagedBatch(g, W.permutation(45, "fo", g.num_blocks), seed=45,
+                   kv_scales=(0.75, 1.5) if dtype == "e4m3" else (1.0, 1.0))
+    ids = b.new_seqs(5)
+    b.append(ids, [B - 1, B, 3 * B + 5, 1, 700], "prompt", layer=-1)
+    kids = [b.fork(ids[2]), b.fork(ids[4])]
+    run = np.array(ids + kids, np.int32)
+    n, Wd = len(run), 64
+    act = "bf16" if dtype == "e4m3" else dtype
+    td = torch_dtype(act)
+    meta_host = torch.zeros(n * (Wd + 2), dtype=torch.int32).pin_memory()
+    meta_dev = torch.zeros(n * (Wd + 2), dtype=torch.int32, device="cuda")
+    ws = torch.empty(pkv.pkv_decode_workspace_size(b.lib, n), dtype=torch.uint8, device="cuda")
+    scale = 1.0 / math.sqrt(d)
+    for step in range(3):
+        layer = step % 2
+        q = W.normal(45, f"q{step}", (n, H_q, d), act)
+        kn = W.normal(45, f"k{step}", (n, H_kv, d), act)
+        vn = W.normal(45, f"v{step}", (n, H_kv, d), act)
+        out = torch.full((n, H_q, d), float("nan"), dtype=td, device="cuda")
+        pkv.pkv_decode_step(b.lib, layer, run, Wd, to_dev(q, act), to_dev(kn, act), to_dev(vn, act), b.kp, b.vp,
+                            scale, out, meta_host, meta_dev, ws)
+        oslots, ocows = b.orc.append(run.tolist(), [1] * n)
+        assert np.array_equal(meta_host[:n].numpy(), oslots)
+        if len(ocows):
+            oracle.copy_blocks(g, ocows, b.hk, b.hv)
+        oracle.write_slots(g, layer, kn, vn, oslots, b.hk, b.hv, b.k_scale, b.v_scale)
+        pkv.pkv_check_device_error()
+        tables, lens = b.tables(run.tolist(), Wd)
+        check_attention(out_f64(out, act), b.decode_ref(q, tables, lens, scale, layer=layer), act)
+        b.check_state()
+        b.check_pools_bitexact()
