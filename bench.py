@@ -91,6 +91,9 @@ class ClockSampler:
         self.proc = None
         self.file = None
 
+    def mark(self):
+        """Per-step marks need NVML's timestamps; nvidia-smi's 200 ms samples have none."""
+
     def start(self):
         try:
             self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
@@ -129,7 +132,10 @@ class ClockSampler:
 
 class NvmlSampler:
     """Read-only NVML queries (SM clock, max SM clock, clock-event reasons) every
-    10 ms from a thread while the timed region runs."""
+    millisecond from a thread while the timed region runs, each stamped with the host
+    clock; mark() stamps a timed step, and each step is given the sample nearest to it."""
+
+    INTERVAL_S = 0.001
 
     REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
                0x80: "hw_power_brake_slowdown"}
@@ -154,6 +160,7 @@ class NvmlSampler:
         self.reason_fn = getattr(self.nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
             self.nv.nvmlDeviceGetCurrentClocksThrottleReasons
         self.samples = []
+        self.marks = []
         self.stop_flag = False
 
     def _sample(self):
@@ -162,12 +169,15 @@ class NvmlSampler:
         self.nv.nvmlDeviceGetClockInfo(self.h, 1, c.byref(mhz))  # NVML_CLOCK_SM
         self.nv.nvmlDeviceGetMaxClockInfo(self.h, 1, c.byref(mx))
         self.reason_fn(self.h, c.byref(rs))
-        self.samples.append((mhz.value, mx.value, rs.value))
+        self.samples.append((mhz.value, mx.value, rs.value, time.perf_counter()))
 
     def _loop(self):
         while not self.stop_flag:
             self._sample()
-            time.sleep(0.01)
+            time.sleep(self.INTERVAL_S)
+
+    def mark(self):
+        self.marks.append(time.perf_counter())
 
     def start(self):
         self.thread = self.threading.Thread(target=self._loop, daemon=True)
@@ -180,8 +190,15 @@ class NvmlSampler:
             self._sample()
         sm = [s[0] for s in self.samples]
         reasons = sorted({name for s in self.samples for bit, name in self.REASONS.items() if s[2] & bit})
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(s[1] for s in self.samples),
-                "reasons": reasons, "samples": len(self.samples), "source": "NVML every 10 ms"}
+        out = {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(s[1] for s in self.samples),
+               "reasons": reasons, "samples": len(self.samples), "source": "NVML every 1 ms"}
+        if self.marks:
+            ts = np.array([s[3] for s in self.samples])
+            near = [self.samples[int(np.abs(ts - m).argmin())][0] for m in self.marks]
+            out["per_step"] = {"steps": len(near), "sm_mhz_min": min(near), "sm_mhz_median": statistics.median(near),
+                               "sm_mhz_max": max(near),
+                               "note": "the sample nearest each timed step's launch (host clock)"}
+        return out
 
 
 def clock_sampler(torch, dev):
@@ -653,6 +670,7 @@ def run_decode(args, torch, pkv, dev, world, rank):
     e_start.record()
     for i, t in enumerate(range(args.warmup, args.warmup + args.steps)):
         r.step(t, timed=True, events=evs[i])
+        clocks.mark()
     e_end.record()
     torch.cuda.synchronize()
     launches = pkv.pkv_launch_count() - launches0
@@ -708,8 +726,98 @@ def run_decode(args, torch, pkv, dev, world, rank):
     return line, r
 
 
+def measure_link(torch, dev, nbytes: int = 1 << 30, reps: int = 3):
+    """Copy-engine ceiling of the host link: pinned cudaMemcpyAsync of nbytes per direction
+    (2 untimed, then `reps` timed back to back), in GB/s."""
+    probe_d = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    probe_h = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    link = {}
+    for name, (dst, src) in (("d2h", (probe_h, probe_d)), ("h2d", (probe_d, probe_h))):
+        for _ in range(2):
+            dst.copy_(src, non_blocking=True)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(reps):
+            dst.copy_(src, non_blocking=True)
+        b.record()
+        torch.cuda.synchronize()
+        link[name] = reps * nbytes / (a.elapsed_time(b) / 1e3) / 1e9
+    del probe_d, probe_h
+    return link
+
+
+def rated_link_gbs(torch, dev):
+    """Rated per-direction bandwidth of this GPU's host link: the sum of its NVLink-C2C links'
+    speeds as `nvidia-smi c2c -s` reports them (a read-only query), or None."""
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+        out = subprocess.run(["nvidia-smi", "c2c", "-s"], capture_output=True, text=True, timeout=20).stdout
+    except Exception:
+        return None
+    total, mine = 0.0, False
+    for line in out.splitlines():
+        if line.startswith("GPU "):
+            mine = uuid in line
+        elif mine and "C2C Link" in line and "GB/s" in line:
+            try:
+                total += float(line.split(":")[1].split()[0])
+            except (IndexError, ValueError):
+                pass
+    return round(total, 1) if total > 0 else None
+
+
+def swap_record(torch, pkv, dev, n_chunks: int = 64):
+    """A bounded swap measurement for the decode lines: n_chunks 80-layer chunks of 16 blocks
+    (5 MiB each) evicted to pinned host frames and restored into fresh blocks, twice, with
+    the SM copy kernel; GB/s per direction against the link measured in the same run."""
+    wl = W.swap(n_chunks=n_chunks, num_blocks=n_chunks * 16 * 3 // 2)
+    g = wl.geometry
+    cb = wl.extra["chunk_blocks"]
+    pool = pkv.pkv_pool_create(g.L, g.H_q, g.H_kv, g.d_head, g.block_size, g.dtype, g.num_blocks, wl.free_order)
+    ids = [pkv.pkv_seq_create(pool) for _ in range(n_chunks)]
+    pkv.pkv_plan_append(pool, ids, wl.lengths)
+    kp = W.device_normal(wl.seed, "k_pool", g.pool_shape(), g.dtype, dev)
+    vp = W.device_normal(wl.seed, "v_pool", g.pool_shape(), g.dtype, dev)
+    frame = 2 * g.L * g.H_kv * g.block_size * g.d_head * g.elem_bytes
+    host = torch.empty(n_chunks * cb * frame, dtype=torch.uint8, pin_memory=True)
+    order = [int(x) for x in wl.extra["evict_order"]]
+    frames = [np.arange(i * cb, (i + 1) * cb, dtype=np.int64) for i in range(n_chunks)]
+    t_out, t_in = [], []
+    for rnd in range(3):  # one untimed round, two timed
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        e[0].record()
+        for i, s in enumerate(order):
+            pkv.pkv_swap_out(pool, ids[s], kp, vp, host, n_chunks * cb, frames[i])
+        e[1].record()
+        for s in order[::-1]:
+            pkv.pkv_swap_in(pool, ids[s], host, n_chunks * cb, cb, kp, vp)
+        e[2].record()
+        torch.cuda.synchronize()
+        if rnd:
+            t_out.append(e[0].elapsed_time(e[1]) / 1e3)
+            t_in.append(e[1].elapsed_time(e[2]) / 1e3)
+    pkv.pkv_check_device_error()
+    del kp, vp, host
+    link = measure_link(torch, dev)
+    rated = rated_link_gbs(torch, dev)
+    nbytes = n_chunks * cb * frame
+    out_gbs, in_gbs = nbytes / statistics.mean(t_out) / 1e9, nbytes / statistics.mean(t_in) / 1e9
+    rec = {"workload": f"{n_chunks} chunks x 16 blocks of the 80-layer 70B geometry ({nbytes / 1e9:.2f} GB) out to "
+                       "pinned host frames and back into fresh blocks, SM copy kernel, mean of 2 rounds",
+           "out_gbs": round(out_gbs, 1), "in_gbs": round(in_gbs, 1),
+           "link_gbs": {k: round(v, 1) for k, v in link.items()},
+           "link_source": "1 GiB pinned cudaMemcpyAsync per direction, this run",
+           "frac": round(min(out_gbs / link["d2h"], in_gbs / link["h2d"]), 4)}
+    if rated:
+        rec["rated_link_gbs"] = rated
+        rec["rated_source"] = "sum of this GPU's NVLink-C2C link speeds (nvidia-smi c2c -s), per direction"
+        rec["frac_of_rated"] = round(min(out_gbs, in_gbs) / rated, 4)
+    return rec
+
+
 def run_swap(args, torch, pkv, dev, world, rank):
-    wl = W.swap()
+    wl = W.swap() if args.swap_chunks == 512 else W.swap(n_chunks=args.swap_chunks,
+                                                         num_blocks=args.swap_chunks * 16 * 3 // 2)
     g = wl.geometry
     nchunk = len(wl.lengths)
     cb = wl.extra["chunk_blocks"]
@@ -727,20 +835,8 @@ def run_swap(args, torch, pkv, dev, world, rank):
     frames_of = {s: np.arange(i * cb, (i + 1) * cb, dtype=np.int64) for i, s in enumerate(ids)}
 
     # host-link roofline: one 1 GiB pinned copy each way on the copy engines
-    probe_d = torch.empty(1 << 30, dtype=torch.uint8, device=dev)
-    probe_h = torch.empty(1 << 30, dtype=torch.uint8, pin_memory=True)
-    link = {}
-    for name, (dst, src) in (("d2h", (probe_h, probe_d)), ("h2d", (probe_d, probe_h))):
-        for _ in range(2):
-            dst.copy_(src, non_blocking=True)
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        for _ in range(3):
-            dst.copy_(src, non_blocking=True)
-        b.record()
-        torch.cuda.synchronize()
-        link[name] = 3 * (1 << 30) / (a.elapsed_time(b) / 1e3) / 1e9
-    del probe_d, probe_h
+    link = measure_link(torch, dev)
+    rated = rated_link_gbs(torch, dev)
 
     out_ms, in_ms = [], []
 
@@ -784,12 +880,14 @@ def run_swap(args, torch, pkv, dev, world, rank):
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": g.dtype, "data": "synthetic",
-        "config": {"workload": "swap: 80-layer 70B GQA geometry (327,680 B/token), 512 chunks x 16 blocks "
-                               "(42.9 GB) evicted to pinned host memory and restored into new blocks",
+        "config": {"workload": f"swap: 80-layer 70B GQA geometry (327,680 B/token), {nchunk} chunks x 16 blocks "
+                               f"({nchunk * cb * frame / 1e9:.1f} GB) evicted to pinned host memory and restored "
+                               "into new blocks",
                    "engine": "copy engines" if args.swap_engine else "SM kernel",
-                   "l2": "inputs larger than L2 (43 GB per direction)", "parallelism": "replicas (no collectives)"},
+                   "l2": f"inputs larger than L2 ({nchunk * cb * frame / 1e9:.1f} GB per direction)" if nchunk * cb * frame > (256 << 20) else "inputs smaller than L2 (diagnostic size)", "parallelism": "replicas (no collectives)"},
         "swap_out_gbs": round(out_gbs, 1), "swap_in_gbs": round(in_gbs, 1),
         "host_link_gbs": {k: round(v, 1) for k, v in link.items()},
+        "rated_link_gbs": rated, "frac_of_rated": round(min(out_gbs, in_gbs) / rated, 4) if rated else None,
         "roofline": {"bound": "host-link", "achieved": round(min(out_gbs, in_gbs), 1), "peak": round(peak, 1),
                      "unit": "GB/s", "frac": round(min(out_gbs / link["d2h"], in_gbs / link["h2d"]), 4),
                      "traffic": None, "kernel": "pkv_swap_out / pkv_swap_in",
@@ -1192,6 +1290,10 @@ def main():
     ap.add_argument("--workload", choices=["agent32k", "chat", "forked", "swap", "tiny", "overlap", "prefill"],
                     default="agent32k")
     ap.add_argument("--swap-engine", type=int, default=0, help="swap workload: 0 SM kernel, 1 copy engines")
+    ap.add_argument("--swap-chunks", type=int, default=512,
+                    help="swap workload: chunks evicted and restored (default 512, 42.9 GB; fewer for small captures)")
+    ap.add_argument("--no-swap-record", action="store_true",
+                    help="decode workloads: skip the bounded swap measurement added to the line")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--context", type=int, default=0, help="agent workload: tokens per sequence (default 32768)")
     ap.add_argument("--n-seq", type=int, default=0, help="agent workload: sequences (default 48)")
@@ -1254,6 +1356,13 @@ def main():
             ref = reference_arm(argparse.Namespace(workload="swap", steps=2, warmup=1), 1, 0)
             line["cpu_baseline"] = dict(ref["cpu_baseline"])
             line["cpu_baseline"]["sample"] += " (host-tier copy baseline)"
+    if world == 1 and runner is not None and not args.no_swap_record and args.workload != "tiny":
+        # the second target of the metric (swap GB/s against the host link), bounded, after the decode
+        # measurement; the decode pools are released first
+        runner.kp = runner.vp = None
+        runner._launchers = {}
+        torch.cuda.empty_cache()
+        line["swap"] = swap_record(torch, pkv, dev)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
