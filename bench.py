@@ -1001,6 +1001,136 @@ def run_overlap(args, torch, pkv, dev, world, rank):
     }, None
 
 
+def run_reload_prefill(args, torch, pkv, dev, world, rank):
+    """Pipelined chunked reload behind the observation's chunked prefill ("KV Cache Management",
+    "Asynchronous paged swapping"): a paused 80-layer sequence's history (16,384 tokens, 5.4 GB)
+    returns from pinned host frames a range of layers at a time on one stream while a 2,048-token
+    observation is prefilled in 512-token chunks on another (per layer: append, then prefill
+    attention over the history and the chunk); layer l of the first chunk waits only for the
+    range holding l.  Phases: reload alone, prefill alone, serial (whole reload, then prefill),
+    pipelined; hidden = (T_reload + T_prefill - T_pipelined) / T_reload."""
+    L, hist, obs, C, per_range = 80, args.context or 16384, 2048, 512, args.reload_layers
+    seed = W.SEEDS["swap"] + 2
+    nb_hist, nb_obs = -(-hist // 16), -(-(hist + obs) // 16) - hist // 16
+    N = nb_hist + nb_obs + 64
+    g = W.Geometry(L=L, H_q=64, H_kv=8, d_head=128, block_size=16, dtype="bf16", num_blocks=N)
+    fo = W.permutation(seed, "reload_fo", N)
+    kp = W.device_normal(seed, "k_pool", g.pool_shape(), g.dtype, dev)
+    vp = W.device_normal(seed, "v_pool", g.pool_shape(), g.dtype, dev)
+    frame = 2 * g.L * g.H_kv * g.block_size * g.d_head * g.elem_bytes
+    host = torch.empty(nb_hist * frame, dtype=torch.uint8, pin_memory=True)
+    frames = np.arange(nb_hist, dtype=np.int64)
+    k_new = W.device_normal(seed, "k_obs", (L, obs, g.H_kv, g.d_head), g.dtype, dev)
+    v_new = W.device_normal(seed, "v_obs", (L, obs, g.H_kv, g.d_head), g.dtype, dev)
+    q = W.device_normal(seed, "q_obs", (L, obs, g.H_q, g.d_head), g.dtype, dev)
+    out = torch.empty((C, g.H_q, g.d_head), dtype=torch.bfloat16, device=dev)
+    offs = torch.tensor([0, C], dtype=torch.int32, device=dev)
+    ranges = [(l0, min(L, l0 + per_range)) for l0 in range(0, L, per_range)]
+    s_copy, s_pre = torch.cuda.Stream(), torch.cuda.Stream()
+    scale = 1.0 / math.sqrt(g.d_head)
+
+    def paused_state():
+        """A fresh control plane whose one sequence holds the history, evicted to the host frames."""
+        pool = pkv.pkv_pool_create(g.L, g.H_q, g.H_kv, g.d_head, g.block_size, g.dtype, N, fo)
+        pkv.pkv_pool_set_swap_engine(pool, args.swap_engine)
+        seq = pkv.pkv_seq_create(pool)
+        pkv.pkv_plan_append(pool, [seq], [hist])
+        pkv.pkv_swap_out(pool, seq, kp, vp, host, nb_hist, frames, stream=s_copy)
+        torch.cuda.synchronize()
+        return pool, seq
+
+    def reload(pool, seq, by_range, stream):
+        evs = {}
+        for l0, l1 in (ranges if by_range else [(0, L)]):
+            pkv.pkv_swap_in_layers(pool, seq, host, nb_hist, nb_hist, l0, l1, kp, vp, stream=stream)
+            ev = torch.cuda.Event()
+            ev.record(stream)
+            for layer in range(l0, l1):
+                evs[layer] = ev
+        return evs
+
+    def prefill(pool, seq, stream, evs=None):
+        slots, _ = pkv.pkv_plan_append(pool, [seq], [obs])
+        W_ = -(-(hist + obs) // 16)
+        tables, _ = pkv.pkv_export_tables(pool, [seq], W_)
+        d_slots = torch.from_numpy(slots.copy()).to(dev, non_blocking=True)
+        d_tables = torch.from_numpy(tables.copy()).to(dev, non_blocking=True)
+        d_lens = [torch.tensor([hist + (c + 1) * C], dtype=torch.int32).to(dev, non_blocking=True)
+                  for c in range(obs // C)]
+        waited = set()
+        for c in range(obs // C):
+            for layer in range(L):
+                if evs is not None and evs[layer] not in waited:
+                    stream.wait_event(evs[layer])
+                    waited.add(evs[layer])
+                pkv.pkv_append_kv(pool, layer, k_new[layer, c * C:(c + 1) * C], v_new[layer, c * C:(c + 1) * C],
+                                  d_slots[c * C:(c + 1) * C], kp, vp, stream=stream)
+                pkv.pkv_prefill_attention(pool, layer, q[layer, c * C:(c + 1) * C], offs, C, kp, vp, d_tables,
+                                          d_lens[c], scale, out, stream=stream)
+
+    def timed(fn):
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(s_pre)
+        s_copy.wait_event(a)
+        fn()
+        e_copy = torch.cuda.Event()
+        e_copy.record(s_copy)
+        s_pre.wait_event(e_copy)
+        b.record(s_pre)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / 1e3
+
+    def run(mode):
+        pool, seq = paused_state()
+        if mode == "reload":
+            return timed(lambda: reload(pool, seq, True, s_copy))
+        if mode == "prefill":
+            reload(pool, seq, False, s_copy)
+            torch.cuda.synchronize()
+            return timed(lambda: prefill(pool, seq, s_pre))
+        if mode == "serial":
+            return timed(lambda: (reload(pool, seq, False, s_pre), prefill(pool, seq, s_pre)))
+        return timed(lambda: prefill(pool, seq, s_pre, reload(pool, seq, True, s_copy)))
+
+    for mode in ("reload", "prefill", "pipelined"):  # warm-up
+        run(mode)
+    clocks = clock_sampler(torch, dev)
+    clocks.start()
+    l0 = pkv.pkv_launch_count()
+    reps = max(1, args.steps)
+    t = {m: statistics.median(run(m) for _ in range(reps)) for m in ("reload", "prefill", "serial", "pipelined")}
+    launches = pkv.pkv_launch_count() - l0
+    clk = clocks.stop()
+    pkv.pkv_check_device_error()
+    rb = nb_hist * frame
+    flop = L * sum(4.0 * g.H_q * g.d_head * (hist + c * C + i + 1) for c in range(obs // C) for i in range(C))
+    hidden = (t["reload"] + t["prefill"] - t["pipelined"]) / t["reload"]
+    peak, _ = load_peaks()
+    tflops = flop / t["pipelined"] / 1e12
+    return {
+        "metric": METRIC, "value": round(rb / t["pipelined"] / 1e9, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": reps, "warmup": 1, "ms_per_step": round(t["pipelined"] * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"reload_prefill: an 80-layer 70B GQA sequence's {hist}-token history "
+                               f"({rb / 1e9:.2f} GB) reloaded from pinned host frames {per_range} layers at a time "
+                               f"while a {obs}-token observation is prefilled in {C}-token chunks",
+                   "engine": "copy engines" if args.swap_engine else "SM kernel",
+                   "l2": "inputs larger than L2", "parallelism": "replicas (no collectives)"},
+        "hidden_reload_fraction": round(hidden, 3),
+        "exposed_reload_ms": round((t["pipelined"] - t["prefill"]) * 1e3, 3),
+        "ms": {k: round(v * 1e3, 3) for k, v in t.items()},
+        "reload_gbs_alone": round(rb / t["reload"] / 1e9, 1),
+        "prefill_tflops_alone": round(flop / t["prefill"] / 1e12, 1), "prefill_tflops_pipelined": round(tflops, 1),
+        "roofline": {"bound": "host-link", "achieved": round(rb / t["reload"] / 1e9, 1), "peak": None,
+                     "unit": "GB/s", "frac": None, "traffic": None,
+                     "kernel": "pkv_swap_in_layers (reload alone); see the swap workload for the link's peak"},
+        "e2e": {"value": round(rb / t["pipelined"] / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": rb,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": int(launches), "clocks": clk,
+    }, None
+
+
 def run_prefill(args, torch, pkv, dev, world, rank):
     """Chunked prefill: 8 sequences with 16,384 cached tokens each take a 512-token chunk.
     Each step forks the 8 histories (no data moves), plans and writes the chunks'
@@ -1182,7 +1312,7 @@ def reference_arm(args, world, rank):
                              "sample": "oracle chunked-prefill attention, 1 sequence x 32 queries x 16,416 keys"},
             "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         }
-    if args.workload in ("swap", "overlap"):
+    if args.workload in ("swap", "overlap", "reload_prefill"):
         wl = W.swap(n_chunks=16)
         g = wl.geometry
         nb = 64
@@ -1287,9 +1417,12 @@ def main():
     ap.add_argument("--steps", type=int, default=None, help="timed steps (default 100; swap 4)")
     ap.add_argument("--warmup", type=int, default=None, help="warm-up steps (default 10; swap 3)")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["agent32k", "chat", "forked", "swap", "tiny", "overlap", "prefill"],
+    ap.add_argument("--workload", choices=["agent32k", "chat", "forked", "swap", "tiny", "overlap", "prefill",
+                                           "reload_prefill"],
                     default="agent32k")
     ap.add_argument("--swap-engine", type=int, default=0, help="swap workload: 0 SM kernel, 1 copy engines")
+    ap.add_argument("--reload-layers", type=int, default=1,
+                    help="reload_prefill workload: layers per reload range (default 1)")
     ap.add_argument("--swap-chunks", type=int, default=512,
                     help="swap workload: chunks evicted and restored (default 512, 42.9 GB; fewer for small captures)")
     ap.add_argument("--no-swap-record", action="store_true",
@@ -1308,7 +1441,7 @@ def main():
                     help="ncu dram bytes per decode launch, if captured for this kernel version")
     args = ap.parse_args()
     if args.steps is None:
-        args.steps = {"swap": 4, "overlap": 8, "prefill": 20}.get(args.workload, 100)
+        args.steps = {"swap": 4, "overlap": 8, "prefill": 20, "reload_prefill": 3}.get(args.workload, 100)
     if args.warmup is None:
         args.warmup = 3 if args.workload == "swap" else 10
     if args.warmup < 3:
@@ -1341,6 +1474,8 @@ def main():
         line, runner = run_overlap(args, torch, pkv, dev, world, rank)
     elif args.workload == "prefill":
         line, runner = run_prefill(args, torch, pkv, dev, world, rank)
+    elif args.workload == "reload_prefill":
+        line, runner = run_reload_prefill(args, torch, pkv, dev, world, rank)
     else:
         line, runner = run_decode(args, torch, pkv, dev, world, rank)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

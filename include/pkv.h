@@ -362,8 +362,28 @@ int pkv_swap_in(pkv_pool* pool, int32_t seq, const void* host, int64_t host_fram
  * the copy engines, pkv_pool_set_swap_engine(pool, 1), so the SMs stay with
  * attention) while other sequences decode; record an event after it and make the
  * stream that decodes the restored sequence wait on that event. */
-enum pkv_tier { PKV_TIER_HBM = 0, PKV_TIER_HOST = 1 };
+enum pkv_tier { PKV_TIER_HBM = 0, PKV_TIER_HOST = 1, PKV_TIER_RELOADING = 2 };
 int pkv_seq_residency(const pkv_pool* pool, int32_t seq, int32_t* tier);
+
+/* Reload a swapped-out sequence a range of layers at a time ([KVM] "Asynchronous paged
+ * swapping", "Pipelined Chunked Reload and Observation Prefill": the history streams in over
+ * the copy path while the observation's own prefill runs, instead of a stall for the whole
+ * transfer).  The first call (layer_begin 0) allocates the n fresh blocks from the FIFO front
+ * (all or nothing) and points the table at them, as pkv_swap_in does; every call copies layers
+ * [layer_begin, layer_end) of every block from the host frames recorded at swap-out (one
+ * contiguous piece of each block image and frame half, both [L][H_kv][B][d]).  Ranges must
+ * follow each other from layer 0 to L; until the last one the sequence's residency is
+ * PKV_TIER_RELOADING and its recorded frames are kept (pkv_seq_host_slots).  Asynchronous on
+ * `stream`: record an event after each range and make the stream that appends to or attends
+ * over layer l of this sequence wait for the event of the range holding l -- the copy writes
+ * whole block images of those layers, including slots a later append fills.
+ * new_block_ids: optional HOST int32 [n], the table after the call.  Errors: INVALID_ARG (not
+ * swapped out and not being reloaded, a range out of order or beyond L, n not the swapped block
+ * count), BAD_BLOCK_ID (a recorded frame beyond host_frames), OUT_OF_BLOCKS (first call only);
+ * a failed call changes nothing. */
+int pkv_swap_in_layers(pkv_pool* pool, int32_t seq, const void* host, int64_t host_frames, int32_t n,
+                       int32_t layer_begin, int32_t layer_end, void* k_pool, void* v_pool, int32_t* new_block_ids,
+                       pkv_stream_t stream);
 
 /* Host frames recorded for a swapped-out sequence: HOST int64 [capacity], *n = count. */
 int pkv_seq_host_slots(const pkv_pool* pool, int32_t seq, int64_t* out, int32_t capacity, int32_t* n);

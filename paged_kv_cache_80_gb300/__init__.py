@@ -24,7 +24,7 @@ __all__ = [
     "StepLauncher",
     "pkv_prefill_attention",
     "pkv_copy_blocks", "pkv_swap_out",
-    "pkv_swap_in", "pkv_seq_host_slots", "pkv_seq_residency", "TIER_HBM", "TIER_HOST", "pkv_pool_set_swap_engine", "pkv_check_device_error", "pkv_launch_count",
+    "pkv_swap_in", "pkv_swap_in_layers", "pkv_seq_host_slots", "pkv_seq_residency", "TIER_HBM", "TIER_HOST", "TIER_RELOADING", "pkv_pool_set_swap_engine", "pkv_check_device_error", "pkv_launch_count",
     "pkv_selftest_bounded_wait", "pkv_device_code_version", "pkv_pool_set_kv_scales", "pkv_pool_kv_scales",
     "PrefixStats", "pkv_prefix_cache_create", "pkv_prefix_cache_destroy", "pkv_prefix_match", "pkv_prefix_attach",
     "pkv_prefix_insert", "pkv_prefix_release", "pkv_prefix_evict", "pkv_prefix_get_stats", "pkv_prefix_export",
@@ -120,6 +120,7 @@ def _L():
             "pkv_swap_in": ([vp, i32, vp, i64, i32, vp, vp, P32, vp], ctypes.c_int),
             "pkv_seq_host_slots": ([vp, i32, P64, i32, P32], ctypes.c_int),
             "pkv_seq_residency": ([vp, i32, P32], ctypes.c_int),
+            "pkv_swap_in_layers": ([vp, i32, vp, i64, i32, i32, i32, vp, vp, P32, vp], ctypes.c_int),
             "pkv_pool_set_swap_engine": ([vp, i32], ctypes.c_int),
             "pkv_pool_set_kv_scales": ([vp, ctypes.c_float, ctypes.c_float], ctypes.c_int),
             "pkv_pool_kv_scales": ([vp, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_float)], ctypes.c_int),
@@ -371,7 +372,7 @@ def pkv_pool_kv_scales(pool: PoolLike):
     return k.value, v.value
 
 
-TIER_HBM, TIER_HOST = 0, 1
+TIER_HBM, TIER_HOST, TIER_RELOADING = 0, 1, 2
 
 
 def pkv_seq_residency(pool: PoolLike, seq: int) -> int:
@@ -607,6 +608,17 @@ def pkv_swap_in(pool: PoolLike, seq: int, host, host_frames: int, n: int, k_pool
     ids = np.zeros(max(n, 1), np.int32)
     _check(_L().pkv_swap_in(_h(pool), seq, _host_ptr(host, "host"), host_frames, n, _dev(k_pool, "k_pool"),
                             _dev(v_pool, "v_pool"), _p32(ids), _stream(stream)), "pkv_swap_in")
+    return ids[:n]
+
+
+def pkv_swap_in_layers(pool: PoolLike, seq: int, host, host_frames: int, n: int, layer_begin: int, layer_end: int,
+                       k_pool, v_pool, stream=None) -> np.ndarray:
+    """Reload layers [layer_begin, layer_end) of a swapped-out sequence (the first call, at layer
+    0, allocates and remaps); returns the sequence's table."""
+    ids = np.zeros(max(n, 1), np.int32)
+    _check(_L().pkv_swap_in_layers(_h(pool), seq, _host_ptr(host, "host"), host_frames, n, layer_begin, layer_end,
+                                   _dev(k_pool, "k_pool"), _dev(v_pool, "v_pool"), _p32(ids), _stream(stream)),
+           "pkv_swap_in_layers")
     return ids[:n]
 
 

@@ -16,6 +16,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cstdlib>
 #include <cmath>
 #include <cstring>
 #include <string>
@@ -489,6 +490,7 @@ int pkv_swap_out(pkv_pool* pool, int32_t seq, const void* k_pool, const void* v_
   SeqState* s = find_seq(P, seq);
   if (!s) return unknown_seq(P, seq);
   if (s->swapped) return fail(PKV_ERR_INVALID_ARG, "sequence is already swapped out");
+  if (s->reload_next >= 0) return fail(PKV_ERR_INVALID_ARG, "sequence is still being reloaded");
   if (static_cast<int64_t>(s->table.size()) != n)
     return fail(PKV_ERR_INVALID_ARG, "n must equal the sequence's block count (" + std::to_string(s->table.size()) + ")");
   std::unordered_map<int64_t, int> seen;
@@ -573,13 +575,92 @@ int pkv_swap_in(pkv_pool* pool, int32_t seq, const void* host, int64_t host_fram
   return PKV_OK;
 }
 
+// CTAs of the SM copier in a reload by layers: 32 keep the host link at its copy rate (~205 GB/s
+// alone) and leave the other SMs to the prefill the reload runs behind (16 reach ~175 GB/s; 128
+// slow the prefill).  PKV_RELOAD_CTAS overrides it for tuning.
+static int reload_ctas() {
+  if (const char* e = std::getenv("PKV_RELOAD_CTAS")) return std::max(1, std::atoi(e));
+  return 32;
+}
+
+int pkv_swap_in_layers(pkv_pool* pool, int32_t seq, const void* host, int64_t host_frames, int32_t n,
+                       int32_t layer_begin, int32_t layer_end, void* k_pool, void* v_pool, int32_t* new_block_ids,
+                       pkv_stream_t stream) {
+  pkv::clear_error();
+  if (!pool || n < 0 || (n > 0 && (!k_pool || !v_pool || !host)))
+    return fail(PKV_ERR_INVALID_ARG, "bad arguments to pkv_swap_in_layers");
+  Pool& P = *as_pool(pool);
+  SeqState* s = find_seq(P, seq);
+  if (!s) return unknown_seq(P, seq);
+  const int32_t L = P.geo.L;
+  if (layer_begin < 0 || layer_end <= layer_begin || layer_end > L)
+    return fail(PKV_ERR_INVALID_ARG, "layer range must satisfy 0 <= layer_begin < layer_end <= L");
+  const bool first = s->swapped;
+  if (first) {
+    if (layer_begin != 0) return fail(PKV_ERR_INVALID_ARG, "a reload starts at layer 0");
+  } else {
+    if (s->reload_next < 0) return fail(PKV_ERR_INVALID_ARG, "sequence is neither swapped out nor being reloaded");
+    if (layer_begin != s->reload_next)
+      return fail(PKV_ERR_INVALID_ARG, "layer ranges must follow each other: the next one starts at layer " +
+                                           std::to_string(s->reload_next));
+  }
+  if (static_cast<int64_t>(s->host_frames.size()) != n)
+    return fail(PKV_ERR_INVALID_ARG, "n must equal the sequence's swapped block count (" +
+                                         std::to_string(s->host_frames.size()) + ")");
+  for (int64_t f : s->host_frames)
+    if (f >= host_frames) return fail(PKV_ERR_BAD_BLOCK_ID, "recorded host frame beyond host_frames");
+  if (first && P.free.size() < n)
+    return fail(PKV_ERR_OUT_OF_BLOCKS, "swap-in needs " + std::to_string(n) + " blocks, " +
+                                           std::to_string(P.free.size()) + " free");
+  if (n > 0) {
+    const int kReloadCtas = reload_ctas();
+    void* dhost = const_cast<void*>(host);
+    if (P.swap_engine == 0 && !(dhost = device_view_of_host(dhost)))
+      return fail(PKV_ERR_INVALID_ARG, "host tier is not device-accessible (use page-locked memory)");
+    // a block image and a frame half are [L][H_kv][B][d]: the layer range is one contiguous piece of each
+    const int64_t layer_bytes = P.block_bytes / L;
+    const int64_t off = layer_begin * layer_bytes, bytes = (layer_end - layer_begin) * layer_bytes;
+    std::vector<pkv::CopyItem> kit(n), vit(n);
+    for (int32_t j = 0; j < n; ++j) {
+      const int64_t frame = s->host_frames[j] * 2 * P.block_bytes;
+      const int64_t blk = static_cast<int64_t>(first ? P.free.front_at(j) : s->table[j]) * P.block_bytes;
+      kit[j] = {frame + off, blk + off};
+      vit[j] = {frame + P.block_bytes + off, blk + off};
+    }
+    // a reload shares the GPU with the prefill it runs behind: the SM copier takes a few SMs only
+    // (kReloadCtas CTAs keep the host link busy), not one CTA per 128 KiB
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    int rc = P.swap_engine == 0 ? pkv::launch_copy_images(dhost, k_pool, kit.data(), n, bytes, st, kReloadCtas)
+                                : copy_engine(dhost, k_pool, kit.data(), n, bytes, st);
+    if (rc == PKV_OK)
+      rc = P.swap_engine == 0 ? pkv::launch_copy_images(dhost, v_pool, vit.data(), n, bytes, st, kReloadCtas)
+                              : copy_engine(dhost, v_pool, vit.data(), n, bytes, st);
+    if (rc != PKV_OK) return rc;
+  }
+  if (first) {  // allocate and remap exactly as pkv_swap_in does
+    for (int32_t j = 0; j < n; ++j) {
+      const int32_t p = P.free.pop_front();
+      P.ref[p] = 1;
+      s->table.push_back(p);
+    }
+    s->swapped = false;
+  }
+  if (new_block_ids) std::copy(s->table.begin(), s->table.end(), new_block_ids);
+  s->reload_next = layer_end;
+  if (layer_end == L) {  // every layer is back
+    s->host_frames.clear();
+    s->reload_next = -1;
+  }
+  return PKV_OK;
+}
+
 int pkv_seq_residency(const pkv_pool* pool, int32_t seq, int32_t* tier) {
   pkv::clear_error();
   if (!pool || !tier) return fail(PKV_ERR_INVALID_ARG, "NULL argument");
   const Pool& P = *as_pool(pool);
   const SeqState* s = find_seq(P, seq);
   if (!s) return unknown_seq(P, seq);
-  *tier = s->swapped ? PKV_TIER_HOST : PKV_TIER_HBM;
+  *tier = s->swapped ? PKV_TIER_HOST : (s->reload_next >= 0 ? PKV_TIER_RELOADING : PKV_TIER_HBM);
   return PKV_OK;
 }
 
@@ -589,7 +670,7 @@ int pkv_seq_host_slots(const pkv_pool* pool, int32_t seq, int64_t* out, int32_t 
   const Pool& P = *as_pool(pool);
   const SeqState* s = find_seq(P, seq);
   if (!s) return unknown_seq(P, seq);
-  if (!s->swapped) return fail(PKV_ERR_INVALID_ARG, "sequence is not swapped out");
+  if (!s->swapped && s->reload_next < 0) return fail(PKV_ERR_INVALID_ARG, "sequence is not swapped out");
   *n = static_cast<int32_t>(s->host_frames.size());
   if (out)
     for (int32_t j = 0; j < *n && j < capacity; ++j) out[j] = s->host_frames[j];

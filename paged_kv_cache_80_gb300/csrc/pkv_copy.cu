@@ -239,8 +239,38 @@ __global__ void __launch_bounds__(kCopyThreads) copy_images_kernel(const __grid_
   }
 }
 
+// The same copies from a fixed number of CTAs, each looping over (image, 128 KiB segment)
+// items: a transfer that shares the GPU with compute (a reload behind prefill) takes only the
+// SMs the host link needs, not one CTA per segment.
+__global__ void __launch_bounds__(kCopyThreads) copy_images_few_kernel(const __grid_constant__ CopyBatch b,
+                                                                       int32_t segs) {
+  const int64_t nvec = b.bytes >> 4;
+  const int64_t seg_vec = kCopySeg >> 4;
+  constexpr int64_t step = static_cast<int64_t>(kCopyThreads) * kCopyUnroll;
+  for (int64_t w = blockIdx.x; w < static_cast<int64_t>(b.n) * segs; w += gridDim.x) {
+    const int img = static_cast<int>(w / segs);
+    const int4* __restrict__ src = reinterpret_cast<const int4*>(b.src[img]);
+    int4* __restrict__ dst = reinterpret_cast<int4*>(b.dst[img]);
+    const int64_t beg = (w - static_cast<int64_t>(img) * segs) * seg_vec;
+    const int64_t end = min(nvec, beg + seg_vec);
+    for (int64_t base = beg + threadIdx.x; base < end; base += step) {
+      int4 v[kCopyUnroll];
+#pragma unroll
+      for (int u = 0; u < kCopyUnroll; ++u) {
+        const int64_t k = base + static_cast<int64_t>(u) * kCopyThreads;
+        if (k < end) v[u] = __ldcs(src + k);
+      }
+#pragma unroll
+      for (int u = 0; u < kCopyUnroll; ++u) {
+        const int64_t k = base + static_cast<int64_t>(u) * kCopyThreads;
+        if (k < end) __stcs(dst + k, v[u]);
+      }
+    }
+  }
+}
+
 int launch_copy_images(const void* src_base, void* dst_base, const CopyItem* items, int64_t n, int64_t bytes,
-                       void* stream) {
+                       void* stream, int max_ctas) {
   if (n == 0 || bytes == 0) return PKV_OK;
   if ((bytes & 15) || (reinterpret_cast<uintptr_t>(src_base) & 15) || (reinterpret_cast<uintptr_t>(dst_base) & 15))
     return fail(PKV_ERR_INVALID_ARG, "copy: images and bases must be 16-byte aligned");
@@ -256,8 +286,14 @@ int launch_copy_images(const void* src_base, void* dst_base, const CopyItem* ite
       b.dst[j] = static_cast<char*>(dst_base) + items[i0 + j].dst_off;
     }
     b.n = m;
-    dim3 grid(static_cast<unsigned>(segs), static_cast<unsigned>(m));
-    copy_images_kernel<<<grid, kCopyThreads, 0, s>>>(b);
+    if (max_ctas > 0) {
+      const int64_t items_n = static_cast<int64_t>(m) * segs;
+      copy_images_few_kernel<<<static_cast<unsigned>(std::min<int64_t>(items_n, max_ctas)), kCopyThreads, 0, s>>>(
+          b, static_cast<int32_t>(segs));
+    } else {
+      dim3 grid(static_cast<unsigned>(segs), static_cast<unsigned>(m));
+      copy_images_kernel<<<grid, kCopyThreads, 0, s>>>(b);
+    }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return fail(PKV_ERR_CUDA, std::string("copy launch: ") + cudaGetErrorString(e));
     count_launch();

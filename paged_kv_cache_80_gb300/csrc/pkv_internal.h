@@ -39,7 +39,8 @@ struct SeqState {
   int64_t len = 0;                  // tokens written
   uint8_t state = 0;                // 0 live, 1 released
   bool swapped = false;             // blocks live in host frames
-  std::vector<int64_t> host_frames; // frames holding the blocks while swapped
+  std::vector<int64_t> host_frames; // frames holding the blocks while swapped (or being reloaded)
+  int32_t reload_next = -1;         // a reload by layer ranges: layers [reload_next, L) still to copy
 };
 
 struct TensorMaps;  // cached TMA descriptors (defined in pkv_decode.cu)
@@ -91,9 +92,10 @@ int launch_append(const Pool& P, int32_t layer, const void* k_new, const void* v
                   int32_t n_tok, void* k_pool, void* v_pool, void* stream, bool lets_dependents = false);
 
 // Copy `n` contiguous images of `bytes` bytes each, image i from src_base +
-// items[i].src_off to dst_base + items[i].dst_off (device-accessible pointers).
+// items[i].src_off to dst_base + items[i].dst_off (device-accessible pointers).  max_ctas > 0:
+// from at most that many CTAs (a copy that runs beside compute), else one CTA per 128 KiB.
 int launch_copy_images(const void* src_base, void* dst_base, const CopyItem* items, int64_t n, int64_t bytes,
-                       void* stream);
+                       void* stream, int max_ctas = 0);
 
 int decode_workspace_bytes(const Pool& P, int32_t n_seq, size_t* bytes);
 // The new token of each sequence of a decode step (k_new / v_new rows [n_seq][H_kv][d], slot
