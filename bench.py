@@ -47,11 +47,11 @@ METRIC = "paged decode attention KV GB/s & tokens/s (% of 8 TB/s HBM); swap GB/s
 # of one decode launch, per (stored K/V type, query heads per KV head), from ncu
 # captures of agent 48 x 4,096 (summary in profiles/) of the kernels built from the
 # sources with this digest.  Reported only while the sources hash to TRAFFIC_SOURCES_SHA256.
-TRAFFIC_SOURCES_SHA256 = "67d79765b0f2906f356190f872eadd0b84d69d51b5a40b1fe1204d12def797cc"
+TRAFFIC_SOURCES_SHA256 = "73a8616c7c3c6223dc9175ab1c36a53fa880663b71df309e5ec1ffe4bdc9f65c"
 TRAFFIC_RECORD = {
-    ("bf16", 8): 1.0104,   # 811.6 + 4.7 MB DRAM for 807.9 MB algorithmic
-    ("e4m3", 8): 1.0163,   # 407.0 + 4.4 MB for 404.8 MB
-    ("bf16", 16): 1.0137,  # 814.4 + 6.2 MB for 809.5 MB
+    ("bf16", 8): 1.0078,   # 811.5 + 3.2 MB DRAM for 808.3 MB algorithmic (mean of 2 launches)
+    ("e4m3", 8): 1.0119,   # 407.0 + 2.9 MB for 405.1 MB
+    ("bf16", 16): 1.0111,  # 814.3 + 4.5 MB for 809.9 MB
 }
 
 
@@ -724,6 +724,26 @@ def run_decode(args, torch, pkv, dev, world, rank):
         "clocks": clk,
     }
     return line, r
+
+
+def config_records(args, torch, pkv, dev, world, rank, steps: int = 20):
+    """Bounded runs of the other decode configurations (tiny, chat, forked) for the default
+    line: the same measurement as `--workload <name>` at `steps` timed steps, reduced to its
+    key figures."""
+    recs = {}
+    for name in ("tiny", "chat", "forked"):
+        sub = argparse.Namespace(**vars(args))
+        sub.workload, sub.steps, sub.warmup = name, steps, 3
+        sub.l2_flush, sub.kv_dtype, sub.q_heads, sub.context, sub.n_seq, sub.traffic = False, "bf16", 0, 0, 0, None
+        ln, r = run_decode(sub, torch, pkv, dev, world, rank)
+        recs[name] = {"workload": ln["config"]["workload"], "value": ln["value"], "unit": ln["unit"],
+                      "ms_per_step": ln["ms_per_step"], "tokens_per_s": ln["tokens_per_s"],
+                      "decode_call": {k: ln["roofline"][k] for k in ("achieved", "frac", "avg_launch_ms")},
+                      "e2e": ln["e2e"]["value"], "gpu_launches": ln["gpu_launches"],
+                      "sm_mhz": ln["clocks"]["sm_mhz"] if ln["clocks"] else None, "steps": steps}
+        del r
+        torch.cuda.empty_cache()
+    return recs
 
 
 def measure_link(torch, dev, nbytes: int = 1 << 30, reps: int = 3):
@@ -1425,6 +1445,8 @@ def main():
                     help="reload_prefill workload: layers per reload range (default 1)")
     ap.add_argument("--swap-chunks", type=int, default=512,
                     help="swap workload: chunks evicted and restored (default 512, 42.9 GB; fewer for small captures)")
+    ap.add_argument("--no-config-records", action="store_true",
+                    help="default line: skip the bounded tiny / chat / forked runs added to it")
     ap.add_argument("--no-swap-record", action="store_true",
                     help="decode workloads: skip the bounded swap measurement added to the line")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -1498,6 +1520,11 @@ def main():
         runner._launchers = {}
         torch.cuda.empty_cache()
         line["swap"] = swap_record(torch, pkv, dev)
+    if (world == 1 and args.workload == "agent32k" and not (args.context or args.n_seq or args.q_heads)
+            and args.kv_dtype == "bf16" and not args.no_config_records):
+        # driver-observed figures for the other decode configurations, bounded
+        runner = None
+        line["other_configs"] = config_records(args, torch, pkv, dev, world, rank)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
