@@ -370,10 +370,11 @@ class DecodeRunner:
         host memory and its result is read on the host before the next step's inputs are
         sent.  The host half of step t + 1 (pkv_step_plan: slots, tables, CoW pairs -- it needs
         no result of step t) runs while step t is on the GPU, as a serving loop's scheduler
-        does; the device half (pkv_step_launch_host through a StepLauncher, which binds the
-        buffers that stay the same from step to step) copies the inputs in, runs the step and
-        copies the result out."""
+        does; the device half (pkv_step_launch_packed through a PackedStepLauncher, which binds
+        the buffers that stay the same from step to step) copies the step's packed inputs and
+        its metadata in, runs the step and copies the result out."""
         torch, pkv, g = self.torch, self.pkv, self.g
+        rk = g.H_kv * g.d_head * self.act_bytes
 
         def plan(t):
             ids = self.running(t)
@@ -390,13 +391,9 @@ class DecodeRunner:
             if cur is not None:
                 ids, pool, k, hnp, hbuf, dmeta, cows = cur
                 n = len(ids)
-
-                def rows(x):  # the first n rows (the whole buffer when every sequence runs)
-                    return x if x.shape[0] == n else x[:n]
-
-                q, kn, vn = rows(self.q_e2e), rows(self.kn_e2e), rows(self.vn_e2e)
-                self.launcher_for(pool)(n, self.Wd, cows, rows(host[0][t]), rows(host[1][t]), rows(host[2][t]),
-                                        rows(self.out_host), hbuf, dmeta, attn_events=events[i] if events else None)
+                in_bytes = self.off_v + n * rk
+                self.launcher_for(pool)(n, self.Wd, cows, host[t], self.off_k, self.off_v, in_bytes, self.out_host,
+                                        dmeta, meta_host=hbuf, attn_events=events[i] if events else None)
                 self.flush_l2(t)
                 nbytes = self.staging.mark(k, n * (self.Wd + 2))
                 self.pool = pool
@@ -417,21 +414,21 @@ class DecodeRunner:
                                       2 * n * g.H_kv * g.d_head * (self.act_bytes + g.elem_bytes))
                 self.tokens.append(n)
                 self.h2d_meta += nbytes
-            self.e2e_in_bytes += nbytes + (q.numel() + kn.numel() + vn.numel()) * self.act_bytes
+            self.e2e_in_bytes += nbytes + in_bytes
             self.e2e_out_bytes += n * g.H_q * g.d_head * self.act_bytes
 
     def launcher_for(self, pool):
-        """pkv_step_launch_host with this runner's device staging, pools, scale and workspace
-        bound once: a StepLauncher per (control-plane state, stream).  The key holds the Pool
-        object itself (it stays alive while cached) and the stream the launcher is fixed to,
-        torch's current stream."""
+        """pkv_step_launch_packed with this runner's device staging, pools, scale and workspace
+        bound once: a PackedStepLauncher per (control-plane state, stream).  The key holds the
+        Pool object itself (it stays alive while cached) and the stream the launcher is fixed
+        to, torch's current stream."""
         if not hasattr(self, "_launchers"):
             self._launchers = {}
         stream = self.torch.cuda.current_stream().cuda_stream
         key = (pool, stream)
         if key not in self._launchers:
-            self._launchers[key] = self.pkv.StepLauncher(pool, 0, self.q_e2e, self.kn_e2e, self.vn_e2e, self.out,
-                                                         self.kp, self.vp, self.scale, self.ws, stream=stream)
+            self._launchers[key] = self.pkv.PackedStepLauncher(pool, 0, self.in_e2e, self.out, self.kp, self.vp,
+                                                               self.scale, self.ws, stream=stream)
         return self._launchers[key]
 
     def _refresh_handle(self):
@@ -443,19 +440,20 @@ class DecodeRunner:
         pass
 
     def prepare_e2e(self):
+        """Each step's inputs packed in one pinned host buffer, q (n_max rows), then k_new and
+        v_new (n_max rows each); a step of n sequences copies q's and k_new's n_max rows and
+        v_new's first n (the layout does not depend on n)."""
         torch, g = self.torch, self.g
         n = self.n_max
-        sh_q = (self.total_steps, n, g.H_q, g.d_head)
-        sh_k = (self.total_steps, n, g.H_kv, g.d_head)
-        # host copies of the step inputs, in pinned memory
-        host = []
-        for src in (self.q, self.kn, self.vn):
-            h = torch.empty(src.shape, dtype=src.dtype, pin_memory=True)
-            h.copy_(src)
-            host.append(h)
-        self.q_e2e = torch.empty(sh_q[1:], dtype=self.td, device=self.dev)
-        self.kn_e2e = torch.empty(sh_k[1:], dtype=self.td, device=self.dev)
-        self.vn_e2e = torch.empty(sh_k[1:], dtype=self.td, device=self.dev)
+        rq, rk = g.H_q * g.d_head * self.act_bytes, g.H_kv * g.d_head * self.act_bytes
+        self.off_k, self.off_v = n * rq, n * (rq + rk)
+        step_bytes = n * (rq + 2 * rk)
+        host = torch.empty((self.total_steps, step_bytes), dtype=torch.uint8, pin_memory=True)
+        for t in range(self.total_steps):
+            for src, o0, o1 in ((self.q, 0, self.off_k), (self.kn, self.off_k, self.off_v),
+                                (self.vn, self.off_v, step_bytes)):
+                host[t, o0:o1].view(self.td).copy_(src[t].reshape(-1))
+        self.in_e2e = torch.empty(step_bytes, dtype=torch.uint8, device=self.dev)
         self.out_host = torch.empty(self.out.shape, dtype=self.td, pin_memory=True)
         return host
 
@@ -535,12 +533,14 @@ class ChatRunner(DecodeRunner):
     def running(self, t):
         k = t % self.sched_steps
         self.pool, ids = self.states[t // self.sched_steps]
-        return self.all_ids[self.gen_np > k]
+        if not hasattr(self, "_run_by_k"):  # the schedule's running sets and releases, made once
+            self._run_by_k = [self.all_ids[self.gen_np > j] for j in range(self.sched_steps)]
+            self._done_by_k = [[int(x) for x in self.all_ids[self.gen_np == j + 1]] for j in range(self.sched_steps)]
+        return self._run_by_k[k]
 
     def after_step(self, t, ids):
-        k = t % self.sched_steps
-        for s in ids[self.gen_np[ids] == k + 1]:  # generated budget reached: release
-            self.pkv.pkv_seq_free(self.pool, int(s))
+        for s in self._done_by_k[t % self.sched_steps]:  # generated budget reached: release
+            self.pkv.pkv_seq_free(self.pool, s)
 
 
 class ForkedRunner(DecodeRunner):

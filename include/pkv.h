@@ -198,8 +198,12 @@ int pkv_decode_workspace_size(const pkv_pool* pool, int32_t n_seq, size_t* bytes
  *   block_tables: device int32 [n_seq][W];  seq_lens: device int32 [n_seq]
  *                 (0 <= len <= W*B; len 0 gives a zero output).
  *   workspace   : device, >= pkv_decode_workspace_size bytes, 256-byte aligned;
- *                 no state survives between calls.
- * Calls on one workspace must not overlap on the GPU.
+ *                 its contents need no initialisation and no state survives
+ *                 between calls (the split-pair counters carry a tag unique to
+ *                 each launch, so whatever a word held before counts as zero).
+ * Calls on one workspace must not overlap on the GPU.  On the tensor-core path a
+ * call is one kernel launch for up to 4,096 sequences (every CTA plans its own
+ * warps from seq_lens); larger batches launch a plan kernel first.
  * bf16/f16 with d_head 64 or 128, and FP8 with d_head 128, with G <= 16 and B a
  * multiple of 16 run on the tensor-core path (TMA-staged tiles, mma.sync; groups
  * of 9 to 16 query heads as two 8-head column blocks); other geometries on CUDA
@@ -262,6 +266,26 @@ int pkv_step_launch_host(pkv_pool* pool, int32_t layer, int32_t n, int32_t W, co
                          void* v_pool, float scale, const int32_t* meta_host, int32_t* meta_dev, void* workspace,
                          size_t ws_bytes, pkv_event_t attn_begin, pkv_event_t attn_end, pkv_stream_t stream);
 
+/* The device half of a decode step with the step's inputs packed in one page-locked
+ * host buffer.  (The pages have no counterpart of this call; it is the step for callers
+ * whose inputs arrive in host memory, with the fewest copies per step.)  On the stream:
+ * ONE cudaMemcpyAsync of in_bytes from in_host to in_dev (device, same layout), then, if
+ * meta_host is not NULL, the metadata copy as in pkv_step_launch (NULL: the caller has
+ * already queued meta_dev's contents, e.g. right after pkv_step_plan, while the previous
+ * step ran), the shared-block copies, the append and the attention, and ONE copy of the
+ * n result rows from out_dev to out_host.
+ *   in_host / in_dev: q [n][H_q][d_head] at byte 0, k_new [n][H_kv][d_head] at off_k,
+ *                     v_new [n][H_kv][d_head] at off_v (activation type; offsets multiples
+ *                     of 16, each part before the next; in_bytes >= off_v + the v_new rows);
+ *   out_host [n][H_q][d_head] page-locked; out_dev device.
+ * Every other argument is as for pkv_step_launch.  Errors: INVALID_ARG for a layout that
+ * does not hold n rows; otherwise as pkv_step_launch. */
+int pkv_step_launch_packed(pkv_pool* pool, int32_t layer, int32_t n, int32_t W, const int32_t* cow_pairs,
+                           int32_t n_cow, const void* in_host, void* in_dev, size_t off_k, size_t off_v,
+                           size_t in_bytes, void* out_host, void* out_dev, void* k_pool, void* v_pool, float scale,
+                           const int32_t* meta_host, int32_t* meta_dev, void* workspace, size_t ws_bytes,
+                           pkv_event_t attn_begin, pkv_event_t attn_end, pkv_stream_t stream);
+
 /* pkv_decode_step with the step's inputs and result in HOST memory.  (The pages
  * have no counterpart of this call; it is the step for callers whose per-step
  * inputs arrive in, and whose result is read from, host memory.)  On the stream:
@@ -297,7 +321,7 @@ int pkv_decode_step_host(pkv_pool* pool, int32_t layer, const int32_t* seq_ids, 
  *   - A batch that needs more scratch than 24 MiB is rejected with
  *     PKV_ERR_INVALID_ARG (the partials of one persistent grid on a 152-SM GB300
  *     take about 10 MB for groups of up to 8 query heads and 20 MB for 9 to 16;
- *     each sequence adds 8 + 4 * H_kv bytes).
+ *     each sequence adds 8 bytes).
  *   - Every call on a device shares the one array and leaves its contents behind;
  *     nothing in it needs to start at zero.  Calls whose GPU work overlaps (two
  *     streams, or two threads) race on it: order them on one stream.

@@ -21,7 +21,7 @@ __all__ = [
     "pkv_seq_free", "pkv_seq_len", "pkv_plan_append", "pkv_export_tables", "pkv_refcounts", "pkv_free_list",
     "pkv_append_kv", "pkv_decode_workspace_size", "pkv_decode_attention", "pkv_decode_attention_noalloc",
     "pkv_decode_step", "pkv_decode_step_host", "pkv_step_plan", "pkv_step_launch", "pkv_step_launch_host",
-    "StepLauncher",
+    "StepLauncher", "PackedStepLauncher",
     "pkv_prefill_attention",
     "pkv_copy_blocks", "pkv_swap_out",
     "pkv_swap_in", "pkv_swap_in_layers", "pkv_seq_host_slots", "pkv_seq_residency", "TIER_HBM", "TIER_HOST", "TIER_RELOADING", "pkv_pool_set_swap_engine", "pkv_check_device_error", "pkv_launch_count",
@@ -116,6 +116,9 @@ def _L():
                                  ctypes.c_size_t, vp, vp, vp], ctypes.c_int),
             "pkv_step_launch_host": ([vp, i32, i32, i32, vp, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                       ctypes.c_float, vp, vp, vp, ctypes.c_size_t, vp, vp, vp], ctypes.c_int),
+            "pkv_step_launch_packed": ([vp, i32, i32, i32, vp, i32, vp, vp, ctypes.c_size_t, ctypes.c_size_t,
+                                        ctypes.c_size_t, vp, vp, vp, vp, ctypes.c_float, vp, vp, vp, ctypes.c_size_t,
+                                        vp, vp, vp], ctypes.c_int),
             "pkv_swap_out": ([vp, i32, vp, vp, vp, i64, P64, i32, P32, vp], ctypes.c_int),
             "pkv_swap_in": ([vp, i32, vp, i64, i32, vp, vp, P32, vp], ctypes.c_int),
             "pkv_seq_host_slots": ([vp, i32, P64, i32, P32], ctypes.c_int),
@@ -575,6 +578,57 @@ class StepLauncher:
                        _host_ptr(out_host, "out_host"), q, k, v, o, kp, vp, self._scale,
                        _host_ptr(meta_host, "meta_host"), _dev(meta_dev, "meta_dev"), self._ws[0], self._ws[1], ev0,
                        ev1, self._stream), "pkv_step_launch_host")
+
+
+class PackedStepLauncher:
+    """pkv_step_launch_packed with the buffers that stay the same from step to step bound once:
+    the device input staging `in_dev` (q, k_new, v_new at the offsets each call gives, one
+    copy per step), the device result rows `out_dev`, the pools, the scale, the workspace
+    and the stream (fixed at construction: torch's current stream then, when None).  Each call
+    takes the page-locked host input buffer of the step (q at byte 0, k_new at off_k, v_new at
+    off_v; `in_bytes` of it are copied), the host result buffer, the device metadata buffer
+    and, unless the caller already queued the metadata copy, the host metadata.  The launcher
+    holds references to the pool and every bound buffer."""
+
+    def __init__(self, pool: PoolLike, layer: int, in_dev, out_dev, k_pool, v_pool, scale: float, workspace,
+                 stream=None):
+        self._pool = pool
+        self._layer = int(layer)
+        g = pool.geometry if isinstance(pool, Pool) else pkv_pool_geometry(pool)
+        ab = {F32: 4, F16: 2, BF16: 2, E4M3: 2}[g.dtype]
+        self._row_q, self._row_k = ab * g.H_q * g.d_head, ab * g.H_kv * g.d_head
+        self._in_bytes = _nbytes(in_dev)
+        self._rows = _nbytes(out_dev) // self._row_q
+        self._dev = (_dev(in_dev, "in_dev"), _dev(out_dev, "out_dev"), _dev(k_pool, "k_pool"), _dev(v_pool, "v_pool"))
+        self._scale = float(scale)
+        self._ws = (_dev(workspace, "workspace"), workspace.numel() * workspace.element_size())
+        self._stream = _stream(stream)
+        self._f = _L().pkv_step_launch_packed
+        self._keep = (pool, in_dev, out_dev, k_pool, v_pool, workspace)
+
+    @property
+    def stream(self) -> int:
+        return self._stream
+
+    def __call__(self, n: int, W: int, cow_pairs, in_host, off_k: int, off_v: int, in_bytes: int, out_host, meta_dev,
+                 meta_host=None, attn_events=None) -> None:
+        if n > self._rows:
+            raise ValueError(f"n = {n} exceeds the {self._rows} rows of the bound out_dev")
+        mb = 4 * n * (W + 2)
+        _require_bytes((in_host, in_bytes, "in_host"), (out_host, n * self._row_q, "out_host"),
+                       (meta_dev, mb, "meta_dev"))
+        if in_bytes > self._in_bytes:
+            raise ValueError(f"in_bytes = {in_bytes} exceeds the {self._in_bytes} bytes of the bound in_dev")
+        if meta_host is not None:
+            _require_bytes((meta_host, mb, "meta_host"))
+        cp = _i32(cow_pairs).reshape(-1)
+        ev0, ev1 = _events(attn_events)
+        ind, outd, kp, vp = self._dev
+        _check(self._f(_h(self._pool), self._layer, n, W, _a(cp), cp.size // 2, _host_ptr(in_host, "in_host"), ind,
+                       int(off_k), int(off_v), int(in_bytes), _host_ptr(out_host, "out_host"), outd, kp, vp,
+                       self._scale, None if meta_host is None else _host_ptr(meta_host, "meta_host"),
+                       _dev(meta_dev, "meta_dev"), self._ws[0], self._ws[1], ev0, ev1, self._stream),
+               "pkv_step_launch_packed")
 
 
 def pkv_prefill_attention(pool: PoolLike, layer: int, q, q_offsets, max_q: int, k_pool, v_pool, block_tables,

@@ -717,22 +717,24 @@ int pkv_step_plan(pkv_pool* pool, const int32_t* seq_ids, int32_t n, int32_t W, 
   return pkv_export_tables(pool, seq_ids, n, tables, W, lens);
 }
 
-int pkv_step_launch(pkv_pool* pool, int32_t layer, int32_t n, int32_t W, const int32_t* cow_pairs, int32_t n_cow,
-                    const void* q, const void* k_new, const void* v_new, void* k_pool, void* v_pool, float scale,
-                    void* out, const int32_t* meta_host, int32_t* meta_dev, void* workspace, size_t ws_bytes,
-                    pkv_event_t attn_begin, pkv_event_t attn_end, pkv_stream_t stream) {
-  pkv::clear_error();
-  if (!pool || n < 0 || W <= 0 || n_cow < 0) return fail(PKV_ERR_INVALID_ARG, "bad arguments to pkv_step_launch");
+// The device half of a decode step; meta_host NULL: meta_dev already holds the plan.
+static int step_launch(pkv_pool* pool, int32_t layer, int32_t n, int32_t W, const int32_t* cow_pairs, int32_t n_cow,
+                       const void* q, const void* k_new, const void* v_new, void* k_pool, void* v_pool, float scale,
+                       void* out, const int32_t* meta_host, int32_t* meta_dev, void* workspace, size_t ws_bytes,
+                       pkv_event_t attn_begin, pkv_event_t attn_end, pkv_stream_t stream) {
+  if (!pool || n < 0 || W <= 0 || n_cow < 0) return fail(PKV_ERR_INVALID_ARG, "bad arguments to the step launch");
   if (n == 0) return PKV_OK;
-  if (!q || !k_new || !v_new || !k_pool || !v_pool || !out || !meta_host || !meta_dev || !workspace ||
-      (n_cow > 0 && !cow_pairs))
+  if (!q || !k_new || !v_new || !k_pool || !v_pool || !out || !meta_dev || !workspace || (n_cow > 0 && !cow_pairs))
     return fail(PKV_ERR_INVALID_ARG, "NULL buffer");
   if (layer < 0 || layer >= as_pool(pool)->geo.L) return fail(PKV_ERR_INVALID_ARG, "layer out of range");
   if (int rc = step_workspace_check(pool, n, ws_bytes)) return rc;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  const size_t meta_bytes = sizeof(int32_t) * static_cast<size_t>(n) * (W + 2);
-  cudaError_t e = cudaMemcpyAsync(meta_dev, meta_host, meta_bytes, cudaMemcpyHostToDevice, st);
-  if (e != cudaSuccess) return fail(PKV_ERR_CUDA, std::string("cudaMemcpyAsync (step metadata): ") + cudaGetErrorString(e));
+  if (meta_host) {
+    const size_t meta_bytes = sizeof(int32_t) * static_cast<size_t>(n) * (W + 2);
+    cudaError_t e = cudaMemcpyAsync(meta_dev, meta_host, meta_bytes, cudaMemcpyHostToDevice, st);
+    if (e != cudaSuccess)
+      return fail(PKV_ERR_CUDA, std::string("cudaMemcpyAsync (step metadata): ") + cudaGetErrorString(e));
+  }
   if (n_cow > 0)
     if (int rc = pkv_copy_blocks(pool, cow_pairs, n_cow, k_pool, v_pool, stream)) return rc;
   // append and attention in one launch on the tensor-core path (the kernel writes each new
@@ -744,6 +746,44 @@ int pkv_step_launch(pkv_pool* pool, int32_t layer, int32_t n, int32_t W, const i
                                   stream, &fuse))
     return rc;
   if (attn_end) cudaEventRecord(reinterpret_cast<cudaEvent_t>(attn_end), st);
+  return PKV_OK;
+}
+
+int pkv_step_launch(pkv_pool* pool, int32_t layer, int32_t n, int32_t W, const int32_t* cow_pairs, int32_t n_cow,
+                    const void* q, const void* k_new, const void* v_new, void* k_pool, void* v_pool, float scale,
+                    void* out, const int32_t* meta_host, int32_t* meta_dev, void* workspace, size_t ws_bytes,
+                    pkv_event_t attn_begin, pkv_event_t attn_end, pkv_stream_t stream) {
+  pkv::clear_error();
+  if (n > 0 && !meta_host) return fail(PKV_ERR_INVALID_ARG, "NULL buffer");
+  return step_launch(pool, layer, n, W, cow_pairs, n_cow, q, k_new, v_new, k_pool, v_pool, scale, out, meta_host,
+                     meta_dev, workspace, ws_bytes, attn_begin, attn_end, stream);
+}
+
+int pkv_step_launch_packed(pkv_pool* pool, int32_t layer, int32_t n, int32_t W, const int32_t* cow_pairs,
+                           int32_t n_cow, const void* in_host, void* in_dev, size_t off_k, size_t off_v,
+                           size_t in_bytes, void* out_host, void* out_dev, void* k_pool, void* v_pool, float scale,
+                           const int32_t* meta_host, int32_t* meta_dev, void* workspace, size_t ws_bytes,
+                           pkv_event_t attn_begin, pkv_event_t attn_end, pkv_stream_t stream) {
+  pkv::clear_error();
+  if (!pool || n < 0 || W <= 0) return fail(PKV_ERR_INVALID_ARG, "bad arguments to pkv_step_launch_packed");
+  if (n == 0) return PKV_OK;
+  if (!in_host || !in_dev || !out_host || !out_dev) return fail(PKV_ERR_INVALID_ARG, "NULL buffer");
+  const pkv_geometry& g = as_pool(pool)->geo;
+  const size_t ab = static_cast<size_t>(pkv::act_size(g.dtype));
+  const size_t qb = ab * n * g.H_q * g.d_head, kb = ab * n * g.H_kv * g.d_head;
+  if ((off_k | off_v) & 15) return fail(PKV_ERR_INVALID_ARG, "off_k and off_v must be multiples of 16");
+  if (off_k < qb || off_v < off_k + kb || in_bytes < off_v + kb)
+    return fail(PKV_ERR_INVALID_ARG, "packed input: q, k_new and v_new of n rows must fit before off_k, before "
+                                     "off_v and before in_bytes");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(in_dev, in_host, in_bytes, cudaMemcpyHostToDevice, st);
+  if (e != cudaSuccess) return fail(PKV_ERR_CUDA, std::string("cudaMemcpyAsync (step input): ") + cudaGetErrorString(e));
+  char* d = static_cast<char*>(in_dev);
+  if (int rc = step_launch(pool, layer, n, W, cow_pairs, n_cow, d, d + off_k, d + off_v, k_pool, v_pool, scale,
+                           out_dev, meta_host, meta_dev, workspace, ws_bytes, attn_begin, attn_end, stream))
+    return rc;
+  e = cudaMemcpyAsync(out_host, out_dev, qb, cudaMemcpyDeviceToHost, st);
+  if (e != cudaSuccess) return fail(PKV_ERR_CUDA, std::string("cudaMemcpyAsync (step result): ") + cudaGetErrorString(e));
   return PKV_OK;
 }
 

@@ -413,11 +413,13 @@ __global__ void __launch_bounds__(NW * 32) decode_tc_kernel(const __grid_constan
   const uint32_t bar0 = smem_u32(region + S * C::STAGE_BYTES + 64 * 16);
   const uint32_t stage0 = smem_u32(region);
 
-  if (lane == 0) {
-    for (int st = 0; st < S; ++st) mbar_init(bar0 + 8 * st, 1);
-    fence_barrier_init();
-  }
-  __syncwarp();
+  auto init_barriers = [&] {
+    if (lane == 0) {
+      for (int st = 0; st < S; ++st) mbar_init(bar0 + 8 * st, 1);
+      fence_barrier_init();
+    }
+    __syncwarp();
+  };
 
   // ---- this warp's range of the batch's tiles and its first tile: planned here by every CTA
   // (small batches), or read from the plan kernel, which this kernel then follows as a
@@ -431,10 +433,12 @@ __global__ void __launch_bounds__(NW * 32) decode_tc_kernel(const __grid_constan
   int4 w0;
   if (a.self_plan) {
     self_plan<NW>(a, s_start, s_q, &s_total);
+    init_barriers();  // after the plan's loads, which need no barrier
     total = s_total;
     w0 = s_start[warp];
     cq = s_q[warp];
   } else {
+    init_barriers();  // while the plan kernel runs
     asm volatile("griddepcontrol.wait;" ::: "memory");
     total = a.hdr[0];
     w0 = a.wstart[gw];
@@ -785,32 +789,35 @@ __global__ void __launch_bounds__(NW * 32) decode_tc_kernel(const __grid_constan
   // no arrival.
   if (pend_pair >= 0 || end_pair >= 0) {
     __syncwarp();
-    if (lane == 0) __threadfence();
-    auto arrive = [&](int pair, int pbeg, int nt) {
-      const int s = pair / a.H_kv, g = pair - (pair / a.H_kv) * a.H_kv;
+    if (lane < 2) __threadfence();
+    // lane 0 counts the pair that ended inside the range, lane 1 the one at its end, at once
+    const int pair = lane == 0 ? pend_pair : end_pair;
+    const int pbeg = lane == 0 ? pend_pbeg : end_pbeg, nt = lane == 0 ? pend_nt : end_nt;
+    int last = 0;
+    if (lane < 2 && pair >= 0) {
       const int wa = pbeg / R, wb = (pbeg + nt - 1) / R;
-      int arrived = 0;
-      if (lane == 0) {
-        unsigned long long* c = a.counters + wa;
-        unsigned long long cur = *reinterpret_cast<volatile unsigned long long*>(c);
-        for (;;) {
-          const bool ours = (cur >> 16) == a.epoch;
-          const unsigned long long prev = atomicCAS(c, cur, ours ? cur + 1 : ((a.epoch << 16) | 1ull));
-          if (prev == cur) {
-            arrived = ours ? static_cast<int>(cur & 0xffffull) : 0;
-            break;
-          }
-          cur = prev;
+      unsigned long long* c = a.counters + wa;
+      unsigned long long cur = *reinterpret_cast<volatile unsigned long long*>(c);
+      for (;;) {
+        const bool ours = (cur >> 16) == a.epoch;
+        const unsigned long long prev = atomicCAS(c, cur, ours ? cur + 1 : ((a.epoch << 16) | 1ull));
+        if (prev == cur) {
+          last = (ours ? static_cast<int>(cur & 0xffffull) : 0) == wb - wa;
+          break;
         }
+        cur = prev;
       }
-      arrived = __shfl_sync(0xffffffffu, arrived, 0);
-      if (arrived == wb - wa) {
-        __threadfence();
-        merge_pair<TA, D, F8, NB>(a, s, g, pbeg, wa, wb, R, lane);
-      }
-    };
-    if (pend_pair >= 0) arrive(pend_pair, pend_pbeg, pend_nt);
-    if (end_pair >= 0) arrive(end_pair, end_pbeg, end_nt);
+    }
+    const unsigned lasts = __ballot_sync(0xffffffffu, last);
+    if (lasts) __threadfence();
+#pragma unroll 1
+    for (int k = 0; k < 2; ++k) {
+      if (!(lasts & (1u << k))) continue;
+      const int p = k == 0 ? pend_pair : end_pair;
+      const int pb = k == 0 ? pend_pbeg : end_pbeg, n_t = k == 0 ? pend_nt : end_nt;
+      const int s = p / a.H_kv, g = p - (p / a.H_kv) * a.H_kv;
+      merge_pair<TA, D, F8, NB>(a, s, g, pb, pb / R, (pb + n_t - 1) / R, R, lane);
+    }
   }
 }
 

@@ -117,12 +117,14 @@ def test_decode_step_host_buffers_match_oracle(dtype):
     b.check_pools_bitexact()
 
 
-@pytest.mark.parametrize("dtype,api", [("bf16", "function"), ("e4m3", "function"), ("bf16", "launcher")])
+@pytest.mark.parametrize("dtype,api", [("bf16", "function"), ("e4m3", "function"), ("bf16", "launcher"),
+                                       ("bf16", "packed"), ("e4m3", "packed_early_meta")])
 def test_step_plan_ahead_then_launch_host_match_oracle(dtype, api):
-    """pkv_step_plan of step t + 1 runs while step t (pkv_step_launch_host, or a StepLauncher
-    with the fixed buffers bound once) is on the GPU, as a serving loop's scheduler would; every
-    step's result matches the oracle and the pools and control-plane state stay identical to the
-    oracle's."""
+    """pkv_step_plan of step t + 1 runs while step t (pkv_step_launch_host, a StepLauncher with
+    the fixed buffers bound once, or a PackedStepLauncher: one packed input copy, the metadata
+    copied by the call or queued by the caller right after the plan) is on the GPU, as a serving
+    loop's scheduler would; every step's result matches the oracle and the pools and
+    control-plane state stay identical to the oracle's."""
     import torch
 
     g = W.Geometry(L=1, H_q=64, H_kv=8, d_head=128, block_size=16, dtype=dtype, num_blocks=256)
@@ -145,6 +147,11 @@ def test_step_plan_ahead_then_launch_host_match_oracle(dtype, api):
     pin = lambda x: torch.from_numpy(x.copy()).pin_memory().view(torch.bfloat16)
     plans = {}
     launcher = pkv.StepLauncher(b.lib, 0, q_dev, k_dev, v_dev, o_dev, b.kp, b.vp, scale, ws)
+    rq, rk = g.H_q * g.d_head * 2, g.H_kv * g.d_head * 2
+    off_k, off_v = n * rq + 48, n * rq + 48 + n * rk + 16  # any 16-byte multiples that keep the parts apart
+    in_bytes = off_v + n * rk
+    in_dev = torch.empty(in_bytes + 64, dtype=torch.uint8, device="cuda")
+    packed = pkv.PackedStepLauncher(b.lib, 0, in_dev, o_dev, b.kp, b.vp, scale, ws)
 
     def plan(t):
         m = metas[t % 2]
@@ -163,6 +170,15 @@ def test_step_plan_ahead_then_launch_host_match_oracle(dtype, api):
         out_host.fill_(float("nan"))
         if api == "launcher":
             launcher(n, Wd, cows, pin(q), pin(kn), pin(vn), out_host, metas[t % 2], mdev[t % 2])
+        elif api.startswith("packed"):
+            in_host = torch.zeros(in_bytes, dtype=torch.uint8).pin_memory()
+            for x, o in ((q, 0), (kn, off_k), (vn, off_v)):
+                in_host[o:o + x.nbytes].copy_(torch.from_numpy(x.reshape(-1).view(np.uint8)))
+            if api == "packed_early_meta":
+                mdev[t % 2].copy_(metas[t % 2], non_blocking=True)
+                packed(n, Wd, cows, in_host, off_k, off_v, in_bytes, out_host, mdev[t % 2])
+            else:
+                packed(n, Wd, cows, in_host, off_k, off_v, in_bytes, out_host, mdev[t % 2], meta_host=metas[t % 2])
         else:
             pkv.pkv_step_launch_host(b.lib, 0, n, Wd, cows, pin(q), pin(kn), pin(vn), out_host, q_dev, k_dev, v_dev,
                                      o_dev, b.kp, b.vp, scale, metas[t % 2], mdev[t % 2], ws)

@@ -64,7 +64,7 @@ def test_noalloc_rejects_a_batch_beyond_its_scratch():
 
     g = W.Geometry(L=1, H_q=64, H_kv=8, d_head=128, block_size=16, dtype="bf16", num_blocks=64)
     lib = pkv.pkv_pool_create(g.L, g.H_q, g.H_kv, g.d_head, g.block_size, g.dtype, g.num_blocks)
-    n = 2_000_000  # 8 + 4 * H_kv bytes of scratch per sequence on top of the partials: beyond 24 MiB
+    n = 2_000_000  # 8 bytes of scratch per sequence on top of ~10 MB of partials: beyond 24 MiB
     lens = torch.zeros(n, dtype=torch.int32, device="cuda")
     tables = torch.zeros((n, 1), dtype=torch.int32, device="cuda")
     pool_k = torch.zeros(g.pool_shape(), dtype=torch.bfloat16, device="cuda")
