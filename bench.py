@@ -370,32 +370,32 @@ class DecodeRunner:
         host memory and its result is read on the host before the next step's inputs are
         sent.  The host half of step t + 1 (pkv_step_plan: slots, tables, CoW pairs -- it needs
         no result of step t) runs while step t is on the GPU, as a serving loop's scheduler
-        does; the device half (pkv_step_launch_packed through a PackedStepLauncher, which binds
-        the buffers that stay the same from step to step) copies the step's packed inputs and
-        its metadata in, runs the step and copies the result out."""
+        does, and writes its metadata into step t + 1's packed input buffer; the device half
+        (pkv_step_launch_packed through a PackedStepLauncher, which binds the buffers that stay
+        the same from step to step) copies the packed inputs and metadata in with one copy,
+        runs the step and copies the result out."""
         torch, pkv, g = self.torch, self.pkv, self.g
-        rk = g.H_kv * g.d_head * self.act_bytes
+        mrow = self.Wd + 2
 
         def plan(t):
             ids = self.running(t)
             if len(ids) == 0:
                 return None
-            k, hnp, hbuf, dmeta = self.staging.next()
-            cows = pkv.pkv_step_plan(self.pool, ids, self.Wd, hbuf)
-            return ids, self.pool, k, hnp, hbuf, dmeta, cows
+            mview = host[t, self.off_meta:self.off_meta + 4 * len(ids) * mrow].view(torch.int32)
+            cows = pkv.pkv_step_plan(self.pool, ids, self.Wd, mview)
+            return ids, self.pool, mview, cows
 
         nxt = plan(t0)
         for i in range(steps):
             t = t0 + i
             cur, nxt = nxt, None
             if cur is not None:
-                ids, pool, k, hnp, hbuf, dmeta, cows = cur
+                ids, pool, mview, cows = cur
                 n = len(ids)
-                in_bytes = self.off_v + n * rk
+                in_bytes = self.off_meta + 4 * n * mrow
                 self.launcher_for(pool)(n, self.Wd, cows, host[t], self.off_k, self.off_v, in_bytes, self.out_host,
-                                        dmeta, meta_host=hbuf, attn_events=events[i] if events else None)
+                                        off_meta=self.off_meta, attn_events=events[i] if events else None)
                 self.flush_l2(t)
-                nbytes = self.staging.mark(k, n * (self.Wd + 2))
                 self.pool = pool
                 self.after_step(t, ids)
             if i + 1 < steps:
@@ -407,14 +407,13 @@ class DecodeRunner:
             if timed:
                 if events:
                     self.decode_ms.append(events[i])
-                lens = hnp[n + n * self.Wd:n + n * self.Wd + n]
+                lens = mview.numpy()[n + n * self.Wd:n + n * self.Wd + n]
                 kvb = int(lens.sum(dtype=np.int64)) * g.H_kv * g.d_head * g.elem_bytes * 2
                 self.kv_bytes.append(kvb)
                 self.alg_bytes.append(kvb + 2 * n * g.H_q * g.d_head * self.act_bytes + n * self.Wd * 4 + n * 4 +
                                       2 * n * g.H_kv * g.d_head * (self.act_bytes + g.elem_bytes))
                 self.tokens.append(n)
-                self.h2d_meta += nbytes
-            self.e2e_in_bytes += nbytes + in_bytes
+            self.e2e_in_bytes += in_bytes
             self.e2e_out_bytes += n * g.H_q * g.d_head * self.act_bytes
 
     def launcher_for(self, pool):
@@ -440,18 +439,20 @@ class DecodeRunner:
         pass
 
     def prepare_e2e(self):
-        """Each step's inputs packed in one pinned host buffer, q (n_max rows), then k_new and
-        v_new (n_max rows each); a step of n sequences copies q's and k_new's n_max rows and
-        v_new's first n (the layout does not depend on n)."""
+        """Each step's inputs packed in one pinned host buffer: q, k_new and v_new (n_max rows
+        each), then the step's metadata, which pkv_step_plan writes there; a step of n
+        sequences copies the three input parts whole and the metadata of its n rows (the layout
+        does not depend on n)."""
         torch, g = self.torch, self.g
         n = self.n_max
         rq, rk = g.H_q * g.d_head * self.act_bytes, g.H_kv * g.d_head * self.act_bytes
         self.off_k, self.off_v = n * rq, n * (rq + rk)
-        step_bytes = n * (rq + 2 * rk)
+        self.off_meta = n * (rq + 2 * rk)
+        step_bytes = self.off_meta + 4 * n * (self.Wd + 2)
         host = torch.empty((self.total_steps, step_bytes), dtype=torch.uint8, pin_memory=True)
         for t in range(self.total_steps):
             for src, o0, o1 in ((self.q, 0, self.off_k), (self.kn, self.off_k, self.off_v),
-                                (self.vn, self.off_v, step_bytes)):
+                                (self.vn, self.off_v, self.off_meta)):
                 host[t, o0:o1].view(self.td).copy_(src[t].reshape(-1))
         self.in_e2e = torch.empty(step_bytes, dtype=torch.uint8, device=self.dev)
         self.out_host = torch.empty(self.out.shape, dtype=self.td, pin_memory=True)

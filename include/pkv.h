@@ -269,22 +269,25 @@ int pkv_step_launch_host(pkv_pool* pool, int32_t layer, int32_t n, int32_t W, co
 /* The device half of a decode step with the step's inputs packed in one page-locked
  * host buffer.  (The pages have no counterpart of this call; it is the step for callers
  * whose inputs arrive in host memory, with the fewest copies per step.)  On the stream:
- * ONE cudaMemcpyAsync of in_bytes from in_host to in_dev (device, same layout), then, if
- * meta_host is not NULL, the metadata copy as in pkv_step_launch (NULL: the caller has
- * already queued meta_dev's contents, e.g. right after pkv_step_plan, while the previous
- * step ran), the shared-block copies, the append and the attention, and ONE copy of the
- * n result rows from out_dev to out_host.
+ * ONE cudaMemcpyAsync of in_bytes from in_host to in_dev (device, same layout), the
+ * metadata copy if the metadata is elsewhere (see below), the shared-block copies, the
+ * append and the attention, and ONE copy of the n result rows from out_dev to out_host.
  *   in_host / in_dev: q [n][H_q][d_head] at byte 0, k_new [n][H_kv][d_head] at off_k,
- *                     v_new [n][H_kv][d_head] at off_v (activation type; offsets multiples
- *                     of 16, each part before the next; in_bytes >= off_v + the v_new rows);
+ *                     v_new [n][H_kv][d_head] at off_v (activation type), and, when off_meta
+ *                     is not 0, the step's metadata [n * (W + 2)] int32 at off_meta (where
+ *                     pkv_step_plan wrote it into in_host; meta_host and meta_dev are then
+ *                     ignored and may be NULL).  Offsets are multiples of 16, each part
+ *                     before the next, in_bytes covers the last part.
+ *   off_meta 0: meta_host as in pkv_step_launch (copied to meta_dev by the call), or NULL
+ *               when the caller has already queued meta_dev's contents on the stream.
  *   out_host [n][H_q][d_head] page-locked; out_dev device.
  * Every other argument is as for pkv_step_launch.  Errors: INVALID_ARG for a layout that
  * does not hold n rows; otherwise as pkv_step_launch. */
 int pkv_step_launch_packed(pkv_pool* pool, int32_t layer, int32_t n, int32_t W, const int32_t* cow_pairs,
                            int32_t n_cow, const void* in_host, void* in_dev, size_t off_k, size_t off_v,
-                           size_t in_bytes, void* out_host, void* out_dev, void* k_pool, void* v_pool, float scale,
-                           const int32_t* meta_host, int32_t* meta_dev, void* workspace, size_t ws_bytes,
-                           pkv_event_t attn_begin, pkv_event_t attn_end, pkv_stream_t stream);
+                           size_t off_meta, size_t in_bytes, void* out_host, void* out_dev, void* k_pool,
+                           void* v_pool, float scale, const int32_t* meta_host, int32_t* meta_dev, void* workspace,
+                           size_t ws_bytes, pkv_event_t attn_begin, pkv_event_t attn_end, pkv_stream_t stream);
 
 /* pkv_decode_step with the step's inputs and result in HOST memory.  (The pages
  * have no counterpart of this call; it is the step for callers whose per-step

@@ -117,8 +117,8 @@ def _L():
             "pkv_step_launch_host": ([vp, i32, i32, i32, vp, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                       ctypes.c_float, vp, vp, vp, ctypes.c_size_t, vp, vp, vp], ctypes.c_int),
             "pkv_step_launch_packed": ([vp, i32, i32, i32, vp, i32, vp, vp, ctypes.c_size_t, ctypes.c_size_t,
-                                        ctypes.c_size_t, vp, vp, vp, vp, ctypes.c_float, vp, vp, vp, ctypes.c_size_t,
-                                        vp, vp, vp], ctypes.c_int),
+                                        ctypes.c_size_t, ctypes.c_size_t, vp, vp, vp, vp, ctypes.c_float, vp, vp, vp,
+                                        ctypes.c_size_t, vp, vp, vp], ctypes.c_int),
             "pkv_swap_out": ([vp, i32, vp, vp, vp, i64, P64, i32, P32, vp], ctypes.c_int),
             "pkv_swap_in": ([vp, i32, vp, i64, i32, vp, vp, P32, vp], ctypes.c_int),
             "pkv_seq_host_slots": ([vp, i32, P64, i32, P32], ctypes.c_int),
@@ -610,25 +610,32 @@ class PackedStepLauncher:
     def stream(self) -> int:
         return self._stream
 
-    def __call__(self, n: int, W: int, cow_pairs, in_host, off_k: int, off_v: int, in_bytes: int, out_host, meta_dev,
-                 meta_host=None, attn_events=None) -> None:
+    def __call__(self, n: int, W: int, cow_pairs, in_host, off_k: int, off_v: int, in_bytes: int, out_host,
+                 meta_dev=None, meta_host=None, off_meta: int = 0, attn_events=None) -> None:
+        """One step; the metadata is either packed in in_host at off_meta (written there by
+        pkv_step_plan; meta_dev and meta_host unused), or copied from meta_host to meta_dev by
+        the call, or (meta_host None) already queued into meta_dev by the caller."""
         if n > self._rows:
             raise ValueError(f"n = {n} exceeds the {self._rows} rows of the bound out_dev")
         mb = 4 * n * (W + 2)
-        _require_bytes((in_host, in_bytes, "in_host"), (out_host, n * self._row_q, "out_host"),
-                       (meta_dev, mb, "meta_dev"))
+        _require_bytes((in_host, in_bytes, "in_host"), (out_host, n * self._row_q, "out_host"))
         if in_bytes > self._in_bytes:
             raise ValueError(f"in_bytes = {in_bytes} exceeds the {self._in_bytes} bytes of the bound in_dev")
-        if meta_host is not None:
-            _require_bytes((meta_host, mb, "meta_host"))
+        if not off_meta:
+            if meta_dev is None:
+                raise ValueError("meta_dev is needed unless the metadata is packed (off_meta)")
+            _require_bytes((meta_dev, mb, "meta_dev"))
+            if meta_host is not None:
+                _require_bytes((meta_host, mb, "meta_host"))
         cp = _i32(cow_pairs).reshape(-1)
         ev0, ev1 = _events(attn_events)
         ind, outd, kp, vp = self._dev
         _check(self._f(_h(self._pool), self._layer, n, W, _a(cp), cp.size // 2, _host_ptr(in_host, "in_host"), ind,
-                       int(off_k), int(off_v), int(in_bytes), _host_ptr(out_host, "out_host"), outd, kp, vp,
-                       self._scale, None if meta_host is None else _host_ptr(meta_host, "meta_host"),
-                       _dev(meta_dev, "meta_dev"), self._ws[0], self._ws[1], ev0, ev1, self._stream),
-               "pkv_step_launch_packed")
+                       int(off_k), int(off_v), int(off_meta), int(in_bytes), _host_ptr(out_host, "out_host"), outd,
+                       kp, vp, self._scale,
+                       None if (off_meta or meta_host is None) else _host_ptr(meta_host, "meta_host"),
+                       None if off_meta else _dev(meta_dev, "meta_dev"), self._ws[0], self._ws[1], ev0, ev1,
+                       self._stream), "pkv_step_launch_packed")
 
 
 def pkv_prefill_attention(pool: PoolLike, layer: int, q, q_offsets, max_q: int, k_pool, v_pool, block_tables,

@@ -761,9 +761,9 @@ int pkv_step_launch(pkv_pool* pool, int32_t layer, int32_t n, int32_t W, const i
 
 int pkv_step_launch_packed(pkv_pool* pool, int32_t layer, int32_t n, int32_t W, const int32_t* cow_pairs,
                            int32_t n_cow, const void* in_host, void* in_dev, size_t off_k, size_t off_v,
-                           size_t in_bytes, void* out_host, void* out_dev, void* k_pool, void* v_pool, float scale,
-                           const int32_t* meta_host, int32_t* meta_dev, void* workspace, size_t ws_bytes,
-                           pkv_event_t attn_begin, pkv_event_t attn_end, pkv_stream_t stream) {
+                           size_t off_meta, size_t in_bytes, void* out_host, void* out_dev, void* k_pool,
+                           void* v_pool, float scale, const int32_t* meta_host, int32_t* meta_dev, void* workspace,
+                           size_t ws_bytes, pkv_event_t attn_begin, pkv_event_t attn_end, pkv_stream_t stream) {
   pkv::clear_error();
   if (!pool || n < 0 || W <= 0) return fail(PKV_ERR_INVALID_ARG, "bad arguments to pkv_step_launch_packed");
   if (n == 0) return PKV_OK;
@@ -771,10 +771,16 @@ int pkv_step_launch_packed(pkv_pool* pool, int32_t layer, int32_t n, int32_t W, 
   const pkv_geometry& g = as_pool(pool)->geo;
   const size_t ab = static_cast<size_t>(pkv::act_size(g.dtype));
   const size_t qb = ab * n * g.H_q * g.d_head, kb = ab * n * g.H_kv * g.d_head;
-  if ((off_k | off_v) & 15) return fail(PKV_ERR_INVALID_ARG, "off_k and off_v must be multiples of 16");
-  if (off_k < qb || off_v < off_k + kb || in_bytes < off_v + kb)
-    return fail(PKV_ERR_INVALID_ARG, "packed input: q, k_new and v_new of n rows must fit before off_k, before "
-                                     "off_v and before in_bytes");
+  const size_t mb = sizeof(int32_t) * static_cast<size_t>(n) * (W + 2);
+  if ((off_k | off_v | off_meta) & 15) return fail(PKV_ERR_INVALID_ARG, "offsets must be multiples of 16");
+  if (off_k < qb || off_v < off_k + kb || in_bytes < off_v + kb || (off_meta && (off_meta < off_v + kb ||
+                                                                                 in_bytes < off_meta + mb)))
+    return fail(PKV_ERR_INVALID_ARG, "packed input: q, k_new, v_new (and the metadata) of n rows must fit before "
+                                     "off_k, off_v, off_meta and in_bytes");
+  if (off_meta) {  // the metadata travels with the inputs
+    meta_host = nullptr;
+    meta_dev = reinterpret_cast<int32_t*>(static_cast<char*>(in_dev) + off_meta);
+  }
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = cudaMemcpyAsync(in_dev, in_host, in_bytes, cudaMemcpyHostToDevice, st);
   if (e != cudaSuccess) return fail(PKV_ERR_CUDA, std::string("cudaMemcpyAsync (step input): ") + cudaGetErrorString(e));

@@ -118,7 +118,8 @@ def test_decode_step_host_buffers_match_oracle(dtype):
 
 
 @pytest.mark.parametrize("dtype,api", [("bf16", "function"), ("e4m3", "function"), ("bf16", "launcher"),
-                                       ("bf16", "packed"), ("e4m3", "packed_early_meta")])
+                                       ("bf16", "packed"), ("e4m3", "packed_early_meta"),
+                                       ("bf16", "packed_meta_inside")])
 def test_step_plan_ahead_then_launch_host_match_oracle(dtype, api):
     """pkv_step_plan of step t + 1 runs while step t (pkv_step_launch_host, a StepLauncher with
     the fixed buffers bound once, or a PackedStepLauncher: one packed input copy, the metadata
@@ -150,7 +151,8 @@ def test_step_plan_ahead_then_launch_host_match_oracle(dtype, api):
     rq, rk = g.H_q * g.d_head * 2, g.H_kv * g.d_head * 2
     off_k, off_v = n * rq + 48, n * rq + 48 + n * rk + 16  # any 16-byte multiples that keep the parts apart
     in_bytes = off_v + n * rk
-    in_dev = torch.empty(in_bytes + 64, dtype=torch.uint8, device="cuda")
+    off_meta = in_bytes + 32  # the metadata packed after the inputs (the "packed_meta_inside" calls)
+    in_dev = torch.empty(off_meta + 4 * n * (Wd + 2) + 64, dtype=torch.uint8, device="cuda")
     packed = pkv.PackedStepLauncher(b.lib, 0, in_dev, o_dev, b.kp, b.vp, scale, ws)
 
     def plan(t):
@@ -171,10 +173,13 @@ def test_step_plan_ahead_then_launch_host_match_oracle(dtype, api):
         if api == "launcher":
             launcher(n, Wd, cows, pin(q), pin(kn), pin(vn), out_host, metas[t % 2], mdev[t % 2])
         elif api.startswith("packed"):
-            in_host = torch.zeros(in_bytes, dtype=torch.uint8).pin_memory()
+            in_host = torch.zeros(off_meta + 4 * n * (Wd + 2), dtype=torch.uint8).pin_memory()
             for x, o in ((q, 0), (kn, off_k), (vn, off_v)):
                 in_host[o:o + x.nbytes].copy_(torch.from_numpy(x.reshape(-1).view(np.uint8)))
-            if api == "packed_early_meta":
+            if api == "packed_meta_inside":
+                in_host[off_meta:].view(torch.int32).copy_(metas[t % 2][:n * (Wd + 2)])
+                packed(n, Wd, cows, in_host, off_k, off_v, off_meta + 4 * n * (Wd + 2), out_host, off_meta=off_meta)
+            elif api == "packed_early_meta":
                 mdev[t % 2].copy_(metas[t % 2], non_blocking=True)
                 packed(n, Wd, cows, in_host, off_k, off_v, in_bytes, out_host, mdev[t % 2])
             else:
