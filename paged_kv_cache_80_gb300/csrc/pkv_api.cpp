@@ -123,6 +123,15 @@ void* device_view_of_host(void* host) {
   return nullptr;
 }
 
+// CTAs of the SM copier for swaps: 32 keep the host link at its copy rate (out 188 / in 205 GB/s,
+// as with one CTA per 128 KiB of every image) and leave the other SMs to whatever runs beside the
+// swap (a reload behind decode: 86 % hidden instead of 75 %).  PKV_SWAP_CTAS overrides it for tuning
+// (0: one CTA per 128 KiB).
+int swap_ctas() {
+  if (const char* e = std::getenv("PKV_SWAP_CTAS")) return std::max(0, std::atoi(e));
+  return 32;
+}
+
 // Copy n images of `bytes` with the copy engines.
 int copy_engine(const void* src_base, void* dst_base, const pkv::CopyItem* items, int64_t n, int64_t bytes,
                 cudaStream_t s) {
@@ -512,10 +521,11 @@ int pkv_swap_out(pkv_pool* pool, int32_t seq, const void* k_pool, const void* v_
       vit[j] = {s->table[j] * P.block_bytes, frame + P.block_bytes};
     }
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    int rc = P.swap_engine == 0 ? pkv::launch_copy_images(k_pool, dhost, kit.data(), n, P.block_bytes, st)
+    const int ctas = swap_ctas();
+    int rc = P.swap_engine == 0 ? pkv::launch_copy_images(k_pool, dhost, kit.data(), n, P.block_bytes, st, ctas)
                                 : copy_engine(k_pool, dhost, kit.data(), n, P.block_bytes, st);
     if (rc == PKV_OK)
-      rc = P.swap_engine == 0 ? pkv::launch_copy_images(v_pool, dhost, vit.data(), n, P.block_bytes, st)
+      rc = P.swap_engine == 0 ? pkv::launch_copy_images(v_pool, dhost, vit.data(), n, P.block_bytes, st, ctas)
                               : copy_engine(v_pool, dhost, vit.data(), n, P.block_bytes, st);
     if (rc != PKV_OK) return rc;
   }
@@ -557,10 +567,11 @@ int pkv_swap_in(pkv_pool* pool, int32_t seq, const void* host, int64_t host_fram
       vit[j] = {frame + P.block_bytes, blk};
     }
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    int rc = P.swap_engine == 0 ? pkv::launch_copy_images(dhost, k_pool, kit.data(), n, P.block_bytes, st)
+    const int ctas = swap_ctas();
+    int rc = P.swap_engine == 0 ? pkv::launch_copy_images(dhost, k_pool, kit.data(), n, P.block_bytes, st, ctas)
                                 : copy_engine(dhost, k_pool, kit.data(), n, P.block_bytes, st);
     if (rc == PKV_OK)
-      rc = P.swap_engine == 0 ? pkv::launch_copy_images(dhost, v_pool, vit.data(), n, P.block_bytes, st)
+      rc = P.swap_engine == 0 ? pkv::launch_copy_images(dhost, v_pool, vit.data(), n, P.block_bytes, st, ctas)
                               : copy_engine(dhost, v_pool, vit.data(), n, P.block_bytes, st);
     if (rc != PKV_OK) return rc;
   }
