@@ -47,11 +47,11 @@ METRIC = "paged decode attention KV GB/s & tokens/s (% of 8 TB/s HBM); swap GB/s
 # of one decode launch, per (stored K/V type, query heads per KV head), from ncu
 # captures of agent 48 x 4,096 (summary in profiles/) of the kernels built from the
 # sources with this digest.  Reported only while the sources hash to TRAFFIC_SOURCES_SHA256.
-TRAFFIC_SOURCES_SHA256 = "a82df1b1e878ed12a8bb88b3335d90e536f0b6e0e6a05b941858e7a6fcf9bcaa"
+TRAFFIC_SOURCES_SHA256 = "e652ec76c3fcba2743a3f447b7b48b64e490e502c708eecbd8d6e2d57997c172"
 TRAFFIC_RECORD = {
-    ("bf16", 8): 1.0077,   # 811.5 + 3.1 MB DRAM for 808.3 MB algorithmic (mean of 2 launches)
-    ("e4m3", 8): 1.0117,   # 406.9 + 2.9 MB for 405.1 MB
-    ("bf16", 16): 1.0111,  # 814.4 + 4.5 MB for 809.9 MB
+    ("bf16", 8): 1.0078,   # 811.5 + 3.1 MB DRAM for 808.3 MB algorithmic (mean of 2 launches)
+    ("e4m3", 8): 1.0122,   # 406.9 + 3.1 MB for 405.1 MB
+    ("bf16", 16): 1.0113,  # 814.4 + 4.6 MB for 809.9 MB
 }
 
 

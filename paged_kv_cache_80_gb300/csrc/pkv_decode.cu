@@ -797,7 +797,9 @@ __global__ void __launch_bounds__(NW * 32) decode_tc_kernel(const __grid_constan
     if (lane < 2 && pair >= 0) {
       const int wa = pbeg / R, wb = (pbeg + nt - 1) / R;
       unsigned long long* c = a.counters + wa;
-      unsigned long long cur = *reinterpret_cast<volatile unsigned long long*>(c);
+      // first guess: every other contributor is in (right for the last one, which merges, so its
+      // count takes one atomic); a wrong guess returns the word and the loop goes on from it
+      unsigned long long cur = (a.epoch << 16) | static_cast<unsigned long long>(wb - wa);
       for (;;) {
         const bool ours = (cur >> 16) == a.epoch;
         const unsigned long long prev = atomicCAS(c, cur, ours ? cur + 1 : ((a.epoch << 16) | 1ull));
