@@ -190,8 +190,11 @@ class NvmlSampler:
             self._sample()
         sm = [s[0] for s in self.samples]
         reasons = sorted({name for s in self.samples for bit, name in self.REASONS.items() if s[2] & bit})
+        ts_all = [s[3] for s in self.samples]
+        gap = (ts_all[-1] - ts_all[0]) / (len(ts_all) - 1) * 1e3 if len(ts_all) > 1 else None
         out = {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(s[1] for s in self.samples),
-               "reasons": reasons, "samples": len(self.samples), "source": "NVML every 1 ms"}
+               "reasons": reasons, "samples": len(self.samples),
+               "source": "NVML, back to back with a 1 ms pause" + (f" (one sample every {gap:.1f} ms)" if gap else "")}
         if self.marks:
             ts = np.array([s[3] for s in self.samples])
             near = [self.samples[int(np.abs(ts - m).argmin())][0] for m in self.marks]
