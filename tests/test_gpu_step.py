@@ -288,3 +288,41 @@ def test_decode_step_appends_inside_the_attention_launch(H_q, H_kv, d, B, dtype)
         check_attention(out_f64(out, act), b.decode_ref(q, tables, lens, scale, layer=layer), act)
         b.check_state()
         b.check_pools_bitexact()
+
+
+def test_packed_step_rejects_a_layout_that_does_not_hold_the_rows():
+    """pkv_step_launch_packed checks its packed layout (parts in order, 16-byte offsets, each
+    holding n rows, in_bytes covering the last part) before any copy or launch: a bad layout
+    is INVALID_ARG and the pools stay as they were."""
+    import torch
+
+    g = W.Geometry(L=1, H_q=16, H_kv=2, d_head=128, block_size=16, dtype="bf16", num_blocks=64)
+    b = PagedBatch(g, None, seed=46)
+    ids = b.new_seqs(2)
+    b.append(ids, [10, 40], "p")
+    n, Wd = 2, 4
+    rq, rk = g.H_q * g.d_head * 2, g.H_kv * g.d_head * 2
+    ws = torch.empty(pkv.pkv_decode_workspace_size(b.lib, n), dtype=torch.uint8, device="cuda")
+    out_dev = torch.empty((n, g.H_q, g.d_head), dtype=torch.bfloat16, device="cuda")
+    in_dev = torch.zeros(1 << 16, dtype=torch.uint8, device="cuda")
+    in_host = torch.zeros(1 << 16, dtype=torch.uint8).pin_memory()
+    out_host = torch.zeros((n, g.H_q, g.d_head), dtype=torch.bfloat16).pin_memory()
+    meta_dev = torch.zeros(n * (Wd + 2), dtype=torch.int32, device="cuda")
+    launcher = pkv.PackedStepLauncher(b.lib, 0, in_dev, out_dev, b.kp, b.vp, 0.1, ws)
+    kp0, vp0 = b.kp.clone(), b.vp.clone()
+    ok_k, ok_v = n * rq, n * rq + n * rk
+    bad = [
+        (ok_k - 16, ok_v, ok_v + n * rk, 0),            # q rows overrun k_new
+        (ok_k, ok_k, ok_v + n * rk, 0),                 # k_new rows overrun v_new
+        (ok_k, ok_v, ok_v + n * rk - 16, 0),            # in_bytes short of the v_new rows
+        (ok_k + 8, ok_v + 16, ok_v + 16 + n * rk, 0),   # an offset not a multiple of 16
+        (ok_k, ok_v, ok_v + n * rk + 64, ok_v + 16),    # metadata inside the v_new rows
+    ]
+    for off_k, off_v, in_bytes, off_meta in bad:
+        with pytest.raises(pkv.PkvError) as e:
+            launcher(n, Wd, np.zeros((0, 2), np.int32), in_host, off_k, off_v, in_bytes, out_host, meta_dev,
+                     off_meta=off_meta)
+        assert e.value.name == "PKV_ERR_INVALID_ARG"
+    torch.cuda.synchronize()
+    assert torch.equal(b.kp, kp0) and torch.equal(b.vp, vp0)
+    b.check_state()
