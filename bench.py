@@ -47,7 +47,7 @@ METRIC = "paged decode attention KV GB/s & tokens/s (% of 8 TB/s HBM); swap GB/s
 # of one decode launch, per (stored K/V type, query heads per KV head), from ncu
 # captures of agent 48 x 4,096 (summary in profiles/) of the kernels built from the
 # sources with this digest.  Reported only while the sources hash to TRAFFIC_SOURCES_SHA256.
-TRAFFIC_SOURCES_SHA256 = "e652ec76c3fcba2743a3f447b7b48b64e490e502c708eecbd8d6e2d57997c172"
+TRAFFIC_SOURCES_SHA256 = "730211c7a02d2541df18d90f7fba0d6b7ab3a046bd8dc96bc0af03ae1af36511"
 TRAFFIC_RECORD = {
     ("bf16", 8): 1.0078,   # 811.5 + 3.1 MB DRAM for 808.3 MB algorithmic (mean of 2 launches)
     ("e4m3", 8): 1.0122,   # 406.9 + 3.1 MB for 405.1 MB
@@ -56,12 +56,18 @@ TRAFFIC_RECORD = {
 
 
 def decode_sources_digest() -> str:
+    """SHA-256 of the decode kernel's sources with comments and blank space removed (a
+    comment-only edit leaves the recorded traffic valid; any code change voids it)."""
     import hashlib
+    import re
 
     h = hashlib.sha256()
     for f in ("pkv_decode.cu", "pkv_attn.cuh", "pkv_device.cuh"):
-        with open(os.path.join(ROOT, "paged_kv_cache_80_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "paged_kv_cache_80_gb300", "csrc", f)) as fh:
+            text = fh.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()
 NOMINAL_HBM_GBS = 8000.0
 

@@ -8,7 +8,11 @@
 // The kernel takes the block table and walks the sequence's logical blocks,
 // fetching each physical block where it lies.
 //
-// Tensor-core path (bf16/f16, d_head 64 or 128, G <= 8, B a multiple of 16):
+// Tensor-core path (bf16/f16, d_head 64 or 128, G <= 16, B a multiple of 16):
+//   * One launch per call for up to 4,096 sequences: every CTA plans its own warps from
+//     the lengths (tiles per sequence, their prefix, each warp's first tile); larger
+//     batches launch a one-CTA plan kernel first, which the attention kernel follows
+//     as its programmatic dependent.
 //   * Work unit = a 16-token tile of one (sequence, KV head) pair: the K and V
 //     slabs of 16 x d_head elements, contiguous in the pool.  All tiles of the
 //     batch are laid end to end (sequence-major, then KV head) and cut into equal
@@ -27,8 +31,12 @@
 //     m_new = max(m_prev, m_blk), l_new = l_prev e^{m_prev-m_new} + l_blk e^{m_blk-m_new},
 //     O_new likewise), in base 2 with log2(e) folded into the scale.
 //   * A pair fully inside one warp's range is normalised and written directly; a
-//     pair split across warps leaves (m, l, O) partials that a merge kernel
-//     combines with the same rule.
+//     pair split across warps leaves (m, l, O) partials.  At the end of its range a
+//     warp publishes its partials and counts them (an epoch-tagged counter per split
+//     pair, so the workspace needs no clearing); the warp that completes a pair's count
+//     merges its partials with the same rule.
+//   * Groups of 9 to 16 query heads run as two 8-head column blocks: every K / V
+//     fragment feeds two mma.
 // FP8 pools (E4M3 codes, "KV Cache Management" b_elem = 1): the same kernel with
 //   16 x 128-byte tiles (one TMA box each); every lane reads its operand bytes with
 //   16-byte shared loads and converts code pairs to binary16 (exact), so the mma

@@ -208,3 +208,38 @@ def test_workspace_contents_do_not_matter():
         pkv.pkv_check_device_error()
         got = out.double().cpu().numpy()
         check_attention(got, b.decode_ref(q, tables, sl, 0.088), "bf16")
+
+
+def test_two_streams_with_their_own_workspaces_at_once():
+    """Two decode calls in flight at once on two streams, each with its own workspace (the
+    split-pair counters live in the workspace, tagged per launch): both match the oracle, over
+    several rounds of back-to-back launches."""
+    import torch
+
+    g = W.Geometry(L=1, H_q=64, H_kv=8, d_head=128, block_size=16, dtype="bf16", num_blocks=3000)
+    b = PagedBatch(g, W.permutation(22, "fo", g.num_blocks), seed=22)
+    lens = [20000, 7, 900, 1, 3000, 16, 17, 5000]
+    ids = b.new_seqs(len(lens))
+    b.append(ids, lens, "prompt")
+    halves = [ids[0::2], ids[1::2]]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    work = []
+    for k, part in enumerate(halves):
+        tables, sl = b.tables(part)
+        ws = torch.empty(pkv.pkv_decode_workspace_size(b.lib, len(part)), dtype=torch.uint8, device="cuda")
+        work.append((part, tables, sl, torch.from_numpy(tables).cuda(), torch.from_numpy(sl).cuda(), ws))
+    torch.cuda.synchronize()
+    for rnd in range(3):
+        outs, qs = [], []
+        for k, (part, tables, sl, dt, dl, ws) in enumerate(work):
+            q = W.normal(22, f"q{rnd}{k}", (len(part), g.H_q, g.d_head), "bf16")
+            out = torch.full((len(part), g.H_q, g.d_head), float("nan"), dtype=torch.bfloat16, device="cuda")
+            qd = to_dev(q, "bf16")
+            with torch.cuda.stream(streams[k]):
+                pkv.pkv_decode_attention(b.lib, 0, qd, b.kp, b.vp, dt, dl, 0.0884, out, ws, stream=streams[k])
+            outs.append((out, qd))
+            qs.append(q)
+        torch.cuda.synchronize()
+        pkv.pkv_check_device_error()
+        for k, (part, tables, sl, dt, dl, ws) in enumerate(work):
+            check_attention(outs[k][0].double().cpu().numpy(), b.decode_ref(qs[k], tables, sl, 0.0884), "bf16")
