@@ -229,7 +229,12 @@ int pkv_decode_attention(const pkv_pool* pool, int32_t layer, const void* q, con
  *             until that copy has run (e.g. a ring of buffers and events).
  *   workspace: as for pkv_decode_attention (pkv_decode_workspace_size(pool, n)).
  *   attn_begin, attn_end: optional cudaEvent_t (NULL = none) recorded on the
- *             stream just before and after the attention kernels.
+ *             stream just before the append and just after the attention (on the
+ *             tensor-core path the attention kernel is the append kernel's
+ *             programmatic dependent: it starts, plans its warps and reads its first
+ *             table entries while the new tokens are written, and waits for the append
+ *             before loading any K/V; the append kernel lets only this launch start
+ *             early -- pkv_append_kv called on its own does not).
  * Arguments are validated before anything changes; after the plan is applied,
  * only a CUDA launch failure (PKV_ERR_CUDA) can still fail the call. */
 typedef struct CUevent_st* pkv_event_t; /* identical to cudaEvent_t */
