@@ -386,23 +386,24 @@ class DecodeRunner:
         torch, pkv, g = self.torch, self.pkv, self.g
         mrow = self.Wd + 2
 
+        rows, metas, metas_np = self._e2e_views
+
         def plan(t):
             ids = self.running(t)
             if len(ids) == 0:
                 return None
-            mview = host[t, self.off_meta:self.off_meta + 4 * len(ids) * mrow].view(torch.int32)
-            cows = pkv.pkv_step_plan(self.pool, ids, self.Wd, mview)
-            return ids, self.pool, mview, cows
+            cows = pkv.pkv_step_plan(self.pool, ids, self.Wd, metas[t])
+            return ids, self.pool, metas_np[t], cows
 
         nxt = plan(t0)
         for i in range(steps):
             t = t0 + i
             cur, nxt = nxt, None
             if cur is not None:
-                ids, pool, mview, cows = cur
+                ids, pool, mnp, cows = cur
                 n = len(ids)
                 in_bytes = self.off_meta + 4 * n * mrow
-                self.launcher_for(pool)(n, self.Wd, cows, host[t], self.off_k, self.off_v, in_bytes, self.out_host,
+                self.launcher_for(pool)(n, self.Wd, cows, rows[t], self.off_k, self.off_v, in_bytes, self.out_host,
                                         off_meta=self.off_meta, attn_events=events[i] if events else None)
                 self.flush_l2(t)
                 self.pool = pool
@@ -416,7 +417,7 @@ class DecodeRunner:
             if timed:
                 if events:
                     self.decode_ms.append(events[i])
-                lens = mview.numpy()[n + n * self.Wd:n + n * self.Wd + n]
+                lens = mnp[n + n * self.Wd:n + n * self.Wd + n]
                 kvb = int(lens.sum(dtype=np.int64)) * g.H_kv * g.d_head * g.elem_bytes * 2
                 self.kv_bytes.append(kvb)
                 self.alg_bytes.append(kvb + 2 * n * g.H_q * g.d_head * self.act_bytes + n * self.Wd * 4 + n * 4 +
@@ -470,6 +471,11 @@ class DecodeRunner:
                 host[t, o0:o1].view(self.td).copy_(src[t].reshape(-1))
         self.in_e2e = torch.empty(step_bytes, dtype=torch.uint8, device=self.dev)
         self.out_host = torch.empty(self.out.shape, dtype=self.td, pin_memory=True)
+        # per step: the packed row, its metadata part as int32 (pkv_step_plan writes there) and a
+        # numpy view of it, made once so that the loop does no tensor slicing
+        rows = [host[t] for t in range(self.total_steps)]
+        metas = [r[self.off_meta:].view(torch.int32) for r in rows]
+        self._e2e_views = (rows, metas, [m.numpy() for m in metas])
         return host
 
     def inputs_for_steps(self, tag):
