@@ -307,7 +307,7 @@ class DecodeRunner:
         self.out = torch.empty((n_max, g.H_q, g.d_head), dtype=td, device=self.dev)
         self.ws = torch.empty(self.pkv.pkv_decode_workspace_size(self.pool, n_max), dtype=torch.uint8,
                               device=self.dev)
-        self.staging = Staging(torch, self.dev, n_max * (self.Wd + 2))
+        self.staging = Staging(torch, self.dev, self.pkv.pkv_step_meta_ints(self.pool, n_max, self.Wd))
         self.stream = torch.cuda.current_stream().cuda_stream
         self._fast_pool = self.pool
         self._prepare_fast()
@@ -360,7 +360,7 @@ class DecodeRunner:
         if rc:
             pkv._check(rc, "pkv_decode_step")
         self.flush_l2(t)
-        nbytes = self.staging.mark(k, n * (self.Wd + 2))
+        nbytes = self.staging.mark(k, pkv.pkv_step_meta_ints(self.pool, n, self.Wd))
         if timed:
             self.decode_ms.append(events)
             lens = hnp[n + n * self.Wd:n + n * self.Wd + n]
@@ -384,7 +384,6 @@ class DecodeRunner:
         the same from step to step) copies the packed inputs and metadata in with one copy,
         runs the step and copies the result out."""
         torch, pkv, g = self.torch, self.pkv, self.g
-        mrow = self.Wd + 2
 
         rows, metas, metas_np = self._e2e_views
 
@@ -402,7 +401,7 @@ class DecodeRunner:
             if cur is not None:
                 ids, pool, mnp, cows = cur
                 n = len(ids)
-                in_bytes = self.off_meta + 4 * n * mrow
+                in_bytes = self.off_meta + 4 * pkv.pkv_step_meta_ints(pool, n, self.Wd)
                 self.launcher_for(pool)(n, self.Wd, cows, rows[t], self.off_k, self.off_v, in_bytes, self.out_host,
                                         off_meta=self.off_meta, attn_events=events[i] if events else None)
                 self.flush_l2(t)
@@ -463,7 +462,7 @@ class DecodeRunner:
         rq, rk = g.H_q * g.d_head * self.act_bytes, g.H_kv * g.d_head * self.act_bytes
         self.off_k, self.off_v = n * rq, n * (rq + rk)
         self.off_meta = n * (rq + 2 * rk)
-        step_bytes = self.off_meta + 4 * n * (self.Wd + 2)
+        step_bytes = self.off_meta + 4 * self.pkv.pkv_step_meta_ints(self.pool, n, self.Wd)
         host = torch.empty((self.total_steps, step_bytes), dtype=torch.uint8, pin_memory=True)
         for t in range(self.total_steps):
             for src, o0, o1 in ((self.q, 0, self.off_k), (self.kn, self.off_k, self.off_v),
@@ -567,7 +566,7 @@ class ChatRunner(DecodeRunner):
 class ForkedRunner(DecodeRunner):
     name = "forked"
 
-    def __init__(self, torch, pkv, dev, total_steps, n_branch=64, kv_dtype="bf16"):
+    def __init__(self, torch, pkv, dev, total_steps, n_branch=64, kv_dtype="bf16", share=8):
         super().__init__(torch, pkv, dev, total_steps)
         wl = W.forked(n_branch=n_branch)
         self.wl, self.seed = wl, wl.seed
@@ -576,6 +575,9 @@ class ForkedRunner(DecodeRunner):
         self.n_max = n_branch
         self.scale = wl.scale
         self.pool = self._new_pool(wl.free_order)
+        self.share = share
+        if share:  # the branches' shared prefix attended once per step (before the workspace is sized)
+            pkv.pkv_pool_set_prefix_sharing(self.pool, share, 1, 0)
         self.kp = W.device_normal(self.seed, "k_pool", g.pool_shape(), g.dtype, dev)
         self.vp = W.device_normal(self.seed, "v_pool", g.pool_shape(), g.dtype, dev)
         parent = pkv.pkv_seq_create(self.pool)
@@ -588,15 +590,20 @@ class ForkedRunner(DecodeRunner):
             kn = W.device_normal(self.seed, "suffix_k", (len(slots), g.H_kv, g.d_head), self.act, dev)
             vn = W.device_normal(self.seed, "suffix_v", (len(slots), g.H_kv, g.d_head), self.act, dev)
             pkv.pkv_append_kv(self.pool, 0, kn, vn, torch.from_numpy(slots).to(dev), self.kp, self.vp)
-        self.unique_tokens = int(wl.lengths[0]) + sum(suffix)
+        self.unique_tokens = int(wl.lengths[0]) + sum(suffix)  # grows by one token per branch per step
         self.ids_np = np.array(self.ids, np.int32)
         self.Wd = -(-(int(wl.lengths[0]) + 2048 + total_steps + 1) // g.block_size)
         self.inputs_for_steps("forked")
         self._alloc_common(n_branch)
         self.config = workload_config("forked", g, n_branch, prefix=int(wl.lengths[0]))
+        self.share_desc = (f"on: runs of >= {share} rows sharing their first blocks attend to them once per step "
+                           "(pkv_pool_set_prefix_sharing)" if share else "off: every branch reads the prefix")
 
     def running(self, t):
         return self.ids_np
+
+    def after_step(self, t, ids):
+        self.unique_tokens += len(ids)
 
 
 class TinyRunner(DecodeRunner):
@@ -668,6 +675,8 @@ RUNNERS = {"agent32k": AgentRunner, "chat": ChatRunner, "forked": ForkedRunner, 
 def run_decode(args, torch, pkv, dev, world, rank):
     total = args.warmup + args.steps + 2 + args.steps  # timed region, then e2e warm-up + e2e steps
     kw = {} if args.workload == "tiny" else {"kv_dtype": args.kv_dtype}
+    if args.workload == "forked":
+        kw["share"] = args.share
     if args.workload == "agent32k" and (args.context or args.n_seq or args.q_heads):
         r = AgentRunner(torch, pkv, dev, total, n_seq=args.n_seq or 48, context=args.context or 32768,
                         q_heads=args.q_heads, **kw)
@@ -688,6 +697,7 @@ def run_decode(args, torch, pkv, dev, world, rank):
     e_end = torch.cuda.Event(enable_timing=True)
     evs = r.make_events(args.steps)
     launches0 = pkv.pkv_launch_count()
+    u0 = getattr(r, "unique_tokens", None)
     e_start.record()
     for i, t in enumerate(range(args.warmup, args.warmup + args.steps)):
         r.step(t, timed=True, events=evs[i])
@@ -747,6 +757,15 @@ def run_decode(args, torch, pkv, dev, world, rank):
         "gpu_launches": int(launches),
         "clocks": clk,
     }
+    if u0 is not None:  # forked: the distinct K/V a step reads (prefix once, every branch's own tokens)
+        n = len(r.ids_np)
+        per_tok = g.H_kv * g.d_head * g.elem_bytes * 2
+        ub = (u0 + n * (args.steps + 1) / 2) * per_tok
+        line["shared_prefix"] = r.share_desc
+        line["unique"] = {"kv_bytes_per_step": int(ub), "gb_per_s_decode_call": round(ub / (dec_avg / 1e3) / 1e9, 1),
+                          "frac": round(ub / (dec_avg / 1e3) / 1e9 / peak, 4),
+                          "note": "distinct K/V bytes (the shared prefix counted once) / decode-call time, "
+                                  "against the same HBM peak; value counts every branch's logical bytes"}
     return line, r
 
 
@@ -765,6 +784,9 @@ def config_records(args, torch, pkv, dev, world, rank, steps: int = 20):
                       "decode_call": {k: ln["roofline"][k] for k in ("achieved", "frac", "avg_launch_ms")},
                       "e2e": ln["e2e"]["value"], "gpu_launches": ln["gpu_launches"],
                       "sm_mhz": ln["clocks"]["sm_mhz"] if ln["clocks"] else None, "steps": steps}
+        if "unique" in ln:
+            recs[name]["unique"] = {k: ln["unique"][k] for k in ("kv_bytes_per_step", "gb_per_s_decode_call", "frac")}
+            recs[name]["shared_prefix"] = ln["shared_prefix"]
         del r
         torch.cuda.empty_cache()
     return recs
@@ -1469,6 +1491,8 @@ def main():
                     help="reload_prefill workload: layers per reload range (default 1)")
     ap.add_argument("--swap-chunks", type=int, default=512,
                     help="swap workload: chunks evicted and restored (default 512, 42.9 GB; fewer for small captures)")
+    ap.add_argument("--share", type=int, default=8,
+                    help="forked: prefix sharing, the least rows of a run that shares its first blocks (0: off)")
     ap.add_argument("--no-config-records", action="store_true",
                     help="default line: skip the bounded tiny / chat / forked runs added to it")
     ap.add_argument("--no-swap-record", action="store_true",

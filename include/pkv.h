@@ -183,7 +183,8 @@ int pkv_append_kv(const pkv_pool* pool, int32_t layer, const void* k_new, const 
                   const int32_t* slot_mapping, int32_t n_tok, void* k_pool, void* v_pool, pkv_stream_t stream);
 
 /* Bytes of device workspace pkv_decode_attention needs for n_seq sequences on
- * the current device. */
+ * the current device (with prefix sharing on, also room for the shared-prefix
+ * partials of a decode step of n_seq sequences). */
 int pkv_decode_workspace_size(const pkv_pool* pool, int32_t n_seq, size_t* bytes);
 
 /* Decode attention over the block tables ([KVM] PagedAttention model: the kernel
@@ -223,10 +224,12 @@ int pkv_decode_attention(const pkv_pool* pool, int32_t layer, const void* q, con
  *             v_new and out belongs to seq_ids[i].
  *   q, out  : device [n][H_q][d_head];  k_new, v_new: device [n][H_kv][d_head].
  *   W       : table width; every sequence needs ceil((len + 1) / B) <= W.
- *   meta_host: page-locked host int32 [n * (W + 2)]: the step writes its slot
- *             mapping, tables and lengths there and copies them to meta_dev
- *             (device int32, same size) on the stream; do not reuse meta_host
- *             until that copy has run (e.g. a ring of buffers and events).
+ *   meta_host: page-locked host int32 [pkv_step_meta_ints(pool, n, W)] (n * (W + 2)
+ *             with prefix sharing off): the step writes its slot mapping, tables
+ *             and lengths there (and, with sharing on, its shared-prefix plan) and
+ *             copies them to meta_dev (device int32, same size, 16-byte aligned) on
+ *             the stream; do not reuse meta_host until that copy has run (e.g. a
+ *             ring of buffers and events).
  *   workspace: as for pkv_decode_attention (pkv_decode_workspace_size(pool, n)).
  *   attn_begin, attn_end: optional cudaEvent_t (NULL = none) recorded on the
  *             stream just before the append and just after the attention (on the
@@ -238,6 +241,32 @@ int pkv_decode_attention(const pkv_pool* pool, int32_t layer, const void* q, con
  * Arguments are validated before anything changes; after the plan is applied,
  * only a CUDA launch failure (PKV_ERR_CUDA) can still fail the call. */
 typedef struct CUevent_st* pkv_event_t; /* identical to cudaEvent_t */
+
+/* Shared prefixes in decode steps.  (The pages share a forked prefix's blocks in
+ * memory -- [KVM] "Zero-copy deliberation via copy-on-write branching": the parent
+ * and every branch map the same physical blocks -- and every branch still reads
+ * them in attention; this option reads them once per step for all branches.)
+ * With sharing on, a decode step (pkv_decode_step, pkv_step_plan + a launch call)
+ * finds runs of consecutive batch rows whose tables begin with the same physical
+ * blocks -- at least min_blocks of them, in at least min_members rows; every row
+ * after the first shares at least half of what the rows before it share; the run's
+ * prefix stops before the block of each row's last token -- and attends to those
+ * blocks once for the whole run (a tcgen05 kernel, all the run's queries of a KV
+ * head as 128-row tiles against each key tile, in splits of whole blocks sized so
+ * that its grid comes near target_ctas CTAs) and to each row's own blocks in the
+ * decode kernel, which merges the two with the online-softmax rule ([KVM] "Chunked
+ * prefill mechanics").  The result is the same attention (within rounding).
+ *   min_members: 0 turns sharing off (the default); else >= 2.
+ *   min_blocks : >= 1.
+ *   target_ctas: <= 0 takes the current device's SM count (PKV_ERR_CUDA without one).
+ * Needs a bf16, f16 or E4M3 pool with d_head 128, at most 16 query heads per KV head
+ * and B a multiple of 16 (else PKV_ERR_UNSUPPORTED).  While it is on, the step
+ * metadata is pkv_step_meta_ints(pool, n, W) int32 (the plan follows the lengths
+ * from a 16-byte boundary) and pkv_decode_workspace_size includes room for the
+ * prefix kernel's partials (2 n + 1024 slots of H_q x (d_head + 2) floats). */
+int pkv_pool_set_prefix_sharing(pkv_pool* pool, int32_t min_members, int32_t min_blocks, int32_t target_ctas);
+/* int32 count of one step's metadata for n sequences and table width W. */
+int pkv_step_meta_ints(const pkv_pool* pool, int32_t n, int32_t W, int64_t* ints);
 int pkv_decode_step(pkv_pool* pool, int32_t layer, const int32_t* seq_ids, int32_t n, int32_t W, const void* q,
                     const void* k_new, const void* v_new, void* k_pool, void* v_pool, float scale, void* out,
                     int32_t* meta_host, int32_t* meta_dev, void* workspace, size_t ws_bytes, pkv_event_t attn_begin,
@@ -248,8 +277,8 @@ int pkv_decode_step(pkv_pool* pool, int32_t layer, const int32_t* seq_ids, int32
  * one).  (The pages have no counterpart of these calls.)
  * pkv_step_plan: the host half -- checks the sequences as pkv_decode_step does, then
  *   plans one new token per sequence (pkv_plan_append) and writes the slot mapping,
- *   tables and lengths into meta_host (host int32 [n * (W + 2)], as for
- *   pkv_decode_step) and the copy-on-write pairs into cow_pairs (host int32 [2 n];
+ *   tables and lengths into meta_host (host int32 [pkv_step_meta_ints(pool, n, W)],
+ *   as for pkv_decode_step) and the copy-on-write pairs into cow_pairs (host int32 [2 n];
  *   their count in *n_cow).  On failure nothing changes.
  * pkv_step_launch: the device half, on the stream: copies meta_host to meta_dev,
  *   copies the shared blocks, appends k_new / v_new at the planned slots and attends
@@ -279,7 +308,7 @@ int pkv_step_launch_host(pkv_pool* pool, int32_t layer, int32_t n, int32_t W, co
  * append and the attention, and ONE copy of the n result rows from out_dev to out_host.
  *   in_host / in_dev: q [n][H_q][d_head] at byte 0, k_new [n][H_kv][d_head] at off_k,
  *                     v_new [n][H_kv][d_head] at off_v (activation type), and, when off_meta
- *                     is not 0, the step's metadata [n * (W + 2)] int32 at off_meta (where
+ *                     is not 0, the step's metadata [pkv_step_meta_ints] int32 at off_meta (where
  *                     pkv_step_plan wrote it into in_host; meta_host and meta_dev are then
  *                     ignored and may be NULL).  Offsets are multiples of 16, each part
  *                     before the next, in_bytes covers the last part.

@@ -24,7 +24,7 @@ __all__ = [
     "StepLauncher", "PackedStepLauncher",
     "pkv_prefill_attention",
     "pkv_copy_blocks", "pkv_swap_out",
-    "pkv_swap_in", "pkv_swap_in_layers", "pkv_seq_host_slots", "pkv_seq_residency", "TIER_HBM", "TIER_HOST", "TIER_RELOADING", "pkv_pool_set_swap_engine", "pkv_check_device_error", "pkv_launch_count",
+    "pkv_swap_in", "pkv_swap_in_layers", "pkv_seq_host_slots", "pkv_seq_residency", "TIER_HBM", "TIER_HOST", "TIER_RELOADING", "pkv_pool_set_swap_engine", "pkv_pool_set_prefix_sharing", "pkv_step_meta_ints", "pkv_check_device_error", "pkv_launch_count",
     "pkv_selftest_bounded_wait", "pkv_device_code_version", "pkv_pool_set_kv_scales", "pkv_pool_kv_scales",
     "PrefixStats", "pkv_prefix_cache_create", "pkv_prefix_cache_destroy", "pkv_prefix_match", "pkv_prefix_attach",
     "pkv_prefix_insert", "pkv_prefix_release", "pkv_prefix_evict", "pkv_prefix_get_stats", "pkv_prefix_export",
@@ -125,6 +125,8 @@ def _L():
             "pkv_seq_residency": ([vp, i32, P32], ctypes.c_int),
             "pkv_swap_in_layers": ([vp, i32, vp, i64, i32, i32, i32, vp, vp, P32, vp], ctypes.c_int),
             "pkv_pool_set_swap_engine": ([vp, i32], ctypes.c_int),
+            "pkv_pool_set_prefix_sharing": ([vp, i32, i32, i32], ctypes.c_int),
+            "pkv_step_meta_ints": ([vp, i32, i32, P64], ctypes.c_int),
             "pkv_pool_set_kv_scales": ([vp, ctypes.c_float, ctypes.c_float], ctypes.c_int),
             "pkv_pool_kv_scales": ([vp, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_float)], ctypes.c_int),
             "pkv_check_device_error": ([vp, P32, P64], ctypes.c_int),
@@ -217,6 +219,7 @@ class Pool:
     def __init__(self, handle: ctypes.c_void_p, geometry: Geometry):
         self.handle = handle
         self.geometry = geometry
+        self._meta_ints = {}  # (n, W) -> step metadata int32 count (cleared when sharing changes)
 
     @property
     def _as_parameter_(self):
@@ -241,13 +244,34 @@ def _nbytes(t) -> int:
     return int(t.nbytes) if isinstance(t, np.ndarray) else t.numel() * t.element_size()
 
 
+def pkv_step_meta_ints(pool: PoolLike, n: int, W: int) -> int:
+    """int32 count of one decode step's metadata (n*(W+2) with prefix sharing off)."""
+    if isinstance(pool, Pool):
+        v = pool._meta_ints.get((n, W))
+        if v is not None:
+            return v
+    out = ctypes.c_int64()
+    _check(_L().pkv_step_meta_ints(_h(pool), int(n), int(W), ctypes.byref(out)), "pkv_step_meta_ints")
+    if isinstance(pool, Pool):
+        pool._meta_ints[(n, W)] = out.value
+    return out.value
+
+
+def pkv_pool_set_prefix_sharing(pool: PoolLike, min_members: int, min_blocks: int = 1, target_ctas: int = 0) -> None:
+    """Decode steps attend to blocks shared by runs of batch rows once per run (0 turns it off)."""
+    _check(_L().pkv_pool_set_prefix_sharing(_h(pool), int(min_members), int(min_blocks), int(target_ctas)),
+           "pkv_pool_set_prefix_sharing")
+    if isinstance(pool, Pool):
+        pool._meta_ints.clear()
+
+
 def _step_bytes(pool: PoolLike, n: int, W: int):
     """Bytes a decode step of n sequences reads or writes in each buffer: metadata
-    (n*(W+2) int32), q / out rows (n*H_q*d_head activations), k_new / v_new rows
+    (pkv_step_meta_ints int32), q / out rows (n*H_q*d_head activations), k_new / v_new rows
     (n*H_kv*d_head activations; activations are bf16 around an FP8 pool)."""
     g = pool.geometry if isinstance(pool, Pool) else pkv_pool_geometry(pool)
     ab = {F32: 4, F16: 2, BF16: 2, E4M3: 2}[g.dtype]
-    return 4 * n * (W + 2), ab * n * g.H_q * g.d_head, ab * n * g.H_kv * g.d_head
+    return 4 * pkv_step_meta_ints(pool, n, W), ab * n * g.H_q * g.d_head, ab * n * g.H_kv * g.d_head
 
 
 def _require_bytes(*bufs):
@@ -477,7 +501,7 @@ def pkv_step_plan(pool: PoolLike, seq_ids, W: int, meta_host) -> np.ndarray:
     (pinned int32, >= n*(W+2)); returns the copy-on-write pairs [n_cow][2]."""
     ids = _i32(seq_ids)
     n = ids.size
-    _require_bytes((meta_host, 4 * n * (W + 2), "meta_host"))
+    _require_bytes((meta_host, 4 * pkv_step_meta_ints(pool, n, W), "meta_host"))
     cows = np.zeros(max(2 * n, 2), np.int32)
     n_cow = ctypes.c_int32(0)
     _check(_L().pkv_step_plan(_h(pool), _a(ids), n, W, _host_ptr(meta_host, "meta_host"), _a(cows),
@@ -567,7 +591,7 @@ class StepLauncher:
                  attn_events=None) -> None:
         if n > self._rows:
             raise ValueError(f"n = {n} exceeds the {self._rows} rows of the bound device buffers")
-        mb, qb, kb = 4 * n * (W + 2), n * self._row_q, n * self._row_k
+        mb, qb, kb = 4 * pkv_step_meta_ints(self._pool, n, W), n * self._row_q, n * self._row_k
         _require_bytes((meta_host, mb, "meta_host"), (meta_dev, mb, "meta_dev"), (q_host, qb, "q_host"),
                        (k_new_host, kb, "k_new_host"), (v_new_host, kb, "v_new_host"), (out_host, qb, "out_host"))
         cp = _i32(cow_pairs).reshape(-1)
@@ -617,7 +641,7 @@ class PackedStepLauncher:
         the call, or (meta_host None) already queued into meta_dev by the caller."""
         if n > self._rows:
             raise ValueError(f"n = {n} exceeds the {self._rows} rows of the bound out_dev")
-        mb = 4 * n * (W + 2)
+        mb = 4 * pkv_step_meta_ints(self._pool, n, W)
         _require_bytes((in_host, in_bytes, "in_host"), (out_host, n * self._row_q, "out_host"))
         if in_bytes > self._in_bytes:
             raise ValueError(f"in_bytes = {in_bytes} exceeds the {self._in_bytes} bytes of the bound in_dev")

@@ -417,6 +417,42 @@ int pkv_pool_set_swap_engine(pkv_pool* pool, int32_t engine) {
 
 // ------------------------------------------------------------------ data plane
 
+int pkv_pool_set_prefix_sharing(pkv_pool* pool, int32_t min_members, int32_t min_blocks, int32_t target_ctas) {
+  pkv::clear_error();
+  if (!pool) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
+  Pool& P = *as_pool(pool);
+  if (min_members == 0) {
+    P.share_min_members = 0;
+    return PKV_OK;
+  }
+  if (min_members < 2 || min_blocks < 1)
+    return fail(PKV_ERR_INVALID_ARG, "min_members must be 0 (off) or >= 2, and min_blocks >= 1");
+  if (!pkv::share_geometry_ok(P.geo))
+    return fail(PKV_ERR_UNSUPPORTED, "shared prefixes need a bf16, f16 or E4M3 pool with d_head 128, at most 16 "
+                                     "query heads per KV head and a block size that is a multiple of 16");
+  if (target_ctas <= 0) {
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess || sms <= 0) {
+      cudaGetLastError();
+      return fail(PKV_ERR_CUDA, "no device to size the prefix kernel's grid from: give target_ctas");
+    }
+    target_ctas = sms;
+  }
+  P.share_min_members = min_members;
+  P.share_min_blocks = min_blocks;
+  P.share_ctas = target_ctas;
+  return PKV_OK;
+}
+
+int pkv_step_meta_ints(const pkv_pool* pool, int32_t n, int32_t W, int64_t* ints) {
+  pkv::clear_error();
+  if (!pool || n < 0 || W <= 0 || !ints) return fail(PKV_ERR_INVALID_ARG, "bad arguments to pkv_step_meta_ints");
+  *ints = pkv::step_meta_ints(*as_pool(pool), n, W);
+  return PKV_OK;
+}
+
 int pkv_append_kv(const pkv_pool* pool, int32_t layer, const void* k_new, const void* v_new,
                   const int32_t* slot_mapping, int32_t n_tok, void* k_pool, void* v_pool, pkv_stream_t stream) {
   pkv::clear_error();
@@ -711,6 +747,102 @@ static int step_workspace_check(pkv_pool* pool, int32_t n, size_t ws_bytes) {
   return PKV_OK;
 }
 
+// The shared-prefix plan of a step's batch (layout in pkv_internal.h), from the tables after the
+// step's append.  A run of consecutive rows is a group when every row after the first shares at
+// least min_blocks leading blocks with the first (the same physical blocks: a fork's prefix)
+// and at least half of what the rows before it share; the group's prefix is the blocks all of
+// them share, cut so that every row keeps at least one token of its own (so no row's shared
+// blocks are written in this step).  Groups of fewer than min_members rows are dropped.  Each
+// group's prefix is cut into splits of whole blocks so that the prefix kernel's grid (CTAs =
+// member pairs of 128-row tiles x KV heads x splits, over all groups) comes near share_ctas,
+// splits of at least 256 keys, within the plan's item and slot caps.
+static void plan_sharing(Pool& P, const int32_t* ids, int32_t n, int32_t* plan) {
+  const int64_t B = P.geo.block_size;
+  int32_t* rows = plan + 4;
+  int32_t* items = plan + 4 + 4 * static_cast<int64_t>(n);
+  std::fill(plan, plan + 4 + 4 * static_cast<int64_t>(n), 0);
+  std::vector<int32_t>& grp = P.share_scratch;  // (row_begin, row_end, blocks, splits) per group
+  grp.clear();
+  for (int32_t i = 0; i < n;) {
+    const SeqState& a = P.seqs[ids[i]];
+    int64_t c = (a.len - 1) / B;  // blocks that leave row i a token of its own
+    int32_t j = i + 1;
+    while (j < n && c >= P.share_min_blocks) {
+      const SeqState& b = P.seqs[ids[j]];
+      const int64_t cb = std::min<int64_t>(c, (b.len - 1) / B);
+      int64_t k = 0;
+      while (k < cb && a.table[k] == b.table[k]) ++k;
+      if (k < P.share_min_blocks || 2 * k < c) break;
+      c = k;
+      ++j;
+    }
+    if (j - i >= P.share_min_members && c >= P.share_min_blocks) {
+      grp.insert(grp.end(), {i, j, static_cast<int32_t>(c), 1});
+      i = j;
+    } else {
+      ++i;
+    }
+  }
+  const int64_t ng = static_cast<int64_t>(grp.size()) / 4;
+  if (ng == 0) return;
+  const int64_t G = P.geo.H_q / P.geo.H_kv, per_cta = 2 * (128 / G);
+  auto ctas_of = [&](int64_t gi) { return (grp[4 * gi + 1] - grp[4 * gi] + per_cta - 1) / per_cta * P.geo.H_kv; };
+  double total = 0.0;
+  for (int64_t gi = 0; gi < ng; ++gi) total += static_cast<double>(ctas_of(gi)) * grp[4 * gi + 2];
+  int64_t n_items = 0, n_slots = 0;
+  for (int64_t gi = 0; gi < ng; ++gi) {
+    const int64_t ct = ctas_of(gi), kb = grp[4 * gi + 2];
+    const double want = P.share_ctas * (static_cast<double>(ct) * kb / total) / ct;
+    const int64_t most = std::max<int64_t>(1, kb * B / 256);
+    grp[4 * gi + 3] = static_cast<int32_t>(std::max<int64_t>(1, std::min<int64_t>(most, static_cast<int64_t>(want))));
+    n_items += grp[4 * gi + 3];
+    n_slots += static_cast<int64_t>(grp[4 * gi + 3]) * (grp[4 * gi + 1] - grp[4 * gi]);
+  }
+  // within the caps: fewer splits where there are most, then fewer groups
+  while (n_items > pkv::share_item_cap(n) || n_slots > pkv::share_slot_cap(n)) {
+    int64_t best = -1;
+    for (int64_t gi = 0; gi < ng; ++gi)
+      if (grp[4 * gi + 3] > 1 && (best < 0 || grp[4 * gi + 3] > grp[4 * best + 3])) best = gi;
+    if (best < 0) break;
+    --grp[4 * best + 3];
+    --n_items;
+    n_slots -= grp[4 * best + 1] - grp[4 * best];
+  }
+  int64_t kept = ng;
+  while (kept > 0 && (n_items > pkv::share_item_cap(n) || n_slots > pkv::share_slot_cap(n))) {
+    --kept;
+    n_items -= grp[4 * kept + 3];
+    n_slots -= static_cast<int64_t>(grp[4 * kept + 3]) * (grp[4 * kept + 1] - grp[4 * kept]);
+  }
+  int32_t it = 0, slot = 0, max_members = 0;
+  for (int64_t gi = 0; gi < kept; ++gi) {
+    const int32_t rb = grp[4 * gi], re = grp[4 * gi + 1], kb = grp[4 * gi + 2], m = re - rb;
+    const int32_t bps = (kb + grp[4 * gi + 3] - 1) / grp[4 * gi + 3];
+    const int32_t splits = (kb + bps - 1) / bps;
+    for (int32_t k = 0; k < splits; ++k, ++it) {
+      int32_t* e = items + 8 * static_cast<int64_t>(it);
+      e[0] = rb;
+      e[1] = re;
+      e[2] = k * bps;
+      e[3] = std::min(kb, (k + 1) * bps);
+      e[4] = slot + k * m;
+      e[5] = e[6] = e[7] = 0;
+    }
+    for (int32_t r = rb; r < re; ++r) {
+      int32_t* w = rows + 4 * static_cast<int64_t>(r);
+      w[0] = kb;
+      w[1] = splits;
+      w[2] = slot + (r - rb);
+      w[3] = m;
+    }
+    slot += splits * m;
+    max_members = std::max(max_members, m);
+  }
+  plan[0] = it;
+  plan[1] = max_members;
+  plan[2] = slot;
+}
+
 int pkv_step_plan(pkv_pool* pool, const int32_t* seq_ids, int32_t n, int32_t W, int32_t* meta_host,
                   int32_t* cow_pairs, int32_t* n_cow) {
   pkv::clear_error();
@@ -725,14 +857,23 @@ int pkv_step_plan(pkv_pool* pool, const int32_t* seq_ids, int32_t n, int32_t W, 
   int32_t* tables = meta_host + n;
   int32_t* lens = meta_host + n + static_cast<int64_t>(n) * W;
   if (int rc = pkv_plan_append(pool, seq_ids, ones.data(), n, slots, cow_pairs, n_cow)) return rc;
-  return pkv_export_tables(pool, seq_ids, n, tables, W, lens);
+  if (int rc = pkv_export_tables(pool, seq_ids, n, tables, W, lens)) return rc;
+  Pool& P = *as_pool(pool);
+  if (pkv::share_on(P)) {
+    int32_t* plan = meta_host + pkv::share_plan_offset(n, W);
+    std::fill(meta_host + static_cast<int64_t>(n) * (W + 2), plan, 0);  // the alignment gap
+    plan_sharing(P, seq_ids, n, plan);
+  }
+  return PKV_OK;
 }
 
-// The device half of a decode step; meta_host NULL: meta_dev already holds the plan.
+// The device half of a decode step; meta_host NULL: meta_dev already holds the plan, whose host
+// copy is at plan_host (read for the shared-prefix header).
 static int step_launch(pkv_pool* pool, int32_t layer, int32_t n, int32_t W, const int32_t* cow_pairs, int32_t n_cow,
                        const void* q, const void* k_new, const void* v_new, void* k_pool, void* v_pool, float scale,
                        void* out, const int32_t* meta_host, int32_t* meta_dev, void* workspace, size_t ws_bytes,
-                       pkv_event_t attn_begin, pkv_event_t attn_end, pkv_stream_t stream) {
+                       pkv_event_t attn_begin, pkv_event_t attn_end, pkv_stream_t stream,
+                       const int32_t* plan_host = nullptr) {
   if (!pool || n < 0 || W <= 0 || n_cow < 0) return fail(PKV_ERR_INVALID_ARG, "bad arguments to the step launch");
   if (n == 0) return PKV_OK;
   if (!q || !k_new || !v_new || !k_pool || !v_pool || !out || !meta_dev || !workspace || (n_cow > 0 && !cow_pairs))
@@ -740,11 +881,22 @@ static int step_launch(pkv_pool* pool, int32_t layer, int32_t n, int32_t W, cons
   if (layer < 0 || layer >= as_pool(pool)->geo.L) return fail(PKV_ERR_INVALID_ARG, "layer out of range");
   if (int rc = step_workspace_check(pool, n, ws_bytes)) return rc;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const Pool& P = *as_pool(pool);
   if (meta_host) {
-    const size_t meta_bytes = sizeof(int32_t) * static_cast<size_t>(n) * (W + 2);
+    const size_t meta_bytes = sizeof(int32_t) * static_cast<size_t>(pkv::step_meta_ints(P, n, W));
     cudaError_t e = cudaMemcpyAsync(meta_dev, meta_host, meta_bytes, cudaMemcpyHostToDevice, st);
     if (e != cudaSuccess)
       return fail(PKV_ERR_CUDA, std::string("cudaMemcpyAsync (step metadata): ") + cudaGetErrorString(e));
+    plan_host = meta_host;
+  }
+  pkv::ShareLaunch share{nullptr, 0, 0};
+  if (pkv::share_on(P) && plan_host) {
+    const int64_t off = pkv::share_plan_offset(n, W);
+    const int32_t* hdr = plan_host + off;
+    if (hdr[0] < 0 || hdr[0] > pkv::share_item_cap(n) || hdr[1] < 0 || hdr[1] > n || hdr[2] < 0 ||
+        hdr[2] > pkv::share_slot_cap(n))
+      return fail(PKV_ERR_INVALID_ARG, "the step metadata's shared-prefix plan is corrupt");
+    share = pkv::ShareLaunch{meta_dev + off, hdr[0], hdr[1]};
   }
   if (n_cow > 0)
     if (int rc = pkv_copy_blocks(pool, cow_pairs, n_cow, k_pool, v_pool, stream)) return rc;
@@ -754,7 +906,7 @@ static int step_launch(pkv_pool* pool, int32_t layer, int32_t n, int32_t W, cons
   const pkv::AppendFuse fuse{k_new, v_new, meta_dev, k_pool, v_pool};
   if (int rc = pkv::launch_decode(*as_pool(pool), layer, q, k_pool, v_pool, meta_dev + n, W,
                                   meta_dev + n + static_cast<int64_t>(n) * W, n, scale, out, workspace, ws_bytes,
-                                  stream, &fuse))
+                                  stream, &fuse, &share))
     return rc;
   if (attn_end) cudaEventRecord(reinterpret_cast<cudaEvent_t>(attn_end), st);
   return PKV_OK;
@@ -782,13 +934,15 @@ int pkv_step_launch_packed(pkv_pool* pool, int32_t layer, int32_t n, int32_t W, 
   const pkv_geometry& g = as_pool(pool)->geo;
   const size_t ab = static_cast<size_t>(pkv::act_size(g.dtype));
   const size_t qb = ab * n * g.H_q * g.d_head, kb = ab * n * g.H_kv * g.d_head;
-  const size_t mb = sizeof(int32_t) * static_cast<size_t>(n) * (W + 2);
+  const size_t mb = sizeof(int32_t) * static_cast<size_t>(pkv::step_meta_ints(*as_pool(pool), n, W));
   if ((off_k | off_v | off_meta) & 15) return fail(PKV_ERR_INVALID_ARG, "offsets must be multiples of 16");
   if (off_k < qb || off_v < off_k + kb || in_bytes < off_v + kb || (off_meta && (off_meta < off_v + kb ||
                                                                                  in_bytes < off_meta + mb)))
     return fail(PKV_ERR_INVALID_ARG, "packed input: q, k_new, v_new (and the metadata) of n rows must fit before "
                                      "off_k, off_v, off_meta and in_bytes");
+  const int32_t* plan_host = meta_host;
   if (off_meta) {  // the metadata travels with the inputs
+    plan_host = reinterpret_cast<const int32_t*>(static_cast<const char*>(in_host) + off_meta);
     meta_host = nullptr;
     meta_dev = reinterpret_cast<int32_t*>(static_cast<char*>(in_dev) + off_meta);
   }
@@ -797,7 +951,7 @@ int pkv_step_launch_packed(pkv_pool* pool, int32_t layer, int32_t n, int32_t W, 
   if (e != cudaSuccess) return fail(PKV_ERR_CUDA, std::string("cudaMemcpyAsync (step input): ") + cudaGetErrorString(e));
   char* d = static_cast<char*>(in_dev);
   if (int rc = step_launch(pool, layer, n, W, cow_pairs, n_cow, d, d + off_k, d + off_v, k_pool, v_pool, scale,
-                           out_dev, meta_host, meta_dev, workspace, ws_bytes, attn_begin, attn_end, stream))
+                           out_dev, meta_host, meta_dev, workspace, ws_bytes, attn_begin, attn_end, stream, plan_host))
     return rc;
   e = cudaMemcpyAsync(out_host, out_dev, qb, cudaMemcpyDeviceToHost, st);
   if (e != cudaSuccess) return fail(PKV_ERR_CUDA, std::string("cudaMemcpyAsync (step result): ") + cudaGetErrorString(e));

@@ -51,6 +51,17 @@ struct DecodeArgs {
   int32_t total_warps;
   int32_t self_plan;           // 1: every CTA plans its own warps from seq_lens (no plan kernel)
   unsigned long long epoch;    // 48-bit tag of this launch (nonzero, unique in the process)
+  // Shared prefixes (all null without one).  share[s] = {kb, items, slot0, stride}: the first kb
+  // table blocks of sequence s are a prefix it shares with other rows of the batch, attended by
+  // the prefix kernel, whose `items` partials for s sit in slots slot0 + i * stride; the decode
+  // kernel attends to the rest and folds those partials in.  share_items: the prefix kernel's
+  // work items, 8 ints each {row_begin, row_end, kb0, kb1, slot_base, 0, 0, 0}.  prior_ml /
+  // prior_o: per (slot, query head) the running max m (base 2) and sum l, and O relative to 2^m.
+  const int4* share;
+  const int32_t* share_items;
+  float* prior_ml;
+  float* prior_o;
+  int64_t prior_slots;  // slots prior_ml / prior_o hold
 };
 
 template <typename T>
@@ -228,5 +239,9 @@ int get_tensor_maps(Pool& P, const void* k, const void* v, CUtensorMap* tk, CUte
 // Fields of DecodeArgs shared by every attention launch.
 int fill_args(const Pool& P, int32_t layer, const void* q, void* out, const int32_t* tables, int32_t W,
               const int32_t* seq_lens, int32_t n_seq, float scale, DecodeArgs* a);
+// The prefix kernel of a decode step with shared prefixes (pkv_prefill.cu): one CTA per (pair
+// of 128-row tiles of the item's rows, KV head, work item); a carries share_items and prior_*.
+int launch_prefix_share(Pool& P, const DecodeArgs& a, const void* q, const void* k_pool, const void* v_pool,
+                        int32_t n_items, int32_t max_members, cudaStream_t st);
 
 }  // namespace pkv

@@ -80,6 +80,34 @@ constexpr int kPlanSmemInts = 8192;  // prefix entries the plan kernel keeps in 
 
 __device__ __forceinline__ int run_total_from(const DecodeArgs& a) { return *const_cast<volatile int32_t*>(a.hdr); }
 
+// The keys of sequence s that this kernel attends to: `len` tokens from table block `kb` on.
+// kb is the shared prefix's block count (share[s].x) when one is given and leaves at least one
+// token, else 0 (an out-of-range value is recorded and ignored); len is the length clamped to
+// the table's capacity [0, W*B], minus the prefix.  `record` reports bad values.
+struct Span {
+  int32_t len, kb;
+};
+__device__ __forceinline__ Span seq_span(const DecodeArgs& a, int s, bool record) {
+  int32_t len = a.seq_lens[s];
+  const int64_t maxlen = static_cast<int64_t>(a.W) * a.B;
+  if (len < 0 || len > maxlen) {
+    if (record) record_error(a.err, DERR_DECODE_LEN, s);
+    len = len < 0 ? 0 : static_cast<int32_t>(maxlen);
+  }
+  int32_t kb = 0;
+  if (a.share) {
+    kb = a.share[s].x;
+    if (kb < 0 || static_cast<int64_t>(kb) * a.B >= len) {
+      if (record && kb != 0) record_error(a.err, DERR_SHARE, s);
+      kb = 0;
+    }
+  }
+  return Span{len - kb * a.B, kb};
+}
+__device__ __forceinline__ int32_t clamped_len(const DecodeArgs& a, int s, bool record) {
+  return seq_span(a, s, record).len;
+}
+
 // One CTA: clamp lengths, tiles per sequence, exclusive prefix, total tile count.
 __global__ void __launch_bounds__(1024) plan_kernel(const DecodeArgs a) {
   // let the attention kernel launch now; it waits for this grid before reading its outputs
@@ -88,14 +116,9 @@ __global__ void __launch_bounds__(1024) plan_kernel(const DecodeArgs a) {
   const int tid = threadIdx.x;
   const int per = (a.n_seq + blockDim.x - 1) / blockDim.x;
   const int s0 = min(a.n_seq, tid * per), s1 = min(a.n_seq, s0 + per);
-  const int64_t maxlen = static_cast<int64_t>(a.W) * a.B;
   int32_t local = 0;
   for (int s = s0; s < s1; ++s) {
-    int32_t len = a.seq_lens[s];
-    if (len < 0 || len > maxlen) {
-      record_error(a.err, DERR_DECODE_LEN, s);
-      len = len < 0 ? 0 : static_cast<int32_t>(maxlen);
-    }
+    const int32_t len = seq_span(a, s, true).len;
     a.lens_c[s] = len;
     local += (len + TILE - 1) / TILE;
   }
@@ -166,16 +189,6 @@ __global__ void __launch_bounds__(1024) plan_kernel(const DecodeArgs a) {
 // Sequences up to which every CTA of the attention kernel plans its own warps (no plan kernel).
 constexpr int kSelfPlanMaxSeqs = 4096;
 
-// Length of sequence s clamped to the table's capacity [0, W*B]; `record` reports a bad one.
-__device__ __forceinline__ int32_t clamped_len(const DecodeArgs& a, int s, bool record) {
-  int32_t len = a.seq_lens[s];
-  const int64_t maxlen = static_cast<int64_t>(a.W) * a.B;
-  if (len < 0 || len > maxlen) {
-    if (record) record_error(a.err, DERR_DECODE_LEN, s);
-    len = len < 0 ? 0 : static_cast<int32_t>(maxlen);
-  }
-  return len;
-}
 
 // The plan kernel's work for this CTA's NW warps only, from the lengths: tiles per
 // sequence, their block-wide exclusive prefix, the total, and each warp's first tile
@@ -336,6 +349,55 @@ __device__ __forceinline__ void store_group(TO* out, const float4 (&acc)[D / 16]
   }
 }
 
+// Fold the shared-prefix partials of sequence s into a lane's part of head block nb of
+// KV head g before the output is written: acc (the lane's O^T fragments, in store_group's
+// layout) is relative to 2^M with sum L per head of the lane (M0, L0: head h0; M1, L1: h0 + 1),
+// and so is the result ("Chunked prefill mechanics" merge rule: m = max, l and O rescaled by
+// 2^(m_part - m)).  Nothing to fold for a sequence without a valid shared prefix.
+template <int D, bool F8>
+__device__ __forceinline__ void fold_prior(const DecodeArgs& a, int s, int g, int nb, int lane,
+                                           float4 (&acc)[D / 16], float& M0, float& M1, float& L0, float& L1) {
+  if (!a.share || seq_span(a, s, false).kb == 0) return;
+  const int4 sh = a.share[s];
+  if (sh.y < 1 || sh.z < 0 || sh.w < 0 ||
+      static_cast<int64_t>(sh.z) + static_cast<int64_t>(sh.y - 1) * sh.w >= a.prior_slots) {
+    if (lane == 0 && nb == 0) record_error(a.err, DERR_SHARE, s);
+    return;
+  }
+  const int h0 = 2 * (lane & 3), trow = lane >> 2;
+  const int hl = GPAD * nb + h0;  // the lane's first head within the group
+  const bool live0 = hl < a.G, live1 = hl + 1 < a.G;
+  const int64_t hq = static_cast<int64_t>(g) * a.G + hl;
+#pragma unroll 1
+  for (int it = 0; it < sh.y; ++it) {
+    const int64_t row = (static_cast<int64_t>(sh.z) + static_cast<int64_t>(it) * sh.w) * a.H_q + hq;
+    const float* ml = a.prior_ml + 2 * row;
+    const float* o0 = a.prior_o + row * D;
+    const float m0 = live0 ? __ldcg(ml) : -INFINITY, l0 = live0 ? __ldcg(ml + 1) : 0.f;
+    const float m1 = live1 ? __ldcg(ml + 2) : -INFINITY, l1 = live1 ? __ldcg(ml + 3) : 0.f;
+    const float n0 = fmaxf(M0, m0), n1 = fmaxf(M1, m1);
+    const float r0 = exp2f(M0 - n0), r1 = exp2f(M1 - n1);
+    const float e0 = live0 ? exp2f(m0 - n0) : 0.f, e1 = live1 ? exp2f(m1 - n1) : 0.f;
+#pragma unroll
+    for (int c = 0; c < D / 16; ++c) {
+      // store_group's element positions: 16-bit pools d = 16c + trow (x, y) and + 8 (z, w);
+      // FP8 pools d = 16 trow + 2c (x, y) and + 1 (z, w); x, z head h0 and y, w head h0 + 1
+      const int da = F8 ? 16 * trow + 2 * c : 16 * c + trow;
+      const int db = F8 ? da + 1 : da + 8;
+      const float pa0 = live0 ? __ldcg(o0 + da) : 0.f, pb0 = live0 ? __ldcg(o0 + db) : 0.f;
+      const float pa1 = live1 ? __ldcg(o0 + D + da) : 0.f, pb1 = live1 ? __ldcg(o0 + D + db) : 0.f;
+      acc[c].x = acc[c].x * r0 + pa0 * e0;
+      acc[c].y = acc[c].y * r1 + pa1 * e1;
+      acc[c].z = acc[c].z * r0 + pb0 * e0;
+      acc[c].w = acc[c].w * r1 + pb1 * e1;
+    }
+    L0 = L0 * r0 + l0 * e0;
+    L1 = L1 * r1 + l1 * e1;
+    M0 = n0;
+    M1 = n1;
+  }
+}
+
 // Merge the partials of one split pair (contributing warps wa..wb) and write its
 // G output rows.  Run by one whole warp; lane l owns float4 l of every d-chunk of
 // each head block, merged one block at a time.  Partials are read through L2
@@ -387,6 +449,7 @@ __device__ __forceinline__ void merge_pair(const DecodeArgs& a, int s, int g, in
       M0 = n0;
       M1 = n1;
     }
+    fold_prior<D, F8>(a, s, g, nb, lane, acc, M0, M1, L0, L1);
     const float i0 = a.v_mul / L0, i1 = a.v_mul / L1;
     store_group<TO, D, F8>(out + GPAD * nb * D, acc, i0, i1, lane, a.G - GPAD * nb);
   }
@@ -480,12 +543,13 @@ __global__ void __launch_bounds__(NW * 32) decode_tc_kernel(const __grid_constan
       const int tok0 = jj * TILE;
       const int lb = tok0 / a.B;
       const int sub = tok0 - lb * a.B;
-      int blk = a.tables[static_cast<int64_t>(ss) * a.W + lb];
+      const Span sp = seq_span(a, ss, false);
+      int blk = a.tables[static_cast<int64_t>(ss) * a.W + sp.kb + lb];
       if (blk < 0 || blk >= a.num_blocks) {
         record_error(a.err, DERR_DECODE_BLOCK, blk);
         blk = 0;
       }
-      const int valid = min(TILE, clamped_len(a, ss, false) - tok0);
+      const int valid = min(TILE, sp.len - tok0);
       int flags = valid;
       if (jj == 0) flags |= F_FIRST;
       if (jj == nn - 1) flags |= F_LAST;
@@ -748,10 +812,12 @@ __global__ void __launch_bounds__(NW * 32) decode_tc_kernel(const __grid_constan
 #pragma unroll
         for (int nb = 0; nb < NB; ++nb) {
           if (GPAD * nb >= a.G) break;
-          const float i0 = a.v_mul / Ls[nb][0], i1 = a.v_mul / Ls[nb][1];
           float4 acc4[C::NKC];
 #pragma unroll
           for (int c = 0; c < C::NKC; ++c) acc4[c] = make_float4(o[nb][c][0], o[nb][c][1], o[nb][c][2], o[nb][c][3]);
+          float M0 = m[nb][0], M1 = m[nb][1], L0 = Ls[nb][0], L1 = Ls[nb][1];
+          fold_prior<D, F8>(a, s, g, nb, lane, acc4, M0, M1, L0, L1);
+          const float i0 = a.v_mul / L0, i1 = a.v_mul / L1;
           store_group<TA, D, F8>(out + GPAD * nb * D, acc4, i0, i1, lane, a.G - GPAD * nb);
         }
       } else {
@@ -983,11 +1049,11 @@ int tc_grid(const Pool& P, int* grid, int* warps, int* smem) {
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct WsLayout {
-  size_t prefix, lens, counters, wstart, partials, total;
+  size_t prefix, lens, counters, wstart, partials, prior_ml, prior_o, total;
 };
 
-WsLayout ws_layout(int n_seq, int H_kv, int64_t total_warps, int D, int G) {
-  (void)H_kv;
+// n_prior > 0: room for that many shared-prefix partial slots (m, l and O per query head) at the end.
+WsLayout ws_layout(int n_seq, int H_kv, int64_t total_warps, int D, int G, int64_t n_prior = 0) {
   WsLayout w;
   w.prefix = kHdrBytes;
   w.lens = w.prefix + align256(sizeof(int32_t) * (n_seq + 1));
@@ -996,7 +1062,9 @@ WsLayout ws_layout(int n_seq, int H_kv, int64_t total_warps, int D, int G) {
   w.partials = w.wstart + align256(sizeof(int4) * total_warps);
   const int nb = G > GPAD ? 2 : 1;  // head blocks (the kernel's TcCfg::PSTRIDE)
   const int pstride = nb * (D / 16) * 32 * 4 + 2 * GPAD * nb;
-  w.total = w.partials + align256(sizeof(float) * total_warps * 2 * pstride);
+  w.prior_ml = w.partials + align256(sizeof(float) * total_warps * 2 * pstride);
+  w.prior_o = w.prior_ml + align256(sizeof(float) * 2 * n_prior * H_kv * G);
+  w.total = w.prior_o + align256(sizeof(float) * static_cast<size_t>(D) * n_prior * H_kv * G);
   return w;
 }
 
@@ -1209,6 +1277,11 @@ int get_tensor_maps(Pool& P, const void* k, const void* v, CUtensorMap* tk, CUte
   return PKV_OK;
 }
 
+// Shared-prefix partial slots a workspace holds for n_seq sequences (0 with sharing off).
+int64_t share_slots(const Pool& P, int32_t n_seq) {
+  return share_on(P) && share_geometry_ok(P.geo) ? share_slot_cap(n_seq) : 0;
+}
+
 int decode_workspace_bytes(const Pool& P, int32_t n_seq, size_t* bytes) {
   int64_t warps_total = 0;
   if (tc_eligible(P)) {
@@ -1216,13 +1289,14 @@ int decode_workspace_bytes(const Pool& P, int32_t n_seq, size_t* bytes) {
     if (int rc = tc_grid(P, &grid, &nw, &smem)) return rc;
     warps_total = static_cast<int64_t>(grid) * nw;
   }
-  *bytes = ws_layout(n_seq, P.geo.H_kv, warps_total, P.geo.d_head, P.geo.H_q / P.geo.H_kv).total;
+  *bytes = ws_layout(n_seq, P.geo.H_kv, warps_total, P.geo.d_head, P.geo.H_q / P.geo.H_kv, share_slots(P, n_seq))
+               .total;
   return PKV_OK;
 }
 
 int launch_decode(Pool& P, int32_t layer, const void* q, const void* k_pool, const void* v_pool,
                   const int32_t* tables, int32_t W, const int32_t* seq_lens, int32_t n_seq, float scale, void* out,
-                  void* ws, size_t ws_bytes, void* stream, const AppendFuse* fuse) {
+                  void* ws, size_t ws_bytes, void* stream, const AppendFuse* fuse, const ShareLaunch* share) {
   const auto& g = P.geo;
   const int G = g.H_q / g.H_kv;
   if (G > SIMT_GMAX || (G > GPAD && g.d_head > 128))
@@ -1238,7 +1312,9 @@ int launch_decode(Pool& P, int32_t layer, const void* q, const void* k_pool, con
   if (tc_eligible(P)) {
     int grid = 0, nw = 0, smem = 0;
     if (int rc = tc_grid(P, &grid, &nw, &smem)) return rc;
-    const WsLayout L = ws_layout(n_seq, g.H_kv, static_cast<int64_t>(grid) * nw, g.d_head, G);
+    const bool shared = share && share->n_items > 0;
+    const WsLayout L =
+        ws_layout(n_seq, g.H_kv, static_cast<int64_t>(grid) * nw, g.d_head, G, shared ? share_slot_cap(n_seq) : 0);
     if (ws_bytes < L.total) return fail(PKV_ERR_INVALID_ARG, "workspace too small: need " + std::to_string(L.total));
     if ((reinterpret_cast<uintptr_t>(q) & 15) || (reinterpret_cast<uintptr_t>(out) & 15))
       return fail(PKV_ERR_INVALID_ARG, "q and out must be 16-byte aligned");
@@ -1253,6 +1329,16 @@ int launch_decode(Pool& P, int32_t layer, const void* q, const void* k_pool, con
     a.partials = reinterpret_cast<float*>(w + L.partials);
     a.total_warps = grid * nw;
     CUtensorMap maps[2] = {tk, tv};
+    if (shared) {  // the shared blocks once per run of rows, before the step's append and decode
+      if (reinterpret_cast<uintptr_t>(share->plan_dev) & 15)
+        return fail(PKV_ERR_INVALID_ARG, "the shared-prefix plan must be 16-byte aligned");
+      a.share = reinterpret_cast<const int4*>(share->plan_dev + 4);
+      a.share_items = share->plan_dev + 4 + 4 * static_cast<int64_t>(n_seq);
+      a.prior_ml = reinterpret_cast<float*>(w + L.prior_ml);
+      a.prior_o = reinterpret_cast<float*>(w + L.prior_o);
+      a.prior_slots = share_slot_cap(n_seq);
+      if (int rc = launch_prefix_share(P, a, q, k_pool, v_pool, share->n_items, share->max_members, st)) return rc;
+    }
     bool after_append = false;
     if (fuse) {  // the step's append kernel first, letting the attention launch start under it
       after_append = n_seq <= kSelfPlanMaxSeqs;
@@ -1263,6 +1349,8 @@ int launch_decode(Pool& P, int32_t layer, const void* q, const void* k_pool, con
     return launch_tc_sequence(a, maps, tc_kernel_for(P, &smem), grid, nw, smem, st, after_append);
   }
 
+  if (share && share->n_items > 0)
+    return fail(PKV_ERR_UNSUPPORTED, "shared prefixes need the tensor-core decode path");
   if (fuse)
     if (int rc = launch_append(P, layer, fuse->k_new, fuse->v_new, fuse->slots, n_seq, fuse->k_pool, fuse->v_pool,
                                stream))

@@ -62,6 +62,9 @@ struct Pool {
   int32_t swap_engine = 0;  // 0 SM kernel, 1 copy engine
   float k_scale = 1.f, v_scale = 1.f;  // FP8 pools: stored code * scale
   int32_t n_prefix_caches = 0;         // live radix prefix caches holding references
+  // shared prefixes in decode steps (pkv_pool_set_prefix_sharing): off while share_min_members == 0
+  int32_t share_min_members = 0, share_min_blocks = 1, share_ctas = 0;
+  std::vector<int32_t> share_scratch;  // planner scratch
 
   std::mutex tmap_mu;
   TensorMaps* tmaps = nullptr;
@@ -71,6 +74,38 @@ struct Pool {
 inline int64_t elem_size(int32_t dtype) { return dtype == PKV_F32 ? 4 : (dtype == PKV_E4M3 ? 1 : 2); }
 // Bytes of one activation element (q, out, new keys/values): bf16 around an FP8 pool.
 inline int64_t act_size(int32_t dtype) { return dtype == PKV_E4M3 ? 2 : elem_size(dtype); }
+
+// ------------------------------------------------------------------ shared prefixes
+//
+// A decode step whose batch holds runs of rows that share their first table blocks (branches
+// forked from one parent: "Zero-copy deliberation via copy-on-write branching") attends to the
+// shared blocks once for the whole run, in the prefix kernel, and to each row's own blocks in the
+// decode kernel, which folds the prefix kernel's partials in.  The plan (int32), made on the host
+// with the step's metadata and copied with it: a header {n_items, max_members, n_slots, 0}; per
+// batch row {kb, items, slot0, stride} (the row's first kb blocks are shared; its partials sit in
+// slots slot0 + i * stride, i < items); then up to share_item_cap(n) work items of 8 ints
+// {row_begin, row_end, kb0, kb1, slot_base, 0, 0, 0}: the rows, the range of row_begin's table
+// blocks, and the slot of row_begin's partial.
+inline int64_t share_item_cap(int64_t n) { return n + 256; }
+inline int64_t share_slot_cap(int64_t n) { return 2 * n + 1024; }
+inline int64_t share_plan_ints(int64_t n) { return 4 + 4 * n + 8 * share_item_cap(n); }
+// The geometry the prefix kernel takes (tcgen05, d_head 128, up to 16 query heads per KV head).
+inline bool share_geometry_ok(const pkv_geometry& g) {
+  const int64_t G = g.H_q / g.H_kv;
+  return (g.dtype == PKV_BF16 || g.dtype == PKV_F16 || g.dtype == PKV_E4M3) && g.d_head == 128 && G <= 16 &&
+         g.block_size % 16 == 0 && g.num_blocks * g.L * g.H_kv * g.block_size < (int64_t(1) << 31);
+}
+inline bool share_on(const Pool& P) { return P.share_min_members > 0; }
+// Step metadata: slots [n], tables [n][W], lens [n], then (sharing on) the plan from a 16-byte boundary.
+inline int64_t share_plan_offset(int64_t n, int64_t W) { return (n * (W + 2) + 3) / 4 * 4; }
+inline int64_t step_meta_ints(const Pool& P, int64_t n, int64_t W) {
+  return share_on(P) ? share_plan_offset(n, W) + share_plan_ints(n) : n * (W + 2);
+}
+// The shared-prefix part of a decode launch: the plan on the device and its header's counts.
+struct ShareLaunch {
+  const int32_t* plan_dev;
+  int32_t n_items, max_members;
+};
 
 // ------------------------------------------------------------------ device side
 
@@ -110,7 +145,8 @@ struct AppendFuse {
 };
 int launch_decode(Pool& P, int32_t layer, const void* q, const void* k_pool, const void* v_pool,
                   const int32_t* tables, int32_t W, const int32_t* seq_lens, int32_t n_seq, float scale, void* out,
-                  void* ws, size_t ws_bytes, void* stream, const AppendFuse* fuse = nullptr);
+                  void* ws, size_t ws_bytes, void* stream, const AppendFuse* fuse = nullptr,
+                  const ShareLaunch* share = nullptr);
 int launch_prefill(Pool& P, int32_t layer, const void* q, const int32_t* q_off, int32_t n_tok, int32_t max_q,
                    const void* k_pool, const void* v_pool, const int32_t* tables, int32_t W, const int32_t* seq_lens,
                    int32_t n_seq, float scale, void* out, void* stream);
@@ -125,6 +161,7 @@ enum DeviceErr : int32_t {
   DERR_DECODE_TIMEOUT = 4,  // a bounded mbarrier wait gave up
   DERR_SELFTEST_TIMEOUT = 5,  // the self-test's wait gave up (expected)
   DERR_PREFILL_CHUNK = 6,     // a chunk longer than max_q
+  DERR_SHARE = 7,             // a shared-prefix plan entry out of range
 };
 
 }  // namespace pkv

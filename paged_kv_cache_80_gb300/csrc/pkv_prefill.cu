@@ -377,7 +377,12 @@ __device__ __forceinline__ uint32_t bf16x2_rn_f16x2(uint32_t w) {
 
 // T: the type of q and out; KV8: an E4M3 pool, whose products run on binary16 operands (the
 // codes convert exactly; q is rounded to binary16 as on the FP8 decode path).
-template <typename T, bool KV8>
+// SH: the shared-prefix form for decode.  CTA z takes work item z of a.share_items: the decode
+// queries of batch rows [rb, re) (rows that share their first table blocks), every one of them
+// against all keys of blocks [kb0, kb1) of row rb's table (no causal edge: the prefix precedes
+// every query); the epilogue leaves the partial (m, l, unnormalised O) of each (row, head) in
+// slot slot_base + (row - rb) of a.prior_ml / a.prior_o for the decode kernel to fold in.
+template <typename T, bool KV8, bool SH = false>
 __global__ void __launch_bounds__(UM_THREADS, 1) prefill_umma_kernel(const __grid_constant__ CUtensorMap tmq,
                                                                       const __grid_constant__ CUtensorMap tmk,
                                                                       const __grid_constant__ CUtensorMap tmv3,
@@ -391,21 +396,36 @@ __global__ void __launch_bounds__(UM_THREADS, 1) prefill_umma_kernel(const __gri
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int G = a.G;
   const int QB = 128 / G;  // queries per tile
-  const int qbeg = q_off[s];
-  const int Cs = q_off[s + 1] - qbeg;
+  const int32_t* item = SH ? a.share_items + 8 * static_cast<int64_t>(s) : nullptr;
+  const int qbeg = SH ? item[0] : q_off[s];
+  const int Cs = SH ? item[1] - item[0] : q_off[s + 1] - qbeg;
   const int i0 = qb * 2 * QB;  // first query of tile A
   if (qb == gridDim.x - 1 && tid == 0 && g == 0 && Cs > i0 + 2 * QB) record_error(a.err, DERR_PREFILL_CHUNK, s);
   if (i0 >= Cs) return;  // uniform over the CTA, before any barrier or TMEM use
-  const int len = a.seq_lens[s];
-  if (Cs < 0 || len < Cs || len > static_cast<int64_t>(a.W) * a.B) {
-    if (tid == 0 && qb == 0 && g == 0) record_error(a.err, DERR_DECODE_LEN, s);
-    return;
+  int nkeys, P = 0;
+  int64_t trow0;  // the first table entry of the keys
+  if constexpr (SH) {
+    const int kb0 = item[2], kb1 = item[3];
+    if (qbeg < 0 || item[1] > a.n_seq || kb0 < 0 || kb1 <= kb0 || kb1 > a.W || item[4] < 0 ||
+        static_cast<int64_t>(item[4]) + Cs > a.prior_slots) {
+      if (tid == 0 && qb == 0 && g == 0) record_error(a.err, DERR_SHARE, s);
+      return;
+    }
+    nkeys = (kb1 - kb0) * a.B;
+    trow0 = static_cast<int64_t>(qbeg) * a.W + kb0;
+  } else {
+    const int len = a.seq_lens[s];
+    if (Cs < 0 || len < Cs || len > static_cast<int64_t>(a.W) * a.B) {
+      if (tid == 0 && qb == 0 && g == 0) record_error(a.err, DERR_DECODE_LEN, s);
+      return;
+    }
+    P = len - Cs;
+    nkeys = P + min(Cs, i0 + (i0 + QB < Cs ? 2 : 1) * QB);  // the last query's position + 1
+    trow0 = static_cast<int64_t>(s) * a.W;
   }
   const int nq = i0 + QB < Cs ? 2 : 1;  // tiles with rows in the chunk
   const int i1 = min(Cs, i0 + nq * QB);
-  const int P = len - Cs;
-  const int pmax = P + i1 - 1;
-  const int nkeys = pmax + 1;
+  const int pmax = nkeys - 1;
   const int nt = (nkeys + UM_KEYS - 1) / UM_KEYS;
   const bool tail = nkeys < nt * UM_KEYS;  // the last tile has keys past the sequence end
 
@@ -501,7 +521,7 @@ __global__ void __launch_bounds__(UM_THREADS, 1) prefill_umma_kernel(const __gri
         }
       }
       auto block_at = [&](int lb) -> int {
-        int blk = a.tables[static_cast<int64_t>(s) * a.W + lb];
+        int blk = a.tables[trow0 + lb];
         if (blk < 0 || blk >= a.num_blocks) {
           record_error(a.err, DERR_DECODE_BLOCK, blk);
           blk = 0;
@@ -686,7 +706,7 @@ __global__ void __launch_bounds__(UM_THREADS, 1) prefill_umma_kernel(const __gri
       const uint32_t o_addr = lane_addr + 256 + 128 * X;
       const int qi = i0 + X * QB + r / G, h = r % G;
       const bool valid = r < QB * G && qi < i1;
-      const int lim = valid ? P + qi : pmax;  // last visible key
+      const int lim = (valid && !SH) ? P + qi : pmax;  // last visible key
       float m = -INFINITY, l = 0.f;
       bool ok = true;
       // E4M3 pools: this warpgroup converts a staged tile of codes (K or V of key tile c) into
@@ -818,7 +838,25 @@ __global__ void __launch_bounds__(UM_THREADS, 1) prefill_umma_kernel(const __gri
         if (ok && conv_v && j + 2 < nt) ok = convert(j + 2, false);
       }
       if (ok) ok = __all_sync(0xffffffffu, wait(o_done + 8 * (2 * X + ((nt - 1) & 1)), ((nt - 1) >> 1) & 1, 1000));
-      if (ok) {
+      if (ok && SH) {
+        // the partial of (row qbeg + qi, head g G + h): m, l and O relative to 2^m, unscaled
+        tc_fence_after();
+        const int64_t row = (static_cast<int64_t>(item[4]) + qi) * a.H_q + g * G + h;
+        float4* dst = reinterpret_cast<float4*>(a.prior_o + row * D);
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(o_addr + 32 * c, o);
+          tmem_ld_wait();
+          if (valid) {
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+              dst[8 * c + v] = make_float4(__uint_as_float(o[4 * v]), __uint_as_float(o[4 * v + 1]),
+                                           __uint_as_float(o[4 * v + 2]), __uint_as_float(o[4 * v + 3]));
+          }
+        }
+        if (valid) *reinterpret_cast<float2*>(a.prior_ml + 2 * row) = make_float2(m, l);
+      } else if (ok) {
         tc_fence_after();
         const float inv = a.v_mul / l;  // v_scale of an E4M3 pool, else 1
         T* out = static_cast<T*>(a.out) + (static_cast<int64_t>(qbeg + qi) * a.H_q + g * G + h) * D;
@@ -900,7 +938,69 @@ void simt_prefill_t(const DecodeArgs& a, const int32_t* q_off, const void* kp, c
 #undef PKV_PF_SIMT
 }
 
+// TMA descriptors of the tcgen05 kernel: q as {d, H_q, n_tok} (a box of {64, G, 128 / G} lands as
+// 128 (query, head) rows of 128 bytes), K as the decode kernel's 16-token slabs, V as
+// {64, rows, 2 d chunks} (a {64, 16, 2} box is one 16-token slab of both chunks, 4 KB; E4M3
+// pools copy slabs of codes with the 2-D map and convert them in the kernel).
+int umma_maps(Pool& P, const void* q, int32_t n_tok, const void* k_pool, const void* v_pool, bool kv8,
+              CUtensorMap* maps) {
+  const auto& g = P.geo;
+  const int G = g.H_q / g.H_kv;
+  if (int rc = get_tensor_maps(P, k_pool, v_pool, &maps[1], &maps[2])) return rc;
+  if (!kv8) {
+    cuuint64_t vd[3] = {64, static_cast<cuuint64_t>(g.num_blocks) * g.L * g.H_kv * g.block_size, 2};
+    cuuint64_t vs[2] = {256, 128};
+    cuuint32_t vb[3] = {64, TILE, 2};
+    cuuint32_t ve[3] = {1, 1, 1};
+    const CUtensorMapDataType vt =
+        g.dtype == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    CUresult r = encode_fn()(&maps[2], vt, 3, const_cast<void*>(v_pool), vd, vs, vb, ve, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled (v slabs) failed: " + std::to_string(r));
+  }
+  const int QB = 128 / G;
+  const CUtensorMapDataType dt =
+      g.dtype == PKV_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;  // q: bf16 for E4M3
+  cuuint64_t dims[3] = {128, static_cast<cuuint64_t>(g.H_q), static_cast<cuuint64_t>(std::max(n_tok, 1))};
+  cuuint64_t strides[2] = {256, static_cast<cuuint64_t>(g.H_q) * 256};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(G), static_cast<cuuint32_t>(QB)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = encode_fn()(&maps[0], dt, 3, const_cast<void*>(q), dims, strides, box, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled (q) failed: " + std::to_string(r));
+  return PKV_OK;
+}
+
 }  // namespace
+
+int launch_prefix_share(Pool& P, const DecodeArgs& a, const void* q, const void* k_pool, const void* v_pool,
+                        int32_t n_items, int32_t max_members, cudaStream_t st) {
+  const auto& g = P.geo;
+  const int G = g.H_q / g.H_kv;
+  if (n_items <= 0) return PKV_OK;
+  if (!share_geometry_ok(g) || !encode_fn())
+    return fail(PKV_ERR_UNSUPPORTED, "shared prefixes need a tensor-core pool with d_head 128");
+  const bool kv8 = g.dtype == PKV_E4M3;
+  CUtensorMap maps[3];
+  if (int rc = umma_maps(P, q, a.n_seq, k_pool, v_pool, kv8, maps)) return rc;
+  const void* k = kv8 ? reinterpret_cast<const void*>(&prefill_umma_kernel<__nv_bfloat16, true, true>)
+                  : g.dtype == PKV_BF16 ? reinterpret_cast<const void*>(&prefill_umma_kernel<__nv_bfloat16, false, true>)
+                                        : reinterpret_cast<const void*>(&prefill_umma_kernel<__half, false, true>);
+  const int smem = um_smem(kv8);
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return fail(PKV_ERR_CUDA, std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e));
+  const int QB = 128 / G;
+  dim3 grid((max_members + 2 * QB - 1) / (2 * QB), g.H_kv, n_items);
+  DecodeArgs args_copy = a;
+  const int32_t* no_off = nullptr;
+  void* args[] = {&maps[0], &maps[1], &maps[2], &args_copy, const_cast<int32_t**>(&no_off)};
+  e = cudaLaunchKernel(k, grid, dim3(UM_THREADS), args, smem, st);
+  if (e != cudaSuccess) return fail(PKV_ERR_CUDA, std::string("shared-prefix launch: ") + cudaGetErrorString(e));
+  count_launch();
+  return PKV_OK;
+}
 
 int launch_prefill(Pool& P, int32_t layer, const void* q, const int32_t* q_off, int32_t n_tok, int32_t max_q,
                    const void* k_pool, const void* v_pool, const int32_t* tables, int32_t W, const int32_t* seq_lens,
@@ -922,39 +1022,14 @@ int launch_prefill(Pool& P, int32_t layer, const void* q, const int32_t* q_off, 
     if ((reinterpret_cast<uintptr_t>(q) & 15) || (reinterpret_cast<uintptr_t>(out) & 15))
       return fail(PKV_ERR_INVALID_ARG, "q and out must be 16-byte aligned");
     CUtensorMap maps[3];
-    if (int rc = get_tensor_maps(P, k_pool, v_pool, &maps[1], &maps[2])) return rc;
-    // V as {64, rows, 2 d chunks}: a {64, 16, 2} box is one 16-token slab, both chunks, 4 KB
-    // (E4M3 pools copy slabs of codes with the 2-D maps and convert them in the kernel)
-    if (!tc8) {
-      cuuint64_t vd[3] = {64, static_cast<cuuint64_t>(g.num_blocks) * g.L * g.H_kv * g.block_size, 2};
-      cuuint64_t vs[2] = {256, 128};
-      cuuint32_t vb[3] = {64, TILE, 2};
-      cuuint32_t ve[3] = {1, 1, 1};
-      const CUtensorMapDataType vt =
-          g.dtype == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-      CUresult r = encode_fn()(&maps[2], vt, 3, const_cast<void*>(v_pool), vd, vs, vb, ve, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-      if (r != CUDA_SUCCESS) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled (v slabs) failed: " + std::to_string(r));
-    }
-    // q as {d, H_q, n_tok}: a box of {64, G, 128 / G} lands as 128 (query, head) rows of 128 bytes
-    const int QB = 128 / G;
-    const CUtensorMapDataType dt =
-        g.dtype == PKV_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;  // q: bf16 for E4M3
-    cuuint64_t dims[3] = {128, static_cast<cuuint64_t>(g.H_q), static_cast<cuuint64_t>(std::max(n_tok, 1))};
-    cuuint64_t strides[2] = {256, static_cast<cuuint64_t>(g.H_q) * 256};
-    cuuint32_t box[3] = {64, static_cast<cuuint32_t>(G), static_cast<cuuint32_t>(QB)};
-    cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = encode_fn()(&maps[0], dt, 3, const_cast<void*>(q), dims, strides, box, estr,
-                             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled (q) failed: " + std::to_string(r));
+    if (int rc = umma_maps(P, q, n_tok, k_pool, v_pool, tc8, maps)) return rc;
     const void* k = tc8 ? reinterpret_cast<const void*>(&prefill_umma_kernel<__nv_bfloat16, true>)
                     : g.dtype == PKV_BF16 ? reinterpret_cast<const void*>(&prefill_umma_kernel<__nv_bfloat16, false>)
                                           : reinterpret_cast<const void*>(&prefill_umma_kernel<__half, false>);
     const int smem = um_smem(tc8);
     e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return fail(PKV_ERR_CUDA, std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e));
+    const int QB = 128 / G;
     dim3 grid((max_q + 2 * QB - 1) / (2 * QB), g.H_kv, n_seq);
     void* args[] = {&maps[0], &maps[1], &maps[2], &a, const_cast<int32_t**>(&q_off)};
     e = cudaLaunchKernel(k, grid, dim3(UM_THREADS), args, smem, st);
