@@ -54,14 +54,18 @@ struct DecodeArgs {
   // Shared prefixes (all null without one).  share[s] = {kb, items, slot0, stride}: the first kb
   // table blocks of sequence s are a prefix it shares with other rows of the batch, attended by
   // the prefix kernel, whose `items` partials for s sit in slots slot0 + i * stride; the decode
-  // kernel attends to the rest and folds those partials in.  share_items: the prefix kernel's
-  // work items, 8 ints each {row_begin, row_end, kb0, kb1, slot_base, 0, 0, 0}.  prior_ml /
-  // prior_o: per (slot, query head) the running max m (base 2) and sum l, and O relative to 2^m.
+  // kernel attends to the rest and leaves its partial of such a row in sfx_ml / sfx_o (row s)
+  // instead of writing out; the combine kernel merges the two into out.  share_items: the
+  // prefix kernel's work items, 8 ints each {row_begin, row_end, kb0, kb1, slot_base, 0, 0, 0}.
+  // Partials: per (slot or row, query head) the running max m (base 2) and sum l, and O
+  // relative to 2^m.
   const int4* share;
   const int32_t* share_items;
   float* prior_ml;
   float* prior_o;
   int64_t prior_slots;  // slots prior_ml / prior_o hold
+  float* sfx_ml;
+  float* sfx_o;
 };
 
 template <typename T>

@@ -349,53 +349,40 @@ __device__ __forceinline__ void store_group(TO* out, const float4 (&acc)[D / 16]
   }
 }
 
-// Fold the shared-prefix partials of sequence s into a lane's part of head block nb of
-// KV head g before the output is written: acc (the lane's O^T fragments, in store_group's
-// layout) is relative to 2^M with sum L per head of the lane (M0, L0: head h0; M1, L1: h0 + 1),
-// and so is the result ("Chunked prefill mechanics" merge rule: m = max, l and O rescaled by
-// 2^(m_part - m)).  Nothing to fold for a sequence without a valid shared prefix.
+// A row with a shared prefix (share[s].x blocks attended by the prefix kernel): the decode
+// kernel's part of its attention, head block nb of KV head g, is left as a partial for the
+// combine kernel -- acc (O^T fragments in store_group's element layout, relative to 2^M) and
+// (M, L) per head of the lane (M0, L0: head h0; M1, L1: h0 + 1).  Returns false, writing
+// nothing, for a row without one.
 template <int D, bool F8>
-__device__ __forceinline__ void fold_prior(const DecodeArgs& a, int s, int g, int nb, int lane,
-                                           float4 (&acc)[D / 16], float& M0, float& M1, float& L0, float& L1) {
-  if (!a.share || seq_span(a, s, false).kb == 0) return;
-  const int4 sh = a.share[s];
-  if (sh.y < 1 || sh.z < 0 || sh.w < 0 ||
-      static_cast<int64_t>(sh.z) + static_cast<int64_t>(sh.y - 1) * sh.w >= a.prior_slots) {
-    if (lane == 0 && nb == 0) record_error(a.err, DERR_SHARE, s);
-    return;
-  }
+__device__ __forceinline__ bool leave_partial(const DecodeArgs& a, int s, int g, int nb, int lane,
+                                              const float4 (&acc)[D / 16], float M0, float M1, float L0, float L1) {
+  if (!a.share || seq_span(a, s, false).kb == 0) return false;
   const int h0 = 2 * (lane & 3), trow = lane >> 2;
   const int hl = GPAD * nb + h0;  // the lane's first head within the group
   const bool live0 = hl < a.G, live1 = hl + 1 < a.G;
-  const int64_t hq = static_cast<int64_t>(g) * a.G + hl;
-#pragma unroll 1
-  for (int it = 0; it < sh.y; ++it) {
-    const int64_t row = (static_cast<int64_t>(sh.z) + static_cast<int64_t>(it) * sh.w) * a.H_q + hq;
-    const float* ml = a.prior_ml + 2 * row;
-    const float* o0 = a.prior_o + row * D;
-    const float m0 = live0 ? __ldcg(ml) : -INFINITY, l0 = live0 ? __ldcg(ml + 1) : 0.f;
-    const float m1 = live1 ? __ldcg(ml + 2) : -INFINITY, l1 = live1 ? __ldcg(ml + 3) : 0.f;
-    const float n0 = fmaxf(M0, m0), n1 = fmaxf(M1, m1);
-    const float r0 = exp2f(M0 - n0), r1 = exp2f(M1 - n1);
-    const float e0 = live0 ? exp2f(m0 - n0) : 0.f, e1 = live1 ? exp2f(m1 - n1) : 0.f;
+  const int64_t row = static_cast<int64_t>(s) * a.H_q + static_cast<int64_t>(g) * a.G + hl;
+  float* o0 = a.sfx_o + row * D;
 #pragma unroll
-    for (int c = 0; c < D / 16; ++c) {
-      // store_group's element positions: 16-bit pools d = 16c + trow (x, y) and + 8 (z, w);
-      // FP8 pools d = 16 trow + 2c (x, y) and + 1 (z, w); x, z head h0 and y, w head h0 + 1
-      const int da = F8 ? 16 * trow + 2 * c : 16 * c + trow;
-      const int db = F8 ? da + 1 : da + 8;
-      const float pa0 = live0 ? __ldcg(o0 + da) : 0.f, pb0 = live0 ? __ldcg(o0 + db) : 0.f;
-      const float pa1 = live1 ? __ldcg(o0 + D + da) : 0.f, pb1 = live1 ? __ldcg(o0 + D + db) : 0.f;
-      acc[c].x = acc[c].x * r0 + pa0 * e0;
-      acc[c].y = acc[c].y * r1 + pa1 * e1;
-      acc[c].z = acc[c].z * r0 + pb0 * e0;
-      acc[c].w = acc[c].w * r1 + pb1 * e1;
+  for (int c = 0; c < D / 16; ++c) {
+    // 16-bit pools: d = 16c + trow (x, y) and + 8 (z, w); FP8 pools: d = 16 trow + 2c (x, y) and
+    // + 1 (z, w); x, z head h0 and y, w head h0 + 1
+    const int da = F8 ? 16 * trow + 2 * c : 16 * c + trow;
+    const int db = F8 ? da + 1 : da + 8;
+    if (live0) {
+      o0[da] = acc[c].x;
+      o0[db] = acc[c].z;
     }
-    L0 = L0 * r0 + l0 * e0;
-    L1 = L1 * r1 + l1 * e1;
-    M0 = n0;
-    M1 = n1;
+    if (live1) {
+      o0[D + da] = acc[c].y;
+      o0[D + db] = acc[c].w;
+    }
   }
+  if (trow == 0) {
+    if (live0) *reinterpret_cast<float2*>(a.sfx_ml + 2 * row) = make_float2(M0, L0);
+    if (live1) *reinterpret_cast<float2*>(a.sfx_ml + 2 * row + 2) = make_float2(M1, L1);
+  }
+  return true;
 }
 
 // Merge the partials of one split pair (contributing warps wa..wb) and write its
@@ -449,10 +436,76 @@ __device__ __forceinline__ void merge_pair(const DecodeArgs& a, int s, int g, in
       M0 = n0;
       M1 = n1;
     }
-    fold_prior<D, F8>(a, s, g, nb, lane, acc, M0, M1, L0, L1);
+    if (leave_partial<D, F8>(a, s, g, nb, lane, acc, M0, M1, L0, L1)) continue;
     const float i0 = a.v_mul / L0, i1 = a.v_mul / L1;
     store_group<TO, D, F8>(out + GPAD * nb * D, acc, i0, i1, lane, a.G - GPAD * nb);
   }
+}
+
+// The combine kernel of a decode step with shared prefixes: one warp per (row, query head) of
+// the rows that have one, lane l holding d = 4l .. 4l + 3 (d_head 128).  It merges the decode
+// kernel's partial of the row (its own blocks) with the prefix kernel's partials of the row (the
+// splits of the shared blocks) by the online-softmax rule ("Chunked prefill mechanics": m the
+// largest, each l and O scaled by 2^(m_part - m)) and writes O / l (times v_scale for an FP8 pool).
+template <typename TO>
+__global__ void __launch_bounds__(256) share_combine_kernel(const DecodeArgs a) {
+  constexpr int D = 128;
+  // launched as the programmatic dependent of the decode kernel: resident early, it waits here
+  // until that grid has completed and its partials are visible
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int lane = threadIdx.x & 31;
+  const int64_t p = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);  // (row, head)
+  if (p >= static_cast<int64_t>(a.n_seq) * a.H_q) return;
+  const int s = static_cast<int>(p / a.H_q);
+  if (seq_span(a, s, false).kb == 0) return;  // written by the decode kernel
+  const int4 sh = a.share[s];
+  if (sh.y < 1 || sh.z < 0 || sh.w < 0 ||
+      static_cast<int64_t>(sh.z) + static_cast<int64_t>(sh.y - 1) * sh.w >= a.prior_slots) {
+    if (lane == 0 && p % a.H_q == 0) record_error(a.err, DERR_SHARE, s);
+    return;
+  }
+  const int64_t hq = p % a.H_q;
+  const float2 ml = __ldcg(reinterpret_cast<const float2*>(a.sfx_ml) + p);
+  float m = ml.x, l = ml.y;
+  float4 o = __ldcg(reinterpret_cast<const float4*>(a.sfx_o + p * D) + lane);
+  constexpr int K = 12;  // partials whose loads are in flight at once (a step's splits are usually fewer)
+  for (int i0 = 0; i0 < sh.y; i0 += K) {
+    float2 pm[K];
+    float4 po[K];
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+      if (i0 + k < sh.y) {
+        const int64_t row = (static_cast<int64_t>(sh.z) + static_cast<int64_t>(i0 + k) * sh.w) * a.H_q + hq;
+        pm[k] = __ldcg(reinterpret_cast<const float2*>(a.prior_ml) + row);
+        po[k] = __ldcg(reinterpret_cast<const float4*>(a.prior_o + row * D) + lane);
+      } else {
+        pm[k] = make_float2(-INFINITY, 0.f);
+        po[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+    float mn = m;
+#pragma unroll
+    for (int k = 0; k < K; ++k) mn = fmaxf(mn, pm[k].x);
+    const float r = exp2f(m - mn);
+    l *= r;
+    o.x *= r;
+    o.y *= r;
+    o.z *= r;
+    o.w *= r;
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+      const float e = exp2f(pm[k].x - mn);  // 0 for the padding entries
+      l += pm[k].y * e;
+      o.x += po[k].x * e;
+      o.y += po[k].y * e;
+      o.z += po[k].z * e;
+      o.w += po[k].w * e;
+    }
+    m = mn;
+  }
+  const float inv = a.v_mul / l;
+  TO* out = static_cast<TO*>(a.out) + p * D + 4 * lane;
+  *reinterpret_cast<uint2*>(out) = make_uint2(pack2<TO>(o.x * inv, o.y * inv), pack2<TO>(o.z * inv, o.w * inv));
 }
 
 // Descriptor of one tile, built by the warp a batch at a time:
@@ -477,6 +530,9 @@ __global__ void __launch_bounds__(NW * 32) decode_tc_kernel(const __grid_constan
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int gw = blockIdx.x * NW + warp;
+  // a programmatic dependent launched after this grid (the combine kernel of a step with shared
+  // prefixes) may become resident now; it waits for this grid's completion before reading
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* region = base + warp * SM::WARP_STRIDE;
@@ -815,9 +871,8 @@ __global__ void __launch_bounds__(NW * 32) decode_tc_kernel(const __grid_constan
           float4 acc4[C::NKC];
 #pragma unroll
           for (int c = 0; c < C::NKC; ++c) acc4[c] = make_float4(o[nb][c][0], o[nb][c][1], o[nb][c][2], o[nb][c][3]);
-          float M0 = m[nb][0], M1 = m[nb][1], L0 = Ls[nb][0], L1 = Ls[nb][1];
-          fold_prior<D, F8>(a, s, g, nb, lane, acc4, M0, M1, L0, L1);
-          const float i0 = a.v_mul / L0, i1 = a.v_mul / L1;
+          if (leave_partial<D, F8>(a, s, g, nb, lane, acc4, m[nb][0], m[nb][1], Ls[nb][0], Ls[nb][1])) continue;
+          const float i0 = a.v_mul / Ls[nb][0], i1 = a.v_mul / Ls[nb][1];
           store_group<TA, D, F8>(out + GPAD * nb * D, acc4, i0, i1, lane, a.G - GPAD * nb);
         }
       } else {
@@ -1049,10 +1104,11 @@ int tc_grid(const Pool& P, int* grid, int* warps, int* smem) {
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct WsLayout {
-  size_t prefix, lens, counters, wstart, partials, prior_ml, prior_o, total;
+  size_t prefix, lens, counters, wstart, partials, prior_ml, prior_o, sfx_ml, sfx_o, total;
 };
 
-// n_prior > 0: room for that many shared-prefix partial slots (m, l and O per query head) at the end.
+// n_prior > 0: room for that many shared-prefix partial slots (m, l and O per query head) at the
+// end, and for the decode kernel's partial of every row.
 WsLayout ws_layout(int n_seq, int H_kv, int64_t total_warps, int D, int G, int64_t n_prior = 0) {
   WsLayout w;
   w.prefix = kHdrBytes;
@@ -1063,8 +1119,11 @@ WsLayout ws_layout(int n_seq, int H_kv, int64_t total_warps, int D, int G, int64
   const int nb = G > GPAD ? 2 : 1;  // head blocks (the kernel's TcCfg::PSTRIDE)
   const int pstride = nb * (D / 16) * 32 * 4 + 2 * GPAD * nb;
   w.prior_ml = w.partials + align256(sizeof(float) * total_warps * 2 * pstride);
+  const int64_t n_sfx = n_prior > 0 ? n_seq : 0;
   w.prior_o = w.prior_ml + align256(sizeof(float) * 2 * n_prior * H_kv * G);
-  w.total = w.prior_o + align256(sizeof(float) * static_cast<size_t>(D) * n_prior * H_kv * G);
+  w.sfx_ml = w.prior_o + align256(sizeof(float) * static_cast<size_t>(D) * n_prior * H_kv * G);
+  w.sfx_o = w.sfx_ml + align256(sizeof(float) * 2 * n_sfx * H_kv * G);
+  w.total = w.sfx_o + align256(sizeof(float) * static_cast<size_t>(D) * n_sfx * H_kv * G);
   return w;
 }
 
@@ -1337,6 +1396,8 @@ int launch_decode(Pool& P, int32_t layer, const void* q, const void* k_pool, con
       a.prior_ml = reinterpret_cast<float*>(w + L.prior_ml);
       a.prior_o = reinterpret_cast<float*>(w + L.prior_o);
       a.prior_slots = share_slot_cap(n_seq);
+      a.sfx_ml = reinterpret_cast<float*>(w + L.sfx_ml);
+      a.sfx_o = reinterpret_cast<float*>(w + L.sfx_o);
       if (int rc = launch_prefix_share(P, a, q, k_pool, v_pool, share->n_items, share->max_members, st)) return rc;
     }
     bool after_append = false;
@@ -1346,7 +1407,26 @@ int launch_decode(Pool& P, int32_t layer, const void* q, const void* k_pool, con
                                  stream, after_append))
         return rc;
     }
-    return launch_tc_sequence(a, maps, tc_kernel_for(P, &smem), grid, nw, smem, st, after_append);
+    if (int rc = launch_tc_sequence(a, maps, tc_kernel_for(P, &smem), grid, nw, smem, st, after_append)) return rc;
+    if (shared) {  // the rows with a shared prefix: their two partials merged into out
+      const int64_t warps = static_cast<int64_t>(n_seq) * g.H_q;
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(static_cast<unsigned>((warps + 7) / 8));
+      cfg.blockDim = dim3(256);
+      cfg.stream = st;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      attr[0].val.programmaticStreamSerializationAllowed = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      const void* k = g.dtype == PKV_F16 ? reinterpret_cast<const void*>(&share_combine_kernel<__half>)
+                                         : reinterpret_cast<const void*>(&share_combine_kernel<__nv_bfloat16>);
+      void* args[] = {&a};
+      const cudaError_t e = cudaLaunchKernelExC(&cfg, k, args);
+      if (e != cudaSuccess) return fail(PKV_ERR_CUDA, std::string("combine launch: ") + cudaGetErrorString(e));
+      count_launch();
+    }
+    return PKV_OK;
   }
 
   if (share && share->n_items > 0)
