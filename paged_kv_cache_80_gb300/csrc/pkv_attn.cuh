@@ -245,6 +245,8 @@ int fill_args(const Pool& P, int32_t layer, const void* q, void* out, const int3
               const int32_t* seq_lens, int32_t n_seq, float scale, DecodeArgs* a);
 // The prefix kernel of a decode step with shared prefixes (pkv_prefill.cu): one CTA per (pair
 // of 128-row tiles of the item's rows, KV head, work item); a carries share_items and prior_*.
+// Launched as the programmatic dependent of the decode kernel just before it (it reads nothing
+// that kernel writes, and waits for that grid only before it completes).
 int launch_prefix_share(Pool& P, const DecodeArgs& a, const void* q, const void* k_pool, const void* v_pool,
                         int32_t n_items, int32_t max_members, cudaStream_t st);
 

@@ -450,8 +450,8 @@ __device__ __forceinline__ void merge_pair(const DecodeArgs& a, int s, int g, in
 template <typename TO>
 __global__ void __launch_bounds__(256) share_combine_kernel(const DecodeArgs a) {
   constexpr int D = 128;
-  // launched as the programmatic dependent of the decode kernel: resident early, it waits here
-  // until that grid has completed and its partials are visible
+  // launched as the programmatic dependent of the prefix kernel, which completes only after the
+  // decode kernel has: it waits here until both grids' partials are visible
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int lane = threadIdx.x & 31;
   const int64_t p = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);  // (row, head)
@@ -1398,7 +1398,6 @@ int launch_decode(Pool& P, int32_t layer, const void* q, const void* k_pool, con
       a.prior_slots = share_slot_cap(n_seq);
       a.sfx_ml = reinterpret_cast<float*>(w + L.sfx_ml);
       a.sfx_o = reinterpret_cast<float*>(w + L.sfx_o);
-      if (int rc = launch_prefix_share(P, a, q, k_pool, v_pool, share->n_items, share->max_members, st)) return rc;
     }
     bool after_append = false;
     if (fuse) {  // the step's append kernel first, letting the attention launch start under it
@@ -1408,7 +1407,11 @@ int launch_decode(Pool& P, int32_t layer, const void* q, const void* k_pool, con
         return rc;
     }
     if (int rc = launch_tc_sequence(a, maps, tc_kernel_for(P, &smem), grid, nw, smem, st, after_append)) return rc;
-    if (shared) {  // the rows with a shared prefix: their two partials merged into out
+    if (shared) {
+      // the shared blocks once per run of rows: the prefix kernel takes SMs as the decode grid
+      // leaves them, and its partials are still in L2 for the combine kernel
+      if (int rc = launch_prefix_share(P, a, q, k_pool, v_pool, share->n_items, share->max_members, st)) return rc;
+      // the rows with a shared prefix: their two partials merged into out
       const int64_t warps = static_cast<int64_t>(n_seq) * g.H_q;
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(static_cast<unsigned>((warps + 7) / 8));

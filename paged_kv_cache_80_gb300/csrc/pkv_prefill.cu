@@ -401,7 +401,11 @@ __global__ void __launch_bounds__(UM_THREADS, 1) prefill_umma_kernel(const __gri
   const int Cs = SH ? item[1] - item[0] : q_off[s + 1] - qbeg;
   const int i0 = qb * 2 * QB;  // first query of tile A
   if (qb == gridDim.x - 1 && tid == 0 && g == 0 && Cs > i0 + 2 * QB) record_error(a.err, DERR_PREFILL_CHUNK, s);
-  if (i0 >= Cs) return;  // uniform over the CTA, before any barrier or TMEM use
+  if (i0 >= Cs) {  // uniform over the CTA, before any barrier or TMEM use
+    if constexpr (SH)
+      if (tid == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
+    return;
+  }
   int nkeys, P = 0;
   int64_t trow0;  // the first table entry of the keys
   if constexpr (SH) {
@@ -409,6 +413,7 @@ __global__ void __launch_bounds__(UM_THREADS, 1) prefill_umma_kernel(const __gri
     if (qbeg < 0 || item[1] > a.n_seq || kb0 < 0 || kb1 <= kb0 || kb1 > a.W || item[4] < 0 ||
         static_cast<int64_t>(item[4]) + Cs > a.prior_slots) {
       if (tid == 0 && qb == 0 && g == 0) record_error(a.err, DERR_SHARE, s);
+      if (tid == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
       return;
     }
     nkeys = (kb1 - kb0) * a.B;
@@ -881,6 +886,10 @@ __global__ void __launch_bounds__(UM_THREADS, 1) prefill_umma_kernel(const __gri
   tc_fence_before();
   __syncthreads();
   if (warp == 8) tmem_dealloc(tmem, 512);
+  // the shared-prefix form runs as the decode kernel's programmatic dependent; it completes only
+  // after that grid has, so that the combine kernel, which waits for this grid, sees both
+  if constexpr (SH)
+    if (tid == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 // Chunked prefill on CUDA cores: one CTA per (query row, KV head).  The row's
@@ -996,7 +1005,18 @@ int launch_prefix_share(Pool& P, const DecodeArgs& a, const void* q, const void*
   DecodeArgs args_copy = a;
   const int32_t* no_off = nullptr;
   void* args[] = {&maps[0], &maps[1], &maps[2], &args_copy, const_cast<int32_t**>(&no_off)};
-  e = cudaLaunchKernel(k, grid, dim3(UM_THREADS), args, smem, st);
+  // the decode kernel's programmatic dependent: its CTAs take the SMs that decode CTAs leave
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(UM_THREADS);
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelExC(&cfg, k, args);
   if (e != cudaSuccess) return fail(PKV_ERR_CUDA, std::string("shared-prefix launch: ") + cudaGetErrorString(e));
   count_launch();
   return PKV_OK;
