@@ -754,8 +754,20 @@ static int step_workspace_check(pkv_pool* pool, int32_t n, size_t ws_bytes) {
 // them share, cut so that every row keeps at least one token of its own (so no row's shared
 // blocks are written in this step).  Groups of fewer than min_members rows are dropped.  Each
 // group's prefix is cut into splits of whole blocks so that the prefix kernel's grid (CTAs =
-// member pairs of 128-row tiles x KV heads x splits, over all groups) comes near share_ctas,
+// member pairs of 128-row tiles x KV heads x splits, over all groups) comes near a target,
 // splits of at least 256 keys, within the plan's item and slot caps.
+//
+// The target: the prefix kernel is bound by the tensor cores and the decode of the rows' own
+// blocks by HBM, which on this GPU needs only ~96 SMs for its full rate.  With 16-bit pools and
+// groups of up to 8 query heads the step can run the two side by side: the decode on S SMs (one
+// 8-warp CTA on each, header word 3 = S) and the prefix kernel's CTAs, one per SM, on the others.
+// S and the target come from a time model of the two kernels measured on GB300 -- decode: 10 us +
+// own K/V bytes / min(6.95 TB/s, S x 70 GB/s) (a CTA's shared memory caps its bytes in flight;
+// 70 GB/s an SM is what the forked shape's short pairs reach); prefix: 12 us + (keys of a split) x
+// (128-row tiles of a CTA) x 8.6 ns -- taking the S that minimises the larger of the two, unless
+// running them one after the other on all share_ctas SMs (header word 3 = 0) is estimated faster.
+// (FP8 pools move half the bytes per tile in flight, so their decode keeps every SM.)  The model
+// only places work; any choice gives the same results.
 static void plan_sharing(Pool& P, const int32_t* ids, int32_t n, int32_t* plan) {
   const int64_t B = P.geo.block_size;
   int32_t* rows = plan + 4;
@@ -785,16 +797,57 @@ static void plan_sharing(Pool& P, const int32_t* ids, int32_t n, int32_t* plan) 
   }
   const int64_t ng = static_cast<int64_t>(grp.size()) / 4;
   if (ng == 0) return;
-  const int64_t G = P.geo.H_q / P.geo.H_kv, per_cta = 2 * (128 / G);
+  const int64_t G = P.geo.H_q / P.geo.H_kv, QB = 128 / G, per_cta = 2 * QB;
   auto ctas_of = [&](int64_t gi) { return (grp[4 * gi + 1] - grp[4 * gi] + per_cta - 1) / per_cta * P.geo.H_kv; };
   double total = 0.0;
   for (int64_t gi = 0; gi < ng; ++gi) total += static_cast<double>(ctas_of(gi)) * grp[4 * gi + 2];
+  // splits of every group for a grid target; returns (CTAs, the longest CTA's keys x tiles)
+  auto assign = [&](double target, int64_t* ctas, double* longest) {
+    *ctas = 0;
+    *longest = 0.0;
+    for (int64_t gi = 0; gi < ng; ++gi) {
+      const int64_t ct = ctas_of(gi), kb = grp[4 * gi + 2], m = grp[4 * gi + 1] - grp[4 * gi];
+      const double want = target * (static_cast<double>(ct) * kb / total) / ct;
+      const int64_t most = std::max<int64_t>(1, kb * B / 256);
+      const int64_t sp = std::max<int64_t>(1, std::min<int64_t>(most, static_cast<int64_t>(want)));
+      grp[4 * gi + 3] = static_cast<int32_t>(sp);
+      const int64_t bps = (kb + sp - 1) / sp;
+      *ctas += ct * ((kb + bps - 1) / bps);
+      *longest = std::max(*longest, static_cast<double>(bps * B) * (m > QB ? 2 : 1));
+    }
+  };
+  int32_t decode_sms = 0;
+  {
+    // the decode's own bytes: every row's tokens after its shared blocks
+    double own = 0.0;
+    for (int32_t r = 0, gi = 0; r < n; ++r) {
+      while (gi < ng && grp[4 * gi + 1] <= r) ++gi;
+      const int64_t kb = (gi < ng && grp[4 * gi] <= r) ? grp[4 * gi + 2] : 0;
+      own += static_cast<double>(P.seqs[ids[r]].len - kb * B);
+    }
+    own *= static_cast<double>(P.geo.H_kv) * P.geo.d_head * pkv::elem_size(P.geo.dtype) * 2;
+    auto t_decode = [&](double sms) { return 10e-6 + own / std::min(6.95e12, sms * 70e9); };
+    auto t_prefix = [&](double longest) { return 12e-6 + longest * 8.6e-9; };
+    int64_t ctas = 0;
+    double longest = 0.0;
+    assign(P.share_ctas, &ctas, &longest);
+    double best = t_decode(P.share_ctas) + t_prefix(longest), best_target = P.share_ctas;
+    if (G <= 8 && P.geo.dtype != PKV_E4M3)
+      for (int32_t target = 8; target <= P.share_ctas - 8; target += 4) {
+        assign(target, &ctas, &longest);
+        const int64_t sms = P.share_ctas - ctas;
+        if (sms < 8) continue;
+        const double t = std::max(t_decode(static_cast<double>(sms)), t_prefix(longest));
+        if (t < best) {
+          best = t;
+          best_target = target;
+          decode_sms = static_cast<int32_t>(sms);
+        }
+      }
+    assign(best_target, &ctas, &longest);
+  }
   int64_t n_items = 0, n_slots = 0;
   for (int64_t gi = 0; gi < ng; ++gi) {
-    const int64_t ct = ctas_of(gi), kb = grp[4 * gi + 2];
-    const double want = P.share_ctas * (static_cast<double>(ct) * kb / total) / ct;
-    const int64_t most = std::max<int64_t>(1, kb * B / 256);
-    grp[4 * gi + 3] = static_cast<int32_t>(std::max<int64_t>(1, std::min<int64_t>(most, static_cast<int64_t>(want))));
     n_items += grp[4 * gi + 3];
     n_slots += static_cast<int64_t>(grp[4 * gi + 3]) * (grp[4 * gi + 1] - grp[4 * gi]);
   }
@@ -841,6 +894,7 @@ static void plan_sharing(Pool& P, const int32_t* ids, int32_t n, int32_t* plan) 
   plan[0] = it;
   plan[1] = max_members;
   plan[2] = slot;
+  plan[3] = it > 0 ? decode_sms : 0;
 }
 
 int pkv_step_plan(pkv_pool* pool, const int32_t* seq_ids, int32_t n, int32_t W, int32_t* meta_host,
@@ -894,9 +948,9 @@ static int step_launch(pkv_pool* pool, int32_t layer, int32_t n, int32_t W, cons
     const int64_t off = pkv::share_plan_offset(n, W);
     const int32_t* hdr = plan_host + off;
     if (hdr[0] < 0 || hdr[0] > pkv::share_item_cap(n) || hdr[1] < 0 || hdr[1] > n || hdr[2] < 0 ||
-        hdr[2] > pkv::share_slot_cap(n))
+        hdr[2] > pkv::share_slot_cap(n) || hdr[3] < 0 || hdr[3] > P.share_ctas)
       return fail(PKV_ERR_INVALID_ARG, "the step metadata's shared-prefix plan is corrupt");
-    share = pkv::ShareLaunch{meta_dev + off, hdr[0], hdr[1]};
+    share = pkv::ShareLaunch{meta_dev + off, hdr[0], hdr[1], hdr[3]};
   }
   if (n_cow > 0)
     if (int rc = pkv_copy_blocks(pool, cow_pairs, n_cow, k_pool, v_pool, stream)) return rc;

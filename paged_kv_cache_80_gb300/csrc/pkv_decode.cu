@@ -1055,14 +1055,15 @@ KernelPtr pick_tc(const TcVariant& v, int G, int* smem) {
   return tc_kernel_ptr<T, D, 2, 4>();
 }
 
-KernelPtr tc_kernel_for(const Pool& P, int* smem) {
-  const TcVariant v = tc_variant(P);
+KernelPtr tc_kernel_with(const Pool& P, const TcVariant& v, int* smem) {
   const int G = P.geo.H_q / P.geo.H_kv;
   if (P.geo.dtype == PKV_E4M3) return pick_tc<E4M3, 128>(v, G, smem);
   const bool bf = P.geo.dtype == PKV_BF16;
   if (P.geo.d_head == 128) return bf ? pick_tc<__nv_bfloat16, 128>(v, G, smem) : pick_tc<__half, 128>(v, G, smem);
   return bf ? pick_tc<__nv_bfloat16, 64>(v, G, smem) : pick_tc<__half, 64>(v, G, smem);
 }
+
+KernelPtr tc_kernel_for(const Pool& P, int* smem) { return tc_kernel_with(P, tc_variant(P), smem); }
 
 // Persistent grid for the tensor-core kernel: resident CTAs per SM x SM count.
 int tc_grid(const Pool& P, int* grid, int* warps, int* smem) {
@@ -1372,6 +1373,19 @@ int launch_decode(Pool& P, int32_t layer, const void* q, const void* k_pool, con
     int grid = 0, nw = 0, smem = 0;
     if (int rc = tc_grid(P, &grid, &nw, &smem)) return rc;
     const bool shared = share && share->n_items > 0;
+    KernelPtr kern = tc_kernel_for(P, &smem);
+    if (shared && share->decode_sms > 0 && G <= GPAD) {
+      // beside the prefix kernel: one 8-warp CTA on each of decode_sms SMs, its dynamic shared
+      // memory raised so that no SM takes two (the prefix kernel's CTAs take the other SMs)
+      kern = tc_kernel_with(P, TcVariant{2, 8}, &smem);
+      smem = std::max(smem, 116 * 1024);
+      const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      if (e != cudaSuccess) return fail(PKV_ERR_CUDA, std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e));
+      int sms = 0;
+      if (int rc = device_sm_count(&sms)) return rc;
+      grid = std::min(share->decode_sms, sms);
+      nw = 8;
+    }
     const WsLayout L =
         ws_layout(n_seq, g.H_kv, static_cast<int64_t>(grid) * nw, g.d_head, G, shared ? share_slot_cap(n_seq) : 0);
     if (ws_bytes < L.total) return fail(PKV_ERR_INVALID_ARG, "workspace too small: need " + std::to_string(L.total));
@@ -1406,7 +1420,7 @@ int launch_decode(Pool& P, int32_t layer, const void* q, const void* k_pool, con
                                  stream, after_append))
         return rc;
     }
-    if (int rc = launch_tc_sequence(a, maps, tc_kernel_for(P, &smem), grid, nw, smem, st, after_append)) return rc;
+    if (int rc = launch_tc_sequence(a, maps, kern, grid, nw, smem, st, after_append)) return rc;
     if (shared) {
       // the shared blocks once per run of rows: the prefix kernel takes SMs as the decode grid
       // leaves them, and its partials are still in L2 for the combine kernel

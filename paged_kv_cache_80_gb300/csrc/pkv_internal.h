@@ -62,7 +62,8 @@ struct Pool {
   int32_t swap_engine = 0;  // 0 SM kernel, 1 copy engine
   float k_scale = 1.f, v_scale = 1.f;  // FP8 pools: stored code * scale
   int32_t n_prefix_caches = 0;         // live radix prefix caches holding references
-  // shared prefixes in decode steps (pkv_pool_set_prefix_sharing): off while share_min_members == 0
+  // shared prefixes in decode steps (pkv_pool_set_prefix_sharing): off while share_min_members == 0;
+  // share_ctas: the SMs a step may use
   int32_t share_min_members = 0, share_min_blocks = 1, share_ctas = 0;
   std::vector<int32_t> share_scratch;  // planner scratch
 
@@ -80,10 +81,10 @@ inline int64_t act_size(int32_t dtype) { return dtype == PKV_E4M3 ? 2 : elem_siz
 // A decode step whose batch holds runs of rows that share their first table blocks (branches
 // forked from one parent: "Zero-copy deliberation via copy-on-write branching") attends to the
 // shared blocks once for the whole run, in the prefix kernel, and to each row's own blocks in the
-// decode kernel, which folds the prefix kernel's partials in.  The plan (int32), made on the host
-// with the step's metadata and copied with it: a header {n_items, max_members, n_slots, 0}; per
-// batch row {kb, items, slot0, stride} (the row's first kb blocks are shared; its partials sit in
-// slots slot0 + i * stride, i < items); then up to share_item_cap(n) work items of 8 ints
+// decode kernel; the combine kernel merges the two.  The plan (int32), made on the host with the
+// step's metadata and copied with it: a header {n_items, max_members, n_slots, decode SMs}; per
+// batch row {kb, items, slot0, stride} (the row's first kb blocks are shared; its prefix partials
+// sit in slots slot0 + i * stride, i < items); then up to share_item_cap(n) work items of 8 ints
 // {row_begin, row_end, kb0, kb1, slot_base, 0, 0, 0}: the rows, the range of row_begin's table
 // blocks, and the slot of row_begin's partial.
 inline int64_t share_item_cap(int64_t n) { return n + 256; }
@@ -101,10 +102,12 @@ inline int64_t share_plan_offset(int64_t n, int64_t W) { return (n * (W + 2) + 3
 inline int64_t step_meta_ints(const Pool& P, int64_t n, int64_t W) {
   return share_on(P) ? share_plan_offset(n, W) + share_plan_ints(n) : n * (W + 2);
 }
-// The shared-prefix part of a decode launch: the plan on the device and its header's counts.
+// The shared-prefix part of a decode launch: the plan on the device and its header's counts;
+// decode_sms > 0: the decode kernel runs as one 8-warp CTA on each of that many SMs, beside the
+// prefix kernel on the others (0: on every SM, then the prefix kernel).
 struct ShareLaunch {
   const int32_t* plan_dev;
-  int32_t n_items, max_members;
+  int32_t n_items, max_members, decode_sms;
 };
 
 // ------------------------------------------------------------------ device side

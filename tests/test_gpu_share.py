@@ -71,6 +71,8 @@ def test_shared_prefix_steps_match_oracle(dtype, H_q):
         torch.cuda.synchronize()
         hdr = _plan_header(meta_host.numpy(), n, Wd)
         assert hdr[0] >= 3 and hdr[1] == 37, hdr  # three groups, the largest of 37 rows
+        if H_q == 128:
+            assert hdr[3] == 0  # groups of 16 heads: decode on every SM, then the prefix kernel
         oslots, ocows = b.orc.append(run.tolist(), [1] * n)
         if len(ocows):
             oracle.copy_blocks(g, ocows, b.hk, b.hv)
@@ -152,6 +154,7 @@ def test_forked_workload_with_sharing_sampled():
         torch.cuda.synchronize()
         hdr = _plan_header(meta_host.numpy(), n, Wd)
         assert hdr[0] > 1 and hdr[1] == 64, hdr  # one group of all 64 branches, in several splits
+        assert hdr[3] > 0, hdr  # the decode of the branches' own blocks beside the prefix kernel
         oslots, ocows = b.orc.append(run.tolist(), [1] * n)
         if len(ocows):
             oracle.copy_blocks(g, ocows, b.hk, b.hv)
@@ -161,6 +164,42 @@ def test_forked_workload_with_sharing_sampled():
         got = out_f64(out, "bf16")
         assert np.all(np.isfinite(got))
         check_attention(got[sample], b.decode_ref(q[sample], tables[sample], lens[sample], wl.scale), "bf16")
+    b.check_pools_bitexact()
+
+
+@pytest.mark.parametrize("side_by_side", [True, False])
+def test_both_schedules_give_the_oracle_result(side_by_side):
+    """The same step with the decode beside the prefix kernel (header word 3 > 0, as planned)
+    and with it forced to run on every SM first (word 3 = 0 written into the plan)."""
+    import torch
+
+    b, run = _build("bf16", 64, seed=74, members=(64,), prefixes=(3000,))
+    g = b.g
+    n, Wd = len(run), 320
+    mi = pkv.pkv_step_meta_ints(b.lib, n, Wd)
+    meta_host = torch.zeros(mi, dtype=torch.int32).pin_memory()
+    meta_dev = torch.zeros(mi, dtype=torch.int32, device="cuda")
+    ws = torch.empty(pkv.pkv_decode_workspace_size(b.lib, n), dtype=torch.uint8, device="cuda")
+    scale = 1.0 / math.sqrt(g.d_head)
+    q = W.normal(74, "q", (n, g.H_q, g.d_head), "bf16")
+    kn = W.normal(74, "k", (n, g.H_kv, g.d_head), "bf16")
+    vn = W.normal(74, "v", (n, g.H_kv, g.d_head), "bf16")
+    cows = pkv.pkv_step_plan(b.lib, run, Wd, meta_host)
+    off = (n * (Wd + 2) + 3) // 4 * 4
+    assert int(meta_host[off + 3]) > 0  # planned side by side
+    if not side_by_side:
+        meta_host[off + 3] = 0
+    out = torch.full((n, g.H_q, g.d_head), float("nan"), dtype=torch.bfloat16, device="cuda")
+    pkv.pkv_step_launch(b.lib, 0, n, Wd, cows, to_dev(q, "bf16"), to_dev(kn, "bf16"), to_dev(vn, "bf16"), b.kp,
+                        b.vp, scale, out, meta_host, meta_dev, ws)
+    torch.cuda.synchronize()
+    oslots, ocows = b.orc.append(run.tolist(), [1] * n)
+    if len(ocows):
+        oracle.copy_blocks(g, ocows, b.hk, b.hv)
+    oracle.write_slots(g, 0, kn, vn, oslots, b.hk, b.hv)
+    pkv.pkv_check_device_error()
+    tables, lens = b.tables(run.tolist(), Wd)
+    check_attention(out_f64(out, "bf16"), b.decode_ref(q, tables, lens, scale), "bf16")
     b.check_pools_bitexact()
 
 

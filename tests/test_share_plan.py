@@ -101,9 +101,14 @@ def test_two_groups_among_unrelated_rows():
     assert set(groups) == {(1, 41), (42, 52)}
     assert rows[1, 0] == 1000 // 16  # 62 full blocks of P's prefix
     assert rows[42, 0] == 4104 // 16  # 256 full blocks of Q's (the tail block went to copies)
-    # the grid: (members / 32 rounded up) x 8 KV heads per split, near the 152 target
+    # the prefix grid: (members / 32 rounded up) x 8 KV heads per split; with the decode beside it
+    # on hdr[3] SMs (one CTA each) the two fit the 152 target together, else the grid alone comes
+    # near it
     ctas = sum(((re - rb + 31) // 32) * 8 * len(v) for (rb, re), v in groups.items())
-    assert 100 <= ctas <= 152
+    if hdr[3]:
+        assert 8 <= hdr[3] and ctas + hdr[3] <= 152
+    else:
+        assert 100 <= ctas <= 152
 
 
 def test_small_runs_are_not_grouped_and_min_blocks_holds():
@@ -167,6 +172,38 @@ def test_sixteen_head_groups_take_sixteen_members_per_cta():
     ((rb, re), its), = groups.items()
     assert (rb, re) == (0, 40)
     assert len(its) == 152 // (3 * 8)  # 40 members: 3 CTAs of 16 per KV head and split
+    assert hdr[3] == 0  # groups of 16 heads: the decode runs on every SM, then the prefix kernel
+
+
+def test_side_by_side_split_for_the_forked_shape():
+    """64 branches over a 1,023-block prefix with suffixes of ~1,000 tokens: the decode of the
+    branches' own blocks goes beside the prefix kernel (header word 3 = its SMs), and the two
+    grids together fit the SM count."""
+    pool = _pool(N=16384)
+    pkv.pkv_pool_set_prefix_sharing(pool, 8, 1, 152)
+    rng = np.random.default_rng(9)
+    _, kids = _forked_batch(pool, 16376, 64, [int(x) for x in rng.integers(0, 2048, 64)])
+    n, W = len(kids), 1200
+    meta = np.zeros(pkv.pkv_step_meta_ints(pool, n, W), np.int32)
+    pkv.pkv_step_plan(pool, kids, W, meta)
+    _, tables, lens, hdr, rows, items = _parse(meta, n, W)
+    groups = _check_plan(n, 16, tables, lens, hdr, rows, items, 2 * n + 1024)
+    ((rb, re), its), = groups.items()
+    assert (rb, re) == (0, 64) and rows[0, 0] == 1023
+    ctas = 2 * 8 * len(its)
+    assert 16 <= hdr[3] <= 152 - ctas
+
+
+def test_fp8_pools_keep_the_decode_on_every_sm():
+    pool = _pool(dtype="e4m3", N=16384)
+    pkv.pkv_pool_set_prefix_sharing(pool, 8, 1, 152)
+    _, kids = _forked_batch(pool, 16376, 64, [1000] * 64)
+    n, W = len(kids), 1200
+    meta = np.zeros(pkv.pkv_step_meta_ints(pool, n, W), np.int32)
+    pkv.pkv_step_plan(pool, kids, W, meta)
+    _, tables, lens, hdr, rows, items = _parse(meta, n, W)
+    _check_plan(n, 16, tables, lens, hdr, rows, items, 2 * n + 1024)
+    assert hdr[3] == 0 and hdr[0] == 152 // 16
 
 
 def test_option_validation():
