@@ -226,7 +226,8 @@ int pkv_decode_attention(const pkv_pool* pool, int32_t layer, const void* q, con
  *   W       : table width; every sequence needs ceil((len + 1) / B) <= W.
  *   meta_host: page-locked host int32 [pkv_step_meta_ints(pool, n, W)] (n * (W + 2)
  *             with prefix sharing off): the step writes its slot mapping, tables
- *             and lengths there (and, with sharing on, its shared-prefix plan) and
+ *             (entries past each table's end are left as they were) and lengths
+ *             there (and, with sharing on, its shared-prefix plan) and
  *             copies them to meta_dev (device int32, same size, 16-byte aligned) on
  *             the stream; do not reuse meta_host until that copy has run (e.g. a
  *             ring of buffers and events).

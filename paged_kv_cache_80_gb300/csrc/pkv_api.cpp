@@ -102,6 +102,18 @@ int unknown_seq(const Pool& P, int32_t id, bool releasing = false) {
   return fail(PKV_ERR_INVALID_ARG, "unknown or released sequence " + std::to_string(id));
 }
 
+// Token t's logical block t / B and offset t mod B: a shift and a mask when B is a power of two
+// (a 64-bit division costs tens of cycles, and a decode step takes several per sequence).
+struct BlockIdx {
+  int64_t B;
+  int sh;
+  explicit BlockIdx(int64_t b)
+      : B(b), sh((b & (b - 1)) == 0 ? __builtin_ctzll(static_cast<unsigned long long>(b)) : -1) {}
+  int64_t blk(int64_t t) const { return sh >= 0 ? t >> sh : t / B; }
+  int64_t off(int64_t t) const { return sh >= 0 ? t & (B - 1) : t % B; }
+  int64_t blocks(int64_t tokens) const { return blk(tokens + B - 1); }  // ceil(tokens / B)
+};
+
 // Drop one owner of block p; at zero it goes to the back of the FIFO.
 void drop_owner(Pool& P, int32_t p) {
   if (--P.ref[p] == 0) P.free.push_back(p);
@@ -294,22 +306,25 @@ int pkv_plan_append(pkv_pool* pool, const int32_t* seq_ids, const int32_t* n_new
   }
 
   // dry run: blocks needed, with owner counts as earlier copies in this call leave them
+  const BlockIdx bi(B);
   int64_t needed = 0;
   for (int32_t i : order) {
     if (n_new[i] == 0) continue;
     const SeqState& s = P.seqs[seq_ids[i]];
     const int64_t len = s.len;
-    if (len % B != 0) {
-      const int32_t tail = s.table[len / B];
+    if (bi.off(len) != 0) {
+      const int32_t tail = s.table[bi.blk(len)];
       if (P.ref[tail] - P.dropped[tail] > 1) {
         ++needed;
         ++P.dropped[tail];
       }
     }
-    needed += (len + n_new[i] + B - 1) / B - (len + B - 1) / B;  // positions with o == 0
+    needed += bi.blocks(len + n_new[i]) - bi.blocks(len);  // positions with o == 0
   }
-  for (int32_t i : order)  // reset the scratch counts
-    if (n_new[i] != 0 && P.seqs[seq_ids[i]].len % B != 0) P.dropped[P.seqs[seq_ids[i]].table[P.seqs[seq_ids[i]].len / B]] = 0;
+  for (int32_t i : order) {  // reset the scratch counts
+    const SeqState& s = P.seqs[seq_ids[i]];
+    if (n_new[i] != 0 && bi.off(s.len) != 0) P.dropped[s.table[bi.blk(s.len)]] = 0;
+  }
   if (needed > P.free.size())
     return fail(PKV_ERR_OUT_OF_BLOCKS, "append needs " + std::to_string(needed) + " blocks, " +
                                            std::to_string(P.free.size()) + " free");
@@ -325,7 +340,7 @@ int pkv_plan_append(pkv_pool* pool, const int32_t* seq_ids, const int32_t* n_new
     int32_t* out = slot_mapping + first_tok[i];
     for (int32_t k = 0; k < n_new[i]; ++k) {
       const int64_t t = s.len;
-      const int64_t l = t / B, o = t % B;
+      const int64_t l = bi.blk(t), o = bi.off(t);
       if (o == 0) {
         s.table.push_back(P.free.pop_front());
         P.ref[s.table.back()] = 1;
@@ -728,12 +743,12 @@ int pkv_seq_host_slots(const pkv_pool* pool, int32_t seq, int64_t* out, int32_t 
 // tables still fit W after one more token.
 static int step_check(pkv_pool* pool, const int32_t* seq_ids, int32_t n, int32_t W) {
   const Pool& CP = *as_pool(pool);
-  const int64_t B = CP.geo.block_size;
+  const BlockIdx bi(CP.geo.block_size);
   for (int32_t i = 0; i < n; ++i) {
     const SeqState* s = find_seq(CP, seq_ids[i]);
     if (!s) return unknown_seq(CP, seq_ids[i]);
     if (s->swapped) return fail(PKV_ERR_INVALID_ARG, "sequence " + std::to_string(seq_ids[i]) + " is swapped out");
-    if ((s->len + 1 + B - 1) / B > W)
+    if (bi.blocks(s->len + 1) > W)
       return fail(PKV_ERR_INVALID_ARG, "W = " + std::to_string(W) + " cannot hold sequence " +
                                            std::to_string(seq_ids[i]) + " after the step");
   }
@@ -912,8 +927,14 @@ int pkv_step_plan(pkv_pool* pool, const int32_t* seq_ids, int32_t n, int32_t W, 
   int32_t* tables = meta_host + n;
   int32_t* lens = meta_host + n + static_cast<int64_t>(n) * W;
   if (int rc = pkv_plan_append(pool, seq_ids, ones.data(), n, slots, cow_pairs, n_cow)) return rc;
-  if (int rc = pkv_export_tables(pool, seq_ids, n, tables, W, lens)) return rc;
+  // the tables and lengths after the append (the sequences were checked above); entries past a
+  // table's end are left as they were: no kernel reads them
   Pool& P = *as_pool(pool);
+  for (int32_t i = 0; i < n; ++i) {
+    const SeqState& s = P.seqs[seq_ids[i]];
+    std::copy(s.table.begin(), s.table.end(), tables + static_cast<int64_t>(i) * W);
+    lens[i] = static_cast<int32_t>(s.len);
+  }
   if (pkv::share_on(P)) {
     int32_t* plan = meta_host + pkv::share_plan_offset(n, W);
     std::fill(meta_host + static_cast<int64_t>(n) * (W + 2), plan, 0);  // the alignment gap
