@@ -965,7 +965,14 @@ static int step_launch(pkv_pool* pool, int32_t layer, int32_t n, int32_t W, cons
       return fail(PKV_ERR_CUDA, std::string("cudaMemcpyAsync (step metadata): ") + cudaGetErrorString(e));
     plan_host = meta_host;
   }
-  pkv::ShareLaunch share{nullptr, 0, 0};
+  pkv::ShareLaunch share{nullptr, 0, 0, 0};
+  bool long_batch = false;
+  if (plan_host) {  // the lengths after the append: tiles per (sequence, KV head) pair on average
+    const int32_t* lens = plan_host + n + static_cast<int64_t>(n) * W;
+    int64_t tiles = 0;
+    for (int32_t i = 0; i < n; ++i) tiles += (static_cast<int64_t>(lens[i]) + 15) / 16;
+    long_batch = tiles >= 1024ll * n;
+  }
   if (pkv::share_on(P) && plan_host) {
     const int64_t off = pkv::share_plan_offset(n, W);
     const int32_t* hdr = plan_host + off;
@@ -982,7 +989,7 @@ static int step_launch(pkv_pool* pool, int32_t layer, int32_t n, int32_t W, cons
   const pkv::AppendFuse fuse{k_new, v_new, meta_dev, k_pool, v_pool};
   if (int rc = pkv::launch_decode(*as_pool(pool), layer, q, k_pool, v_pool, meta_dev + n, W,
                                   meta_dev + n + static_cast<int64_t>(n) * W, n, scale, out, workspace, ws_bytes,
-                                  stream, &fuse, &share))
+                                  stream, &fuse, &share, long_batch))
     return rc;
   if (attn_end) cudaEventRecord(reinterpret_cast<cudaEvent_t>(attn_end), st);
   return PKV_OK;

@@ -146,10 +146,12 @@ struct AppendFuse {
   void* k_pool;
   void* v_pool;
 };
+// long_batch: the caller knows (from the lengths on the host) that the batch averages at least
+// 1,024 tiles per (sequence, KV head) pair; such a batch streams faster from a smaller grid.
 int launch_decode(Pool& P, int32_t layer, const void* q, const void* k_pool, const void* v_pool,
                   const int32_t* tables, int32_t W, const int32_t* seq_lens, int32_t n_seq, float scale, void* out,
                   void* ws, size_t ws_bytes, void* stream, const AppendFuse* fuse = nullptr,
-                  const ShareLaunch* share = nullptr);
+                  const ShareLaunch* share = nullptr, bool long_batch = false);
 int launch_prefill(Pool& P, int32_t layer, const void* q, const int32_t* q_off, int32_t n_tok, int32_t max_q,
                    const void* k_pool, const void* v_pool, const int32_t* tables, int32_t W, const int32_t* seq_lens,
                    int32_t n_seq, float scale, void* out, void* stream);
