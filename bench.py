@@ -45,13 +45,15 @@ METRIC = "paged decode attention KV GB/s & tokens/s (% of 8 TB/s HBM); swap GB/s
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per algorithmic byte
 # of one decode launch, per (stored K/V type, query heads per KV head), from ncu
-# captures of agent 48 x 4,096 (summary in profiles/) of the kernels built from the
-# sources with this digest.  Reported only while the sources hash to TRAFFIC_SOURCES_SHA256.
-TRAFFIC_SOURCES_SHA256 = "730211c7a02d2541df18d90f7fba0d6b7ab3a046bd8dc96bc0af03ae1af36511"
+# captures (summary in profiles/) of the kernels built from the sources with this
+# digest: bf16 with 8-head groups at agent 48 x 16,384 (a long batch, so the same
+# 120/152 grid as agent 48 x 32,768), the others at 48 x 4,096.  Reported only while
+# the sources hash to TRAFFIC_SOURCES_SHA256.
+TRAFFIC_SOURCES_SHA256 = "63ac7138d124537f5a199204638ff7d3560bbbc3464e9678d66356f856e53d15"
 TRAFFIC_RECORD = {
-    ("bf16", 8): 1.0078,   # 811.5 + 3.1 MB DRAM for 808.3 MB algorithmic (mean of 2 launches)
-    ("e4m3", 8): 1.0122,   # 406.9 + 3.1 MB for 405.1 MB
-    ("bf16", 16): 1.0113,  # 814.4 + 4.6 MB for 809.9 MB
+    ("bf16", 8): 1.0018,   # 3,227.3 + 2.8 MB DRAM for 3,224.4 MB algorithmic (mean of 2 launches)
+    ("e4m3", 8): 1.0124,   # 406.9 + 3.2 MB for 405.1 MB
+    ("bf16", 16): 1.0115,  # 814.4 + 4.8 MB for 809.9 MB
 }
 
 
