@@ -203,6 +203,48 @@ def test_both_schedules_give_the_oracle_result(side_by_side):
     b.check_pools_bitexact()
 
 
+def test_shared_prefix_beyond_the_in_kernel_plan():
+    """4,500 rows in 450 runs of 10 branches (a 40-token prefix: 2 shared blocks each): past
+    4,096 sequences the decode kernel follows the plan kernel, which also starts each row's
+    tiles after its shared blocks; every row against the oracle."""
+    import torch
+
+    g = W.Geometry(L=1, H_q=64, H_kv=8, d_head=128, block_size=16, dtype="bf16", num_blocks=16384)
+    b = PagedBatch(g, W.permutation(75, "fo", g.num_blocks), seed=75)
+    pkv.pkv_pool_set_prefix_sharing(b.lib, 4, 1, 0)
+    rng = W.substream(75, "suffix")
+    parents = b.new_seqs(450)
+    b.append(parents, [40] * 450, "prefix")
+    run = []
+    for p_ in parents:
+        run += [b.fork(p_) for _ in range(10)]
+    b.append(run, [int(x) for x in rng.integers(0, 30, len(run))], "suffix")
+    run = np.array(run, np.int32)
+    n, Wd = len(run), 8
+    mi = pkv.pkv_step_meta_ints(b.lib, n, Wd)
+    meta_host = torch.zeros(mi, dtype=torch.int32).pin_memory()
+    meta_dev = torch.zeros(mi, dtype=torch.int32, device="cuda")
+    ws = torch.empty(pkv.pkv_decode_workspace_size(b.lib, n), dtype=torch.uint8, device="cuda")
+    scale = 1.0 / math.sqrt(g.d_head)
+    q = W.normal(75, "q", (n, g.H_q, g.d_head), "bf16")
+    kn = W.normal(75, "k", (n, g.H_kv, g.d_head), "bf16")
+    vn = W.normal(75, "v", (n, g.H_kv, g.d_head), "bf16")
+    out = torch.full((n, g.H_q, g.d_head), float("nan"), dtype=torch.bfloat16, device="cuda")
+    pkv.pkv_decode_step(b.lib, 0, run, Wd, to_dev(q, "bf16"), to_dev(kn, "bf16"), to_dev(vn, "bf16"), b.kp, b.vp,
+                        scale, out, meta_host, meta_dev, ws)
+    torch.cuda.synchronize()
+    hdr = _plan_header(meta_host.numpy(), n, Wd)
+    assert hdr[0] >= 450 and hdr[1] == 10, hdr  # every run is a group
+    oslots, ocows = b.orc.append(run.tolist(), [1] * n)
+    if len(ocows):
+        oracle.copy_blocks(g, ocows, b.hk, b.hv)
+    oracle.write_slots(g, 0, kn, vn, oslots, b.hk, b.hv)
+    pkv.pkv_check_device_error()
+    tables, lens = b.tables(run.tolist(), Wd)
+    check_attention(out_f64(out, "bf16"), b.decode_ref(q, tables, lens, scale), "bf16")
+    b.check_state()
+
+
 def test_corrupt_plan_header_is_rejected():
     import torch
 
