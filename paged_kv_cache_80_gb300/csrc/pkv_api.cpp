@@ -927,18 +927,28 @@ int pkv_step_plan(pkv_pool* pool, const int32_t* seq_ids, int32_t n, int32_t W, 
   int32_t* tables = meta_host + n;
   int32_t* lens = meta_host + n + static_cast<int64_t>(n) * W;
   if (int rc = pkv_plan_append(pool, seq_ids, ones.data(), n, slots, cow_pairs, n_cow)) return rc;
-  // the tables and lengths after the append (the sequences were checked above); entries past a
-  // table's end are left as they were: no kernel reads them
   Pool& P = *as_pool(pool);
-  for (int32_t i = 0; i < n; ++i) {
-    const SeqState& s = P.seqs[seq_ids[i]];
-    std::copy(s.table.begin(), s.table.end(), tables + static_cast<int64_t>(i) * W);
-    lens[i] = static_cast<int32_t>(s.len);
-  }
+  // with sharing on, the plan first: a run's shared blocks are read only from its first row's
+  // table (the prefix kernel), so the other rows' copies of them need not be written
+  const int32_t* share_rows = nullptr;
+  std::vector<uint8_t>& first = P.share_first;
   if (pkv::share_on(P)) {
     int32_t* plan = meta_host + pkv::share_plan_offset(n, W);
     std::fill(meta_host + static_cast<int64_t>(n) * (W + 2), plan, 0);  // the alignment gap
     plan_sharing(P, seq_ids, n, plan);
+    share_rows = plan + 4;
+    first.assign(n, 0);
+    const int32_t* items = plan + 4 + 4 * static_cast<int64_t>(n);
+    for (int32_t it = 0; it < plan[0]; ++it) first[items[8 * it]] = 1;
+  }
+  // the tables and lengths after the append (the sequences were checked above); entries past a
+  // table's end, and a run's shared entries in its rows after the first, are left as they were:
+  // no kernel reads them
+  for (int32_t i = 0; i < n; ++i) {
+    const SeqState& s = P.seqs[seq_ids[i]];
+    const int64_t from = (share_rows && !first[i]) ? share_rows[4 * static_cast<int64_t>(i)] : 0;
+    std::copy(s.table.begin() + from, s.table.end(), tables + static_cast<int64_t>(i) * W + from);
+    lens[i] = static_cast<int32_t>(s.len);
   }
   return PKV_OK;
 }

@@ -66,6 +66,7 @@ struct Pool {
   // share_ctas: the SMs a step may use
   int32_t share_min_members = 0, share_min_blocks = 1, share_ctas = 0;
   std::vector<int32_t> share_scratch;  // planner scratch
+  std::vector<uint8_t> share_first;    // planner scratch: rows that begin a run
 
   std::mutex tmap_mu;
   TensorMaps* tmaps = nullptr;

@@ -31,8 +31,10 @@ def _parse(meta, n, W, sharing=True):
     return slots, tables, lens, hdr, rows, items
 
 
-def _check_plan(n, B, tables, lens, hdr, rows, items, slot_cap):
-    """Everything the device side relies on, from the plan alone."""
+def _check_plan(n, B, tables, lens, hdr, rows, items, slot_cap, full=None):
+    """Everything the device side relies on, from the plan alone.  `tables` are the step
+    metadata's tables (a run's shared entries are written only in its first row); `full` are
+    the pool's own tables of the same rows (pkv_export_tables), when given."""
     n_items, max_members, n_slots = int(hdr[0]), int(hdr[1]), int(hdr[2])
     assert len(items) == n_items
     used = np.zeros(n_slots, np.int32)
@@ -58,10 +60,19 @@ def _check_plan(n, B, tables, lens, hdr, rows, items, slot_cap):
             assert not in_group[r]
             in_group[r] = True
             assert tuple(rows[r]) == (kb, len(its), its[0][2] + (r - rb), re - rb)
-            assert np.array_equal(tables[r, :kb], tables[rb, :kb]), "the shared blocks are the first member's"
             assert kb * B < lens[r], "each member keeps a token of its own after the shared blocks"
+            if full is not None:
+                nb = -(-int(lens[r]) // B)
+                assert np.array_equal(full[r, :kb], full[rb, :kb]), "the shared blocks are the first member's"
+                assert np.array_equal(tables[r, kb:nb], full[r, kb:nb]), "the row's own entries are written"
+                if r == rb:
+                    assert np.array_equal(tables[r, :nb], full[r, :nb]), "the first row's table is whole"
     assert not rows[~in_group].any(), "rows outside groups have no prefix"
     return groups
+
+
+def _full(pool, ids, W):
+    return pkv.pkv_export_tables(pool, ids, W)[0]
 
 
 def _forked_batch(pool, prefix, n_kids, suffixes):
@@ -97,7 +108,7 @@ def test_two_groups_among_unrelated_rows():
     cows = pkv.pkv_step_plan(pool, ids, W, meta)
     assert len(cows) == 10 + sum(1 for k in range(40) if pkv.pkv_seq_len(pool, kp[k]) - 1 == 1000 and 1000 % 16)
     _, tables, lens, hdr, rows, items = _parse(meta, n, W)
-    groups = _check_plan(n, 16, tables, lens, hdr, rows, items, 2 * n + 1024)
+    groups = _check_plan(n, 16, tables, lens, hdr, rows, items, 2 * n + 1024, _full(pool, ids, W))
     assert set(groups) == {(1, 41), (42, 52)}
     assert rows[1, 0] == 1000 // 16  # 62 full blocks of P's prefix
     assert rows[42, 0] == 4104 // 16  # 256 full blocks of Q's (the tail block went to copies)
@@ -122,7 +133,7 @@ def test_small_runs_are_not_grouped_and_min_blocks_holds():
     meta = np.zeros(pkv.pkv_step_meta_ints(pool, n, W), np.int32)
     pkv.pkv_step_plan(pool, ids, W, meta)
     _, tables, lens, hdr, rows, items = _parse(meta, n, W)
-    groups = _check_plan(n, 16, tables, lens, hdr, rows, items, 2 * n + 1024)
+    groups = _check_plan(n, 16, tables, lens, hdr, rows, items, 2 * n + 1024, _full(pool, ids, W))
     assert set(groups) == {(8, 14)}
     assert rows[8, 0] == 8
 
@@ -139,7 +150,7 @@ def test_prefix_stops_before_each_rows_last_token():
     meta = np.zeros(pkv.pkv_step_meta_ints(pool, n, W), np.int32)
     pkv.pkv_step_plan(pool, ids, W, meta)
     _, tables, lens, hdr, rows, items = _parse(meta, n, W)
-    _check_plan(n, 16, tables, lens, hdr, rows, items, 2 * n + 1024)
+    _check_plan(n, 16, tables, lens, hdr, rows, items, 2 * n + 1024, _full(pool, ids, W))
     assert list(rows[:4, 0]) == [4] * 4 and list(rows[4:, 0]) == [3] * 4
 
 
@@ -153,7 +164,7 @@ def test_caps_hold_with_a_huge_grid_target():
     meta = np.zeros(pkv.pkv_step_meta_ints(pool, n, W), np.int32)
     pkv.pkv_step_plan(pool, ids, W, meta)
     _, tables, lens, hdr, rows, items = _parse(meta, n, W)
-    groups = _check_plan(n, 16, tables, lens, hdr, rows, items, 2 * n + 1024)
+    groups = _check_plan(n, 16, tables, lens, hdr, rows, items, 2 * n + 1024, _full(pool, ids, W))
     assert len(groups) == 20
     assert hdr[2] <= 2 * n + 1024 and hdr[0] <= n + 256
     for its in groups.values():
@@ -168,7 +179,7 @@ def test_sixteen_head_groups_take_sixteen_members_per_cta():
     meta = np.zeros(pkv.pkv_step_meta_ints(pool, n, W), np.int32)
     pkv.pkv_step_plan(pool, kids, W, meta)
     _, tables, lens, hdr, rows, items = _parse(meta, n, W)
-    groups = _check_plan(n, 16, tables, lens, hdr, rows, items, 2 * n + 1024)
+    groups = _check_plan(n, 16, tables, lens, hdr, rows, items, 2 * n + 1024, _full(pool, kids, W))
     ((rb, re), its), = groups.items()
     assert (rb, re) == (0, 40)
     assert len(its) == 152 // (3 * 8)  # 40 members: 3 CTAs of 16 per KV head and split
@@ -187,7 +198,7 @@ def test_side_by_side_split_for_the_forked_shape():
     meta = np.zeros(pkv.pkv_step_meta_ints(pool, n, W), np.int32)
     pkv.pkv_step_plan(pool, kids, W, meta)
     _, tables, lens, hdr, rows, items = _parse(meta, n, W)
-    groups = _check_plan(n, 16, tables, lens, hdr, rows, items, 2 * n + 1024)
+    groups = _check_plan(n, 16, tables, lens, hdr, rows, items, 2 * n + 1024, _full(pool, kids, W))
     ((rb, re), its), = groups.items()
     assert (rb, re) == (0, 64) and rows[0, 0] == 1023
     ctas = 2 * 8 * len(its)
@@ -202,7 +213,7 @@ def test_fp8_pools_keep_the_decode_on_every_sm():
     meta = np.zeros(pkv.pkv_step_meta_ints(pool, n, W), np.int32)
     pkv.pkv_step_plan(pool, kids, W, meta)
     _, tables, lens, hdr, rows, items = _parse(meta, n, W)
-    _check_plan(n, 16, tables, lens, hdr, rows, items, 2 * n + 1024)
+    _check_plan(n, 16, tables, lens, hdr, rows, items, 2 * n + 1024, _full(pool, kids, W))
     assert hdr[3] == 0 and hdr[0] == 152 // 16
 
 
