@@ -255,8 +255,11 @@ typedef struct CUevent_st* pkv_event_t; /* identical to cudaEvent_t */
  * blocks once for the whole run (a tcgen05 kernel, all the run's queries of a KV
  * head as 128-row tiles against each key tile, in splits of whole blocks sized so
  * that its grid comes near target_ctas CTAs) and to each row's own blocks in the
- * decode kernel, which merges the two with the online-softmax rule ([KVM] "Chunked
- * prefill mechanics").  The result is the same attention (within rounding).
+ * decode kernel; a combine kernel merges the two with the online-softmax rule ([KVM]
+ * "Chunked prefill mechanics").  With 16-bit pools and up to 8 query heads per KV head
+ * the step may run the decode on part of the SMs beside the prefix kernel on the
+ * others (the split comes from a time model of the two kernels).  The result is the
+ * same attention (within rounding).
  *   min_members: 0 turns sharing off (the default); else >= 2.
  *   min_blocks : >= 1.
  *   target_ctas: <= 0 takes the current device's SM count (PKV_ERR_CUDA without one).
@@ -578,7 +581,10 @@ int pkv_device_code_version(int32_t* binary_version, int32_t* ptx_version);
 
 /* Synchronize the stream, then read and clear the current device's error word.
  * Returns DEVICE_CHECK if a kernel recorded a bad index since the last check;
- * *code (kernel-specific, nonzero) and *detail (the offending value) describe it.
+ * *code and *detail (the offending value) describe it: 1 a slot out of range (append),
+ * 2 a sequence length < 0 or > W * B, 3 a block id out of range in a table, 4 a bounded
+ * wait that gave up (detail: where), 6 a prefill chunk longer than max_q, 7 a
+ * shared-prefix plan entry out of range (detail: the sequence or work item).
  * Either output pointer may be NULL. */
 int pkv_check_device_error(pkv_stream_t stream, int32_t* code, int64_t* detail);
 

@@ -381,7 +381,7 @@ __device__ __forceinline__ uint32_t bf16x2_rn_f16x2(uint32_t w) {
 // queries of batch rows [rb, re) (rows that share their first table blocks), every one of them
 // against all keys of blocks [kb0, kb1) of row rb's table (no causal edge: the prefix precedes
 // every query); the epilogue leaves the partial (m, l, unnormalised O) of each (row, head) in
-// slot slot_base + (row - rb) of a.prior_ml / a.prior_o for the decode kernel to fold in.
+// slot slot_base + (row - rb) of a.prior_ml / a.prior_o for the combine kernel.
 template <typename T, bool KV8, bool SH = false>
 __global__ void __launch_bounds__(UM_THREADS, 1) prefill_umma_kernel(const __grid_constant__ CUtensorMap tmq,
                                                                       const __grid_constant__ CUtensorMap tmk,
