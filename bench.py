@@ -491,7 +491,8 @@ class DecodeRunner:
 class AgentRunner(DecodeRunner):
     name = "agent32k"
 
-    def __init__(self, torch, pkv, dev, total_steps, n_seq=48, context=32768, kv_dtype="bf16", q_heads=0):
+    def __init__(self, torch, pkv, dev, total_steps, n_seq=48, context=32768, kv_dtype="bf16", q_heads=0,
+                 shared=0, share=8):
         super().__init__(torch, pkv, dev, total_steps)
         wl = W.agent(n_seq, context, spare_steps=total_steps + 16)
         self.wl, self.seed = wl, wl.seed
@@ -503,9 +504,22 @@ class AgentRunner(DecodeRunner):
         self.n_max = n_seq
         self.scale = wl.scale
         self.pool = self._new_pool(wl.free_order)
-        self.ids = [pkv.pkv_seq_create(self.pool) for _ in range(n_seq)]
+        if shared:
+            # "KV Cache Management", structured prefix sharing: every agent's context begins with the
+            # same `shared` tokens (one parent's, forked: the same physical blocks), then its own
+            if share:
+                pkv.pkv_pool_set_prefix_sharing(self.pool, share, 1, 0)
+            parent = pkv.pkv_seq_create(self.pool)
+            pkv.pkv_plan_append(self.pool, [parent], [shared])
+            self.ids = [pkv.pkv_seq_fork(self.pool, parent) for _ in range(n_seq)]
+            pkv.pkv_plan_append(self.pool, self.ids, [context - shared] * n_seq)
+            self.unique_tokens = shared + n_seq * (context - shared)  # grows by one token per agent per step
+            self.share_desc = (f"on: runs of >= {share} rows sharing their first blocks attend to them once per step "
+                               "(pkv_pool_set_prefix_sharing)" if share else "off: every agent reads the prefix")
+        else:
+            self.ids = [pkv.pkv_seq_create(self.pool) for _ in range(n_seq)]
+            pkv.pkv_plan_append(self.pool, self.ids, [context] * n_seq)
         self.ids_np = np.array(self.ids, np.int32)
-        pkv.pkv_plan_append(self.pool, self.ids, [context] * n_seq)
         # the pool's contents are the prompt keys/values: N(0,1) drawn on the device
         self.kp = W.device_normal(self.seed, "k_pool", g.pool_shape(), g.dtype, dev)
         self.vp = W.device_normal(self.seed, "v_pool", g.pool_shape(), g.dtype, dev)
@@ -513,9 +527,17 @@ class AgentRunner(DecodeRunner):
         self.inputs_for_steps("agent")
         self._alloc_common(n_seq)
         self.config = dict(workload_config("agent32k", g, n_seq, context), pool_blocks=g.num_blocks)
+        if shared:
+            self.config["workload"] += (f"; the first {shared:,} tokens shared by all (one parent's prefix, forked: "
+                                        "structured prefix sharing)")
+            self.config["shared_prefix_tokens"] = shared
 
     def running(self, t):
         return self.ids_np
+
+    def after_step(self, t, ids):
+        if hasattr(self, "unique_tokens"):
+            self.unique_tokens += len(ids)
 
 
 class ChatRunner(DecodeRunner):
@@ -679,9 +701,9 @@ def run_decode(args, torch, pkv, dev, world, rank):
     kw = {} if args.workload == "tiny" else {"kv_dtype": args.kv_dtype}
     if args.workload == "forked":
         kw["share"] = args.share
-    if args.workload == "agent32k" and (args.context or args.n_seq or args.q_heads):
+    if args.workload == "agent32k" and (args.context or args.n_seq or args.q_heads or args.shared_prefix):
         r = AgentRunner(torch, pkv, dev, total, n_seq=args.n_seq or 48, context=args.context or 32768,
-                        q_heads=args.q_heads, **kw)
+                        q_heads=args.q_heads, shared=args.shared_prefix, share=args.share, **kw)
     else:
         r = RUNNERS[args.workload](torch, pkv, dev, total, **kw)
     if args.l2_flush:
@@ -791,6 +813,7 @@ def config_records(args, torch, pkv, dev, world, rank, steps: int = 20):
         sub = argparse.Namespace(**vars(args))
         sub.workload, sub.steps, sub.warmup = name, steps, 3
         sub.l2_flush, sub.kv_dtype, sub.q_heads, sub.context, sub.n_seq, sub.traffic = False, "bf16", 0, 0, 0, None
+        sub.shared_prefix = 0
         ln, r = run_decode(sub, torch, pkv, dev, world, rank)
         recs[name] = {"workload": ln["config"]["workload"], "value": ln["value"], "unit": ln["unit"],
                       "ms_per_step": ln["ms_per_step"], "tokens_per_s": ln["tokens_per_s"],
@@ -1506,7 +1529,11 @@ def main():
     ap.add_argument("--swap-chunks", type=int, default=512,
                     help="swap workload: chunks evicted and restored (default 512, 42.9 GB; fewer for small captures)")
     ap.add_argument("--share", type=int, default=8,
-                    help="forked: prefix sharing, the least rows of a run that shares its first blocks (0: off)")
+                    help="forked / --shared-prefix: prefix sharing, the least rows of a run that shares its first "
+                         "blocks (0: off)")
+    ap.add_argument("--shared-prefix", type=int, default=0,
+                    help="agent32k: the first S tokens of every context are one parent's prefix, forked (structured "
+                         "prefix sharing, e.g. 24576 with --context 32768)")
     ap.add_argument("--no-config-records", action="store_true",
                     help="default line: skip the bounded tiny / chat / forked runs added to it")
     ap.add_argument("--no-swap-record", action="store_true",

@@ -14,7 +14,7 @@ import pytest
 import oracle
 import paged_kv_cache_80_gb300 as pkv
 import workloads as W
-from helpers import PagedBatch, check_attention, out_f64, to_dev
+from helpers import PagedBatch, check_attention, out_f64, to_dev, to_raw
 
 pytestmark = pytest.mark.gpu
 
@@ -243,6 +243,64 @@ def test_shared_prefix_beyond_the_in_kernel_plan():
     tables, lens = b.tables(run.tolist(), Wd)
     check_attention(out_f64(out, "bf16"), b.decode_ref(q, tables, lens, scale), "bf16")
     b.check_state()
+
+
+def test_agents_over_a_shared_prompt_sampled():
+    """Structured prefix sharing ("KV Cache Management", Step 5: a 24,576-token shared system
+    prompt and repository index, 8,192 tokens of each agent's own): 48 agents forked from one
+    parent, one decode step with sharing on (pkv_step_plan, then pkv_step_launch), the shape
+    `bench.py --shared-prefix 24576` times.  Sampled agents against the oracle, which gets host
+    copies of exactly their blocks from before the step plus the step's new tokens written on
+    the host."""
+    import torch
+
+    wl = W.agent(48, 32768, spare_steps=32)
+    g = wl.geometry
+    kp = W.device_normal(wl.seed, "k_pool_shared", g.pool_shape(), g.dtype, "cuda")
+    vp = W.device_normal(wl.seed, "v_pool_shared", g.pool_shape(), g.dtype, "cuda")
+    b = PagedBatch(g, wl.free_order, seed=wl.seed, host_pool=False, fill_device=(kp, vp))
+    pkv.pkv_pool_set_prefix_sharing(b.lib, 8, 1, 0)
+    (parent,) = b.new_seqs(1)
+    b.append([parent], [24576], "prompt", plan_only=True)
+    kids = [b.fork(parent) for _ in range(48)]
+    b.append(kids, [8192] * 48, "own", plan_only=True)
+    run = np.array(kids, np.int32)
+    n, Wd = len(run), 2050
+    mi = pkv.pkv_step_meta_ints(b.lib, n, Wd)
+    meta_host = torch.zeros(mi, dtype=torch.int32).pin_memory()
+    meta_dev = torch.zeros(mi, dtype=torch.int32, device="cuda")
+    ws = torch.empty(pkv.pkv_decode_workspace_size(b.lib, n), dtype=torch.uint8, device="cuda")
+    cows = pkv.pkv_step_plan(b.lib, run, Wd, meta_host)
+    oslots, ocows = b.orc.append(run.tolist(), [1] * n)
+    assert np.array_equal(meta_host[:n].numpy(), oslots) and len(cows) == len(ocows) == 0
+    assert _plan_header(meta_host.numpy(), n, Wd)[1] == 48  # one run of all 48 agents
+    sample = [0, 23, 47]
+    tables, lens = b.tables(run.tolist(), Wd)
+    used = sorted({int(x) for r in sample for x in tables[r, : -(-int(lens[r]) // g.block_size)]})
+    remap = {blk: j for j, blk in enumerate(used)}
+    idx = torch.tensor(used, dtype=torch.long, device="cuda")
+    hk = to_raw(kp.index_select(0, idx), g.dtype)  # before the step writes anything
+    hv = to_raw(vp.index_select(0, idx), g.dtype)
+    q = W.normal(wl.seed, "sq", (n, g.H_q, g.d_head), g.dtype)
+    kn = W.normal(wl.seed, "sk", (n, g.H_kv, g.d_head), g.dtype)
+    vn = W.normal(wl.seed, "sv", (n, g.H_kv, g.d_head), g.dtype)
+    out = torch.full((n, g.H_q, g.d_head), float("nan"), dtype=torch.bfloat16, device="cuda")
+    pkv.pkv_step_launch(b.lib, 0, n, Wd, cows, to_dev(q, "bf16"), to_dev(kn, "bf16"), to_dev(vn, "bf16"), kp, vp,
+                        wl.scale, out, meta_host, meta_dev, ws)
+    torch.cuda.synchronize()
+    pkv.pkv_check_device_error()
+    got = out_f64(out, "bf16")
+    assert np.all(np.isfinite(got))
+    gc = W.Geometry(g.L, g.H_q, g.H_kv, g.d_head, g.block_size, g.dtype, len(used))
+    cslots = np.array([remap[int(oslots[r]) // g.block_size] * g.block_size + int(oslots[r]) % g.block_size
+                       for r in sample], np.int32)
+    oracle.write_slots(gc, 0, kn[sample], vn[sample], cslots, hk, hv)
+    ct = np.zeros((len(sample), Wd), np.int32)
+    for i, r in enumerate(sample):
+        nb = -(-int(lens[r]) // g.block_size)
+        ct[i, :nb] = [remap[int(x)] for x in tables[r, :nb]]
+    ref = oracle.decode_attention(gc, 0, q[sample], hk, hv, ct, lens[sample], wl.scale)
+    check_attention(got[sample], ref, "bf16")
 
 
 def test_corrupt_plan_header_is_rejected():
