@@ -361,8 +361,8 @@ int pkv_decode_step_host(pkv_pool* pool, int32_t layer, const int32_t* seq_ids, 
  *     before any stream capture.
  *   - A batch that needs more scratch than 24 MiB is rejected with
  *     PKV_ERR_INVALID_ARG (the partials of one persistent grid on a 152-SM GB300
- *     take about 10 MB for groups of up to 8 query heads and 20 MB for 9 to 16;
- *     each sequence adds 8 bytes).
+ *     take about 10 MB for 16-bit pools with groups of up to 8 query heads, 18 MB
+ *     for FP8 pools and 20 MB for groups of 9 to 16; each sequence adds 8 bytes).
  *   - Every call on a device shares the one array and leaves its contents behind;
  *     nothing in it needs to start at zero.  Calls whose GPU work overlaps (two
  *     streams, or two threads) race on it: order them on one stream.

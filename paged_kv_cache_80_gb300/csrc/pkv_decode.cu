@@ -977,17 +977,17 @@ struct TcVariant {
 };
 
 // Pipeline depth and warps per CTA; PKV_TC_VARIANT selects another for tuning.  An
-// FP8 tile carries half the bytes of a 16-bit one and more instructions, so its
-// default pipeline is twice as deep and its CTAs smaller: 4 stages x 2 warps, 4 CTAs
-// (8 warps) per SM, the same bytes in flight as the 16-bit default.
-// Groups of 9 to 16 query heads (two head blocks) hold twice the accumulators (255
-// registers a thread), so at most 8 warps fit an SM: every pool type takes 2 stages x
-// 4 warps there (FP8, agent 48 x 32,768 with 16-head groups: 0.81 of the copy peak, against
-// 0.79 for 3 x 2 and 0.61 for 4 x 2, which fits only 6 warps); FP8 is built in 3 x 2 as well.
+// FP8 tile carries half the bytes of a 16-bit one and more instructions per byte, so
+// its default CTAs are small: 2 stages x 2 warps, 7 CTAs (14 warps) per SM at 146
+// registers (agent 48 x 32,768: 1.014 of the copy peak against 0.996 for 4 x 2 and 1.010
+// for 2 x 4; 12 x 131,072: 1.018 against 0.999; chat's attention 36.7 against 38.8 us).
+// Groups of 9 to 16 query heads (two head blocks) hold twice the accumulators: every pool
+// type takes 2 stages x 4 warps there (FP8 with 16-head groups: 0.906 against 0.745 for
+// 3 x 2); FP8 is built in 3 x 2 as well.
 TcVariant tc_variant(const Pool& P) {
   static const TcVariant table[] = {{2, 4}, {3, 4}, {4, 4}, {2, 8}, {3, 2}, {6, 4}, {2, 2}, {4, 2}, {3, 1}};
   const bool fp8 = P.geo.dtype == PKV_E4M3, wide = P.geo.H_q / P.geo.H_kv > GPAD;
-  int idx = fp8 && !wide ? 7 : 0;
+  int idx = fp8 && !wide ? 6 : 0;
   if (const char* e = std::getenv("PKV_TC_VARIANT")) {
     // only variants built for this pool type: 0-4 for 16-bit pools, 0-8 for FP8; 0 (and 4
     // for FP8) with groups of 9 to 16 heads (pick_tc builds no others)
@@ -1475,9 +1475,10 @@ int launch_decode(Pool& P, int32_t layer, const void* q, const void* k_pool, con
 namespace pkv {
 namespace {
 
-// 24 MiB: the stream-K partials of one persistent grid (about 10 MB on a 152-SM
-// GB300 for groups of up to 8 query heads, about 20 MB for 9 to 16) plus
-// per-sequence prefix and length arrays.  Held by every GPU that loads the library
+// 24 MiB: the stream-K partials of one persistent grid (on a 152-SM GB300 about 10 MB
+// for 16-bit pools with groups of up to 8 query heads, 18 MB for FP8 pools -- more,
+// smaller CTAs -- and 20 MB for groups of 9 to 16) plus per-sequence prefix and
+// length arrays.  Held by every GPU that loads the library
 // until the process exits.
 constexpr size_t kNoallocScratchBytes = size_t(24) << 20;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
