@@ -798,7 +798,8 @@ static void plan_sharing(Pool& P, const int32_t* ids, int32_t n, int32_t* plan) 
       const SeqState& b = P.seqs[ids[j]];
       const int64_t cb = std::min<int64_t>(c, (b.len - 1) / B);
       int64_t k = 0;  // the common leading entries: 64 at a time while they match, then one by one
-      while (k + 64 <= cb && std::memcmp(a.table.data() + k, b.table.data() + k, 64 * sizeof(int32_t)) == 0) k += 64;
+      while (k + 64 <= cb && std::memcmp(a.table.data() + k, b.table.data() + k, 64 * sizeof(int32_t)) == 0)
+        k += 64;
       while (k < cb && a.table[k] == b.table[k]) ++k;
       if (k < P.share_min_blocks || 2 * k < c) break;
       c = k;

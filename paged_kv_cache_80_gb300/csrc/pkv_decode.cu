@@ -530,8 +530,9 @@ __global__ void __launch_bounds__(NW * 32) decode_tc_kernel(const __grid_constan
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int gw = blockIdx.x * NW + warp;
-  // a programmatic dependent launched after this grid (the combine kernel of a step with shared
-  // prefixes) may become resident now; it waits for this grid's completion before reading
+  // a programmatic dependent launched after this grid (the prefix kernel of a step with shared
+  // prefixes) may become resident now; it reads nothing this grid writes, and waits for this
+  // grid before it completes
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -1409,7 +1410,7 @@ int launch_decode(Pool& P, int32_t layer, const void* q, const void* k_pool, con
     a.partials = reinterpret_cast<float*>(w + L.partials);
     a.total_warps = grid * nw;
     CUtensorMap maps[2] = {tk, tv};
-    if (shared) {  // the shared blocks once per run of rows, before the step's append and decode
+    if (shared) {  // the plan's rows and work items, and the partials' room in the workspace
       if (reinterpret_cast<uintptr_t>(share->plan_dev) & 15)
         return fail(PKV_ERR_INVALID_ARG, "the shared-prefix plan must be 16-byte aligned");
       a.share = reinterpret_cast<const int4*>(share->plan_dev + 4);
