@@ -303,6 +303,57 @@ def test_agents_over_a_shared_prompt_sampled():
     check_attention(got[sample], ref, "bf16")
 
 
+def _one_step_against_oracle(b, run, Wd, seed):
+    """One pkv_decode_step over `run`, every row against the oracle; returns the plan header."""
+    import torch
+
+    g = b.g
+    n = len(run)
+    mi = pkv.pkv_step_meta_ints(b.lib, n, Wd)
+    meta_host = torch.zeros(mi, dtype=torch.int32).pin_memory()
+    meta_dev = torch.zeros(mi, dtype=torch.int32, device="cuda")
+    ws = torch.empty(pkv.pkv_decode_workspace_size(b.lib, n), dtype=torch.uint8, device="cuda")
+    scale = 1.0 / math.sqrt(g.d_head)
+    q = W.normal(seed, "q", (n, g.H_q, g.d_head), "bf16")
+    kn = W.normal(seed, "k", (n, g.H_kv, g.d_head), "bf16")
+    vn = W.normal(seed, "v", (n, g.H_kv, g.d_head), "bf16")
+    out = torch.full((n, g.H_q, g.d_head), float("nan"), dtype=torch.bfloat16, device="cuda")
+    pkv.pkv_decode_step(b.lib, 0, run, Wd, to_dev(q, "bf16"), to_dev(kn, "bf16"), to_dev(vn, "bf16"), b.kp, b.vp,
+                        scale, out, meta_host, meta_dev, ws)
+    torch.cuda.synchronize()
+    hdr = _plan_header(meta_host.numpy(), n, Wd)
+    oslots, ocows = b.orc.append(run.tolist(), [1] * n)
+    if len(ocows):
+        oracle.copy_blocks(g, ocows, b.hk, b.hv)
+    oracle.write_slots(g, 0, kn, vn, oslots, b.hk, b.hv)
+    pkv.pkv_check_device_error()
+    tables, lens = b.tables(run.tolist(), Wd)
+    check_attention(out_f64(out, "bf16"), b.decode_ref(q, tables, lens, scale), "bf16")
+    b.check_pools_bitexact()
+    return hdr
+
+
+def test_rows_with_a_single_token_of_their_own():
+    """40 branches of a 4,096-token prefix (256 full blocks) with no suffix: after the step each
+    row's only own token is the step's, in a block of its own."""
+    g = W.Geometry(L=1, H_q=64, H_kv=8, d_head=128, block_size=16, dtype="bf16", num_blocks=1024)
+    b = PagedBatch(g, W.permutation(76, "fo", g.num_blocks), seed=76)
+    pkv.pkv_pool_set_prefix_sharing(b.lib, 4, 1, 0)
+    (parent,) = b.new_seqs(1)
+    b.append([parent], [4096], "prefix")
+    run = np.array([b.fork(parent) for _ in range(40)], np.int32)
+    hdr = _one_step_against_oracle(b, run, 260, 76)
+    assert hdr[0] >= 1 and hdr[1] == 40, hdr
+
+
+def test_sharing_on_without_a_run_long_enough():
+    """Sharing on, but no run reaches min_members: the plan is empty and the step is the plain
+    decode (with the larger metadata)."""
+    b, run = _build("bf16", 64, seed=77, members=(5, 6), prefixes=(700, 900), min_members=8)
+    hdr = _one_step_against_oracle(b, run, 80, 77)
+    assert hdr == [0, 0, 0, 0], hdr
+
+
 def test_corrupt_plan_header_is_rejected():
     import torch
 
