@@ -805,15 +805,18 @@ def run_decode(args, torch, pkv, dev, world, rank):
 
 
 def config_records(args, torch, pkv, dev, world, rank, steps: int = 20):
-    """Bounded runs of the other decode configurations (tiny, chat, forked) for the default
-    line: the same measurement as `--workload <name>` at `steps` timed steps, reduced to its
-    key figures."""
+    """Bounded runs of the other decode configurations (tiny, chat, forked, and the agents over a
+    shared 24,576-token prompt of "KV Cache Management", Step 5) for the default line: the same
+    measurement as `--workload <name>` (`--workload agent32k --shared-prefix 24576`) at `steps`
+    timed steps, reduced to its key figures."""
     recs = {}
-    for name in ("tiny", "chat", "forked"):
+    for name in ("tiny", "chat", "forked", "agent_shared_prompt"):
         sub = argparse.Namespace(**vars(args))
         sub.workload, sub.steps, sub.warmup = name, steps, 3
         sub.l2_flush, sub.kv_dtype, sub.q_heads, sub.context, sub.n_seq, sub.traffic = False, "bf16", 0, 0, 0, None
         sub.shared_prefix = 0
+        if name == "agent_shared_prompt":
+            sub.workload, sub.shared_prefix, sub.share = "agent32k", 24576, 8
         ln, r = run_decode(sub, torch, pkv, dev, world, rank)
         recs[name] = {"workload": ln["config"]["workload"], "value": ln["value"], "unit": ln["unit"],
                       "ms_per_step": ln["ms_per_step"], "tokens_per_s": ln["tokens_per_s"],
@@ -1535,7 +1538,7 @@ def main():
                     help="agent32k: the first S tokens of every context are one parent's prefix, forked (structured "
                          "prefix sharing, e.g. 24576 with --context 32768)")
     ap.add_argument("--no-config-records", action="store_true",
-                    help="default line: skip the bounded tiny / chat / forked runs added to it")
+                    help="default line: skip the bounded tiny / chat / forked / shared-prompt agent runs added to it")
     ap.add_argument("--no-swap-record", action="store_true",
                     help="decode workloads: skip the bounded swap measurement added to the line")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -1610,7 +1613,8 @@ def main():
         runner._last_launcher = None
         torch.cuda.empty_cache()
         line["swap"] = swap_record(torch, pkv, dev)
-    if (world == 1 and args.workload == "agent32k" and not (args.context or args.n_seq or args.q_heads)
+    if (world == 1 and args.workload == "agent32k" and not (args.context or args.n_seq or args.q_heads
+                                                            or args.shared_prefix)
             and args.kv_dtype == "bf16" and not args.no_config_records):
         # driver-observed figures for the other decode configurations, bounded
         runner = None
