@@ -84,3 +84,32 @@ def test_full_size_buffers_pass_the_size_checks():
     with pytest.raises(TypeError, match="CUDA tensor"):
         pkv.pkv_step_launch(lib, 0, n, W, np.zeros((0, 2), np.int32), b["q"], b["k_new"], b["v_new"], kp, kp, 0.1,
                             b["out"], b["meta_host"], b["meta_dev"], ws)
+
+
+def test_sharing_enlarges_the_metadata_the_binding_checks():
+    """With prefix sharing on, a step's metadata holds the shared-prefix plan after the lengths:
+    a buffer of the plain n*(W+2) int32 is now too small, for the planning call as for the
+    launches, and is rejected before the library writes past it."""
+    lib = pkv.pkv_pool_create(1, 16, 2, 128, 16, "bf16", 256)
+    parent = pkv.pkv_seq_create(lib)
+    pkv.pkv_plan_append(lib, [parent], [100])
+    ids = np.array([pkv.pkv_seq_fork(lib, parent) for _ in range(5)], np.int32)
+    n, W = len(ids), 12
+    assert pkv.pkv_step_meta_ints(lib, n, W) == n * (W + 2)
+    pkv.pkv_pool_set_prefix_sharing(lib, 4, 1, 152)
+    need = pkv.pkv_step_meta_ints(lib, n, W)
+    assert need > n * (W + 2)
+    before = [pkv.pkv_seq_len(lib, s) for s in ids]
+    with pytest.raises(ValueError, match="meta_host"):
+        pkv.pkv_step_plan(lib, ids, W, torch.zeros(n * (W + 2), dtype=torch.int32))
+    assert [pkv.pkv_seq_len(lib, s) for s in ids] == before  # nothing planned
+    meta = torch.zeros(need, dtype=torch.int32)
+    pkv.pkv_step_plan(lib, ids, W, meta)  # the right size plans: one group of the 5 branches
+    off = (n * (W + 2) + 3) // 4 * 4
+    assert int(meta[off]) >= 1 and int(meta[off + 1]) == 5
+    q = torch.zeros((n, 16, 128), dtype=torch.bfloat16)
+    kv = torch.zeros((n, 2, 128), dtype=torch.bfloat16)
+    ws = torch.zeros(16, dtype=torch.uint8)
+    with pytest.raises(ValueError, match="meta_dev"):
+        pkv.pkv_step_launch(lib, 0, n, W, np.zeros((0, 2), np.int32), q, kv, kv, q, q, 0.1, q, meta,
+                            torch.zeros(n * (W + 2), dtype=torch.int32), ws)
