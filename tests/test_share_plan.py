@@ -228,3 +228,46 @@ def test_option_validation():
         with pytest.raises(pkv.PkvError) as e:
             pkv.pkv_pool_set_prefix_sharing(_pool(**kw), 4, 1, 152)
         assert e.value.name == "PKV_ERR_UNSUPPORTED", kw
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_random_fork_trees_and_batch_orders(seed):
+    """Seeded random pools: parents of random lengths, branches forked at random depths (some
+    from branches), random suffixes, unrelated sequences, a random batch order and random
+    option values; every plan must satisfy the invariants the kernels rely on."""
+    rng = np.random.default_rng(1000 + seed)
+    B = int(rng.choice([16, 32]))
+    H_q = int(rng.choice([64, 128]))
+    pool = _pool(H_q=H_q, B=B, N=8192)
+    pkv.pkv_pool_set_prefix_sharing(pool, int(rng.integers(2, 6)), int(rng.integers(1, 4)),
+                                    int(rng.choice([64, 152, 300])))
+    seqs = []
+    for _ in range(int(rng.integers(1, 4))):  # fork trees
+        root = pkv.pkv_seq_create(pool)
+        pkv.pkv_plan_append(pool, [root], [int(rng.integers(1, 600))])
+        nodes = [root]
+        for _ in range(int(rng.integers(2, 20))):
+            parent = nodes[int(rng.integers(0, len(nodes)))]
+            kid = pkv.pkv_seq_fork(pool, parent)
+            grow = int(rng.integers(0, 120))
+            if grow:
+                pkv.pkv_plan_append(pool, [kid], [grow])
+            nodes.append(kid)
+        seqs += nodes
+    for _ in range(int(rng.integers(0, 6))):  # unrelated sequences
+        s = pkv.pkv_seq_create(pool)
+        pkv.pkv_plan_append(pool, [s], [int(rng.integers(0, 300))])
+        seqs.append(s)
+    ids = np.array(seqs, np.int32)
+    if rng.random() < 0.5:
+        ids = ids[rng.permutation(len(ids))]
+    else:
+        ids = np.sort(ids)  # branches of one tree next to each other
+    n = len(ids)
+    W = max(pkv.pkv_seq_len(pool, int(s)) for s in ids) // B + 2
+    for step in range(2):
+        meta = np.zeros(pkv.pkv_step_meta_ints(pool, n, W), np.int32)
+        pkv.pkv_step_plan(pool, ids, W, meta)
+        _, tables, lens, hdr, rows, items = _parse(meta, n, W)
+        _check_plan(n, B, tables, lens, hdr, rows, items, 2 * n + 1024, _full(pool, ids, W))
+        assert 0 <= hdr[3] <= 300
