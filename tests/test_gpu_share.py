@@ -354,6 +354,43 @@ def test_sharing_on_without_a_run_long_enough():
     assert hdr == [0, 0, 0, 0], hdr
 
 
+def test_shared_prefix_step_on_the_second_layer():
+    """A two-layer pool: the step runs on layer 1, so the prefix kernel, the decode and the
+    append all address layer 1's slabs of every block."""
+    import torch
+
+    g = W.Geometry(L=2, H_q=64, H_kv=8, d_head=128, block_size=16, dtype="bf16", num_blocks=512)
+    b = PagedBatch(g, W.permutation(78, "fo", g.num_blocks), seed=78)
+    pkv.pkv_pool_set_prefix_sharing(b.lib, 4, 1, 0)
+    (parent,) = b.new_seqs(1)
+    b.append([parent], [1500], "prefix", layer=-1)
+    run = [b.fork(parent) for _ in range(12)]
+    b.append(run, [int(x) for x in W.substream(78, "sfx").integers(0, 60, 12)], "suffix", layer=-1)
+    run = np.array(run, np.int32)
+    n, Wd = len(run), 100
+    mi = pkv.pkv_step_meta_ints(b.lib, n, Wd)
+    meta_host = torch.zeros(mi, dtype=torch.int32).pin_memory()
+    meta_dev = torch.zeros(mi, dtype=torch.int32, device="cuda")
+    ws = torch.empty(pkv.pkv_decode_workspace_size(b.lib, n), dtype=torch.uint8, device="cuda")
+    scale = 1.0 / math.sqrt(g.d_head)
+    q = W.normal(78, "q", (n, g.H_q, g.d_head), "bf16")
+    kn = W.normal(78, "k", (n, g.H_kv, g.d_head), "bf16")
+    vn = W.normal(78, "v", (n, g.H_kv, g.d_head), "bf16")
+    out = torch.full((n, g.H_q, g.d_head), float("nan"), dtype=torch.bfloat16, device="cuda")
+    pkv.pkv_decode_step(b.lib, 1, run, Wd, to_dev(q, "bf16"), to_dev(kn, "bf16"), to_dev(vn, "bf16"), b.kp, b.vp,
+                        scale, out, meta_host, meta_dev, ws)
+    torch.cuda.synchronize()
+    assert _plan_header(meta_host.numpy(), n, Wd)[1] == 12
+    oslots, ocows = b.orc.append(run.tolist(), [1] * n)
+    if len(ocows):
+        oracle.copy_blocks(g, ocows, b.hk, b.hv)
+    oracle.write_slots(g, 1, kn, vn, oslots, b.hk, b.hv)
+    pkv.pkv_check_device_error()
+    tables, lens = b.tables(run.tolist(), Wd)
+    check_attention(out_f64(out, "bf16"), b.decode_ref(q, tables, lens, scale, layer=1), "bf16")
+    b.check_pools_bitexact()
+
+
 def test_corrupt_plan_header_is_rejected():
     import torch
 
