@@ -317,7 +317,9 @@ int pkv_step_launch_host(pkv_pool* pool, int32_t layer, int32_t n, int32_t W, co
  *                     ignored and may be NULL).  Offsets are multiples of 16, each part
  *                     before the next, in_bytes covers the last part.
  *   off_meta 0: meta_host as in pkv_step_launch (copied to meta_dev by the call), or NULL
- *               when the caller has already queued meta_dev's contents on the stream.
+ *               when the caller has already queued meta_dev's contents on the stream
+ *               (not with prefix sharing on: the call reads the plan from the host copy,
+ *               PKV_ERR_INVALID_ARG before anything is queued).
  *   out_host [n][H_q][d_head] page-locked; out_dev device.
  * Every other argument is as for pkv_step_launch.  Errors: INVALID_ARG for a layout that
  * does not hold n rows; otherwise as pkv_step_launch. */

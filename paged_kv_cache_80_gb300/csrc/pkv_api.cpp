@@ -976,6 +976,8 @@ static int step_launch(pkv_pool* pool, int32_t layer, int32_t n, int32_t W, cons
       return fail(PKV_ERR_CUDA, std::string("cudaMemcpyAsync (step metadata): ") + cudaGetErrorString(e));
     plan_host = meta_host;
   }
+  if (pkv::share_on(P) && !plan_host)
+    return fail(PKV_ERR_INVALID_ARG, "with prefix sharing on, the launch needs the step's host metadata");
   pkv::ShareLaunch share{nullptr, 0, 0, 0};
   bool long_batch = false;
   if (plan_host) {  // the lengths after the append: tiles per (sequence, KV head) pair on average
@@ -1034,6 +1036,9 @@ int pkv_step_launch_packed(pkv_pool* pool, int32_t layer, int32_t n, int32_t W, 
                                                                                  in_bytes < off_meta + mb)))
     return fail(PKV_ERR_INVALID_ARG, "packed input: q, k_new, v_new (and the metadata) of n rows must fit before "
                                      "off_k, off_v, off_meta and in_bytes");
+  if (pkv::share_on(*as_pool(pool)) && !off_meta && !meta_host)
+    return fail(PKV_ERR_INVALID_ARG, "with prefix sharing on, the launch reads the step's plan from the host "
+                                     "metadata: pass meta_host or pack the metadata (off_meta)");
   const int32_t* plan_host = meta_host;
   if (off_meta) {  // the metadata travels with the inputs
     plan_host = reinterpret_cast<const int32_t*>(static_cast<const char*>(in_host) + off_meta);

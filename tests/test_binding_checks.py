@@ -113,3 +113,22 @@ def test_sharing_enlarges_the_metadata_the_binding_checks():
     with pytest.raises(ValueError, match="meta_dev"):
         pkv.pkv_step_launch(lib, 0, n, W, np.zeros((0, 2), np.int32), q, kv, kv, q, q, 0.1, q, meta,
                             torch.zeros(n * (W + 2), dtype=torch.int32), ws)
+
+
+def test_sharing_needs_the_host_metadata_in_a_packed_launch():
+    """With sharing on, a packed launch whose metadata the caller queued itself (off_meta 0,
+    meta_host NULL) is rejected before anything is queued: the call reads the step's plan from
+    the host copy (and the plan leaves a run's shared entries only in its first row's table)."""
+    import ctypes
+
+    lib = pkv.pkv_pool_create(1, 16, 2, 128, 16, "bf16", 64)
+    pkv.pkv_pool_set_prefix_sharing(lib, 4, 1, 152)
+    n, W = 4, 8
+    rq, rk = 16 * 128 * 2, 2 * 128 * 2
+    off_k, off_v = n * rq, n * (rq + rk)
+    in_bytes = n * (rq + 2 * rk)
+    fake = ctypes.c_void_p(256)  # never dereferenced: the call fails on its arguments first
+    rc = pkv._L().pkv_step_launch_packed(lib.handle, 0, n, W, None, 0, fake, fake, off_k, off_v, 0, in_bytes, fake,
+                                          fake, fake, fake, 0.1, None, fake, fake, 1 << 20, None, None, None)
+    assert pkv._L().pkv_status_name(rc).decode() == "PKV_ERR_INVALID_ARG"
+    assert "sharing" in pkv._L().pkv_last_error_message().decode()
