@@ -260,6 +260,8 @@ typedef struct CUevent_st* pkv_event_t; /* identical to cudaEvent_t */
  * the step may run the decode on part of the SMs beside the prefix kernel on the
  * others (the split comes from a time model of the two kernels).  The result is the
  * same attention (within rounding).
+ * Change the option only between steps: a step planned (pkv_step_plan) with one setting
+ * must be launched with the same, since the setting decides the metadata's layout.
  *   min_members: 0 turns sharing off (the default); else >= 2.
  *   min_blocks : >= 1.
  *   target_ctas: <= 0 takes the current device's SM count (PKV_ERR_CUDA without one).
